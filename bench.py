@@ -1,0 +1,538 @@
+"""Benchmark: useful TFLOP/s, % of roofline and us per call of the convolution forward pass.
+
+Default workload: the Whisper-tiny conv frontend at batch 1 (page "[ET-VK] conv1d runs at
+~3% of the GPU's matmul throughput ...", sections "Measurements" and "The conv2d path
+already solves this"): conv1d 80 -> 384 k3 s1 p1 on L=3000 + GELU, then conv1d 384 -> 384
+k3 s2 p1 + GELU, in fp32 and in bf16.  One step runs all four layers through the C-ABI.
+Useful FLOPs = 2 x MACs, padded taps counted (the page's convention).
+
+Timing: W warm-up steps, then exactly K steps between CUDA events on the launching stream,
+bracketed by a barrier and a device synchronise; each layer is one CUDA graph (the conv
+kernel plus, for split plans, the reduction) and events between the graphs give every
+layer's device time.  Steps rotate over enough copies of every input, packed weight and
+output that one rotation exceeds twice the L2 cache, so no step finds its data in L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Under torchrun each rank runs an independent replica on its own GPU (the forward pass
+has no exchange step); rank 0 prints the JSON line with the max time over ranks.
+--impl reference times the CPU oracle (fp64 direct loops) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "conv fwd useful TFLOP/s and % of roofline at 1 GB300; µs per call"
+L2_BYTES = 129 * 1000 * 1000
+FFMA_PER_SM_PER_CLK = 128          # fp32 lanes per SM
+SM_COUNT = 152
+SM_MAX_MHZ = 2070.0
+
+
+# ----------------------------------------------------------------------------- workloads
+def frontend_workloads(name):
+    from convolution_forward_implicit_gb300.workloads import WORKLOADS
+    if name == "whisper_frontend":
+        return [WORKLOADS["whisper_frontend_f32"], WORKLOADS["whisper_frontend_bf16"]]
+    if name in WORKLOADS:
+        return [WORKLOADS[name]]
+    raise SystemExit(f"unknown workload {name}")
+
+
+def workload_description(name):
+    if name == "whisper_frontend":
+        return ("whisper_tiny_conv_frontend: conv1d 80->384 k3 s1 p1 L=3000 +GELU, conv1d 384->384 k3 s2 p1 "
+                "(L 3000->1500) +GELU, batch 1, fp32 and bf16 I/O")
+    return name
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(v: float, ws: int, device=None) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while running (clocks, power, throttle reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return self.summary()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- our arm
+class LayerRun:
+    """One layer of one workload: its plan, per-rotation-set buffers and CUDA graphs."""
+
+    def __init__(self, wl, li, layer, R, x_sets, w, b):
+        import torch
+        from convolution_forward_implicit_gb300.binding import ConvPlan
+        self.wl, self.li, self.layer = wl, li, layer
+        self.plan = ConvPlan(*layer.plan_args(wl.dtype_code))
+        self.plan.allocate()
+        tdt = self.plan.torch_dtype()
+        self.x_sets = x_sets
+        self.wp_sets, self.b_sets, self.y_sets = [], [], []
+        for r in range(R):
+            wp = torch.empty_like(self.plan.w_packed)
+            self.plan.prepack(w)
+            wp.copy_(self.plan.w_packed)
+            self.wp_sets.append(wp)
+            self.b_sets.append(b.clone() if b is not None else None)
+            self.y_sets.append(torch.empty(self.plan.y_shape(), dtype=tdt, device="cuda"))
+        self.graphs = []
+        fields = dict(kv.split("=", 1) for kv in self.plan.describe().split())
+        self.kernels_per_call = 1 + (1 if int(fields.get("splits", "1")) > 1 else 0)   # conv (+ split-K reduction)
+
+    def call(self, r):
+        from convolution_forward_implicit_gb300.binding import conv_fwd
+        import torch
+        b = self.b_sets[r]
+        conv_fwd(self.plan.handle, self.x_sets[r].data_ptr(), self.wp_sets[r].data_ptr(),
+                 0 if b is None else b.data_ptr(), self.y_sets[r].data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+    def capture(self, R):
+        import torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for r in range(R):
+                self.call(r)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        for r in range(R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.call(r)
+            self.graphs.append(g)
+
+    @property
+    def flops(self):
+        return self.plan.flops
+
+    def name(self):
+        return f"{self.wl.dtype}_L{self.li + 1}"
+
+    def bytes_alg(self):
+        L = self.layer
+        esz = 2 if self.wl.dtype == "bf16" else 4
+        n_out = int(np.prod(self.plan.y_shape()))
+        n_x = int(np.prod(L.x_shape()))
+        n_w = int(np.prod(L.w_shape()))
+        n_b = L.G * L.K if L.bias_bound is not None else 0
+        return esz * (n_out + n_x + n_w + n_b)
+
+
+def to_device(a, dtype):
+    import torch
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def setup_layers(wls, R):
+    """Layers of every workload; layer l+1 of a workload reads layer l's output set."""
+    from convolution_forward_implicit_gb300.workloads import gen_inputs
+    runs, inputs = [], []
+    for wl in wls:
+        x, params = gen_inputs(wl)
+        xd = to_device(x, wl.dtype)
+        x_sets = [xd.clone() for _ in range(R)]
+        inputs.append((wl, x, x_sets))
+        for li, layer in enumerate(wl.layers):
+            w, b = params[li]
+            lr = LayerRun(wl, li, layer, R, x_sets, to_device(w, wl.dtype),
+                          to_device(b, wl.dtype) if b is not None else None)
+            runs.append(lr)
+            x_sets = [y.view(-1) for y in lr.y_sets]
+    return runs, inputs
+
+
+def rotation_sets(wls):
+    """Copies needed so that one rotation of activations, packed weights and outputs
+    exceeds twice the L2 cache."""
+    per_set = 0
+    for wl in wls:
+        for layer in wl.layers:
+            esz = 2 if wl.dtype == "bf16" else 4
+            per_set += esz * (int(np.prod(layer.x_shape())) + int(np.prod(layer.w_shape())))
+    # outputs are roughly the inputs of the next layer plus the last output
+    per_set = int(per_set * 1.6) + 1
+    return max(4, int(np.ceil(2.2 * L2_BYTES / per_set))), per_set
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    wls = frontend_workloads(args.workload)
+    R, per_set = rotation_sets(wls)
+    runs, inputs = setup_layers(wls, R)
+    for lr in runs:
+        lr.capture(R)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        for lr in runs:
+            lr.graphs[i % R].replay()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    for lr in runs:
+        lr.plan.check()
+
+    K = args.steps
+    nL = len(runs)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nL + 1)] for _ in range(K)]
+    clocks = ClockSampler(local).start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    for i in range(K):
+        ev[i][0].record(stream)
+        r = i % R
+        for j, lr in enumerate(runs):
+            lr.graphs[r].replay()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][nL])
+    per_layer_ms = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K for j in range(nL)]
+    # keep sampling clocks over a sustained window of the same steps (at least ~1.5 s)
+    t_end = time.time() + 1.5
+    i = 0
+    while time.time() < t_end:
+        for _ in range(200):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+    clk = clocks.stop()
+    for lr in runs:
+        lr.plan.check()
+    total_ms = max_over_ranks(total_ms, ws, torch.device("cuda", local))
+
+    step_flops = sum(lr.flops for lr in runs)
+    ms_per_step = total_ms / K
+    value = ws * step_flops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end: pinned host inputs in, final outputs back to pinned host memory
+    e2e = run_e2e(args, runs, inputs, R, stream, ws, local)
+
+    # ---- roofline of the dominant kernel
+    dom = int(np.argmax(per_layer_ms))
+    lr = runs[dom]
+    roof = roofline_for(lr, per_layer_ms[dom])
+
+    launches = K * sum(lr.kernels_per_call for lr in runs)
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "us_per_call": {lr.name(): round(t * 1e3, 3) for lr, t in zip(runs, per_layer_ms)},
+        "useful_gflop_per_step": round(step_flops / 1e9, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "+".join(sorted({wl.dtype for wl in wls}, key=lambda d: d != "f32")),
+        "data": "synthetic (seeded N(0,1) inputs, U(+-1/sqrt(C_in*taps)) weights, U(+-0.05) bias)",
+        "config": {"workload": workload_description(args.workload),
+                   "l2": f"inputs larger than L2: {R} rotating sets of activations, packed weights and outputs "
+                         f"(~{R * per_set / 1e6:.0f} MB per rotation, L2 129 MB)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "plans": {lr.name(): lr.plan.describe() for lr in runs}},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(wls)
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, runs, inputs, R, stream, ws, local):
+    import torch
+    host_in, host_out = [], []
+    for (wl, x, x_sets) in inputs:
+        h = to_device(x, wl.dtype).cpu().pin_memory()
+        host_in.append((h, x_sets))
+    last = {}
+    for lr in runs:
+        last[lr.wl.name] = lr
+    for lr in last.values():
+        host_out.append((torch.empty(lr.y_sets[0].shape, dtype=lr.y_sets[0].dtype).pin_memory(), lr))
+    bi = sum(h.numel() * h.element_size() for h, _ in host_in)
+    bo = sum(h.numel() * h.element_size() for h, _ in host_out)
+    K = args.steps
+
+    def e2e_step(i):
+        r = i % R
+        for h, x_sets in host_in:
+            x_sets[r].copy_(h, non_blocking=True)
+        for lr in runs:
+            lr.graphs[r].replay()
+        for h, lr in host_out:
+            h.copy_(lr.y_sets[r], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(K):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, torch.device("cuda", local))
+    flops = sum(lr.flops for lr in runs)
+    return {"value": round(ws * flops * K / (ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
+            "ms_per_step": round(ms / K, 6), "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def roofline_for(lr, ms):
+    """Roofline of one layer's kernel: the slower of its compute pipe and HBM bytes."""
+    peaks, src = measured_peaks()
+    flops = lr.flops
+    t_s = ms * 1e-3
+    byts = lr.bytes_alg()
+    desc = lr.plan.describe()
+    hbm = peaks["hbm_gbs"] * 1e9
+    if "variant=tc_bf16" in desc:
+        pipe = peaks["bf16_tflops"] * 1e12
+        bound_c, unit_peak = "tensor", peaks["bf16_tflops"]
+        note = f"bf16 dense tensor peak, burst, {src}"
+    else:
+        pipe = SM_COUNT * FFMA_PER_SM_PER_CLK * 2 * SM_MAX_MHZ * 1e6
+        bound_c, unit_peak = "alu", pipe / 1e12
+        note = "FFMA peak = 152 SMs x 128 fp32 lanes x 2 flop x 2070 MHz (derived)"
+    if flops / pipe >= byts / hbm:
+        ach = flops / t_s / 1e12
+        return {"bound": bound_c, "achieved": round(ach, 4), "peak": round(unit_peak, 2), "unit": "TFLOP/s",
+                "frac": round(ach / unit_peak, 4), "traffic": None, "kernel": lr.name(),
+                "plan": desc, "peak_source": note, "algorithmic_flops": flops, "algorithmic_bytes": byts}
+    ach = byts / t_s / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None, "kernel": lr.name(), "plan": desc,
+            "peak_source": f"HBM copy bandwidth, {src}", "algorithmic_flops": flops, "algorithmic_bytes": byts}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def _oracle_layer_time(wl, li, layer, x, w, b, nthreads, sample_frac=1.0, seed=0):
+    """Time the oracle on one layer (whole output, or a sample of outputs split over threads).
+    Returns (seconds, useful flops computed)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    from convolution_forward_implicit_gb300 import synthetic as syn
+    from convolution_forward_implicit_gb300.binding import CONV_EPI_BIAS, CONV_EPI_BIAS_GELU, CONV_EPI_GELU
+    g = oracle.Geom(layer.N, layer.G, layer.C, layer.K, layer.spatial, layer.filter, layer.stride, layer.pad,
+                    layer.dilation)
+    gelu = layer.epilogue in (CONV_EPI_BIAS_GELU, CONV_EPI_GELU)
+    xf, wf = syn.as_f32(x, wl.dtype), syn.as_f32(w, wl.dtype)
+    bf = syn.as_f32(b, wl.dtype) if (b is not None and layer.epilogue in (CONV_EPI_BIAS, CONV_EPI_BIAS_GELU)) else None
+    total = int(np.prod(g.y_shape()))
+    per_out = 2.0 * layer.C * layer.taps
+    if sample_frac >= 1.0:
+        t = time.perf_counter()
+        out, _ = oracle.conv_fwd(g, xf, wf, bf, gelu=gelu, nthreads=nthreads)
+        return time.perf_counter() - t, per_out * total, out
+    n = max(1, int(total * sample_frac))
+    idx = np.random.default_rng(seed).choice(total, size=n, replace=False)
+    coords = np.array(np.unravel_index(idx, g.y_shape())).T.astype(np.int64)
+    chunks = np.array_split(coords, nthreads)
+    t = time.perf_counter()
+    with ThreadPoolExecutor(nthreads) as ex:
+        list(ex.map(lambda c: oracle.conv_fwd_points(g, xf, wf, bf, gelu, c), chunks))
+    return time.perf_counter() - t, per_out * n, None
+
+
+def cpu_baseline(wls):
+    """The oracle as it stands on the host cores: one whole step of the workload (every
+    layer, each reading the oracle's own previous output, rounded to the I/O type)."""
+    from convolution_forward_implicit_gb300 import synthetic as syn
+    from convolution_forward_implicit_gb300.workloads import gen_inputs
+    nthreads = os.cpu_count() or 1
+    secs, flops = 0.0, 0.0
+    for wl in wls:
+        x, params = gen_inputs(wl)
+        cur = x
+        for li, layer in enumerate(wl.layers):
+            w, b = params[li]
+            dt, fl, out = _oracle_layer_time(wl, li, layer, cur, w, b, nthreads)
+            secs += dt
+            flops += fl
+            cur = syn.to_storage(out.reshape(-1), wl.dtype)
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"one full step (every layer, whole output), {flops / 1e9:.2f} GFLOP in {secs:.2f} s"}
+
+
+def run_reference(args, ws, rank, local):
+    """The oracle as the reference arm: each step evaluates a fixed random sample of each
+    layer's outputs (1/32 of them) on all host cores; throughput counts the sampled FLOPs."""
+    if rank != 0:
+        return
+    from convolution_forward_implicit_gb300 import synthetic as syn
+    from convolution_forward_implicit_gb300.workloads import gen_inputs
+    import oracle
+    oracle.build()
+    wls = frontend_workloads(args.workload)
+    nthreads = os.cpu_count() or 1
+    data = []
+    for wl in wls:
+        x, params = gen_inputs(wl)
+        for li, layer in enumerate(wl.layers):
+            # the oracle's speed does not depend on the values: later layers read a fresh N(0,1) draw
+            xin = x if li == 0 else syn.gen_normal(7 + li, layer.x_shape(), wl.dtype)
+            data.append((wl, li, layer, xin, params[li][0], params[li][1]))
+    frac = 1.0 / 32
+
+    def ref_step(seed):
+        secs, flops = 0.0, 0.0
+        for (wl, li, layer, xin, w, b) in data:
+            dt, fl, _ = _oracle_layer_time(wl, li, layer, xin, w, b, nthreads, sample_frac=frac, seed=seed)
+            secs += dt
+            flops += fl
+        return secs, flops
+
+    for i in range(args.warmup):
+        ref_step(i)
+    tot_s, tot_f = 0.0, 0.0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s, f = ref_step(1000 + i)
+        tot_s += s
+        tot_f += f
+    wall = time.perf_counter() - t0
+    value = tot_f / wall / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "+".join(sorted({wl.dtype for wl in wls}, key=lambda d: d != "f32")),
+            "data": "synthetic", "config": {"workload": workload_description(args.workload),
+                                            "parallelism": "host threads"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+                             "sample": f"each step: a fixed random 1/32 of every layer's outputs, fp64 direct loops"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="whisper_frontend")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_setup()
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "ours":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, ws, rank, local)
+        else:
+            run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,446 @@
+// C-ABI of the convolution-forward library: plans, weight prepacking, the forward
+// dispatch, the split-K reduction and the device error word.  Declarations and the
+// contract of every entry point are in include/conv.h.
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <new>
+
+#include "../../include/conv.h"
+#include "internal.h"
+
+using namespace convfwd;
+
+// ----------------------------------------------------------------------------- device error word
+namespace {
+__device__ unsigned int g_error_word;   // bit flags raised by kernels that abandon a wait
+
+std::mutex g_err_mu;
+unsigned* g_err_ptr[64];
+
+unsigned* error_word_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+// ----------------------------------------------------------------------------- prepack kernels
+// Tensor-core layout: per (group, N tile, 64-wide K block) a BN x 128-byte tile whose
+// 16-byte chunk j of row n sits at chunk position j ^ (n & 7): the 128-byte swizzle the
+// MMA's shared-memory descriptor expects, so the tile is copied into shared memory as is.
+__global__ void prepack_tc_kernel(const uint4* __restrict__ w, uint4* __restrict__ out, int K, int C, int taps,
+                                  int BN, int num_nt, int nkb, int nchunks, int cpt, long long total16) {
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total16;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int j = (int)(idx & 7);
+        long long r = idx >> 3;
+        const int n = (int)(r % BN); r /= BN;
+        const int kb = (int)(r % nkb); r /= nkb;
+        const int nt = (int)(r % num_nt);
+        const int g = (int)(r / num_nt);
+        const int k = nt * BN + n;
+        const int q = kb * 8 + j;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (k < K && q < nchunks) {
+            const int tap = q / cpt;
+            const int c0 = (q - tap * cpt) * 8;
+            v = w[((((long long)g * K + k) * taps + tap) * C + c0) / 8];
+        }
+        const long long tile = (((long long)g * num_nt + nt) * nkb + kb) * BN + n;
+        out[tile * 8 + (j ^ (n & 7))] = v;
+    }
+}
+
+// FFMA layout: [G][taps*C][Kpad], output channels contiguous, zero beyond K.
+template <typename T>
+__global__ void prepack_simt_kernel(const T* __restrict__ w, T* __restrict__ out, int K, int C, int taps, int Kg,
+                                    int Kpad, long long total) {
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int n = (int)(idx % Kpad);
+        const long long r = idx / Kpad;
+        const int kk = (int)(r % Kg);
+        const int g = (int)(r / Kg);
+        const int tap = kk / C;
+        const int c = kk - tap * C;
+        out[idx] = n < K ? w[(((long long)g * K + n) * taps + tap) * C + c] : T(0.0f);
+    }
+}
+
+// ----------------------------------------------------------------------------- split-K reduction
+// y = epilogue(sum over splits, in split order, of the fp32 partials): a fixed order,
+// so results do not change from run to run.
+__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ void from_f(float& d, float v) { d = v; }
+__device__ __forceinline__ void from_f(__nv_bfloat16& d, float v) { d = __float2bfloat16_rn(v); }
+
+template <typename T>
+__global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, long long MGK, int GK,
+                                     const T* __restrict__ bias, T* __restrict__ y, int epi) {
+    const bool add_bias = epi == EPI_BIAS || epi == EPI_BIAS_GELU;
+    const bool do_gelu = epi == EPI_BIAS_GELU || epi == EPI_GELU;
+    if ((GK & 3) == 0) {
+        const long long n4 = MGK / 4;
+        for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+             i += (long long)gridDim.x * blockDim.x) {
+            float4 a = __ldg(reinterpret_cast<const float4*>(ws) + i);
+            for (int s = 1; s < splits; ++s) {
+                const float4 b = __ldg(reinterpret_cast<const float4*>(ws + (long long)s * MGK) + i);
+                a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+            }
+            float v[4] = {a.x, a.y, a.z, a.w};
+            const int col = (int)((i * 4) % GK);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (add_bias) v[e] += to_f(bias[col + e]);
+                if (do_gelu) v[e] = gelu_f(v[e]);
+                from_f(y[i * 4 + e], v[e]);
+            }
+        }
+    } else {
+        for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < MGK;
+             i += (long long)gridDim.x * blockDim.x) {
+            float a = ws[i];
+            for (int s = 1; s < splits; ++s) a += ws[(long long)s * MGK + i];
+            if (add_bias) a += to_f(bias[i % GK]);
+            if (do_gelu) a = gelu_f(a);
+            from_f(y[i], a);
+        }
+    }
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------------------- plan
+enum Variant { VAR_TC_BF16 = 0, VAR_SIMT = 1 };
+
+struct conv_plan {
+    int ndim;
+    int64_t spatial[3], filter[3], stride[3], pad[3], dil[3], out_spatial[3];
+    conv_dtype dtype;
+    conv_epilogue epi;
+    Geom g;
+    int sm_count;
+    Variant variant;
+    // tensor-core plan
+    int BN, stages, num_mt, num_nt, nkb, nchunks, cpt, splits, kbps, total_units, grid;
+    // SIMT plan
+    int BM, Kg, Kpad, nkt, ktps, vec;
+    size_t prepack_bytes, workspace_bytes;
+    void* workspace;
+    size_t workspace_size;
+    double flops;
+    char desc[320];
+};
+
+static int env_int(const char* name, int dflt) {
+    const char* v = getenv(name);
+    if (!v || !*v) return dflt;
+    return atoi(v);
+}
+
+static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+static int query_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 152; }
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    return n;
+}
+
+// Tensor-core tile choice: BN from the compiled set, the smallest padded width for K
+// <= 256, else 256 or 128, whichever wastes fewer columns; then split-K when the tiles
+// alone leave SMs idle (page "onnxruntime PR #33639", "Description": large tiles for
+// large problems, split-K for small problems because it fills the GPU better).
+static void plan_tc(conv_plan* p) {
+    const Geom& g = p->g;
+    int bn;
+    if (g.K <= 16) bn = 16;
+    else if (g.K <= 32) bn = 32;
+    else if (g.K <= 64) bn = 64;
+    else if (g.K <= 128) bn = 128;
+    else if (g.K <= 256) bn = 256;
+    else bn = (cdiv(g.K, 256) * 256 - g.K <= cdiv(g.K, 128) * 128 - g.K) ? 256 : 128;
+    const int force_bn = env_int("CONV_FORCE_BN", 0);
+    if (force_bn == 16 || force_bn == 32 || force_bn == 64 || force_bn == 128 || force_bn == 256) bn = force_bn;
+    p->BN = bn;
+    p->stages = bn == 256 ? 4 : bn == 128 ? 6 : 8;
+    p->cpt = g.C / 8;
+    p->nchunks = g.taps * p->cpt;
+    p->nkb = (int)cdiv(p->nchunks, 8);
+    p->num_mt = (int)cdiv(g.M, 128);
+    p->num_nt = (int)cdiv(g.K, bn);
+    const int64_t units = (int64_t)p->num_mt * g.G * p->num_nt;
+    int splits = 1;
+    if (units < p->sm_count && p->nkb >= 4) {
+        splits = (int)std::min<int64_t>(p->sm_count / units, p->nkb / 2);
+        splits = std::max(1, std::min(splits, 16));
+    }
+    const int force = env_int("CONV_FORCE_SPLITK", 0);
+    if (force >= 1) splits = std::min(force, p->nkb);
+    p->kbps = (int)cdiv(p->nkb, splits);
+    p->splits = (int)cdiv(p->nkb, p->kbps);     // every split non-empty
+    p->total_units = (int)(units * p->splits);
+    p->grid = std::min(p->total_units, p->sm_count);
+    p->prepack_bytes = (size_t)g.G * p->num_nt * p->nkb * bn * 128;
+    p->workspace_bytes = p->splits > 1 ? (size_t)p->splits * g.M * g.G * g.K * sizeof(float) : 0;
+    snprintf(p->desc, sizeof(p->desc),
+             "variant=tc_bf16 gather=cp.async tile=128x%d k_block=64 stages=%d splits=%d units=%d grid=%d "
+             "k_blocks=%d",
+             bn, p->stages, p->splits, p->total_units, p->grid, p->nkb);
+}
+
+static void plan_simt(conv_plan* p) {
+    const Geom& g = p->g;
+    p->Kg = g.taps * g.C;
+    p->nkt = (int)cdiv(p->Kg, 8);
+    p->num_nt = (int)cdiv(g.K, 128);
+    p->Kpad = p->num_nt * 128;
+    const int64_t tiles128 = cdiv(g.M, 128) * p->num_nt * g.G;
+    p->BM = tiles128 >= p->sm_count ? 128 : 64;
+    const int force_bm = env_int("CONV_FORCE_BM", 0);
+    if (force_bm == 64 || force_bm == 128) p->BM = force_bm;
+    p->num_mt = (int)cdiv(g.M, p->BM);
+    const int64_t tiles = (int64_t)p->num_mt * p->num_nt * g.G;
+    int splits = 1;
+    if (tiles < p->sm_count && p->nkt >= 32) {
+        splits = (int)std::min<int64_t>(p->sm_count / tiles, p->nkt / 16);
+        splits = std::max(1, std::min(splits, 16));
+    }
+    const int force = env_int("CONV_FORCE_SPLITK", 0);
+    if (force >= 1) splits = std::min(force, p->nkt);
+    p->ktps = (int)cdiv(p->nkt, splits);
+    p->splits = (int)cdiv(p->nkt, p->ktps);
+    p->vec = (g.C % 4 == 0 && g.K % 4 == 0) ? 1 : 0;
+    const size_t esz = p->dtype == CONV_BF16 ? 2 : 4;
+    p->prepack_bytes = (size_t)g.G * p->Kg * p->Kpad * esz;
+    p->workspace_bytes = p->splits > 1 ? (size_t)p->splits * g.M * g.G * g.K * sizeof(float) : 0;
+    snprintf(p->desc, sizeof(p->desc),
+             "variant=simt_%s tile=%dx128 k_step=8 splits=%d grid=%dx%dx%d vec=%d",
+             p->dtype == CONV_BF16 ? "bf16" : "f32", p->BM, p->splits, p->num_mt, p->num_nt,
+             g.G * p->splits, p->vec);
+}
+
+extern "C" {
+
+conv_status conv_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, int64_t C, int64_t K,
+                             const int64_t* spatial, const int64_t* filter, const int64_t* stride,
+                             const int64_t* pad, const int64_t* dilation, conv_dtype dtype,
+                             conv_epilogue epilogue) {
+    if (!out) return CONV_ERR_INVALID_ARG;
+    if (ndim < 1 || ndim > 3 || !spatial || !filter || !stride || !pad || !dilation) return CONV_ERR_INVALID_ARG;
+    if (N < 1 || G < 1 || C < 1 || K < 1) return CONV_ERR_INVALID_ARG;
+    if (dtype != CONV_F32 && dtype != CONV_BF16) return CONV_ERR_INVALID_ARG;
+    if (epilogue < CONV_EPI_NONE || epilogue > CONV_EPI_GELU) return CONV_ERR_INVALID_ARG;
+    int64_t sp[3] = {1, 1, 1}, fl[3] = {1, 1, 1}, st[3] = {1, 1, 1}, pa[3] = {0, 0, 0}, di[3] = {1, 1, 1},
+            os[3];
+    const int off = 3 - ndim;   // conv1d -> D = H = 1, conv2d -> D = 1
+    for (int i = 0; i < ndim; ++i) {
+        if (spatial[i] < 1 || filter[i] < 1 || stride[i] < 1 || pad[i] < 0 || dilation[i] < 1)
+            return CONV_ERR_INVALID_ARG;
+        sp[off + i] = spatial[i]; fl[off + i] = filter[i]; st[off + i] = stride[i];
+        pa[off + i] = pad[i]; di[off + i] = dilation[i];
+    }
+    const int64_t LIM = (int64_t)1 << 30;
+    for (int i = 0; i < 3; ++i) {
+        if (sp[i] > LIM || fl[i] > LIM || st[i] > LIM || pa[i] > LIM || di[i] > LIM) return CONV_ERR_UNSUPPORTED;
+        const int64_t span = sp[i] + 2 * pa[i] - di[i] * (fl[i] - 1) - 1;
+        if (span < 0) return CONV_ERR_INVALID_ARG;   // empty output
+        os[i] = span / st[i] + 1;
+    }
+    if (N > LIM || G > LIM || C > LIM || K > LIM) return CONV_ERR_UNSUPPORTED;
+    const int64_t M = N * os[0] * os[1] * os[2];
+    const int64_t taps = fl[0] * fl[1] * fl[2];
+    // the kernels index pixels, channels-by-taps and K blocks in 32 bits
+    if (M >= ((int64_t)1 << 31) - 256 || taps * C >= ((int64_t)1 << 30) || G * C >= ((int64_t)1 << 30) ||
+        G * K >= ((int64_t)1 << 30) || N * sp[0] * sp[1] * sp[2] >= ((int64_t)1 << 40))
+        return CONV_ERR_UNSUPPORTED;
+
+    conv_plan* p = new (std::nothrow) conv_plan();
+    if (!p) return CONV_ERR_INVALID_ARG;
+    p->ndim = ndim;
+    for (int i = 0; i < 3; ++i) {
+        p->spatial[i] = sp[i]; p->filter[i] = fl[i]; p->stride[i] = st[i];
+        p->pad[i] = pa[i]; p->dil[i] = di[i]; p->out_spatial[i] = os[i];
+    }
+    p->dtype = dtype;
+    p->epi = epilogue;
+    Geom& g = p->g;
+    g.N = (int)N; g.G = (int)G; g.C = (int)C; g.K = (int)K;
+    g.D = (int)sp[0]; g.H = (int)sp[1]; g.W = (int)sp[2];
+    g.Z = (int)fl[0]; g.Y = (int)fl[1]; g.X = (int)fl[2];
+    g.sd = (int)st[0]; g.sh = (int)st[1]; g.sw = (int)st[2];
+    g.pd = (int)pa[0]; g.ph = (int)pa[1]; g.pw = (int)pa[2];
+    g.dd = (int)di[0]; g.dh = (int)di[1]; g.dw = (int)di[2];
+    g.Do = (int)os[0]; g.Ho = (int)os[1]; g.Wo = (int)os[2];
+    g.M = (int)M;
+    g.taps = (int)taps;
+    p->flops = 2.0 * (double)M * (double)G * (double)K * (double)taps * (double)C;
+    p->sm_count = query_sm_count();
+    const bool tc_ok = dtype == CONV_BF16 && C % 8 == 0 && K % 8 == 0 && env_int("CONV_FORCE_SIMT", 0) == 0;
+    if (tc_ok) {
+        p->variant = VAR_TC_BF16;
+        plan_tc(p);
+    } else {
+        p->variant = VAR_SIMT;
+        plan_simt(p);
+    }
+    *out = p;
+    return CONV_OK;
+}
+
+conv_status conv_plan_output_shape(conv_plan_t plan, int64_t* out_spatial) {
+    if (!plan || !out_spatial) return CONV_ERR_INVALID_ARG;
+    for (int i = 0; i < plan->ndim; ++i) out_spatial[i] = plan->out_spatial[3 - plan->ndim + i];
+    return CONV_OK;
+}
+
+size_t conv_prepacked_weight_bytes(conv_plan_t plan) { return plan ? plan->prepack_bytes : 0; }
+
+size_t conv_workspace_bytes(conv_plan_t plan) { return plan ? plan->workspace_bytes : 0; }
+
+conv_status conv_plan_set_workspace(conv_plan_t plan, void* workspace, size_t bytes) {
+    if (!plan) return CONV_ERR_INVALID_ARG;
+    if (plan->workspace_bytes && (!workspace || bytes < plan->workspace_bytes)) return CONV_ERR_WORKSPACE;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 15u)) return CONV_ERR_ALIGNMENT;
+    plan->workspace = workspace;
+    plan->workspace_size = bytes;
+    return CONV_OK;
+}
+
+static bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+conv_status conv_prepack_weights(conv_plan_t plan, const void* w, void* w_packed, void* stream) {
+    if (!plan || !w || !w_packed) return CONV_ERR_INVALID_ARG;
+    if (misaligned(w) || misaligned(w_packed)) return CONV_ERR_ALIGNMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Geom& g = plan->g;
+    const int threads = 256;
+    if (plan->variant == VAR_TC_BF16) {
+        const long long total16 = (long long)(plan->prepack_bytes / 16);
+        const int blocks = (int)std::min<long long>(cdiv(total16, threads), 65535);
+        prepack_tc_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint4*>(w), static_cast<uint4*>(w_packed),
+                                                     g.K, g.C, g.taps, plan->BN, plan->num_nt, plan->nkb,
+                                                     plan->nchunks, plan->cpt, total16);
+    } else {
+        const long long total = (long long)g.G * plan->Kg * plan->Kpad;
+        const int blocks = (int)std::min<long long>(cdiv(total, threads), 65535);
+        if (plan->dtype == CONV_BF16)
+            prepack_simt_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
+                static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(w_packed), g.K, g.C, g.taps,
+                plan->Kg, plan->Kpad, total);
+        else
+            prepack_simt_kernel<float><<<blocks, threads, 0, s>>>(static_cast<const float*>(w),
+                                                                  static_cast<float*>(w_packed), g.K, g.C,
+                                                                  g.taps, plan->Kg, plan->Kpad, total);
+    }
+    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+static conv_status launch_reduce(conv_plan_t plan, const void* bias, void* y, cudaStream_t s) {
+    const Geom& g = plan->g;
+    const long long MGK = (long long)g.M * g.G * g.K;
+    const int threads = 256;
+    const long long work = (g.G * g.K) % 4 == 0 ? MGK / 4 : MGK;
+    const int blocks = (int)std::min<long long>(cdiv(work, threads), (long long)plan->sm_count * 8);
+    const float* ws = static_cast<const float*>(plan->workspace);
+    if (plan->dtype == CONV_BF16)
+        splitk_reduce_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
+            ws, plan->splits, MGK, g.G * g.K, static_cast<const __nv_bfloat16*>(bias),
+            static_cast<__nv_bfloat16*>(y), (int)plan->epi);
+    else
+        splitk_reduce_kernel<float><<<blocks, threads, 0, s>>>(ws, plan->splits, MGK, g.G * g.K,
+                                                               static_cast<const float*>(bias),
+                                                               static_cast<float*>(y), (int)plan->epi);
+    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, const void* bias, void* y,
+                     void* stream) {
+    if (!plan || !x || !w_packed || !y) return CONV_ERR_INVALID_ARG;
+    const bool needs_bias = plan->epi == CONV_EPI_BIAS || plan->epi == CONV_EPI_BIAS_GELU;
+    if (needs_bias && !bias) return CONV_ERR_INVALID_ARG;
+    if (misaligned(x) || misaligned(w_packed) || misaligned(y) || (needs_bias && misaligned(bias)))
+        return CONV_ERR_ALIGNMENT;
+    if (plan->workspace_bytes && (!plan->workspace || plan->workspace_size < plan->workspace_bytes))
+        return CONV_ERR_WORKSPACE;
+    unsigned* err = error_word_ptr();
+    if (!err) return CONV_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (plan->variant == VAR_TC_BF16) {
+        TcParams tp;
+        tp.g = plan->g;
+        tp.x = x; tp.wpack = w_packed; tp.bias = needs_bias ? bias : nullptr; tp.y = y;
+        tp.ws = static_cast<float*>(plan->workspace);
+        tp.err = err;
+        tp.BN = plan->BN; tp.num_mt = plan->num_mt; tp.num_nt = plan->num_nt; tp.nkb = plan->nkb;
+        tp.nchunks = plan->nchunks; tp.cpt = plan->cpt; tp.splits = plan->splits; tp.kbps = plan->kbps;
+        tp.epi = (int)plan->epi; tp.total_units = plan->total_units;
+        e = launch_tc_bf16(tp, plan->stages, plan->grid, s);
+    } else {
+        SimtParams sp;
+        sp.g = plan->g;
+        sp.x = x; sp.wpack = w_packed; sp.bias = needs_bias ? bias : nullptr; sp.y = y;
+        sp.ws = static_cast<float*>(plan->workspace);
+        sp.Kg = plan->Kg; sp.Kpad = plan->Kpad; sp.num_mt = plan->num_mt; sp.num_nt = plan->num_nt;
+        sp.nkt = plan->nkt; sp.splits = plan->splits; sp.ktps = plan->ktps; sp.epi = (int)plan->epi;
+        e = launch_simt(sp, plan->dtype == CONV_BF16, plan->BM, plan->vec != 0, s);
+    }
+    if (e != cudaSuccess) return CONV_ERR_CUDA;
+    if (plan->splits > 1) return launch_reduce(plan, needs_bias ? bias : nullptr, y, s);
+    return CONV_OK;
+}
+
+conv_status conv_plan_check(conv_plan_t plan, void* stream) {
+    if (!plan) return CONV_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CONV_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v)) != cudaSuccess) return CONV_ERR_CUDA;
+    if (v) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return CONV_ERR_CUDA;
+        return CONV_ERR_TIMEOUT;
+    }
+    return CONV_OK;
+}
+
+conv_status conv_plan_destroy(conv_plan_t plan) {
+    delete plan;
+    return CONV_OK;
+}
+
+const char* conv_status_string(conv_status status) {
+    switch (status) {
+        case CONV_OK: return "CONV_OK";
+        case CONV_ERR_INVALID_ARG: return "CONV_ERR_INVALID_ARG";
+        case CONV_ERR_UNSUPPORTED: return "CONV_ERR_UNSUPPORTED";
+        case CONV_ERR_ALIGNMENT: return "CONV_ERR_ALIGNMENT";
+        case CONV_ERR_WORKSPACE: return "CONV_ERR_WORKSPACE";
+        case CONV_ERR_CUDA: return "CONV_ERR_CUDA";
+        case CONV_ERR_TIMEOUT: return "CONV_ERR_TIMEOUT";
+    }
+    return "CONV_ERR_UNKNOWN";
+}
+
+const char* conv_plan_describe(conv_plan_t plan) { return plan ? plan->desc : ""; }
+
+double conv_plan_flops(conv_plan_t plan) { return plan ? plan->flops : 0.0; }
+
+}  // extern "C"

@@ -1,0 +1,163 @@
+/*
+ * conv.h -- C ABI of the GB300 implicit-GEMM convolution-forward library
+ * (libconvfwd.so).
+ *
+ * The operation (page "composable_kernel dispatcher/heuristics/LEARNINGS_GROUPED_CONV.md",
+ * introduction and section 2; page "[ET-VK] conv1d runs at ~3% of the GPU's matmul
+ * throughput ...", sections "Measurements", "The conv2d path already solves this" and
+ * "Suggested fix"):
+ *
+ *   y[n, o, g, k] = act( bias[g, k] + sum_{t, c} x[n, o*stride + t*dilation - pad, g, c] * w[g, k, t, c] )
+ *
+ * a dense or grouped cross-correlation over 1, 2 or 3 spatial dimensions with stride,
+ * symmetric zero padding and dilation; act is the identity or the exact (erf) GELU.
+ * A 1D problem is run as the H = 1 (and D = 1) case of the same path, never by a
+ * separate kernel; a 2D problem is the D = 1 case.
+ *
+ * Layouts (channels last, dense, row major):
+ *   x      N  [D] [H] W  G C        (conv1d: N L C with G = 1)
+ *   w      G  K  [Z] [Y] X  C       (conv1d: K kw C)
+ *   y      N  [Do][Ho] Wo G K
+ *   bias   G*K
+ * Output size per spatial dimension: O = floor((I + 2*pad - dil*(F-1) - 1) / stride) + 1.
+ *
+ * Arithmetic: fp32 I/O is computed in fp32 (FFMA, no TF32); bf16 I/O multiplies bf16
+ * on the tensor cores and accumulates in fp32; the epilogue (bias, GELU) runs in fp32
+ * and the bf16 output is rounded once, to nearest even.
+ *
+ * Conventions for every call:
+ *  - Ownership: the caller allocates and frees every device buffer (x, w, w_packed,
+ *    bias, y, workspace).  A plan owns only host memory; it never allocates device
+ *    memory.
+ *  - Pointers: x, w, w_packed, bias, y and the workspace are device pointers and must
+ *    be 16-byte aligned (CONV_ERR_ALIGNMENT otherwise).
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls enqueue work and return; they never synchronise.  conv_fwd makes
+ *    no allocation and no host-device copy, so it may be captured in a CUDA graph.
+ *  - Errors: every call returns a conv_status.  Launch failures return CONV_ERR_CUDA.
+ *    A kernel that gives up on a pipeline wait (a bounded spin) records the fact in a
+ *    device-side error word and exits; conv_plan_check() reads and clears it.
+ *  - Threads: a plan may be used from several host threads and streams at once as long
+ *    as calls that use a workspace are given disjoint workspaces.
+ */
+#ifndef CONVFWD_CONV_H
+#define CONVFWD_CONV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CONV_OK = 0,
+    CONV_ERR_INVALID_ARG = 1,   /* a size, count or pointer argument is out of range   */
+    CONV_ERR_UNSUPPORTED = 2,   /* well formed, but outside what the library implements */
+    CONV_ERR_ALIGNMENT = 3,     /* a pointer or a channel count breaks 16-byte alignment */
+    CONV_ERR_WORKSPACE = 4,     /* the plan needs a workspace and none (or too small) set */
+    CONV_ERR_CUDA = 5,          /* a CUDA runtime call or a kernel launch failed          */
+    CONV_ERR_TIMEOUT = 6        /* a kernel abandoned a pipeline wait (see conv_plan_check) */
+} conv_status;
+
+typedef enum { CONV_F32 = 0, CONV_BF16 = 1 } conv_dtype;   /* I/O type of x, w, bias, y */
+
+typedef enum {
+    CONV_EPI_NONE = 0,        /* y = acc                         */
+    CONV_EPI_BIAS = 1,        /* y = acc + bias                  */
+    CONV_EPI_BIAS_GELU = 2,   /* y = GELU(acc + bias), erf form  */
+    CONV_EPI_GELU = 3         /* y = GELU(acc)                   */
+} conv_epilogue;
+
+typedef struct conv_plan* conv_plan_t;
+
+/*
+ * Build a plan: validate the problem, normalise it to three spatial dimensions
+ * (conv1d -> D = H = 1, conv2d -> D = 1; page "[ET-VK] conv1d ...", "Suggested fix"),
+ * form the GEMM view per group (M = N*Do*Ho*Wo, N_gemm = K, K_gemm = taps*C) and pick
+ * the kernel variant and tiling (page "onnxruntime PR #33639", "Description": large
+ * tiles for large problems, split-K where tiles alone cannot fill the GPU, each choice
+ * checked against the device's limits).
+ *   ndim      1, 2 or 3
+ *   N G C K   batch, groups, input channels per group, output channels per group (>= 1)
+ *   spatial   ndim input extents, outermost first (D, H, W)
+ *   filter    ndim filter extents (Z, Y, X)
+ *   stride, pad, dilation   ndim values each; stride >= 1, pad >= 0, dilation >= 1
+ * bf16 problems with C and K multiples of 8 run on the tensor cores; other bf16
+ * problems and all fp32 problems run on the FFMA kernel.
+ * Returns CONV_ERR_INVALID_ARG for a bad argument or an empty output,
+ * CONV_ERR_UNSUPPORTED when an index would overflow the kernels' 32-bit coordinates.  The plan queries the current
+ * device's SM count; without a device it plans for 152 SMs.  *out is set only on CONV_OK.
+ */
+conv_status conv_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, int64_t C, int64_t K,
+                             const int64_t* spatial, const int64_t* filter, const int64_t* stride,
+                             const int64_t* pad, const int64_t* dilation, conv_dtype dtype,
+                             conv_epilogue epilogue);
+
+/* Output extents (ndim values, outermost first) into out_spatial. */
+conv_status conv_plan_output_shape(conv_plan_t plan, int64_t* out_spatial);
+
+/* Bytes of the prepacked weight buffer that conv_prepack_weights writes (0 on a NULL plan). */
+size_t conv_prepacked_weight_bytes(conv_plan_t plan);
+
+/* Bytes of device workspace conv_fwd needs (0 unless the plan splits the reduction). */
+size_t conv_workspace_bytes(conv_plan_t plan);
+
+/*
+ * Attach a caller-owned device workspace of at least conv_workspace_bytes(plan) bytes.
+ * The plan keeps the pointer, not the memory.  CONV_ERR_WORKSPACE if too small.
+ */
+conv_status conv_plan_set_workspace(conv_plan_t plan, void* workspace, size_t bytes);
+
+/*
+ * Weight prepack, once per weight tensor (page "[ET-VK] conv1d ...", "Suggested fix":
+ * weight prepacking is part of the conv2d machinery the conv1d case reuses).
+ * Reads w (layout G K [Z][Y] X C, the plan's dtype) and writes the plan-specific packed
+ * image into w_packed (conv_prepacked_weight_bytes(plan) bytes): for the tensor-core
+ * variant, per group, per N tile and per 64-element K block, a 128-byte-swizzled
+ * K-major tile that is copied into shared memory verbatim; for the FFMA variant, a
+ * (taps*C) x K_padded row-major matrix.  Asynchronous on `stream`.
+ */
+conv_status conv_prepack_weights(conv_plan_t plan, const void* w, void* w_packed, void* stream);
+
+/*
+ * The forward pass (the hot path).  x, w_packed (from conv_prepack_weights with the
+ * same plan), bias (G*K values of the plan's dtype; required when the epilogue adds a
+ * bias, ignored otherwise) and y are device pointers; y must not overlap x.
+ * Enqueues the kernel(s) on `stream` and returns; launch errors come back as
+ * CONV_ERR_CUDA.  Plans that split the reduction need a workspace set first.
+ */
+conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, const void* bias, void* y,
+                     void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word.  Returns
+ * CONV_ERR_TIMEOUT if a kernel abandoned a pipeline wait since the last check,
+ * CONV_ERR_CUDA if the stream reports an error, CONV_OK otherwise.
+ */
+conv_status conv_plan_check(conv_plan_t plan, void* stream);
+
+/* Free the plan's host memory.  NULL is accepted. */
+conv_status conv_plan_destroy(conv_plan_t plan);
+
+/* Static string naming a status code. */
+const char* conv_status_string(conv_status status);
+
+/*
+ * Static-per-plan description of the choice made: variant, tile, stages, splits,
+ * grid and gather mode.  Valid until the plan is destroyed.
+ */
+const char* conv_plan_describe(conv_plan_t plan);
+
+/*
+ * Useful FLOPs of one conv_fwd: 2 * N*Do*Ho*Wo * G*K * taps*C, padded taps counted
+ * (the convention of page "[ET-VK] conv1d ...", "Measurements": 31.3 GFLOP/s for the
+ * 80 -> 384 layer at 17.7 ms).  0 on a NULL plan.
+ */
+double conv_plan_flops(conv_plan_t plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONVFWD_CONV_H */

@@ -1,0 +1,145 @@
+"""Shared test helpers: run one layer through the C-ABI on the GPU, run the oracle on the
+same inputs, and compare under the per-element bound.
+
+Tolerance (the bound the conv path must meet, per output element):
+    |gpu - oracle| <= L * rel * S + 2 * u_out * |oracle|
+  rel   = 1e-5 for fp32 I/O, 8e-3 for bf16 I/O (fp32 accumulation);
+  S     = sum |x*w| over the receptive field (fp64, from the oracle);
+  L     = 1.13 when a GELU follows (a bound on the slope of x*Phi(x)), else 1;
+  u_out = unit roundoff of the output type (2^-24 fp32, 2^-8 bf16): the single rounding
+          of the stored result, and the fp32 bias add / GELU evaluation, which S does not
+          scale because the bias is outside the sum.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from convolution_forward_implicit_gb300 import synthetic as syn
+from convolution_forward_implicit_gb300.binding import (CONV_BF16, CONV_EPI_BIAS_GELU, CONV_EPI_GELU, CONV_F32,
+                                                        ConvPlan)
+
+GELU_LIPSCHITZ = 1.13
+
+
+def rel_for(dtype: str) -> float:
+    return 1e-5 if dtype == "f32" else 8e-3
+
+
+def uout_for(dtype: str) -> float:
+    return 2.0 ** -24 if dtype == "f32" else 2.0 ** -8
+
+
+def tolerance(dtype, epilogue, ref, S):
+    L = GELU_LIPSCHITZ if epilogue in (CONV_EPI_BIAS_GELU, CONV_EPI_GELU) else 1.0
+    return L * rel_for(dtype) * S + 2.0 * uout_for(dtype) * np.abs(ref) + 1e-30
+
+
+def to_device(a: np.ndarray, dtype: str):
+    import torch
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def from_device(t, dtype: str) -> np.ndarray:
+    """Storage array back on the host (float32, or uint16 bf16 bits)."""
+    import torch
+    if dtype == "bf16":
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.float().cpu().numpy()
+
+
+def geom_of(layer) -> oracle.Geom:
+    return oracle.Geom(layer.N, layer.G, layer.C, layer.K, layer.spatial, layer.filter, layer.stride, layer.pad,
+                       layer.dilation)
+
+
+def has_bias(epilogue) -> bool:
+    from convolution_forward_implicit_gb300.binding import CONV_EPI_BIAS
+    return epilogue in (CONV_EPI_BIAS, CONV_EPI_BIAS_GELU)
+
+
+def run_gpu(layer, dtype: str, x, w, b, env=None, stream=None, guard=0):
+    """One conv_fwd through the C-ABI.  Returns (storage output, plan description).
+    With guard > 0 the output sits inside a buffer with `guard` sentinel elements on each
+    side, and the sentinels are checked afterwards."""
+    import os
+    import torch
+    code = CONV_BF16 if dtype == "bf16" else CONV_F32
+    old = {}
+    for k, v in (env or {}).items():
+        old[k] = os.environ.get(k)
+        os.environ[k] = str(v)
+    try:
+        plan = ConvPlan(*layer.plan_args(code))
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    plan.allocate()
+    xd, wd = to_device(x, dtype), to_device(w, dtype)
+    bd = to_device(b, dtype) if b is not None else None
+    plan.prepack(wd)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    n = int(np.prod(plan.y_shape()))
+    if guard:
+        buf = torch.full((n + 2 * guard,), -12345.0, dtype=tdt, device="cuda")
+        buf = buf.view(-1)
+        # keep the 16-byte alignment of the output start
+        y = buf[guard:guard + n].view(plan.y_shape())
+    else:
+        y = torch.empty(plan.y_shape(), dtype=tdt, device="cuda")
+    plan.forward(xd, bd if has_bias(layer.epilogue) else None, y)
+    plan.check()
+    torch.cuda.synchronize()
+    if guard:
+        sent = torch.cat([buf[:guard], buf[guard + n:]]).float()
+        assert bool((sent == -12345.0).all()), "kernel wrote outside its output"
+    desc = plan.describe()
+    out = from_device(y.contiguous(), dtype)
+    plan.close()
+    return out, desc
+
+
+def oracle_full(layer, dtype, x, w, b):
+    g = geom_of(layer)
+    gelu = layer.epilogue in (CONV_EPI_BIAS_GELU, CONV_EPI_GELU)
+    bb = syn.as_f32(b, dtype) if (b is not None and has_bias(layer.epilogue)) else None
+    ref, S = oracle.conv_fwd(g, syn.as_f32(x, dtype), syn.as_f32(w, dtype), bb, gelu=gelu)
+    return ref.reshape(-1), S.reshape(-1)
+
+
+def oracle_points(layer, dtype, x, w, b, flat_idx, y_shape):
+    g = geom_of(layer)
+    gelu = layer.epilogue in (CONV_EPI_BIAS_GELU, CONV_EPI_GELU)
+    bb = syn.as_f32(b, dtype) if (b is not None and has_bias(layer.epilogue)) else None
+    # y_shape is the caller's ndim form; the oracle indexes n, od, oh, ow, g, k
+    full_shape = g.y_shape()
+    coords = np.array(np.unravel_index(flat_idx, full_shape)).T
+    ref, S = oracle.conv_fwd_points(g, syn.as_f32(x, dtype), syn.as_f32(w, dtype), bb, gelu, coords)
+    return ref, S
+
+
+def assert_within(dtype, epilogue, got_storage, ref, S, what=""):
+    got = syn.as_f32(got_storage, dtype).astype(np.float64).reshape(-1)
+    tol = tolerance(dtype, epilogue, ref, S)
+    err = np.abs(got - ref)
+    bad = np.nonzero(~(err <= tol))[0]
+    if len(bad):
+        i = bad[np.argmax(err[bad] / tol[bad])]
+        raise AssertionError(f"{what}: {len(bad)}/{len(ref)} outside bound; worst at {i}: gpu={got[i]!r} "
+                             f"oracle={ref[i]!r} S={S[i]!r} tol={tol[i]!r}")
+    ratio = float(np.max(err / tol)) if len(err) else 0.0
+    cos = float(np.dot(got, ref) / (np.linalg.norm(got) * np.linalg.norm(ref) + 1e-300))
+    return ratio, cos
+
+
+def sample_indices(total: int, n: int, seed: int) -> np.ndarray:
+    """n distinct pseudo-random flat indices plus the first and last elements."""
+    rng = np.random.default_rng(seed)
+    n = min(n, total)
+    idx = rng.choice(total, size=n, replace=False) if total > n else np.arange(total)
+    return np.unique(np.concatenate([idx, [0, total - 1]])).astype(np.int64)

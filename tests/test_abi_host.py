@@ -1,0 +1,176 @@
+"""Host-side checks of the C-ABI library that need no GPU: it loads, exports every symbol
+include/conv.h declares, and its plan logic (validation, output shape, FLOP count,
+variant choice, argument checks of conv_fwd) behaves as documented.  No call here
+launches a kernel."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from convolution_forward_implicit_gb300 import binding as B
+from convolution_forward_implicit_gb300.workloads import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from convolution_forward_implicit_gb300.build import build_library
+    build_library()
+    return B.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "conv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_][a-z_0-9]*\**\s+\**(conv_[a-z_0-9]+)\s*\(", src, re.M)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(B.EXPORTED)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = B.conv_status_string(code)
+        assert s.startswith("CONV_") and "UNKNOWN" not in s
+    assert B.conv_status_string(99) == "CONV_ERR_UNKNOWN"
+
+
+def plan(ndim=1, N=1, G=1, C=8, K=8, spatial=(10,), filt=(3,), stride=(1,), pad=(1,), dil=(1,), dtype=B.CONV_BF16,
+         epi=B.CONV_EPI_BIAS):
+    return B.conv_plan_create(ndim, N, G, C, K, spatial, filt, stride, pad, dil, dtype, epi)
+
+
+@pytest.mark.parametrize("kw", [dict(ndim=0), dict(ndim=4, spatial=(1, 1, 1, 1), filt=(1,) * 4, stride=(1,) * 4,
+                                                     pad=(0,) * 4, dil=(1,) * 4),
+                                dict(N=0), dict(G=0), dict(C=0), dict(K=-1), dict(stride=(0,)), dict(pad=(-1,)),
+                                dict(dil=(0,)), dict(spatial=(0,)), dict(filt=(0,)),
+                                dict(spatial=(2,), filt=(5,), pad=(0,)),           # empty output
+                                dict(dtype=7), dict(epi=9)])
+def test_plan_rejects_invalid_arguments(lib, kw):
+    with pytest.raises(B.ConvError) as e:
+        plan(**kw)
+    assert e.value.status == B.CONV_ERR_INVALID_ARG
+
+
+def test_plan_rejects_sizes_beyond_32_bit_indexing(lib):
+    with pytest.raises(B.ConvError) as e:
+        plan(N=1 << 20, spatial=(1 << 12,))
+    assert e.value.status == B.CONV_ERR_UNSUPPORTED
+
+
+def test_output_shape_and_flops_agree_with_the_oracle(lib):
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        nd = int(rng.integers(1, 4))
+        sp = [int(rng.integers(1, 40)) for _ in range(nd)]
+        f = [int(rng.integers(1, 6)) for _ in range(nd)]
+        s = [int(rng.integers(1, 4)) for _ in range(nd)]
+        p = [int(rng.integers(0, 4)) for _ in range(nd)]
+        d = [int(rng.integers(1, 4)) for _ in range(nd)]
+        G, C, K, N = (int(rng.integers(1, 5)), int(rng.integers(1, 40)), int(rng.integers(1, 40)),
+                      int(rng.integers(1, 4)))
+        g = oracle.Geom(N, G, C, K, sp, f, s, p, d)
+        empty = min(g.out_spatial) <= 0
+        dtype = B.CONV_BF16 if rng.integers(0, 2) else B.CONV_F32
+        if empty:
+            with pytest.raises(B.ConvError):
+                B.conv_plan_create(nd, N, G, C, K, sp, f, s, p, d, dtype, B.CONV_EPI_NONE)
+            continue
+        h = B.conv_plan_create(nd, N, G, C, K, sp, f, s, p, d, dtype, B.CONV_EPI_NONE)
+        try:
+            assert B.conv_plan_output_shape(h, nd) == g.out_spatial[3 - nd:]
+            assert B.conv_plan_flops(h) == 2.0 * g.macs()
+            desc = B.conv_plan_describe(h)
+            if dtype == B.CONV_BF16 and C % 8 == 0 and K % 8 == 0:
+                assert "variant=tc_bf16" in desc
+            else:
+                assert "variant=simt" in desc
+            assert B.conv_prepacked_weight_bytes(h) % 16 == 0 or "simt" in desc
+            assert B.conv_prepacked_weight_bytes(h) > 0
+        finally:
+            B.conv_plan_destroy(h)
+
+
+def test_workloads_plan_and_report_page_output_lengths(lib):
+    """The Whisper layers give 3000 and 1500 outputs, as printed on the page."""
+    wl = WORKLOADS["whisper_frontend_bf16"]
+    outs = []
+    for layer in wl.layers:
+        h = B.conv_plan_create(*layer.plan_args(B.CONV_BF16))
+        outs.append(B.conv_plan_output_shape(h, 1)[0])
+        B.conv_plan_destroy(h)
+    assert outs == [3000, 1500]
+    for wl in WORKLOADS.values():
+        for layer in wl.layers:
+            h = B.conv_plan_create(*layer.plan_args(wl.dtype_code))
+            assert B.conv_plan_describe(h)
+            B.conv_plan_destroy(h)
+
+
+def test_split_k_plan_needs_a_workspace(lib):
+    os.environ["CONV_FORCE_SPLITK"] = "3"
+    try:
+        h = plan(C=128, K=128, spatial=(700,))
+    finally:
+        os.environ.pop("CONV_FORCE_SPLITK")
+    try:
+        need = B.conv_workspace_bytes(h)
+        assert need > 0 and "splits=3" in B.conv_plan_describe(h)
+        with pytest.raises(B.ConvError) as e:
+            B.conv_plan_set_workspace(h, 0, 0)
+        assert e.value.status == B.CONV_ERR_WORKSPACE
+        with pytest.raises(B.ConvError) as e:
+            B.conv_plan_set_workspace(h, 4096, need - 1)
+        assert e.value.status == B.CONV_ERR_WORKSPACE
+        with pytest.raises(B.ConvError) as e:      # conv_fwd refuses before touching the GPU
+            B.conv_fwd(h, 4096, 4096, 4096, 4096, 0)
+        assert e.value.status == B.CONV_ERR_WORKSPACE
+    finally:
+        B.conv_plan_destroy(h)
+
+
+def test_conv_fwd_argument_checks_precede_any_launch(lib):
+    h = plan()
+    try:
+        for args, status in [((0, 4096, 4096, 4096), B.CONV_ERR_INVALID_ARG),
+                             ((4096, 4096, 0, 4096), B.CONV_ERR_INVALID_ARG),      # bias required
+                             ((4097, 4096, 4096, 4096), B.CONV_ERR_ALIGNMENT),
+                             ((4096, 4104, 4096, 4096), B.CONV_ERR_ALIGNMENT),
+                             ((4096, 4096, 4096, 4100), B.CONV_ERR_ALIGNMENT)]:
+            with pytest.raises(B.ConvError) as e:
+                B.conv_fwd(h, *args, 0)
+            assert e.value.status == status
+        assert lib.conv_fwd(None, None, None, None, None, None) == B.CONV_ERR_INVALID_ARG
+        assert lib.conv_prepack_weights(h, None, None, None) == B.CONV_ERR_INVALID_ARG
+        assert lib.conv_plan_output_shape(None, None) == B.CONV_ERR_INVALID_ARG
+        assert lib.conv_prepacked_weight_bytes(None) == 0 and lib.conv_workspace_bytes(None) == 0
+        assert lib.conv_plan_destroy(None) == B.CONV_OK
+    finally:
+        B.conv_plan_destroy(h)
+
+
+def test_tile_and_split_choice_fill_the_gpu(lib):
+    """Small problems split the reduction so that tiles x splits cover the SMs without a
+    second wave; large ones do not split."""
+    def desc_of(layer, code):
+        h = B.conv_plan_create(*layer.plan_args(code))
+        d = B.conv_plan_describe(h)
+        B.conv_plan_destroy(h)
+        return dict(kv.split("=") for kv in d.split())
+    l2 = WORKLOADS["whisper_frontend_bf16"].layers[1]
+    d = desc_of(l2, B.CONV_BF16)
+    assert int(d["splits"]) > 1 and int(d["units"]) <= 152
+    big = WORKLOADS["grouped3d_g4_c64_d1"].layers[0]
+    d = desc_of(big, B.CONV_BF16)
+    assert d["splits"] == "1" and d["tile"] == "128x64"
+    d = desc_of(WORKLOADS["sweep_bf16_n32"].layers[1], B.CONV_BF16)
+    assert d["tile"] == "128x256"

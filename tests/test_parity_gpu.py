@@ -1,0 +1,236 @@
+"""GPU parity: the CUDA path through the C-ABI against the CPU oracle, element by element,
+on the same seeded inputs.  Every test here needs a GB300 and the built library."""
+import os
+import zlib
+
+import numpy as np
+import pytest
+
+from convolution_forward_implicit_gb300 import synthetic as syn
+from convolution_forward_implicit_gb300.binding import (CONV_BF16, CONV_EPI_BIAS, CONV_EPI_BIAS_GELU,
+                                                        CONV_EPI_GELU, CONV_EPI_NONE, CONV_ERR_ALIGNMENT,
+                                                        CONV_ERR_WORKSPACE, CONV_F32, ConvError, ConvPlan)
+from convolution_forward_implicit_gb300.workloads import WORKLOADS, Layer, gen_inputs
+from tests.helpers import (assert_within, has_bias, oracle_full, oracle_points, run_gpu, sample_indices,
+                           to_device)
+
+pytestmark = pytest.mark.gpu
+
+FULL_ORACLE_MACS = 3e9     # above this the oracle checks sampled outputs
+
+
+def make_inputs(layer, dtype, seed, kind="normal"):
+    if kind == "int":
+        x = syn.gen_int(seed, layer.x_shape(), -3, 3, dtype)
+        w = syn.gen_int(seed + 1, layer.w_shape(), -3, 3, dtype)
+        b = syn.gen_int(seed + 2, (layer.G * layer.K,), -2, 2, dtype)
+    else:
+        x = syn.gen_normal(seed, layer.x_shape(), dtype)
+        w = syn.gen_uniform_pm(seed + 1, layer.w_shape(), layer.w_bound, dtype)
+        b = syn.gen_uniform_pm(seed + 2, (layer.G * layer.K,), 0.05, dtype)
+    return x, w, b
+
+
+def L(ndim, N, G, C, K, spatial, filt, stride, pad, dil, epi=CONV_EPI_BIAS_GELU):
+    return Layer(ndim, N, G, C, K, tuple(spatial), tuple(filt), tuple(stride), tuple(pad), tuple(dil), epi,
+                 0.05 if has_bias(epi) else None)
+
+
+# Small problems spanning several tiles with ragged tails, every ndim, groups, stride,
+# padding, dilation and epilogue; bf16 cases with C, K multiples of 8 take the tensor-core
+# path, the others the FFMA path.
+SMALL = [
+    ("1d_tc_ragged", "bf16", L(1, 2, 1, 64, 72, (301,), (3,), (1,), (1,), (1,))),
+    ("1d_tc_s2", "bf16", L(1, 1, 1, 80, 384, (517,), (3,), (2,), (1,), (1,))),
+    ("1d_tc_dil_pad", "bf16", L(1, 3, 2, 16, 24, (97,), (5,), (2,), (4,), (3,), CONV_EPI_BIAS)),
+    ("2d_tc_group", "bf16", L(2, 2, 4, 32, 40, (19, 23), (3, 3), (1, 1), (1, 1), (1, 1), CONV_EPI_NONE)),
+    ("2d_tc_dil2", "bf16", L(2, 1, 2, 64, 64, (30, 27), (3, 3), (1, 1), (1, 1), (2, 2), CONV_EPI_GELU)),
+    ("2d_tc_stride2_big_pad", "bf16", L(2, 2, 1, 24, 200, (17, 15), (5, 3), (2, 3), (3, 2), (1, 2))),
+    ("3d_tc", "bf16", L(3, 2, 2, 8, 16, (6, 9, 11), (3, 3, 3), (1, 1, 1), (1, 1, 1), (2, 1, 2), CONV_EPI_BIAS)),
+    ("3d_tc_k8", "bf16", L(3, 1, 3, 8, 8, (5, 7, 6), (3, 2, 3), (1, 2, 1), (1, 0, 1), (1, 1, 2))),
+    ("1d_tc_k264", "bf16", L(1, 1, 1, 40, 264, (260,), (3,), (1,), (1,), (1,))),
+    ("2d_tc_k512", "bf16", L(2, 1, 1, 16, 512, (12, 13), (3, 3), (1, 1), (1, 1), (1, 1))),
+    ("1d_bf16_simt_oddC", "bf16", L(1, 2, 1, 5, 7, (203,), (3,), (1,), (1,), (1,))),
+    ("2d_bf16_simt_c12", "bf16", L(2, 1, 3, 12, 20, (11, 14), (3, 3), (1, 1), (1, 1), (1, 1))),
+    ("1d_f32", "f32", L(1, 1, 1, 80, 384, (300,), (3,), (1,), (1,), (1,), CONV_EPI_BIAS)),
+    ("1d_f32_s2", "f32", L(1, 2, 1, 48, 96, (257,), (3,), (2,), (1,), (1,))),
+    ("2d_f32_group_dil", "f32", L(2, 2, 4, 8, 12, (21, 17), (3, 3), (1, 1), (2, 2), (2, 2), CONV_EPI_NONE)),
+    ("3d_f32", "f32", L(3, 1, 2, 16, 20, (5, 9, 10), (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), CONV_EPI_BIAS)),
+    ("2d_f32_odd", "f32", L(2, 3, 1, 3, 5, (13, 11), (2, 3), (1, 2), (0, 1), (1, 1))),
+    ("1d_f32_1x1", "f32", L(1, 4, 2, 20, 36, (77,), (1,), (1,), (0,), (1,))),
+    ("2d_bf16_1x1", "bf16", L(2, 2, 2, 32, 48, (9, 10), (1, 1), (1, 1), (0, 0), (1, 1))),
+    ("2d_tc_taps_in_padding", "bf16", L(2, 1, 1, 16, 16, (4, 4), (3, 3), (3, 3), (5, 5), (4, 4))),
+    ("1d_tc_tiny_M", "bf16", L(1, 1, 1, 8, 16, (1,), (1,), (1,), (0,), (1,))),
+]
+
+
+@pytest.mark.parametrize("name,dtype,layer", SMALL, ids=[s[0] for s in SMALL])
+def test_small_problems_full_parity(name, dtype, layer):
+    x, w, b = make_inputs(layer, dtype, 1000 + zlib.crc32(name.encode()) % 1000)
+    got, desc = run_gpu(layer, dtype, x, w, b, guard=64)
+    ref, S = oracle_full(layer, dtype, x, w, b)
+    assert_within(dtype, layer.epilogue, got, ref, S, f"{name} [{desc}]")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_split_k_matches_oracle_and_is_deterministic(splits, dtype):
+    layer = L(1, 1, 1, 128, 128, (700,), (3,), (2,), (1,), (1,))
+    x, w, b = make_inputs(layer, dtype, 77)
+    env = {"CONV_FORCE_SPLITK": splits}
+    got, desc = run_gpu(layer, dtype, x, w, b, env=env, guard=64)
+    assert f"splits={splits}" in desc or splits > 1
+    ref, S = oracle_full(layer, dtype, x, w, b)
+    assert_within(dtype, layer.epilogue, got, ref, S, desc)
+    again, _ = run_gpu(layer, dtype, x, w, b, env=env)
+    assert np.array_equal(got, again)
+
+
+@pytest.mark.parametrize("bn", [16, 32, 64, 128, 256])
+def test_every_tensor_core_tile_width(bn):
+    layer = L(2, 1, 2, 24, 136, (13, 37), (3, 3), (1, 1), (1, 1), (1, 1))
+    x, w, b = make_inputs(layer, "bf16", 500 + bn)
+    got, desc = run_gpu(layer, "bf16", x, w, b, env={"CONV_FORCE_BN": bn}, guard=64)
+    assert f"tile=128x{bn}" in desc
+    ref, S = oracle_full(layer, "bf16", x, w, b)
+    assert_within("bf16", layer.epilogue, got, ref, S, desc)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_integer_inputs_bit_exact(dtype):
+    """Integer x, w in [-3, 3], bias in [-2, 2]: every partial sum is an integer below 2^24,
+    so fp32 accumulation is exact in any order; fp32 output equals the oracle exactly and
+    bf16 output equals the oracle rounded to nearest even."""
+    layers = [L(1, 2, 1, 128, 80, (150,), (3,), (2,), (1,), (1,), CONV_EPI_BIAS),
+              L(2, 1, 4, 16, 24, (14, 12), (3, 3), (1, 1), (2, 1), (2, 1), CONV_EPI_BIAS),
+              L(3, 1, 2, 24, 16, (5, 6, 7), (3, 3, 3), (1, 1, 2), (1, 1, 1), (1, 1, 1), CONV_EPI_BIAS)]
+    for li, layer in enumerate(layers):
+        for splits in (1, 3):
+            x, w, b = make_inputs(layer, dtype, 900 + li, kind="int")
+            got, desc = run_gpu(layer, dtype, x, w, b, env={"CONV_FORCE_SPLITK": splits})
+            ref, _ = oracle_full(layer, dtype, x, w, b)
+            if dtype == "f32":
+                assert np.array_equal(got.reshape(-1).astype(np.float64), ref), desc
+            else:
+                assert np.array_equal(got.reshape(-1), syn.f32_to_bf16_bits(ref.astype(np.float32))), desc
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_delta_kernel_identity_and_shift_exact(dtype):
+    G, C = 2, 16
+    for t0 in [(1, 1), (0, 2), (2, 0)]:
+        layer = L(2, 2, G, C, C, (9, 20), (3, 3), (1, 1), (2, 2), (2, 2), CONV_EPI_NONE)
+        x = syn.gen_normal(31, layer.x_shape(), dtype)
+        w = np.zeros(layer.w_shape(), np.float32)
+        for gi in range(G):
+            for k in range(C):
+                w[gi, k, t0[0], t0[1], k] = 1.0
+        w = syn.to_storage(w.astype(np.float64), dtype)
+        got, desc = run_gpu(layer, dtype, x, w, None)
+        xs = syn.as_f32(x, dtype).reshape(layer.x_shape())
+        ref = np.zeros_like(xs)
+        sh = [(t - 1) * 2 for t in t0]
+        for oh in range(9):
+            for ow in range(20):
+                ih, iw = oh + sh[0], ow + sh[1]
+                if 0 <= ih < 9 and 0 <= iw < 20:
+                    ref[:, oh, ow] = xs[:, ih, iw]
+        assert np.array_equal(syn.as_f32(got, dtype).reshape(ref.shape), ref), desc
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_conv1d_is_bit_identical_to_conv2d_with_h1(dtype):
+    l1 = L(1, 2, 1, 64, 96, (301,), (3,), (2,), (1,), (2,))
+    l2 = L(2, 2, 1, 64, 96, (1, 301), (1, 3), (1, 2), (0, 1), (1, 2))
+    x, w, b = make_inputs(l1, dtype, 5)
+    a, _ = run_gpu(l1, dtype, x, w, b)
+    c, _ = run_gpu(l2, dtype, x.reshape(l2.x_shape()), w.reshape(l2.w_shape()), b)
+    assert np.array_equal(a.reshape(-1), c.reshape(-1))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_grouped_equals_independent_convs(dtype):
+    G = 3
+    lg = L(2, 2, G, 16, 24, (11, 13), (3, 3), (1, 1), (1, 1), (1, 2), CONV_EPI_BIAS)
+    l1 = L(2, 2, 1, 16, 24, (11, 13), (3, 3), (1, 1), (1, 1), (1, 2), CONV_EPI_BIAS)
+    x, w, b = make_inputs(lg, dtype, 6)
+    one_split = {"CONV_FORCE_SPLITK": 1}     # same reduction order in both runs
+    got, _ = run_gpu(lg, dtype, x, w, b, env=one_split)
+    got = syn.as_f32(got, dtype).reshape(2, 11, 13, G, 24)
+    xs, ws, bs = x.reshape(lg.x_shape()), w.reshape(lg.w_shape()), b.reshape(G, 24)
+    for gi in range(G):
+        one, _ = run_gpu(l1, dtype, np.ascontiguousarray(xs[..., gi:gi + 1, :]), np.ascontiguousarray(ws[gi:gi + 1]),
+                         np.ascontiguousarray(bs[gi]), env=one_split)
+        assert np.array_equal(syn.as_f32(one, dtype).reshape(2, 11, 13, 24), got[..., gi, :])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_linearity_power_of_two_exact(dtype):
+    layer = L(2, 1, 2, 32, 32, (15, 16), (3, 3), (1, 1), (1, 1), (1, 1), CONV_EPI_NONE)
+    x, w, _ = make_inputs(layer, dtype, 8)
+    x2 = syn.to_storage(2.0 * syn.as_f32(x, dtype).astype(np.float64), dtype)
+    a, _ = run_gpu(layer, dtype, x, w, None)
+    c, _ = run_gpu(layer, dtype, x2, w, None)
+    assert np.array_equal(2.0 * syn.as_f32(a, dtype), syn.as_f32(c, dtype))
+
+
+def test_error_paths_workspace_and_alignment():
+    import torch
+    layer = L(1, 1, 1, 64, 128, (700,), (3,), (2,), (1,), (1,))
+    os.environ["CONV_FORCE_SPLITK"] = "3"
+    try:
+        plan = ConvPlan(*layer.plan_args(CONV_BF16))
+    finally:
+        os.environ.pop("CONV_FORCE_SPLITK")
+    x = torch.zeros(layer.x_shape(), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(plan.y_shape(), dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros(128, dtype=torch.bfloat16, device="cuda")
+    plan.w_packed = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ConvError) as e:
+        plan.forward(x, b, y)
+    assert e.value.status == CONV_ERR_WORKSPACE
+    plan.allocate()
+    xflat = x.view(-1)
+    with pytest.raises(ConvError) as e:
+        from convolution_forward_implicit_gb300.binding import conv_fwd
+        conv_fwd(plan.handle, xflat[1:].data_ptr(), plan.w_packed.data_ptr(), b.data_ptr(), y.data_ptr(), 0)
+    assert e.value.status == CONV_ERR_ALIGNMENT
+    plan.check()
+    plan.close()
+
+
+def _workload_parity(name, sample_n=6000):
+    wl = WORKLOADS[name]
+    x, params = gen_inputs(wl)
+    cur = x
+    report = []
+    for li, layer in enumerate(wl.layers):
+        w, b = params[li]
+        got, desc = run_gpu(layer, wl.dtype, cur, w, b)
+        macs = int(np.prod(got.shape)) * layer.C * layer.taps
+        if macs <= FULL_ORACLE_MACS:
+            ref, S = oracle_full(layer, wl.dtype, cur, w, b)
+            ratio, cos = assert_within(wl.dtype, layer.epilogue, got, ref, S, f"{name} layer {li} [{desc}]")
+        else:
+            idx = sample_indices(got.size, sample_n, 17 + li)
+            ref, S = oracle_points(layer, wl.dtype, cur, w, b, idx, got.shape)
+            ratio, cos = assert_within(wl.dtype, layer.epilogue, got.reshape(-1)[idx], ref, S,
+                                       f"{name} layer {li} sampled [{desc}]")
+            assert np.isfinite(syn.as_f32(got, wl.dtype)).all()
+        report.append((li, desc, ratio, cos))
+        cur = got.reshape(layer.N, *layer_out_spatial(layer), layer.G * layer.K)   # next layer's input (GPU bits)
+    return report
+
+
+def layer_out_spatial(layer):
+    import oracle
+    return tuple(oracle.out_len(i, f, s, p, d) for i, f, s, p, d in
+                 zip(layer.spatial, layer.filter, layer.stride, layer.pad, layer.dilation))
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workload_full_size_parity(name):
+    """Every workload at its full size, in the configuration the benchmark times.  Chained
+    layers: layer l+1's oracle reads the GPU's layer-l output bits, so each layer meets
+    the bound on its own."""
+    _workload_parity(name)
