@@ -22,6 +22,7 @@ __all__ = [
     "conv_plan_create", "conv_plan_output_shape", "conv_prepacked_weight_bytes", "conv_workspace_bytes",
     "conv_plan_set_workspace", "conv_prepack_weights", "conv_fwd", "conv_plan_check", "conv_plan_destroy",
     "conv_status_string", "conv_plan_describe", "conv_plan_flops", "ConvPlan", "EXPORTED",
+    "conv_fwd_static_scratch", "CONV_STATIC_SCRATCH_BYTES",
 ]
 
 CONV_OK, CONV_ERR_INVALID_ARG, CONV_ERR_UNSUPPORTED, CONV_ERR_ALIGNMENT = 0, 1, 2, 3
@@ -50,7 +51,9 @@ _SIGS = {
     "conv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "conv_plan_describe": (ctypes.c_char_p, [_VP]),
     "conv_plan_flops": (ctypes.c_double, [_VP]),
+    "conv_fwd_static_scratch": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP]),
 }
+CONV_STATIC_SCRATCH_BYTES = 16 << 20
 EXPORTED = tuple(_SIGS)
 
 
@@ -129,6 +132,13 @@ def conv_prepack_weights(plan: int, w_ptr: int, w_packed_ptr: int, stream: int =
 def conv_fwd(plan: int, x_ptr: int, w_packed_ptr: int, bias_ptr: int, y_ptr: int, stream: int = 0):
     _check(load_library().conv_fwd(plan, x_ptr, w_packed_ptr, bias_ptr or None, y_ptr, stream or None),
            "conv_fwd")
+
+
+def conv_fwd_static_scratch(plan: int, x_ptr: int, w_packed_ptr: int, bias_ptr: int, y_ptr: int, stream: int = 0):
+    """conv_fwd for callers that cannot allocate: split-K scratch lives in the library's
+    own device array (CONV_STATIC_SCRATCH_BYTES); see include/conv.h."""
+    _check(load_library().conv_fwd_static_scratch(plan, x_ptr, w_packed_ptr, bias_ptr or None, y_ptr,
+                                                  stream or None), "conv_fwd_static_scratch")
 
 
 def conv_plan_check(plan: int, stream: int = 0):

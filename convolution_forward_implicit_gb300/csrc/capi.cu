@@ -441,6 +441,91 @@ const char* conv_status_string(conv_status status) {
 
 const char* conv_plan_describe(conv_plan_t plan) { return plan ? plan->desc : ""; }
 
+}  // extern "C"
+
+// ----------------------------------------------------------------------------- allocation-free forward
+// Split-K partial sums in a file-scope device array, for callers that cannot allocate
+// device memory (see conv_fwd_static_scratch in conv.h).
+namespace {
+__device__ __align__(256) float g_static_scratch[CONV_STATIC_SCRATCH_BYTES / sizeof(float)];
+
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[64];
+
+// Device address of the array on the current device, looked up once per device.
+float* static_scratch_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+        g_scratch_ptr[dev] = static_cast<float*>(p);
+    }
+    return g_scratch_ptr[dev];
+}
+
+conv_status launch_reduce_into(conv_plan_t plan, const float* ws, const void* bias, void* y, cudaStream_t s) {
+    const Geom& g = plan->g;
+    const long long MGK = (long long)g.M * g.G * g.K;
+    const int threads = 256;
+    const long long work = (g.G * g.K) % 4 == 0 ? MGK / 4 : MGK;
+    const int blocks = (int)std::min<long long>(cdiv(work, threads), (long long)plan->sm_count * 8);
+    if (plan->dtype == CONV_BF16)
+        splitk_reduce_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
+            ws, plan->splits, MGK, g.G * g.K, static_cast<const __nv_bfloat16*>(bias),
+            static_cast<__nv_bfloat16*>(y), (int)plan->epi);
+    else
+        splitk_reduce_kernel<float><<<blocks, threads, 0, s>>>(ws, plan->splits, MGK, g.G * g.K,
+                                                               static_cast<const float*>(bias),
+                                                               static_cast<float*>(y), (int)plan->epi);
+    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" conv_status conv_fwd_static_scratch(conv_plan_t plan, const void* x, const void* w_packed,
+                                               const void* bias, void* y, void* stream) {
+    if (!plan || !x || !w_packed || !y) return CONV_ERR_INVALID_ARG;
+    const bool needs_bias = plan->epi == CONV_EPI_BIAS || plan->epi == CONV_EPI_BIAS_GELU;
+    if (needs_bias && !bias) return CONV_ERR_INVALID_ARG;
+    if (misaligned(x) || misaligned(w_packed) || misaligned(y) || (needs_bias && misaligned(bias)))
+        return CONV_ERR_ALIGNMENT;
+    if (plan->workspace_bytes > CONV_STATIC_SCRATCH_BYTES) return CONV_ERR_WORKSPACE;
+    float* scratch = nullptr;
+    if (plan->workspace_bytes) {
+        scratch = static_scratch_ptr();
+        if (!scratch) return CONV_ERR_CUDA;
+    }
+    unsigned* err = error_word_ptr();
+    if (!err) return CONV_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (plan->variant == VAR_TC_BF16) {
+        TcParams tp;
+        tp.g = plan->g;
+        tp.x = x; tp.wpack = w_packed; tp.bias = needs_bias ? bias : nullptr; tp.y = y;
+        tp.ws = scratch;
+        tp.err = err;
+        tp.BN = plan->BN; tp.num_mt = plan->num_mt; tp.num_nt = plan->num_nt; tp.nkb = plan->nkb;
+        tp.nchunks = plan->nchunks; tp.cpt = plan->cpt; tp.splits = plan->splits; tp.kbps = plan->kbps;
+        tp.epi = (int)plan->epi; tp.total_units = plan->total_units;
+        e = launch_tc_bf16(tp, plan->stages, plan->grid, s);
+    } else {
+        SimtParams sp;
+        sp.g = plan->g;
+        sp.x = x; sp.wpack = w_packed; sp.bias = needs_bias ? bias : nullptr; sp.y = y;
+        sp.ws = scratch;
+        sp.Kg = plan->Kg; sp.Kpad = plan->Kpad; sp.num_mt = plan->num_mt; sp.num_nt = plan->num_nt;
+        sp.nkt = plan->nkt; sp.splits = plan->splits; sp.ktps = plan->ktps; sp.epi = (int)plan->epi;
+        e = launch_simt(sp, plan->dtype == CONV_BF16, plan->BM, plan->vec != 0, s);
+    }
+    if (e != cudaSuccess) return CONV_ERR_CUDA;
+    if (plan->splits > 1) return launch_reduce_into(plan, scratch, needs_bias ? bias : nullptr, y, s);
+    return CONV_OK;
+}
+
+extern "C" {
+
 double conv_plan_flops(conv_plan_t plan) { return plan ? plan->flops : 0.0; }
 
 }  // extern "C"

@@ -156,6 +156,38 @@ const char* conv_plan_describe(conv_plan_t plan);
  */
 double conv_plan_flops(conv_plan_t plan);
 
+/*
+ * Forward pass for callers that cannot allocate device memory.  (The pages have no
+ * counterpart: this is an interface convenience of this library.)
+ *
+ * Some callers cannot call cudaMalloc: a plugin or custom operator that a host
+ * framework hands only its input and output buffers and no allocator, or a
+ * latency-critical loop that must not allocate after start-up (cudaMalloc may
+ * synchronise the device).  Such callers cannot provide the split-K workspace that
+ * conv_fwd needs for small problems.  This entry point computes the same result as
+ * conv_fwd, but keeps the split-K partial sums in a device array that is part of the
+ * library itself (CONV_STATIC_SCRATCH_BYTES bytes, reserved on every GPU that loads
+ * the library, until the process exits).  The caller still passes x, w_packed, bias
+ * and y; the plan's own workspace, if any, is not used.
+ *
+ *  - Limit: a plan whose conv_workspace_bytes() exceeds CONV_STATIC_SCRATCH_BYTES is
+ *    rejected with CONV_ERR_WORKSPACE before anything is launched.  Plans that do not
+ *    split the reduction need no scratch and always run.
+ *  - No allocation: the call makes no cudaMalloc, cudaFree or other allocating call.
+ *  - Set-up: the first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make that first
+ *    call before any stream capture begins.
+ *  - Sharing: every call in the process uses the same array.  It keeps whatever the
+ *    last call left in it; nothing in it has to start at zero, because every split
+ *    writes its whole partial sum before the reduction reads it.  Calls that overlap on
+ *    the GPU (on different streams, or from different host threads) race on the array
+ *    and give wrong results: serialise them.
+ * Errors as for conv_fwd.
+ */
+#define CONV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+conv_status conv_fwd_static_scratch(conv_plan_t plan, const void* x, const void* w_packed, const void* bias,
+                                    void* y, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
