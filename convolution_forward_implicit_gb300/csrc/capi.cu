@@ -11,6 +11,8 @@
 #include <mutex>
 #include <new>
 
+#include <cudaTypedefs.h>
+
 #include "../../include/conv.h"
 #include "internal.h"
 
@@ -39,8 +41,12 @@ unsigned* error_word_ptr() {
 // Tensor-core layout: per (group, N tile, 64-wide K block) a BN x 128-byte tile whose
 // 16-byte chunk j of row n sits at chunk position j ^ (n & 7): the 128-byte swizzle the
 // MMA's shared-memory descriptor expects, so the tile is copied into shared memory as is.
+// K order: per_tap = 0 packs the (tap, c) chunks densely (K block kb holds chunks
+// 8kb..8kb+7, crossing taps); per_tap = 1 gives every tap cbt whole 64-channel blocks
+// (K block kb = tap*cbt + b holds channels 64b..64b+63 of that tap), matching one TMA box.
 __global__ void prepack_tc_kernel(const uint4* __restrict__ w, uint4* __restrict__ out, int K, int C, int taps,
-                                  int BN, int num_nt, int nkb, int nchunks, int cpt, long long total16) {
+                                  int BN, int num_nt, int nkb, int nchunks, int cpt, int per_tap, int cbt,
+                                  long long total16) {
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total16;
          idx += (long long)gridDim.x * blockDim.x) {
         const int j = (int)(idx & 7);
@@ -50,15 +56,53 @@ __global__ void prepack_tc_kernel(const uint4* __restrict__ w, uint4* __restrict
         const int nt = (int)(r % num_nt);
         const int g = (int)(r / num_nt);
         const int k = nt * BN + n;
-        const int q = kb * 8 + j;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (k < K && q < nchunks) {
-            const int tap = q / cpt;
-            const int c0 = (q - tap * cpt) * 8;
-            v = w[((((long long)g * K + k) * taps + tap) * C + c0) / 8];
+        int tap, c0;
+        bool ok;
+        if (per_tap) {
+            tap = kb / cbt;
+            c0 = (kb - tap * cbt) * 64 + j * 8;
+            ok = c0 < C;
+        } else {
+            const int q = kb * 8 + j;
+            ok = q < nchunks;
+            tap = ok ? q / cpt : 0;
+            c0 = (q - tap * cpt) * 8;
         }
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (k < K && ok) v = w[((((long long)g * K + k) * taps + tap) * C + c0) / 8];
         const long long tile = (((long long)g * num_nt + nt) * nkb + kb) * BN + n;
         out[tile * 8 + (j ^ (n & 7))] = v;
+    }
+}
+
+// 3xTF32 layout: per (group, N tile, K block) a BN x 128-byte tile of the high parts
+// (w with its low 13 mantissa bits cleared: exact in TF32) followed by the same tile of the
+// low parts (w - high, exact in fp32), both 128-byte swizzled.  K block kb = tap*cbt + b
+// holds channels 32b..32b+31 of that tap; 16-byte chunk j holds channels 32b+4j..+3.
+__global__ void prepack_tf32x3_kernel(const float4* __restrict__ w, uint4* __restrict__ out, int K, int C,
+                                      int taps, int BN, int num_nt, int nkb, int cbt, long long total16) {
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total16;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int j = (int)(idx & 7);
+        long long r = idx >> 3;
+        const int n = (int)(r % BN); r /= BN;
+        const int kb = (int)(r % nkb); r /= nkb;
+        const int nt = (int)(r % num_nt);
+        const int g = (int)(r / num_nt);
+        const int k = nt * BN + n;
+        const int tap = kb / cbt;
+        const int c0 = (kb - tap * cbt) * 32 + j * 4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < K && c0 < C) v = w[((((long long)g * K + k) * taps + tap) * C + c0) / 4];
+        uint4 hi, lo;
+        hi.x = __float_as_uint(v.x) & 0xFFFFE000u; hi.y = __float_as_uint(v.y) & 0xFFFFE000u;
+        hi.z = __float_as_uint(v.z) & 0xFFFFE000u; hi.w = __float_as_uint(v.w) & 0xFFFFE000u;
+        lo.x = __float_as_uint(v.x - __uint_as_float(hi.x)); lo.y = __float_as_uint(v.y - __uint_as_float(hi.y));
+        lo.z = __float_as_uint(v.z - __uint_as_float(hi.z)); lo.w = __float_as_uint(v.w - __uint_as_float(hi.w));
+        const long long tile = (((long long)g * num_nt + nt) * nkb + kb);
+        const long long rowpos = (long long)n * 8 + (j ^ (n & 7));
+        out[tile * 2 * BN * 8 + rowpos] = hi;
+        out[tile * 2 * BN * 8 + (long long)BN * 8 + rowpos] = lo;
     }
 }
 
@@ -125,7 +169,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, l
 }  // namespace
 
 // ----------------------------------------------------------------------------- plan
-enum Variant { VAR_TC_BF16 = 0, VAR_SIMT = 1 };
+enum Variant { VAR_TC = 0, VAR_SIMT = 1 };
 
 struct conv_plan {
     int ndim;
@@ -137,6 +181,7 @@ struct conv_plan {
     Variant variant;
     // tensor-core plan
     int BN, stages, num_mt, num_nt, nkb, nchunks, cpt, splits, kbps, total_units, grid;
+    int tma, map_kind, BW, BH, tiles_w, tiles_h, cbt, tf32;
     // SIMT plan
     int BM, Kg, Kpad, nkt, ktps, vec;
     size_t prepack_bytes, workspace_bytes;
@@ -164,11 +209,95 @@ static int query_sm_count() {
     return n;
 }
 
+// ---- activation tensor map (TMA gather) ----
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!tried) {
+        tried = true;
+        void* f = nullptr;
+        void* init = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        // the encoder needs an initialised driver, which a plan made before any CUDA
+        // context exists would not have: initialise it (idempotent)
+        if (cudaGetDriverEntryPointByVersion("cuInit", &init, 2000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess &&
+            reinterpret_cast<PFN_cuInit_v2000>(init)(0) == CUDA_SUCCESS &&
+            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// The input as a 5-D tensor for tiled TMA boxes of one 128-byte channel block (64 bf16 or
+// 32 fp32 channels) x BW x BH output pixels:
+// map_kind 0: {G*C, W, H, D, N} (C a multiple of the block, or G = 1: a box never reads another
+// group's channels); map_kind 1: {C, G, W, H, N} (D = Z = 1).  The conv stride is the
+// box's element stride; padding and the channel tail read as zero (out of range).
+static bool encode_act_map(const conv_plan* p, const void* x, CUtensorMap* map) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const Geom& g = p->g;
+    const cuuint64_t e = p->tf32 ? 4 : 2;         // fp32 or bf16
+    const cuuint32_t cblk = p->tf32 ? 32 : 64;    // channels in one 128-byte row
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5], es[5];
+    if (p->map_kind == 0) {
+        dims[0] = (cuuint64_t)g.G * g.C; dims[1] = g.W; dims[2] = g.H; dims[3] = g.D; dims[4] = g.N;
+        strides[0] = dims[0] * e;
+        strides[1] = strides[0] * g.W;
+        strides[2] = strides[1] * g.H;
+        strides[3] = strides[2] * g.D;
+        box[0] = cblk; box[1] = (cuuint32_t)(p->BW * g.sw); box[2] = (cuuint32_t)(p->BH * g.sh); box[3] = 1; box[4] = 1;
+        es[0] = 1; es[1] = (cuuint32_t)g.sw; es[2] = (cuuint32_t)g.sh; es[3] = 1; es[4] = 1;
+    } else {
+        dims[0] = g.C; dims[1] = g.G; dims[2] = g.W; dims[3] = g.H; dims[4] = g.N;
+        strides[0] = (cuuint64_t)g.C * e;
+        strides[1] = (cuuint64_t)g.G * g.C * e;
+        strides[2] = strides[1] * g.W;
+        strides[3] = strides[2] * g.H;
+        box[0] = cblk; box[1] = 1; box[2] = (cuuint32_t)(p->BW * g.sw); box[3] = (cuuint32_t)(p->BH * g.sh); box[4] = 1;
+        es[0] = 1; es[1] = 1; es[2] = (cuuint32_t)g.sw; es[3] = (cuuint32_t)g.sh; es[4] = 1;
+    }
+    const CUresult r = fn(map, p->tf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+                          const_cast<void*>(x), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Output tile BH x BW (<= 128 pixels of one output plane) that wastes the fewest MMA rows.
+static void choose_tile_shape(conv_plan* p) {
+    const Geom& g = p->g;
+    int best_bw = 1, best_bh = 1;
+    double best = -1.0;
+    for (int k = 1; k <= 16; ++k) {
+        const int bw = std::min<int64_t>(128, cdiv(g.Wo, k));
+        if (bw * g.sw > 256) continue;
+        int bh = std::max(1, std::min(g.Ho, 128 / bw));
+        while (bh > 1 && bh * g.sh > 256) --bh;
+        const double tiles = (double)cdiv(g.Wo, bw) * (double)cdiv(g.Ho, bh);
+        const double eff = (double)g.Wo * g.Ho / (tiles * 128.0);
+        if (eff > best + 1e-9) { best = eff; best_bw = bw; best_bh = bh; }
+        if (bw == 1) break;
+    }
+    p->BW = best_bw;
+    p->BH = best_bh;
+    p->tiles_w = (int)cdiv(g.Wo, best_bw);
+    p->tiles_h = (int)cdiv(g.Ho, best_bh);
+}
+
 // Tensor-core tile choice: BN from the compiled set, the smallest padded width for K
 // <= 256, else 256 or 128, whichever wastes fewer columns; then split-K when the tiles
 // alone leave SMs idle (page "onnxruntime PR #33639", "Description": large tiles for
 // large problems, split-K for small problems because it fills the GPU better).
-static void plan_tc(conv_plan* p) {
+static bool plan_tc(conv_plan* p, bool tf32) {
     const Geom& g = p->g;
     int bn;
     if (g.K <= 16) bn = 16;
@@ -179,12 +308,45 @@ static void plan_tc(conv_plan* p) {
     else bn = (cdiv(g.K, 256) * 256 - g.K <= cdiv(g.K, 128) * 128 - g.K) ? 256 : 128;
     const int force_bn = env_int("CONV_FORCE_BN", 0);
     if (force_bn == 16 || force_bn == 32 || force_bn == 64 || force_bn == 128 || force_bn == 256) bn = force_bn;
+    p->tf32 = tf32 ? 1 : 0;
     p->BN = bn;
-    p->stages = bn == 256 ? 4 : bn == 128 ? 6 : 8;
+    p->stages = tc_stages_for(bn, p->tf32);
     p->cpt = g.C / 8;
     p->nchunks = g.taps * p->cpt;
-    p->nkb = (int)cdiv(p->nchunks, 8);
-    p->num_mt = (int)cdiv(g.M, 128);
+    // Gather: TMA boxes when the tensor map can express the problem and a tap has at
+    // least one full 128-byte channel block; otherwise (bf16 only) 16-byte cp.async chunks
+    // packed densely across taps.
+    const int cblk = tf32 ? 32 : 64;
+    int map_kind = -1;
+    if (g.C % cblk == 0 || g.G == 1) map_kind = 0;
+    else if (g.D == 1 && g.Z == 1) map_kind = 1;
+    bool tma = map_kind >= 0 && g.C >= cblk && g.sw <= 8 && g.sh <= 8;
+    const char* force_gather = getenv("CONV_FORCE_GATHER");
+    if (!tf32 && force_gather && strcmp(force_gather, "cpasync") == 0) tma = false;
+    if (tma) {
+        p->map_kind = map_kind;
+        choose_tile_shape(p);
+        // A trial encode with a placeholder address checks the box against the driver's
+        // limits.  The encoder needs a current context: make the current device's primary
+        // context current first (without a device the rules above decide alone).
+        int dev = 0;
+        if (encode_fn() && cudaGetDevice(&dev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess) {
+            CUtensorMap probe;
+            if (!encode_act_map(p, reinterpret_cast<const void*>((uintptr_t)4096), &probe)) tma = false;
+        }
+        cudaGetLastError();
+    }
+    if (tf32 && !tma) return false;   // 3xTF32 needs the TMA gather
+    p->tma = tma ? 1 : 0;
+    if (tma) {
+        p->cbt = (int)cdiv(g.C, cblk);
+        p->nkb = g.taps * p->cbt;
+        p->num_mt = g.N * g.Do * p->tiles_h * p->tiles_w;
+    } else {
+        p->map_kind = 0; p->BW = 128; p->BH = 1; p->tiles_w = p->tiles_h = 1; p->cbt = 0;
+        p->nkb = (int)cdiv(p->nchunks, 8);
+        p->num_mt = (int)cdiv(g.M, 128);
+    }
     p->num_nt = (int)cdiv(g.K, bn);
     const int64_t units = (int64_t)p->num_mt * g.G * p->num_nt;
     int splits = 1;
@@ -198,12 +360,20 @@ static void plan_tc(conv_plan* p) {
     p->splits = (int)cdiv(p->nkb, p->kbps);     // every split non-empty
     p->total_units = (int)(units * p->splits);
     p->grid = std::min(p->total_units, p->sm_count);
-    p->prepack_bytes = (size_t)g.G * p->num_nt * p->nkb * bn * 128;
+    p->prepack_bytes = (size_t)g.G * p->num_nt * p->nkb * bn * 128 * (tf32 ? 2 : 1);
     p->workspace_bytes = p->splits > 1 ? (size_t)p->splits * g.M * g.G * g.K * sizeof(float) : 0;
-    snprintf(p->desc, sizeof(p->desc),
-             "variant=tc_bf16 gather=cp.async tile=128x%d k_block=64 stages=%d splits=%d units=%d grid=%d "
-             "k_blocks=%d",
-             bn, p->stages, p->splits, p->total_units, p->grid, p->nkb);
+    if (p->tma)
+        snprintf(p->desc, sizeof(p->desc),
+                 "variant=%s gather=tma tile=128x%d pixels=%dx%d k_block=%d stages=%d splits=%d units=%d "
+                 "grid=%d k_blocks=%d map=%d",
+                 tf32 ? "tc_tf32x3" : "tc_bf16", bn, p->BH, p->BW, cblk, p->stages, p->splits, p->total_units,
+                 p->grid, p->nkb, p->map_kind);
+    else
+        snprintf(p->desc, sizeof(p->desc),
+                 "variant=tc_bf16 gather=cp.async tile=128x%d k_block=64 stages=%d splits=%d units=%d grid=%d "
+                 "k_blocks=%d",
+                 bn, p->stages, p->splits, p->total_units, p->grid, p->nkb);
+    return true;
 }
 
 static void plan_simt(conv_plan* p) {
@@ -293,10 +463,14 @@ conv_status conv_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, i
     g.taps = (int)taps;
     p->flops = 2.0 * (double)M * (double)G * (double)K * (double)taps * (double)C;
     p->sm_count = query_sm_count();
-    const bool tc_ok = dtype == CONV_BF16 && C % 8 == 0 && K % 8 == 0 && env_int("CONV_FORCE_SIMT", 0) == 0;
-    if (tc_ok) {
-        p->variant = VAR_TC_BF16;
-        plan_tc(p);
+    // bf16 with C, K multiples of 8: tcgen05 kind::f16.  fp32 with C, K multiples of 4 that the
+    // TMA gather can express: tcgen05 3xTF32.  Everything else: the FFMA kernel.
+    const bool no_tc = env_int("CONV_FORCE_SIMT", 0) != 0;
+    bool tc = false;
+    if (!no_tc && dtype == CONV_BF16 && C % 8 == 0 && K % 8 == 0) tc = plan_tc(p, false);
+    if (!no_tc && dtype == CONV_F32 && C % 4 == 0 && K % 4 == 0) tc = plan_tc(p, true);
+    if (tc) {
+        p->variant = VAR_TC;
     } else {
         p->variant = VAR_SIMT;
         plan_simt(p);
@@ -332,12 +506,18 @@ conv_status conv_prepack_weights(conv_plan_t plan, const void* w, void* w_packed
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Geom& g = plan->g;
     const int threads = 256;
-    if (plan->variant == VAR_TC_BF16) {
+    if (plan->variant == VAR_TC && plan->tf32) {
+        const long long total16 = (long long)(plan->prepack_bytes / 32);   // hi and lo written per chunk
+        const int blocks = (int)std::min<long long>(cdiv(total16, threads), 65535);
+        prepack_tf32x3_kernel<<<blocks, threads, 0, s>>>(static_cast<const float4*>(w), static_cast<uint4*>(w_packed),
+                                                         g.K, g.C, g.taps, plan->BN, plan->num_nt, plan->nkb,
+                                                         plan->cbt, total16);
+    } else if (plan->variant == VAR_TC) {
         const long long total16 = (long long)(plan->prepack_bytes / 16);
         const int blocks = (int)std::min<long long>(cdiv(total16, threads), 65535);
         prepack_tc_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint4*>(w), static_cast<uint4*>(w_packed),
                                                      g.K, g.C, g.taps, plan->BN, plan->num_nt, plan->nkb,
-                                                     plan->nchunks, plan->cpt, total16);
+                                                     plan->nchunks, plan->cpt, plan->tma, plan->cbt, total16);
     } else {
         const long long total = (long long)g.G * plan->Kg * plan->Kpad;
         const int blocks = (int)std::min<long long>(cdiv(total, threads), 65535);
@@ -384,7 +564,7 @@ conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, cons
     if (!err) return CONV_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (plan->variant == VAR_TC_BF16) {
+    if (plan->variant == VAR_TC) {
         TcParams tp;
         tp.g = plan->g;
         tp.x = x; tp.wpack = w_packed; tp.bias = needs_bias ? bias : nullptr; tp.y = y;
@@ -393,7 +573,11 @@ conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, cons
         tp.BN = plan->BN; tp.num_mt = plan->num_mt; tp.num_nt = plan->num_nt; tp.nkb = plan->nkb;
         tp.nchunks = plan->nchunks; tp.cpt = plan->cpt; tp.splits = plan->splits; tp.kbps = plan->kbps;
         tp.epi = (int)plan->epi; tp.total_units = plan->total_units;
-        e = launch_tc_bf16(tp, plan->stages, plan->grid, s);
+        tp.tma = plan->tma; tp.map_kind = plan->map_kind; tp.BW = plan->BW; tp.BH = plan->BH;
+        tp.tiles_w = plan->tiles_w; tp.tiles_h = plan->tiles_h; tp.cbt = plan->cbt; tp.tf32 = plan->tf32;
+        CUtensorMap map;
+        if (plan->tma && !encode_act_map(plan, x, &map)) return CONV_ERR_CUDA;
+        e = launch_tc(tp, plan->tma ? &map : nullptr, plan->stages, plan->grid, s);
     } else {
         SimtParams sp;
         sp.g = plan->g;
@@ -500,7 +684,7 @@ extern "C" conv_status conv_fwd_static_scratch(conv_plan_t plan, const void* x, 
     if (!err) return CONV_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (plan->variant == VAR_TC_BF16) {
+    if (plan->variant == VAR_TC) {
         TcParams tp;
         tp.g = plan->g;
         tp.x = x; tp.wpack = w_packed; tp.bias = needs_bias ? bias : nullptr; tp.y = y;
@@ -509,7 +693,11 @@ extern "C" conv_status conv_fwd_static_scratch(conv_plan_t plan, const void* x, 
         tp.BN = plan->BN; tp.num_mt = plan->num_mt; tp.num_nt = plan->num_nt; tp.nkb = plan->nkb;
         tp.nchunks = plan->nchunks; tp.cpt = plan->cpt; tp.splits = plan->splits; tp.kbps = plan->kbps;
         tp.epi = (int)plan->epi; tp.total_units = plan->total_units;
-        e = launch_tc_bf16(tp, plan->stages, plan->grid, s);
+        tp.tma = plan->tma; tp.map_kind = plan->map_kind; tp.BW = plan->BW; tp.BH = plan->BH;
+        tp.tiles_w = plan->tiles_w; tp.tiles_h = plan->tiles_h; tp.cbt = plan->cbt; tp.tf32 = plan->tf32;
+        CUtensorMap map;
+        if (plan->tma && !encode_act_map(plan, x, &map)) return CONV_ERR_CUDA;
+        e = launch_tc(tp, plan->tma ? &map : nullptr, plan->stages, plan->grid, s);
     } else {
         SimtParams sp;
         sp.g = plan->g;

@@ -1,5 +1,6 @@
 // Internal definitions shared by the library's translation units (not installed).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -25,10 +26,10 @@ enum : unsigned { ERR_WAIT_TIMEOUT = 1u };
 // ---- tensor-core (tcgen05) bf16 implicit GEMM ----
 struct TcParams {
     Geom g;
-    const void* x;          // bf16 N D H W G C
-    const void* wpack;      // swizzled tiles [G][NT][NKB][BN x 128 B]
-    const void* bias;       // bf16 G*K or null
-    void* y;                // bf16 N Do Ho Wo G K
+    const void* x;          // bf16 or fp32, N D H W G C
+    const void* wpack;      // swizzled tiles [G][NT][NKB][BN x 128 B] (3xTF32: hi tile then lo tile)
+    const void* bias;       // G*K of the I/O type, or null
+    void* y;                // N Do Ho Wo G K of the I/O type
     float* ws;              // split-K partials [splits][M][G*K] fp32 (splits > 1)
     unsigned* err;          // device error word
     int BN;                 // N tile (output channels per CTA tile)
@@ -39,12 +40,19 @@ struct TcParams {
     int splits, kbps;       // split-K factor and K blocks per split
     int epi;
     int total_units;        // num_mt*G*num_nt*splits
+    // TMA gather: one tiled-tensor load per K block of a BH x BW block of output pixels
+    // (one (n, od) plane) for one tap and one 64-channel block.
+    int tma;                // 1: TMA gather, 0: cp.async gather
+    int map_kind;           // 0: tensor dims {G*C, W, H, D, N}; 1: {C, G, W, H, N} (D = Z = 1)
+    int BW, BH;             // output tile extent along W and H (BW*BH <= 128 rows)
+    int tiles_w, tiles_h;   // tiles per output plane
+    int cbt;                // channel blocks per tap (64 bf16 or 32 fp32 channels; kb = tap*cbt + block)
+    int tf32;               // 1: fp32 I/O as 3xTF32 (TMA gather only)
 };
 
-// Launch the tensor-core kernel for a (BN, stages) pair chosen by the plan.
-cudaError_t launch_tc_bf16(const TcParams& p, int stages, int grid, cudaStream_t stream);
-size_t tc_smem_bytes(int BN, int stages);
-bool tc_config_supported(int BN, int stages);
+// Launch the tensor-core kernel for the (BN, stages) pair the plan picked (see tc_stages_for).
+cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, int stages, int grid, cudaStream_t stream);
+int tc_stages_for(int BN, int tf32);
 
 // ---- SIMT FFMA implicit GEMM (fp32 I/O; also bf16 where channel counts rule out the tensor path) ----
 struct SimtParams {

@@ -1,0 +1,669 @@
+// Implicit-GEMM convolution forward on the sm_103a tensor cores (tcgen05), fp32
+// accumulation in tensor memory, fused bias + GELU epilogue.  bf16 I/O multiplies bf16
+// operands (kind::f16); fp32 I/O runs as 3xTF32 (kind::tf32): every fp32 operand is split
+// into an exactly-TF32 high part and a low remainder, and three TF32 products (lo*hi,
+// hi*lo, hi*hi) recover fp32-level products.
+//
+// GEMM view per group g (page "composable_kernel ... LEARNINGS_GROUPED_CONV.md",
+// introduction: NHWGC x GKYXC -> NHWGK): rows m are output pixels (n, od, oh, ow),
+// columns are output channels k, and the reduction runs over (tap, c) with c innermost,
+// so that one 16-byte chunk of the reduction is 8 consecutive channels of one input
+// pixel.  The im2col matrix of page "[ET-VK] conv1d runs at ~3% ...", section "The
+// conv2d path already solves this", is never materialised: each A tile is gathered
+// straight from the channels-last input, zero-filled where a tap falls in the padding.
+//
+// One persistent CTA per SM, 9 warps in three roles:
+//   warps 0-3  epilogue: tcgen05.ld the 128 x BN accumulator (warp w owns TMEM lanes
+//              32w..32w+31), add bias, GELU, round to bf16, 16-byte stores; or store
+//              fp32 partials when the reduction is split.
+//   warps 4-7  producer: per 64-wide K block, 8 cp.async (16 B, zero-fill) per thread
+//              gather the 128 x 128 B activation tile into the 128-byte-swizzled K-major
+//              layout; one thread bulk-copies the prepacked weight tile (already in
+//              swizzled order) with cp.async.bulk and an mbarrier transaction count.
+//   warp 8     MMA: one thread issues tcgen05.mma (M = 128, N = BN, K = 16) x 4 per
+//              K block and tcgen05.commit to free the stage; the accumulator is double
+//              buffered in TMEM so the epilogue of tile i overlaps the main loop of i+1.
+// Every mbarrier wait is bounded: after ~1 s it raises the device error word, sets a
+// CTA-wide abort flag and the CTA winds down (drains copies, waits for issued MMAs,
+// frees TMEM).
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace convfwd {
+namespace {
+
+constexpr int BM = 128;
+constexpr int EPI_WARPS = 4;
+constexpr int LAG = 2;                                 // K blocks a cp.async producer keeps in flight
+constexpr uint32_t A_BYTES = BM * 128;                 // 128 pixels x 64 bf16
+constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier ----
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait.  Returns false if this CTA is aborting (the limit ran out here or elsewhere).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if ((n & 63u) == 0 && globaltimer() - t0 > WAIT_LIMIT_NS) {
+            *abort_flag = 1;
+            atomicOr(err, ERR_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// ---- async copies ----
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Tiled TMA load of a 5-D box (coordinates innermost first; out-of-range elements read 0).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            int c4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// ---- tcgen05 ----
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+// 32 lanes x 32 bits, 16 consecutive columns: thread t of the warp gets lane (base + t).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 B,
+// 8-row groups 1024 B apart.  Fields: start address >> 4 (bits 0-13), leading byte
+// offset >> 4 (16-29, unused for this layout), stride byte offset >> 4 (32-45),
+// descriptor version 1 (46-48), swizzle mode 2 = 128 B (61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction descriptor: D fp32 (bit 4), A and B format (bits 7-9, 10-12: 1 = bf16
+// for kind::f16, 2 = tf32 for kind::tf32), both K-major, N >> 3 at bits 17-22, M >> 4 at
+// bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int m, int n, uint32_t ab_format) {
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Kernel kinds: bf16 operands gathered by cp.async (any C multiple of 8), bf16 gathered by
+// TMA boxes, and fp32 I/O as three TF32 products per useful product (3xTF32, TMA gather).
+enum Kind { KIND_BF16_CPASYNC = 0, KIND_BF16_TMA = 1, KIND_TF32X3 = 2 };
+
+template <int KIND>
+struct Traits {
+    static constexpr bool TMA = KIND != KIND_BF16_CPASYNC;
+    static constexpr bool TF32 = KIND == KIND_TF32X3;
+    static constexpr int PROD_WARPS = TMA ? 1 : 4;
+    static constexpr int CVT_WARPS = TF32 ? 4 : 0;
+    static constexpr int MMA_WARP = EPI_WARPS + PROD_WARPS;
+    static constexpr int CVT_WARP0 = MMA_WARP + 1;
+    static constexpr int THREADS = (CVT_WARP0 + CVT_WARPS) * 32;
+    static constexpr int PROD_THREADS = PROD_WARPS * 32;
+    static constexpr uint32_t FULL_COUNT = TMA ? 1u : (uint32_t)(PROD_THREADS + 1);
+    static constexpr uint32_t A_STAGE = TF32 ? 2 * A_BYTES : A_BYTES;   // 3xTF32: hi tile, then lo tile
+};
+
+template <int BN, int KIND>
+struct Cfg {
+    static constexpr uint32_t B_TILE = BN * 128;
+    static constexpr uint32_t B_STAGE = Traits<KIND>::TF32 ? 2 * B_TILE : B_TILE;
+    static constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;    // power of two for BN in {16..256}
+};
+
+__device__ __forceinline__ void decode_unit(const TcParams& p, int u, int& mt, int& g, int& nt, int& split) {
+    split = u % p.splits;
+    int r = u / p.splits;
+    nt = r % p.num_nt;
+    r /= p.num_nt;
+    g = r % p.g.G;
+    mt = r / p.g.G;
+}
+
+// TMA tiles: mt -> (n, od, oh0, ow0) of a BH x BW block of one output plane.
+struct TileOrigin {
+    int n, od, oh0, ow0;
+};
+__device__ __forceinline__ TileOrigin tile_origin(const TcParams& p, int mt) {
+    TileOrigin t;
+    const int tw = mt % p.tiles_w;
+    int r = mt / p.tiles_w;
+    const int th = r % p.tiles_h;
+    r /= p.tiles_h;
+    t.od = r % p.g.Do;
+    t.n = r / p.g.Do;
+    t.oh0 = th * p.BH;
+    t.ow0 = tw * p.BW;
+    return t;
+}
+
+template <int BN, int STAGES, int KIND>
+__global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
+    conv_fwd_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map) {
+    using C = Cfg<BN, KIND>;
+    using T = Traits<KIND>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (sbase - raw);
+    const uint32_t sA = sbase;
+    const uint32_t sB = sbase + STAGES * T::A_STAGE;
+    const uint32_t bar0 = sbase + STAGES * (T::A_STAGE + C::B_STAGE);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto cvt_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (3 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (3 * STAGES + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (3 * STAGES + 4);
+    uint8_t* misc = smem + (bar0 + 8u * (3 * STAGES + 5) - sbase);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), T::FULL_COUNT);
+            mbar_init(empty_bar(s), 1);
+            mbar_init(cvt_bar(s), T::CVT_WARPS > 0 ? T::CVT_WARPS : 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+    if (T::TMA && warp == EPI_WARPS && lane == 0)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&act_map)) : "memory");
+    if (warp == T::MMA_WARP) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const Geom& g = p.g;
+    const int GC = g.G * g.C;
+    const int GK = g.G * g.K;
+
+    if (warp >= EPI_WARPS && warp < T::MMA_WARP) {
+        const uint8_t* wp = reinterpret_cast<const uint8_t*>(p.wpack);
+        if (T::TMA) {
+            // -------------------------------------------------------- producer (TMA)
+            if (lane == 0) {
+                const uint32_t a_tx = (uint32_t)(p.BW * p.BH) * 128u;
+                const int cblk = T::TF32 ? 32 : 64;     // channels in one 128-byte row
+                uint32_t it = 0;
+                bool aborted = false;
+                for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
+                    int mt, gi, nt, split;
+                    decode_unit(p, u, mt, gi, nt, split);
+                    const TileOrigin to = tile_origin(p, mt);
+                    const int kb0 = split * p.kbps;
+                    const int kb1 = min(kb0 + p.kbps, p.nkb);
+                    const int w0 = to.ow0 * g.sw - g.pw, h0 = to.oh0 * g.sh - g.ph, d0 = to.od * g.sd - g.pd;
+                    for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                        const int s = it % STAGES;
+                        const uint32_t ph = (it / STAGES) & 1u;
+                        if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p.err)) { aborted = true; break; }
+                        mbar_arrive_expect_tx(full_bar(s), a_tx + C::B_STAGE);
+                        const int tap = kb / p.cbt;
+                        const int c0 = (kb - tap * p.cbt) * cblk;
+                        const int zz = tap / (g.Y * g.X);
+                        const int rem = tap - zz * g.Y * g.X;
+                        const int yy = rem / g.X;
+                        const int xx = rem - yy * g.X;
+                        const int wi = w0 + xx * g.dw, hi = h0 + yy * g.dh;
+                        if (p.map_kind == 0)
+                            tma_load_5d(sA + s * T::A_STAGE, &act_map, gi * g.C + c0, wi, hi, d0 + zz * g.dd, to.n,
+                                        full_bar(s));
+                        else
+                            tma_load_5d(sA + s * T::A_STAGE, &act_map, c0, gi, wi, hi, to.n, full_bar(s));
+                        const size_t off = ((size_t)(gi * p.num_nt + nt) * p.nkb + kb) * C::B_STAGE;
+                        bulk_g2s(sB + s * C::B_STAGE, wp + off, C::B_STAGE, full_bar(s));
+                    }
+                }
+            }
+            __syncwarp();
+        } else {
+            // -------------------------------------------------------- producer (cp.async)
+            const int pt = threadIdx.x - EPI_WARPS * 32;
+            const int j = pt & 7;        // 16-byte chunk of the 128-byte row
+            const int rb = pt >> 3;      // rows rb, rb+16, ..., rb+112
+            const uint32_t swz = (uint32_t)((j ^ (rb & 7)) << 4);
+            const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x);
+            uint32_t it = 0;
+            bool aborted = false;
+            for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
+                int mt, gi, nt, split;
+                decode_unit(p, u, mt, gi, nt, split);
+                const int kb0 = split * p.kbps;
+                const int kb1 = min(kb0 + p.kbps, p.nkb);
+                int rn[8], rd[8], rh[8], rw[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int m = mt * BM + rb + 16 * i;
+                    if (m < g.M) {
+                        int t = m;
+                        const int ow = t % g.Wo; t /= g.Wo;
+                        const int oh = t % g.Ho; t /= g.Ho;
+                        const int od = t % g.Do;
+                        rn[i] = t / g.Do;
+                        rd[i] = od * g.sd - g.pd;
+                        rh[i] = oh * g.sh - g.ph;
+                        rw[i] = ow * g.sw - g.pw;
+                    } else {
+                        rn[i] = -1; rd[i] = 0; rh[i] = 0; rw[i] = 0;
+                    }
+                }
+                const __nv_bfloat16* xg = x + (size_t)gi * g.C;
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p.err)) { aborted = true; break; }
+                    if (pt == 0) {
+                        mbar_arrive_expect_tx(full_bar(s), C::B_STAGE);
+                        const size_t off = ((size_t)(gi * p.num_nt + nt) * p.nkb + kb) * C::B_STAGE;
+                        bulk_g2s(sB + s * C::B_STAGE, wp + off, C::B_STAGE, full_bar(s));
+                    }
+                    const int q = kb * 8 + j;
+                    const bool qok = q < p.nchunks;
+                    const int tap = qok ? q / p.cpt : 0;
+                    const int c0 = (q - tap * p.cpt) * 8;
+                    const int zz = tap / (g.Y * g.X);
+                    const int rem = tap - zz * g.Y * g.X;
+                    const int yy = rem / g.X;
+                    const int xx = rem - yy * g.X;
+                    const int dz = zz * g.dd, dy = yy * g.dh, dx = xx * g.dw;
+                    const uint32_t dst0 = sA + s * T::A_STAGE + swz;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int id = rd[i] + dz, ih = rh[i] + dy, iw = rw[i] + dx;
+                        const bool ok = qok && rn[i] >= 0 && (unsigned)id < (unsigned)g.D &&
+                                        (unsigned)ih < (unsigned)g.H && (unsigned)iw < (unsigned)g.W;
+                        const __nv_bfloat16* src =
+                            ok ? xg + ((((size_t)rn[i] * g.D + id) * g.H + ih) * g.W + iw) * GC + c0 : x;
+                        cp_async_16(dst0 + (uint32_t)(rb + 16 * i) * 128u, src, ok ? 16u : 0u);
+                    }
+                    cp_async_commit();
+                    if (it >= (uint32_t)LAG) {
+                        cp_async_wait<LAG>();
+                        fence_proxy_async();
+                        mbar_arrive(full_bar((it - LAG) % STAGES));
+                    }
+                }
+            }
+            cp_async_wait<0>();
+            fence_proxy_async();
+            if (!aborted) {
+                const uint32_t first = it > (uint32_t)LAG ? it - LAG : 0u;
+                for (uint32_t k = first; k < it; ++k) mbar_arrive(full_bar(k % STAGES));
+            }
+        }
+    } else if (warp == T::MMA_WARP) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_f32acc(BM, BN, T::TF32 ? 2u : 1u);
+            uint32_t it = 0, tile_i = 0;
+            bool aborted = false;
+            for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x, ++tile_i) {
+                int mt, gi, nt, split;
+                decode_unit(p, u, mt, gi, nt, split);
+                const int kb0 = split * p.kbps;
+                const int kb1 = min(kb0 + p.kbps, p.nkb);
+                const int acc = tile_i & 1;
+                const uint32_t aph = (tile_i >> 1) & 1u;
+                if (!wait_bar(tempty_bar(acc), aph ^ 1u, abort_flag, p.err)) { aborted = true; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!wait_bar(T::TF32 ? cvt_bar(s) : full_bar(s), ph, abort_flag, p.err)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sw128_desc(sA + s * T::A_STAGE);
+                    const uint64_t bd = sw128_desc(sB + s * C::B_STAGE);
+                    if (T::TF32) {
+                        // hi tiles first in the stage, lo tiles after: +A_BYTES / +B_TILE bytes
+                        const uint64_t alo = ad + (A_BYTES >> 4), blo = bd + (C::B_TILE >> 4);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {   // 4 x K=8 tf32 = 32 fp32 = one 128-byte row
+                            mma_tf32(d_tmem, alo + 2u * k, bd + 2u * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                            mma_tf32(d_tmem, ad + 2u * k, blo + 2u * k, IDESC, 1u);
+                            mma_tf32(d_tmem, ad + 2u * k, bd + 2u * k, IDESC, 1u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)   // 4 x K=16 = 64 bf16 = one 128-byte row; +32 B each
+                            mma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(s));
+                }
+                if (!aborted) mma_commit(tfull_bar(acc));
+            }
+            if (aborted) {
+                // wait (bounded) until every MMA issued so far has completed
+                mma_commit(drain_bar);
+                const unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
+            }
+        }
+        __syncwarp();
+    } else if (T::TF32 && warp >= T::CVT_WARP0) {
+        // ------------------------------------------------------------ hi/lo split (3xTF32)
+        // Every fp32 activation x becomes hi = x with its low 13 mantissa bits cleared (exact
+        // in TF32) and lo = x - hi (exact in fp32); the MMA then sums lo*w_hi + hi*w_lo + hi*w_hi.
+        const int ct = threadIdx.x - T::CVT_WARP0 * 32;
+        const int n16 = p.BW * p.BH * 8;   // 16-byte chunks the TMA box wrote
+        uint32_t it = 0;
+        bool aborted = false;
+        for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
+            int mt, gi, nt, split;
+            decode_unit(p, u, mt, gi, nt, split);
+            const int kb0 = split * p.kbps;
+            const int kb1 = min(kb0 + p.kbps, p.nkb);
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1u;
+                if (!wait_bar(full_bar(s), ph, abort_flag, p.err)) { aborted = true; break; }
+                uint4* hi = reinterpret_cast<uint4*>(smem + s * T::A_STAGE);
+                uint4* lo = reinterpret_cast<uint4*>(smem + s * T::A_STAGE + A_BYTES);
+                for (int i = ct; i < n16; i += T::CVT_WARPS * 32) {
+                    const uint4 v = hi[i];
+                    uint4 h, l;
+                    h.x = v.x & 0xFFFFE000u; h.y = v.y & 0xFFFFE000u; h.z = v.z & 0xFFFFE000u; h.w = v.w & 0xFFFFE000u;
+                    l.x = __float_as_uint(__uint_as_float(v.x) - __uint_as_float(h.x));
+                    l.y = __float_as_uint(__uint_as_float(v.y) - __uint_as_float(h.y));
+                    l.z = __float_as_uint(__uint_as_float(v.z) - __uint_as_float(h.z));
+                    l.w = __float_as_uint(__uint_as_float(v.w) - __uint_as_float(h.w));
+                    hi[i] = h;
+                    lo[i] = l;
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cvt_bar(s));
+            }
+        }
+    } else if (warp < EPI_WARPS) {
+        // ------------------------------------------------------------ epilogue
+        const int wq = warp;                 // TMEM lane quarter
+        const int r = wq * 32 + lane;        // accumulator row = pixel within the tile
+        const bool add_bias = (p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU) && p.splits == 1;
+        const bool do_gelu = (p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU) && p.splits == 1;
+        uint32_t tile_i = 0;
+        for (int u = blockIdx.x; u < p.total_units; u += gridDim.x, ++tile_i) {
+            int mt, gi, nt, split;
+            decode_unit(p, u, mt, gi, nt, split);
+            const int acc = tile_i & 1;
+            const uint32_t aph = (tile_i >> 1) & 1u;
+            if (!wait_bar(tfull_bar(acc), aph, abort_flag, p.err)) break;
+            tc_fence_after();
+            int m;
+            bool row_ok;
+            if (T::TMA) {
+                const TileOrigin to = tile_origin(p, mt);
+                const int oh = to.oh0 + r / p.BW, ow = to.ow0 + r % p.BW;
+                row_ok = r < p.BW * p.BH && oh < g.Ho && ow < g.Wo;
+                m = ((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow;
+            } else {
+                m = mt * BM + r;
+                row_ok = m < g.M;
+            }
+            const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int cb = 0; cb < BN; cb += 16) {
+                const int n = nt * BN + cb;
+                if (n >= g.K) break;                       // warp-uniform
+                uint32_t v[16];
+                __syncwarp();                              // tcgen05.ld is warp-aligned
+                tmem_ld16(taddr + cb, v);
+                tmem_ld_wait();
+                if (row_ok) {
+                    float f[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]);
+                    // K is a multiple of 8 (bf16) or 4 (fp32): groups of 4 columns are whole
+                    const int quads = min(4, (g.K - n) / 4);
+                    if (p.splits > 1) {
+                        float* dst = p.ws + ((size_t)split * g.M + m) * GK + (size_t)gi * g.K + n;
+                        for (int q = 0; q < quads; ++q)
+                            reinterpret_cast<float4*>(dst)[q] =
+                                make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+                    } else {
+                        if (add_bias) {
+                            if (T::TF32) {
+                                const float4* bp = reinterpret_cast<const float4*>(
+                                    reinterpret_cast<const float*>(p.bias) + (size_t)gi * g.K + n);
+                                for (int q = 0; q < quads; ++q) {
+                                    const float4 b4 = __ldg(bp + q);
+                                    f[4 * q] += b4.x; f[4 * q + 1] += b4.y; f[4 * q + 2] += b4.z; f[4 * q + 3] += b4.w;
+                                }
+                            } else {
+                                const uint2* bp = reinterpret_cast<const uint2*>(
+                                    reinterpret_cast<const __nv_bfloat16*>(p.bias) + (size_t)gi * g.K + n);
+                                for (int q = 0; q < quads; ++q) {
+                                    const uint2 b2 = __ldg(bp + q);
+                                    f[4 * q] += __uint_as_float(b2.x << 16);
+                                    f[4 * q + 1] += __uint_as_float(b2.x & 0xFFFF0000u);
+                                    f[4 * q + 2] += __uint_as_float(b2.y << 16);
+                                    f[4 * q + 3] += __uint_as_float(b2.y & 0xFFFF0000u);
+                                }
+                            }
+                        }
+                        if (do_gelu) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) f[e] = gelu_f(f[e]);
+                        }
+                        if (T::TF32) {
+                            float* dst = reinterpret_cast<float*>(p.y) + (size_t)m * GK + (size_t)gi * g.K + n;
+                            for (int q = 0; q < quads; ++q)
+                                reinterpret_cast<float4*>(dst)[q] =
+                                    make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+                        } else {
+                            __nv_bfloat16* dst =
+                                reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)m * GK + (size_t)gi * g.K + n;
+                            for (int h = 0; h < quads / 2; ++h) {
+                                uint4 o;
+                                o.x = pack_bf16x2(f[8 * h + 0], f[8 * h + 1]);
+                                o.y = pack_bf16x2(f[8 * h + 2], f[8 * h + 3]);
+                                o.z = pack_bf16x2(f[8 * h + 4], f[8 * h + 5]);
+                                o.w = pack_bf16x2(f[8 * h + 6], f[8 * h + 7]);
+                                reinterpret_cast<uint4*>(dst + 8 * h)[0] = o;
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == T::MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <int BN, int STAGES, int KIND>
+constexpr size_t smem_bytes_for() {
+    return 1024 + (size_t)STAGES * (Traits<KIND>::A_STAGE + Cfg<BN, KIND>::B_STAGE) + 8 * (3 * STAGES + 5) + 16;
+}
+
+template <int BN, int STAGES, int KIND>
+cudaError_t launch_one(const TcParams& p, const CUtensorMap& map, int grid, cudaStream_t stream) {
+    auto kern = conv_fwd_tc_kernel<BN, STAGES, KIND>;
+    constexpr size_t smem = smem_bytes_for<BN, STAGES, KIND>();
+    static_assert(smem <= 232448, "shared memory budget");
+    // opt in to the large dynamic shared memory once per device (not inside graph capture)
+    static bool attr_set[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    kern<<<grid, Traits<KIND>::THREADS, smem, stream>>>(p, map);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// (BN, stages) pairs compiled into the library, per kind; the plan picks one.
+#define TC_BF16_CONFIGS(X) X(256, 4) X(128, 6) X(64, 8) X(32, 8) X(16, 8)
+#define TC_TF32_CONFIGS(X) X(256, 2) X(128, 3) X(64, 4) X(32, 5) X(16, 5)
+
+int tc_stages_for(int BN, int tf32) {
+#define X(bn, st) if (BN == bn) return st;
+    if (tf32) { TC_TF32_CONFIGS(X) } else { TC_BF16_CONFIGS(X) }
+#undef X
+    return 0;
+}
+
+cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, int stages, int grid, cudaStream_t stream) {
+    static const CUtensorMap unused{};
+    const CUtensorMap& map = act_map ? *act_map : unused;
+    if (p.tma && !act_map) return cudaErrorInvalidValue;
+    if (p.tf32) {
+        if (!p.tma) return cudaErrorInvalidValue;
+#define X(bn, st) \
+    if (p.BN == bn && stages == st) return launch_one<bn, st, KIND_TF32X3>(p, map, grid, stream);
+        TC_TF32_CONFIGS(X)
+#undef X
+        return cudaErrorInvalidValue;
+    }
+#define X(bn, st)                                                                              \
+    if (p.BN == bn && stages == st)                                                            \
+        return p.tma ? launch_one<bn, st, KIND_BF16_TMA>(p, map, grid, stream)                 \
+                     : launch_one<bn, st, KIND_BF16_CPASYNC>(p, map, grid, stream);
+    TC_BF16_CONFIGS(X)
+#undef X
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace convfwd

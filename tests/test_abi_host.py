@@ -90,8 +90,12 @@ def test_output_shape_and_flops_agree_with_the_oracle(lib):
             assert B.conv_plan_output_shape(h, nd) == g.out_spatial[3 - nd:]
             assert B.conv_plan_flops(h) == 2.0 * g.macs()
             desc = B.conv_plan_describe(h)
+            tf32_ok = (C % 4 == 0 and K % 4 == 0 and C >= 32 and max(s) <= 8 and
+                       (C % 32 == 0 or G == 1 or nd <= 2))
             if dtype == B.CONV_BF16 and C % 8 == 0 and K % 8 == 0:
                 assert "variant=tc_bf16" in desc
+            elif dtype == B.CONV_F32 and tf32_ok:
+                assert "variant=tc_tf32x3" in desc
             else:
                 assert "variant=simt" in desc
             assert B.conv_prepacked_weight_bytes(h) % 16 == 0 or "simt" in desc

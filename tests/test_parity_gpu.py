@@ -61,6 +61,20 @@ SMALL = [
     ("2d_bf16_1x1", "bf16", L(2, 2, 2, 32, 48, (9, 10), (1, 1), (1, 1), (0, 0), (1, 1))),
     ("2d_tc_taps_in_padding", "bf16", L(2, 1, 1, 16, 16, (4, 4), (3, 3), (3, 3), (5, 5), (4, 4))),
     ("1d_tc_tiny_M", "bf16", L(1, 1, 1, 8, 16, (1,), (1,), (1,), (0,), (1,))),
+    # TMA gather: both tensor-map layouts, strides, dilation, ragged tiles
+    ("2d_tma_map1_c72", "bf16", L(2, 2, 2, 72, 40, (13, 21), (3, 3), (1, 1), (1, 1), (1, 1))),
+    ("1d_tma_s2_dil", "bf16", L(1, 2, 1, 64, 64, (400,), (5,), (2,), (4,), (2,))),
+    ("2d_tma_stride2", "bf16", L(2, 1, 1, 128, 64, (30, 35), (3, 3), (2, 2), (1, 1), (1, 1))),
+    ("3d_tma_c64_dil", "bf16", L(3, 1, 2, 64, 64, (5, 9, 10), (3, 3, 3), (1, 1, 1), (2, 2, 2), (2, 2, 2),
+                                 CONV_EPI_BIAS)),
+    ("3d_g2_c96_cpasync", "bf16", L(3, 1, 2, 96, 32, (4, 6, 7), (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1))),
+    ("2d_tma_wide_w", "bf16", L(2, 1, 1, 64, 48, (3, 300), (3, 3), (1, 3), (1, 1), (1, 1))),
+    # fp32 I/O on the tensor cores (3xTF32)
+    ("1d_tf32_s2_k384", "f32", L(1, 1, 1, 384, 384, (301,), (3,), (2,), (1,), (1,))),
+    ("2d_tf32_group_map1", "f32", L(2, 2, 3, 40, 24, (11, 13), (3, 3), (1, 1), (1, 1), (1, 1), CONV_EPI_BIAS)),
+    ("2d_tf32_g2_c32_dil", "f32", L(2, 1, 2, 32, 36, (17, 19), (3, 3), (1, 1), (2, 2), (2, 2), CONV_EPI_NONE)),
+    ("3d_tf32_c64", "f32", L(3, 1, 2, 64, 40, (4, 7, 9), (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), CONV_EPI_BIAS)),
+    ("1d_tf32_k4", "f32", L(1, 3, 1, 32, 4, (129,), (3,), (1,), (1,), (1,))),
 ]
 
 
@@ -94,6 +108,30 @@ def test_every_tensor_core_tile_width(bn):
     assert f"tile=128x{bn}" in desc
     ref, S = oracle_full(layer, "bf16", x, w, b)
     assert_within("bf16", layer.epilogue, got, ref, S, desc)
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256])
+def test_every_tile_width_with_tma_gather(bn):
+    layer = L(2, 2, 1, 64, 200, (9, 37), (3, 3), (1, 1), (1, 1), (1, 1))
+    x, w, b = make_inputs(layer, "bf16", 600 + bn)
+    got, desc = run_gpu(layer, "bf16", x, w, b, env={"CONV_FORCE_BN": bn}, guard=64)
+    assert f"tile=128x{bn}" in desc and "gather=tma" in desc
+    ref, S = oracle_full(layer, "bf16", x, w, b)
+    assert_within("bf16", layer.epilogue, got, ref, S, desc)
+
+
+@pytest.mark.parametrize("case", [0, 1, 2])
+def test_tma_and_cp_async_gathers_agree(case):
+    layer = [L(1, 1, 1, 80, 384, (517,), (3,), (2,), (1,), (1,)),
+             L(2, 2, 4, 64, 64, (14, 14), (3, 3), (1, 1), (2, 2), (2, 2), CONV_EPI_NONE),
+             L(3, 1, 2, 64, 64, (4, 8, 8), (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), CONV_EPI_BIAS)][case]
+    x, w, b = make_inputs(layer, "bf16", 700 + case)
+    ref, S = oracle_full(layer, "bf16", x, w, b)
+    a, da = run_gpu(layer, "bf16", x, w, b)
+    c, dc = run_gpu(layer, "bf16", x, w, b, env={"CONV_FORCE_GATHER": "cpasync"})
+    assert "gather=tma" in da and "gather=cp.async" in dc
+    assert_within("bf16", layer.epilogue, a, ref, S, da)
+    assert_within("bf16", layer.epilogue, c, ref, S, dc)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -234,3 +272,31 @@ def test_workload_full_size_parity(name):
     layers: layer l+1's oracle reads the GPU's layer-l output bits, so each layer meets
     the bound on its own."""
     _workload_parity(name)
+
+
+def test_plan_made_before_any_cuda_context_still_uses_tma():
+    """A plan created in a fresh process before any CUDA call picks the TMA gather."""
+    import subprocess
+    import sys
+    code = ("from convolution_forward_implicit_gb300 import binding as B\n"
+            "h = B.conv_plan_create(1, 1, 1, 128, 128, (500,), (3,), (1,), (1,), (1,), B.CONV_BF16, 0)\n"
+            "print(B.conv_plan_describe(h))\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert "gather=tma" in out.stdout, out.stdout
+
+
+@pytest.mark.parametrize("case", [0, 1])
+def test_tf32x3_and_ffma_both_meet_the_fp32_bound(case):
+    """fp32 I/O: the 3xTF32 tensor-core kernel and the FFMA kernel on the same inputs."""
+    layer = [L(1, 1, 1, 80, 384, (3000,), (3,), (1,), (1,), (1,), CONV_EPI_BIAS_GELU),
+             L(1, 1, 1, 384, 384, (3000,), (3,), (2,), (1,), (1,), CONV_EPI_BIAS_GELU)][case]
+    x, w, b = make_inputs(layer, "f32", 800 + case)
+    ref, S = oracle_full(layer, "f32", x, w, b)
+    a, da = run_gpu(layer, "f32", x, w, b)
+    c, dc = run_gpu(layer, "f32", x, w, b, env={"CONV_FORCE_SIMT": 1})
+    assert "tc_tf32x3" in da and "simt" in dc
+    ra, _ = assert_within("f32", layer.epilogue, a, ref, S, da)
+    rc, _ = assert_within("f32", layer.epilogue, c, ref, S, dc)
+    assert ra < 0.5, f"3xTF32 uses {ra:.2f} of the fp32 bound"
