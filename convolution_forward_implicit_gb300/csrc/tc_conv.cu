@@ -35,7 +35,7 @@ namespace convfwd {
 namespace {
 
 constexpr int BM = 128;
-constexpr int EPI_WARPS = 4;
+constexpr int EPI_WARPS = 8;                           // two per TMEM lane quarter, splitting the columns
 constexpr int LAG = 2;                                 // K blocks a cp.async producer keeps in flight
 constexpr uint32_t A_BYTES = BM * 128;                 // 128 pixels x 64 bf16
 constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;
@@ -86,6 +86,15 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
             return false;
         }
     }
+}
+
+// Bounded wait taken by lane 0 for the whole (converged) warp; every lane returns lane 0's
+// outcome, so a warp never splits at an abort and later meets itself at a warp barrier.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned* err) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, err) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // ---- async copies ----
@@ -199,11 +208,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 // TMA boxes, and fp32 I/O as three TF32 products per useful product (3xTF32, TMA gather).
 enum Kind { KIND_BF16_CPASYNC = 0, KIND_BF16_TMA = 1, KIND_TF32X3 = 2 };
 
+// A thread has at most one TMA copy in flight (measured on this GPU: a second copy from the
+// same thread starts only when the first completes, ~700 cycles each), so the TMA producer
+// spreads its copies over 4 warps, pipeline stage s belonging to warp s % 4, where lane 0
+// copies the activation box and lane 1 the weight tile.
 template <int KIND>
 struct Traits {
     static constexpr bool TMA = KIND != KIND_BF16_CPASYNC;
     static constexpr bool TF32 = KIND == KIND_TF32X3;
-    static constexpr int PROD_WARPS = TMA ? 1 : 4;
+    static constexpr int PROD_WARPS = 4;
     static constexpr int CVT_WARPS = TF32 ? 4 : 0;
     static constexpr int MMA_WARP = EPI_WARPS + PROD_WARPS;
     static constexpr int CVT_WARP0 = MMA_WARP + 1;
@@ -305,7 +318,8 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
         const uint8_t* wp = reinterpret_cast<const uint8_t*>(p.wpack);
         if (T::TMA) {
             // -------------------------------------------------------- producer (TMA)
-            if (lane == 0) {
+            const int pw = warp - EPI_WARPS;
+            if (lane < 2) {
                 const uint32_t a_tx = (uint32_t)(p.BW * p.BH) * 128u;
                 const int cblk = T::TF32 ? 32 : 64;     // channels in one 128-byte row
                 uint32_t it = 0;
@@ -318,24 +332,36 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
                     const int kb1 = min(kb0 + p.kbps, p.nkb);
                     const int w0 = to.ow0 * g.sw - g.pw, h0 = to.oh0 * g.sh - g.ph, d0 = to.od * g.sd - g.pd;
                     for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                        // stage s belongs to producer warp s % PROD_WARPS: a warp then refills a
+                        // stage only after it has seen the stage's previous phase complete, so no
+                        // parity wait is ever more than one phase ahead of its barrier
+                        if ((int)((it % STAGES) % T::PROD_WARPS) != pw) continue;
                         const int s = it % STAGES;
                         const uint32_t ph = (it / STAGES) & 1u;
-                        if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p.err)) { aborted = true; break; }
-                        mbar_arrive_expect_tx(full_bar(s), a_tx + C::B_STAGE);
-                        const int tap = kb / p.cbt;
-                        const int c0 = (kb - tap * p.cbt) * cblk;
-                        const int zz = tap / (g.Y * g.X);
-                        const int rem = tap - zz * g.Y * g.X;
-                        const int yy = rem / g.X;
-                        const int xx = rem - yy * g.X;
-                        const int wi = w0 + xx * g.dw, hi = h0 + yy * g.dh;
-                        if (p.map_kind == 0)
-                            tma_load_5d(sA + s * T::A_STAGE, &act_map, gi * g.C + c0, wi, hi, d0 + zz * g.dd, to.n,
-                                        full_bar(s));
-                        else
-                            tma_load_5d(sA + s * T::A_STAGE, &act_map, c0, gi, wi, hi, to.n, full_bar(s));
-                        const size_t off = ((size_t)(gi * p.num_nt + nt) * p.nkb + kb) * C::B_STAGE;
-                        bulk_g2s(sB + s * C::B_STAGE, wp + off, C::B_STAGE, full_bar(s));
+                        // lane 0 waits and both lanes follow its outcome, so they never part ways
+                        int ok = 1;
+                        if (lane == 0) ok = wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p.err) ? 1 : 0;
+                        ok = __shfl_sync(0x3u, ok, 0);
+                        if (!ok) { aborted = true; break; }
+                        if (lane == 0) mbar_arrive_expect_tx(full_bar(s), a_tx + C::B_STAGE);
+                        __syncwarp(0x3u);
+                        if (lane == 0) {
+                            const int tap = kb / p.cbt;
+                            const int c0 = (kb - tap * p.cbt) * cblk;
+                            const int zz = tap / (g.Y * g.X);
+                            const int rem = tap - zz * g.Y * g.X;
+                            const int yy = rem / g.X;
+                            const int xx = rem - yy * g.X;
+                            const int wi = w0 + xx * g.dw, hi = h0 + yy * g.dh;
+                            if (p.map_kind == 0)
+                                tma_load_5d(sA + s * T::A_STAGE, &act_map, gi * g.C + c0, wi, hi, d0 + zz * g.dd,
+                                            to.n, full_bar(s));
+                            else
+                                tma_load_5d(sA + s * T::A_STAGE, &act_map, c0, gi, wi, hi, to.n, full_bar(s));
+                        } else {
+                            const size_t off = ((size_t)(gi * p.num_nt + nt) * p.nkb + kb) * C::B_STAGE;
+                            bulk_g2s(sB + s * C::B_STAGE, wp + off, C::B_STAGE, full_bar(s));
+                        }
                     }
                 }
             }
@@ -483,7 +509,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
-                if (!wait_bar(full_bar(s), ph, abort_flag, p.err)) { aborted = true; break; }
+                if (!wait_bar_warp(full_bar(s), ph, abort_flag, p.err)) { aborted = true; break; }
                 uint4* hi = reinterpret_cast<uint4*>(smem + s * T::A_STAGE);
                 uint4* lo = reinterpret_cast<uint4*>(smem + s * T::A_STAGE + A_BYTES);
                 for (int i = ct; i < n16; i += T::CVT_WARPS * 32) {
@@ -504,8 +530,11 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
         }
     } else if (warp < EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
-        const int wq = warp;                 // TMEM lane quarter
+        const int wq = warp & 3;             // TMEM lane quarter
         const int r = wq * 32 + lane;        // accumulator row = pixel within the tile
+        constexpr int COLS = BN / 2 < 16 ? 16 : BN / 2;   // columns per epilogue warp
+        const int cb_begin = (warp >> 2) * COLS;
+        const int cb_end = cb_begin + COLS < BN ? cb_begin + COLS : BN;
         const bool add_bias = (p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU) && p.splits == 1;
         const bool do_gelu = (p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU) && p.splits == 1;
         uint32_t tile_i = 0;
@@ -514,7 +543,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
             decode_unit(p, u, mt, gi, nt, split);
             const int acc = tile_i & 1;
             const uint32_t aph = (tile_i >> 1) & 1u;
-            if (!wait_bar(tfull_bar(acc), aph, abort_flag, p.err)) break;
+            if (!wait_bar_warp(tfull_bar(acc), aph, abort_flag, p.err)) break;
             tc_fence_after();
             int m;
             bool row_ok;
@@ -529,7 +558,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
             }
             const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
-            for (int cb = 0; cb < BN; cb += 16) {
+            for (int cb = cb_begin; cb < cb_end; cb += 16) {
                 const int n = nt * BN + cb;
                 if (n >= g.K) break;                       // warp-uniform
                 uint32_t v[16];
