@@ -181,7 +181,7 @@ struct conv_plan {
     Variant variant;
     // tensor-core plan
     int BN, stages, num_mt, num_nt, nkb, nchunks, cpt, splits, kbps, total_units, grid;
-    int tma, map_kind, BW, BH, tiles_w, tiles_h, cbt, tf32;
+    int tma, map_kind, BW, BH, tiles_w, tiles_h, cbt, tf32, sleep_mask;
     // SIMT plan
     int BM, Kg, Kpad, nkt, ktps, vec;
     size_t prepack_bytes, workspace_bytes;
@@ -337,6 +337,8 @@ static bool plan_tc(conv_plan* p, bool tf32) {
         cudaGetLastError();
     }
     if (tf32 && !tma) return false;   // 3xTF32 needs the TMA gather
+    // the epilogue warps wait a whole main loop per tile: they sleep; the rest poll
+    p->sleep_mask = env_int("CONV_WAIT_SLEEP", 2);
     p->tma = tma ? 1 : 0;
     if (tma) {
         p->cbt = (int)cdiv(g.C, cblk);
@@ -575,6 +577,7 @@ conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, cons
         tp.epi = (int)plan->epi; tp.total_units = plan->total_units;
         tp.tma = plan->tma; tp.map_kind = plan->map_kind; tp.BW = plan->BW; tp.BH = plan->BH;
         tp.tiles_w = plan->tiles_w; tp.tiles_h = plan->tiles_h; tp.cbt = plan->cbt; tp.tf32 = plan->tf32;
+        tp.sleep_mask = plan->sleep_mask;
         CUtensorMap map;
         if (plan->tma && !encode_act_map(plan, x, &map)) return CONV_ERR_CUDA;
         e = launch_tc(tp, plan->tma ? &map : nullptr, plan->stages, plan->grid, s);
@@ -695,6 +698,7 @@ extern "C" conv_status conv_fwd_static_scratch(conv_plan_t plan, const void* x, 
         tp.epi = (int)plan->epi; tp.total_units = plan->total_units;
         tp.tma = plan->tma; tp.map_kind = plan->map_kind; tp.BW = plan->BW; tp.BH = plan->BH;
         tp.tiles_w = plan->tiles_w; tp.tiles_h = plan->tiles_h; tp.cbt = plan->cbt; tp.tf32 = plan->tf32;
+        tp.sleep_mask = plan->sleep_mask;
         CUtensorMap map;
         if (plan->tma && !encode_act_map(plan, x, &map)) return CONV_ERR_CUDA;
         e = launch_tc(tp, plan->tma ? &map : nullptr, plan->stages, plan->grid, s);

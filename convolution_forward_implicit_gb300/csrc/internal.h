@@ -48,6 +48,7 @@ struct TcParams {
     int tiles_w, tiles_h;   // tiles per output plane
     int cbt;                // channel blocks per tap (64 bf16 or 32 fp32 channels; kb = tap*cbt + block)
     int tf32;               // 1: fp32 I/O as 3xTF32 (TMA gather only)
+    int sleep_mask;         // which roles wait with a suspend hint: 1 producer, 2 epilogue, 4 MMA, 8 splitter
 };
 
 // Launch the tensor-core kernel for the (BN, stages) pair the plan picked (see tc_stages_for).

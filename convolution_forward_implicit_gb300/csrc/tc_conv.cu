@@ -60,6 +60,23 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
+// try_wait with a suspend-time hint: a waiting thread sleeps until the phase completes (or
+// the hint runs out) instead of spinning, so waiting warps do not take issue slots from the
+// warps that work.
+// Which roles sleep is a plan choice (TcParams::sleep_mask): waking a suspended thread costs
+// latency, which matters on the critical path (the MMA issuer, refills of a short ring).
+constexpr uint32_t SUSPEND_HINT_NS = 1000000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(SUSPEND_HINT_NS)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -73,14 +90,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait.  Returns false if this CTA is aborting (the limit ran out here or elsewhere).
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         unsigned* err) {
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned* err,
+                                         bool sleep = false) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (sleep ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if ((n & 63u) == 0 && globaltimer() - t0 > WAIT_LIMIT_NS) {
+        if (globaltimer() - t0 > WAIT_LIMIT_NS) {
             *abort_flag = 1;
             atomicOr(err, ERR_WAIT_TIMEOUT);
             return false;
@@ -91,9 +108,9 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // Bounded wait taken by lane 0 for the whole (converged) warp; every lane returns lane 0's
 // outcome, so a warp never splits at an abort and later meets itself at a warp barrier.
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                              unsigned* err) {
+                                              unsigned* err, bool sleep = false) {
     int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, err) ? 1 : 0;
+    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, err, sleep) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -199,6 +216,23 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(int m, int n, uint32_t ab_fo
 
 __device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
 
+// GELU for bf16 outputs: v * Phi(v) with erf from Abramowitz & Stegun, Handbook of
+// Mathematical Functions, eq. 7.1.28 (after Hastings): erf(z) = 1 - (1 + a1 z + ... + a6 z^6)^-16
+// for z >= 0, |error| <= 3e-7.  Evaluated in fp32 the GELU's relative error stays below 1e-6,
+// far under the bf16 rounding step, at one reciprocal and no exponential per value.
+__device__ __forceinline__ float gelu_bf16out(float v) {
+    const float z = fabsf(v) * 0.70710678118654752f;
+    float y = fmaf(z, 0.0000430638f, 0.0002765672f);
+    y = fmaf(z, y, 0.0001520143f);
+    y = fmaf(z, y, 0.0092705272f);
+    y = fmaf(z, y, 0.0422820123f);
+    y = fmaf(z, y, 0.0705230784f);
+    y = fmaf(z, y, 1.0f);
+    y = y * y; y = y * y; y = y * y; y = y * y;         // (.)^16
+    const float h = __fdividef(0.5f * v, y);            // 0.5 v (1 - erf(|v|/sqrt 2)); 0 once y overflows
+    return v >= 0.0f ? v - h : h;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -259,6 +293,108 @@ __device__ __forceinline__ TileOrigin tile_origin(const TcParams& p, int mt) {
     return t;
 }
 
+constexpr int STG_WARP_BYTES = 32 * 128;   // one warp's staging buffer: 32 rows x 128 B
+
+// Epilogue of one warp's 32 rows x [cb_begin, cb_end) accumulator columns (see the
+// epilogue role in the kernel).  ESZ is the stored element size: 2 for bf16 outputs, 4 for
+// fp32 outputs and for split-K partial sums.
+template <int BN, int ESZ, typename RowOffset>
+__device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t taddr, int lane, int wq, int cb_begin,
+                                                int cb_end, int nt, int gi, int split, bool partial, bool add_bias,
+                                                bool do_gelu, uint8_t* stg, RowOffset row_offset) {
+    constexpr int COLS = BN / 2 < 16 ? 16 : BN / 2;
+    constexpr int CW = COLS < 128 / ESZ ? COLS : 128 / ESZ;   // columns per chunk
+    constexpr int RB = CW * ESZ;                             // bytes per row segment (32..128)
+    constexpr int LPR = RB / 16;                             // 16-byte slots (= store lanes) per row
+    constexpr int RPI = 32 / LPR;                            // rows per store instruction
+    constexpr int SH = LPR == 8 ? 0 : LPR == 4 ? 1 : LPR == 2 ? 2 : 3;   // log2(8 / LPR)
+    constexpr int EPS = 16 / ESZ;                            // elements per 16-byte slot
+    const Geom& g = p.g;
+    const int GK = g.G * g.K;
+    // the store-phase rows of this lane are the same for every chunk of the tile
+    long long roff[LPR];
+#pragma unroll
+    for (int i = 0; i < LPR; ++i) roff[i] = row_offset(wq * 32 + lane / LPR + RPI * i);
+    const int slot = lane % LPR;
+    const int swz = (lane >> SH) & (LPR - 1);   // this lane's row: slot j sits at j ^ swz
+    for (int cb = cb_begin; cb < cb_end; cb += CW) {
+        const int n0 = nt * BN + cb;
+        if (n0 >= g.K) break;                               // warp-uniform
+        // 16 columns at a time: TMEM -> fp32 -> bias, GELU -> this lane's row slots in staging
+#pragma unroll
+        for (int q = 0; q < CW / 16; ++q) {
+            const int nq = n0 + 16 * q;
+            uint32_t v[16];
+            __syncwarp();                                   // tcgen05.ld is warp-aligned
+            tmem_ld16(taddr + (uint32_t)(cb + 16 * q), v);
+            tmem_ld_wait();
+            float f[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]);
+            if (add_bias) {
+                // only whole 8-column groups inside K are read; columns past K are never stored
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (nq + 8 * j >= g.K) break;
+                    if (ESZ == 4) {
+                        const float4* bp = reinterpret_cast<const float4*>(
+                                               reinterpret_cast<const float*>(p.bias) + (size_t)gi * g.K + nq) +
+                                           2 * j;
+                        const float4 a = __ldg(bp);
+                        const float4 b = (nq + 8 * j + 4 < g.K) ? __ldg(bp + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        f[8 * j] += a.x; f[8 * j + 1] += a.y; f[8 * j + 2] += a.z; f[8 * j + 3] += a.w;
+                        f[8 * j + 4] += b.x; f[8 * j + 5] += b.y; f[8 * j + 6] += b.z; f[8 * j + 7] += b.w;
+                    } else {
+                        const uint4 b4 = __ldg(reinterpret_cast<const uint4*>(
+                                                   reinterpret_cast<const __nv_bfloat16*>(p.bias) + (size_t)gi * g.K +
+                                                   nq) +
+                                               j);
+                        const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            f[8 * j + 2 * e] += __uint_as_float(bw[e] << 16);
+                            f[8 * j + 2 * e + 1] += __uint_as_float(bw[e] & 0xFFFF0000u);
+                        }
+                    }
+                }
+            }
+            if (do_gelu) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) f[e] = ESZ == 2 ? gelu_bf16out(f[e]) : gelu_f(f[e]);
+            }
+            constexpr int SPQ = 16 / EPS;                   // 16-byte slots per 16 columns
+#pragma unroll
+            for (int t = 0; t < SPQ; ++t) {
+                const int j = q * SPQ + t;
+                uint4 o;
+                if (ESZ == 4) {
+                    o = make_uint4(__float_as_uint(f[4 * t]), __float_as_uint(f[4 * t + 1]),
+                                   __float_as_uint(f[4 * t + 2]), __float_as_uint(f[4 * t + 3]));
+                } else {
+                    o.x = pack_bf16x2(f[8 * t + 0], f[8 * t + 1]);
+                    o.y = pack_bf16x2(f[8 * t + 2], f[8 * t + 3]);
+                    o.z = pack_bf16x2(f[8 * t + 4], f[8 * t + 5]);
+                    o.w = pack_bf16x2(f[8 * t + 6], f[8 * t + 7]);
+                }
+                *reinterpret_cast<uint4*>(stg + lane * RB + ((j ^ swz) << 4)) = o;
+            }
+        }
+        __syncwarp();
+        // row-wise store: lanes slot..slot+LPR-1 of a row write its whole segment
+        const int col = n0 + slot * EPS;
+        uint8_t* base = partial ? reinterpret_cast<uint8_t*>(p.ws) + ((size_t)split * g.M * GK) * 4
+                                : reinterpret_cast<uint8_t*>(p.y);
+#pragma unroll
+        for (int i = 0; i < LPR; ++i) {
+            const int rr = lane / LPR + RPI * i;           // row within the warp's 32
+            const uint4 o = *reinterpret_cast<const uint4*>(stg + rr * RB + ((slot ^ ((rr >> SH) & (LPR - 1))) << 4));
+            if (roff[i] >= 0 && col < g.K)
+                *reinterpret_cast<uint4*>(base + (size_t)(roff[i] + (long long)gi * g.K + col) * ESZ) = o;
+        }
+        __syncwarp();                                       // staging is rewritten by the next chunk
+    }
+}
+
 template <int BN, int STAGES, int KIND>
 __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
     conv_fwd_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map) {
@@ -270,7 +406,8 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
     uint8_t* smem = smem_raw + (sbase - raw);
     const uint32_t sA = sbase;
     const uint32_t sB = sbase + STAGES * T::A_STAGE;
-    const uint32_t bar0 = sbase + STAGES * (T::A_STAGE + C::B_STAGE);
+    constexpr uint32_t STG_OFFSET = STAGES * (T::A_STAGE + C::B_STAGE);       // epilogue staging
+    const uint32_t bar0 = sbase + STG_OFFSET + EPI_WARPS * STG_WARP_BYTES;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto cvt_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
@@ -340,7 +477,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
                         const uint32_t ph = (it / STAGES) & 1u;
                         // lane 0 waits and both lanes follow its outcome, so they never part ways
                         int ok = 1;
-                        if (lane == 0) ok = wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p.err) ? 1 : 0;
+                        if (lane == 0) ok = wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p.err, p.sleep_mask & 1) ? 1 : 0;
                         ok = __shfl_sync(0x3u, ok, 0);
                         if (!ok) { aborted = true; break; }
                         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), a_tx + C::B_STAGE);
@@ -401,7 +538,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p.err)) { aborted = true; break; }
+                    if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p.err, p.sleep_mask & 1)) { aborted = true; break; }
                     if (pt == 0) {
                         mbar_arrive_expect_tx(full_bar(s), C::B_STAGE);
                         const size_t off = ((size_t)(gi * p.num_nt + nt) * p.nkb + kb) * C::B_STAGE;
@@ -454,13 +591,13 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
                 const int kb1 = min(kb0 + p.kbps, p.nkb);
                 const int acc = tile_i & 1;
                 const uint32_t aph = (tile_i >> 1) & 1u;
-                if (!wait_bar(tempty_bar(acc), aph ^ 1u, abort_flag, p.err)) { aborted = true; break; }
+                if (!wait_bar(tempty_bar(acc), aph ^ 1u, abort_flag, p.err, (p.sleep_mask & 4) != 0)) { aborted = true; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_bar(T::TF32 ? cvt_bar(s) : full_bar(s), ph, abort_flag, p.err)) {
+                    if (!wait_bar(T::TF32 ? cvt_bar(s) : full_bar(s), ph, abort_flag, p.err, (p.sleep_mask & 4) != 0)) {
                         aborted = true;
                         break;
                     }
@@ -509,7 +646,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
-                if (!wait_bar_warp(full_bar(s), ph, abort_flag, p.err)) { aborted = true; break; }
+                if (!wait_bar_warp(full_bar(s), ph, abort_flag, p.err, (p.sleep_mask & 8) != 0)) { aborted = true; break; }
                 uint4* hi = reinterpret_cast<uint4*>(smem + s * T::A_STAGE);
                 uint4* lo = reinterpret_cast<uint4*>(smem + s * T::A_STAGE + A_BYTES);
                 for (int i = ct; i < n16; i += T::CVT_WARPS * 32) {
@@ -530,97 +667,51 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
         }
     } else if (warp < EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
-        const int wq = warp & 3;             // TMEM lane quarter
-        const int r = wq * 32 + lane;        // accumulator row = pixel within the tile
-        constexpr int COLS = BN / 2 < 16 ? 16 : BN / 2;   // columns per epilogue warp
+        // Warp w owns the 32 accumulator rows of TMEM lane quarter w % 4 and half of the
+        // columns.  It works in chunks of columns that make one output row segment of at most
+        // 128 bytes: read TMEM, add bias, GELU, convert, and write its 32 row segments into a
+        // shared staging buffer (16-byte slots XOR-swizzled by row: conflict-free both ways);
+        // then the warp reads the buffer back row-wise and stores whole row segments, so one
+        // store instruction writes 4 full 128-byte segments instead of 32 scattered 16-byte
+        // pieces.  Split plans store fp32 partial sums to the workspace the same way.
+        const int wq = warp & 3;
+        constexpr int COLS = BN / 2 < 16 ? 16 : BN / 2;
         const int cb_begin = (warp >> 2) * COLS;
         const int cb_end = cb_begin + COLS < BN ? cb_begin + COLS : BN;
-        const bool add_bias = (p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU) && p.splits == 1;
-        const bool do_gelu = (p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU) && p.splits == 1;
+        const bool partial = p.splits > 1;
+        const bool add_bias = (p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU) && !partial;
+        const bool do_gelu = (p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU) && !partial;
+        uint8_t* stg = smem + STG_OFFSET + warp * STG_WARP_BYTES;
         uint32_t tile_i = 0;
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x, ++tile_i) {
             int mt, gi, nt, split;
             decode_unit(p, u, mt, gi, nt, split);
             const int acc = tile_i & 1;
             const uint32_t aph = (tile_i >> 1) & 1u;
-            if (!wait_bar_warp(tfull_bar(acc), aph, abort_flag, p.err)) break;
+            if (!wait_bar_warp(tfull_bar(acc), aph, abort_flag, p.err, (p.sleep_mask & 2) != 0)) break;
             tc_fence_after();
-            int m;
-            bool row_ok;
-            if (T::TMA) {
-                const TileOrigin to = tile_origin(p, mt);
-                const int oh = to.oh0 + r / p.BW, ow = to.ow0 + r % p.BW;
-                row_ok = r < p.BW * p.BH && oh < g.Ho && ow < g.Wo;
-                m = ((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow;
-            } else {
-                m = mt * BM + r;
-                row_ok = m < g.M;
-            }
-            const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
-#pragma unroll 1
-            for (int cb = cb_begin; cb < cb_end; cb += 16) {
-                const int n = nt * BN + cb;
-                if (n >= g.K) break;                       // warp-uniform
-                uint32_t v[16];
-                __syncwarp();                              // tcgen05.ld is warp-aligned
-                tmem_ld16(taddr + cb, v);
-                tmem_ld_wait();
-                if (row_ok) {
-                    float f[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]);
-                    // K is a multiple of 8 (bf16) or 4 (fp32): groups of 4 columns are whole
-                    const int quads = min(4, (g.K - n) / 4);
-                    if (p.splits > 1) {
-                        float* dst = p.ws + ((size_t)split * g.M + m) * GK + (size_t)gi * g.K + n;
-                        for (int q = 0; q < quads; ++q)
-                            reinterpret_cast<float4*>(dst)[q] =
-                                make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
-                    } else {
-                        if (add_bias) {
-                            if (T::TF32) {
-                                const float4* bp = reinterpret_cast<const float4*>(
-                                    reinterpret_cast<const float*>(p.bias) + (size_t)gi * g.K + n);
-                                for (int q = 0; q < quads; ++q) {
-                                    const float4 b4 = __ldg(bp + q);
-                                    f[4 * q] += b4.x; f[4 * q + 1] += b4.y; f[4 * q + 2] += b4.z; f[4 * q + 3] += b4.w;
-                                }
-                            } else {
-                                const uint2* bp = reinterpret_cast<const uint2*>(
-                                    reinterpret_cast<const __nv_bfloat16*>(p.bias) + (size_t)gi * g.K + n);
-                                for (int q = 0; q < quads; ++q) {
-                                    const uint2 b2 = __ldg(bp + q);
-                                    f[4 * q] += __uint_as_float(b2.x << 16);
-                                    f[4 * q + 1] += __uint_as_float(b2.x & 0xFFFF0000u);
-                                    f[4 * q + 2] += __uint_as_float(b2.y << 16);
-                                    f[4 * q + 3] += __uint_as_float(b2.y & 0xFFFF0000u);
-                                }
-                            }
-                        }
-                        if (do_gelu) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) f[e] = gelu_f(f[e]);
-                        }
-                        if (T::TF32) {
-                            float* dst = reinterpret_cast<float*>(p.y) + (size_t)m * GK + (size_t)gi * g.K + n;
-                            for (int q = 0; q < quads; ++q)
-                                reinterpret_cast<float4*>(dst)[q] =
-                                    make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
-                        } else {
-                            __nv_bfloat16* dst =
-                                reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)m * GK + (size_t)gi * g.K + n;
-                            for (int h = 0; h < quads / 2; ++h) {
-                                uint4 o;
-                                o.x = pack_bf16x2(f[8 * h + 0], f[8 * h + 1]);
-                                o.y = pack_bf16x2(f[8 * h + 2], f[8 * h + 3]);
-                                o.z = pack_bf16x2(f[8 * h + 4], f[8 * h + 5]);
-                                o.w = pack_bf16x2(f[8 * h + 6], f[8 * h + 7]);
-                                reinterpret_cast<uint4*>(dst + 8 * h)[0] = o;
-                            }
-                        }
-                    }
+            TileOrigin to{0, 0, 0, 0};
+            if (T::TMA) to = tile_origin(p, mt);
+            // element offset of accumulator row rr's pixel, or -1 if the row is outside the output
+            auto row_offset = [&](int rr) -> long long {
+                int m;
+                if (T::TMA) {
+                    const int oh = to.oh0 + rr / p.BW, ow = to.ow0 + rr % p.BW;
+                    if (rr >= p.BW * p.BH || oh >= g.Ho || ow >= g.Wo) return -1;
+                    m = ((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow;
+                } else {
+                    m = mt * BM + rr;
+                    if (m >= g.M) return -1;
                 }
-            }
+                return (long long)m * GK;
+            };
+            const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
+            if (partial || T::TF32)
+                epilogue_chunks<BN, 4>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
+                                       do_gelu, stg, row_offset);
+            else
+                epilogue_chunks<BN, 2>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
+                                       do_gelu, stg, row_offset);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -637,7 +728,8 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
 
 template <int BN, int STAGES, int KIND>
 constexpr size_t smem_bytes_for() {
-    return 1024 + (size_t)STAGES * (Traits<KIND>::A_STAGE + Cfg<BN, KIND>::B_STAGE) + 8 * (3 * STAGES + 5) + 16;
+    return 1024 + (size_t)STAGES * (Traits<KIND>::A_STAGE + Cfg<BN, KIND>::B_STAGE) + EPI_WARPS * STG_WARP_BYTES +
+           8 * (3 * STAGES + 5) + 16;
 }
 
 template <int BN, int STAGES, int KIND>
@@ -665,7 +757,7 @@ cudaError_t launch_one(const TcParams& p, const CUtensorMap& map, int grid, cuda
 
 // (BN, stages) pairs compiled into the library, per kind; the plan picks one.
 #define TC_BF16_CONFIGS(X) X(256, 4) X(128, 6) X(64, 8) X(32, 8) X(16, 8)
-#define TC_TF32_CONFIGS(X) X(256, 2) X(128, 3) X(64, 4) X(32, 5) X(16, 5)
+#define TC_TF32_CONFIGS(X) X(256, 2) X(128, 3) X(64, 4) X(32, 4) X(16, 5)
 
 int tc_stages_for(int BN, int tf32) {
 #define X(bn, st) if (BN == bn) return st;

@@ -300,3 +300,39 @@ def test_tf32x3_and_ffma_both_meet_the_fp32_bound(case):
     ra, _ = assert_within("f32", layer.epilogue, a, ref, S, da)
     rc, _ = assert_within("f32", layer.epilogue, c, ref, S, dc)
     assert ra < 0.5, f"3xTF32 uses {ra:.2f} of the fp32 bound"
+
+
+def test_gelu_epilogue_on_every_bf16_value_in_range():
+    """Identity 1x1 conv with a GELU epilogue over every bf16 value in [-8, 8]: the output
+    must be the exact (erf) GELU rounded to bf16, give or take one bf16 unit in the last
+    place where the value sits next to a rounding boundary.  In the far negative tail, where
+    GELU(v) is below 1e-3 |v|, an erf evaluated to a fixed absolute accuracy cannot give
+    the tiny value to a few ulps; there the bound is the absolute one, 1e-6 |v|, plus the
+    output's own bf16 rounding."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = syn.bf16_bits_to_f32(bits)
+    keep = np.isfinite(vals) & (np.abs(vals) <= 8.0)
+    vals = np.unique(vals[keep])
+    C = 16
+    n = (len(vals) + C - 1) // C
+    xs = np.zeros(n * C, np.float32)
+    xs[:len(vals)] = vals
+    layer = L(1, 1, 1, C, C, (n,), (1,), (1,), (0,), (1,), CONV_EPI_GELU)
+    x = syn.f32_to_bf16_bits(xs).reshape(layer.x_shape())
+    w = syn.f32_to_bf16_bits(np.eye(C, dtype=np.float32)).reshape(layer.w_shape())
+    got, desc = run_gpu(layer, "bf16", x, w, None)
+    ref, _ = oracle_full(layer, "bf16", x, w, None)
+    ref_bits = syn.f32_to_bf16_bits(ref.astype(np.float32))
+    gi = got.reshape(-1).astype(np.int64)
+    ri = ref_bits.astype(np.int64)
+    # bf16 bit patterns of same-sign values differ by the ulp count
+    same_sign = (gi >> 15) == (ri >> 15)
+    ulps = np.where(same_sign, np.abs(gi - ri), np.abs(gi & 0x7FFF) + np.abs(ri & 0x7FFF))
+    v = xs.astype(np.float64)
+    tail = np.abs(ref) < 1e-3 * np.abs(v)
+    assert ulps[~tail].max() <= 1, desc
+    assert (ulps[~tail] == 0).mean() > 0.99, desc
+    gotf = syn.bf16_bits_to_f32(got.reshape(-1)).astype(np.float64)
+    rt = np.abs(ref[tail])
+    ulp = np.where(rt > 0, 2.0 ** (np.floor(np.log2(np.maximum(rt, 1e-300))) - 7), 0.0)   # bf16 ulp at |ref|
+    assert np.all(np.abs(gotf[tail] - ref[tail]) <= 1e-6 * np.abs(v[tail]) + ulp + 1e-30), desc
