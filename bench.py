@@ -7,9 +7,11 @@ k3 s2 p1 + GELU, in fp32 and in bf16.  One step runs all four layers through the
 Useful FLOPs = 2 x MACs, padded taps counted (the page's convention).
 
 Timing: W warm-up steps, then exactly K steps between CUDA events on the launching stream,
-bracketed by a barrier and a device synchronise; each layer is one CUDA graph (the conv
-kernel plus, for split plans, the reduction) and events between the graphs give every
-layer's device time.  Steps rotate over enough copies of every input, packed weight and
+bracketed by a barrier and a device synchronise.  A step is one CUDA graph holding every
+layer (each conv_fwd call: the conv kernel, plus the reduction for split plans), with
+timing events recorded inside the graph between the layers, which give each layer's
+device time (where PyTorch cannot record events inside a graph, each layer is its own
+graph and the events sit between them).  Steps rotate over enough copies of every input, packed weight and
 output that one rotation exceeds twice the L2 cache, so no step finds its data in L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
@@ -241,6 +243,37 @@ def rotation_sets(wls):
     return max(4, int(np.ceil(2.2 * L2_BYTES / per_set))), per_set
 
 
+def capture_steps(runs, R):
+    """One CUDA graph per rotation set holding every layer of the step, with timing events
+    recorded between the layers inside the graph.  Returns (graphs, events) or None when
+    this PyTorch cannot record events inside a graph."""
+    import torch
+    try:
+        events = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(runs) + 1)]
+                  for _ in range(R)]
+    except TypeError:
+        return None
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for r in range(R):
+            for lr in runs:
+                lr.call(r)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graphs = []
+    for r in range(R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream()
+            events[r][0].record(cs)
+            for j, lr in enumerate(runs):
+                lr.call(r)
+                events[r][j + 1].record(cs)
+        graphs.append(g)
+    return graphs, events
+
+
 def run_ours(args, ws, rank, local):
     import torch
     torch.cuda.set_device(local)
@@ -249,13 +282,30 @@ def run_ours(args, ws, rank, local):
     wls = frontend_workloads(args.workload)
     R, per_set = rotation_sets(wls)
     runs, inputs = setup_layers(wls, R)
-    for lr in runs:
-        lr.capture(R)
     stream = torch.cuda.current_stream()
+    cap = capture_steps(runs, R)
+    if cap is not None:
+        graphs, gev = cap
+        step_graphs = graphs
+        graph_mode = "one graph per step (all layers), timing events inside the graph"
+    else:
+        for lr in runs:
+            lr.capture(R)
+        step_graphs = None
+        graph_mode = "one graph per layer, timing events between graphs"
+
+    K = args.steps
+    nL = len(runs)
+    ev = None if step_graphs is not None else [[torch.cuda.Event(enable_timing=True) for _ in range(nL + 1)]
+                                               for _ in range(K)]
 
     def step(i):
-        for lr in runs:
-            lr.graphs[i % R].replay()
+        r = i % R
+        if step_graphs is not None:
+            step_graphs[r].replay()
+        else:
+            for lr in runs:
+                lr.graphs[r].replay()
 
     for i in range(args.warmup):
         step(i)
@@ -263,22 +313,31 @@ def run_ours(args, ws, rank, local):
     for lr in runs:
         lr.plan.check()
 
-    K = args.steps
-    nL = len(runs)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nL + 1)] for _ in range(K)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local).start()
     barrier(ws)
     torch.cuda.synchronize()
+    e_start.record(stream)
     for i in range(K):
-        ev[i][0].record(stream)
-        r = i % R
-        for j, lr in enumerate(runs):
-            lr.graphs[r].replay()
-            ev[i][j + 1].record(stream)
+        if ev is None:
+            step(i)
+        else:
+            ev[i][0].record(stream)
+            for j, lr in enumerate(runs):
+                lr.graphs[i % R].replay()
+                ev[i][j + 1].record(stream)
+    e_end.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][nL])
-    per_layer_ms = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K for j in range(nL)]
+    total_ms = e_start.elapsed_time(e_end)
+    if ev is None:
+        # the last replay of every rotation set's graph inside the timed region
+        last = sorted({i % R: i for i in range(K)}.keys())
+        per_layer_ms = [sum(gev[r][j].elapsed_time(gev[r][j + 1]) for r in last) / len(last) for j in range(nL)]
+        layer_samples = len(last)
+    else:
+        per_layer_ms = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K for j in range(nL)]
+        layer_samples = K
     # keep sampling clocks over a sustained window of the same steps (at least ~1.5 s)
     t_end = time.time() + 1.5
     i = 0
@@ -297,12 +356,14 @@ def run_ours(args, ws, rank, local):
     value = ws * step_flops / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end: pinned host inputs in, final outputs back to pinned host memory
-    e2e = run_e2e(args, runs, inputs, R, stream, ws, local)
+    e2e = run_e2e(args, runs, inputs, R, stream, ws, local, step)
 
     # ---- roofline of the dominant kernel
     dom = int(np.argmax(per_layer_ms))
     lr = runs[dom]
     roof = roofline_for(lr, per_layer_ms[dom])
+    roof["duration_us"] = round(per_layer_ms[dom] * 1e3, 3)
+    roof["duration_samples"] = layer_samples
 
     launches = K * sum(lr.kernels_per_call for lr in runs)
     line = {
@@ -316,6 +377,7 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": workload_description(args.workload),
                    "l2": f"inputs larger than L2: {R} rotating sets of activations, packed weights and outputs "
                          f"(~{R * per_set / 1e6:.0f} MB per rotation, L2 129 MB)",
+                   "graphs": graph_mode,
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "plans": {lr.name(): lr.plan.describe() for lr in runs}},
         "roofline": roof,
@@ -328,7 +390,9 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, runs, inputs, R, stream, ws, local):
+def run_e2e(args, runs, inputs, R, stream, ws, local, step):
+    """The same step through the public API with host buffers: each step copies its inputs
+    from pinned host memory, runs every layer, and copies the final outputs back."""
     import torch
     host_in, host_out = [], []
     for (wl, x, x_sets) in inputs:
@@ -347,8 +411,7 @@ def run_e2e(args, runs, inputs, R, stream, ws, local):
         r = i % R
         for h, x_sets in host_in:
             x_sets[r].copy_(h, non_blocking=True)
-        for lr in runs:
-            lr.graphs[r].replay()
+        step(i)
         for h, lr in host_out:
             h.copy_(lr.y_sets[r], non_blocking=True)
 
@@ -390,6 +453,13 @@ def roofline_for(lr, ms):
         pipe = peaks["bf16_tflops"] * 1e12
         bound_c, unit_peak = "tensor", peaks["bf16_tflops"]
         note = f"bf16 dense tensor peak, burst, {src}"
+    elif "variant=tc_tf32x3" in desc:
+        # TF32 peak = measured bf16 peak x nominal TF32/bf16 (1.1/2.25 PFLOP/s); 3xTF32 issues three
+        # TF32 products per useful product, so the useful-flop peak is a third of that
+        tf32 = peaks["bf16_tflops"] * (1.1 / 2.25)
+        pipe = tf32 / 3.0 * 1e12
+        bound_c, unit_peak = "tensor", tf32 / 3.0
+        note = f"TF32 dense peak (bf16 {src} x 1.1/2.25) / 3 products per useful product"
     else:
         pipe = SM_COUNT * FFMA_PER_SM_PER_CLK * 2 * SM_MAX_MHZ * 1e6
         bound_c, unit_peak = "alu", pipe / 1e12

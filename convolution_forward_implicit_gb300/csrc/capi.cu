@@ -13,7 +13,7 @@
 
 #include <cudaTypedefs.h>
 
-#include "../../include/conv.h"
+#include "conv.h"
 #include "internal.h"
 
 using namespace convfwd;
@@ -349,10 +349,19 @@ static bool plan_tc(conv_plan* p, bool tf32) {
         p->nkb = (int)cdiv(p->nchunks, 8);
         p->num_mt = (int)cdiv(g.M, 128);
     }
+    // Small problems: narrower N tiles first (more CTAs, one launch, no partial sums), unless
+    // each tile would then run a long reduction (K blocks weighted by the MMAs per block: 3
+    // for 3xTF32), where splitting K finishes sooner; split-K also when even 32-wide tiles
+    // leave more than half the SMs idle.
+    if (force_bn == 0 && p->nkb * (tf32 ? 3 : 1) <= 32) {
+        while (bn > 32 && (int64_t)p->num_mt * g.G * cdiv(g.K, bn) * 4 < (int64_t)p->sm_count * 3) bn /= 2;
+        p->BN = bn;
+        p->stages = tc_stages_for(bn, p->tf32);
+    }
     p->num_nt = (int)cdiv(g.K, bn);
     const int64_t units = (int64_t)p->num_mt * g.G * p->num_nt;
     int splits = 1;
-    if (units < p->sm_count && p->nkb >= 4) {
+    if (units * 2 < p->sm_count && p->nkb >= 4) {
         splits = (int)std::min<int64_t>(p->sm_count / units, p->nkb / 2);
         splits = std::max(1, std::min(splits, 16));
     }
