@@ -44,9 +44,13 @@ unsigned* error_word_ptr() {
 // K order: per_tap = 0 packs the (tap, c) chunks densely (K block kb holds chunks
 // 8kb..8kb+7, crossing taps); per_tap = 1 gives every tap cbt whole 64-channel blocks
 // (K block kb = tap*cbt + b holds channels 64b..64b+63 of that tap), matching one TMA box.
+// Packed small groups (pack > 1): the kernel sees G/pack groups of pack*C channels and
+// pack*K outputs; the packed weight of a super-group is block diagonal, output k' = jK + k
+// drawing only on input channels c' = jC + c of the same original group j, zero elsewhere.
+// K, C are the kernel's (packed) per-group extents, Ko, Co the caller's.
 __global__ void prepack_tc_kernel(const uint4* __restrict__ w, uint4* __restrict__ out, int K, int C, int taps,
                                   int BN, int num_nt, int nkb, int nchunks, int cpt, int per_tap, int cbt,
-                                  long long total16) {
+                                  int pack, int Ko, int Co, long long total16) {
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total16;
          idx += (long long)gridDim.x * blockDim.x) {
         const int j = (int)(idx & 7);
@@ -69,7 +73,13 @@ __global__ void prepack_tc_kernel(const uint4* __restrict__ w, uint4* __restrict
             c0 = (q - tap * cpt) * 8;
         }
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (k < K && ok) v = w[((((long long)g * K + k) * taps + tap) * C + c0) / 8];
+        if (k < K && ok) {
+            const int jk = k / Ko, jc = c0 / Co;        // original group within the super-group
+            if (jk == jc) {
+                const long long go = (long long)g * pack + jk;
+                v = w[(((go * Ko + (k - jk * Ko)) * taps + tap) * Co + (c0 - jc * Co)) / 8];
+            }
+        }
         const long long tile = (((long long)g * num_nt + nt) * nkb + kb) * BN + n;
         out[tile * 8 + (j ^ (n & 7))] = v;
     }
@@ -182,6 +192,7 @@ struct conv_plan {
     // tensor-core plan
     int BN, stages, num_mt, num_nt, nkb, nchunks, cpt, splits, kbps, total_units, grid;
     int tma, map_kind, BW, BH, tiles_w, tiles_h, cbt, tf32, sleep_mask;
+    int pack, Go, Co, Ko;   // small-group packing factor and the caller's G, C, K
     // SIMT plan
     int BM, Kg, Kpad, nkt, ktps, vec;
     size_t prepack_bytes, workspace_bytes;
@@ -478,10 +489,26 @@ conv_status conv_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, i
     // TMA gather can express: tcgen05 3xTF32.  Everything else: the FFMA kernel.
     const bool no_tc = env_int("CONV_FORCE_SIMT", 0) != 0;
     bool tc = false;
+    p->pack = 1; p->Go = g.G; p->Co = g.C; p->Ko = g.K;
+    // Groups narrower than one 64-channel block: pack 64/C of them into a super-group with a
+    // block-diagonal weight, so each tap still fills a whole 128-byte TMA box row (the MMA
+    // does pack-fold redundant work on the zero blocks; the useful FLOP count is unchanged).
+    if (!no_tc && dtype == CONV_BF16 && C % 8 == 0 && K % 8 == 0 && C < 64 && 64 % C == 0 &&
+        G % (64 / C) == 0 && (int64_t)K * (64 / C) <= 4096 && env_int("CONV_NO_PACK", 0) == 0) {
+        p->pack = (int)(64 / C);
+        g.G = (int)(G / p->pack); g.C = 64; g.K = (int)(K * p->pack);
+    }
     if (!no_tc && dtype == CONV_BF16 && C % 8 == 0 && K % 8 == 0) tc = plan_tc(p, false);
+    if (!tc && p->pack > 1) {   // not planned on the tensor cores after all: the caller's geometry
+        p->pack = 1; g.G = p->Go; g.C = p->Co; g.K = p->Ko;
+    }
     if (!no_tc && dtype == CONV_F32 && C % 4 == 0 && K % 4 == 0) tc = plan_tc(p, true);
     if (tc) {
         p->variant = VAR_TC;
+        if (p->pack > 1) {
+            const size_t n = strlen(p->desc);
+            snprintf(p->desc + n, sizeof(p->desc) - n, " pack=%d", p->pack);
+        }
     } else {
         p->variant = VAR_SIMT;
         plan_simt(p);
@@ -528,7 +555,8 @@ conv_status conv_prepack_weights(conv_plan_t plan, const void* w, void* w_packed
         const int blocks = (int)std::min<long long>(cdiv(total16, threads), 65535);
         prepack_tc_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint4*>(w), static_cast<uint4*>(w_packed),
                                                      g.K, g.C, g.taps, plan->BN, plan->num_nt, plan->nkb,
-                                                     plan->nchunks, plan->cpt, plan->tma, plan->cbt, total16);
+                                                     plan->nchunks, plan->cpt, plan->tma, plan->cbt, plan->pack,
+                                                     plan->Ko, plan->Co, total16);
     } else {
         const long long total = (long long)g.G * plan->Kg * plan->Kpad;
         const int blocks = (int)std::min<long long>(cdiv(total, threads), 65535);

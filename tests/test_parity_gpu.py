@@ -336,3 +336,32 @@ def test_gelu_epilogue_on_every_bf16_value_in_range():
     rt = np.abs(ref[tail])
     ulp = np.where(rt > 0, 2.0 ** (np.floor(np.log2(np.maximum(rt, 1e-300))) - 7), 0.0)   # bf16 ulp at |ref|
     assert np.all(np.abs(gotf[tail] - ref[tail]) <= 1e-6 * np.abs(v[tail]) + ulp + 1e-30), desc
+
+
+PACKED = [
+    ("2d_g32_c8", L(2, 2, 32, 8, 8, (13, 15), (3, 3), (1, 1), (1, 1), (1, 1), CONV_EPI_NONE)),
+    ("2d_g16_c8_k16_d2", L(2, 1, 16, 8, 16, (12, 17), (3, 3), (1, 1), (2, 2), (2, 2))),
+    ("2d_g8_c16_k8_s2", L(2, 2, 8, 16, 8, (15, 13), (3, 3), (2, 2), (1, 1), (1, 1), CONV_EPI_BIAS)),
+    ("1d_g4_c32_k40", L(1, 3, 4, 32, 40, (97,), (3,), (1,), (1,), (1,))),
+    ("3d_g16_c8", L(3, 1, 16, 8, 8, (4, 7, 9), (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), CONV_EPI_BIAS)),
+]
+
+
+@pytest.mark.parametrize("name,layer", PACKED, ids=[p[0] for p in PACKED])
+def test_packed_small_groups_match_oracle_and_unpacked(name, layer):
+    """Groups narrower than 64 channels run packed into block-diagonal super-groups; the
+    same problem with packing disabled takes the cp.async path.  Both meet the bound, and
+    on integer inputs both are exact."""
+    x, w, b = make_inputs(layer, "bf16", 1200 + zlib.crc32(name.encode()) % 500)
+    ref, S = oracle_full(layer, "bf16", x, w, b)
+    a, da = run_gpu(layer, "bf16", x, w, b, guard=64)
+    c, dc = run_gpu(layer, "bf16", x, w, b, env={"CONV_NO_PACK": 1})
+    assert "pack=" in da and "pack=" not in dc
+    assert_within("bf16", layer.epilogue, a, ref, S, da)
+    assert_within("bf16", layer.epilogue, c, ref, S, dc)
+    from dataclasses import replace
+    li = replace(layer, epilogue=CONV_EPI_BIAS, bias_bound=0.05)     # integer sums are exact; GELU is not
+    xi, wi, bi = make_inputs(li, "bf16", 1300, kind="int")
+    refi, _ = oracle_full(li, "bf16", xi, wi, bi)
+    ai, _ = run_gpu(li, "bf16", xi, wi, bi)
+    assert np.array_equal(ai.reshape(-1), syn.f32_to_bf16_bits(refi.astype(np.float32))), da
