@@ -48,9 +48,11 @@ unsigned* error_word_ptr() {
 // pack*K outputs; the packed weight of a super-group is block diagonal, output k' = jK + k
 // drawing only on input channels c' = jC + c of the same original group j, zero elsewhere.
 // K, C are the kernel's (packed) per-group extents, Ko, Co the caller's.
+// K order 2 (slab mode) walks k-groups (input plane z, channel block b) and within each the
+// Y*X taps of that plane: K block kb = ((z*cbt + b)*Y + y)*X + x.
 __global__ void prepack_tc_kernel(const uint4* __restrict__ w, uint4* __restrict__ out, int K, int C, int taps,
                                   int BN, int num_nt, int nkb, int nchunks, int cpt, int per_tap, int cbt,
-                                  int pack, int Ko, int Co, long long total16) {
+                                  int pack, int Ko, int Co, int Y, int X, long long total16) {
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total16;
          idx += (long long)gridDim.x * blockDim.x) {
         const int j = (int)(idx & 7);
@@ -62,7 +64,13 @@ __global__ void prepack_tc_kernel(const uint4* __restrict__ w, uint4* __restrict
         const int k = nt * BN + n;
         int tap, c0;
         bool ok;
-        if (per_tap) {
+        if (per_tap == 2) {
+            const int kg = kb / (Y * X), t = kb - kg * (Y * X);
+            const int z = kg / cbt, b = kg - z * cbt;
+            tap = (z * Y + t / X) * X + t % X;
+            c0 = b * 64 + j * 8;
+            ok = c0 < C;
+        } else if (per_tap) {
             tap = kb / cbt;
             c0 = (kb - tap * cbt) * 64 + j * 8;
             ok = c0 < C;
@@ -90,7 +98,8 @@ __global__ void prepack_tc_kernel(const uint4* __restrict__ w, uint4* __restrict
 // low parts (w - high, exact in fp32), both 128-byte swizzled.  K block kb = tap*cbt + b
 // holds channels 32b..32b+31 of that tap; 16-byte chunk j holds channels 32b+4j..+3.
 __global__ void prepack_tf32x3_kernel(const float4* __restrict__ w, uint4* __restrict__ out, int K, int C,
-                                      int taps, int BN, int num_nt, int nkb, int cbt, long long total16) {
+                                      int taps, int BN, int num_nt, int nkb, int cbt, int slab_order, int Y, int X,
+                                      long long total16) {
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total16;
          idx += (long long)gridDim.x * blockDim.x) {
         const int j = (int)(idx & 7);
@@ -100,8 +109,16 @@ __global__ void prepack_tf32x3_kernel(const float4* __restrict__ w, uint4* __res
         const int nt = (int)(r % num_nt);
         const int g = (int)(r / num_nt);
         const int k = nt * BN + n;
-        const int tap = kb / cbt;
-        const int c0 = (kb - tap * cbt) * 32 + j * 4;
+        int tap, c0;
+        if (slab_order) {   // K block kb = ((z*cbt + b)*Y + y)*X + x, as for bf16
+            const int kg = kb / (Y * X), t = kb - kg * (Y * X);
+            const int z = kg / cbt, b = kg - z * cbt;
+            tap = (z * Y + t / X) * X + t % X;
+            c0 = b * 32 + j * 4;
+        } else {
+            tap = kb / cbt;
+            c0 = (kb - tap * cbt) * 32 + j * 4;
+        }
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (k < K && c0 < C) v = w[((((long long)g * K + k) * taps + tap) * C + c0) / 4];
         uint4 hi, lo;
@@ -193,6 +210,8 @@ struct conv_plan {
     int BN, stages, num_mt, num_nt, nkb, nchunks, cpt, splits, kbps, total_units, grid;
     int tma, map_kind, BW, BH, tiles_w, tiles_h, cbt, tf32, sleep_mask;
     int pack, Go, Co, Ko;   // small-group packing factor and the caller's G, C, K
+    int slab, slab_bws, slab_hr, slab_nkg, slab_nbg, slab_btaps, slab_sa, slab_sb, slab_a_stage;
+    size_t slab_smem;
     // SIMT plan
     int BM, Kg, Kpad, nkt, ktps, vec;
     size_t prepack_bytes, workspace_bytes;
@@ -259,22 +278,27 @@ static bool encode_act_map(const conv_plan* p, const void* x, CUtensorMap* map) 
     const cuuint32_t cblk = p->tf32 ? 32 : 64;    // channels in one 128-byte row
     cuuint64_t dims[5], strides[4];
     cuuint32_t box[5], es[5];
+    // per-tap boxes cover BW x BH output pixels (stride as element stride); slab boxes cover
+    // the tile's input rows: BWs x HR pixels at unit stride
+    const cuuint32_t bx = p->slab ? (cuuint32_t)p->slab_bws : (cuuint32_t)(p->BW * g.sw);
+    const cuuint32_t by = p->slab ? (cuuint32_t)p->slab_hr : (cuuint32_t)(p->BH * g.sh);
+    const cuuint32_t ex = p->slab ? 1u : (cuuint32_t)g.sw, ey = p->slab ? 1u : (cuuint32_t)g.sh;
     if (p->map_kind == 0) {
         dims[0] = (cuuint64_t)g.G * g.C; dims[1] = g.W; dims[2] = g.H; dims[3] = g.D; dims[4] = g.N;
         strides[0] = dims[0] * e;
         strides[1] = strides[0] * g.W;
         strides[2] = strides[1] * g.H;
         strides[3] = strides[2] * g.D;
-        box[0] = cblk; box[1] = (cuuint32_t)(p->BW * g.sw); box[2] = (cuuint32_t)(p->BH * g.sh); box[3] = 1; box[4] = 1;
-        es[0] = 1; es[1] = (cuuint32_t)g.sw; es[2] = (cuuint32_t)g.sh; es[3] = 1; es[4] = 1;
+        box[0] = cblk; box[1] = bx; box[2] = by; box[3] = 1; box[4] = 1;
+        es[0] = 1; es[1] = ex; es[2] = ey; es[3] = 1; es[4] = 1;
     } else {
         dims[0] = g.C; dims[1] = g.G; dims[2] = g.W; dims[3] = g.H; dims[4] = g.N;
         strides[0] = (cuuint64_t)g.C * e;
         strides[1] = (cuuint64_t)g.G * g.C * e;
         strides[2] = strides[1] * g.W;
         strides[3] = strides[2] * g.H;
-        box[0] = cblk; box[1] = 1; box[2] = (cuuint32_t)(p->BW * g.sw); box[3] = (cuuint32_t)(p->BH * g.sh); box[4] = 1;
-        es[0] = 1; es[1] = 1; es[2] = (cuuint32_t)g.sw; es[3] = (cuuint32_t)g.sh; es[4] = 1;
+        box[0] = cblk; box[1] = 1; box[2] = bx; box[3] = by; box[4] = 1;
+        es[0] = 1; es[1] = 1; es[2] = ex; es[3] = ey; es[4] = 1;
     }
     const CUresult r = fn(map, p->tf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
                           const_cast<void*>(x), dims, strides, box, es,
@@ -304,11 +328,37 @@ static void choose_tile_shape(conv_plan* p) {
     p->tiles_h = (int)cdiv(g.Ho, best_bh);
 }
 
+// Slab geometry for a stride-1 problem (see tc_slab.cu): output tiles of BH rows x BW columns
+// whose slab (BH + dh(Y-1)) x (BW + dw(X-1)) input pixels fit a 128-row accumulator.  Returns
+// false when the problem has no such tile.
+static bool choose_slab_shape(conv_plan* p) {
+    const Geom& g = p->g;
+    const int reach_w = g.dw * (g.X - 1), reach_h = g.dh * (g.Y - 1);
+    const int bw = std::min(g.Wo, 128 - reach_w);
+    if (bw < 8) return false;
+    const int bws = bw + reach_w;
+    const int bh = std::max(1, std::min(g.Ho, 128 / bws));
+    const int hr = bh + reach_h;
+    if (bws > 256 || hr > 256) return false;
+    p->BW = bw; p->BH = bh;
+    p->tiles_w = (int)cdiv(g.Wo, bw);
+    p->tiles_h = (int)cdiv(g.Ho, bh);
+    p->slab_bws = bws; p->slab_hr = hr;
+    p->slab_nbg = g.Y; p->slab_btaps = g.X;
+    // a window may read up to reach_h*bws + reach_w + 128 rows from the stage start
+    const int64_t rows = std::max<int64_t>((int64_t)reach_h * bws + reach_w + 128, (int64_t)hr * bws);
+    p->slab_a_stage = (int)(cdiv(rows * 128, 1024) * 1024 * (p->tf32 ? 2 : 1));
+    return true;
+}
+
 // Tensor-core tile choice: BN from the compiled set, the smallest padded width for K
 // <= 256, else 256 or 128, whichever wastes fewer columns; then split-K when the tiles
 // alone leave SMs idle (page "onnxruntime PR #33639", "Description": large tiles for
 // large problems, split-K for small problems because it fills the GPU better).
-static bool plan_tc(conv_plan* p, bool tf32) {
+static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab = true);
+static bool plan_tc_per_tap_retry(conv_plan* p, bool tf32) { return plan_tc(p, tf32, false); }
+
+static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     const Geom& g = p->g;
     int bn;
     if (g.K <= 16) bn = 16;
@@ -334,16 +384,30 @@ static bool plan_tc(conv_plan* p, bool tf32) {
     bool tma = map_kind >= 0 && g.C >= cblk && g.sw <= 8 && g.sh <= 8;
     const char* force_gather = getenv("CONV_FORCE_GATHER");
     if (!tf32 && force_gather && strcmp(force_gather, "cpasync") == 0) tma = false;
+    // Slab mode for stride-1 problems with several taps per plane (one box serves them all);
+    // its shared-memory fit is checked once the N tile is known.
+    p->slab = 0;
+    const bool want_slab = allow_slab && tma && g.sw == 1 && g.sh == 1 && g.sd == 1 && g.Y * g.X >= 3 &&
+                           !(force_gather && strcmp(force_gather, "tma") == 0);
     if (tma) {
         p->map_kind = map_kind;
-        choose_tile_shape(p);
+        if (want_slab && choose_slab_shape(p)) p->slab = 1;
+        else choose_tile_shape(p);
         // A trial encode with a placeholder address checks the box against the driver's
         // limits.  The encoder needs a current context: make the current device's primary
         // context current first (without a device the rules above decide alone).
         int dev = 0;
         if (encode_fn() && cudaGetDevice(&dev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess) {
             CUtensorMap probe;
-            if (!encode_act_map(p, reinterpret_cast<const void*>((uintptr_t)4096), &probe)) tma = false;
+            if (!encode_act_map(p, reinterpret_cast<const void*>((uintptr_t)4096), &probe)) {
+                if (p->slab) {
+                    p->slab = 0;
+                    choose_tile_shape(p);
+                    if (!encode_act_map(p, reinterpret_cast<const void*>((uintptr_t)4096), &probe)) tma = false;
+                } else {
+                    tma = false;
+                }
+            }
         }
         cudaGetLastError();
     }
@@ -378,13 +442,36 @@ static bool plan_tc(conv_plan* p, bool tf32) {
     }
     const int force = env_int("CONV_FORCE_SPLITK", 0);
     if (force >= 1) splits = std::min(force, p->nkb);
+    if (p->slab) {
+        // slab mode runs whole reductions per tile and needs its rings to fit
+        p->slab_sa = 2;
+        p->slab_sb = 0;
+        for (int sb = 8; sb >= 2; --sb)
+            if (slab_smem_bytes(bn, p->tf32, 2, sb, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
+                p->slab_sb = sb;
+                break;
+            }
+        if (splits > 1 || p->slab_sb < 2) {
+            p->slab = 0;                               // back to per-tap boxes
+            choose_tile_shape(p);
+            return plan_tc_per_tap_retry(p, tf32);
+        }
+        p->slab_nkg = g.Z * p->cbt;
+        p->slab_smem = slab_smem_bytes(bn, p->tf32, p->slab_sa, p->slab_sb, (size_t)p->slab_a_stage, p->slab_btaps);
+    }
     p->kbps = (int)cdiv(p->nkb, splits);
     p->splits = (int)cdiv(p->nkb, p->kbps);     // every split non-empty
     p->total_units = (int)(units * p->splits);
     p->grid = std::min(p->total_units, p->sm_count);
     p->prepack_bytes = (size_t)g.G * p->num_nt * p->nkb * bn * 128 * (tf32 ? 2 : 1);
     p->workspace_bytes = p->splits > 1 ? (size_t)p->splits * g.M * g.G * g.K * sizeof(float) : 0;
-    if (p->tma)
+    if (p->slab)
+        snprintf(p->desc, sizeof(p->desc),
+                 "variant=%s gather=tma-slab tile=128x%d pixels=%dx%d slab=%dx%d k_block=%d stages=%d+%d splits=1 "
+                 "units=%d grid=%d k_blocks=%d map=%d",
+                 tf32 ? "tc_tf32x3" : "tc_bf16", bn, p->BH, p->BW, p->slab_hr, p->slab_bws, cblk, p->slab_sa,
+                 p->slab_sb, p->total_units, p->grid, p->nkb, p->map_kind);
+    else if (p->tma)
         snprintf(p->desc, sizeof(p->desc),
                  "variant=%s gather=tma tile=128x%d pixels=%dx%d k_block=%d stages=%d splits=%d units=%d "
                  "grid=%d k_blocks=%d map=%d",
@@ -549,14 +636,14 @@ conv_status conv_prepack_weights(conv_plan_t plan, const void* w, void* w_packed
         const int blocks = (int)std::min<long long>(cdiv(total16, threads), 65535);
         prepack_tf32x3_kernel<<<blocks, threads, 0, s>>>(static_cast<const float4*>(w), static_cast<uint4*>(w_packed),
                                                          g.K, g.C, g.taps, plan->BN, plan->num_nt, plan->nkb,
-                                                         plan->cbt, total16);
+                                                         plan->cbt, plan->slab, g.Y, g.X, total16);
     } else if (plan->variant == VAR_TC) {
         const long long total16 = (long long)(plan->prepack_bytes / 16);
         const int blocks = (int)std::min<long long>(cdiv(total16, threads), 65535);
         prepack_tc_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint4*>(w), static_cast<uint4*>(w_packed),
                                                      g.K, g.C, g.taps, plan->BN, plan->num_nt, plan->nkb,
-                                                     plan->nchunks, plan->cpt, plan->tma, plan->cbt, plan->pack,
-                                                     plan->Ko, plan->Co, total16);
+                                                     plan->nchunks, plan->cpt, plan->slab ? 2 : plan->tma,
+                                                     plan->cbt, plan->pack, plan->Ko, plan->Co, g.Y, g.X, total16);
     } else {
         const long long total = (long long)g.G * plan->Kg * plan->Kpad;
         const int blocks = (int)std::min<long long>(cdiv(total, threads), 65535);
@@ -615,9 +702,13 @@ conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, cons
         tp.tma = plan->tma; tp.map_kind = plan->map_kind; tp.BW = plan->BW; tp.BH = plan->BH;
         tp.tiles_w = plan->tiles_w; tp.tiles_h = plan->tiles_h; tp.cbt = plan->cbt; tp.tf32 = plan->tf32;
         tp.sleep_mask = plan->sleep_mask;
+        tp.slab = plan->slab; tp.slab_bws = plan->slab_bws; tp.slab_hr = plan->slab_hr; tp.slab_nkg = plan->slab_nkg;
+        tp.slab_nbg = plan->slab_nbg; tp.slab_btaps = plan->slab_btaps; tp.slab_sa = plan->slab_sa;
+        tp.slab_sb = plan->slab_sb; tp.slab_a_stage = plan->slab_a_stage;
         CUtensorMap map;
         if (plan->tma && !encode_act_map(plan, x, &map)) return CONV_ERR_CUDA;
-        e = launch_tc(tp, plan->tma ? &map : nullptr, plan->stages, plan->grid, s);
+        e = plan->slab ? launch_slab(tp, &map, plan->grid, plan->slab_smem, s)
+                       : launch_tc(tp, plan->tma ? &map : nullptr, plan->stages, plan->grid, s);
     } else {
         SimtParams sp;
         sp.g = plan->g;
@@ -736,9 +827,13 @@ extern "C" conv_status conv_fwd_static_scratch(conv_plan_t plan, const void* x, 
         tp.tma = plan->tma; tp.map_kind = plan->map_kind; tp.BW = plan->BW; tp.BH = plan->BH;
         tp.tiles_w = plan->tiles_w; tp.tiles_h = plan->tiles_h; tp.cbt = plan->cbt; tp.tf32 = plan->tf32;
         tp.sleep_mask = plan->sleep_mask;
+        tp.slab = plan->slab; tp.slab_bws = plan->slab_bws; tp.slab_hr = plan->slab_hr; tp.slab_nkg = plan->slab_nkg;
+        tp.slab_nbg = plan->slab_nbg; tp.slab_btaps = plan->slab_btaps; tp.slab_sa = plan->slab_sa;
+        tp.slab_sb = plan->slab_sb; tp.slab_a_stage = plan->slab_a_stage;
         CUtensorMap map;
         if (plan->tma && !encode_act_map(plan, x, &map)) return CONV_ERR_CUDA;
-        e = launch_tc(tp, plan->tma ? &map : nullptr, plan->stages, plan->grid, s);
+        e = plan->slab ? launch_slab(tp, &map, plan->grid, plan->slab_smem, s)
+                       : launch_tc(tp, plan->tma ? &map : nullptr, plan->stages, plan->grid, s);
     } else {
         SimtParams sp;
         sp.g = plan->g;

@@ -48,12 +48,27 @@ struct TcParams {
     int tiles_w, tiles_h;   // tiles per output plane
     int cbt;                // channel blocks per tap (64 bf16 or 32 fp32 channels; kb = tap*cbt + block)
     int tf32;               // 1: fp32 I/O as 3xTF32 (TMA gather only)
-    int sleep_mask;         // which roles wait with a suspend hint: 1 producer, 2 epilogue, 4 MMA, 8 splitter
+    int sleep_mask;         // which roles wait with a suspend hint: 1 producer, 2 epilogue, 4 MMA
+    // slab mode (stride 1): one box of HR input rows x BWs pixels per (tile, input plane,
+    // channel block) serves all Y*X taps of that plane as row-shifted windows
+    int slab;               // 1: slab mode (always with tma = 1)
+    int slab_bws;           // slab row pitch in pixels: BW + dw*(X-1)
+    int slab_hr;            // slab rows: BH + dh*(Y-1)
+    int slab_nkg;           // k-groups per tile: Z * cbt (input plane, channel block)
+    int slab_nbg;           // weight ring stages per k-group (filter rows Y)
+    int slab_btaps;         // taps per weight stage (filter columns X)
+    int slab_sa, slab_sb;   // slab ring and weight ring stages
+    int slab_a_stage;       // bytes per slab stage (3xTF32: hi half then lo half)
 };
+
+constexpr size_t SLAB_SMEM_MAX = 232448;   // dynamic shared memory a block may opt in to
 
 // Launch the tensor-core kernel for the (BN, stages) pair the plan picked (see tc_stages_for).
 cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, int stages, int grid, cudaStream_t stream);
 int tc_stages_for(int BN, int tf32);
+// Slab-mode kernel; smem from slab_smem_bytes.
+cudaError_t launch_slab(const TcParams& p, const CUtensorMap* act_map, int grid, size_t smem, cudaStream_t stream);
+size_t slab_smem_bytes(int BN, int tf32, int sa, int sb, size_t a_stage, int btaps);
 
 // ---- SIMT FFMA implicit GEMM (fp32 I/O; also bf16 where channel counts rule out the tensor path) ----
 struct SimtParams {

@@ -1,0 +1,346 @@
+// Device helpers shared by the tensor-core convolution kernels: PTX wrappers for mbarrier,
+// TMA/bulk copies and tcgen05, the shared-memory matrix descriptor, the GELU forms, output
+// tile decoding and the staged, coalesced epilogue.  Included inside each kernel file.
+#pragma once
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace convfwd {
+namespace {
+
+constexpr int BM = 128;
+constexpr int EPI_WARPS = 8;                           // two per TMEM lane quarter, splitting the columns
+constexpr int LAG = 2;                                 // K blocks a cp.async producer keeps in flight
+constexpr uint32_t A_BYTES = BM * 128;                 // 128 pixels x 64 bf16
+constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier ----
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+// try_wait with a suspend-time hint: a waiting thread sleeps until the phase completes (or
+// the hint runs out) instead of spinning, so waiting warps do not take issue slots from the
+// warps that work.
+// Which roles sleep is a plan choice (TcParams::sleep_mask): waking a suspended thread costs
+// latency, which matters on the critical path (the MMA issuer, refills of a short ring).
+constexpr uint32_t SUSPEND_HINT_NS = 1000000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(SUSPEND_HINT_NS)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait.  Returns false if this CTA is aborting (the limit ran out here or elsewhere).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned* err,
+                                         bool sleep = false) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (sleep ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+            *abort_flag = 1;
+            atomicOr(err, ERR_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Bounded wait taken by lane 0 for the whole (converged) warp; every lane returns lane 0's
+// outcome, so a warp never splits at an abort and later meets itself at a warp barrier.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned* err, bool sleep = false) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, err, sleep) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// ---- async copies ----
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Tiled TMA load of a 5-D box (coordinates innermost first; out-of-range elements read 0).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            int c4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// ---- tcgen05 ----
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+// 32 lanes x 32 bits, 16 consecutive columns: thread t of the warp gets lane (base + t).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 B,
+// 8-row groups 1024 B apart.  Fields: start address >> 4 (bits 0-13), leading byte
+// offset >> 4 (16-29, unused for this layout), stride byte offset >> 4 (32-45),
+// descriptor version 1 (46-48), swizzle mode 2 = 128 B (61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction descriptor: D fp32 (bit 4), A and B format (bits 7-9, 10-12: 1 = bf16
+// for kind::f16, 2 = tf32 for kind::tf32), both K-major, N >> 3 at bits 17-22, M >> 4 at
+// bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int m, int n, uint32_t ab_format) {
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
+
+// GELU for bf16 outputs: v * Phi(v) with erf from Abramowitz & Stegun, Handbook of
+// Mathematical Functions, eq. 7.1.28 (after Hastings): erf(z) = 1 - (1 + a1 z + ... + a6 z^6)^-16
+// for z >= 0, |error| <= 3e-7.  Evaluated in fp32 the GELU's relative error stays below 1e-6,
+// far under the bf16 rounding step, at one reciprocal and no exponential per value.
+__device__ __forceinline__ float gelu_bf16out(float v) {
+    const float z = fabsf(v) * 0.70710678118654752f;
+    float y = fmaf(z, 0.0000430638f, 0.0002765672f);
+    y = fmaf(z, y, 0.0001520143f);
+    y = fmaf(z, y, 0.0092705272f);
+    y = fmaf(z, y, 0.0422820123f);
+    y = fmaf(z, y, 0.0705230784f);
+    y = fmaf(z, y, 1.0f);
+    y = y * y; y = y * y; y = y * y; y = y * y;         // (.)^16
+    const float h = __fdividef(0.5f * v, y);            // 0.5 v (1 - erf(|v|/sqrt 2)); 0 once y overflows
+    return v >= 0.0f ? v - h : h;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void decode_unit(const TcParams& p, int u, int& mt, int& g, int& nt, int& split) {
+    split = u % p.splits;
+    int r = u / p.splits;
+    nt = r % p.num_nt;
+    r /= p.num_nt;
+    g = r % p.g.G;
+    mt = r / p.g.G;
+}
+
+// TMA tiles: mt -> (n, od, oh0, ow0) of a BH x BW block of one output plane.
+struct TileOrigin {
+    int n, od, oh0, ow0;
+};
+__device__ __forceinline__ TileOrigin tile_origin(const TcParams& p, int mt) {
+    TileOrigin t;
+    const int tw = mt % p.tiles_w;
+    int r = mt / p.tiles_w;
+    const int th = r % p.tiles_h;
+    r /= p.tiles_h;
+    t.od = r % p.g.Do;
+    t.n = r / p.g.Do;
+    t.oh0 = th * p.BH;
+    t.ow0 = tw * p.BW;
+    return t;
+}
+
+constexpr int STG_WARP_BYTES = 32 * 128;   // one warp's staging buffer: 32 rows x 128 B
+
+// Epilogue of one warp's 32 rows x [cb_begin, cb_end) accumulator columns (see the
+// epilogue role in the kernel).  ESZ is the stored element size: 2 for bf16 outputs, 4 for
+// fp32 outputs and for split-K partial sums.
+template <int BN, int ESZ, typename RowOffset>
+__device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t taddr, int lane, int wq, int cb_begin,
+                                                int cb_end, int nt, int gi, int split, bool partial, bool add_bias,
+                                                bool do_gelu, uint8_t* stg, RowOffset row_offset) {
+    constexpr int COLS = BN / 2 < 16 ? 16 : BN / 2;
+    constexpr int CW = COLS < 128 / ESZ ? COLS : 128 / ESZ;   // columns per chunk
+    constexpr int RB = CW * ESZ;                             // bytes per row segment (32..128)
+    constexpr int LPR = RB / 16;                             // 16-byte slots (= store lanes) per row
+    constexpr int RPI = 32 / LPR;                            // rows per store instruction
+    constexpr int SH = LPR == 8 ? 0 : LPR == 4 ? 1 : LPR == 2 ? 2 : 3;   // log2(8 / LPR)
+    constexpr int EPS = 16 / ESZ;                            // elements per 16-byte slot
+    const Geom& g = p.g;
+    const int GK = g.G * g.K;
+    // the store-phase rows of this lane are the same for every chunk of the tile
+    long long roff[LPR];
+#pragma unroll
+    for (int i = 0; i < LPR; ++i) roff[i] = row_offset(wq * 32 + lane / LPR + RPI * i);
+    const int slot = lane % LPR;
+    const int swz = (lane >> SH) & (LPR - 1);   // this lane's row: slot j sits at j ^ swz
+    for (int cb = cb_begin; cb < cb_end; cb += CW) {
+        const int n0 = nt * BN + cb;
+        if (n0 >= g.K) break;                               // warp-uniform
+        // 16 columns at a time: TMEM -> fp32 -> bias, GELU -> this lane's row slots in staging
+#pragma unroll
+        for (int q = 0; q < CW / 16; ++q) {
+            const int nq = n0 + 16 * q;
+            uint32_t v[16];
+            __syncwarp();                                   // tcgen05.ld is warp-aligned
+            tmem_ld16(taddr + (uint32_t)(cb + 16 * q), v);
+            tmem_ld_wait();
+            float f[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]);
+            if (add_bias) {
+                // only whole 8-column groups inside K are read; columns past K are never stored
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (nq + 8 * j >= g.K) break;
+                    if (ESZ == 4) {
+                        const float4* bp = reinterpret_cast<const float4*>(
+                                               reinterpret_cast<const float*>(p.bias) + (size_t)gi * g.K + nq) +
+                                           2 * j;
+                        const float4 a = __ldg(bp);
+                        const float4 b = (nq + 8 * j + 4 < g.K) ? __ldg(bp + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        f[8 * j] += a.x; f[8 * j + 1] += a.y; f[8 * j + 2] += a.z; f[8 * j + 3] += a.w;
+                        f[8 * j + 4] += b.x; f[8 * j + 5] += b.y; f[8 * j + 6] += b.z; f[8 * j + 7] += b.w;
+                    } else {
+                        const uint4 b4 = __ldg(reinterpret_cast<const uint4*>(
+                                                   reinterpret_cast<const __nv_bfloat16*>(p.bias) + (size_t)gi * g.K +
+                                                   nq) +
+                                               j);
+                        const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            f[8 * j + 2 * e] += __uint_as_float(bw[e] << 16);
+                            f[8 * j + 2 * e + 1] += __uint_as_float(bw[e] & 0xFFFF0000u);
+                        }
+                    }
+                }
+            }
+            if (do_gelu) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) f[e] = ESZ == 2 ? gelu_bf16out(f[e]) : gelu_f(f[e]);
+            }
+            constexpr int SPQ = 16 / EPS;                   // 16-byte slots per 16 columns
+#pragma unroll
+            for (int t = 0; t < SPQ; ++t) {
+                const int j = q * SPQ + t;
+                uint4 o;
+                if (ESZ == 4) {
+                    o = make_uint4(__float_as_uint(f[4 * t]), __float_as_uint(f[4 * t + 1]),
+                                   __float_as_uint(f[4 * t + 2]), __float_as_uint(f[4 * t + 3]));
+                } else {
+                    o.x = pack_bf16x2(f[8 * t + 0], f[8 * t + 1]);
+                    o.y = pack_bf16x2(f[8 * t + 2], f[8 * t + 3]);
+                    o.z = pack_bf16x2(f[8 * t + 4], f[8 * t + 5]);
+                    o.w = pack_bf16x2(f[8 * t + 6], f[8 * t + 7]);
+                }
+                *reinterpret_cast<uint4*>(stg + lane * RB + ((j ^ swz) << 4)) = o;
+            }
+        }
+        __syncwarp();
+        // row-wise store: lanes slot..slot+LPR-1 of a row write its whole segment
+        const int col = n0 + slot * EPS;
+        uint8_t* base = partial ? reinterpret_cast<uint8_t*>(p.ws) + ((size_t)split * g.M * GK) * 4
+                                : reinterpret_cast<uint8_t*>(p.y);
+#pragma unroll
+        for (int i = 0; i < LPR; ++i) {
+            const int rr = lane / LPR + RPI * i;           // row within the warp's 32
+            const uint4 o = *reinterpret_cast<const uint4*>(stg + rr * RB + ((slot ^ ((rr >> SH) & (LPR - 1))) << 4));
+            if (roff[i] >= 0 && col < g.K)
+                *reinterpret_cast<uint4*>(base + (size_t)(roff[i] + (long long)gi * g.K + col) * ESZ) = o;
+        }
+        __syncwarp();                                       // staging is rewritten by the next chunk
+    }
+}
+
+}  // namespace
+}  // namespace convfwd

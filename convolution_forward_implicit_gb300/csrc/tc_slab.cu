@@ -1,0 +1,353 @@
+// Slab mode of the tensor-core implicit GEMM, for convolutions with stride 1: one TMA box
+// per (output tile, input plane, channel block) brings the input rows the whole tile needs
+// (the tile's rows plus the filter's reach), and every tap of that plane reads the box as a
+// row-shifted window through the MMA's shared-memory descriptor.  The same input bytes serve
+// Y*X taps, where the per-tap mode copies them once per tap.
+//
+// Layout.  An output tile is BH rows x BW columns of one output plane.  The slab holds
+// HR = BH + dh*(Y-1) input rows of BWs = BW + dw*(X-1) pixels each, starting at input column
+// ow0 - pw, each pixel one 128-byte row of channels (64 bf16 or 32 fp32), 128-byte swizzled
+// by the TMA.  Accumulator row r stands for output pixel (oh0 + r / BWs, ow0 + r % BWs): with
+// the slab's row pitch BWs, tap (y, x) is the 128-row window starting at slab row
+// y*dh*BWs + x*dw.  Rows whose column r % BWs lands past BW are computed and discarded.
+// Windows start at arbitrary 128-byte rows.  The tensor core takes the swizzle phase of a
+// row from its absolute shared-memory address, as the TMA did when it wrote the row, so a
+// window's descriptor is the plain one at its start address, with the matrix base offset
+// field left 0 (measured: setting it to the start's phase corrupts every window that is
+// not 1024-byte aligned).
+//
+// Roles (warps): 0-7 epilogue (as in the per-tap kernel), 8 slab copies, 9-11 weight copies
+// (X taps' weight tiles in one bulk copy; ring stage s owned by warp 9 + s % 3), 12 MMA
+// issue, 13-16 (3xTF32 only) the hi/lo split of each slab.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace convfwd {
+namespace {
+
+constexpr int SLAB_MAX_SA = 4;
+constexpr int SLAB_MAX_SB = 8;
+
+template <bool TF32>
+struct SlabRoles {
+    static constexpr int A_WARP = EPI_WARPS;
+    static constexpr int B_WARP0 = EPI_WARPS + 1;
+    static constexpr int B_WARPS = 3;
+    static constexpr int MMA_WARP = EPI_WARPS + 4;
+    static constexpr int CVT_WARP0 = MMA_WARP + 1;
+    static constexpr int CVT_WARPS = TF32 ? 4 : 0;
+    static constexpr int THREADS = (CVT_WARP0 + CVT_WARPS) * 32;
+};
+
+template <int BN, bool TF32>
+__global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
+    conv_fwd_slab_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map) {
+    using R = SlabRoles<TF32>;
+    constexpr uint32_t B_TILE = BN * 128;
+    constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+    const int SA = p.slab_sa, SB = p.slab_sb;
+    const uint32_t a_stage = (uint32_t)p.slab_a_stage;           // TF32: hi half, then lo half
+    const uint32_t a_half = TF32 ? a_stage / 2 : a_stage;
+    const uint32_t b_tap = TF32 ? 2 * B_TILE : B_TILE;            // one tap's weights (TF32: hi, lo)
+    const uint32_t b_stage = (uint32_t)p.slab_btaps * b_tap;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (sbase - raw);
+    const uint32_t sA = sbase;
+    const uint32_t sB = sA + SA * a_stage;
+    const uint32_t stg_off = SA * a_stage + SB * b_stage;
+    const uint32_t bar0 = sbase + stg_off + EPI_WARPS * STG_WARP_BYTES;
+    auto full_a = [&](int s) { return bar0 + 8u * s; };
+    auto empty_a = [&](int s) { return bar0 + 8u * (SLAB_MAX_SA + s); };
+    auto cvt_a = [&](int s) { return bar0 + 8u * (2 * SLAB_MAX_SA + s); };
+    auto full_b = [&](int s) { return bar0 + 8u * (3 * SLAB_MAX_SA + s); };
+    auto empty_b = [&](int s) { return bar0 + 8u * (3 * SLAB_MAX_SA + SLAB_MAX_SB + s); };
+    const uint32_t bar_t = bar0 + 8u * (3 * SLAB_MAX_SA + 2 * SLAB_MAX_SB);
+    auto tfull_bar = [&](int a) { return bar_t + 8u * a; };
+    auto tempty_bar = [&](int a) { return bar_t + 8u * (2 + a); };
+    const uint32_t drain_bar = bar_t + 8u * 4;
+    uint8_t* misc = smem + (drain_bar + 8u - sbase);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(full_a(s), 1);
+            mbar_init(empty_a(s), 1);
+            mbar_init(cvt_a(s), R::CVT_WARPS > 0 ? R::CVT_WARPS : 1);
+        }
+        for (int s = 0; s < SB; ++s) {
+            mbar_init(full_b(s), 1);
+            mbar_init(empty_b(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+    if (warp == R::A_WARP && lane == 0)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&act_map)) : "memory");
+    if (warp == R::MMA_WARP) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const Geom& g = p.g;
+    const int cblk = TF32 ? 32 : 64;
+    const int nbg = p.slab_nbg;          // weight stages per k-group (filter rows)
+    const int btaps = p.slab_btaps;      // taps per weight stage (filter columns)
+
+    if (warp == R::A_WARP) {
+        // ------------------------------------------------------------ slab copies
+        if (lane == 0) {
+            const uint32_t a_tx = (uint32_t)(p.slab_hr * p.slab_bws) * 128u;
+            uint32_t ia = 0;
+            bool aborted = false;
+            for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
+                int mt, gi, nt, split;
+                decode_unit(p, u, mt, gi, nt, split);
+                const TileOrigin to = tile_origin(p, mt);
+                const int w0 = to.ow0 - g.pw, h0 = to.oh0 - g.ph;
+                for (int kg = 0; kg < p.slab_nkg; ++kg, ++ia) {
+                    const int zz = kg / p.cbt, cb = kg - zz * p.cbt;
+                    const int s = ia % SA;
+                    const uint32_t ph = (ia / SA) & 1u;
+                    if (!wait_bar(empty_a(s), ph ^ 1u, abort_flag, p.err, p.sleep_mask & 1)) { aborted = true; break; }
+                    mbar_arrive_expect_tx(full_a(s), a_tx);
+                    if (p.map_kind == 0)
+                        tma_load_5d(sA + s * a_stage, &act_map, gi * g.C + cb * cblk, w0, h0,
+                                    to.od - g.pd + zz * g.dd, to.n, full_a(s));
+                    else
+                        tma_load_5d(sA + s * a_stage, &act_map, cb * cblk, gi, w0, h0, to.n, full_a(s));
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp >= R::B_WARP0 && warp < R::B_WARP0 + R::B_WARPS) {
+        // ------------------------------------------------------------ weight copies
+        if (lane == 0) {
+            const uint8_t* wp = reinterpret_cast<const uint8_t*>(p.wpack);
+            const int bw = warp - R::B_WARP0;
+            uint32_t ib = 0;
+            bool aborted = false;
+            for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
+                int mt, gi, nt, split;
+                decode_unit(p, u, mt, gi, nt, split);
+                for (int kg = 0; kg < p.slab_nkg && !aborted; ++kg) {
+                    for (int bg = 0; bg < nbg; ++bg, ++ib) {
+                        const int s = ib % SB;
+                        if (s % R::B_WARPS != bw) continue;    // each ring stage has one owner warp
+                        const uint32_t ph = (ib / SB) & 1u;
+                        if (!wait_bar(empty_b(s), ph ^ 1u, abort_flag, p.err, p.sleep_mask & 1)) {
+                            aborted = true;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(full_b(s), b_stage);
+                        const int kb = (kg * nbg + bg) * btaps;    // weights are packed in slab order
+                        const size_t off = ((size_t)(gi * p.num_nt + nt) * p.nkb + kb) * b_tap;
+                        bulk_g2s(sB + s * b_stage, wp + off, b_stage, full_b(s));
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == R::MMA_WARP) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_f32acc(BM, BN, TF32 ? 2u : 1u);
+            uint32_t ia = 0, ib = 0, tile_i = 0;
+            bool aborted = false;
+            for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x, ++tile_i) {
+                const int acc = tile_i & 1;
+                const uint32_t aph = (tile_i >> 1) & 1u;
+                if (!wait_bar(tempty_bar(acc), aph ^ 1u, abort_flag, p.err, (p.sleep_mask & 4) != 0)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                uint32_t first = 1;
+                for (int kg = 0; kg < p.slab_nkg && !aborted; ++kg, ++ia) {
+                    const int sa = ia % SA;
+                    const uint32_t pha = (ia / SA) & 1u;
+                    if (!wait_bar(TF32 ? cvt_a(sa) : full_a(sa), pha, abort_flag, p.err, (p.sleep_mask & 4) != 0)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + sa * a_stage;
+                    for (int bg = 0; bg < nbg; ++bg, ++ib) {
+                        const int sb = ib % SB;
+                        const uint32_t phb = (ib / SB) & 1u;
+                        if (!wait_bar(full_b(sb), phb, abort_flag, p.err, (p.sleep_mask & 4) != 0)) {
+                            aborted = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        for (int t = 0; t < btaps; ++t) {
+                            const uint32_t row = (uint32_t)(bg * g.dh * p.slab_bws + t * g.dw);
+                            const uint32_t a_addr = a0 + row * 128u;
+                            const uint64_t ad = sw128_desc(a_addr);
+                            const uint64_t bd = sw128_desc(sB + sb * b_stage + t * b_tap);
+                            if (TF32) {
+                                const uint64_t alo = sw128_desc(a_addr + a_half);
+                                const uint64_t blo = bd + (B_TILE >> 4);
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    mma_tf32(d_tmem, alo + 2u * k, bd + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
+                                    mma_tf32(d_tmem, ad + 2u * k, blo + 2u * k, IDESC, 1u);
+                                    mma_tf32(d_tmem, ad + 2u * k, bd + 2u * k, IDESC, 1u);
+                                }
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    mma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
+                            }
+                            first = 0;
+                        }
+                        mma_commit(empty_b(sb));
+                    }
+                    mma_commit(empty_a(sa));
+                }
+                if (!aborted) mma_commit(tfull_bar(acc));
+            }
+            if (aborted) {
+                mma_commit(drain_bar);
+                const unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
+            }
+        }
+        __syncwarp();
+    } else if (TF32 && warp >= R::CVT_WARP0) {
+        // ------------------------------------------------------------ hi/lo split (3xTF32)
+        // Every fp32 x of the slab becomes hi = x with its low 13 mantissa bits cleared (exact
+        // in TF32) and lo = x - hi (exact in fp32); the MMA sums lo*w_hi + hi*w_lo + hi*w_hi.
+        const int ct = threadIdx.x - R::CVT_WARP0 * 32;
+        const int n16 = p.slab_hr * p.slab_bws * 8;
+        uint32_t ia = 0;
+        bool aborted = false;
+        for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
+            for (int kg = 0; kg < p.slab_nkg; ++kg, ++ia) {
+                const int s = ia % SA;
+                const uint32_t ph = (ia / SA) & 1u;
+                if (!wait_bar_warp(full_a(s), ph, abort_flag, p.err)) { aborted = true; break; }
+                uint4* hi = reinterpret_cast<uint4*>(smem + s * a_stage);
+                uint4* lo = reinterpret_cast<uint4*>(smem + s * a_stage + a_half);
+                for (int i = ct; i < n16; i += R::CVT_WARPS * 32) {
+                    const uint4 v = hi[i];
+                    uint4 h, l;
+                    h.x = v.x & 0xFFFFE000u; h.y = v.y & 0xFFFFE000u; h.z = v.z & 0xFFFFE000u; h.w = v.w & 0xFFFFE000u;
+                    l.x = __float_as_uint(__uint_as_float(v.x) - __uint_as_float(h.x));
+                    l.y = __float_as_uint(__uint_as_float(v.y) - __uint_as_float(h.y));
+                    l.z = __float_as_uint(__uint_as_float(v.z) - __uint_as_float(h.z));
+                    l.w = __float_as_uint(__uint_as_float(v.w) - __uint_as_float(h.w));
+                    hi[i] = h;
+                    lo[i] = l;
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cvt_a(s));
+            }
+        }
+    } else if (warp < EPI_WARPS) {
+        // ------------------------------------------------------------ epilogue
+        const int wq = warp & 3;
+        constexpr int COLS = BN / 2 < 16 ? 16 : BN / 2;
+        const int cb_begin = (warp >> 2) * COLS;
+        const int cb_end = cb_begin + COLS < BN ? cb_begin + COLS : BN;
+        const bool add_bias = p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU;
+        const bool do_gelu = p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU;
+        uint8_t* stg = smem + stg_off + warp * STG_WARP_BYTES;
+        uint32_t tile_i = 0;
+        for (int u = blockIdx.x; u < p.total_units; u += gridDim.x, ++tile_i) {
+            int mt, gi, nt, split;
+            decode_unit(p, u, mt, gi, nt, split);
+            const int acc = tile_i & 1;
+            const uint32_t aph = (tile_i >> 1) & 1u;
+            if (!wait_bar_warp(tfull_bar(acc), aph, abort_flag, p.err, (p.sleep_mask & 2) != 0)) break;
+            tc_fence_after();
+            const TileOrigin to = tile_origin(p, mt);
+            // output pixel of accumulator row rr (row pitch BWs), or -1 if it is not stored
+            auto row_offset = [&](int rr) -> long long {
+                const int rh = rr / p.slab_bws, rw = rr - rh * p.slab_bws;
+                const int oh = to.oh0 + rh, ow = to.ow0 + rw;
+                if (rh >= p.BH || rw >= p.BW || oh >= g.Ho || ow >= g.Wo) return -1;
+                return (long long)(((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow) * (g.G * g.K);
+            };
+            const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
+            if (TF32)
+                epilogue_chunks<BN, 4>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, 0, false, add_bias, do_gelu, stg,
+                                       row_offset);
+            else
+                epilogue_chunks<BN, 2>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, 0, false, add_bias, do_gelu, stg,
+                                       row_offset);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == R::MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+template <int BN, bool TF32>
+cudaError_t launch_slab_one(const TcParams& p, const CUtensorMap& map, int grid, size_t smem, cudaStream_t stream) {
+    auto kern = conv_fwd_slab_kernel<BN, TF32>;
+    static bool attr_set[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SLAB_SMEM_MAX);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    kern<<<grid, SlabRoles<TF32>::THREADS, smem, stream>>>(p, map);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t slab_smem_bytes(int BN, int tf32, int sa, int sb, size_t a_stage, int btaps) {
+    const size_t b_stage = (size_t)btaps * BN * 128 * (tf32 ? 2 : 1);
+    return 1024 + (size_t)sa * a_stage + (size_t)sb * b_stage + (size_t)EPI_WARPS * STG_WARP_BYTES +
+           8 * (3 * SLAB_MAX_SA + 2 * SLAB_MAX_SB + 5) + 16;
+}
+
+cudaError_t launch_slab(const TcParams& p, const CUtensorMap* act_map, int grid, size_t smem, cudaStream_t stream) {
+    if (!act_map || p.slab_sa < 2 || p.slab_sa > SLAB_MAX_SA || p.slab_sb < 2 || p.slab_sb > SLAB_MAX_SB ||
+        smem > SLAB_SMEM_MAX)
+        return cudaErrorInvalidValue;
+#define X(bn)                                                                                    \
+    if (p.BN == bn)                                                                              \
+        return p.tf32 ? launch_slab_one<bn, true>(p, *act_map, grid, smem, stream)               \
+                      : launch_slab_one<bn, false>(p, *act_map, grid, smem, stream);
+    X(16) X(32) X(64) X(128) X(256)
+#undef X
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace convfwd

@@ -365,3 +365,47 @@ def test_packed_small_groups_match_oracle_and_unpacked(name, layer):
     refi, _ = oracle_full(li, "bf16", xi, wi, bi)
     ai, _ = run_gpu(li, "bf16", xi, wi, bi)
     assert np.array_equal(ai.reshape(-1), syn.f32_to_bf16_bits(refi.astype(np.float32))), da
+
+
+SLAB = [
+    ("2d_d1", "bf16", L(2, 2, 2, 64, 64, (14, 14), (3, 3), (1, 1), (1, 1), (1, 1), CONV_EPI_BIAS)),
+    ("2d_d2_nopad", "bf16", L(2, 1, 2, 64, 48, (19, 17), (3, 3), (1, 1), (0, 0), (2, 2))),
+    ("2d_wide_w", "bf16", L(2, 1, 1, 64, 64, (5, 300), (3, 3), (1, 1), (1, 1), (1, 1), CONV_EPI_NONE)),
+    ("2d_5x3_c128", "bf16", L(2, 1, 1, 128, 96, (11, 23), (5, 3), (1, 1), (2, 1), (1, 1))),
+    ("3d_d1", "bf16", L(3, 1, 2, 64, 64, (5, 9, 10), (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), CONV_EPI_BIAS)),
+    ("3d_d2", "bf16", L(3, 1, 1, 64, 32, (6, 11, 13), (3, 3, 3), (1, 1, 1), (1, 1, 1), (2, 2, 2), CONV_EPI_BIAS)),
+    ("1d_k3_c80", "bf16", L(1, 2, 1, 80, 136, (517,), (3,), (1,), (1,), (1,))),
+    ("1d_k5_d2", "bf16", L(1, 1, 1, 64, 64, (300,), (5,), (1,), (4,), (2,))),
+    ("1d_k3_d8_aligned_windows", "bf16", L(1, 1, 1, 64, 64, (400,), (3,), (1,), (8,), (8,), CONV_EPI_NONE)),
+    ("2d_aligned_windows", "bf16", L(2, 1, 1, 64, 64, (6, 16), (3, 3), (1, 1), (1, 8), (1, 8), CONV_EPI_NONE)),
+    ("2d_map1_g2_c72", "bf16", L(2, 2, 2, 72, 40, (13, 21), (3, 3), (1, 1), (1, 1), (1, 1))),
+    ("packed_g32_c8", "bf16", L(2, 1, 32, 8, 8, (13, 15), (3, 3), (1, 1), (1, 1), (2, 2), CONV_EPI_NONE)),
+    ("1d_tf32_c80", "f32", L(1, 1, 1, 80, 384, (300,), (3,), (1,), (1,), (1,))),
+    ("2d_tf32_g2_c32", "f32", L(2, 1, 2, 32, 36, (17, 19), (3, 3), (1, 1), (2, 2), (2, 2), CONV_EPI_BIAS)),
+    ("3d_tf32_c64", "f32", L(3, 1, 1, 64, 40, (4, 7, 9), (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), CONV_EPI_BIAS)),
+]
+
+
+@pytest.mark.parametrize("name,dtype,layer", SLAB, ids=[s[0] for s in SLAB])
+def test_slab_mode_matches_oracle_and_per_tap(name, dtype, layer):
+    """Stride-1 problems take the slab gather (one box per tile and input plane, taps as
+    shifted windows); the same problem with per-tap boxes must meet the same bound."""
+    x, w, b = make_inputs(layer, dtype, 1500 + zlib.crc32(name.encode()) % 500)
+    ref, S = oracle_full(layer, dtype, x, w, b)
+    # small problems would split K (which slab mode does not do): keep whole reductions
+    a, da = run_gpu(layer, dtype, x, w, b, env={"CONV_FORCE_SPLITK": 1}, guard=64)
+    c, dc = run_gpu(layer, dtype, x, w, b, env={"CONV_FORCE_GATHER": "tma"})
+    assert "gather=tma-slab" in da and "gather=tma " in dc + " ", (da, dc)
+    assert_within(dtype, layer.epilogue, a, ref, S, da)
+    assert_within(dtype, layer.epilogue, c, ref, S, dc)
+
+
+@pytest.mark.parametrize("bn", [32, 64, 128])
+def test_slab_mode_every_tile_width(bn):
+    layer = L(2, 1, 1, 64, 200, (9, 37), (3, 3), (1, 1), (1, 1), (1, 1))
+    x, w, b = make_inputs(layer, "bf16", 1700 + bn)
+    got, desc = run_gpu(layer, "bf16", x, w, b, env={"CONV_FORCE_BN": bn, "CONV_FORCE_SPLITK": 1},
+                        guard=64)
+    assert f"tile=128x{bn}" in desc and "tma-slab" in desc, desc
+    ref, S = oracle_full(layer, "bf16", x, w, b)
+    assert_within("bf16", layer.epilogue, got, ref, S, desc)
