@@ -210,7 +210,7 @@ struct conv_plan {
     int BN, stages, num_mt, num_nt, nkb, nchunks, cpt, splits, kbps, total_units, grid;
     int tma, map_kind, BW, BH, tiles_w, tiles_h, cbt, tf32, sleep_mask;
     int pack, Go, Co, Ko;   // small-group packing factor and the caller's G, C, K
-    int slab, slab_bws, slab_hr, slab_nkg, slab_nbg, slab_btaps, slab_sa, slab_sb, slab_a_stage;
+    int slab, slab_bws, slab_hr, slab_nkg, slab_nbg, slab_btaps, slab_sa, slab_sb, slab_a_stage, slab_resident;
     size_t slab_smem;
     // SIMT plan
     int BM, Kg, Kpad, nkt, ktps, vec;
@@ -443,20 +443,31 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     const int force = env_int("CONV_FORCE_SPLITK", 0);
     if (force >= 1) splits = std::min(force, p->nkb);
     if (p->slab) {
-        // slab mode runs whole reductions per tile and needs its rings to fit
+        // slab mode runs whole reductions per tile and needs its rings to fit: the weights of
+        // one (group, N tile) resident with a 3- or 2-stage slab ring where they fit, else a
+        // ring of weight stages
+        p->slab_nkg = g.Z * p->cbt;
+        const int nchunk = p->slab_nkg * p->slab_nbg;
         p->slab_sa = 2;
         p->slab_sb = 0;
-        for (int sb = 8; sb >= 2; --sb)
+        p->slab_resident = 0;
+        for (int sa = 3; sa >= 2 && !p->slab_resident; --sa)
+            if (env_int("CONV_FORCE_SLAB_STREAM", 0) == 0 &&
+                slab_smem_bytes(bn, p->tf32, sa, nchunk, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
+                p->slab_resident = 1;
+                p->slab_sa = sa;
+                p->slab_sb = nchunk;
+            }
+        for (int sb = 8; sb >= 2 && !p->slab_resident; --sb)
             if (slab_smem_bytes(bn, p->tf32, 2, sb, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
                 p->slab_sb = sb;
                 break;
             }
-        if (splits > 1 || p->slab_sb < 2) {
+        if (splits > 1 || (!p->slab_resident && p->slab_sb < 2)) {
             p->slab = 0;                               // back to per-tap boxes
             choose_tile_shape(p);
             return plan_tc_per_tap_retry(p, tf32);
         }
-        p->slab_nkg = g.Z * p->cbt;
         p->slab_smem = slab_smem_bytes(bn, p->tf32, p->slab_sa, p->slab_sb, (size_t)p->slab_a_stage, p->slab_btaps);
     }
     p->kbps = (int)cdiv(p->nkb, splits);
@@ -467,10 +478,11 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     p->workspace_bytes = p->splits > 1 ? (size_t)p->splits * g.M * g.G * g.K * sizeof(float) : 0;
     if (p->slab)
         snprintf(p->desc, sizeof(p->desc),
-                 "variant=%s gather=tma-slab tile=128x%d pixels=%dx%d slab=%dx%d k_block=%d stages=%d+%d splits=1 "
+                 "variant=%s gather=tma-slab tile=128x%d pixels=%dx%d slab=%dx%d k_block=%d stages=%d+%d%s splits=1 "
                  "units=%d grid=%d k_blocks=%d map=%d",
                  tf32 ? "tc_tf32x3" : "tc_bf16", bn, p->BH, p->BW, p->slab_hr, p->slab_bws, cblk, p->slab_sa,
-                 p->slab_sb, p->total_units, p->grid, p->nkb, p->map_kind);
+                 p->slab_resident ? 1 : p->slab_sb, p->slab_resident ? "w" : "", p->total_units, p->grid, p->nkb,
+                 p->map_kind);
     else if (p->tma)
         snprintf(p->desc, sizeof(p->desc),
                  "variant=%s gather=tma tile=128x%d pixels=%dx%d k_block=%d stages=%d splits=%d units=%d "
@@ -704,7 +716,7 @@ conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, cons
         tp.sleep_mask = plan->sleep_mask;
         tp.slab = plan->slab; tp.slab_bws = plan->slab_bws; tp.slab_hr = plan->slab_hr; tp.slab_nkg = plan->slab_nkg;
         tp.slab_nbg = plan->slab_nbg; tp.slab_btaps = plan->slab_btaps; tp.slab_sa = plan->slab_sa;
-        tp.slab_sb = plan->slab_sb; tp.slab_a_stage = plan->slab_a_stage;
+        tp.slab_sb = plan->slab_sb; tp.slab_a_stage = plan->slab_a_stage; tp.slab_resident = plan->slab_resident;
         CUtensorMap map;
         if (plan->tma && !encode_act_map(plan, x, &map)) return CONV_ERR_CUDA;
         e = plan->slab ? launch_slab(tp, &map, plan->grid, plan->slab_smem, s)
@@ -829,7 +841,7 @@ extern "C" conv_status conv_fwd_static_scratch(conv_plan_t plan, const void* x, 
         tp.sleep_mask = plan->sleep_mask;
         tp.slab = plan->slab; tp.slab_bws = plan->slab_bws; tp.slab_hr = plan->slab_hr; tp.slab_nkg = plan->slab_nkg;
         tp.slab_nbg = plan->slab_nbg; tp.slab_btaps = plan->slab_btaps; tp.slab_sa = plan->slab_sa;
-        tp.slab_sb = plan->slab_sb; tp.slab_a_stage = plan->slab_a_stage;
+        tp.slab_sb = plan->slab_sb; tp.slab_a_stage = plan->slab_a_stage; tp.slab_resident = plan->slab_resident;
         CUtensorMap map;
         if (plan->tma && !encode_act_map(plan, x, &map)) return CONV_ERR_CUDA;
         e = plan->slab ? launch_slab(tp, &map, plan->grid, plan->slab_smem, s)

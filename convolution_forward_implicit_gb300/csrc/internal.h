@@ -57,7 +57,8 @@ struct TcParams {
     int slab_nkg;           // k-groups per tile: Z * cbt (input plane, channel block)
     int slab_nbg;           // weight ring stages per k-group (filter rows Y)
     int slab_btaps;         // taps per weight stage (filter columns X)
-    int slab_sa, slab_sb;   // slab ring and weight ring stages
+    int slab_sa, slab_sb;   // slab ring and weight ring stages (resident: weight chunks held)
+    int slab_resident;      // 1: the weights of one (group, N tile) stay in shared memory
     int slab_a_stage;       // bytes per slab stage (3xTF32: hi half then lo half)
 };
 

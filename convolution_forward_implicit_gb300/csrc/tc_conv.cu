@@ -356,8 +356,6 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
             decode_unit(p, u, mt, gi, nt, split);
             const int acc = tile_i & 1;
             const uint32_t aph = (tile_i >> 1) & 1u;
-            if (!wait_bar_warp(tfull_bar(acc), aph, abort_flag, p.err, (p.sleep_mask & 2) != 0)) break;
-            tc_fence_after();
             TileOrigin to{0, 0, 0, 0};
             if (T::TMA) to = tile_origin(p, mt);
             // element offset of accumulator row rr's pixel, or -1 if the row is outside the output
@@ -373,13 +371,19 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
                 }
                 return (long long)m * GK;
             };
+            const bool wide = partial || T::TF32;     // fp32 stores
+            long long roff[EPI_MAX_LPR];
+            if (wide) epilogue_rows<BN, 4>(lane, wq, row_offset, roff);
+            else epilogue_rows<BN, 2>(lane, wq, row_offset, roff);
+            if (!wait_bar_warp(tfull_bar(acc), aph, abort_flag, p.err, (p.sleep_mask & 2) != 0)) break;
+            tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
-            if (partial || T::TF32)
+            if (wide)
                 epilogue_chunks<BN, 4>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
-                                       do_gelu, stg, row_offset);
+                                       do_gelu, stg, roff);
             else
                 epilogue_chunks<BN, 2>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
-                                       do_gelu, stg, row_offset);
+                                       do_gelu, stg, roff);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));

@@ -84,9 +84,14 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
             mbar_init(empty_a(s), 1);
             mbar_init(cvt_a(s), R::CVT_WARPS > 0 ? R::CVT_WARPS : 1);
         }
-        for (int s = 0; s < SB; ++s) {
-            mbar_init(full_b(s), 1);
-            mbar_init(empty_b(s), 1);
+        if (p.slab_resident) {
+            mbar_init(full_b(0), R::B_WARPS);
+            mbar_init(empty_b(0), 1);
+        } else {
+            for (int s = 0; s < SB; ++s) {
+                mbar_init(full_b(s), 1);
+                mbar_init(empty_b(s), 1);
+            }
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
@@ -144,13 +149,37 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
         if (lane == 0) {
             const uint8_t* wp = reinterpret_cast<const uint8_t*>(p.wpack);
             const int bw = warp - R::B_WARP0;
-            uint32_t ib = 0;
+            const int nchunk = p.slab_nkg * nbg;    // chunks of btaps taps, in slab order
             bool aborted = false;
-            for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
-                int mt, gi, nt, split;
-                decode_unit(p, u, mt, gi, nt, split);
-                for (int kg = 0; kg < p.slab_nkg && !aborted; ++kg) {
-                    for (int bg = 0; bg < nbg; ++bg, ++ib) {
+            if (p.slab_resident) {
+                // The whole weight set of the current (group, N tile) stays in shared memory;
+                // it is reloaded only when the next unit changes group or N tile.  Each copy
+                // warp brings every third chunk; all three arrive on the one full barrier.
+                int prev = -1;
+                uint32_t j = 0;
+                for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
+                    int mt, gi, nt, split;
+                    decode_unit(p, u, mt, gi, nt, split);
+                    const int key = gi * p.num_nt + nt;
+                    if (key == prev) continue;
+                    prev = key;
+                    if (!wait_bar(empty_b(0), (j & 1u) ^ 1u, abort_flag, p.err, p.sleep_mask & 1)) {
+                        aborted = true;
+                        break;
+                    }
+                    const int mine = nchunk > bw ? (nchunk - bw + R::B_WARPS - 1) / R::B_WARPS : 0;
+                    mbar_arrive_expect_tx(full_b(0), (uint32_t)mine * b_stage);
+                    const size_t base = (size_t)key * p.nkb * b_tap;
+                    for (int c = bw; c < nchunk; c += R::B_WARPS)
+                        bulk_g2s(sB + c * b_stage, wp + base + (size_t)c * b_stage, b_stage, full_b(0));
+                    ++j;
+                }
+            } else {
+                uint32_t ib = 0;
+                for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
+                    int mt, gi, nt, split;
+                    decode_unit(p, u, mt, gi, nt, split);
+                    for (int c = 0; c < nchunk; ++c, ++ib) {
                         const int s = ib % SB;
                         if (s % R::B_WARPS != bw) continue;    // each ring stage has one owner warp
                         const uint32_t ph = (ib / SB) & 1u;
@@ -159,8 +188,8 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(full_b(s), b_stage);
-                        const int kb = (kg * nbg + bg) * btaps;    // weights are packed in slab order
-                        const size_t off = ((size_t)(gi * p.num_nt + nt) * p.nkb + kb) * b_tap;
+                        // chunk c = kg*nbg + bg holds K blocks c*btaps .. c*btaps + btaps-1
+                        const size_t off = ((size_t)(gi * p.num_nt + nt) * p.nkb + (size_t)c * btaps) * b_tap;
                         bulk_g2s(sB + s * b_stage, wp + off, b_stage, full_b(s));
                     }
                 }
@@ -168,67 +197,102 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
         }
         __syncwarp();
     } else if (warp == R::MMA_WARP) {
-        // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
-            constexpr uint32_t IDESC = idesc_f32acc(BM, BN, TF32 ? 2u : 1u);
-            uint32_t ia = 0, ib = 0, tile_i = 0;
-            bool aborted = false;
-            for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x, ++tile_i) {
-                const int acc = tile_i & 1;
-                const uint32_t aph = (tile_i >> 1) & 1u;
-                if (!wait_bar(tempty_bar(acc), aph ^ 1u, abort_flag, p.err, (p.sleep_mask & 4) != 0)) {
+        // ------------------------------------------------------------ MMA issue (whole warp)
+        constexpr uint32_t IDESC = idesc_f32acc(BM, BN, TF32 ? 2u : 1u);
+        const bool msleep = (p.sleep_mask & 4) != 0;
+        const bool resident = p.slab_resident != 0;
+        uint32_t ia = 0, ib = 0, tile_i = 0, jw = 0;
+        int prev = -1;
+        bool aborted = false;
+        for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x, ++tile_i) {
+            const int acc = tile_i & 1;
+            const uint32_t aph = (tile_i >> 1) & 1u;
+            int key = 0, next_key = -1;
+            if (resident) {
+                int mt, gi, nt, split;
+                decode_unit(p, u, mt, gi, nt, split);
+                key = gi * p.num_nt + nt;
+                if (u + (int)gridDim.x < p.total_units) {
+                    decode_unit(p, u + gridDim.x, mt, gi, nt, split);
+                    next_key = gi * p.num_nt + nt;
+                }
+            }
+            if (!wait_bar_warp(tempty_bar(acc), aph ^ 1u, abort_flag, p.err, msleep)) {
+                aborted = true;
+                break;
+            }
+            if (resident) {
+                if (key != prev) {
+                    if (!wait_bar_warp(full_b(0), jw & 1u, abort_flag, p.err, msleep)) {
+                        aborted = true;
+                        break;
+                    }
+                    ++jw;
+                    prev = key;
+                }
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            uint32_t first = 1;
+            for (int kg = 0; kg < p.slab_nkg && !aborted; ++kg, ++ia) {
+                const int sa = ia % SA;
+                const uint32_t pha = (ia / SA) & 1u;
+                if (!wait_bar_warp(TF32 ? cvt_a(sa) : full_a(sa), pha, abort_flag, p.err, msleep)) {
                     aborted = true;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                uint32_t first = 1;
-                for (int kg = 0; kg < p.slab_nkg && !aborted; ++kg, ++ia) {
-                    const int sa = ia % SA;
-                    const uint32_t pha = (ia / SA) & 1u;
-                    if (!wait_bar(TF32 ? cvt_a(sa) : full_a(sa), pha, abort_flag, p.err, (p.sleep_mask & 4) != 0)) {
-                        aborted = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a0 = sA + sa * a_stage;
-                    for (int bg = 0; bg < nbg; ++bg, ++ib) {
-                        const int sb = ib % SB;
+                const uint32_t a0 = sA + sa * a_stage;
+                for (int bg = 0; bg < nbg; ++bg) {
+                    uint32_t b0;
+                    int sb = 0;
+                    if (resident) {
+                        b0 = sB + (uint32_t)(kg * nbg + bg) * b_stage;
+                    } else {
+                        sb = ib % SB;
                         const uint32_t phb = (ib / SB) & 1u;
-                        if (!wait_bar(full_b(sb), phb, abort_flag, p.err, (p.sleep_mask & 4) != 0)) {
+                        ++ib;
+                        if (!wait_bar_warp(full_b(sb), phb, abort_flag, p.err, msleep)) {
                             aborted = true;
                             break;
                         }
                         tc_fence_after();
-                        for (int t = 0; t < btaps; ++t) {
-                            const uint32_t row = (uint32_t)(bg * g.dh * p.slab_bws + t * g.dw);
-                            const uint32_t a_addr = a0 + row * 128u;
-                            const uint64_t ad = sw128_desc(a_addr);
-                            const uint64_t bd = sw128_desc(sB + sb * b_stage + t * b_tap);
-                            if (TF32) {
-                                const uint64_t alo = sw128_desc(a_addr + a_half);
-                                const uint64_t blo = bd + (B_TILE >> 4);
-#pragma unroll
-                                for (int k = 0; k < 4; ++k) {
-                                    mma_tf32(d_tmem, alo + 2u * k, bd + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
-                                    mma_tf32(d_tmem, ad + 2u * k, blo + 2u * k, IDESC, 1u);
-                                    mma_tf32(d_tmem, ad + 2u * k, bd + 2u * k, IDESC, 1u);
-                                }
-                            } else {
-#pragma unroll
-                                for (int k = 0; k < 4; ++k)
-                                    mma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
-                            }
-                            first = 0;
-                        }
-                        mma_commit(empty_b(sb));
+                        b0 = sB + sb * b_stage;
                     }
-                    mma_commit(empty_a(sa));
+                    for (int t = 0; t < btaps; ++t) {
+                        const uint32_t row = (uint32_t)(bg * g.dh * p.slab_bws + t * g.dw);
+                        const uint32_t a_addr = a0 + row * 128u;
+                        const uint64_t ad = sw128_desc(a_addr);
+                        const uint64_t bd = sw128_desc(b0 + t * b_tap);
+                        if (TF32) {
+                            const uint64_t alo = sw128_desc(a_addr + a_half);
+                            const uint64_t blo = bd + (B_TILE >> 4);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                mma_tf32_warp(d_tmem, alo + 2u * k, bd + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
+                                mma_tf32_warp(d_tmem, ad + 2u * k, blo + 2u * k, IDESC, 1u);
+                                mma_tf32_warp(d_tmem, ad + 2u * k, bd + 2u * k, IDESC, 1u);
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                mma_bf16_warp(d_tmem, ad + 2u * k, bd + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
+                        }
+                        first = 0;
+                    }
+                    if (!resident) mma_commit_warp(empty_b(sb));
                 }
-                if (!aborted) mma_commit(tfull_bar(acc));
+                mma_commit_warp(empty_a(sa));
             }
-            if (aborted) {
-                mma_commit(drain_bar);
+            if (aborted) break;
+            // the weight set is released after the last tile that uses it
+            if (resident && next_key != key) mma_commit_warp(empty_b(0));
+            mma_commit_warp(tfull_bar(acc));
+        }
+        if (aborted) {
+            // wait (bounded) until every MMA issued so far has completed
+            mma_commit_warp(drain_bar);
+            if (lane == 0) {
                 const unsigned long long t0 = globaltimer();
                 while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
             }
@@ -280,8 +344,6 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
             decode_unit(p, u, mt, gi, nt, split);
             const int acc = tile_i & 1;
             const uint32_t aph = (tile_i >> 1) & 1u;
-            if (!wait_bar_warp(tfull_bar(acc), aph, abort_flag, p.err, (p.sleep_mask & 2) != 0)) break;
-            tc_fence_after();
             const TileOrigin to = tile_origin(p, mt);
             // output pixel of accumulator row rr (row pitch BWs), or -1 if it is not stored
             auto row_offset = [&](int rr) -> long long {
@@ -290,13 +352,18 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
                 if (rh >= p.BH || rw >= p.BW || oh >= g.Ho || ow >= g.Wo) return -1;
                 return (long long)(((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow) * (g.G * g.K);
             };
+            long long roff[EPI_MAX_LPR];
+            if (TF32) epilogue_rows<BN, 4>(lane, wq, row_offset, roff);
+            else epilogue_rows<BN, 2>(lane, wq, row_offset, roff);
+            if (!wait_bar_warp(tfull_bar(acc), aph, abort_flag, p.err, (p.sleep_mask & 2) != 0)) break;
+            tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
             if (TF32)
                 epilogue_chunks<BN, 4>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, 0, false, add_bias, do_gelu, stg,
-                                       row_offset);
+                                       roff);
             else
                 epilogue_chunks<BN, 2>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, 0, false, add_bias, do_gelu, stg,
-                                       row_offset);
+                                       roff);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -338,8 +405,8 @@ size_t slab_smem_bytes(int BN, int tf32, int sa, int sb, size_t a_stage, int bta
 }
 
 cudaError_t launch_slab(const TcParams& p, const CUtensorMap* act_map, int grid, size_t smem, cudaStream_t stream) {
-    if (!act_map || p.slab_sa < 2 || p.slab_sa > SLAB_MAX_SA || p.slab_sb < 2 || p.slab_sb > SLAB_MAX_SB ||
-        smem > SLAB_SMEM_MAX)
+    if (!act_map || p.slab_sa < 2 || p.slab_sa > SLAB_MAX_SA ||
+        (!p.slab_resident && (p.slab_sb < 2 || p.slab_sb > SLAB_MAX_SB)) || smem > SLAB_SMEM_MAX)
         return cudaErrorInvalidValue;
 #define X(bn)                                                                                    \
     if (p.BN == bn)                                                                              \

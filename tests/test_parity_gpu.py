@@ -379,6 +379,7 @@ SLAB = [
     ("1d_k3_d8_aligned_windows", "bf16", L(1, 1, 1, 64, 64, (400,), (3,), (1,), (8,), (8,), CONV_EPI_NONE)),
     ("2d_aligned_windows", "bf16", L(2, 1, 1, 64, 64, (6, 16), (3, 3), (1, 1), (1, 8), (1, 8), CONV_EPI_NONE)),
     ("2d_map1_g2_c72", "bf16", L(2, 2, 2, 72, 40, (13, 21), (3, 3), (1, 1), (1, 1), (1, 1))),
+    ("2d_weight_reload_g3", "bf16", L(2, 8, 3, 64, 64, (30, 60), (3, 3), (1, 1), (1, 1), (1, 1), CONV_EPI_BIAS)),
     ("packed_g32_c8", "bf16", L(2, 1, 32, 8, 8, (13, 15), (3, 3), (1, 1), (1, 1), (2, 2), CONV_EPI_NONE)),
     ("1d_tf32_c80", "f32", L(1, 1, 1, 80, 384, (300,), (3,), (1,), (1,), (1,))),
     ("2d_tf32_g2_c32", "f32", L(2, 1, 2, 32, 36, (17, 19), (3, 3), (1, 1), (2, 2), (2, 2), CONV_EPI_BIAS)),
@@ -409,3 +410,14 @@ def test_slab_mode_every_tile_width(bn):
     assert f"tile=128x{bn}" in desc and "tma-slab" in desc, desc
     ref, S = oracle_full(layer, "bf16", x, w, b)
     assert_within("bf16", layer.epilogue, got, ref, S, desc)
+
+
+@pytest.mark.parametrize("name", ["2d_d1", "3d_d2", "1d_tf32_c80", "2d_weight_reload_g3"])
+def test_slab_mode_streamed_weights(name):
+    """Slab mode with the weights streamed through a ring of stages instead of held resident."""
+    dtype, layer = next((d, l) for n, d, l in SLAB if n == name)
+    x, w, b = make_inputs(layer, dtype, 1800 + zlib.crc32(name.encode()) % 500)
+    got, desc = run_gpu(layer, dtype, x, w, b, env={"CONV_FORCE_SPLITK": 1, "CONV_FORCE_SLAB_STREAM": 1}, guard=64)
+    assert "tma-slab" in desc and "w " not in desc, desc
+    ref, S = oracle_full(layer, dtype, x, w, b)
+    assert_within(dtype, layer.epilogue, got, ref, S, desc)
