@@ -201,22 +201,20 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
         constexpr uint32_t IDESC = idesc_f32acc(BM, BN, TF32 ? 2u : 1u);
         const bool msleep = (p.sleep_mask & 4) != 0;
         const bool resident = p.slab_resident != 0;
+        // weight set of unit u: (group, N tile) = u mod KT (slab plans do not split K); from one
+        // unit of this CTA to its next the key advances by gridDim.x mod KT
+        const int KT = p.g.G * p.num_nt;
+        const int kstep = (int)(gridDim.x % (unsigned)KT);
+        int key = (int)(blockIdx.x % (unsigned)KT);
         uint32_t ia = 0, ib = 0, tile_i = 0, jw = 0;
         int prev = -1;
         bool aborted = false;
         for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x, ++tile_i) {
             const int acc = tile_i & 1;
             const uint32_t aph = (tile_i >> 1) & 1u;
-            int key = 0, next_key = -1;
-            if (resident) {
-                int mt, gi, nt, split;
-                decode_unit(p, u, mt, gi, nt, split);
-                key = gi * p.num_nt + nt;
-                if (u + (int)gridDim.x < p.total_units) {
-                    decode_unit(p, u + gridDim.x, mt, gi, nt, split);
-                    next_key = gi * p.num_nt + nt;
-                }
-            }
+            int next_key = key + kstep;
+            if (next_key >= KT) next_key -= KT;
+            if (u + (int)gridDim.x >= p.total_units) next_key = -1;
             if (!wait_bar_warp(tempty_bar(acc), aph ^ 1u, abort_flag, p.err, msleep)) {
                 aborted = true;
                 break;
@@ -288,6 +286,7 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
             // the weight set is released after the last tile that uses it
             if (resident && next_key != key) mma_commit_warp(empty_b(0));
             mma_commit_warp(tfull_bar(acc));
+            key = next_key;
         }
         if (aborted) {
             // wait (bounded) until every MMA issued so far has completed
