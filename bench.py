@@ -441,6 +441,49 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def _strip_comments(text):
+    """C/C++ source without its comments and blank lines (string literals kept as they are)."""
+    import re
+    pattern = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"', re.S)
+    text = pattern.sub(lambda m: m.group(0) if m.group(0).startswith('"') else "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
+def kernel_source_hash():
+    """First 16 hex digits of a SHA-256 over the kernel sources and the public header with
+    comments removed, so a DRAM traffic figure taken by ncu can be matched to the code it
+    was measured on (a change to comments alone keeps the hash)."""
+    import glob
+    import hashlib
+    files = []
+    for pat in ("convolution_forward_implicit_gb300/csrc/*.cu", "convolution_forward_implicit_gb300/csrc/*.cuh",
+                "convolution_forward_implicit_gb300/csrc/*.h", "include/*.h"):
+        files += glob.glob(os.path.join(ROOT, pat))
+    h = hashlib.sha256()
+    for f in sorted(files):
+        h.update(os.path.relpath(f, ROOT).encode())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_strip_comments(fh.read()).encode())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(desc):
+    """DRAM bytes per launch (read + write) of the kernel a plan runs, from the `traffic:` lines
+    of the committed ncu summaries, or None when none matches the plan and the current sources."""
+    cur = kernel_source_hash()
+    for f in sorted(os.listdir(os.path.join(ROOT, "profiles"))) if os.path.isdir(os.path.join(ROOT, "profiles")) else []:
+        if not f.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(ROOT, "profiles", f)) as fh:
+            for line in fh:
+                if not line.startswith("traffic: "):
+                    continue
+                parts = line[len("traffic: "):].strip().split(" ", 2)
+                if len(parts) == 3 and parts[0] == cur and parts[2] == desc:
+                    return int(parts[1])
+    return None
+
+
 def roofline_for(lr, ms):
     """Roofline of one layer's kernel: the slower of its compute pipe and HBM bytes."""
     peaks, src = measured_peaks()
@@ -467,11 +510,11 @@ def roofline_for(lr, ms):
     if flops / pipe >= byts / hbm:
         ach = flops / t_s / 1e12
         return {"bound": bound_c, "achieved": round(ach, 4), "peak": round(unit_peak, 2), "unit": "TFLOP/s",
-                "frac": round(ach / unit_peak, 4), "traffic": None, "kernel": lr.name(),
+                "frac": round(ach / unit_peak, 4), "traffic": measured_traffic(desc), "kernel": lr.name(),
                 "plan": desc, "peak_source": note, "algorithmic_flops": flops, "algorithmic_bytes": byts}
     ach = byts / t_s / 1e9
     return {"bound": "hbm", "achieved": round(ach, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None, "kernel": lr.name(), "plan": desc,
+            "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": measured_traffic(desc), "kernel": lr.name(), "plan": desc,
             "peak_source": f"HBM copy bandwidth, {src}", "algorithmic_flops": flops, "algorithmic_bytes": byts}
 
 
@@ -581,7 +624,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="whisper_frontend")
+    ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash and exit")
     args = ap.parse_args()
+    if args.source_hash:
+        print(kernel_source_hash())
+        return
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_setup()

@@ -12,17 +12,22 @@
 // conv2d path already solves this", is never materialised: each A tile is gathered
 // straight from the channels-last input, zero-filled where a tap falls in the padding.
 //
-// One persistent CTA per SM, 9 warps in three roles:
-//   warps 0-3  epilogue: tcgen05.ld the 128 x BN accumulator (warp w owns TMEM lanes
-//              32w..32w+31), add bias, GELU, round to bf16, 16-byte stores; or store
-//              fp32 partials when the reduction is split.
-//   warps 4-7  producer: per 64-wide K block, 8 cp.async (16 B, zero-fill) per thread
-//              gather the 128 x 128 B activation tile into the 128-byte-swizzled K-major
-//              layout; one thread bulk-copies the prepacked weight tile (already in
-//              swizzled order) with cp.async.bulk and an mbarrier transaction count.
-//   warp 8     MMA: one thread issues tcgen05.mma (M = 128, N = BN, K = 16) x 4 per
-//              K block and tcgen05.commit to free the stage; the accumulator is double
-//              buffered in TMEM so the epilogue of tile i overlaps the main loop of i+1.
+// One persistent CTA per SM (grid = min(units, SMs)), warp-specialised:
+//   warps 0-7   epilogue: two warps per TMEM lane quarter (warp w owns lanes 32(w%4)..+31
+//               and half of the columns); tcgen05.ld, bias, GELU, rounding, then stores
+//               through a per-warp staging buffer so each store instruction writes whole
+//               row segments (fp32 partial sums instead when the reduction is split).
+//   warps 8-11  producers, per K block (one tap x 64 bf16 or 32 fp32 channels):
+//               TMA gather: one 5-D tiled box of BH x BW output pixels (conv stride as the
+//               element stride, padding as out-of-bounds zero fill) plus one bulk copy of
+//               the prepacked weight tile, issued by the warp that owns the stage;
+//               cp.async gather: 16-byte zero-filling copies of 8-channel chunks packed
+//               densely across taps, for channel counts no box can serve.
+//   warp 12     MMA: one thread issues tcgen05.mma (M = 128, N = BN; 4 x K=16 bf16 or
+//               12 x K=8 tf32 per K block) and tcgen05.commit frees the stage; the
+//               accumulator is double-buffered in TMEM so the epilogue of tile i overlaps
+//               the main loop of tile i+1.
+//   warps 13-16 (3xTF32 only) split each activation tile into hi and lo parts in place.
 // Every mbarrier wait is bounded: after ~1 s it raises the device error word, sets a
 // CTA-wide abort flag and the CTA winds down (drains copies, waits for issued MMAs,
 // frees TMEM).
