@@ -8,13 +8,17 @@ Useful FLOPs = 2 x MACs, padded taps counted (the page's convention).
 
 Timing: W warm-up steps, then exactly K steps between CUDA events on the launching stream,
 bracketed by a barrier and a device synchronise.  A step is one CUDA graph holding every
-layer (each conv_fwd call: the conv kernel, plus the reduction for split plans), with
-timing events recorded inside the graph between the layers, which give each layer's
-device time (where PyTorch cannot record events inside a graph, each layer is its own
-graph and the events sit between them).  Steps rotate over enough copies of every input, packed weight and
-output that one rotation exceeds twice the L2 cache, so no step finds its data in L2.
+layer (each conv_fwd call: the conv kernel, plus the reduction for split plans); by
+default the plans chain their kernels as programmatic dependents (conv_plan_set_overlap),
+so each kernel's set-up and weight loads overlap the previous one (--no-overlap turns
+this off).  Each layer's device time comes from a second run of the same steps with timing
+events recorded inside the graph between the layers (where PyTorch cannot record events
+inside a graph, each layer is its own graph and the events sit between them).  Steps
+rotate over enough copies of every input, packed weight and output that one rotation
+exceeds twice the L2 cache, so no step finds its data in L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+                  [--no-overlap] [--source-hash]
 
 Under torchrun each rank runs an independent replica on its own GPU (the forward pass
 has no exchange step); rank 0 prints the JSON line with the max time over ranks.
@@ -243,16 +247,19 @@ def rotation_sets(wls):
     return max(4, int(np.ceil(2.2 * L2_BYTES / per_set))), per_set
 
 
-def capture_steps(runs, R):
-    """One CUDA graph per rotation set holding every layer of the step, with timing events
-    recorded between the layers inside the graph.  Returns (graphs, events) or None when
-    this PyTorch cannot record events inside a graph."""
+def capture_steps(runs, R, with_events):
+    """One CUDA graph per rotation set holding every layer of the step.  With with_events,
+    timing events are recorded between the layers inside the graph (they give each layer's
+    device time, and they also keep consecutive layers from overlapping); returns (graphs,
+    events), or None when this PyTorch cannot record events inside a graph."""
     import torch
-    try:
-        events = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(runs) + 1)]
-                  for _ in range(R)]
-    except TypeError:
-        return None
+    events = None
+    if with_events:
+        try:
+            events = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(runs) + 1)]
+                      for _ in range(R)]
+        except TypeError:
+            return None
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -266,10 +273,12 @@ def capture_steps(runs, R):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             cs = torch.cuda.current_stream()
-            events[r][0].record(cs)
+            if events:
+                events[r][0].record(cs)
             for j, lr in enumerate(runs):
                 lr.call(r)
-                events[r][j + 1].record(cs)
+                if events:
+                    events[r][j + 1].record(cs)
         graphs.append(g)
     return graphs, events
 
@@ -283,29 +292,30 @@ def run_ours(args, ws, rank, local):
     R, per_set = rotation_sets(wls)
     runs, inputs = setup_layers(wls, R)
     stream = torch.cuda.current_stream()
-    cap = capture_steps(runs, R)
+    if args.overlap:
+        for lr in runs:
+            lr.plan.set_overlap(True)
+    # timed steps: one graph per step with no events inside, so consecutive kernels may overlap
+    step_graphs, _ = capture_steps(runs, R, with_events=False)
+    # per-layer device times: the same steps with events between the layers
+    cap = capture_steps(runs, R, with_events=True)
     if cap is not None:
-        graphs, gev = cap
-        step_graphs = graphs
-        graph_mode = "one graph per step (all layers), timing events inside the graph"
+        layer_graphs, gev = cap
+        graph_mode = ("one graph per step (all layers" + (", chained as programmatic dependents" if args.overlap else "")
+                      + "); per-layer times from a second run of graphs with events between the layers")
     else:
         for lr in runs:
             lr.capture(R)
-        step_graphs = None
-        graph_mode = "one graph per layer, timing events between graphs"
+        layer_graphs, gev = None, None
+        graph_mode = "one graph per step; per-layer times from one graph per layer with events between graphs"
 
     K = args.steps
     nL = len(runs)
-    ev = None if step_graphs is not None else [[torch.cuda.Event(enable_timing=True) for _ in range(nL + 1)]
-                                               for _ in range(K)]
+    ev = None if layer_graphs is not None else [[torch.cuda.Event(enable_timing=True) for _ in range(nL + 1)]
+                                                for _ in range(K)]
 
     def step(i):
-        r = i % R
-        if step_graphs is not None:
-            step_graphs[r].replay()
-        else:
-            for lr in runs:
-                lr.graphs[r].replay()
+        step_graphs[i % R].replay()
 
     for i in range(args.warmup):
         step(i)
@@ -319,19 +329,27 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     e_start.record(stream)
     for i in range(K):
+        step(i)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    total_ms = e_start.elapsed_time(e_end)
+    # per-layer device times over the same number of steps (warm-up first)
+    for i in range(args.warmup):
+        if layer_graphs is not None:
+            layer_graphs[i % R].replay()
+    torch.cuda.synchronize()
+    for i in range(K):
         if ev is None:
-            step(i)
+            layer_graphs[i % R].replay()
         else:
             ev[i][0].record(stream)
             for j, lr in enumerate(runs):
                 lr.graphs[i % R].replay()
                 ev[i][j + 1].record(stream)
-    e_end.record(stream)
     torch.cuda.synchronize()
-    barrier(ws)
-    total_ms = e_start.elapsed_time(e_end)
     if ev is None:
-        # the last replay of every rotation set's graph inside the timed region
+        # the last replay of every rotation set's graph
         last = sorted({i % R: i for i in range(K)}.keys())
         per_layer_ms = [sum(gev[r][j].elapsed_time(gev[r][j + 1]) for r in last) / len(last) for j in range(nL)]
         layer_samples = len(last)
@@ -378,6 +396,7 @@ def run_ours(args, ws, rank, local):
                    "l2": f"inputs larger than L2: {R} rotating sets of activations, packed weights and outputs "
                          f"(~{R * per_set / 1e6:.0f} MB per rotation, L2 129 MB)",
                    "graphs": graph_mode,
+                   "overlap": bool(args.overlap),
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "plans": {lr.name(): lr.plan.describe() for lr in runs}},
         "roofline": roof,
@@ -625,6 +644,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="whisper_frontend")
     ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash and exit")
+    ap.add_argument("--no-overlap", dest="overlap", action="store_false",
+                    help="launch each layer only after the previous one completes (no programmatic dependents)")
     args = ap.parse_args()
     if args.source_hash:
         print(kernel_source_hash())

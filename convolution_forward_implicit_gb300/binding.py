@@ -22,7 +22,7 @@ __all__ = [
     "conv_plan_create", "conv_plan_output_shape", "conv_prepacked_weight_bytes", "conv_workspace_bytes",
     "conv_plan_set_workspace", "conv_prepack_weights", "conv_fwd", "conv_plan_check", "conv_plan_destroy",
     "conv_status_string", "conv_plan_describe", "conv_plan_flops", "ConvPlan", "EXPORTED",
-    "conv_fwd_static_scratch", "CONV_STATIC_SCRATCH_BYTES",
+    "conv_fwd_static_scratch", "CONV_STATIC_SCRATCH_BYTES", "conv_plan_set_overlap",
 ]
 
 CONV_OK, CONV_ERR_INVALID_ARG, CONV_ERR_UNSUPPORTED, CONV_ERR_ALIGNMENT = 0, 1, 2, 3
@@ -52,6 +52,7 @@ _SIGS = {
     "conv_plan_describe": (ctypes.c_char_p, [_VP]),
     "conv_plan_flops": (ctypes.c_double, [_VP]),
     "conv_fwd_static_scratch": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP]),
+    "conv_plan_set_overlap": (ctypes.c_int, [_VP, ctypes.c_int]),
 }
 CONV_STATIC_SCRATCH_BYTES = 16 << 20
 EXPORTED = tuple(_SIGS)
@@ -149,6 +150,12 @@ def conv_plan_destroy(plan: int):
     _check(load_library().conv_plan_destroy(plan), "conv_plan_destroy")
 
 
+def conv_plan_set_overlap(plan: int, enable: bool = True):
+    """Launch this plan's kernels as programmatic dependents of the previous kernel on the
+    stream (see include/conv.h): set-up and packed-weight loads overlap the previous layer."""
+    _check(load_library().conv_plan_set_overlap(plan, 1 if enable else 0), "conv_plan_set_overlap")
+
+
 def conv_plan_describe(plan: int) -> str:
     return load_library().conv_plan_describe(plan).decode()
 
@@ -219,6 +226,9 @@ class ConvPlan:
         conv_fwd(self.handle, x.data_ptr(), self.w_packed.data_ptr(), 0 if bias is None else bias.data_ptr(),
                  y.data_ptr(), s)
         return y
+
+    def set_overlap(self, enable: bool = True):
+        conv_plan_set_overlap(self.handle, enable)
 
     def check(self, stream=None):
         import torch

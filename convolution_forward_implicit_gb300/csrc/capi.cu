@@ -160,7 +160,11 @@ __device__ __forceinline__ void from_f(__nv_bfloat16& d, float v) { d = __float2
 
 template <typename T>
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, long long MGK, int GK,
-                                     const T* __restrict__ bias, T* __restrict__ y, int epi) {
+                                     const T* __restrict__ bias, T* __restrict__ y, int epi, int pdl) {
+    if (pdl) {   // the partial sums come from the conv kernel just before this one
+        griddep_launch();
+        griddep_wait();
+    }
     const bool add_bias = epi == EPI_BIAS || epi == EPI_BIAS_GELU;
     const bool do_gelu = epi == EPI_BIAS_GELU || epi == EPI_GELU;
     if ((GK & 3) == 0) {
@@ -211,6 +215,7 @@ struct conv_plan {
     int tma, map_kind, BW, BH, tiles_w, tiles_h, cbt, tf32, sleep_mask;
     int pack, Go, Co, Ko;   // small-group packing factor and the caller's G, C, K
     int slab, slab_bws, slab_hr, slab_nkg, slab_nbg, slab_btaps, slab_sa, slab_sb, slab_a_stage, slab_resident;
+    int overlap;            // launch as programmatic dependents (conv_plan_set_overlap)
     size_t slab_smem;
     // SIMT plan
     int BM, Kg, Kpad, nkt, ktps, vec;
@@ -671,42 +676,49 @@ conv_status conv_prepack_weights(conv_plan_t plan, const void* w, void* w_packed
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
-static conv_status launch_reduce(conv_plan_t plan, const void* bias, void* y, cudaStream_t s) {
+// The split-K reduction: partial sums in split order, then the epilogue.
+static conv_status launch_reduce(conv_plan_t plan, const float* ws, const void* bias, void* y, cudaStream_t s) {
     const Geom& g = plan->g;
     const long long MGK = (long long)g.M * g.G * g.K;
     const int threads = 256;
     const long long work = (g.G * g.K) % 4 == 0 ? MGK / 4 : MGK;
     const int blocks = (int)std::min<long long>(cdiv(work, threads), (long long)plan->sm_count * 8);
-    const float* ws = static_cast<const float*>(plan->workspace);
+    const bool pdl = plan->overlap != 0;
+    cudaError_t e;
     if (plan->dtype == CONV_BF16)
-        splitk_reduce_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
-            ws, plan->splits, MGK, g.G * g.K, static_cast<const __nv_bfloat16*>(bias),
-            static_cast<__nv_bfloat16*>(y), (int)plan->epi);
+        e = launch_kernel(splitk_reduce_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, s, pdl, ws,
+                          plan->splits, MGK, g.G * g.K, static_cast<const __nv_bfloat16*>(bias),
+                          static_cast<__nv_bfloat16*>(y), (int)plan->epi, (int)pdl);
     else
-        splitk_reduce_kernel<float><<<blocks, threads, 0, s>>>(ws, plan->splits, MGK, g.G * g.K,
-                                                               static_cast<const float*>(bias),
-                                                               static_cast<float*>(y), (int)plan->epi);
-    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+        e = launch_kernel(splitk_reduce_kernel<float>, dim3(blocks), dim3(threads), 0, s, pdl, ws, plan->splits, MGK,
+                          g.G * g.K, static_cast<const float*>(bias), static_cast<float*>(y), (int)plan->epi,
+                          (int)pdl);
+    return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
-conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, const void* bias, void* y,
-                     void* stream) {
+// Argument checks shared by both forward entry points.
+static conv_status check_forward_args(conv_plan_t plan, const void* x, const void* w_packed, const void* bias,
+                                      const void* y) {
     if (!plan || !x || !w_packed || !y) return CONV_ERR_INVALID_ARG;
     const bool needs_bias = plan->epi == CONV_EPI_BIAS || plan->epi == CONV_EPI_BIAS_GELU;
     if (needs_bias && !bias) return CONV_ERR_INVALID_ARG;
     if (misaligned(x) || misaligned(w_packed) || misaligned(y) || (needs_bias && misaligned(bias)))
         return CONV_ERR_ALIGNMENT;
-    if (plan->workspace_bytes && (!plan->workspace || plan->workspace_size < plan->workspace_bytes))
-        return CONV_ERR_WORKSPACE;
+    return CONV_OK;
+}
+
+// Enqueue the forward pass with ws as the split-K workspace (null when the plan has none).
+static conv_status run_forward(conv_plan_t plan, const void* x, const void* w_packed, const void* bias, void* y,
+                               float* ws, cudaStream_t s) {
+    const bool needs_bias = plan->epi == CONV_EPI_BIAS || plan->epi == CONV_EPI_BIAS_GELU;
     unsigned* err = error_word_ptr();
     if (!err) return CONV_ERR_CUDA;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (plan->variant == VAR_TC) {
         TcParams tp;
         tp.g = plan->g;
         tp.x = x; tp.wpack = w_packed; tp.bias = needs_bias ? bias : nullptr; tp.y = y;
-        tp.ws = static_cast<float*>(plan->workspace);
+        tp.ws = ws;
         tp.err = err;
         tp.BN = plan->BN; tp.num_mt = plan->num_mt; tp.num_nt = plan->num_nt; tp.nkb = plan->nkb;
         tp.nchunks = plan->nchunks; tp.cpt = plan->cpt; tp.splits = plan->splits; tp.kbps = plan->kbps;
@@ -717,6 +729,7 @@ conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, cons
         tp.slab = plan->slab; tp.slab_bws = plan->slab_bws; tp.slab_hr = plan->slab_hr; tp.slab_nkg = plan->slab_nkg;
         tp.slab_nbg = plan->slab_nbg; tp.slab_btaps = plan->slab_btaps; tp.slab_sa = plan->slab_sa;
         tp.slab_sb = plan->slab_sb; tp.slab_a_stage = plan->slab_a_stage; tp.slab_resident = plan->slab_resident;
+        tp.pdl = plan->overlap;
         CUtensorMap map;
         if (plan->tma && !encode_act_map(plan, x, &map)) return CONV_ERR_CUDA;
         e = plan->slab ? launch_slab(tp, &map, plan->grid, plan->slab_smem, s)
@@ -725,13 +738,30 @@ conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, cons
         SimtParams sp;
         sp.g = plan->g;
         sp.x = x; sp.wpack = w_packed; sp.bias = needs_bias ? bias : nullptr; sp.y = y;
-        sp.ws = static_cast<float*>(plan->workspace);
+        sp.ws = ws;
         sp.Kg = plan->Kg; sp.Kpad = plan->Kpad; sp.num_mt = plan->num_mt; sp.num_nt = plan->num_nt;
         sp.nkt = plan->nkt; sp.splits = plan->splits; sp.ktps = plan->ktps; sp.epi = (int)plan->epi;
+        sp.pdl = plan->overlap;
         e = launch_simt(sp, plan->dtype == CONV_BF16, plan->BM, plan->vec != 0, s);
     }
     if (e != cudaSuccess) return CONV_ERR_CUDA;
-    if (plan->splits > 1) return launch_reduce(plan, needs_bias ? bias : nullptr, y, s);
+    if (plan->splits > 1) return launch_reduce(plan, ws, needs_bias ? bias : nullptr, y, s);
+    return CONV_OK;
+}
+
+conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, const void* bias, void* y,
+                     void* stream) {
+    const conv_status st = check_forward_args(plan, x, w_packed, bias, y);
+    if (st != CONV_OK) return st;
+    if (plan->workspace_bytes && (!plan->workspace || plan->workspace_size < plan->workspace_bytes))
+        return CONV_ERR_WORKSPACE;
+    return run_forward(plan, x, w_packed, bias, y, static_cast<float*>(plan->workspace),
+                       static_cast<cudaStream_t>(stream));
+}
+
+conv_status conv_plan_set_overlap(conv_plan_t plan, int enable) {
+    if (!plan) return CONV_ERR_INVALID_ARG;
+    plan->overlap = enable ? 1 : 0;
     return CONV_OK;
 }
 
@@ -792,72 +822,19 @@ float* static_scratch_ptr() {
     return g_scratch_ptr[dev];
 }
 
-conv_status launch_reduce_into(conv_plan_t plan, const float* ws, const void* bias, void* y, cudaStream_t s) {
-    const Geom& g = plan->g;
-    const long long MGK = (long long)g.M * g.G * g.K;
-    const int threads = 256;
-    const long long work = (g.G * g.K) % 4 == 0 ? MGK / 4 : MGK;
-    const int blocks = (int)std::min<long long>(cdiv(work, threads), (long long)plan->sm_count * 8);
-    if (plan->dtype == CONV_BF16)
-        splitk_reduce_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
-            ws, plan->splits, MGK, g.G * g.K, static_cast<const __nv_bfloat16*>(bias),
-            static_cast<__nv_bfloat16*>(y), (int)plan->epi);
-    else
-        splitk_reduce_kernel<float><<<blocks, threads, 0, s>>>(ws, plan->splits, MGK, g.G * g.K,
-                                                               static_cast<const float*>(bias),
-                                                               static_cast<float*>(y), (int)plan->epi);
-    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
-}
 }  // namespace
 
 extern "C" conv_status conv_fwd_static_scratch(conv_plan_t plan, const void* x, const void* w_packed,
                                                const void* bias, void* y, void* stream) {
-    if (!plan || !x || !w_packed || !y) return CONV_ERR_INVALID_ARG;
-    const bool needs_bias = plan->epi == CONV_EPI_BIAS || plan->epi == CONV_EPI_BIAS_GELU;
-    if (needs_bias && !bias) return CONV_ERR_INVALID_ARG;
-    if (misaligned(x) || misaligned(w_packed) || misaligned(y) || (needs_bias && misaligned(bias)))
-        return CONV_ERR_ALIGNMENT;
+    const conv_status st = check_forward_args(plan, x, w_packed, bias, y);
+    if (st != CONV_OK) return st;
     if (plan->workspace_bytes > CONV_STATIC_SCRATCH_BYTES) return CONV_ERR_WORKSPACE;
     float* scratch = nullptr;
     if (plan->workspace_bytes) {
         scratch = static_scratch_ptr();
         if (!scratch) return CONV_ERR_CUDA;
     }
-    unsigned* err = error_word_ptr();
-    if (!err) return CONV_ERR_CUDA;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (plan->variant == VAR_TC) {
-        TcParams tp;
-        tp.g = plan->g;
-        tp.x = x; tp.wpack = w_packed; tp.bias = needs_bias ? bias : nullptr; tp.y = y;
-        tp.ws = scratch;
-        tp.err = err;
-        tp.BN = plan->BN; tp.num_mt = plan->num_mt; tp.num_nt = plan->num_nt; tp.nkb = plan->nkb;
-        tp.nchunks = plan->nchunks; tp.cpt = plan->cpt; tp.splits = plan->splits; tp.kbps = plan->kbps;
-        tp.epi = (int)plan->epi; tp.total_units = plan->total_units;
-        tp.tma = plan->tma; tp.map_kind = plan->map_kind; tp.BW = plan->BW; tp.BH = plan->BH;
-        tp.tiles_w = plan->tiles_w; tp.tiles_h = plan->tiles_h; tp.cbt = plan->cbt; tp.tf32 = plan->tf32;
-        tp.sleep_mask = plan->sleep_mask;
-        tp.slab = plan->slab; tp.slab_bws = plan->slab_bws; tp.slab_hr = plan->slab_hr; tp.slab_nkg = plan->slab_nkg;
-        tp.slab_nbg = plan->slab_nbg; tp.slab_btaps = plan->slab_btaps; tp.slab_sa = plan->slab_sa;
-        tp.slab_sb = plan->slab_sb; tp.slab_a_stage = plan->slab_a_stage; tp.slab_resident = plan->slab_resident;
-        CUtensorMap map;
-        if (plan->tma && !encode_act_map(plan, x, &map)) return CONV_ERR_CUDA;
-        e = plan->slab ? launch_slab(tp, &map, plan->grid, plan->slab_smem, s)
-                       : launch_tc(tp, plan->tma ? &map : nullptr, plan->stages, plan->grid, s);
-    } else {
-        SimtParams sp;
-        sp.g = plan->g;
-        sp.x = x; sp.wpack = w_packed; sp.bias = needs_bias ? bias : nullptr; sp.y = y;
-        sp.ws = scratch;
-        sp.Kg = plan->Kg; sp.Kpad = plan->Kpad; sp.num_mt = plan->num_mt; sp.num_nt = plan->num_nt;
-        sp.nkt = plan->nkt; sp.splits = plan->splits; sp.ktps = plan->ktps; sp.epi = (int)plan->epi;
-        e = launch_simt(sp, plan->dtype == CONV_BF16, plan->BM, plan->vec != 0, s);
-    }
-    if (e != cudaSuccess) return CONV_ERR_CUDA;
-    if (plan->splits > 1) return launch_reduce_into(plan, scratch, needs_bias ? bias : nullptr, y, s);
-    return CONV_OK;
+    return run_forward(plan, x, w_packed, bias, y, scratch, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" {

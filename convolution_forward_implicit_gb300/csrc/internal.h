@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace convfwd {
 
 // A problem in the 3-spatial form (conv1d: D = H = 1, conv2d: D = 1), channels last.
@@ -19,6 +21,36 @@ struct Geom {
 };
 
 enum Epi { EPI_NONE = 0, EPI_BIAS = 1, EPI_BIAS_GELU = 2, EPI_GELU = 3 };
+
+#ifdef __CUDACC__
+// Programmatic dependent launch.  griddep_launch: this CTA allows the next kernel on the
+// stream (if launched as a programmatic dependent) to start; griddep_wait: block until the
+// kernel before this one on the stream has completed and its writes are visible.  Every
+// thread that reads data a previous kernel may produce (x, bias) or writes data it may
+// still read (y, workspace) calls griddep_wait first.
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+#endif
+
+// Launch a kernel, as a programmatic dependent of the previous kernel on the stream when
+// pdl is set.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                 bool pdl, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Device error word codes (bit flags).
 enum : unsigned { ERR_WAIT_TIMEOUT = 1u };
@@ -60,6 +92,7 @@ struct TcParams {
     int slab_sa, slab_sb;   // slab ring and weight ring stages (resident: weight chunks held)
     int slab_resident;      // 1: the weights of one (group, N tile) stay in shared memory
     int slab_a_stage;       // bytes per slab stage (3xTF32: hi half then lo half)
+    int pdl;                // 1: launched as a programmatic dependent (see griddep_wait)
 };
 
 constexpr size_t SLAB_SMEM_MAX = 232448;   // dynamic shared memory a block may opt in to
@@ -85,6 +118,7 @@ struct SimtParams {
     int nkt;                // K steps of 8 along Kg
     int splits, ktps;       // split-K factor, K steps per split
     int epi;
+    int pdl;
 };
 
 cudaError_t launch_simt(const SimtParams& p, bool bf16, int BM, bool vec, cudaStream_t stream);

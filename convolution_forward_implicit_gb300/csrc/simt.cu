@@ -70,6 +70,10 @@ __device__ __forceinline__ long long x_offset(const Geom& g, const PixelBase& pb
 
 template <typename T, int BM, bool VEC>
 __global__ void __launch_bounds__(THREADS) conv_fwd_simt_kernel(const __grid_constant__ SimtParams p) {
+    if (p.pdl) {   // a programmatic dependent: let the next kernel start, wait for the previous one
+        griddep_launch();
+        griddep_wait();
+    }
     constexpr int TM = BM / 16;                 // rows per thread
     constexpr int A_LOADERS = BM * 2;           // threads that each load 4 consecutive kk of one row
     __shared__ __align__(16) float As[2][BK][BM + 4];
@@ -226,8 +230,7 @@ __global__ void __launch_bounds__(THREADS) conv_fwd_simt_kernel(const __grid_con
 template <typename T, int BM, bool VEC>
 cudaError_t launch_t(const SimtParams& p, cudaStream_t stream) {
     dim3 grid(p.num_mt, p.num_nt, p.g.G * p.splits);
-    conv_fwd_simt_kernel<T, BM, VEC><<<grid, THREADS, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(conv_fwd_simt_kernel<T, BM, VEC>, grid, dim3(THREADS), 0, stream, p.pdl != 0, p);
 }
 
 }  // namespace

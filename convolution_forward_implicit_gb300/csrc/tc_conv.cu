@@ -119,6 +119,8 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // set up: the next kernel on the stream may start (its own set-up and weight loads)
+    if (p.pdl) griddep_launch();
 
     const Geom& g = p.g;
     const int GC = g.G * g.C;
@@ -134,6 +136,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
                 const int cblk = T::TF32 ? 32 : 64;     // channels in one 128-byte row
                 uint32_t it = 0;
                 bool aborted = false;
+                bool x_ready = !p.pdl;      // x may come from the previous kernel on the stream
                 for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
                     int mt, gi, nt, split;
                     decode_unit(p, u, mt, gi, nt, split);
@@ -156,6 +159,10 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
                         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), a_tx + C::B_STAGE);
                         __syncwarp(0x3u);
                         if (lane == 0) {
+                            if (!x_ready) {
+                                griddep_wait();
+                                x_ready = true;
+                            }
                             const int tap = kb / p.cbt;
                             const int c0 = (kb - tap * p.cbt) * cblk;
                             const int zz = tap / (g.Y * g.X);
@@ -183,6 +190,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
             const int rb = pt >> 3;      // rows rb, rb+16, ..., rb+112
             const uint32_t swz = (uint32_t)((j ^ (rb & 7)) << 4);
             const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x);
+            if (p.pdl) griddep_wait();
             uint32_t it = 0;
             bool aborted = false;
             for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
@@ -253,6 +261,8 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
         }
     } else if (warp == T::MMA_WARP) {
         // ------------------------------------------------------------ MMA issue
+        // bounded waits start once the previous kernel on the stream has completed
+        if (p.pdl) griddep_wait();
         if (lane == 0) {
             constexpr uint32_t IDESC = idesc_f32acc(BM, BN, T::TF32 ? 2u : 1u);
             uint32_t it = 0, tile_i = 0;
@@ -305,6 +315,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
         __syncwarp();
     } else if (T::TF32 && warp >= T::CVT_WARP0) {
         // ------------------------------------------------------------ hi/lo split (3xTF32)
+        if (p.pdl) griddep_wait();
         // Every fp32 activation x becomes hi = x with its low 13 mantissa bits cleared (exact
         // in TF32) and lo = x - hi (exact in fp32); the MMA then sums lo*w_hi + hi*w_lo + hi*w_hi.
         const int ct = threadIdx.x - T::CVT_WARP0 * 32;
@@ -355,6 +366,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
         const bool add_bias = (p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU) && !partial;
         const bool do_gelu = (p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU) && !partial;
         uint8_t* stg = smem + STG_OFFSET + warp * STG_WARP_BYTES;
+        if (p.pdl) griddep_wait();   // y, the workspace and bias may belong to the previous kernel
         uint32_t tile_i = 0;
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x, ++tile_i) {
             int mt, gi, nt, split;
@@ -426,8 +438,7 @@ cudaError_t launch_one(const TcParams& p, const CUtensorMap& map, int grid, cuda
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    kern<<<grid, Traits<KIND>::THREADS, smem, stream>>>(p, map);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(Traits<KIND>::THREADS), smem, stream, p.pdl != 0, p, map);
 }
 
 }  // namespace

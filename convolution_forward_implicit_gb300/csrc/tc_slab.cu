@@ -112,6 +112,8 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // set up: the next kernel on the stream may start (its own set-up and weight loads)
+    if (p.pdl) griddep_launch();
 
     const Geom& g = p.g;
     const int cblk = TF32 ? 32 : 64;
@@ -121,6 +123,7 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
     if (warp == R::A_WARP) {
         // ------------------------------------------------------------ slab copies
         if (lane == 0) {
+            if (p.pdl) griddep_wait();   // x may come from the previous kernel on the stream
             const uint32_t a_tx = (uint32_t)(p.slab_hr * p.slab_bws) * 128u;
             uint32_t ia = 0;
             bool aborted = false;
@@ -163,6 +166,9 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
                     const int key = gi * p.num_nt + nt;
                     if (key == prev) continue;
                     prev = key;
+                    // only the first weight set loads before the previous kernel has completed;
+                    // a wait that can block (and time out) comes after it
+                    if (p.pdl && j == 1) griddep_wait();
                     if (!wait_bar(empty_b(0), (j & 1u) ^ 1u, abort_flag, p.err, p.sleep_mask & 1)) {
                         aborted = true;
                         break;
@@ -176,6 +182,7 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
                 }
             } else {
                 uint32_t ib = 0;
+                bool waited = false;
                 for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
                     int mt, gi, nt, split;
                     decode_unit(p, u, mt, gi, nt, split);
@@ -183,6 +190,12 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
                         const int s = ib % SB;
                         if (s % R::B_WARPS != bw) continue;    // each ring stage has one owner warp
                         const uint32_t ph = (ib / SB) & 1u;
+                        // the first pass over the ring loads before the previous kernel has
+                        // completed; waits that can block (and time out) come after it
+                        if (p.pdl && ib >= (uint32_t)SB && !waited) {
+                            griddep_wait();
+                            waited = true;
+                        }
                         if (!wait_bar(empty_b(s), ph ^ 1u, abort_flag, p.err, p.sleep_mask & 1)) {
                             aborted = true;
                             break;
@@ -198,6 +211,8 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
         __syncwarp();
     } else if (warp == R::MMA_WARP) {
         // ------------------------------------------------------------ MMA issue (whole warp)
+        // bounded waits start once the previous kernel on the stream has completed
+        if (p.pdl) griddep_wait();
         constexpr uint32_t IDESC = idesc_f32acc(BM, BN, TF32 ? 2u : 1u);
         const bool msleep = (p.sleep_mask & 4) != 0;
         const bool resident = p.slab_resident != 0;
@@ -299,6 +314,7 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
         __syncwarp();
     } else if (TF32 && warp >= R::CVT_WARP0) {
         // ------------------------------------------------------------ hi/lo split (3xTF32)
+        if (p.pdl) griddep_wait();
         // Every fp32 x of the slab becomes hi = x with its low 13 mantissa bits cleared (exact
         // in TF32) and lo = x - hi (exact in fp32); the MMA sums lo*w_hi + hi*w_lo + hi*w_hi.
         const int ct = threadIdx.x - R::CVT_WARP0 * 32;
@@ -337,6 +353,7 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
         const bool add_bias = p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU;
         const bool do_gelu = p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU;
         uint8_t* stg = smem + stg_off + warp * STG_WARP_BYTES;
+        if (p.pdl) griddep_wait();   // y and bias may belong to the previous kernel
         uint32_t tile_i = 0;
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x, ++tile_i) {
             int mt, gi, nt, split;
@@ -391,8 +408,7 @@ cudaError_t launch_slab_one(const TcParams& p, const CUtensorMap& map, int grid,
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    kern<<<grid, SlabRoles<TF32>::THREADS, smem, stream>>>(p, map);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(SlabRoles<TF32>::THREADS), smem, stream, p.pdl != 0, p, map);
 }
 
 }  // namespace

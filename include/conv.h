@@ -157,6 +157,23 @@ const char* conv_plan_describe(conv_plan_t plan);
 double conv_plan_flops(conv_plan_t plan);
 
 /*
+ * Let consecutive kernels of a chain overlap (programmatic dependent launch).  With
+ * enable != 0, the kernels conv_fwd launches for this plan are marked so that each may
+ * start while the kernel before it on the stream is still running, when that kernel
+ * allows it (the library's own kernels allow it as soon as each of their CTAs is set
+ * up).  A kernel that starts early builds its shared-memory pipeline and loads the
+ * packed weights, then waits for the previous kernel to complete before it reads x or
+ * bias or writes y or the workspace.  So the overlap is safe whenever w_packed is not
+ * written by the kernel launched just before conv_fwd on the same stream; x, bias and y
+ * may be (a chain of layers, each reading the previous layer's output, is the intended
+ * use).  The pages' first "next step" asks for exactly this chaining of the Whisper
+ * frontend (page "[ET-VK] conv1d ...", "The conv2d path already solves this": the two
+ * convs and their GELUs run as dependent dispatches).  Default: off.  Returns
+ * CONV_ERR_INVALID_ARG on a NULL plan.
+ */
+conv_status conv_plan_set_overlap(conv_plan_t plan, int enable);
+
+/*
  * Forward pass for callers that cannot allocate device memory.  (The pages have no
  * counterpart: this is an interface convenience of this library.)
  *
