@@ -730,6 +730,13 @@ static conv_status run_forward(conv_plan_t plan, const void* x, const void* w_pa
         tp.slab_nbg = plan->slab_nbg; tp.slab_btaps = plan->slab_btaps; tp.slab_sa = plan->slab_sa;
         tp.slab_sb = plan->slab_sb; tp.slab_a_stage = plan->slab_a_stage; tp.slab_resident = plan->slab_resident;
         tp.pdl = plan->overlap;
+        tp.f_splits = make_fastdiv(plan->splits); tp.f_num_nt = make_fastdiv(plan->num_nt);
+        tp.f_G = make_fastdiv(plan->g.G); tp.f_tiles_w = make_fastdiv(plan->tiles_w);
+        tp.f_tiles_h = make_fastdiv(plan->tiles_h); tp.f_Do = make_fastdiv(plan->g.Do);
+        tp.f_Ho = make_fastdiv(plan->g.Ho); tp.f_Wo = make_fastdiv(plan->g.Wo); tp.f_cbt = make_fastdiv(plan->cbt);
+        tp.f_cpt = make_fastdiv(plan->cpt); tp.f_X = make_fastdiv(plan->g.X);
+        tp.f_YX = make_fastdiv(plan->g.Y * plan->g.X); tp.f_BW = make_fastdiv(plan->BW);
+        tp.f_bws = make_fastdiv(plan->slab_bws);
         CUtensorMap map;
         if (plan->tma && !encode_act_map(plan, x, &map)) return CONV_ERR_CUDA;
         e = plan->slab ? launch_slab(tp, &map, plan->grid, plan->slab_smem, s)

@@ -22,6 +22,30 @@ struct Geom {
 
 enum Epi { EPI_NONE = 0, EPI_BIAS = 1, EPI_BIAS_GELU = 2, EPI_GELU = 3 };
 
+// Division by a divisor fixed at plan time, done by a multiplication (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994, the round-up
+// method): with s = ceil(log2 d) and m = floor(2^32 (2^s - d) / d) + 1,
+// floor(n / d) = (mulhi(n, m) + n) >> s for every 0 <= n < 2^31.  The kernels' per-tile
+// index arithmetic (unit -> tile -> pixel) runs on these instead of hardware-less integer
+// division sequences, which cost a few hundred cycles each on the first tile.
+struct FastDiv {
+    uint32_t d, m, s;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    f.d = d < 1 ? 1 : d;
+    uint32_t s = 0;
+    while (s < 31 && (1ull << s) < f.d) ++s;
+    f.s = s;
+    f.m = (uint32_t)((((1ull << s) - f.d) << 32) / f.d + 1);
+    return f;
+}
+#ifdef __CUDACC__
+__device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
+    return (int)((__umulhi((uint32_t)n, f.m) + (uint32_t)n) >> f.s);
+}
+#endif
+
 #ifdef __CUDACC__
 // Programmatic dependent launch.  griddep_launch: this CTA allows the next kernel on the
 // stream (if launched as a programmatic dependent) to start; griddep_wait: block until the
@@ -93,6 +117,8 @@ struct TcParams {
     int slab_resident;      // 1: the weights of one (group, N tile) stay in shared memory
     int slab_a_stage;       // bytes per slab stage (3xTF32: hi half then lo half)
     int pdl;                // 1: launched as a programmatic dependent (see griddep_wait)
+    // divisors of the per-tile index arithmetic
+    FastDiv f_splits, f_num_nt, f_G, f_tiles_w, f_tiles_h, f_Do, f_Ho, f_Wo, f_cbt, f_cpt, f_X, f_YX, f_BW, f_bws;
 };
 
 constexpr size_t SLAB_SMEM_MAX = 232448;   // dynamic shared memory a block may opt in to

@@ -247,13 +247,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 }
 
 __device__ __forceinline__ void decode_unit(const TcParams& p, int u, int& mt, int& g, int& nt, int& split) {
-    split = u % p.splits;
-    int r = u / p.splits;
-    nt = r % p.num_nt;
-    r /= p.num_nt;
-    g = r % p.g.G;
-    mt = r / p.g.G;
+    const int r = fdiv(u, p.f_splits);
+    split = u - r * p.splits;
+    const int r2 = fdiv(r, p.f_num_nt);
+    nt = r - r2 * p.num_nt;
+    mt = fdiv(r2, p.f_G);
+    g = r2 - mt * p.g.G;
 }
+
+// Position in a ring of n pipeline stages: the stage and the parity of its current phase,
+// advanced together (no division per step).
+struct Ring {
+    int n, s;
+    uint32_t ph;
+    __device__ __forceinline__ explicit Ring(int stages) : n(stages), s(0), ph(0) {}
+    __device__ __forceinline__ void next() {
+        if (++s == n) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
 
 // TMA tiles: mt -> (n, od, oh0, ow0) of a BH x BW block of one output plane.
 struct TileOrigin {
@@ -261,12 +275,12 @@ struct TileOrigin {
 };
 __device__ __forceinline__ TileOrigin tile_origin(const TcParams& p, int mt) {
     TileOrigin t;
-    const int tw = mt % p.tiles_w;
-    int r = mt / p.tiles_w;
-    const int th = r % p.tiles_h;
-    r /= p.tiles_h;
-    t.od = r % p.g.Do;
-    t.n = r / p.g.Do;
+    const int r = fdiv(mt, p.f_tiles_w);
+    const int tw = mt - r * p.tiles_w;
+    const int r2 = fdiv(r, p.f_tiles_h);
+    const int th = r - r2 * p.tiles_h;
+    t.n = fdiv(r2, p.f_Do);
+    t.od = r2 - t.n * p.g.Do;
     t.oh0 = th * p.BH;
     t.ow0 = tw * p.BW;
     return t;

@@ -163,11 +163,11 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
                                 griddep_wait();
                                 x_ready = true;
                             }
-                            const int tap = kb / p.cbt;
+                            const int tap = fdiv(kb, p.f_cbt);
                             const int c0 = (kb - tap * p.cbt) * cblk;
-                            const int zz = tap / (g.Y * g.X);
+                            const int zz = fdiv(tap, p.f_YX);
                             const int rem = tap - zz * g.Y * g.X;
-                            const int yy = rem / g.X;
+                            const int yy = fdiv(rem, p.f_X);
                             const int xx = rem - yy * g.X;
                             const int wi = w0 + xx * g.dw, hi = h0 + yy * g.dh;
                             if (p.map_kind == 0)
@@ -203,11 +203,12 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
                 for (int i = 0; i < 8; ++i) {
                     const int m = mt * BM + rb + 16 * i;
                     if (m < g.M) {
-                        int t = m;
-                        const int ow = t % g.Wo; t /= g.Wo;
-                        const int oh = t % g.Ho; t /= g.Ho;
-                        const int od = t % g.Do;
-                        rn[i] = t / g.Do;
+                        const int t1 = fdiv(m, p.f_Wo);
+                        const int ow = m - t1 * g.Wo;
+                        const int t2 = fdiv(t1, p.f_Ho);
+                        const int oh = t1 - t2 * g.Ho;
+                        rn[i] = fdiv(t2, p.f_Do);
+                        const int od = t2 - rn[i] * g.Do;
                         rd[i] = od * g.sd - g.pd;
                         rh[i] = oh * g.sh - g.ph;
                         rw[i] = ow * g.sw - g.pw;
@@ -227,11 +228,11 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
                     }
                     const int q = kb * 8 + j;
                     const bool qok = q < p.nchunks;
-                    const int tap = qok ? q / p.cpt : 0;
+                    const int tap = qok ? fdiv(q, p.f_cpt) : 0;
                     const int c0 = (q - tap * p.cpt) * 8;
-                    const int zz = tap / (g.Y * g.X);
+                    const int zz = fdiv(tap, p.f_YX);
                     const int rem = tap - zz * g.Y * g.X;
-                    const int yy = rem / g.X;
+                    const int yy = fdiv(rem, p.f_X);
                     const int xx = rem - yy * g.X;
                     const int dz = zz * g.dd, dy = yy * g.dh, dx = xx * g.dw;
                     const uint32_t dst0 = sA + s * T::A_STAGE + swz;
@@ -379,7 +380,8 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
             auto row_offset = [&](int rr) -> long long {
                 int m;
                 if (T::TMA) {
-                    const int oh = to.oh0 + rr / p.BW, ow = to.ow0 + rr % p.BW;
+                    const int rh = fdiv(rr, p.f_BW);
+                    const int oh = to.oh0 + rh, ow = to.ow0 + (rr - rh * p.BW);
                     if (rr >= p.BW * p.BH || oh >= g.Ho || ow >= g.Wo) return -1;
                     m = ((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow;
                 } else {

@@ -125,17 +125,17 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
         if (lane == 0) {
             if (p.pdl) griddep_wait();   // x may come from the previous kernel on the stream
             const uint32_t a_tx = (uint32_t)(p.slab_hr * p.slab_bws) * 128u;
-            uint32_t ia = 0;
+            Ring ra(SA);
             bool aborted = false;
             for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
                 int mt, gi, nt, split;
                 decode_unit(p, u, mt, gi, nt, split);
                 const TileOrigin to = tile_origin(p, mt);
                 const int w0 = to.ow0 - g.pw, h0 = to.oh0 - g.ph;
-                for (int kg = 0; kg < p.slab_nkg; ++kg, ++ia) {
-                    const int zz = kg / p.cbt, cb = kg - zz * p.cbt;
-                    const int s = ia % SA;
-                    const uint32_t ph = (ia / SA) & 1u;
+                for (int kg = 0; kg < p.slab_nkg; ++kg, ra.next()) {
+                    const int zz = fdiv(kg, p.f_cbt), cb = kg - zz * p.cbt;
+                    const int s = ra.s;
+                    const uint32_t ph = ra.ph;
                     if (!wait_bar(empty_a(s), ph ^ 1u, abort_flag, p.err, p.sleep_mask & 1)) { aborted = true; break; }
                     mbar_arrive_expect_tx(full_a(s), a_tx);
                     if (p.map_kind == 0)
@@ -182,14 +182,15 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
                 }
             } else {
                 uint32_t ib = 0;
+                Ring rb(SB);
                 bool waited = false;
                 for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
                     int mt, gi, nt, split;
                     decode_unit(p, u, mt, gi, nt, split);
-                    for (int c = 0; c < nchunk; ++c, ++ib) {
-                        const int s = ib % SB;
+                    for (int c = 0; c < nchunk; ++c, ++ib, rb.next()) {
+                        const int s = rb.s;
                         if (s % R::B_WARPS != bw) continue;    // each ring stage has one owner warp
-                        const uint32_t ph = (ib / SB) & 1u;
+                        const uint32_t ph = rb.ph;
                         // the first pass over the ring loads before the previous kernel has
                         // completed; waits that can block (and time out) come after it
                         if (p.pdl && ib >= (uint32_t)SB && !waited) {
@@ -221,7 +222,8 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
         const int KT = p.g.G * p.num_nt;
         const int kstep = (int)(gridDim.x % (unsigned)KT);
         int key = (int)(blockIdx.x % (unsigned)KT);
-        uint32_t ia = 0, ib = 0, tile_i = 0, jw = 0;
+        Ring ra(SA), rb(SB);
+        uint32_t tile_i = 0, jw = 0;
         int prev = -1;
         bool aborted = false;
         for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x, ++tile_i) {
@@ -247,9 +249,9 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             uint32_t first = 1;
-            for (int kg = 0; kg < p.slab_nkg && !aborted; ++kg, ++ia) {
-                const int sa = ia % SA;
-                const uint32_t pha = (ia / SA) & 1u;
+            for (int kg = 0; kg < p.slab_nkg && !aborted; ++kg, ra.next()) {
+                const int sa = ra.s;
+                const uint32_t pha = ra.ph;
                 if (!wait_bar_warp(TF32 ? cvt_a(sa) : full_a(sa), pha, abort_flag, p.err, msleep)) {
                     aborted = true;
                     break;
@@ -262,9 +264,9 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
                     if (resident) {
                         b0 = sB + (uint32_t)(kg * nbg + bg) * b_stage;
                     } else {
-                        sb = ib % SB;
-                        const uint32_t phb = (ib / SB) & 1u;
-                        ++ib;
+                        sb = rb.s;
+                        const uint32_t phb = rb.ph;
+                        rb.next();
                         if (!wait_bar_warp(full_b(sb), phb, abort_flag, p.err, msleep)) {
                             aborted = true;
                             break;
@@ -319,12 +321,12 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
         // in TF32) and lo = x - hi (exact in fp32); the MMA sums lo*w_hi + hi*w_lo + hi*w_hi.
         const int ct = threadIdx.x - R::CVT_WARP0 * 32;
         const int n16 = p.slab_hr * p.slab_bws * 8;
-        uint32_t ia = 0;
+        Ring ra(SA);
         bool aborted = false;
         for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
-            for (int kg = 0; kg < p.slab_nkg; ++kg, ++ia) {
-                const int s = ia % SA;
-                const uint32_t ph = (ia / SA) & 1u;
+            for (int kg = 0; kg < p.slab_nkg; ++kg, ra.next()) {
+                const int s = ra.s;
+                const uint32_t ph = ra.ph;
                 if (!wait_bar_warp(full_a(s), ph, abort_flag, p.err)) { aborted = true; break; }
                 uint4* hi = reinterpret_cast<uint4*>(smem + s * a_stage);
                 uint4* lo = reinterpret_cast<uint4*>(smem + s * a_stage + a_half);
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
             const TileOrigin to = tile_origin(p, mt);
             // output pixel of accumulator row rr (row pitch BWs), or -1 if it is not stored
             auto row_offset = [&](int rr) -> long long {
-                const int rh = rr / p.slab_bws, rw = rr - rh * p.slab_bws;
+                const int rh = fdiv(rr, p.f_bws), rw = rr - rh * p.slab_bws;
                 const int oh = to.oh0 + rh, ow = to.ow0 + rw;
                 if (rh >= p.BH || rw >= p.BW || oh >= g.Ho || ow >= g.Wo) return -1;
                 return (long long)(((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow) * (g.G * g.K);
