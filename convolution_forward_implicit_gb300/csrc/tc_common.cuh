@@ -200,6 +200,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
           "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
         : "r"(taddr));
 }
+// 32 lanes x 32 bits, 32 consecutive columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+}
+template <int QW>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[QW]) {
+    if constexpr (QW == 32) tmem_ld32(taddr, v);
+    else tmem_ld16(taddr, v);
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 B,
@@ -239,6 +255,43 @@ __device__ __forceinline__ float gelu_bf16out(float v) {
     y = y * y; y = y * y; y = y * y; y = y * y;         // (.)^16
     const float h = __fdividef(0.5f * v, y);            // 0.5 v (1 - erf(|v|/sqrt 2)); 0 once y overflows
     return v >= 0.0f ? v - h : h;
+}
+
+// Two fp32 values in one 64-bit register pair, for the packed f32x2 arithmetic of sm_100+
+// (one instruction computes both lanes, each rounded exactly as the scalar operation).
+__device__ __forceinline__ uint64_t f2pk(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2up(uint64_t r, float& a, float& b) { asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r)); }
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// gelu_bf16out on two values at once: the polynomial and the squarings run as packed f32x2
+// operations, so each value gets bit for bit the result of the scalar form.
+__device__ __forceinline__ void gelu2_bf16out(float& a, float& b) {
+    const uint64_t z = f2pk(fabsf(a) * 0.70710678118654752f, fabsf(b) * 0.70710678118654752f);
+    uint64_t y = f2fma(z, f2pk(0.0000430638f, 0.0000430638f), f2pk(0.0002765672f, 0.0002765672f));
+    y = f2fma(z, y, f2pk(0.0001520143f, 0.0001520143f));
+    y = f2fma(z, y, f2pk(0.0092705272f, 0.0092705272f));
+    y = f2fma(z, y, f2pk(0.0422820123f, 0.0422820123f));
+    y = f2fma(z, y, f2pk(0.0705230784f, 0.0705230784f));
+    y = f2fma(z, y, f2pk(1.0f, 1.0f));
+    y = f2mul(y, y); y = f2mul(y, y); y = f2mul(y, y); y = f2mul(y, y);   // (.)^16
+    float ya, yb;
+    f2up(y, ya, yb);
+    const float ha = __fdividef(0.5f * a, ya), hb = __fdividef(0.5f * b, yb);
+    a = a >= 0.0f ? a - ha : ha;
+    b = b >= 0.0f ? b - hb : hb;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -333,21 +386,23 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
     for (int cb = cb_begin; cb < cb_end; cb += CW) {
         const int n0 = nt * BN + cb;
         if (n0 >= g.K) break;                               // warp-uniform
-        // 16 columns at a time: TMEM -> fp32 -> bias, GELU -> this lane's row slots in staging
+        // QW columns per TMEM load (32 where the chunk allows): TMEM -> fp32 -> bias, GELU ->
+        // this lane's row slots in staging
+        constexpr int QW = CW % 32 == 0 ? 32 : 16;
 #pragma unroll
-        for (int q = 0; q < CW / 16; ++q) {
-            const int nq = n0 + 16 * q;
-            uint32_t v[16];
+        for (int q = 0; q < CW / QW; ++q) {
+            const int nq = n0 + QW * q;
+            uint32_t v[QW];
             __syncwarp();                                   // tcgen05.ld is warp-aligned
-            tmem_ld16(taddr + (uint32_t)(cb + 16 * q), v);
+            tmem_ld<QW>(taddr + (uint32_t)(cb + QW * q), v);
             tmem_ld_wait();
-            float f[16];
+            float f[QW];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]);
+            for (int e = 0; e < QW; ++e) f[e] = __uint_as_float(v[e]);
             if (add_bias) {
                 // only whole 8-column groups inside K are read; columns past K are never stored
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < QW / 8; ++j) {
                     if (nq + 8 * j >= g.K) break;
                     if (ESZ == 4) {
                         const float4* bp = reinterpret_cast<const float4*>(
@@ -372,10 +427,15 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
                 }
             }
             if (do_gelu) {
+                if (ESZ == 2) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) f[e] = ESZ == 2 ? gelu_bf16out(f[e]) : gelu_f(f[e]);
+                    for (int e = 0; e < QW; e += 2) gelu2_bf16out(f[e], f[e + 1]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < QW; ++e) f[e] = gelu_f(f[e]);
+                }
             }
-            constexpr int SPQ = 16 / EPS;                   // 16-byte slots per 16 columns
+            constexpr int SPQ = QW / EPS;                   // 16-byte slots per QW columns
 #pragma unroll
             for (int t = 0; t < SPQ; ++t) {
                 const int j = q * SPQ + t;
