@@ -14,6 +14,7 @@
 #include <cudaTypedefs.h>
 
 #include "conv.h"
+#include "gelu.cuh"
 #include "internal.h"
 
 using namespace convfwd;
@@ -152,7 +153,6 @@ __global__ void prepack_simt_kernel(const T* __restrict__ w, T* __restrict__ out
 // ----------------------------------------------------------------------------- split-K reduction
 // y = epilogue(sum over splits, in split order, of the fp32 partials): a fixed order,
 // so results do not change from run to run.
-__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ void from_f(float& d, float v) { d = v; }
@@ -181,7 +181,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, l
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 if (add_bias) v[e] += to_f(bias[col + e]);
-                if (do_gelu) v[e] = gelu_f(v[e]);
+                if (do_gelu) v[e] = gelu(v[e]);
                 from_f(y[i * 4 + e], v[e]);
             }
         }
@@ -191,7 +191,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, l
             float a = ws[i];
             for (int s = 1; s < splits; ++s) a += ws[(long long)s * MGK + i];
             if (add_bias) a += to_f(bias[i % GK]);
-            if (do_gelu) a = gelu_f(a);
+            if (do_gelu) a = gelu(a);
             from_f(y[i], a);
         }
     }

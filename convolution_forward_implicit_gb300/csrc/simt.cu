@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "gelu.cuh"
 #include "internal.h"
 
 namespace convfwd {
@@ -49,7 +50,6 @@ template <> struct Io<__nv_bfloat16> {
     static __device__ __forceinline__ void st1(__nv_bfloat16* p, float a) { p[0] = __float2bfloat16_rn(a); }
 };
 
-__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
 
 // Input offset of reduction index kk for a pixel, or -1 where the tap is in the padding.
 struct PixelBase {
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(THREADS) conv_fwd_simt_kernel(const __grid_con
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 if (add_bias && n + e < g.K) v[e] += Io<T>::ld1(bias + (size_t)gi * g.K + n + e);
-                if (do_gelu) v[e] = gelu_f(v[e]);
+                if (do_gelu) v[e] = gelu(v[e]);
             }
             if (VEC) {
                 Io<T>::st4(y + o, v[0], v[1], v[2], v[3]);

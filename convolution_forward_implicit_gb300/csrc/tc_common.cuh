@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "gelu.cuh"
 #include "internal.h"
 
 namespace convfwd {
@@ -238,62 +239,6 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(int m, int n, uint32_t ab_fo
            ((uint32_t)(m >> 4) << 24);
 }
 
-__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
-
-// GELU for bf16 outputs: v * Phi(v) with erf from Abramowitz & Stegun, Handbook of
-// Mathematical Functions, eq. 7.1.28 (after Hastings): erf(z) = 1 - (1 + a1 z + ... + a6 z^6)^-16
-// for z >= 0, |error| <= 3e-7.  Evaluated in fp32 the GELU's relative error stays below 1e-6,
-// far under the bf16 rounding step, at one reciprocal and no exponential per value.
-__device__ __forceinline__ float gelu_bf16out(float v) {
-    const float z = fabsf(v) * 0.70710678118654752f;
-    float y = fmaf(z, 0.0000430638f, 0.0002765672f);
-    y = fmaf(z, y, 0.0001520143f);
-    y = fmaf(z, y, 0.0092705272f);
-    y = fmaf(z, y, 0.0422820123f);
-    y = fmaf(z, y, 0.0705230784f);
-    y = fmaf(z, y, 1.0f);
-    y = y * y; y = y * y; y = y * y; y = y * y;         // (.)^16
-    const float h = __fdividef(0.5f * v, y);            // 0.5 v (1 - erf(|v|/sqrt 2)); 0 once y overflows
-    return v >= 0.0f ? v - h : h;
-}
-
-// Two fp32 values in one 64-bit register pair, for the packed f32x2 arithmetic of sm_100+
-// (one instruction computes both lanes, each rounded exactly as the scalar operation).
-__device__ __forceinline__ uint64_t f2pk(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void f2up(uint64_t r, float& a, float& b) { asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r)); }
-__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-
-// gelu_bf16out on two values at once: the polynomial and the squarings run as packed f32x2
-// operations, so each value gets bit for bit the result of the scalar form.
-__device__ __forceinline__ void gelu2_bf16out(float& a, float& b) {
-    const uint64_t z = f2pk(fabsf(a) * 0.70710678118654752f, fabsf(b) * 0.70710678118654752f);
-    uint64_t y = f2fma(z, f2pk(0.0000430638f, 0.0000430638f), f2pk(0.0002765672f, 0.0002765672f));
-    y = f2fma(z, y, f2pk(0.0001520143f, 0.0001520143f));
-    y = f2fma(z, y, f2pk(0.0092705272f, 0.0092705272f));
-    y = f2fma(z, y, f2pk(0.0422820123f, 0.0422820123f));
-    y = f2fma(z, y, f2pk(0.0705230784f, 0.0705230784f));
-    y = f2fma(z, y, f2pk(1.0f, 1.0f));
-    y = f2mul(y, y); y = f2mul(y, y); y = f2mul(y, y); y = f2mul(y, y);   // (.)^16
-    float ya, yb;
-    f2up(y, ya, yb);
-    const float ha = __fdividef(0.5f * a, ya), hb = __fdividef(0.5f * b, yb);
-    a = a >= 0.0f ? a - ha : ha;
-    b = b >= 0.0f ? b - hb : hb;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -388,7 +333,8 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
         if (n0 >= g.K) break;                               // warp-uniform
         // QW columns per TMEM load (32 where the chunk allows): TMEM -> fp32 -> bias, GELU ->
         // this lane's row slots in staging
-        constexpr int QW = CW % 32 == 0 ? 32 : 16;
+        // (fp32 outputs keep 16: the 3xTF32 kernels run 544 threads and have fewer registers)
+        constexpr int QW = (ESZ == 2 && CW % 32 == 0) ? 32 : 16;
 #pragma unroll
         for (int q = 0; q < CW / QW; ++q) {
             const int nq = n0 + QW * q;
@@ -429,10 +375,10 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
             if (do_gelu) {
                 if (ESZ == 2) {
 #pragma unroll
-                    for (int e = 0; e < QW; e += 2) gelu2_bf16out(f[e], f[e + 1]);
+                    for (int e = 0; e < QW; e += 2) gelu2(f[e], f[e + 1]);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < QW; ++e) f[e] = gelu_f(f[e]);
+                    for (int e = 0; e < QW; ++e) f[e] = gelu(f[e]);
                 }
             }
             constexpr int SPQ = QW / EPS;                   // 16-byte slots per QW columns
