@@ -216,6 +216,7 @@ struct conv_plan {
     int pack, Go, Co, Ko;   // small-group packing factor and the caller's G, C, K
     int slab, slab_bws, slab_hr, slab_nkg, slab_nbg, slab_btaps, slab_sa, slab_sb, slab_a_stage, slab_resident;
     int overlap;            // launch as programmatic dependents (conv_plan_set_overlap)
+    int epi_warps;          // per-tap kernel epilogue warps (8 or 16)
     size_t slab_smem;
     // SIMT plan
     int BM, Kg, Kpad, nkt, ktps, vec;
@@ -376,7 +377,8 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     if (force_bn == 16 || force_bn == 32 || force_bn == 64 || force_bn == 128 || force_bn == 256) bn = force_bn;
     p->tf32 = tf32 ? 1 : 0;
     p->BN = bn;
-    p->stages = tc_stages_for(bn, p->tf32);
+    p->epi_warps = 8;
+    p->stages = tc_stages_for(bn, p->tf32, 8);
     p->cpt = g.C / 8;
     p->nchunks = g.taps * p->cpt;
     // Gather: TMA boxes when the tensor map can express the problem and a tap has at
@@ -436,7 +438,7 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     if (force_bn == 0 && p->nkb * (tf32 ? 3 : 1) <= 32) {
         while (bn > 32 && (int64_t)p->num_mt * g.G * cdiv(g.K, bn) * 4 < (int64_t)p->sm_count * 3) bn /= 2;
         p->BN = bn;
-        p->stages = tc_stages_for(bn, p->tf32);
+        p->stages = tc_stages_for(bn, p->tf32, 8);
     }
     p->num_nt = (int)cdiv(g.K, bn);
     const int64_t units = (int64_t)p->num_mt * g.G * p->num_nt;
@@ -477,6 +479,17 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     }
     p->kbps = (int)cdiv(p->nkb, splits);
     p->splits = (int)cdiv(p->nkb, p->kbps);     // every split non-empty
+    // Wide bf16 tiles with short reductions (few K blocks per tile, e.g. 128 -> 1280 channels
+    // at 3 taps) spend longer in the epilogue (bias, GELU, stores of BM x BN outputs) than in
+    // the MMAs: they get 16 epilogue warps (4 per TMEM lane quarter), one stage fewer.
+    if (!tf32 && p->tma && !p->slab && bn >= 128) {
+        const int force_ew = env_int("CONV_FORCE_EPI_WARPS", 0);
+        const bool wide_epi = force_ew ? force_ew == 16 : p->kbps <= 16;
+        if (wide_epi) {
+            p->epi_warps = 16;
+            p->stages = tc_stages_for(bn, p->tf32, 16);
+        }
+    }
     p->total_units = (int)(units * p->splits);
     p->grid = std::min(p->total_units, p->sm_count);
     p->prepack_bytes = (size_t)g.G * p->num_nt * p->nkb * bn * 128 * (tf32 ? 2 : 1);
@@ -491,9 +504,9 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     else if (p->tma)
         snprintf(p->desc, sizeof(p->desc),
                  "variant=%s gather=tma tile=128x%d pixels=%dx%d k_block=%d stages=%d splits=%d units=%d "
-                 "grid=%d k_blocks=%d map=%d",
+                 "grid=%d k_blocks=%d map=%d epi_warps=%d",
                  tf32 ? "tc_tf32x3" : "tc_bf16", bn, p->BH, p->BW, cblk, p->stages, p->splits, p->total_units,
-                 p->grid, p->nkb, p->map_kind);
+                 p->grid, p->nkb, p->map_kind, p->epi_warps);
     else
         snprintf(p->desc, sizeof(p->desc),
                  "variant=tc_bf16 gather=cp.async tile=128x%d k_block=64 stages=%d splits=%d units=%d grid=%d "
@@ -730,6 +743,7 @@ static conv_status run_forward(conv_plan_t plan, const void* x, const void* w_pa
         tp.slab_nbg = plan->slab_nbg; tp.slab_btaps = plan->slab_btaps; tp.slab_sa = plan->slab_sa;
         tp.slab_sb = plan->slab_sb; tp.slab_a_stage = plan->slab_a_stage; tp.slab_resident = plan->slab_resident;
         tp.pdl = plan->overlap;
+        tp.epi_warps = plan->epi_warps ? plan->epi_warps : 8;
         tp.f_splits = make_fastdiv(plan->splits); tp.f_num_nt = make_fastdiv(plan->num_nt);
         tp.f_G = make_fastdiv(plan->g.G); tp.f_tiles_w = make_fastdiv(plan->tiles_w);
         tp.f_tiles_h = make_fastdiv(plan->tiles_h); tp.f_Do = make_fastdiv(plan->g.Do);

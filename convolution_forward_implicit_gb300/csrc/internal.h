@@ -117,6 +117,7 @@ struct TcParams {
     int slab_resident;      // 1: the weights of one (group, N tile) stay in shared memory
     int slab_a_stage;       // bytes per slab stage (3xTF32: hi half then lo half)
     int pdl;                // 1: launched as a programmatic dependent (see griddep_wait)
+    int epi_warps;          // per-tap kernel: 8 or 16 epilogue warps
     // divisors of the per-tile index arithmetic
     FastDiv f_splits, f_num_nt, f_G, f_tiles_w, f_tiles_h, f_Do, f_Ho, f_Wo, f_cbt, f_cpt, f_X, f_YX, f_BW, f_bws;
 };
@@ -125,7 +126,7 @@ constexpr size_t SLAB_SMEM_MAX = 232448;   // dynamic shared memory a block may 
 
 // Launch the tensor-core kernel for the (BN, stages) pair the plan picked (see tc_stages_for).
 cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, int stages, int grid, cudaStream_t stream);
-int tc_stages_for(int BN, int tf32);
+int tc_stages_for(int BN, int tf32, int epi_warps);
 // Slab-mode kernel; smem from slab_smem_bytes.
 cudaError_t launch_slab(const TcParams& p, const CUtensorMap* act_map, int grid, size_t smem, cudaStream_t stream);
 size_t slab_smem_bytes(int BN, int tf32, int sa, int sb, size_t a_stage, int btaps);

@@ -289,9 +289,9 @@ constexpr int STG_WARP_BYTES = 32 * 128;   // one warp's staging buffer: 32 rows
 // Epilogue of one warp's 32 rows x [cb_begin, cb_end) accumulator columns (see the
 // epilogue role in the kernel).  ESZ is the stored element size: 2 for bf16 outputs, 4 for
 // fp32 outputs and for split-K partial sums.
-template <int BN, int ESZ>
+// Epilogue geometry of one warp that owns COLS accumulator columns of its 32 rows.
+template <int COLS, int ESZ>
 struct EpiShape {
-    static constexpr int COLS = BN / 2 < 16 ? 16 : BN / 2;
     static constexpr int CW = COLS < 128 / ESZ ? COLS : 128 / ESZ;   // columns per chunk
     static constexpr int RB = CW * ESZ;                             // bytes per row segment (32..128)
     static constexpr int LPR = RB / 16;                             // 16-byte slots (= store lanes) per row
@@ -303,9 +303,9 @@ constexpr int EPI_MAX_LPR = 8;
 // for rows outside the output.  Callers compute them before they wait for the accumulator:
 // the index arithmetic (divisions by the tile's extents) then overlaps the MMAs instead of
 // delaying the epilogue; the empty asm makes the values exist at that point.
-template <int BN, int ESZ, typename RowOffset>
+template <int COLS, int ESZ, typename RowOffset>
 __device__ __forceinline__ void epilogue_rows(int lane, int wq, RowOffset row_offset, long long (&roff)[EPI_MAX_LPR]) {
-    using S = EpiShape<BN, ESZ>;
+    using S = EpiShape<COLS, ESZ>;
 #pragma unroll
     for (int i = 0; i < S::LPR; ++i) {
         roff[i] = row_offset(wq * 32 + lane / S::LPR + S::RPI * i);
@@ -313,11 +313,14 @@ __device__ __forceinline__ void epilogue_rows(int lane, int wq, RowOffset row_of
     }
 }
 
-template <int BN, int ESZ>
+// One warp's share of a tile's epilogue: its 32 accumulator rows (TMEM lane quarter wq) and
+// the columns [cb_begin, cb_end) of the BN-wide tile, COLS of them at most.  QW32: read TMEM
+// 32 columns at a time where the chunk allows (fewer round trips, more registers).
+template <int BN, int COLS, int ESZ, bool QW32 = true>
 __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t taddr, int lane, int wq, int cb_begin,
                                                 int cb_end, int nt, int gi, int split, bool partial, bool add_bias,
                                                 bool do_gelu, uint8_t* stg, const long long (&roff)[EPI_MAX_LPR]) {
-    using S = EpiShape<BN, ESZ>;
+    using S = EpiShape<COLS, ESZ>;
     constexpr int CW = S::CW;
     constexpr int RB = S::RB;
     constexpr int LPR = S::LPR;
@@ -334,7 +337,7 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
         // QW columns per TMEM load (32 where the chunk allows): TMEM -> fp32 -> bias, GELU ->
         // this lane's row slots in staging
         // (fp32 outputs keep 16: the 3xTF32 kernels run 544 threads and have fewer registers)
-        constexpr int QW = (ESZ == 2 && CW % 32 == 0) ? 32 : 16;
+        constexpr int QW = (QW32 && ESZ == 2 && CW % 32 == 0) ? 32 : 16;
 #pragma unroll
         for (int q = 0; q < CW / QW; ++q) {
             const int nq = n0 + QW * q;

@@ -47,13 +47,13 @@ enum Kind { KIND_BF16_CPASYNC = 0, KIND_BF16_TMA = 1, KIND_TF32X3 = 2 };
 // same thread starts only when the first completes, ~700 cycles each), so the TMA producer
 // spreads its copies over 4 warps, pipeline stage s belonging to warp s % 4, where lane 0
 // copies the activation box and lane 1 the weight tile.
-template <int KIND>
+template <int KIND, int EW>
 struct Traits {
     static constexpr bool TMA = KIND != KIND_BF16_CPASYNC;
     static constexpr bool TF32 = KIND == KIND_TF32X3;
     static constexpr int PROD_WARPS = 4;
     static constexpr int CVT_WARPS = TF32 ? 4 : 0;
-    static constexpr int MMA_WARP = EPI_WARPS + PROD_WARPS;
+    static constexpr int MMA_WARP = EW + PROD_WARPS;
     static constexpr int CVT_WARP0 = MMA_WARP + 1;
     static constexpr int THREADS = (CVT_WARP0 + CVT_WARPS) * 32;
     static constexpr int PROD_THREADS = PROD_WARPS * 32;
@@ -64,15 +64,15 @@ struct Traits {
 template <int BN, int KIND>
 struct Cfg {
     static constexpr uint32_t B_TILE = BN * 128;
-    static constexpr uint32_t B_STAGE = Traits<KIND>::TF32 ? 2 * B_TILE : B_TILE;
+    static constexpr uint32_t B_STAGE = KIND == KIND_TF32X3 ? 2 * B_TILE : B_TILE;
     static constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;    // power of two for BN in {16..256}
 };
 
-template <int BN, int STAGES, int KIND>
-__global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
+template <int BN, int STAGES, int KIND, int EW>
+__global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
     conv_fwd_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map) {
     using C = Cfg<BN, KIND>;
-    using T = Traits<KIND>;
+    using T = Traits<KIND, EW>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
     const uint32_t sA = sbase;
     const uint32_t sB = sbase + STAGES * T::A_STAGE;
     constexpr uint32_t STG_OFFSET = STAGES * (T::A_STAGE + C::B_STAGE);       // epilogue staging
-    const uint32_t bar0 = sbase + STG_OFFSET + EPI_WARPS * STG_WARP_BYTES;
+    const uint32_t bar0 = sbase + STG_OFFSET + EW * STG_WARP_BYTES;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto cvt_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
@@ -102,14 +102,14 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), EPI_WARPS);
+            mbar_init(tempty_bar(a), EW);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
     }
-    if (T::TMA && warp == EPI_WARPS && lane == 0)
+    if (T::TMA && warp == EW && lane == 0)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&act_map)) : "memory");
     if (warp == T::MMA_WARP) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -126,11 +126,11 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
     const int GC = g.G * g.C;
     const int GK = g.G * g.K;
 
-    if (warp >= EPI_WARPS && warp < T::MMA_WARP) {
+    if (warp >= EW && warp < T::MMA_WARP) {
         const uint8_t* wp = reinterpret_cast<const uint8_t*>(p.wpack);
         if (T::TMA) {
             // -------------------------------------------------------- producer (TMA)
-            const int pw = warp - EPI_WARPS;
+            const int pw = warp - EW;
             if (lane < 2) {
                 const uint32_t a_tx = (uint32_t)(p.BW * p.BH) * 128u;
                 const int cblk = T::TF32 ? 32 : 64;     // channels in one 128-byte row
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
             __syncwarp();
         } else {
             // -------------------------------------------------------- producer (cp.async)
-            const int pt = threadIdx.x - EPI_WARPS * 32;
+            const int pt = threadIdx.x - EW * 32;
             const int j = pt & 7;        // 16-byte chunk of the 128-byte row
             const int rb = pt >> 3;      // rows rb, rb+16, ..., rb+112
             const uint32_t swz = (uint32_t)((j ^ (rb & 7)) << 4);
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
                 if (lane == 0) mbar_arrive(cvt_bar(s));
             }
         }
-    } else if (warp < EPI_WARPS) {
+    } else if (warp < EW) {
         // ------------------------------------------------------------ epilogue
         // Warp w owns the 32 accumulator rows of TMEM lane quarter w % 4 and half of the
         // columns.  It works in chunks of columns that make one output row segment of at most
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
         // store instruction writes 4 full 128-byte segments instead of 32 scattered 16-byte
         // pieces.  Split plans store fp32 partial sums to the workspace the same way.
         const int wq = warp & 3;
-        constexpr int COLS = BN / 2 < 16 ? 16 : BN / 2;
+        constexpr int COLS = BN / (EW / 4) < 16 ? 16 : BN / (EW / 4);   // EW/4 warps share a lane quarter
         const int cb_begin = (warp >> 2) * COLS;
         const int cb_end = cb_begin + COLS < BN ? cb_begin + COLS : BN;
         const bool partial = p.splits > 1;
@@ -392,16 +392,16 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
             };
             const bool wide = partial || T::TF32;     // fp32 stores
             long long roff[EPI_MAX_LPR];
-            if (wide) epilogue_rows<BN, 4>(lane, wq, row_offset, roff);
-            else epilogue_rows<BN, 2>(lane, wq, row_offset, roff);
+            if (wide) epilogue_rows<COLS, 4>(lane, wq, row_offset, roff);
+            else epilogue_rows<COLS, 2>(lane, wq, row_offset, roff);
             if (!wait_bar_warp(tfull_bar(acc), aph, abort_flag, p.err, (p.sleep_mask & 2) != 0)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
             if (wide)
-                epilogue_chunks<BN, 4>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
+                epilogue_chunks<BN, COLS, 4, EW == 8>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
                                        do_gelu, stg, roff);
             else
-                epilogue_chunks<BN, 2>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
+                epilogue_chunks<BN, COLS, 2, EW == 8>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
                                        do_gelu, stg, roff);
             tc_fence_before();
             __syncwarp();
@@ -417,16 +417,16 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1)
     }
 }
 
-template <int BN, int STAGES, int KIND>
+template <int BN, int STAGES, int KIND, int EW>
 constexpr size_t smem_bytes_for() {
-    return 1024 + (size_t)STAGES * (Traits<KIND>::A_STAGE + Cfg<BN, KIND>::B_STAGE) + EPI_WARPS * STG_WARP_BYTES +
+    return 1024 + (size_t)STAGES * (Traits<KIND, EW>::A_STAGE + Cfg<BN, KIND>::B_STAGE) + EW * STG_WARP_BYTES +
            8 * (3 * STAGES + 5) + 16;
 }
 
-template <int BN, int STAGES, int KIND>
+template <int BN, int STAGES, int KIND, int EW>
 cudaError_t launch_one(const TcParams& p, const CUtensorMap& map, int grid, cudaStream_t stream) {
-    auto kern = conv_fwd_tc_kernel<BN, STAGES, KIND>;
-    constexpr size_t smem = smem_bytes_for<BN, STAGES, KIND>();
+    auto kern = conv_fwd_tc_kernel<BN, STAGES, KIND, EW>;
+    constexpr size_t smem = smem_bytes_for<BN, STAGES, KIND, EW>();
     static_assert(smem <= 232448, "shared memory budget");
     // opt in to the large dynamic shared memory once per device (not inside graph capture)
     static bool attr_set[64];
@@ -440,18 +440,21 @@ cudaError_t launch_one(const TcParams& p, const CUtensorMap& map, int grid, cuda
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    return launch_kernel(kern, dim3(grid), dim3(Traits<KIND>::THREADS), smem, stream, p.pdl != 0, p, map);
+    return launch_kernel(kern, dim3(grid), dim3(Traits<KIND, EW>::THREADS), smem, stream, p.pdl != 0, p, map);
 }
 
 }  // namespace
 
-// (BN, stages) pairs compiled into the library, per kind; the plan picks one.
+// (BN, stages) pairs compiled into the library, per kind and epilogue width; the plan picks one.
 #define TC_BF16_CONFIGS(X) X(256, 4) X(128, 6) X(64, 8) X(32, 8) X(16, 8)
+#define TC_BF16_EPI16_CONFIGS(X) X(256, 3) X(128, 5)
 #define TC_TF32_CONFIGS(X) X(256, 2) X(128, 3) X(64, 4) X(32, 4) X(16, 5)
 
-int tc_stages_for(int BN, int tf32) {
+int tc_stages_for(int BN, int tf32, int epi_warps) {
 #define X(bn, st) if (BN == bn) return st;
-    if (tf32) { TC_TF32_CONFIGS(X) } else { TC_BF16_CONFIGS(X) }
+    if (tf32) { TC_TF32_CONFIGS(X) }
+    else if (epi_warps == 16) { TC_BF16_EPI16_CONFIGS(X) }
+    else { TC_BF16_CONFIGS(X) }
 #undef X
     return 0;
 }
@@ -461,17 +464,26 @@ cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, int stages,
     const CUtensorMap& map = act_map ? *act_map : unused;
     if (p.tma && !act_map) return cudaErrorInvalidValue;
     if (p.tf32) {
-        if (!p.tma) return cudaErrorInvalidValue;
+        if (!p.tma || p.epi_warps != 8) return cudaErrorInvalidValue;
 #define X(bn, st) \
-    if (p.BN == bn && stages == st) return launch_one<bn, st, KIND_TF32X3>(p, map, grid, stream);
+    if (p.BN == bn && stages == st) return launch_one<bn, st, KIND_TF32X3, 8>(p, map, grid, stream);
         TC_TF32_CONFIGS(X)
 #undef X
         return cudaErrorInvalidValue;
     }
+    if (p.epi_warps == 16) {
+        if (!p.tma) return cudaErrorInvalidValue;
+#define X(bn, st) \
+    if (p.BN == bn && stages == st) return launch_one<bn, st, KIND_BF16_TMA, 16>(p, map, grid, stream);
+        TC_BF16_EPI16_CONFIGS(X)
+#undef X
+        return cudaErrorInvalidValue;
+    }
+    if (p.epi_warps != 8) return cudaErrorInvalidValue;
 #define X(bn, st)                                                                              \
     if (p.BN == bn && stages == st)                                                            \
-        return p.tma ? launch_one<bn, st, KIND_BF16_TMA>(p, map, grid, stream)                 \
-                     : launch_one<bn, st, KIND_BF16_CPASYNC>(p, map, grid, stream);
+        return p.tma ? launch_one<bn, st, KIND_BF16_TMA, 8>(p, map, grid, stream)              \
+                     : launch_one<bn, st, KIND_BF16_CPASYNC, 8>(p, map, grid, stream);
     TC_BF16_CONFIGS(X)
 #undef X
     return cudaErrorInvalidValue;

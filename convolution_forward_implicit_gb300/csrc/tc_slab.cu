@@ -349,9 +349,9 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
     } else if (warp < EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
         const int wq = warp & 3;
-        constexpr int COLS = BN / 2 < 16 ? 16 : BN / 2;
-        const int cb_begin = (warp >> 2) * COLS;
-        const int cb_end = cb_begin + COLS < BN ? cb_begin + COLS : BN;
+        constexpr int SCOLS = BN / 2 < 16 ? 16 : BN / 2;   // two warps per TMEM lane quarter
+        const int cb_begin = (warp >> 2) * SCOLS;
+        const int cb_end = cb_begin + SCOLS < BN ? cb_begin + SCOLS : BN;
         const bool add_bias = p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU;
         const bool do_gelu = p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU;
         uint8_t* stg = smem + stg_off + warp * STG_WARP_BYTES;
@@ -371,16 +371,16 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
                 return (long long)(((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow) * (g.G * g.K);
             };
             long long roff[EPI_MAX_LPR];
-            if (TF32) epilogue_rows<BN, 4>(lane, wq, row_offset, roff);
-            else epilogue_rows<BN, 2>(lane, wq, row_offset, roff);
+            if (TF32) epilogue_rows<SCOLS, 4>(lane, wq, row_offset, roff);
+            else epilogue_rows<SCOLS, 2>(lane, wq, row_offset, roff);
             if (!wait_bar_warp(tfull_bar(acc), aph, abort_flag, p.err, (p.sleep_mask & 2) != 0)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
             if (TF32)
-                epilogue_chunks<BN, 4>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, 0, false, add_bias, do_gelu, stg,
+                epilogue_chunks<BN, SCOLS, 4>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, 0, false, add_bias, do_gelu, stg,
                                        roff);
             else
-                epilogue_chunks<BN, 2>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, 0, false, add_bias, do_gelu, stg,
+                epilogue_chunks<BN, SCOLS, 2>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, 0, false, add_bias, do_gelu, stg,
                                        roff);
             tc_fence_before();
             __syncwarp();

@@ -421,3 +421,17 @@ def test_slab_mode_streamed_weights(name):
     assert "tma-slab" in desc and "w " not in desc, desc
     ref, S = oracle_full(layer, dtype, x, w, b)
     assert_within(dtype, layer.epilogue, got, ref, S, desc)
+
+
+@pytest.mark.parametrize("epi_warps", [8, 16])
+@pytest.mark.parametrize("bn", [128, 256])
+def test_per_tap_epilogue_widths(epi_warps, bn):
+    """The per-tap kernel with 8 or 16 epilogue warps (2 or 4 per TMEM lane quarter), bias and
+    GELU, several tiles per CTA and a ragged last tile."""
+    layer = L(1, 3, 1, 128, 640, (1000,), (3,), (1,), (1,), (1,), CONV_EPI_BIAS_GELU)
+    x, w, b = make_inputs(layer, "bf16", 1900 + epi_warps + bn)
+    got, desc = run_gpu(layer, "bf16", x, w, b, env={"CONV_FORCE_EPI_WARPS": epi_warps, "CONV_FORCE_BN": bn,
+                                                    "CONV_FORCE_SPLITK": 1, "CONV_FORCE_GATHER": "tma"}, guard=64)
+    assert f"tile=128x{bn}" in desc and f"epi_warps={epi_warps}" in desc, desc
+    ref, S = oracle_full(layer, "bf16", x, w, b)
+    assert_within("bf16", layer.epilogue, got, ref, S, desc)
