@@ -42,7 +42,11 @@ struct SlabRoles {
     static constexpr int THREADS = (CVT_WARP0 + CVT_WARPS) * 32;
 };
 
-template <int BN, bool TF32>
+// BY, BT: filter rows Y (weight stages per k-group) and columns X (taps per stage) fixed at
+// compile time for the common 3x3 and 1x3 filters, so the MMA issue loop over a k-group's taps
+// unrolls with constant descriptor offsets; 0 reads them from the parameters.  Measured on
+// 3x3 filters: the unrolled issue loop makes the whole kernel 1.2x (2D) to 1.3x (3D) faster.
+template <int BN, bool TF32, int BY, int BT>
 __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
     conv_fwd_slab_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map) {
     using R = SlabRoles<TF32>;
@@ -117,8 +121,8 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
 
     const Geom& g = p.g;
     const int cblk = TF32 ? 32 : 64;
-    const int nbg = p.slab_nbg;          // weight stages per k-group (filter rows)
-    const int btaps = p.slab_btaps;      // taps per weight stage (filter columns)
+    const int nbg = BY > 0 ? BY : p.slab_nbg;        // weight stages per k-group (filter rows)
+    const int btaps = BT > 0 ? BT : p.slab_btaps;   // taps per weight stage (filter columns)
 
     if (warp == R::A_WARP) {
         // ------------------------------------------------------------ slab copies
@@ -396,9 +400,9 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
     }
 }
 
-template <int BN, bool TF32>
+template <int BN, bool TF32, int BY, int BT>
 cudaError_t launch_slab_one(const TcParams& p, const CUtensorMap& map, int grid, size_t smem, cudaStream_t stream) {
-    auto kern = conv_fwd_slab_kernel<BN, TF32>;
+    auto kern = conv_fwd_slab_kernel<BN, TF32, BY, BT>;
     static bool attr_set[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -425,10 +429,14 @@ cudaError_t launch_slab(const TcParams& p, const CUtensorMap* act_map, int grid,
     if (!act_map || p.slab_sa < 2 || p.slab_sa > SLAB_MAX_SA ||
         (!p.slab_resident && (p.slab_sb < 2 || p.slab_sb > SLAB_MAX_SB)) || smem > SLAB_SMEM_MAX)
         return cudaErrorInvalidValue;
-#define X(bn)                                                                                    \
-    if (p.BN == bn)                                                                              \
-        return p.tf32 ? launch_slab_one<bn, true>(p, *act_map, grid, smem, stream)               \
-                      : launch_slab_one<bn, false>(p, *act_map, grid, smem, stream);
+// (3xTF32 keeps the generic loop: unrolled, its 12 MMAs per tap measured slower.)
+#define X(bn)                                                                                                \
+    if (p.BN == bn) {                                                                                        \
+        if (p.tf32) return launch_slab_one<bn, true, 0, 0>(p, *act_map, grid, smem, stream);                \
+        if (p.slab_btaps == 3 && p.slab_nbg == 3) return launch_slab_one<bn, false, 3, 3>(p, *act_map, grid, smem, stream); \
+        if (p.slab_btaps == 3 && p.slab_nbg == 1) return launch_slab_one<bn, false, 1, 3>(p, *act_map, grid, smem, stream); \
+        return launch_slab_one<bn, false, 0, 0>(p, *act_map, grid, smem, stream);                           \
+    }
     X(16) X(32) X(64) X(128) X(256)
 #undef X
     return cudaErrorInvalidValue;
