@@ -215,6 +215,7 @@ struct conv_plan {
     int tma, map_kind, BW, BH, tiles_w, tiles_h, cbt, tf32, sleep_mask;
     int pack, Go, Co, Ko;   // small-group packing factor and the caller's G, C, K
     int slab, slab_bws, slab_hr, slab_nkg, slab_nbg, slab_btaps, slab_sa, slab_sb, slab_a_stage, slab_resident;
+    int slab_nacc, slab_pair_rows, acc_bh;   // tile pairs (see set_slab_pair)
     int overlap;            // launch as programmatic dependents (conv_plan_set_overlap)
     int epi_warps;          // per-tap kernel epilogue warps (8 or 16)
     size_t slab_smem;
@@ -346,7 +347,7 @@ static bool choose_slab_shape(conv_plan* p) {
     const int bh = std::max(1, std::min(g.Ho, 128 / bws));
     const int hr = bh + reach_h;
     if (bws > 256 || hr > 256) return false;
-    p->BW = bw; p->BH = bh;
+    p->BW = bw; p->BH = bh; p->acc_bh = bh; p->slab_nacc = 1; p->slab_pair_rows = 0;
     p->tiles_w = (int)cdiv(g.Wo, bw);
     p->tiles_h = (int)cdiv(g.Ho, bh);
     p->slab_bws = bws; p->slab_hr = hr;
@@ -354,6 +355,29 @@ static bool choose_slab_shape(conv_plan* p) {
     // a window may read up to reach_h*bws + reach_w + 128 rows from the stage start
     const int64_t rows = std::max<int64_t>((int64_t)reach_h * bws + reach_w + 128, (int64_t)hr * bws);
     p->slab_a_stage = (int)(cdiv(rows * 128, 1024) * 1024 * (p->tf32 ? 2 : 1));
+    return true;
+}
+
+// Slab geometry with one accumulator per unit (pair = false) or two stacked along H (pair =
+// true): the unit covers 2 x acc_bh output rows and its slab the rows of both plus the filter's
+// reach.  Returns false where the pair's box would exceed the 256-row TMA box limit.
+static bool set_slab_pair(conv_plan* p, bool pair) {
+    const Geom& g = p->g;
+    const int reach_w = g.dw * (g.X - 1), reach_h = g.dh * (g.Y - 1);
+    const int n = pair ? 2 : 1;
+    const int hr = n * p->acc_bh + reach_h;
+    if (hr > 256) return false;
+    p->slab_nacc = n;
+    p->BH = n * p->acc_bh;
+    p->tiles_h = (int)cdiv(g.Ho, p->BH);
+    p->slab_hr = hr;
+    p->slab_pair_rows = pair ? p->acc_bh * p->slab_bws : 0;
+    // the last window of the last accumulator starts at pair_rows + reach_h*bws + reach_w and
+    // reads 128 rows
+    const int64_t rows = std::max<int64_t>((int64_t)p->slab_pair_rows + (int64_t)reach_h * p->slab_bws + reach_w + 128,
+                                           (int64_t)hr * p->slab_bws);
+    p->slab_a_stage = (int)(cdiv(rows * 128, 1024) * 1024 * (p->tf32 ? 2 : 1));
+    p->num_mt = g.N * g.Do * p->tiles_h * p->tiles_w;
     return true;
 }
 
@@ -441,7 +465,7 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
         p->stages = tc_stages_for(bn, p->tf32, 8);
     }
     p->num_nt = (int)cdiv(g.K, bn);
-    const int64_t units = (int64_t)p->num_mt * g.G * p->num_nt;
+    int64_t units = (int64_t)p->num_mt * g.G * p->num_nt;
     int splits = 1;
     if (units * 2 < p->sm_count && p->nkb >= 4) {
         splits = (int)std::min<int64_t>(p->sm_count / units, p->nkb / 2);
@@ -455,22 +479,38 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
         // ring of weight stages
         p->slab_nkg = g.Z * p->cbt;
         const int nchunk = p->slab_nkg * p->slab_nbg;
-        p->slab_sa = 2;
-        p->slab_sb = 0;
-        p->slab_resident = 0;
-        for (int sa = 3; sa >= 2 && !p->slab_resident; --sa)
-            if (env_int("CONV_FORCE_SLAB_STREAM", 0) == 0 &&
-                slab_smem_bytes(bn, p->tf32, sa, nchunk, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
-                p->slab_resident = 1;
-                p->slab_sa = sa;
-                p->slab_sb = nchunk;
-            }
-        for (int sb = 8; sb >= 2 && !p->slab_resident; --sb)
-            if (slab_smem_bytes(bn, p->tf32, 2, sb, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
-                p->slab_sb = sb;
-                break;
-            }
-        if (splits > 1 || (!p->slab_resident && p->slab_sb < 2)) {
+        auto fit_rings = [&]() {
+            p->slab_sa = 2;
+            p->slab_sb = 0;
+            p->slab_resident = 0;
+            for (int sa = 3; sa >= 2 && !p->slab_resident; --sa)
+                if (env_int("CONV_FORCE_SLAB_STREAM", 0) == 0 &&
+                    slab_smem_bytes(bn, p->tf32, sa, nchunk, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
+                    p->slab_resident = 1;
+                    p->slab_sa = sa;
+                    p->slab_sb = nchunk;
+                }
+            for (int sb = 8; sb >= 2 && !p->slab_resident; --sb)
+                if (slab_smem_bytes(bn, p->tf32, 2, sb, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
+                    p->slab_sb = sb;
+                    break;
+                }
+            return p->slab_resident || p->slab_sb >= 2;
+        };
+        // Tile pairs (bf16, N tile <= 64, several units per CTA, more than one row block):
+        // two accumulators per unit, stacked along H, share one slab and one weight pass.
+        set_slab_pair(p, false);
+        const int force_pair = env_int("CONV_FORCE_SLAB_PAIR", -1);
+        const bool want_pair = !tf32 && bn <= 64 && splits == 1 && g.Ho > p->acc_bh &&
+                               (force_pair >= 0 ? force_pair == 1 : units >= 4LL * p->sm_count);
+        bool fits = false;
+        if (want_pair && set_slab_pair(p, true)) {
+            fits = fit_rings();
+            if (!fits) set_slab_pair(p, false);
+        }
+        if (!fits) fits = fit_rings();
+        units = (int64_t)p->num_mt * g.G * p->num_nt;
+        if (splits > 1 || !fits) {
             p->slab = 0;                               // back to per-tap boxes
             choose_tile_shape(p);
             return plan_tc_per_tap_retry(p, tf32);
@@ -496,11 +536,11 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     p->workspace_bytes = p->splits > 1 ? (size_t)p->splits * g.M * g.G * g.K * sizeof(float) : 0;
     if (p->slab)
         snprintf(p->desc, sizeof(p->desc),
-                 "variant=%s gather=tma-slab tile=128x%d pixels=%dx%d slab=%dx%d k_block=%d stages=%d+%d%s splits=1 "
-                 "units=%d grid=%d k_blocks=%d map=%d",
-                 tf32 ? "tc_tf32x3" : "tc_bf16", bn, p->BH, p->BW, p->slab_hr, p->slab_bws, cblk, p->slab_sa,
-                 p->slab_resident ? 1 : p->slab_sb, p->slab_resident ? "w" : "", p->total_units, p->grid, p->nkb,
-                 p->map_kind);
+                 "variant=%s gather=tma-slab tile=%dx%d pixels=%dx%d slab=%dx%d k_block=%d stages=%d+%d%s splits=1 "
+                 "units=%d grid=%d k_blocks=%d map=%d acc=%d",
+                 tf32 ? "tc_tf32x3" : "tc_bf16", 128 * p->slab_nacc, bn, p->BH, p->BW, p->slab_hr, p->slab_bws, cblk,
+                 p->slab_sa, p->slab_resident ? 1 : p->slab_sb, p->slab_resident ? "w" : "", p->total_units, p->grid,
+                 p->nkb, p->map_kind, p->slab_nacc);
     else if (p->tma)
         snprintf(p->desc, sizeof(p->desc),
                  "variant=%s gather=tma tile=128x%d pixels=%dx%d k_block=%d stages=%d splits=%d units=%d "
@@ -742,6 +782,8 @@ static conv_status run_forward(conv_plan_t plan, const void* x, const void* w_pa
         tp.slab = plan->slab; tp.slab_bws = plan->slab_bws; tp.slab_hr = plan->slab_hr; tp.slab_nkg = plan->slab_nkg;
         tp.slab_nbg = plan->slab_nbg; tp.slab_btaps = plan->slab_btaps; tp.slab_sa = plan->slab_sa;
         tp.slab_sb = plan->slab_sb; tp.slab_a_stage = plan->slab_a_stage; tp.slab_resident = plan->slab_resident;
+        tp.slab_nacc = plan->slab ? plan->slab_nacc : 1; tp.slab_pair_rows = plan->slab_pair_rows;
+        tp.acc_bh = plan->slab ? plan->acc_bh : plan->BH;
         tp.pdl = plan->overlap;
         tp.epi_warps = plan->epi_warps ? plan->epi_warps : 8;
         tp.f_splits = make_fastdiv(plan->splits); tp.f_num_nt = make_fastdiv(plan->num_nt);

@@ -115,6 +115,9 @@ struct TcParams {
     int slab_btaps;         // taps per weight stage (filter columns X)
     int slab_sa, slab_sb;   // slab ring and weight ring stages (resident: weight chunks held)
     int slab_resident;      // 1: the weights of one (group, N tile) stay in shared memory
+    int slab_nacc;          // accumulators per unit: 1, or 2 (two tiles stacked along H)
+    int slab_pair_rows;     // slab row of the second accumulator's windows (acc_bh * BWs)
+    int acc_bh;             // output rows per accumulator (BH / slab_nacc)
     int slab_a_stage;       // bytes per slab stage (3xTF32: hi half then lo half)
     int pdl;                // 1: launched as a programmatic dependent (see griddep_wait)
     int epi_warps;          // per-tap kernel: 8 or 16 epilogue warps

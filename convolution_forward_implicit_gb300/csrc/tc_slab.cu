@@ -46,12 +46,17 @@ struct SlabRoles {
 // compile time for the common 3x3 and 1x3 filters, so the MMA issue loop over a k-group's taps
 // unrolls with constant descriptor offsets; 0 reads them from the parameters.  Measured on
 // 3x3 filters: the unrolled issue loop makes the whole kernel 1.2x (2D) to 1.3x (3D) faster.
-template <int BN, bool TF32, int BY, int BT>
+//
+// NACC: accumulators per unit.  With 2 (tile pairs), a unit is two output tiles stacked along
+// H that share one slab (their halo rows once) and one pass over the weights: every tap issues
+// its MMAs into both accumulators from windows slab_pair_rows apart, against the same weight
+// tile.  The per-unit waits, commits and copies then serve twice the MMAs.
+template <int BN, bool TF32, int BY, int BT, int NACC>
 __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
     conv_fwd_slab_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map) {
     using R = SlabRoles<TF32>;
     constexpr uint32_t B_TILE = BN * 128;
-    constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+    constexpr uint32_t TMEM_COLS = (2 * NACC * BN < 32) ? 32 : 2 * NACC * BN;   // 2 buffers of NACC accumulators
     const int SA = p.slab_sa, SB = p.slab_sb;
     const uint32_t a_stage = (uint32_t)p.slab_a_stage;           // TF32: hi half, then lo half
     const uint32_t a_half = TF32 ? a_stage / 2 : a_stage;
@@ -251,7 +256,7 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
                 }
             }
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * NACC * BN);
             uint32_t first = 1;
             for (int kg = 0; kg < p.slab_nkg && !aborted; ++kg, ra.next()) {
                 const int sa = ra.s;
@@ -280,22 +285,26 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
                     }
                     for (int t = 0; t < btaps; ++t) {
                         const uint32_t row = (uint32_t)(bg * g.dh * p.slab_bws + t * g.dw);
-                        const uint32_t a_addr = a0 + row * 128u;
-                        const uint64_t ad = sw128_desc(a_addr);
                         const uint64_t bd = sw128_desc(b0 + t * b_tap);
-                        if (TF32) {
-                            const uint64_t alo = sw128_desc(a_addr + a_half);
-                            const uint64_t blo = bd + (B_TILE >> 4);
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                mma_tf32_warp(d_tmem, alo + 2u * k, bd + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
-                                mma_tf32_warp(d_tmem, ad + 2u * k, blo + 2u * k, IDESC, 1u);
-                                mma_tf32_warp(d_tmem, ad + 2u * k, bd + 2u * k, IDESC, 1u);
+                        for (int j = 0; j < NACC; ++j) {
+                            const uint32_t a_addr = a0 + (row + (uint32_t)(j * p.slab_pair_rows)) * 128u;
+                            const uint64_t ad = sw128_desc(a_addr);
+                            const uint32_t dj = d_tmem + (uint32_t)(j * BN);
+                            if (TF32) {
+                                const uint64_t alo = sw128_desc(a_addr + a_half);
+                                const uint64_t blo = bd + (B_TILE >> 4);
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    mma_tf32_warp(dj, alo + 2u * k, bd + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
+                                    mma_tf32_warp(dj, ad + 2u * k, blo + 2u * k, IDESC, 1u);
+                                    mma_tf32_warp(dj, ad + 2u * k, bd + 2u * k, IDESC, 1u);
+                                }
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    mma_bf16_warp(dj, ad + 2u * k, bd + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
                             }
-                        } else {
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                mma_bf16_warp(d_tmem, ad + 2u * k, bd + 2u * k, IDESC, (first && k == 0) ? 0u : 1u);
                         }
                         first = 0;
                     }
@@ -367,25 +376,32 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
             const int acc = tile_i & 1;
             const uint32_t aph = (tile_i >> 1) & 1u;
             const TileOrigin to = tile_origin(p, mt);
-            // output pixel of accumulator row rr (row pitch BWs), or -1 if it is not stored
-            auto row_offset = [&](int rr) -> long long {
-                const int rh = fdiv(rr, p.f_bws), rw = rr - rh * p.slab_bws;
-                const int oh = to.oh0 + rh, ow = to.ow0 + rw;
-                if (rh >= p.BH || rw >= p.BW || oh >= g.Ho || ow >= g.Wo) return -1;
-                return (long long)(((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow) * (g.G * g.K);
-            };
-            long long roff[EPI_MAX_LPR];
-            if (TF32) epilogue_rows<SCOLS, 4>(lane, wq, row_offset, roff);
-            else epilogue_rows<SCOLS, 2>(lane, wq, row_offset, roff);
+            // output pixel of row rr (row pitch BWs) of accumulator j (acc_bh output rows each),
+            // or -1 if it is not stored
+            long long roff[NACC][EPI_MAX_LPR];
+#pragma unroll
+            for (int j = 0; j < NACC; ++j) {
+                auto row_offset = [&](int rr) -> long long {
+                    const int rh = fdiv(rr, p.f_bws), rw = rr - rh * p.slab_bws;
+                    const int oh = to.oh0 + j * p.acc_bh + rh, ow = to.ow0 + rw;
+                    if (rh >= p.acc_bh || rw >= p.BW || oh >= g.Ho || ow >= g.Wo) return -1;
+                    return (long long)(((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow) * (g.G * g.K);
+                };
+                if (TF32) epilogue_rows<SCOLS, 4>(lane, wq, row_offset, roff[j]);
+                else epilogue_rows<SCOLS, 2>(lane, wq, row_offset, roff[j]);
+            }
             if (!wait_bar_warp(tfull_bar(acc), aph, abort_flag, p.err, (p.sleep_mask & 2) != 0)) break;
             tc_fence_after();
-            const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
-            if (TF32)
-                epilogue_chunks<BN, SCOLS, 4>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, 0, false, add_bias, do_gelu, stg,
-                                       roff);
-            else
-                epilogue_chunks<BN, SCOLS, 2>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, 0, false, add_bias, do_gelu, stg,
-                                       roff);
+#pragma unroll
+            for (int j = 0; j < NACC; ++j) {
+                const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)((acc * NACC + j) * BN);
+                if (TF32)
+                    epilogue_chunks<BN, SCOLS, 4>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, 0, false, add_bias,
+                                                  do_gelu, stg, roff[j]);
+                else
+                    epilogue_chunks<BN, SCOLS, 2>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, 0, false, add_bias,
+                                                  do_gelu, stg, roff[j]);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -400,9 +416,9 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
     }
 }
 
-template <int BN, bool TF32, int BY, int BT>
+template <int BN, bool TF32, int BY, int BT, int NACC = 1>
 cudaError_t launch_slab_one(const TcParams& p, const CUtensorMap& map, int grid, size_t smem, cudaStream_t stream) {
-    auto kern = conv_fwd_slab_kernel<BN, TF32, BY, BT>;
+    auto kern = conv_fwd_slab_kernel<BN, TF32, BY, BT, NACC>;
     static bool attr_set[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -429,10 +445,20 @@ cudaError_t launch_slab(const TcParams& p, const CUtensorMap* act_map, int grid,
     if (!act_map || p.slab_sa < 2 || p.slab_sa > SLAB_MAX_SA ||
         (!p.slab_resident && (p.slab_sb < 2 || p.slab_sb > SLAB_MAX_SB)) || smem > SLAB_SMEM_MAX)
         return cudaErrorInvalidValue;
-// (3xTF32 keeps the generic loop: unrolled, its 12 MMAs per tap measured slower.)
+// (3xTF32 keeps the generic loop: unrolled, its 12 MMAs per tap measured slower; tile pairs
+// are bf16 only, for N tiles up to 64: wider ones run out of registers for two accumulators'
+// row offsets.)
 #define X(bn)                                                                                                \
     if (p.BN == bn) {                                                                                        \
-        if (p.tf32) return launch_slab_one<bn, true, 0, 0>(p, *act_map, grid, smem, stream);                \
+        if (p.tf32) return p.slab_nacc == 1 ? launch_slab_one<bn, true, 0, 0>(p, *act_map, grid, smem, stream) \
+                                             : cudaErrorInvalidValue;                                        \
+        if (p.slab_nacc == 2) {                                                                              \
+            if (bn > 64) return cudaErrorInvalidValue;                                                       \
+            if (p.slab_btaps == 3 && p.slab_nbg == 3)                                                        \
+                return launch_slab_one<bn, false, 3, 3, (bn > 64 ? 1 : 2)>(p, *act_map, grid, smem, stream); \
+            return launch_slab_one<bn, false, 0, 0, (bn > 64 ? 1 : 2)>(p, *act_map, grid, smem, stream);    \
+        }                                                                                                    \
+        if (p.slab_nacc != 1) return cudaErrorInvalidValue;                                                  \
         if (p.slab_btaps == 3 && p.slab_nbg == 3) return launch_slab_one<bn, false, 3, 3>(p, *act_map, grid, smem, stream); \
         if (p.slab_btaps == 3 && p.slab_nbg == 1) return launch_slab_one<bn, false, 1, 3>(p, *act_map, grid, smem, stream); \
         return launch_slab_one<bn, false, 0, 0>(p, *act_map, grid, smem, stream);                           \

@@ -435,3 +435,21 @@ def test_per_tap_epilogue_widths(epi_warps, bn):
     assert f"tile=128x{bn}" in desc and f"epi_warps={epi_warps}" in desc, desc
     ref, S = oracle_full(layer, "bf16", x, w, b)
     assert_within("bf16", layer.epilogue, got, ref, S, desc)
+
+
+PAIR_CASES = ["2d_d1", "2d_d2_nopad", "2d_5x3_c128", "3d_d2", "2d_map1_g2_c72", "packed_g32_c8",
+              "2d_weight_reload_g3"]
+
+
+@pytest.mark.parametrize("stream", [0, 1])
+@pytest.mark.parametrize("name", PAIR_CASES)
+def test_slab_tile_pairs(name, stream):
+    """Slab units of two tiles stacked along H (two accumulators sharing one slab and one
+    weight pass), with the last unit's second tile partly or wholly outside the output."""
+    dtype, layer = next((d, l) for n, d, l in SLAB if n == name)
+    x, w, b = make_inputs(layer, dtype, 2100 + zlib.crc32(name.encode()) % 500 + stream)
+    env = {"CONV_FORCE_SPLITK": 1, "CONV_FORCE_SLAB_PAIR": 1, "CONV_FORCE_SLAB_STREAM": stream}
+    got, desc = run_gpu(layer, dtype, x, w, b, env=env, guard=64)
+    assert "tma-slab" in desc and "acc=2" in desc, desc
+    ref, S = oracle_full(layer, dtype, x, w, b)
+    assert_within(dtype, layer.epilogue, got, ref, S, desc)
