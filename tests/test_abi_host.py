@@ -176,6 +176,7 @@ def test_tile_and_split_choice_fill_the_gpu(lib):
             assert 0.75 * 152 <= int(d["units"]) <= 152, d
     big = WORKLOADS["grouped3d_g4_c64_d1"].layers[0]
     d = desc_of(big, B.CONV_BF16)
-    assert d["splits"] == "1" and d["tile"] == "128x64"
+    # the 3D layer has thousands of tiles: whole reductions, 64-wide N tiles, paired along H
+    assert d["splits"] == "1" and d["tile"] == "256x64" and d["acc"] == "2", d
     d = desc_of(WORKLOADS["sweep_bf16_n32"].layers[1], B.CONV_BF16)
     assert d["tile"] == "128x256"
