@@ -218,6 +218,7 @@ struct conv_plan {
     int slab_nacc, slab_pair_rows, acc_bh;   // tile pairs (see set_slab_pair)
     int overlap;            // launch as programmatic dependents (conv_plan_set_overlap)
     int epi_warps;          // per-tap kernel epilogue warps (8 or 16)
+    int cluster_red;        // split-K partials summed inside a cluster (no workspace, no reduce kernel)
     size_t slab_smem;
     // SIMT plan
     int BM, Kg, Kpad, nkt, ktps, vec;
@@ -533,7 +534,13 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     p->total_units = (int)(units * p->splits);
     p->grid = std::min(p->total_units, p->sm_count);
     p->prepack_bytes = (size_t)g.G * p->num_nt * p->nkb * bn * 128 * (tf32 ? 2 : 1);
-    p->workspace_bytes = p->splits > 1 ? (size_t)p->splits * g.M * g.G * g.K * sizeof(float) : 0;
+    // Split-K plans whose units all run at once (one per CTA) sum their partials inside a
+    // thread-block cluster through distributed shared memory: no workspace, no second kernel.
+    p->cluster_red = 0;
+    if (p->splits >= 2 && p->splits <= 8 && (128 % p->splits) == 0 && p->total_units <= p->sm_count &&
+        g.K % 4 == 0 && env_int("CONV_FORCE_CLUSTER_RED", 1) != 0)
+        p->cluster_red = 1;
+    p->workspace_bytes = (p->splits > 1 && !p->cluster_red) ? (size_t)p->splits * g.M * g.G * g.K * sizeof(float) : 0;
     if (p->slab)
         snprintf(p->desc, sizeof(p->desc),
                  "variant=%s gather=tma-slab tile=%dx%d pixels=%dx%d slab=%dx%d k_block=%d stages=%d+%d%s splits=1 "
@@ -544,9 +551,10 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     else if (p->tma)
         snprintf(p->desc, sizeof(p->desc),
                  "variant=%s gather=tma tile=128x%d pixels=%dx%d k_block=%d stages=%d splits=%d units=%d "
-                 "grid=%d k_blocks=%d map=%d epi_warps=%d",
+                 "grid=%d k_blocks=%d map=%d epi_warps=%d reduce=%s",
                  tf32 ? "tc_tf32x3" : "tc_bf16", bn, p->BH, p->BW, cblk, p->stages, p->splits, p->total_units,
-                 p->grid, p->nkb, p->map_kind, p->epi_warps);
+                 p->grid, p->nkb, p->map_kind, p->epi_warps,
+                 p->splits == 1 ? "none" : p->cluster_red ? "cluster" : "kernel");
     else
         snprintf(p->desc, sizeof(p->desc),
                  "variant=tc_bf16 gather=cp.async tile=128x%d k_block=64 stages=%d splits=%d units=%d grid=%d "
@@ -739,11 +747,11 @@ static conv_status launch_reduce(conv_plan_t plan, const float* ws, const void* 
     const bool pdl = plan->overlap != 0;
     cudaError_t e;
     if (plan->dtype == CONV_BF16)
-        e = launch_kernel(splitk_reduce_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, s, pdl, ws,
+        e = launch_kernel(splitk_reduce_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, s, pdl, 1, ws,
                           plan->splits, MGK, g.G * g.K, static_cast<const __nv_bfloat16*>(bias),
                           static_cast<__nv_bfloat16*>(y), (int)plan->epi, (int)pdl);
     else
-        e = launch_kernel(splitk_reduce_kernel<float>, dim3(blocks), dim3(threads), 0, s, pdl, ws, plan->splits, MGK,
+        e = launch_kernel(splitk_reduce_kernel<float>, dim3(blocks), dim3(threads), 0, s, pdl, 1, ws, plan->splits, MGK,
                           g.G * g.K, static_cast<const float*>(bias), static_cast<float*>(y), (int)plan->epi,
                           (int)pdl);
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
@@ -786,6 +794,7 @@ static conv_status run_forward(conv_plan_t plan, const void* x, const void* w_pa
         tp.acc_bh = plan->slab ? plan->acc_bh : plan->BH;
         tp.pdl = plan->overlap;
         tp.epi_warps = plan->epi_warps ? plan->epi_warps : 8;
+        tp.cluster_red = plan->cluster_red;
         tp.f_splits = make_fastdiv(plan->splits); tp.f_num_nt = make_fastdiv(plan->num_nt);
         tp.f_G = make_fastdiv(plan->g.G); tp.f_tiles_w = make_fastdiv(plan->tiles_w);
         tp.f_tiles_h = make_fastdiv(plan->tiles_h); tp.f_Do = make_fastdiv(plan->g.Do);
@@ -808,7 +817,7 @@ static conv_status run_forward(conv_plan_t plan, const void* x, const void* w_pa
         e = launch_simt(sp, plan->dtype == CONV_BF16, plan->BM, plan->vec != 0, s);
     }
     if (e != cudaSuccess) return CONV_ERR_CUDA;
-    if (plan->splits > 1) return launch_reduce(plan, ws, needs_bias ? bias : nullptr, y, s);
+    if (plan->splits > 1 && !plan->cluster_red) return launch_reduce(plan, ws, needs_bias ? bias : nullptr, y, s);
     return CONV_OK;
 }
 

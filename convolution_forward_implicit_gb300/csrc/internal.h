@@ -57,22 +57,31 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 #endif
 
 // Launch a kernel, as a programmatic dependent of the previous kernel on the stream when
-// pdl is set.
+// pdl is set; with cluster_x > 1, as thread-block clusters of cluster_x consecutive CTAs.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                                 bool pdl, Args&&... args) {
+                                 bool pdl, int cluster_x, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
     if (pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
     }
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
@@ -121,6 +130,8 @@ struct TcParams {
     int slab_a_stage;       // bytes per slab stage (3xTF32: hi half then lo half)
     int pdl;                // 1: launched as a programmatic dependent (see griddep_wait)
     int epi_warps;          // per-tap kernel: 8 or 16 epilogue warps
+    int cluster_red;        // 1: the splits of a tile run as one cluster and sum their partial
+                            // accumulators through distributed shared memory (no workspace)
     // divisors of the per-tile index arithmetic
     FastDiv f_splits, f_num_nt, f_G, f_tiles_w, f_tiles_h, f_Do, f_Ho, f_Wo, f_cbt, f_cpt, f_X, f_YX, f_BW, f_bws;
 };

@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(THREADS) conv_fwd_simt_kernel(const __grid_con
 template <typename T, int BM, bool VEC>
 cudaError_t launch_t(const SimtParams& p, cudaStream_t stream) {
     dim3 grid(p.num_mt, p.num_nt, p.g.G * p.splits);
-    return launch_kernel(conv_fwd_simt_kernel<T, BM, VEC>, grid, dim3(THREADS), 0, stream, p.pdl != 0, p);
+    return launch_kernel(conv_fwd_simt_kernel<T, BM, VEC>, grid, dim3(THREADS), 0, stream, p.pdl != 0, 1, p);
 }
 
 }  // namespace

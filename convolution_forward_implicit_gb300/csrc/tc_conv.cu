@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
     conv_fwd_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map) {
     using C = Cfg<BN, KIND>;
     using T = Traits<KIND, EW>;
+    constexpr int RED_PITCH = BN + 4;   // floats per row of the cluster-reduction buffer
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -390,6 +391,28 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                 }
                 return (long long)m * GK;
             };
+            if (p.cluster_red) {
+                // one unit per CTA: its partial accumulator goes to this CTA's shared memory
+                // (the drained stage area, row pitch BN + 4 floats), for the cluster reduction
+                // after the role loops
+                if (!wait_bar_warp(tfull_bar(acc), aph, abort_flag, p.err, (p.sleep_mask & 2) != 0)) break;
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
+                float* red_row = reinterpret_cast<float*>(smem) + (size_t)(wq * 32 + lane) * RED_PITCH;
+                for (int cb = cb_begin; cb < cb_end; cb += 16) {
+                    uint32_t v[16];
+                    __syncwarp();
+                    tmem_ld16(taddr + (uint32_t)cb, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<uint4*>(red_row + cb + e) = make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
+                continue;
+            }
             const bool wide = partial || T::TF32;     // fp32 stores
             long long roff[EPI_MAX_LPR];
             if (wide) epilogue_rows<COLS, 4>(lane, wq, row_offset, roff);
@@ -407,6 +430,68 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
+    }
+
+    if (p.cluster_red) {
+        // Split-K reduction across the cluster (the p.splits CTAs of one tile, cluster rank =
+        // split): once every partial sits in its CTA's shared memory, CTA k sums rows
+        // [k R, (k+1) R) of all partials in split order (so the result does not depend on
+        // timing), adds bias, applies GELU and stores y.  A second cluster barrier keeps each
+        // CTA's buffer alive until the others have read it.
+        cluster_sync_all();
+        if (warp < EW && blockIdx.x < (unsigned)p.total_units) {
+            int mt, gi, nt, split;
+            decode_unit(p, blockIdx.x, mt, gi, nt, split);
+            TileOrigin to{0, 0, 0, 0};
+            if (T::TMA) to = tile_origin(p, mt);
+            const int S = p.splits;
+            const int R = BM / S;
+            const int r0 = (int)cluster_ctarank() * R;
+            const bool add_bias = p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU;
+            const bool do_gelu = p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU;
+            const uint32_t red0 = smem_u32(smem);
+            const int per_row = BN / 4;
+            for (int i = threadIdx.x; i < R * per_row; i += EW * 32) {
+                const int rr = r0 + i / per_row;
+                const int col = (i - (i / per_row) * per_row) * 4;
+                const int n = nt * BN + col;
+                if (n >= g.K) continue;
+                int m;
+                if (T::TMA) {
+                    const int rh = fdiv(rr, p.f_BW);
+                    const int oh = to.oh0 + rh, ow = to.ow0 + (rr - rh * p.BW);
+                    if (rr >= p.BW * p.BH || oh >= g.Ho || ow >= g.Wo) continue;
+                    m = ((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow;
+                } else {
+                    m = mt * BM + rr;
+                    if (m >= g.M) continue;
+                }
+                const uint32_t off = (uint32_t)(rr * RED_PITCH + col) * 4u;
+                float4 a = ld_cluster_f4(cluster_map(red0 + off, 0));
+                for (int j = 1; j < S; ++j) {
+                    const float4 b = ld_cluster_f4(cluster_map(red0 + off, (uint32_t)j));
+                    a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+                }
+                float v[4] = {a.x, a.y, a.z, a.w};
+                const size_t o = (size_t)m * GK + (size_t)gi * g.K + n;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (add_bias) {
+                        v[e] += T::TF32 ? reinterpret_cast<const float*>(p.bias)[(size_t)gi * g.K + n + e]
+                                        : __bfloat162float(
+                                              reinterpret_cast<const __nv_bfloat16*>(p.bias)[(size_t)gi * g.K + n + e]);
+                    }
+                    if (do_gelu) v[e] = gelu(v[e]);
+                }
+                if (T::TF32) {
+                    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + o) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+                    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.y) + o) =
+                        make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+                }
+            }
+        }
+        cluster_sync_all();
     }
 
     tc_fence_before();
@@ -440,7 +525,7 @@ cudaError_t launch_one(const TcParams& p, const CUtensorMap& map, int grid, cuda
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    return launch_kernel(kern, dim3(grid), dim3(Traits<KIND, EW>::THREADS), smem, stream, p.pdl != 0, p, map);
+    return launch_kernel(kern, dim3(grid), dim3(Traits<KIND, EW>::THREADS), smem, stream, p.pdl != 0, p.cluster_red ? p.splits : 1, p, map);
 }
 
 }  // namespace

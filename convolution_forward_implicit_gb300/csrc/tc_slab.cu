@@ -430,7 +430,7 @@ cudaError_t launch_slab_one(const TcParams& p, const CUtensorMap& map, int grid,
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    return launch_kernel(kern, dim3(grid), dim3(SlabRoles<TF32>::THREADS), smem, stream, p.pdl != 0, p, map);
+    return launch_kernel(kern, dim3(grid), dim3(SlabRoles<TF32>::THREADS), smem, stream, p.pdl != 0, 1, p, map);
 }
 
 }  // namespace

@@ -453,3 +453,21 @@ def test_slab_tile_pairs(name, stream):
     assert "tma-slab" in desc and "acc=2" in desc, desc
     ref, S = oracle_full(layer, dtype, x, w, b)
     assert_within(dtype, layer.epilogue, got, ref, S, desc)
+
+
+@pytest.mark.parametrize("splits", [2, 4, 8])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_cluster_split_k_reduction_equals_the_reduction_kernel(splits, dtype):
+    """Split-K partials summed inside a thread-block cluster through distributed shared
+    memory, in split order, give bit for bit the output of the separate reduction kernel
+    (which sums the same partials in the same order), and meet the oracle's bound."""
+    layer = L(1, 1, 1, 512, 256, (700,), (3,), (2,), (1,), (1,), CONV_EPI_BIAS_GELU)
+    x, w, b = make_inputs(layer, dtype, 2300 + splits)
+    env = {"CONV_FORCE_SPLITK": splits, "CONV_FORCE_GATHER": "tma", "CONV_FORCE_BN": 64}
+    a, da = run_gpu(layer, dtype, x, w, b, env=dict(env, CONV_FORCE_CLUSTER_RED=1), guard=64)
+    c, dc = run_gpu(layer, dtype, x, w, b, env=dict(env, CONV_FORCE_CLUSTER_RED=0), guard=64)
+    assert f"splits={splits}" in da and "reduce=cluster" in da, da
+    assert "reduce=kernel" in dc, dc
+    assert np.array_equal(a, c), "cluster and kernel reductions differ"
+    ref, S = oracle_full(layer, dtype, x, w, b)
+    assert_within(dtype, layer.epilogue, a, ref, S, da)
