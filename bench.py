@@ -52,6 +52,8 @@ def frontend_workloads(name):
     from convolution_forward_implicit_gb300.workloads import WORKLOADS
     if name == "whisper_frontend":
         return [WORKLOADS["whisper_frontend_f32"], WORKLOADS["whisper_frontend_bf16"]]
+    if name == "whisper_mlp":
+        return [WORKLOADS["whisper_mlp_f32"], WORKLOADS["whisper_mlp_bf16"]]
     if name in WORKLOADS:
         return [WORKLOADS[name]]
     raise SystemExit(f"unknown workload {name}")
@@ -61,6 +63,9 @@ def workload_description(name):
     if name == "whisper_frontend":
         return ("whisper_tiny_conv_frontend: conv1d 80->384 k3 s1 p1 L=3000 +GELU, conv1d 384->384 k3 s2 p1 "
                 "(L 3000->1500) +GELU, batch 1, fp32 and bf16 I/O")
+    if name == "whisper_mlp":
+        return ("whisper_tiny_encoder_mlp as 1x1 convs: 384->1536 +bias +GELU, 1536->384 +bias over 1500 "
+                "positions, batch 1, fp32 and bf16 I/O")
     return name
 
 

@@ -93,6 +93,14 @@ def grouped3d(d, N=4, D=16, HW=56, G=4, C=64):
     return Layer(3, N, G, C, C, (D, HW, HW), (3, 3, 3), (1, 1, 1), (1, 1, 1), (d, d, d), CONV_EPI_BIAS, 0.05)
 
 
+def whisper_mlp_layers():
+    """The encoder's feed-forward block as 1x1 convolutions over the 1500 frame positions
+    (page "[ET-VK] conv1d ...", "Measurements": the linear dispatches M=1500, N=1536, K=384
+    and M=1500, N=384, K=1536): 384 -> 1536 with bias and GELU, then 1536 -> 384 with bias."""
+    return (Layer(1, 1, 1, 384, 1536, (1500,), (1,), (1,), (0,), (1,), CONV_EPI_BIAS_GELU, 0.05),
+            Layer(1, 1, 1, 1536, 384, (1500,), (1,), (1,), (0,), (1,), CONV_EPI_BIAS, 0.05))
+
+
 WORKLOADS = {
     "conv1d_f32_80to384_L3000": Workload(
         "conv1d_f32_80to384_L3000", 0, "f32", (_conv1d(1, 80, 384, 3000, 1, CONV_EPI_BIAS),),
@@ -110,6 +118,10 @@ WORKLOADS = {
     "grouped2d_g32_c8_d2": Workload("grouped2d_g32_c8_d2", 4, "bf16", (grouped2d(32, 8, 2),)),
     "grouped3d_g4_c64_d1": Workload("grouped3d_g4_c64_d1", 5, "bf16", (grouped3d(1),)),
     "grouped3d_g4_c64_d2": Workload("grouped3d_g4_c64_d2", 5, "bf16", (grouped3d(2),)),
+    "whisper_mlp_f32": Workload("whisper_mlp_f32", 6, "f32", whisper_mlp_layers(),
+                                "Whisper-tiny encoder MLP as 1x1 convs fp32, 1500 positions"),
+    "whisper_mlp_bf16": Workload("whisper_mlp_bf16", 6, "bf16", whisper_mlp_layers(),
+                                 "Whisper-tiny encoder MLP as 1x1 convs bf16, 1500 positions"),
 }
 
 
