@@ -18,7 +18,10 @@ rotate over enough copies of every input, packed weight and output that one rota
 exceeds twice the L2 cache, so no step finds its data in L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
-                  [--no-overlap] [--source-hash]
+                  [--no-overlap] [--tune ITERS] [--source-hash]
+
+--tune ITERS lets the measured selector (conv_plan_tune) time every candidate plan of each
+layer before the run and keep the fastest; by default the planner's rules choose.
 
 Under torchrun each rank runs an independent replica on its own GPU (the forward pass
 has no exchange step); rank 0 prints the JSON line with the max time over ranks.
@@ -155,13 +158,18 @@ class ClockSampler:
 class LayerRun:
     """One layer of one workload: its plan, per-rotation-set buffers and CUDA graphs."""
 
-    def __init__(self, wl, li, layer, R, x_sets, w, b):
+    def __init__(self, wl, li, layer, R, x_sets, w, b, tune_iters=0):
         import torch
         from convolution_forward_implicit_gb300.binding import ConvPlan
         self.wl, self.li, self.layer = wl, li, layer
         self.plan = ConvPlan(*layer.plan_args(wl.dtype_code))
-        self.plan.allocate()
         tdt = self.plan.torch_dtype()
+        if tune_iters:
+            # the measured selector: time every candidate plan on these buffers, keep the fastest
+            y = torch.empty(self.plan.y_shape(), dtype=tdt, device="cuda")
+            self.plan.tune(x_sets[0], w, b if layer.bias_bound is not None else None, y, iters=tune_iters)
+            del y
+        self.plan.allocate()
         self.x_sets = x_sets
         self.wp_sets, self.b_sets, self.y_sets = [], [], []
         for r in range(R):
@@ -221,7 +229,7 @@ def to_device(a, dtype):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
 
 
-def setup_layers(wls, R):
+def setup_layers(wls, R, tune_iters=0):
     """Layers of every workload; layer l+1 of a workload reads layer l's output set."""
     from convolution_forward_implicit_gb300.workloads import gen_inputs
     runs, inputs = [], []
@@ -233,7 +241,7 @@ def setup_layers(wls, R):
         for li, layer in enumerate(wl.layers):
             w, b = params[li]
             lr = LayerRun(wl, li, layer, R, x_sets, to_device(w, wl.dtype),
-                          to_device(b, wl.dtype) if b is not None else None)
+                          to_device(b, wl.dtype) if b is not None else None, tune_iters)
             runs.append(lr)
             x_sets = [y.view(-1) for y in lr.y_sets]
     return runs, inputs
@@ -295,7 +303,7 @@ def run_ours(args, ws, rank, local):
     __graft_entry__.build()
     wls = frontend_workloads(args.workload)
     R, per_set = rotation_sets(wls)
-    runs, inputs = setup_layers(wls, R)
+    runs, inputs = setup_layers(wls, R, args.tune)
     stream = torch.cuda.current_stream()
     if args.overlap:
         for lr in runs:
@@ -402,6 +410,8 @@ def run_ours(args, ws, rank, local):
                          f"(~{R * per_set / 1e6:.0f} MB per rotation, L2 129 MB)",
                    "graphs": graph_mode,
                    "overlap": bool(args.overlap),
+                   "selector": (f"measured (conv_plan_tune, {args.tune} timed calls per candidate)" if args.tune
+                                else "rules"),
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "plans": {lr.name(): lr.plan.describe() for lr in runs}},
         "roofline": roof,
@@ -651,6 +661,9 @@ def main():
     ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash and exit")
     ap.add_argument("--no-overlap", dest="overlap", action="store_false",
                     help="launch each layer only after the previous one completes (no programmatic dependents)")
+    ap.add_argument("--tune", type=int, default=0, metavar="ITERS",
+                    help="before timing, let the measured selector time every candidate plan of each layer "
+                         "(ITERS calls each) and keep the fastest; 0 = the planner's rules")
     args = ap.parse_args()
     if args.source_hash:
         print(kernel_source_hash())

@@ -53,6 +53,11 @@ _SIGS = {
     "conv_plan_flops": (ctypes.c_double, [_VP]),
     "conv_fwd_static_scratch": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP]),
     "conv_plan_set_overlap": (ctypes.c_int, [_VP, ctypes.c_int]),
+    "conv_tune_scratch_bytes": (ctypes.c_size_t, [_VP]),
+    "conv_plan_tune": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, ctypes.c_int, _VP]),
+    "conv_tune_table_save": (ctypes.c_int, [ctypes.c_char_p]),
+    "conv_tune_table_load": (ctypes.c_int, [ctypes.c_char_p]),
+    "conv_tune_table_clear": (ctypes.c_int, []),
 }
 CONV_STATIC_SCRATCH_BYTES = 16 << 20
 EXPORTED = tuple(_SIGS)
@@ -156,6 +161,30 @@ def conv_plan_set_overlap(plan: int, enable: bool = True):
     _check(load_library().conv_plan_set_overlap(plan, 1 if enable else 0), "conv_plan_set_overlap")
 
 
+def conv_tune_scratch_bytes(plan: int) -> int:
+    return int(load_library().conv_tune_scratch_bytes(plan))
+
+
+def conv_plan_tune(plan: int, x_ptr: int, w_ptr: int, bias_ptr: int, y_ptr: int, scratch_ptr: int,
+                   scratch_bytes: int, iters: int = 10, stream: int = 0):
+    """Time the candidate plans of this problem and switch the plan to the fastest (see
+    include/conv.h); afterwards the packed weight and workspace must be re-made."""
+    _check(load_library().conv_plan_tune(plan, x_ptr, w_ptr, bias_ptr or None, y_ptr, scratch_ptr,
+                                         int(scratch_bytes), int(iters), stream or None), "conv_plan_tune")
+
+
+def conv_tune_table_save(path: str):
+    _check(load_library().conv_tune_table_save(os.fsencode(path)), "conv_tune_table_save")
+
+
+def conv_tune_table_load(path: str):
+    _check(load_library().conv_tune_table_load(os.fsencode(path)), "conv_tune_table_load")
+
+
+def conv_tune_table_clear():
+    _check(load_library().conv_tune_table_clear(), "conv_tune_table_clear")
+
+
 def conv_plan_describe(plan: int) -> str:
     return load_library().conv_plan_describe(plan).decode()
 
@@ -229,6 +258,22 @@ class ConvPlan:
 
     def set_overlap(self, enable: bool = True):
         conv_plan_set_overlap(self.handle, enable)
+
+    def tune(self, x, w, bias, y, iters: int = 10, stream=None):
+        """Measure the candidate plans on these tensors, keep the fastest, and re-make the
+        packed weight and workspace for it.  y is overwritten."""
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
+        nbytes = conv_tune_scratch_bytes(self.handle)
+        scratch = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+        conv_plan_tune(self.handle, x.data_ptr(), w.data_ptr(), 0 if bias is None else bias.data_ptr(),
+                       y.data_ptr(), scratch.data_ptr(), nbytes, iters, s)
+        del scratch
+        self.workspace = None
+        self.w_packed = None
+        self.allocate(x.device)
+        self.prepack(w, stream)
+        return self.describe()
 
     def check(self, stream=None):
         import torch

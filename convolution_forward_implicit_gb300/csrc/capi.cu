@@ -8,7 +8,10 @@
 #include <string.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
+#include <string>
+#include <vector>
 #include <new>
 
 #include <cudaTypedefs.h>
@@ -202,7 +205,29 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, l
 // ----------------------------------------------------------------------------- plan
 enum Variant { VAR_TC = 0, VAR_SIMT = 1 };
 
+// Plan choices that can be fixed instead of decided by rule: by the measured selector
+// (conv_plan_tune and its table) or, for tests, by CONV_FORCE_* environment variables.
+// 0 (or -1 where 0 is a meaningful value) leaves the choice to the rules.
+struct PlanChoice {
+    int simt = 0;          // 1: the FFMA kernel
+    int no_pack = 0;       // 1: never pack groups narrower than 64 channels
+    int bn = 0;            // tensor-core N tile: 16, 32, 64, 128 or 256
+    int bm = 0;            // FFMA M tile: 64 or 128
+    int splits = 0;        // >= 1: split-K factor (capped by the K blocks)
+    int gather = 0;        // 1: cp.async chunks (bf16), 2: per-tap TMA boxes (no slab)
+    int slab_stream = 0;   // 1: slab mode streams its weights through a ring
+    int slab_pair = -1;    // 0 / 1: slab tile pairs off / on
+    int epi_warps = 0;     // 8 or 16 epilogue warps in the per-tap kernel
+    int cluster_red = -1;  // 0: split-K partials through the reduction kernel, not a cluster
+    bool operator==(const PlanChoice& o) const {
+        return simt == o.simt && no_pack == o.no_pack && bn == o.bn && bm == o.bm && splits == o.splits &&
+               gather == o.gather && slab_stream == o.slab_stream && slab_pair == o.slab_pair &&
+               epi_warps == o.epi_warps && cluster_red == o.cluster_red;
+    }
+};
+
 struct conv_plan {
+    PlanChoice ch;
     int ndim;
     int64_t spatial[3], filter[3], stride[3], pad[3], dil[3], out_spatial[3];
     conv_dtype dtype;
@@ -233,6 +258,32 @@ static int env_int(const char* name, int dflt) {
     const char* v = getenv(name);
     if (!v || !*v) return dflt;
     return atoi(v);
+}
+
+// The test hooks: CONV_FORCE_* variables fix a choice; returns whether any was set.
+static bool choice_from_env(PlanChoice& c) {
+    bool any = false;
+    auto take = [&](const char* name, int& field) {
+        const char* v = getenv(name);
+        if (v && *v) {
+            field = atoi(v);
+            any = true;
+        }
+    };
+    take("CONV_FORCE_SIMT", c.simt);
+    take("CONV_NO_PACK", c.no_pack);
+    take("CONV_FORCE_BN", c.bn);
+    take("CONV_FORCE_BM", c.bm);
+    take("CONV_FORCE_SPLITK", c.splits);
+    take("CONV_FORCE_SLAB_STREAM", c.slab_stream);
+    take("CONV_FORCE_SLAB_PAIR", c.slab_pair);
+    take("CONV_FORCE_EPI_WARPS", c.epi_warps);
+    take("CONV_FORCE_CLUSTER_RED", c.cluster_red);
+    if (const char* v = getenv("CONV_FORCE_GATHER")) {
+        if (strcmp(v, "cpasync") == 0) { c.gather = 1; any = true; }
+        else if (strcmp(v, "tma") == 0) { c.gather = 2; any = true; }
+    }
+    return any;
 }
 
 static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -398,7 +449,7 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     else if (g.K <= 128) bn = 128;
     else if (g.K <= 256) bn = 256;
     else bn = (cdiv(g.K, 256) * 256 - g.K <= cdiv(g.K, 128) * 128 - g.K) ? 256 : 128;
-    const int force_bn = env_int("CONV_FORCE_BN", 0);
+    const int force_bn = p->ch.bn;
     if (force_bn == 16 || force_bn == 32 || force_bn == 64 || force_bn == 128 || force_bn == 256) bn = force_bn;
     p->tf32 = tf32 ? 1 : 0;
     p->BN = bn;
@@ -414,13 +465,12 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     if (g.C % cblk == 0 || g.G == 1) map_kind = 0;
     else if (g.D == 1 && g.Z == 1) map_kind = 1;
     bool tma = map_kind >= 0 && g.C >= cblk && g.sw <= 8 && g.sh <= 8;
-    const char* force_gather = getenv("CONV_FORCE_GATHER");
-    if (!tf32 && force_gather && strcmp(force_gather, "cpasync") == 0) tma = false;
+    if (!tf32 && p->ch.gather == 1) tma = false;
     // Slab mode for stride-1 problems with several taps per plane (one box serves them all);
     // its shared-memory fit is checked once the N tile is known.
     p->slab = 0;
     const bool want_slab = allow_slab && tma && g.sw == 1 && g.sh == 1 && g.sd == 1 && g.Y * g.X >= 3 &&
-                           !(force_gather && strcmp(force_gather, "tma") == 0);
+                           p->ch.gather != 2;
     if (tma) {
         p->map_kind = map_kind;
         if (want_slab && choose_slab_shape(p)) p->slab = 1;
@@ -472,8 +522,7 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
         splits = (int)std::min<int64_t>(p->sm_count / units, p->nkb / 2);
         splits = std::max(1, std::min(splits, 16));
     }
-    const int force = env_int("CONV_FORCE_SPLITK", 0);
-    if (force >= 1) splits = std::min(force, p->nkb);
+    if (p->ch.splits >= 1) splits = std::min(p->ch.splits, p->nkb);
     if (p->slab) {
         // slab mode runs whole reductions per tile and needs its rings to fit: the weights of
         // one (group, N tile) resident with a 3- or 2-stage slab ring where they fit, else a
@@ -485,7 +534,7 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
             p->slab_sb = 0;
             p->slab_resident = 0;
             for (int sa = 3; sa >= 2 && !p->slab_resident; --sa)
-                if (env_int("CONV_FORCE_SLAB_STREAM", 0) == 0 &&
+                if (p->ch.slab_stream == 0 &&
                     slab_smem_bytes(bn, p->tf32, sa, nchunk, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
                     p->slab_resident = 1;
                     p->slab_sa = sa;
@@ -501,7 +550,7 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
         // Tile pairs (bf16, N tile <= 64, several units per CTA, more than one row block):
         // two accumulators per unit, stacked along H, share one slab and one weight pass.
         set_slab_pair(p, false);
-        const int force_pair = env_int("CONV_FORCE_SLAB_PAIR", -1);
+        const int force_pair = p->ch.slab_pair;
         const bool want_pair = !tf32 && bn <= 64 && splits == 1 && g.Ho > p->acc_bh &&
                                (force_pair >= 0 ? force_pair == 1 : units >= 4LL * p->sm_count);
         bool fits = false;
@@ -524,7 +573,7 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     // at 3 taps) spend longer in the epilogue (bias, GELU, stores of BM x BN outputs) than in
     // the MMAs: they get 16 epilogue warps (4 per TMEM lane quarter), one stage fewer.
     if (!tf32 && p->tma && !p->slab && bn >= 128) {
-        const int force_ew = env_int("CONV_FORCE_EPI_WARPS", 0);
+        const int force_ew = p->ch.epi_warps;
         const bool wide_epi = force_ew ? force_ew == 16 : p->kbps <= 16;
         if (wide_epi) {
             p->epi_warps = 16;
@@ -538,7 +587,7 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     // thread-block cluster through distributed shared memory: no workspace, no second kernel.
     p->cluster_red = 0;
     if (p->splits >= 2 && p->splits <= 8 && (128 % p->splits) == 0 && p->total_units <= p->sm_count &&
-        g.K % 4 == 0 && env_int("CONV_FORCE_CLUSTER_RED", 1) != 0)
+        g.K % 4 == 0 && p->ch.cluster_red != 0)
         p->cluster_red = 1;
     p->workspace_bytes = (p->splits > 1 && !p->cluster_red) ? (size_t)p->splits * g.M * g.G * g.K * sizeof(float) : 0;
     if (p->slab)
@@ -571,8 +620,7 @@ static void plan_simt(conv_plan* p) {
     p->Kpad = p->num_nt * 128;
     const int64_t tiles128 = cdiv(g.M, 128) * p->num_nt * g.G;
     p->BM = tiles128 >= p->sm_count ? 128 : 64;
-    const int force_bm = env_int("CONV_FORCE_BM", 0);
-    if (force_bm == 64 || force_bm == 128) p->BM = force_bm;
+    if (p->ch.bm == 64 || p->ch.bm == 128) p->BM = p->ch.bm;
     p->num_mt = (int)cdiv(g.M, p->BM);
     const int64_t tiles = (int64_t)p->num_mt * p->num_nt * g.G;
     int splits = 1;
@@ -580,8 +628,7 @@ static void plan_simt(conv_plan* p) {
         splits = (int)std::min<int64_t>(p->sm_count / tiles, p->nkt / 16);
         splits = std::max(1, std::min(splits, 16));
     }
-    const int force = env_int("CONV_FORCE_SPLITK", 0);
-    if (force >= 1) splits = std::min(force, p->nkt);
+    if (p->ch.splits >= 1) splits = std::min(p->ch.splits, p->nkt);
     p->ktps = (int)cdiv(p->nkt, splits);
     p->splits = (int)cdiv(p->nkt, p->ktps);
     p->vec = (g.C % 4 == 0 && g.K % 4 == 0) ? 1 : 0;
@@ -593,6 +640,99 @@ static void plan_simt(conv_plan* p) {
              p->dtype == CONV_BF16 ? "bf16" : "f32", p->BM, p->splits, p->num_mt, p->num_nt,
              g.G * p->splits, p->vec);
 }
+
+// Variant and tiling of a plan whose geometry is set, under its choices p->ch (re-run by the
+// selector with other choices).  Starts from the caller's geometry (Go, Co, Ko).
+static void choose_variant(conv_plan* p) {
+    Geom& g = p->g;
+    const int64_t G = p->Go, C = p->Co, K = p->Ko;
+    g.G = (int)G; g.C = (int)C; g.K = (int)K;
+    p->pack = 1; p->slab = 0; p->tma = 0; p->cluster_red = 0; p->epi_warps = 8; p->splits = 1;
+    // bf16 with C, K multiples of 8: tcgen05 kind::f16.  fp32 with C, K multiples of 4 that the
+    // TMA gather can express: tcgen05 3xTF32.  Everything else: the FFMA kernel.
+    const bool no_tc = p->ch.simt != 0;
+    bool tc = false;
+    // Groups narrower than one 64-channel block: pack 64/C of them into a super-group with a
+    // block-diagonal weight, so each tap still fills a whole 128-byte TMA box row (the MMA
+    // does pack-fold redundant work on the zero blocks; the useful FLOP count is unchanged).
+    if (!no_tc && p->dtype == CONV_BF16 && C % 8 == 0 && K % 8 == 0 && C < 64 && 64 % C == 0 &&
+        G % (64 / C) == 0 && K * (64 / C) <= 4096 && p->ch.no_pack == 0) {
+        p->pack = (int)(64 / C);
+        g.G = (int)(G / p->pack); g.C = 64; g.K = (int)(K * p->pack);
+    }
+    if (!no_tc && p->dtype == CONV_BF16 && C % 8 == 0 && K % 8 == 0) tc = plan_tc(p, false);
+    if (!tc && p->pack > 1) {   // not planned on the tensor cores after all: the caller's geometry
+        p->pack = 1; g.G = (int)G; g.C = (int)C; g.K = (int)K;
+    }
+    if (!no_tc && p->dtype == CONV_F32 && C % 4 == 0 && K % 4 == 0) tc = plan_tc(p, true);
+    if (tc) {
+        p->variant = VAR_TC;
+        if (p->pack > 1) {
+            const size_t n = strlen(p->desc);
+            snprintf(p->desc + n, sizeof(p->desc) - n, " pack=%d", p->pack);
+        }
+    } else {
+        p->variant = VAR_SIMT;
+        p->pack = 1; g.G = (int)G; g.C = (int)C; g.K = (int)K;
+        plan_simt(p);
+    }
+}
+
+// ----------------------------------------------------------------------------- measured selector
+// A process-wide table from a problem (its geometry, dtype, epilogue and the device's SM count)
+// to the choices the selector measured fastest; conv_plan_create consults it.
+static std::mutex g_tune_mu;
+static std::map<std::string, PlanChoice> g_tune_table;
+
+static std::string plan_key(const conv_plan* p) {
+    char buf[400];
+    snprintf(buf, sizeof(buf),
+             "nd=%d N=%d G=%lld C=%lld K=%lld in=%lldx%lldx%lld f=%lldx%lldx%lld s=%lldx%lldx%lld p=%lldx%lldx%lld "
+             "d=%lldx%lldx%lld dtype=%d epi=%d sm=%d",
+             p->ndim, p->g.N, (long long)p->Go, (long long)p->Co, (long long)p->Ko, (long long)p->spatial[0],
+             (long long)p->spatial[1], (long long)p->spatial[2], (long long)p->filter[0], (long long)p->filter[1],
+             (long long)p->filter[2], (long long)p->stride[0], (long long)p->stride[1], (long long)p->stride[2],
+             (long long)p->pad[0], (long long)p->pad[1], (long long)p->pad[2], (long long)p->dil[0],
+             (long long)p->dil[1], (long long)p->dil[2], (int)p->dtype, (int)p->epi, p->sm_count);
+    return buf;
+}
+
+static void tune_table_lookup(const conv_plan* p, PlanChoice& c) {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    auto it = g_tune_table.find(plan_key(p));
+    if (it != g_tune_table.end()) c = it->second;
+}
+
+// The candidates the selector times: the rules' own plan, each N tile x split factor x
+// gather mode, and the FFMA kernel; candidates that land on the same plan are timed once.
+static std::vector<conv_plan> tune_candidates(const conv_plan* p) {
+    std::vector<PlanChoice> cs;
+    cs.push_back(PlanChoice{});
+    for (int bn : {32, 64, 128, 256})
+        for (int sp : {1, 2, 4})
+            for (int ga : {0, 2}) {
+                PlanChoice c;
+                c.bn = bn; c.splits = sp; c.gather = ga;
+                cs.push_back(c);
+            }
+    PlanChoice f;
+    f.simt = 1;
+    cs.push_back(f);
+    std::vector<conv_plan> out;
+    for (const PlanChoice& c : cs) {
+        conv_plan t = *p;
+        t.ch = c;
+        t.workspace = nullptr;
+        t.workspace_size = 0;
+        choose_variant(&t);
+        bool seen = false;
+        for (const conv_plan& o : out) seen = seen || strcmp(o.desc, t.desc) == 0;
+        if (!seen) out.push_back(t);
+    }
+    return out;
+}
+
+static size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 extern "C" {
 
@@ -650,34 +790,13 @@ conv_status conv_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, i
     g.taps = (int)taps;
     p->flops = 2.0 * (double)M * (double)G * (double)K * (double)taps * (double)C;
     p->sm_count = query_sm_count();
-    // bf16 with C, K multiples of 8: tcgen05 kind::f16.  fp32 with C, K multiples of 4 that the
-    // TMA gather can express: tcgen05 3xTF32.  Everything else: the FFMA kernel.
-    const bool no_tc = env_int("CONV_FORCE_SIMT", 0) != 0;
-    bool tc = false;
-    p->pack = 1; p->Go = g.G; p->Co = g.C; p->Ko = g.K;
-    // Groups narrower than one 64-channel block: pack 64/C of them into a super-group with a
-    // block-diagonal weight, so each tap still fills a whole 128-byte TMA box row (the MMA
-    // does pack-fold redundant work on the zero blocks; the useful FLOP count is unchanged).
-    if (!no_tc && dtype == CONV_BF16 && C % 8 == 0 && K % 8 == 0 && C < 64 && 64 % C == 0 &&
-        G % (64 / C) == 0 && (int64_t)K * (64 / C) <= 4096 && env_int("CONV_NO_PACK", 0) == 0) {
-        p->pack = (int)(64 / C);
-        g.G = (int)(G / p->pack); g.C = 64; g.K = (int)(K * p->pack);
-    }
-    if (!no_tc && dtype == CONV_BF16 && C % 8 == 0 && K % 8 == 0) tc = plan_tc(p, false);
-    if (!tc && p->pack > 1) {   // not planned on the tensor cores after all: the caller's geometry
-        p->pack = 1; g.G = p->Go; g.C = p->Co; g.K = p->Ko;
-    }
-    if (!no_tc && dtype == CONV_F32 && C % 4 == 0 && K % 4 == 0) tc = plan_tc(p, true);
-    if (tc) {
-        p->variant = VAR_TC;
-        if (p->pack > 1) {
-            const size_t n = strlen(p->desc);
-            snprintf(p->desc + n, sizeof(p->desc) - n, " pack=%d", p->pack);
-        }
-    } else {
-        p->variant = VAR_SIMT;
-        plan_simt(p);
-    }
+    p->Go = g.G; p->Co = g.C; p->Ko = g.K;
+    // choices: the test hooks if set, else the measured selector's entry for this problem on
+    // this device, else the rules
+    PlanChoice c;
+    if (!choice_from_env(c)) tune_table_lookup(p, c);
+    p->ch = c;
+    choose_variant(p);
     *out = p;
     return CONV_OK;
 }
@@ -912,5 +1031,132 @@ extern "C" conv_status conv_fwd_static_scratch(conv_plan_t plan, const void* x, 
 extern "C" {
 
 double conv_plan_flops(conv_plan_t plan) { return plan ? plan->flops : 0.0; }
+
+}  // extern "C"
+
+// ----------------------------------------------------------------------------- measured selector: entry points
+extern "C" {
+
+size_t conv_tune_scratch_bytes(conv_plan_t plan) {
+    if (!plan) return 0;
+    size_t need = 0;
+    for (const conv_plan& t : tune_candidates(plan)) need = std::max(need, align256(t.prepack_bytes) + t.workspace_bytes);
+    return need;
+}
+
+conv_status conv_plan_tune(conv_plan_t plan, const void* x, const void* w, const void* bias, void* y, void* scratch,
+                           size_t scratch_bytes, int iters, void* stream) {
+    if (!plan || !x || !w || !y || !scratch || iters < 1) return CONV_ERR_INVALID_ARG;
+    const bool needs_bias = plan->epi == CONV_EPI_BIAS || plan->epi == CONV_EPI_BIAS_GELU;
+    if (needs_bias && !bias) return CONV_ERR_INVALID_ARG;
+    if (misaligned(x) || misaligned(w) || misaligned(y) || misaligned(scratch) || (needs_bias && misaligned(bias)))
+        return CONV_ERR_ALIGNMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::vector<conv_plan> cands = tune_candidates(plan);
+    cudaEvent_t e0, e1;
+    if (cudaEventCreate(&e0) != cudaSuccess) return CONV_ERR_CUDA;
+    if (cudaEventCreate(&e1) != cudaSuccess) {
+        cudaEventDestroy(e0);
+        return CONV_ERR_CUDA;
+    }
+    float best = 0.0f;
+    int best_i = -1;
+    conv_status st = CONV_OK;
+    for (size_t i = 0; i < cands.size() && st == CONV_OK; ++i) {
+        conv_plan& t = cands[i];
+        const size_t wbytes = align256(t.prepack_bytes);
+        if (wbytes + t.workspace_bytes > scratch_bytes) continue;
+        uint8_t* wp = static_cast<uint8_t*>(scratch);
+        float* ws = t.workspace_bytes ? reinterpret_cast<float*>(wp + wbytes) : nullptr;
+        if (conv_prepack_weights(&t, w, wp, stream) != CONV_OK) continue;
+        bool ok = true;
+        for (int r = 0; r < 2 && ok; ++r) ok = run_forward(&t, x, wp, bias, y, ws, s) == CONV_OK;
+        ok = ok && cudaEventRecord(e0, s) == cudaSuccess;
+        for (int r = 0; r < iters && ok; ++r) ok = run_forward(&t, x, wp, bias, y, ws, s) == CONV_OK;
+        ok = ok && cudaEventRecord(e1, s) == cudaSuccess;
+        if (cudaStreamSynchronize(s) != cudaSuccess) {   // a failed launch leaves the context unusable
+            st = CONV_ERR_CUDA;
+            break;
+        }
+        // a candidate whose kernels gave up on a wait is not taken
+        unsigned v = 0;
+        if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v)) != cudaSuccess) {
+            st = CONV_ERR_CUDA;
+            break;
+        }
+        if (v) {
+            const unsigned zero = 0;
+            cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+            ok = false;
+        }
+        float ms = 0.0f;
+        if (ok && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess && (best_i < 0 || ms < best)) {
+            best = ms;
+            best_i = (int)i;
+        }
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (st != CONV_OK) return st;
+    if (best_i < 0) return CONV_ERR_WORKSPACE;   // no candidate fitted the scratch buffer
+    const PlanChoice bc = cands[best_i].ch;
+    {
+        std::lock_guard<std::mutex> lk(g_tune_mu);
+        g_tune_table[plan_key(plan)] = bc;
+    }
+    plan->ch = bc;
+    choose_variant(plan);
+    return CONV_OK;
+}
+
+conv_status conv_tune_table_save(const char* path) {
+    if (!path) return CONV_ERR_INVALID_ARG;
+    FILE* f = fopen(path, "w");
+    if (!f) return CONV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    for (const auto& kv : g_tune_table) {
+        const PlanChoice& c = kv.second;
+        fprintf(f, "%s | simt=%d no_pack=%d bn=%d bm=%d splits=%d gather=%d slab_stream=%d slab_pair=%d epi_warps=%d "
+                   "cluster_red=%d\n",
+                kv.first.c_str(), c.simt, c.no_pack, c.bn, c.bm, c.splits, c.gather, c.slab_stream, c.slab_pair,
+                c.epi_warps, c.cluster_red);
+    }
+    const bool ok = fclose(f) == 0;
+    return ok ? CONV_OK : CONV_ERR_INVALID_ARG;
+}
+
+conv_status conv_tune_table_load(const char* path) {
+    if (!path) return CONV_ERR_INVALID_ARG;
+    FILE* f = fopen(path, "r");
+    if (!f) return CONV_ERR_INVALID_ARG;
+    char line[1024];
+    conv_status st = CONV_OK;
+    std::vector<std::pair<std::string, PlanChoice>> rows;
+    while (fgets(line, sizeof(line), f)) {
+        if (line[0] == '\n' || line[0] == '#') continue;
+        char* bar = strstr(line, " | ");
+        PlanChoice c;
+        if (!bar || sscanf(bar + 3,
+                           "simt=%d no_pack=%d bn=%d bm=%d splits=%d gather=%d slab_stream=%d slab_pair=%d "
+                           "epi_warps=%d cluster_red=%d",
+                           &c.simt, &c.no_pack, &c.bn, &c.bm, &c.splits, &c.gather, &c.slab_stream, &c.slab_pair,
+                           &c.epi_warps, &c.cluster_red) != 10) {
+            st = CONV_ERR_INVALID_ARG;
+            break;
+        }
+        rows.emplace_back(std::string(line, bar - line), c);
+    }
+    fclose(f);
+    if (st != CONV_OK) return st;   // a malformed file changes nothing
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    for (auto& r : rows) g_tune_table[r.first] = r.second;
+    return CONV_OK;
+}
+
+conv_status conv_tune_table_clear(void) {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    g_tune_table.clear();
+    return CONV_OK;
+}
 
 }  // extern "C"

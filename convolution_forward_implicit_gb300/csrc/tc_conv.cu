@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
     using C = Cfg<BN, KIND>;
     using T = Traits<KIND, EW>;
     constexpr int RED_PITCH = BN + 4;   // floats per row of the cluster-reduction buffer
+    static_assert((size_t)BM * RED_PITCH * 4 <= (size_t)STAGES * (T::A_STAGE + C::B_STAGE),
+                  "the cluster-reduction buffer reuses the stage area");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;

@@ -174,6 +174,67 @@ double conv_plan_flops(conv_plan_t plan);
 conv_status conv_plan_set_overlap(conv_plan_t plan, int enable);
 
 /*
+ * Measured kernel selection.  conv_plan_create picks a variant and tiling by fixed rules
+ * from the problem's geometry.  The selector instead times the candidate plans of one
+ * problem on this device and keeps the fastest, in a process-wide table that later
+ * conv_plan_create calls for the same problem consult.  The table's key holds every
+ * feature that changes the best kernel: N, G, C, K, the input extents, filter, stride,
+ * padding and dilation per axis, dtype, epilogue and the SM count (page "Learnings --
+ * Grouped-Conv Heuristic (Forward, 2D + 3D)", section 2: dilation must be a feature or
+ * dilated 3D problems are indistinguishable).  Each entry records the whole choice (N
+ * tile, split factor, gather mode, slab streaming and tile pairs, epilogue width, cluster
+ * reduction, FFMA kernel), not a bucket of it (same page, section 1: aliased kernel
+ * names capped the predictor's top-1 accuracy).  Precedence in conv_plan_create: the
+ * CONV_FORCE_* test variables, then the table, then the rules.
+ */
+
+/*
+ * Device bytes conv_plan_tune needs as scratch: the largest packed weight of any
+ * candidate (rounded up to 256 bytes) plus that candidate's split-K workspace.  0 on a
+ * NULL plan.
+ */
+size_t conv_tune_scratch_bytes(conv_plan_t plan);
+
+/*
+ * Time every candidate plan for this problem and switch `plan` to the fastest.
+ *   x, y:     device input (as conv_fwd) and an output buffer of the plan's output shape;
+ *             y is overwritten (many times) with valid conv outputs.
+ *   w:        device weight in the unpacked layout conv_prepack_weights reads.
+ *   bias:     device bias (required for the bias epilogues, else may be NULL).
+ *   scratch:  device buffer of at least conv_tune_scratch_bytes(plan) bytes, 16-byte
+ *             aligned; each candidate's packed weight and workspace are placed in it.
+ *   iters:    timed calls per candidate (>= 1), after two untimed ones; CUDA events on
+ *             `stream` time them.
+ * Synchronizes `stream` once per candidate.  A candidate whose kernels report a wait
+ * timeout is skipped.  On success the plan's variant, tiling, packed-weight layout and
+ * workspace size may all have changed: the caller must query conv_prepacked_weight_bytes
+ * and conv_workspace_bytes again, re-run conv_prepack_weights and re-attach a workspace
+ * before the next conv_fwd.  The choice is also entered in the process-wide table.
+ * Errors: CONV_ERR_INVALID_ARG (NULL plan, x, w, y or scratch; missing bias; iters < 1),
+ * CONV_ERR_ALIGNMENT, CONV_ERR_WORKSPACE (no candidate fits `scratch`), CONV_ERR_CUDA
+ * (a launch or synchronization failed; the plan is unchanged).
+ */
+conv_status conv_plan_tune(conv_plan_t plan, const void* x, const void* w, const void* bias, void* y,
+                           void* scratch, size_t scratch_bytes, int iters, void* stream);
+
+/*
+ * Write the selector's table to a text file, one problem per line ("<key> | <choice>").
+ * CONV_ERR_INVALID_ARG if the file cannot be written.
+ */
+conv_status conv_tune_table_save(const char* path);
+
+/*
+ * Merge a file written by conv_tune_table_save into the table (entries for the same key
+ * are replaced).  A file with any malformed line changes nothing and returns
+ * CONV_ERR_INVALID_ARG, as does a file that cannot be read.  Entries only affect plans
+ * created afterwards.
+ */
+conv_status conv_tune_table_load(const char* path);
+
+/* Empty the selector's table (plans created afterwards use the rules). */
+conv_status conv_tune_table_clear(void);
+
+/*
  * Forward pass for callers that cannot allocate device memory.  (The pages have no
  * counterpart: this is an interface convenience of this library.)
  *

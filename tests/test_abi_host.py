@@ -180,3 +180,76 @@ def test_tile_and_split_choice_fill_the_gpu(lib):
     assert d["splits"] == "1" and d["tile"] == "256x64" and d["acc"] == "2", d
     d = desc_of(WORKLOADS["sweep_bf16_n32"].layers[1], B.CONV_BF16)
     assert d["tile"] == "128x256"
+
+
+def _sm_count():
+    import torch
+    return torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+
+
+def _table_key(layer, code):
+    """The selector table's key for one layer (the file format conv_tune_table_save writes)."""
+    ndim, N, G, C, K, sp, fl, st, pa, di, dtype, epi = layer.plan_args(code)
+    pad3 = lambda v, fill: [fill] * (3 - ndim) + [int(a) for a in v]
+    j = lambda v, fill: "x".join(str(a) for a in pad3(v, fill))
+    return (f"nd={ndim} N={N} G={G} C={C} K={K} in={j(sp, 1)} f={j(fl, 1)} s={j(st, 1)} p={j(pa, 0)} "
+            f"d={j(di, 1)} dtype={dtype} epi={epi} sm={_sm_count()}")
+
+
+def test_selector_table_load_save_and_precedence(lib, tmp_path):
+    """A table entry overrides the rules for exactly its problem; saving writes it back;
+    a malformed file changes nothing; clearing restores the rules."""
+    layer = WORKLOADS["whisper_frontend_bf16"].layers[0]
+    other = WORKLOADS["whisper_frontend_bf16"].layers[1]
+
+    def desc_of(l):
+        h = B.conv_plan_create(*l.plan_args(B.CONV_BF16))
+        d = B.conv_plan_describe(h)
+        B.conv_plan_destroy(h)
+        return d
+
+    B.conv_tune_table_clear()
+    rules, rules_other = desc_of(layer), desc_of(other)
+    assert "tile=128x64" in rules and "variant=simt" not in rules
+    choice = ("simt=1 no_pack=0 bn=0 bm=0 splits=0 gather=0 slab_stream=0 slab_pair=-1 epi_warps=0 "
+              "cluster_red=-1")
+    f = tmp_path / "table.txt"
+    f.write_text(f"# measured choices\n{_table_key(layer, B.CONV_BF16)} | {choice}\n")
+    try:
+        B.conv_tune_table_load(str(f))
+        assert desc_of(layer).startswith("variant=simt_bf16")
+        assert desc_of(other) == rules_other                   # other problems keep the rules
+        out = tmp_path / "saved.txt"
+        B.conv_tune_table_save(str(out))
+        assert out.read_text().splitlines() == [f"{_table_key(layer, B.CONV_BF16)} | {choice}"]
+        bad = tmp_path / "bad.txt"
+        bad.write_text(f"{_table_key(other, B.CONV_BF16)} | {choice}\nnot a table line\n")
+        with pytest.raises(B.ConvError) as e:
+            B.conv_tune_table_load(str(bad))
+        assert e.value.status == B.CONV_ERR_INVALID_ARG
+        assert desc_of(other) == rules_other                   # nothing of the bad file was taken
+        with pytest.raises(B.ConvError):
+            B.conv_tune_table_load(str(tmp_path / "missing.txt"))
+        # the test variables take precedence over the table
+        os.environ["CONV_FORCE_BN"] = "32"
+        try:
+            assert "tile=128x32" in desc_of(layer)
+        finally:
+            os.environ.pop("CONV_FORCE_BN")
+    finally:
+        B.conv_tune_table_clear()
+    assert desc_of(layer) == rules
+
+
+def test_selector_scratch_covers_every_candidate(lib):
+    """conv_tune_scratch_bytes is at least this plan's own packed weight plus workspace."""
+    for layer in WORKLOADS["whisper_frontend_f32"].layers:
+        h = B.conv_plan_create(*layer.plan_args(B.CONV_F32))
+        try:
+            need = B.conv_tune_scratch_bytes(h)
+            own = B.conv_prepacked_weight_bytes(h) + B.conv_workspace_bytes(h)
+            assert need >= own > 0
+        finally:
+            B.conv_plan_destroy(h)
+    assert lib.conv_tune_scratch_bytes(None) == 0
+    assert lib.conv_plan_tune(None, None, None, None, None, None, 0, 1, None) == B.CONV_ERR_INVALID_ARG
