@@ -682,7 +682,12 @@ static void choose_variant(conv_plan* p) {
 // A process-wide table from a problem (its geometry, dtype, epilogue and the device's SM count)
 // to the choices the selector measured fastest; conv_plan_create consults it.
 static std::mutex g_tune_mu;
-static std::map<std::string, PlanChoice> g_tune_table;
+struct TuneEntry {
+    PlanChoice c;
+    double us = -1.0;                                    // measured time of the choice (-1: loaded)
+    std::vector<std::pair<std::string, double>> log;     // every candidate timed: plan, us per call
+};
+static std::map<std::string, TuneEntry> g_tune_table;
 
 static std::string plan_key(const conv_plan* p) {
     char buf[400];
@@ -700,7 +705,7 @@ static std::string plan_key(const conv_plan* p) {
 static void tune_table_lookup(const conv_plan* p, PlanChoice& c) {
     std::lock_guard<std::mutex> lk(g_tune_mu);
     auto it = g_tune_table.find(plan_key(p));
-    if (it != g_tune_table.end()) c = it->second;
+    if (it != g_tune_table.end()) c = it->second.c;
 }
 
 // The candidates the selector times: the rules' own plan, each N tile x split factor x
@@ -1061,6 +1066,7 @@ conv_status conv_plan_tune(conv_plan_t plan, const void* x, const void* w, const
     }
     float best = 0.0f;
     int best_i = -1;
+    std::vector<std::pair<std::string, double>> log;
     conv_status st = CONV_OK;
     for (size_t i = 0; i < cands.size() && st == CONV_OK; ++i) {
         conv_plan& t = cands[i];
@@ -1090,9 +1096,12 @@ conv_status conv_plan_tune(conv_plan_t plan, const void* x, const void* w, const
             ok = false;
         }
         float ms = 0.0f;
-        if (ok && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess && (best_i < 0 || ms < best)) {
-            best = ms;
-            best_i = (int)i;
+        if (ok && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess) {
+            log.emplace_back(t.desc, 1e3 * ms / iters);
+            if (best_i < 0 || ms < best) {
+                best = ms;
+                best_i = (int)i;
+            }
         }
     }
     cudaEventDestroy(e0);
@@ -1102,7 +1111,10 @@ conv_status conv_plan_tune(conv_plan_t plan, const void* x, const void* w, const
     const PlanChoice bc = cands[best_i].ch;
     {
         std::lock_guard<std::mutex> lk(g_tune_mu);
-        g_tune_table[plan_key(plan)] = bc;
+        TuneEntry& e = g_tune_table[plan_key(plan)];
+        e.c = bc;
+        e.us = 1e3 * best / iters;
+        e.log = std::move(log);
     }
     plan->ch = bc;
     choose_variant(plan);
@@ -1115,11 +1127,15 @@ conv_status conv_tune_table_save(const char* path) {
     if (!f) return CONV_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(g_tune_mu);
     for (const auto& kv : g_tune_table) {
-        const PlanChoice& c = kv.second;
+        const PlanChoice& c = kv.second.c;
         fprintf(f, "%s | simt=%d no_pack=%d bn=%d bm=%d splits=%d gather=%d slab_stream=%d slab_pair=%d epi_warps=%d "
-                   "cluster_red=%d\n",
+                   "cluster_red=%d",
                 kv.first.c_str(), c.simt, c.no_pack, c.bn, c.bm, c.splits, c.gather, c.slab_stream, c.slab_pair,
                 c.epi_warps, c.cluster_red);
+        if (kv.second.us >= 0.0) fprintf(f, " | us=%.3f", kv.second.us);
+        fputc('\n', f);
+        // the measurements behind the choice, as comment lines (ignored by the loader)
+        for (const auto& r : kv.second.log) fprintf(f, "#\tus=%.3f\t%s\n", r.second, r.first.c_str());
     }
     const bool ok = fclose(f) == 0;
     return ok ? CONV_OK : CONV_ERR_INVALID_ARG;
@@ -1131,11 +1147,12 @@ conv_status conv_tune_table_load(const char* path) {
     if (!f) return CONV_ERR_INVALID_ARG;
     char line[1024];
     conv_status st = CONV_OK;
-    std::vector<std::pair<std::string, PlanChoice>> rows;
+    std::vector<std::pair<std::string, TuneEntry>> rows;
     while (fgets(line, sizeof(line), f)) {
         if (line[0] == '\n' || line[0] == '#') continue;
         char* bar = strstr(line, " | ");
-        PlanChoice c;
+        TuneEntry te;
+        PlanChoice& c = te.c;
         if (!bar || sscanf(bar + 3,
                            "simt=%d no_pack=%d bn=%d bm=%d splits=%d gather=%d slab_stream=%d slab_pair=%d "
                            "epi_warps=%d cluster_red=%d",
@@ -1144,7 +1161,8 @@ conv_status conv_tune_table_load(const char* path) {
             st = CONV_ERR_INVALID_ARG;
             break;
         }
-        rows.emplace_back(std::string(line, bar - line), c);
+        if (const char* u = strstr(bar + 3, " | us=")) te.us = atof(u + 6);
+        rows.emplace_back(std::string(line, bar - line), te);
     }
     fclose(f);
     if (st != CONV_OK) return st;   // a malformed file changes nothing

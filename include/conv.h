@@ -218,8 +218,11 @@ conv_status conv_plan_tune(conv_plan_t plan, const void* x, const void* w, const
                            void* scratch, size_t scratch_bytes, int iters, void* stream);
 
 /*
- * Write the selector's table to a text file, one problem per line ("<key> | <choice>").
- * CONV_ERR_INVALID_ARG if the file cannot be written.
+ * Write the selector's table to a text file, one problem per line ("<key> | <choice>",
+ * then " | us=<time per call>" for a choice measured in this process), each measured
+ * problem followed by one comment line per candidate timed ("#", tab, "us=<time>", tab,
+ * the candidate's conv_plan_describe text).  CONV_ERR_INVALID_ARG if the file cannot be
+ * written.
  */
 conv_status conv_tune_table_save(const char* path);
 

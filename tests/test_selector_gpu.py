@@ -55,7 +55,14 @@ def test_tuned_plan_matches_oracle_and_table_round_trips(name, dtype, layer, tmp
         assert new_desc() == desc                  # later plans of the problem take the choice
         f = tmp_path / "table.txt"
         B.conv_tune_table_save(str(f))
-        assert len(f.read_text().splitlines()) == 1
+        lines = f.read_text().splitlines()
+        rows = [ln for ln in lines if not ln.startswith("#")]
+        log = [ln.split("\t") for ln in lines if ln.startswith("#")]
+        assert len(rows) == 1 and len(log) >= 2
+        # the row records the fastest candidate's time, and that candidate is the plan taken
+        us = {entry[2]: float(entry[1][3:]) for entry in log}
+        assert desc in us and us[desc] == min(us.values())
+        assert abs(float(rows[0].rsplit("us=", 1)[1]) - us[desc]) < 1e-3
         B.conv_tune_table_clear()
         B.conv_tune_table_load(str(f))
         assert new_desc() == desc
