@@ -50,6 +50,14 @@ def _load():
         lib.oracle_conv_fwd_points.argtypes = [P(ctypes.c_int64), ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                                ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+        for name in ("oracle_conv_bwd_data", "oracle_conv_bwd_weight"):
+            fn = getattr(lib, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [P(ctypes.c_int64), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                           ctypes.c_int]
+        lib.oracle_conv_bwd_points.restype = ctypes.c_int
+        lib.oracle_conv_bwd_points.argtypes = [P(ctypes.c_int64), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                               ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_gelu.restype = None
         lib.oracle_gelu.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
         _lib = lib
@@ -144,3 +152,63 @@ def gelu(v):
     out = np.empty_like(v)
     lib.oracle_gelu(v.ctypes.data, out.ctypes.data, v.size)
     return out
+
+
+def conv_bwd_data(geom: Geom, dy, w, nthreads=None):
+    """Gradient with respect to x (float64, N D H W G C) of the conv's linear part, given dy
+    (N Do Ho Wo G K), and S = sum |dy*w| per element (page "composable_kernel
+    dispatcher/heuristics/LEARNINGS_GROUPED_CONV.md", section 6: the bwd_data variant)."""
+    lib = _load()
+    dy = _f32(dy).reshape(geom.y_shape())
+    w = _f32(w).reshape(geom.w_shape())
+    if min(geom.out_spatial) <= 0:
+        raise ValueError("empty output")
+    out = np.empty(geom.x_shape(), dtype=np.float64)
+    absum = np.empty(geom.x_shape(), dtype=np.float64)
+    p = geom.params()
+    rc = lib.oracle_conv_bwd_data(p.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), dy.ctypes.data, w.ctypes.data,
+                                  out.ctypes.data, absum.ctypes.data, int(nthreads or os.cpu_count() or 1))
+    if rc != 0:
+        raise ValueError("oracle rejected the problem")
+    return out, absum
+
+
+def conv_bwd_weight(geom: Geom, x, dy, nthreads=None):
+    """Gradient with respect to w (float64, G K Z Y X C) given x and dy, and S = sum |dy*x|
+    per element (same page, section 6: the bwd_weight variant)."""
+    lib = _load()
+    x = _f32(x).reshape(geom.x_shape())
+    dy = _f32(dy).reshape(geom.y_shape())
+    if min(geom.out_spatial) <= 0:
+        raise ValueError("empty output")
+    out = np.empty(geom.w_shape(), dtype=np.float64)
+    absum = np.empty(geom.w_shape(), dtype=np.float64)
+    p = geom.params()
+    rc = lib.oracle_conv_bwd_weight(p.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), x.ctypes.data,
+                                    dy.ctypes.data, out.ctypes.data, absum.ctypes.data,
+                                    int(nthreads or os.cpu_count() or 1))
+    if rc != 0:
+        raise ValueError("oracle rejected the problem")
+    return out, absum
+
+
+def conv_bwd_points(geom: Geom, a, b, weight: bool, idx):
+    """Selected backward elements and their S.  weight=False: a = dy, b = w, idx rows of
+    (n, d, h, w, g, c); weight=True: a = x, b = dy, idx rows of (g, k, z, y, x, c)."""
+    lib = _load()
+    if weight:
+        a = _f32(a).reshape(geom.x_shape())
+        b = _f32(b).reshape(geom.y_shape())
+    else:
+        a = _f32(a).reshape(geom.y_shape())
+        b = _f32(b).reshape(geom.w_shape())
+    idx = np.ascontiguousarray(idx, dtype=np.int64).reshape(-1, 6)
+    out = np.empty(len(idx), dtype=np.float64)
+    absum = np.empty(len(idx), dtype=np.float64)
+    p = geom.params()
+    rc = lib.oracle_conv_bwd_points(p.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), a.ctypes.data,
+                                    b.ctypes.data, int(bool(weight)), idx.ctypes.data, len(idx), out.ctypes.data,
+                                    absum.ctypes.data)
+    if rc != 0:
+        raise ValueError("bad problem or index")
+    return out, absum

@@ -182,3 +182,183 @@ void oracle_gelu(const double* v, double* out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = gelu_exact(v[i]);
 }
+
+/*
+ * Backward passes of the same convolution (the "bwd_data" and "bwd_weight" variants that
+ * the page "composable_kernel dispatcher/heuristics/LEARNINGS_GROUPED_CONV.md", section 6,
+ * names for the same NHWGC / GKYXC / NHWGK layouts).  Given dy, the gradient of a loss with
+ * respect to the forward output (N Do Ho Wo G K), these are the gradients with respect to x
+ * and w of the linear map x, w -> sum x*w written above (bias and GELU are outside it):
+ *
+ *   dx[n,i,g,c] = sum over k and taps t of dy[n,o,g,k] * w[g,k,t,c], over the (t, o) with
+ *                 o*s - p + t*d = i in every spatial dimension (o in range)
+ *   dw[g,k,t,c] = sum over n and output positions o of dy[n,o,g,k] * x[n, o*s - p + t*d, g, c],
+ *                 over the o whose input position is in range
+ *
+ * Each is written out from its own definition: dx solves o = (i + p - t*d) / s for every tap
+ * and keeps the exact, in-range quotients; dw walks every output position per tap.  Both
+ * return S = sum |products| per element, as the forward does.
+ */
+
+/* the output position that tap t maps onto input position i in one dimension, or -1 */
+static int64_t source_pos(int64_t i, int64_t t, int64_t s, int64_t p, int64_t d, int64_t O)
+{
+    int64_t num = i + p - t * d;
+    if (num < 0 || num % s != 0) return -1;
+    int64_t o = num / s;
+    return o < O ? o : -1;
+}
+
+static void one_dx(const oracle_geom* g, const float* dy, const float* w, int64_t n, int64_t id,
+                   int64_t ih, int64_t iw, int64_t gi, int64_t c, double* out, double* absum)
+{
+    double acc = 0.0, s = 0.0;
+    for (int64_t z = 0; z < g->Z; ++z) {
+        int64_t od = source_pos(id, z, g->sd, g->pd, g->dd, g->Do);
+        if (od < 0) continue;
+        for (int64_t y = 0; y < g->Y; ++y) {
+            int64_t oh = source_pos(ih, y, g->sh, g->ph, g->dh, g->Ho);
+            if (oh < 0) continue;
+            for (int64_t xx = 0; xx < g->X; ++xx) {
+                int64_t ow = source_pos(iw, xx, g->sw, g->pw, g->dw, g->Wo);
+                if (ow < 0) continue;
+                const float* dyp = dy + ((((n * g->Do + od) * g->Ho + oh) * g->Wo + ow) * g->G + gi) * g->K;
+                for (int64_t k = 0; k < g->K; ++k) {
+                    double prod = (double)dyp[k] *
+                                  (double)w[((((gi * g->K + k) * g->Z + z) * g->Y + y) * g->X + xx) * g->C + c];
+                    acc += prod;
+                    s += fabs(prod);
+                }
+            }
+        }
+    }
+    *out = acc;
+    if (absum) *absum = s;
+}
+
+static void one_dw(const oracle_geom* g, const float* x, const float* dy, int64_t gi, int64_t k, int64_t z,
+                   int64_t y, int64_t xx, int64_t c, double* out, double* absum)
+{
+    double acc = 0.0, s = 0.0;
+    for (int64_t n = 0; n < g->N; ++n)
+        for (int64_t od = 0; od < g->Do; ++od) {
+            int64_t id = od * g->sd - g->pd + z * g->dd;
+            if (id < 0 || id >= g->D) continue;
+            for (int64_t oh = 0; oh < g->Ho; ++oh) {
+                int64_t ih = oh * g->sh - g->ph + y * g->dh;
+                if (ih < 0 || ih >= g->H) continue;
+                for (int64_t ow = 0; ow < g->Wo; ++ow) {
+                    int64_t iw = ow * g->sw - g->pw + xx * g->dw;
+                    if (iw < 0 || iw >= g->W) continue;
+                    double prod = (double)dy[((((n * g->Do + od) * g->Ho + oh) * g->Wo + ow) * g->G + gi) * g->K + k] *
+                                  (double)x[((((n * g->D + id) * g->H + ih) * g->W + iw) * g->G + gi) * g->C + c];
+                    acc += prod;
+                    s += fabs(prod);
+                }
+            }
+        }
+    *out = acc;
+    if (absum) *absum = s;
+}
+
+typedef struct {
+    const oracle_geom* g;
+    const float *a, *b;     /* dx: dy, w;  dw: x, dy */
+    double *out, *absum;
+    int64_t begin, end;     /* dx: rows (n, id, ih);  dw: (g, k) pairs */
+} bwd_job;
+
+static void* run_dx_rows(void* arg)
+{
+    bwd_job* j = (bwd_job*)arg;
+    const oracle_geom* g = j->g;
+    for (int64_t r = j->begin; r < j->end; ++r) {
+        int64_t ih = r % g->H, t = r / g->H;
+        int64_t id = t % g->D, n = t / g->D;
+        for (int64_t iw = 0; iw < g->W; ++iw)
+            for (int64_t gi = 0; gi < g->G; ++gi)
+                for (int64_t c = 0; c < g->C; ++c) {
+                    int64_t e = ((r * g->W + iw) * g->G + gi) * g->C + c;
+                    one_dx(g, j->a, j->b, n, id, ih, iw, gi, c, &j->out[e], j->absum ? &j->absum[e] : NULL);
+                }
+    }
+    return NULL;
+}
+
+static void* run_dw_pairs(void* arg)
+{
+    bwd_job* j = (bwd_job*)arg;
+    const oracle_geom* g = j->g;
+    const int64_t per = g->Z * g->Y * g->X * g->C;
+    for (int64_t r = j->begin; r < j->end; ++r) {
+        int64_t gi = r / g->K, k = r % g->K;
+        for (int64_t z = 0; z < g->Z; ++z)
+            for (int64_t y = 0; y < g->Y; ++y)
+                for (int64_t xx = 0; xx < g->X; ++xx)
+                    for (int64_t c = 0; c < g->C; ++c) {
+                        int64_t e = r * per + ((z * g->Y + y) * g->X + xx) * g->C + c;
+                        one_dw(g, j->a, j->b, gi, k, z, y, xx, c, &j->out[e], j->absum ? &j->absum[e] : NULL);
+                    }
+    }
+    return NULL;
+}
+
+static int run_bwd(const int64_t* params, const float* a, const float* b, double* out, double* absum,
+                   int nthreads, int weight)
+{
+    oracle_geom g;
+    if (fill_geom(&g, params)) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    int64_t rows = weight ? g.G * g.K : g.N * g.D * g.H;
+    if (nthreads > rows) nthreads = (int)rows;
+    pthread_t th[256];
+    bwd_job jobs[256];
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i].g = &g; jobs[i].a = a; jobs[i].b = b; jobs[i].out = out; jobs[i].absum = absum;
+        jobs[i].begin = rows * i / nthreads;
+        jobs[i].end = rows * (i + 1) / nthreads;
+    }
+    void* (*fn)(void*) = weight ? run_dw_pairs : run_dx_rows;
+    for (int i = 1; i < nthreads; ++i) pthread_create(&th[i], NULL, fn, &jobs[i]);
+    fn(&jobs[0]);
+    for (int i = 1; i < nthreads; ++i) pthread_join(th[i], NULL);
+    return 0;
+}
+
+/* Backward data.  dy: N Do Ho Wo G K; w: G K Z Y X C; dx, absum: N D H W G C doubles. */
+int oracle_conv_bwd_data(const int64_t* params, const float* dy, const float* w, double* dx, double* absum,
+                         int nthreads)
+{
+    return run_bwd(params, dy, w, dx, absum, nthreads, 0);
+}
+
+/* Backward weight.  x: N D H W G C; dy: N Do Ho Wo G K; dw, absum: G K Z Y X C doubles. */
+int oracle_conv_bwd_weight(const int64_t* params, const float* x, const float* dy, double* dw, double* absum,
+                           int nthreads)
+{
+    return run_bwd(params, x, dy, dw, absum, nthreads, 1);
+}
+
+/* Selected elements only (rows of n, d, h, w, g, c for dx; g, k, z, y, x, c for dw). */
+int oracle_conv_bwd_points(const int64_t* params, const float* a, const float* b, int weight, const int64_t* idx,
+                           int64_t npts, double* out, double* absum)
+{
+    oracle_geom g;
+    if (fill_geom(&g, params)) return -1;
+    for (int64_t p = 0; p < npts; ++p) {
+        const int64_t* q = idx + 6 * p;
+        if (weight) {
+            if (q[0] < 0 || q[0] >= g.G || q[1] < 0 || q[1] >= g.K || q[2] < 0 || q[2] >= g.Z || q[3] < 0 ||
+                q[3] >= g.Y || q[4] < 0 || q[4] >= g.X || q[5] < 0 || q[5] >= g.C)
+                return -1;
+            one_dw(&g, a, b, q[0], q[1], q[2], q[3], q[4], q[5], &out[p], absum ? &absum[p] : NULL);
+        } else {
+            if (q[0] < 0 || q[0] >= g.N || q[1] < 0 || q[1] >= g.D || q[2] < 0 || q[2] >= g.H || q[3] < 0 ||
+                q[3] >= g.W || q[4] < 0 || q[4] >= g.G || q[5] < 0 || q[5] >= g.C)
+                return -1;
+            one_dx(&g, a, b, q[0], q[1], q[2], q[3], q[4], q[5], &out[p], absum ? &absum[p] : NULL);
+        }
+    }
+    return 0;
+}

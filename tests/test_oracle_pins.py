@@ -278,13 +278,17 @@ def test_points_match_full_output():
 
 # ---------------------------------------------------------------- the pins have teeth
 MUTANTS = {
-    "stride_for_dilation": ("ow * g->sw - g->pw + xx * g->dw", "ow * g->sw - g->pw + xx * g->sw"),
-    "pad_sign": ("oh * g->sh - g->ph + y * g->dh", "oh * g->sh + g->ph + y * g->dh"),
-    "transposed_weight_groups": ("((((gi * g->K + k) * g->Z", "((((k * g->G + gi) * g->Z"),
+    "stride_for_dilation": ("int64_t iw = ow * g->sw - g->pw + xx * g->dw;\n                if",
+                            "int64_t iw = ow * g->sw - g->pw + xx * g->sw;\n                if"),
+    "pad_sign": ("int64_t ih = oh * g->sh - g->ph + y * g->dh;\n            if",
+                 "int64_t ih = oh * g->sh + g->ph + y * g->dh;\n            if"),
+    "transposed_weight_groups": ("const float* wp = w + ((((gi * g->K + k) * g->Z",
+                                 "const float* wp = w + ((((k * g->G + gi) * g->Z"),
     "dropped_bias": ("if (bias) acc += (double)bias[gi * g->K + k];", "if (bias) acc += 0.0;"),
     "tanh_gelu": ("0.5 * v * (1.0 + erf(v / sqrt(2.0)))",
                   "0.5 * v * (1.0 + tanh(sqrt(2.0 / 3.141592653589793) * (v + 0.044715 * v * v * v)))"),
-    "signed_absum": ("s += fabs(prod);", "s += prod;"),
+    "signed_absum": ("s += fabs(prod);\n                }\n            }\n        }\n    }\n    if (bias)",
+                     "s += prod;\n                }\n            }\n        }\n    }\n    if (bias)"),
     "out_len": ("in + 2 * pad - dil * (filt - 1) - 1", "in + 2 * pad - dil * filt"),
     "flipped_kernel": ("const float* wp = w + ((((gi * g->K + k) * g->Z + z) * g->Y + y) * g->X + xx) * g->C;",
                        "const float* wp = w + ((((gi * g->K + k) * g->Z + z) * g->Y + y) * g->X + (g->X - 1 - xx)) * g->C;"),
@@ -328,3 +332,197 @@ def test_pins_catch_planted_mistakes():
             subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-shared", "-fPIC", "-o", so, path,
                                    "-lm", "-lpthread"])
             assert not _check_all_pins(so), f"mutant {name} passed every pin"
+
+
+# ---------------------------------------------------------------- backward passes
+def torch_conv_grads_f64(g: oracle.Geom, x, w, dy):
+    """dx and dw of sum(conv(x, w) * dy) by torch autograd in float64 on the CPU (the
+    library's own convolution backward), layouts permuted back to channels-last."""
+    nd = g.ndim
+    xs = np.asarray(x, np.float64).reshape(g.N, *g.spatial[3 - nd:], g.G * g.C)
+    xt = torch.from_numpy(np.moveaxis(xs, -1, 1).copy()).requires_grad_(True)
+    ws = np.asarray(w, np.float64).reshape(g.G * g.K, *g.filt[3 - nd:], g.C)
+    wt = torch.from_numpy(np.moveaxis(ws, -1, 1).copy()).requires_grad_(True)
+    fn = {1: torch.nn.functional.conv1d, 2: torch.nn.functional.conv2d, 3: torch.nn.functional.conv3d}[nd]
+    yt = fn(xt, wt, None, stride=g.stride[3 - nd:], padding=g.pad[3 - nd:], dilation=g.dilation[3 - nd:],
+            groups=g.G)
+    dys = np.asarray(dy, np.float64).reshape(g.N, *g.out_spatial[3 - nd:], g.G * g.K)
+    (yt * torch.from_numpy(np.moveaxis(dys, -1, 1).copy())).sum().backward()
+    dx = np.moveaxis(xt.grad.numpy(), 1, -1).reshape(g.x_shape())
+    dw = np.moveaxis(wt.grad.numpy(), 1, -1).reshape(g.w_shape())
+    return dx, dw
+
+
+def gen_dy(g, seed, dtype="f32"):
+    return syn.as_f32(syn.gen_normal(seed, g.y_shape(), dtype), dtype)
+
+
+def gen_int_case(g, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.integers(-3, 4, g.x_shape()).astype(np.float32)
+    w = rng.integers(-3, 4, g.w_shape()).astype(np.float32)
+    dy = rng.integers(-3, 4, g.y_shape()).astype(np.float32)
+    return x, w, dy
+
+
+@pytest.mark.parametrize("ndim", [1, 2, 3])
+def test_backward_matches_torch_autograd_f64(ndim):
+    """Library routine: torch's fp64 convolution backward (groups, stride, pad, dilation)."""
+    rng = np.random.default_rng(500 + ndim)
+    for case in range(20 if ndim < 3 else 10):
+        g = rand_problem(rng, ndim)
+        x, w, _ = gen_case(g, 5000 * ndim + case, with_bias=False)
+        dy = gen_dy(g, 5000 * ndim + case + 7)
+        dx, Sx = oracle.conv_bwd_data(g, dy, w, nthreads=2)
+        dw, Sw = oracle.conv_bwd_weight(g, x, dy, nthreads=3)
+        rdx, rdw = torch_conv_grads_f64(g, x, w, dy)
+        np.testing.assert_allclose(dx, rdx, rtol=0, atol=1e-12 * (1.0 + Sx.max()))
+        np.testing.assert_allclose(dw, rdw, rtol=0, atol=1e-12 * (1.0 + Sw.max()))
+
+
+def test_backward_absum_is_backward_of_magnitudes():
+    """S of each backward element equals the same backward applied to |dy| and |w| (|x|), by torch."""
+    rng = np.random.default_rng(510)
+    for ndim in (1, 2, 3):
+        for case in range(5):
+            g = rand_problem(rng, ndim)
+            x, w, _ = gen_case(g, 5100 + 10 * ndim + case, with_bias=False)
+            dy = gen_dy(g, 5200 + 10 * ndim + case)
+            _, Sx = oracle.conv_bwd_data(g, dy, w)
+            _, Sw = oracle.conv_bwd_weight(g, x, dy)
+            rdx, rdw = torch_conv_grads_f64(g, np.abs(x), np.abs(w), np.abs(dy))
+            np.testing.assert_allclose(Sx, rdx, rtol=1e-13, atol=1e-13)
+            np.testing.assert_allclose(Sw, rdw, rtol=1e-13, atol=1e-13)
+
+
+def test_backward_brute_force_impulse_responses():
+    """On tiny integer problems, every dx element is <conv(e_i, w), dy> and every dw element
+    is <conv(x, e_j), dy>, with the forward oracle run on unit impulses: exact."""
+    rng = np.random.default_rng(520)
+    for ndim in (1, 2, 3):
+        for case in range(3):
+            g = rand_problem(rng, ndim)
+            x, w, dy = gen_int_case(g, 5300 + 10 * ndim + case)
+            dx, _ = oracle.conv_bwd_data(g, dy, w)
+            dw, _ = oracle.conv_bwd_weight(g, x, dy)
+            bdx = np.empty(x.size)
+            for i in range(x.size):
+                e = np.zeros(x.size, np.float32)
+                e[i] = 1.0
+                bdx[i] = float((oracle.conv_fwd(g, e, w)[0] * dy).sum())
+            bdw = np.empty(w.size)
+            for j in range(w.size):
+                e = np.zeros(w.size, np.float32)
+                e[j] = 1.0
+                bdw[j] = float((oracle.conv_fwd(g, x, e)[0] * dy).sum())
+            assert np.array_equal(dx.reshape(-1), bdx), (ndim, case)
+            assert np.array_equal(dw.reshape(-1), bdw), (ndim, case)
+
+
+def test_backward_adjoint_identity_exact_on_integers():
+    """<conv(x, w), dy> = <x, dx(dy, w)> = <w, dw(x, dy)>, exactly on integer inputs."""
+    rng = np.random.default_rng(530)
+    for ndim in (1, 2, 3):
+        for case in range(10):
+            g = rand_problem(rng, ndim)
+            x, w, dy = gen_int_case(g, 5400 + 10 * ndim + case)
+            y, _ = oracle.conv_fwd(g, x, w)
+            lhs = float((y * dy).sum())
+            assert lhs == float((oracle.conv_bwd_data(g, dy, w)[0] * x).sum())
+            assert lhs == float((oracle.conv_bwd_weight(g, x, dy)[0] * w).sum())
+
+
+def test_backward_pointwise_is_matmul():
+    """1x1 kernel, stride 1, no padding: dx = dY W and dw = dY^T X per group (numpy)."""
+    g = oracle.Geom(2, 3, 5, 4, (3, 4, 5), (1, 1, 1), (1, 1, 1), (0, 0, 0), (1, 1, 1))
+    x, w, _ = gen_case(g, 43, with_bias=False)
+    dy = gen_dy(g, 44)
+    X = x.reshape(-1, g.G, g.C).astype(np.float64)
+    W = w.reshape(g.G, g.K, g.C).astype(np.float64)
+    DY = dy.reshape(-1, g.G, g.K).astype(np.float64)
+    dx, _ = oracle.conv_bwd_data(g, dy, w)
+    dw, _ = oracle.conv_bwd_weight(g, x, dy)
+    np.testing.assert_allclose(dx.reshape(-1, g.G, g.C), np.einsum("mgk,gkc->mgc", DY, W), rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(dw.reshape(g.G, g.K, g.C), np.einsum("mgk,mgc->gkc", DY, X), rtol=1e-13,
+                               atol=1e-13)
+
+
+def test_stride1_backward_data_is_a_forward_conv_with_flipped_transposed_weights():
+    """Textbook: at stride 1, dx = conv(dy, w') with w'[g,c,t,k] = w[g,k,F-1-t,c] and padding
+    dil*(F-1) - pad (the transposed convolution)."""
+    rng = np.random.default_rng(540)
+    for ndim in (1, 2, 3):
+        for case in range(4):
+            g = rand_problem(rng, ndim)
+            fl = g.filt[3 - ndim:]
+            dl = g.dilation[3 - ndim:]
+            pd = g.pad[3 - ndim:]
+            if any(d * (f - 1) - p < 0 for f, d, p in zip(fl, dl, pd)):
+                continue
+            g = oracle.Geom(g.N, g.G, g.C, g.K, g.spatial[3 - ndim:], fl, (1,) * ndim, pd, dl)
+            _, w, _ = gen_case(g, 5500 + 10 * ndim + case, with_bias=False)
+            dy = gen_dy(g, 5600 + 10 * ndim + case)
+            dx, _ = oracle.conv_bwd_data(g, dy, w)
+            wf = w.reshape(g.w_shape())[:, :, ::-1, ::-1, ::-1, :]             # flip every tap axis
+            wt = np.ascontiguousarray(np.moveaxis(wf, (1, 5), (5, 1)))          # G C Z Y X K
+            gt = oracle.Geom(g.N, g.G, g.K, g.C, g.out_spatial[3 - ndim:], fl, (1,) * ndim,
+                             [d * (f - 1) - p for f, d, p in zip(fl, dl, pd)], dl)
+            assert gt.out_spatial == g.spatial
+            ref, _ = oracle.conv_fwd(gt, dy, wt)
+            np.testing.assert_allclose(dx, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_backward_points_match_full_output():
+    rng = np.random.default_rng(550)
+    g = rand_problem(rng, 3)
+    x, w, _ = gen_case(g, 55, with_bias=False)
+    dy = gen_dy(g, 56)
+    for weight, (full, S) in ((False, oracle.conv_bwd_data(g, dy, w)), (True, oracle.conv_bwd_weight(g, x, dy))):
+        idx = np.array(np.unravel_index(np.arange(full.size), full.shape)).T
+        pts, ps = oracle.conv_bwd_points(g, x if weight else dy, dy if weight else w, weight, idx)
+        assert np.array_equal(pts, full.reshape(-1)) and np.array_equal(ps, S.reshape(-1))
+
+
+BWD_MUTANTS = {
+    "dx_no_divisibility": ("if (num < 0 || num % s != 0) return -1;", "if (num < 0) return -1;"),
+    "dx_pad_sign": ("int64_t num = i + p - t * d;", "int64_t num = i - p - t * d;"),
+    "dx_flipped_tap": ("int64_t ow = source_pos(iw, xx, g->sw, g->pw, g->dw, g->Wo);",
+                       "int64_t ow = source_pos(iw, g->X - 1 - xx, g->sw, g->pw, g->dw, g->Wo);"),
+    "dx_weight_k_c_swapped": ("(double)w[((((gi * g->K + k) * g->Z + z) * g->Y + y) * g->X + xx) * g->C + c];",
+                              "(double)w[((((gi * g->K + (k % g->C) % g->K) * g->Z + z) * g->Y + y) * g->X + xx) * g->C + (c % g->K) % g->C];"),
+    "dw_dilation_for_stride": ("int64_t iw = ow * g->sw - g->pw + xx * g->dw;\n                    if (iw < 0",
+                               "int64_t iw = ow * g->dw - g->pw + xx * g->sw;\n                    if (iw < 0"),
+    "dw_skips_batch": ("for (int64_t n = 0; n < g->N; ++n)\n        for (int64_t od",
+                       "for (int64_t n = 0; n < 1; ++n)\n        for (int64_t od"),
+}
+
+
+def _check_bwd_pins(lib_path):
+    saved, orig_build = oracle._lib, oracle.build
+    try:
+        oracle._lib = None
+        oracle.build = lambda force=False: lib_path
+        for fn in (lambda: test_backward_matches_torch_autograd_f64(1),
+                   lambda: test_backward_matches_torch_autograd_f64(2),
+                   lambda: test_backward_matches_torch_autograd_f64(3)):
+            fn()
+        return True
+    except Exception:
+        return False
+    finally:
+        oracle.build = orig_build
+        oracle._lib = saved
+
+
+def test_backward_pins_catch_planted_mistakes():
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "conv_oracle.c")).read()
+    with tempfile.TemporaryDirectory() as td:
+        for name, (old, new) in BWD_MUTANTS.items():
+            assert src.count(old) == 1, name
+            path = os.path.join(td, f"{name}.c")
+            with open(path, "w") as f:
+                f.write(src.replace(old, new))
+            so = os.path.join(td, f"lib{name}.so")
+            subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-shared", "-fPIC", "-o", so, path,
+                                   "-lm", "-lpthread"])
+            assert not _check_bwd_pins(so), f"mutant {name} passed every backward pin"
