@@ -53,6 +53,14 @@ _SIGS = {
     "conv_plan_flops": (ctypes.c_double, [_VP]),
     "conv_fwd_static_scratch": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP]),
     "conv_plan_set_overlap": (ctypes.c_int, [_VP, ctypes.c_int]),
+    "conv_bwd_data_plan_create": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                                 ctypes.c_int64, ctypes.c_int64, _I64P, _I64P, _I64P, _I64P, _I64P,
+                                                 ctypes.c_int]),
+    "conv_bwd_data": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP]),
+    "conv_bwd_weight_plan_create": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, ctypes.c_int64,
+                                                   ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _I64P, _I64P,
+                                                   _I64P, _I64P, _I64P, ctypes.c_int]),
+    "conv_bwd_weight": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP]),
     "conv_tune_scratch_bytes": (ctypes.c_size_t, [_VP]),
     "conv_plan_tune": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, ctypes.c_int, _VP]),
     "conv_tune_table_save": (ctypes.c_int, [ctypes.c_char_p]),
@@ -111,6 +119,32 @@ def conv_plan_create(ndim, N, G, C, K, spatial, filter, stride, pad, dilation, d
                                          int(dtype), int(epilogue))
     _check(st, "conv_plan_create")
     return h.value
+
+
+def conv_bwd_data_plan_create(ndim, N, G, C, K, spatial, filter, stride, pad, dilation, dtype) -> int:
+    h = _VP()
+    st = load_library().conv_bwd_data_plan_create(ctypes.byref(h), int(ndim), int(N), int(G), int(C), int(K),
+                                                  _arr(spatial), _arr(filter), _arr(stride), _arr(pad),
+                                                  _arr(dilation), int(dtype))
+    _check(st, "conv_bwd_data_plan_create")
+    return h.value
+
+
+def conv_bwd_weight_plan_create(ndim, N, G, C, K, spatial, filter, stride, pad, dilation, dtype) -> int:
+    h = _VP()
+    st = load_library().conv_bwd_weight_plan_create(ctypes.byref(h), int(ndim), int(N), int(G), int(C), int(K),
+                                                    _arr(spatial), _arr(filter), _arr(stride), _arr(pad),
+                                                    _arr(dilation), int(dtype))
+    _check(st, "conv_bwd_weight_plan_create")
+    return h.value
+
+
+def conv_bwd_data(plan: int, dy_ptr: int, w_packed_ptr: int, dx_ptr: int, stream: int = 0):
+    _check(load_library().conv_bwd_data(plan, dy_ptr, w_packed_ptr, dx_ptr, stream or None), "conv_bwd_data")
+
+
+def conv_bwd_weight(plan: int, x_ptr: int, dy_ptr: int, dw_ptr: int, stream: int = 0):
+    _check(load_library().conv_bwd_weight(plan, x_ptr, dy_ptr, dw_ptr, stream or None), "conv_bwd_weight")
 
 
 def conv_plan_output_shape(plan: int, ndim: int):
@@ -196,12 +230,23 @@ def conv_plan_flops(plan: int) -> float:
 class ConvPlan:
     """One plan plus the device buffers it needs (packed weights, workspace), allocated
     with PyTorch on the current device.  Tensors are channels-last, dtype float32 or
-    bfloat16 matching the plan."""
+    bfloat16 matching the plan.  direction: "fwd" (conv_fwd), "bwd_data" (conv_bwd_data)
+    or "bwd_weight" (conv_bwd_weight); the backward plans take the forward problem's
+    description and ignore the epilogue."""
 
-    def __init__(self, ndim, N, G, C, K, spatial, filter, stride, pad, dilation, dtype, epilogue):
+    def __init__(self, ndim, N, G, C, K, spatial, filter, stride, pad, dilation, dtype, epilogue,
+                 direction="fwd"):
         self.ndim, self.N, self.G, self.C, self.K = int(ndim), int(N), int(G), int(C), int(K)
-        self.dtype, self.epilogue = int(dtype), int(epilogue)
-        self.handle = conv_plan_create(ndim, N, G, C, K, spatial, filter, stride, pad, dilation, dtype, epilogue)
+        self.dtype, self.epilogue, self.direction = int(dtype), int(epilogue), direction
+        if direction == "fwd":
+            self.handle = conv_plan_create(ndim, N, G, C, K, spatial, filter, stride, pad, dilation, dtype, epilogue)
+        elif direction == "bwd_data":
+            self.handle = conv_bwd_data_plan_create(ndim, N, G, C, K, spatial, filter, stride, pad, dilation, dtype)
+        elif direction == "bwd_weight":
+            self.handle = conv_bwd_weight_plan_create(ndim, N, G, C, K, spatial, filter, stride, pad, dilation,
+                                                      dtype)
+        else:
+            raise ValueError(f"unknown direction {direction!r}")
         self.spatial = tuple(int(v) for v in spatial)
         self.filter = tuple(int(v) for v in filter)
         self.out_spatial = conv_plan_output_shape(self.handle, self.ndim)
@@ -255,6 +300,20 @@ class ConvPlan:
         conv_fwd(self.handle, x.data_ptr(), self.w_packed.data_ptr(), 0 if bias is None else bias.data_ptr(),
                  y.data_ptr(), s)
         return y
+
+    def backward_data(self, dy, dx, stream=None):
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream(dy.device).cuda_stream
+        conv_bwd_data(self.handle, dy.data_ptr(), self.w_packed.data_ptr(), dx.data_ptr(), s)
+        return dx
+
+    def backward_weight(self, x, dy, dw, stream=None):
+        import torch
+        if self.workspace is None and conv_workspace_bytes(self.handle):
+            self.allocate(x.device)
+        s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
+        conv_bwd_weight(self.handle, x.data_ptr(), dy.data_ptr(), dw.data_ptr(), s)
+        return dw
 
     def set_overlap(self, enable: bool = True):
         conv_plan_set_overlap(self.handle, enable)

@@ -153,6 +153,39 @@ __global__ void prepack_simt_kernel(const T* __restrict__ w, T* __restrict__ out
     }
 }
 
+// Backward data at unit stride: the forward weight of the transposed problem,
+// w'[g][c][tap'][k] = w[g][k][taps-1-tap'][c] (every tap axis flipped, C and K swapped),
+// element type E (2 or 4 bytes), staged for the forward prepack.
+template <typename E>
+__global__ void flip_transpose_kernel(const E* __restrict__ w, E* __restrict__ out, int K, int C, int taps,
+                                      long long total) {
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int k = (int)(idx % K);
+        long long r = idx / K;
+        const int t = (int)(r % taps); r /= taps;
+        const int c = (int)(r % C);
+        const long long g = r / C;
+        out[idx] = w[((g * K + k) * taps + (taps - 1 - t)) * C + c];
+    }
+}
+
+// Backward data on the FFMA pipe: [G][taps*K][Cpad] with B[(tap, k)][c] = w[g][k][tap][c].
+template <typename T>
+__global__ void prepack_dg_simt_kernel(const T* __restrict__ w, T* __restrict__ out, int K, int C, int taps, int Kg,
+                                       int Cpad, long long total) {
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(idx % Cpad);
+        const long long r = idx / Cpad;
+        const int kk = (int)(r % Kg);
+        const int g = (int)(r / Kg);
+        const int tap = kk / K;
+        const int k = kk - tap * K;
+        out[idx] = c < C ? w[(((long long)g * K + k) * taps + tap) * C + c] : T(0.0f);
+    }
+}
+
 // ----------------------------------------------------------------------------- split-K reduction
 // y = epilogue(sum over splits, in split order, of the fp32 partials): a fixed order,
 // so results do not change from run to run.
@@ -203,7 +236,8 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, l
 }  // namespace
 
 // ----------------------------------------------------------------------------- plan
-enum Variant { VAR_TC = 0, VAR_SIMT = 1 };
+enum Variant { VAR_TC = 0, VAR_SIMT = 1, VAR_DG_SIMT = 2, VAR_WG_SIMT = 3 };
+enum Direction { DIR_FWD = 0, DIR_BWD_DATA = 1, DIR_BWD_WEIGHT = 2 };
 
 // Plan choices that can be fixed instead of decided by rule: by the measured selector
 // (conv_plan_tune and its table) or, for tests, by CONV_FORCE_* environment variables.
@@ -248,9 +282,16 @@ struct conv_plan {
     // SIMT plan
     int BM, Kg, Kpad, nkt, ktps, vec;
     size_t prepack_bytes, workspace_bytes;
+    size_t packed_bytes;    // the packed weight alone (prepack_bytes may add a staging area)
     void* workspace;
     size_t workspace_size;
     double flops;
+    // backward plans
+    int dir;                // Direction
+    Geom fg;                // the forward problem (g is the problem the kernels run)
+    int dg_fwd;             // backward data run as the forward conv of dy with flipped, transposed weights
+    size_t dg_src_off;      // where in w_packed the prepack stages those weights
+    int wg_kt, wg_jt, wg_mps;   // backward weight (FFMA): tiles along K and taps*C, pixels per split
     char desc[320];
 };
 
@@ -641,6 +682,8 @@ static void plan_simt(conv_plan* p) {
              g.G * p->splits, p->vec);
 }
 
+static size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
 // Variant and tiling of a plan whose geometry is set, under its choices p->ch (re-run by the
 // selector with other choices).  Starts from the caller's geometry (Go, Co, Ko).
 static void choose_variant(conv_plan* p) {
@@ -676,6 +719,13 @@ static void choose_variant(conv_plan* p) {
         p->pack = 1; g.G = (int)G; g.C = (int)C; g.K = (int)K;
         plan_simt(p);
     }
+    p->packed_bytes = p->prepack_bytes;
+    if (p->dg_fwd) {   // the flipped, transposed weights are staged behind the packed ones
+        p->dg_src_off = align256(p->prepack_bytes);
+        p->prepack_bytes = p->dg_src_off + (size_t)G * C * K * p->g.taps * (p->dtype == CONV_BF16 ? 2 : 4);
+        const size_t n = strlen(p->desc);
+        snprintf(p->desc + n, sizeof(p->desc) - n, " direction=bwd_data(transposed forward)");
+    }
 }
 
 // ----------------------------------------------------------------------------- measured selector
@@ -693,12 +743,12 @@ static std::string plan_key(const conv_plan* p) {
     char buf[400];
     snprintf(buf, sizeof(buf),
              "nd=%d N=%d G=%lld C=%lld K=%lld in=%lldx%lldx%lld f=%lldx%lldx%lld s=%lldx%lldx%lld p=%lldx%lldx%lld "
-             "d=%lldx%lldx%lld dtype=%d epi=%d sm=%d",
+             "d=%lldx%lldx%lld dtype=%d epi=%d dir=%d sm=%d",
              p->ndim, p->g.N, (long long)p->Go, (long long)p->Co, (long long)p->Ko, (long long)p->spatial[0],
              (long long)p->spatial[1], (long long)p->spatial[2], (long long)p->filter[0], (long long)p->filter[1],
              (long long)p->filter[2], (long long)p->stride[0], (long long)p->stride[1], (long long)p->stride[2],
              (long long)p->pad[0], (long long)p->pad[1], (long long)p->pad[2], (long long)p->dil[0],
-             (long long)p->dil[1], (long long)p->dil[2], (int)p->dtype, (int)p->epi, p->sm_count);
+             (long long)p->dil[1], (long long)p->dil[2], (int)p->dtype, (int)p->epi, p->dir, p->sm_count);
     return buf;
 }
 
@@ -737,19 +787,15 @@ static std::vector<conv_plan> tune_candidates(const conv_plan* p) {
     return out;
 }
 
-static size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
-
-extern "C" {
-
-conv_status conv_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, int64_t C, int64_t K,
-                             const int64_t* spatial, const int64_t* filter, const int64_t* stride,
-                             const int64_t* pad, const int64_t* dilation, conv_dtype dtype,
-                             conv_epilogue epilogue) {
+// Validation and the forward geometry shared by the three plan kinds; on success *pp is a
+// new plan with g = fg = the forward problem.
+static conv_status init_plan(conv_plan** pp, conv_plan_t* out, int ndim, int64_t N, int64_t G, int64_t C, int64_t K,
+                             const int64_t* spatial, const int64_t* filter, const int64_t* stride, const int64_t* pad,
+                             const int64_t* dilation, conv_dtype dtype) {
     if (!out) return CONV_ERR_INVALID_ARG;
     if (ndim < 1 || ndim > 3 || !spatial || !filter || !stride || !pad || !dilation) return CONV_ERR_INVALID_ARG;
     if (N < 1 || G < 1 || C < 1 || K < 1) return CONV_ERR_INVALID_ARG;
     if (dtype != CONV_F32 && dtype != CONV_BF16) return CONV_ERR_INVALID_ARG;
-    if (epilogue < CONV_EPI_NONE || epilogue > CONV_EPI_GELU) return CONV_ERR_INVALID_ARG;
     int64_t sp[3] = {1, 1, 1}, fl[3] = {1, 1, 1}, st[3] = {1, 1, 1}, pa[3] = {0, 0, 0}, di[3] = {1, 1, 1},
             os[3];
     const int off = 3 - ndim;   // conv1d -> D = H = 1, conv2d -> D = 1
@@ -782,7 +828,6 @@ conv_status conv_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, i
         p->pad[i] = pa[i]; p->dil[i] = di[i]; p->out_spatial[i] = os[i];
     }
     p->dtype = dtype;
-    p->epi = epilogue;
     Geom& g = p->g;
     g.N = (int)N; g.G = (int)G; g.C = (int)C; g.K = (int)K;
     g.D = (int)sp[0]; g.H = (int)sp[1]; g.W = (int)sp[2];
@@ -793,15 +838,139 @@ conv_status conv_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, i
     g.Do = (int)os[0]; g.Ho = (int)os[1]; g.Wo = (int)os[2];
     g.M = (int)M;
     g.taps = (int)taps;
+    p->fg = g;
+    // useful FLOPs of the forward problem; each backward pass does the same number
     p->flops = 2.0 * (double)M * (double)G * (double)K * (double)taps * (double)C;
     p->sm_count = query_sm_count();
     p->Go = g.G; p->Co = g.C; p->Ko = g.K;
+    *pp = p;
+    return CONV_OK;
+}
+
+// Backward data on the FFMA pipe: rows are the N*D*H*W input pixels, columns the C input
+// channels of a group, the reduction index tap*K + k; packed weight [G][taps*K][Cpad].
+static void plan_dg_simt(conv_plan* p) {
+    const Geom& f = p->fg;
+    p->variant = VAR_DG_SIMT;
+    const int rows = f.N * f.D * f.H * f.W;
+    p->Kg = f.taps * f.K;
+    p->nkt = (int)cdiv(p->Kg, 8);
+    p->num_nt = (int)cdiv(f.C, 128);
+    p->Kpad = p->num_nt * 128;
+    const int64_t tiles128 = cdiv(rows, 128) * p->num_nt * f.G;
+    p->BM = tiles128 >= p->sm_count ? 128 : 64;
+    p->num_mt = (int)cdiv(rows, p->BM);
+    const int64_t tiles = (int64_t)p->num_mt * p->num_nt * f.G;
+    int splits = 1;
+    if (tiles < p->sm_count && p->nkt >= 32) {
+        splits = (int)std::min<int64_t>(p->sm_count / tiles, p->nkt / 16);
+        splits = std::max(1, std::min(splits, 16));
+    }
+    p->ktps = (int)cdiv(p->nkt, splits);
+    p->splits = (int)cdiv(p->nkt, p->ktps);
+    p->vec = (f.C % 4 == 0 && f.K % 4 == 0) ? 1 : 0;
+    const size_t esz = p->dtype == CONV_BF16 ? 2 : 4;
+    p->prepack_bytes = (size_t)f.G * p->Kg * p->Kpad * esz;
+    p->packed_bytes = p->prepack_bytes;
+    p->workspace_bytes = p->splits > 1 ? (size_t)p->splits * rows * f.G * f.C * sizeof(float) : 0;
+    snprintf(p->desc, sizeof(p->desc),
+             "variant=simt_%s direction=bwd_data(gather) tile=%dx128 k_step=8 splits=%d grid=%dx%dx%d vec=%d",
+             p->dtype == CONV_BF16 ? "bf16" : "f32", p->BM, p->splits, p->num_mt, p->num_nt, f.G * p->splits, p->vec);
+}
+
+// Backward weight on the FFMA pipe: 64 x 64 tiles of [K] x [taps*C] per group, the output
+// pixels split across CTAs until the grid covers the SMs twice (at least 64 pixels each).
+static void plan_wg_simt(conv_plan* p) {
+    const Geom& f = p->fg;
+    p->variant = VAR_WG_SIMT;
+    p->wg_kt = (int)cdiv(f.K, 64);
+    p->wg_jt = (int)cdiv((int64_t)f.taps * f.C, 64);
+    const int64_t tiles = (int64_t)p->wg_kt * p->wg_jt * f.G;
+    int splits = (int)std::max<int64_t>(1, std::min<int64_t>(2 * p->sm_count / std::max<int64_t>(tiles, 1),
+                                                             cdiv(f.M, 64)));
+    splits = std::min(splits, 64);
+    p->wg_mps = (int)(cdiv(cdiv(f.M, splits), 8) * 8);
+    p->splits = (int)cdiv(f.M, p->wg_mps);
+    p->prepack_bytes = p->packed_bytes = 0;
+    p->workspace_bytes = p->splits > 1 ? (size_t)p->splits * f.G * f.K * f.taps * f.C * sizeof(float) : 0;
+    snprintf(p->desc, sizeof(p->desc),
+             "variant=simt_%s direction=bwd_weight tile=64x64 pixel_step=8 splits=%d pixels_per_split=%d grid=%dx%dx%d",
+             p->dtype == CONV_BF16 ? "bf16" : "f32", p->splits, p->wg_mps, p->wg_kt, p->wg_jt, f.G * p->splits);
+}
+
+extern "C" {
+
+conv_status conv_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, int64_t C, int64_t K,
+                             const int64_t* spatial, const int64_t* filter, const int64_t* stride,
+                             const int64_t* pad, const int64_t* dilation, conv_dtype dtype,
+                             conv_epilogue epilogue) {
+    if (epilogue < CONV_EPI_NONE || epilogue > CONV_EPI_GELU) return CONV_ERR_INVALID_ARG;
+    conv_plan* p = nullptr;
+    const conv_status st = init_plan(&p, out, ndim, N, G, C, K, spatial, filter, stride, pad, dilation, dtype);
+    if (st != CONV_OK) return st;
+    p->epi = epilogue;
+    p->dir = DIR_FWD;
     // choices: the test hooks if set, else the measured selector's entry for this problem on
     // this device, else the rules
     PlanChoice c;
     if (!choice_from_env(c)) tune_table_lookup(p, c);
     p->ch = c;
     choose_variant(p);
+    *out = p;
+    return CONV_OK;
+}
+
+conv_status conv_bwd_data_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, int64_t C, int64_t K,
+                                      const int64_t* spatial, const int64_t* filter, const int64_t* stride,
+                                      const int64_t* pad, const int64_t* dilation, conv_dtype dtype) {
+    conv_plan* p = nullptr;
+    const conv_status st = init_plan(&p, out, ndim, N, G, C, K, spatial, filter, stride, pad, dilation, dtype);
+    if (st != CONV_OK) return st;
+    p->epi = CONV_EPI_NONE;
+    p->dir = DIR_BWD_DATA;
+    const Geom f = p->fg;
+    if ((int64_t)f.N * f.D * f.H * f.W >= ((int64_t)1 << 31) - 256 || (int64_t)f.taps * K >= ((int64_t)1 << 30)) {
+        delete p;
+        return CONV_ERR_UNSUPPORTED;
+    }
+    // At unit stride dx is the forward convolution of dy with the taps flipped, C and K
+    // swapped and padding dil*(F-1) - pad (the transposed convolution), so every forward
+    // kernel serves it.  Otherwise each input pixel gathers the dy positions that map onto it.
+    const bool transposed = f.sd == 1 && f.sh == 1 && f.sw == 1 && f.dd * (f.Z - 1) >= f.pd &&
+                            f.dh * (f.Y - 1) >= f.ph && f.dw * (f.X - 1) >= f.pw;
+    if (transposed) {
+        Geom& g = p->g;
+        g.C = f.K; g.K = f.C;
+        g.D = f.Do; g.H = f.Ho; g.W = f.Wo;
+        g.pd = f.dd * (f.Z - 1) - f.pd; g.ph = f.dh * (f.Y - 1) - f.ph; g.pw = f.dw * (f.X - 1) - f.pw;
+        g.Do = f.D; g.Ho = f.H; g.Wo = f.W;
+        g.M = f.N * f.D * f.H * f.W;
+        p->Go = g.G; p->Co = g.C; p->Ko = g.K;
+        p->dg_fwd = 1;
+        PlanChoice c;
+        if (!choice_from_env(c)) tune_table_lookup(p, c);
+        p->ch = c;
+        choose_variant(p);
+    } else {
+        plan_dg_simt(p);
+    }
+    *out = p;
+    return CONV_OK;
+}
+
+conv_status conv_bwd_weight_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, int64_t C, int64_t K,
+                                        const int64_t* spatial, const int64_t* filter, const int64_t* stride,
+                                        const int64_t* pad, const int64_t* dilation, conv_dtype dtype) {
+    conv_plan* p = nullptr;
+    const conv_status st = init_plan(&p, out, ndim, N, G, C, K, spatial, filter, stride, pad, dilation, dtype);
+    if (st != CONV_OK) return st;
+    p->epi = CONV_EPI_NONE;
+    p->dir = DIR_BWD_WEIGHT;
+    if ((int64_t)G * K * p->g.taps * C >= ((int64_t)1 << 31)) {
+        delete p;
+        return CONV_ERR_UNSUPPORTED;
+    }
+    plan_wg_simt(p);
     *out = p;
     return CONV_OK;
 }
@@ -829,18 +998,47 @@ static bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) &
 
 conv_status conv_prepack_weights(conv_plan_t plan, const void* w, void* w_packed, void* stream) {
     if (!plan || !w || !w_packed) return CONV_ERR_INVALID_ARG;
+    if (plan->dir == DIR_BWD_WEIGHT) return CONV_ERR_INVALID_ARG;   // nothing to prepack
     if (misaligned(w) || misaligned(w_packed)) return CONV_ERR_ALIGNMENT;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Geom& g = plan->g;
     const int threads = 256;
+    if (plan->variant == VAR_DG_SIMT) {
+        const Geom& f = plan->fg;
+        const long long total = (long long)f.G * plan->Kg * plan->Kpad;
+        const int blocks = (int)std::min<long long>(cdiv(total, threads), 65535);
+        if (plan->dtype == CONV_BF16)
+            prepack_dg_simt_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
+                static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(w_packed), f.K, f.C, f.taps,
+                plan->Kg, plan->Kpad, total);
+        else
+            prepack_dg_simt_kernel<float><<<blocks, threads, 0, s>>>(static_cast<const float*>(w),
+                                                                     static_cast<float*>(w_packed), f.K, f.C, f.taps,
+                                                                     plan->Kg, plan->Kpad, total);
+        return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+    }
+    if (plan->dg_fwd) {   // stage the flipped, transposed weight, then prepack it as a forward weight
+        const Geom& f = plan->fg;
+        void* stage = static_cast<uint8_t*>(w_packed) + plan->dg_src_off;
+        const long long total = (long long)f.G * f.K * f.taps * f.C;
+        const int blocks = (int)std::min<long long>(cdiv(total, threads), 65535);
+        if (plan->dtype == CONV_BF16)
+            flip_transpose_kernel<uint16_t><<<blocks, threads, 0, s>>>(static_cast<const uint16_t*>(w),
+                                                                      static_cast<uint16_t*>(stage), f.K, f.C, f.taps,
+                                                                      total);
+        else
+            flip_transpose_kernel<float><<<blocks, threads, 0, s>>>(static_cast<const float*>(w),
+                                                                   static_cast<float*>(stage), f.K, f.C, f.taps, total);
+        w = stage;
+    }
     if (plan->variant == VAR_TC && plan->tf32) {
-        const long long total16 = (long long)(plan->prepack_bytes / 32);   // hi and lo written per chunk
+        const long long total16 = (long long)(plan->packed_bytes / 32);   // hi and lo written per chunk
         const int blocks = (int)std::min<long long>(cdiv(total16, threads), 65535);
         prepack_tf32x3_kernel<<<blocks, threads, 0, s>>>(static_cast<const float4*>(w), static_cast<uint4*>(w_packed),
                                                          g.K, g.C, g.taps, plan->BN, plan->num_nt, plan->nkb,
                                                          plan->cbt, plan->slab, g.Y, g.X, total16);
     } else if (plan->variant == VAR_TC) {
-        const long long total16 = (long long)(plan->prepack_bytes / 16);
+        const long long total16 = (long long)(plan->packed_bytes / 16);
         const int blocks = (int)std::min<long long>(cdiv(total16, threads), 65535);
         prepack_tc_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint4*>(w), static_cast<uint4*>(w_packed),
                                                      g.K, g.C, g.taps, plan->BN, plan->num_nt, plan->nkb,
@@ -862,29 +1060,33 @@ conv_status conv_prepack_weights(conv_plan_t plan, const void* w, void* w_packed
 }
 
 // The split-K reduction: partial sums in split order, then the epilogue.
-static conv_status launch_reduce(conv_plan_t plan, const float* ws, const void* bias, void* y, cudaStream_t s) {
-    const Geom& g = plan->g;
-    const long long MGK = (long long)g.M * g.G * g.K;
+static conv_status launch_reduce_n(conv_plan_t plan, const float* ws, const void* bias, void* y, long long MGK,
+                                   int GK, int epi, cudaStream_t s) {
     const int threads = 256;
-    const long long work = (g.G * g.K) % 4 == 0 ? MGK / 4 : MGK;
+    const long long work = GK % 4 == 0 ? MGK / 4 : MGK;
     const int blocks = (int)std::min<long long>(cdiv(work, threads), (long long)plan->sm_count * 8);
     const bool pdl = plan->overlap != 0;
     cudaError_t e;
     if (plan->dtype == CONV_BF16)
         e = launch_kernel(splitk_reduce_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, s, pdl, 1, ws,
-                          plan->splits, MGK, g.G * g.K, static_cast<const __nv_bfloat16*>(bias),
-                          static_cast<__nv_bfloat16*>(y), (int)plan->epi, (int)pdl);
+                          plan->splits, MGK, GK, static_cast<const __nv_bfloat16*>(bias),
+                          static_cast<__nv_bfloat16*>(y), epi, (int)pdl);
     else
         e = launch_kernel(splitk_reduce_kernel<float>, dim3(blocks), dim3(threads), 0, s, pdl, 1, ws, plan->splits, MGK,
-                          g.G * g.K, static_cast<const float*>(bias), static_cast<float*>(y), (int)plan->epi,
-                          (int)pdl);
+                          GK, static_cast<const float*>(bias), static_cast<float*>(y), epi, (int)pdl);
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+static conv_status launch_reduce(conv_plan_t plan, const float* ws, const void* bias, void* y, cudaStream_t s) {
+    const Geom& g = plan->g;
+    return launch_reduce_n(plan, ws, bias, y, (long long)g.M * g.G * g.K, g.G * g.K, (int)plan->epi, s);
 }
 
 // Argument checks shared by both forward entry points.
 static conv_status check_forward_args(conv_plan_t plan, const void* x, const void* w_packed, const void* bias,
                                       const void* y) {
     if (!plan || !x || !w_packed || !y) return CONV_ERR_INVALID_ARG;
+    if (plan->dir != DIR_FWD) return CONV_ERR_INVALID_ARG;
     const bool needs_bias = plan->epi == CONV_EPI_BIAS || plan->epi == CONV_EPI_BIAS_GELU;
     if (needs_bias && !bias) return CONV_ERR_INVALID_ARG;
     if (misaligned(x) || misaligned(w_packed) || misaligned(y) || (needs_bias && misaligned(bias)))
@@ -935,6 +1137,7 @@ static conv_status run_forward(conv_plan_t plan, const void* x, const void* w_pa
         sp.g = plan->g;
         sp.x = x; sp.wpack = w_packed; sp.bias = needs_bias ? bias : nullptr; sp.y = y;
         sp.ws = ws;
+        sp.dg = 0; sp.rows = plan->g.M; sp.cols = plan->g.K; sp.rch = plan->g.C;
         sp.Kg = plan->Kg; sp.Kpad = plan->Kpad; sp.num_mt = plan->num_mt; sp.num_nt = plan->num_nt;
         sp.nkt = plan->nkt; sp.splits = plan->splits; sp.ktps = plan->ktps; sp.epi = (int)plan->epi;
         sp.pdl = plan->overlap;
@@ -958,6 +1161,57 @@ conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, cons
 conv_status conv_plan_set_overlap(conv_plan_t plan, int enable) {
     if (!plan) return CONV_ERR_INVALID_ARG;
     plan->overlap = enable ? 1 : 0;
+    return CONV_OK;
+}
+
+// A plan's workspace, or null; CONV_ERR_WORKSPACE when it needs one that is missing.
+static conv_status plan_workspace(conv_plan_t plan, float** ws) {
+    if (plan->workspace_bytes && (!plan->workspace || plan->workspace_size < plan->workspace_bytes))
+        return CONV_ERR_WORKSPACE;
+    *ws = plan->workspace_bytes ? static_cast<float*>(plan->workspace) : nullptr;
+    return CONV_OK;
+}
+
+conv_status conv_bwd_data(conv_plan_t plan, const void* dy, const void* w_packed, void* dx, void* stream) {
+    if (!plan || !dy || !w_packed || !dx || plan->dir != DIR_BWD_DATA) return CONV_ERR_INVALID_ARG;
+    if (misaligned(dy) || misaligned(w_packed) || misaligned(dx)) return CONV_ERR_ALIGNMENT;
+    float* ws = nullptr;
+    const conv_status st = plan_workspace(plan, &ws);
+    if (st != CONV_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (plan->dg_fwd) return run_forward(plan, dy, w_packed, nullptr, dx, ws, s);
+    const Geom& f = plan->fg;
+    SimtParams sp;
+    sp.g = f;
+    sp.x = dy; sp.wpack = w_packed; sp.bias = nullptr; sp.y = dx; sp.ws = ws;
+    sp.dg = 1; sp.rows = f.N * f.D * f.H * f.W; sp.cols = f.C; sp.rch = f.K;
+    sp.Kg = plan->Kg; sp.Kpad = plan->Kpad; sp.num_mt = plan->num_mt; sp.num_nt = plan->num_nt;
+    sp.nkt = plan->nkt; sp.splits = plan->splits; sp.ktps = plan->ktps; sp.epi = EPI_NONE;
+    sp.pdl = plan->overlap;
+    if (launch_simt(sp, plan->dtype == CONV_BF16, plan->BM, plan->vec != 0, s) != cudaSuccess) return CONV_ERR_CUDA;
+    if (plan->splits > 1)
+        return launch_reduce_n(plan, ws, nullptr, dx, (long long)sp.rows * f.G * f.C, f.G * f.C, EPI_NONE, s);
+    return CONV_OK;
+}
+
+conv_status conv_bwd_weight(conv_plan_t plan, const void* x, const void* dy, void* dw, void* stream) {
+    if (!plan || !x || !dy || !dw || plan->dir != DIR_BWD_WEIGHT) return CONV_ERR_INVALID_ARG;
+    if (misaligned(x) || misaligned(dy) || misaligned(dw)) return CONV_ERR_ALIGNMENT;
+    float* ws = nullptr;
+    const conv_status st = plan_workspace(plan, &ws);
+    if (st != CONV_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Geom& f = plan->fg;
+    WgradParams wp;
+    wp.g = f;
+    wp.x = x; wp.dy = dy; wp.dw = dw; wp.ws = ws;
+    wp.num_kt = plan->wg_kt; wp.num_jt = plan->wg_jt; wp.splits = plan->splits; wp.mps = plan->wg_mps;
+    wp.pdl = plan->overlap;
+    if (launch_wgrad_simt(wp, plan->dtype == CONV_BF16, s) != cudaSuccess) return CONV_ERR_CUDA;
+    if (plan->splits > 1) {
+        const long long n = (long long)f.G * f.K * f.taps * f.C;
+        return launch_reduce_n(plan, ws, nullptr, dw, n, f.taps * f.C, EPI_NONE, s);
+    }
     return CONV_OK;
 }
 
@@ -1043,7 +1297,7 @@ double conv_plan_flops(conv_plan_t plan) { return plan ? plan->flops : 0.0; }
 extern "C" {
 
 size_t conv_tune_scratch_bytes(conv_plan_t plan) {
-    if (!plan) return 0;
+    if (!plan || plan->dir == DIR_BWD_WEIGHT || (plan->dir == DIR_BWD_DATA && !plan->dg_fwd)) return 0;
     size_t need = 0;
     for (const conv_plan& t : tune_candidates(plan)) need = std::max(need, align256(t.prepack_bytes) + t.workspace_bytes);
     return need;
@@ -1052,6 +1306,7 @@ size_t conv_tune_scratch_bytes(conv_plan_t plan) {
 conv_status conv_plan_tune(conv_plan_t plan, const void* x, const void* w, const void* bias, void* y, void* scratch,
                            size_t scratch_bytes, int iters, void* stream) {
     if (!plan || !x || !w || !y || !scratch || iters < 1) return CONV_ERR_INVALID_ARG;
+    if (plan->dir == DIR_BWD_WEIGHT || (plan->dir == DIR_BWD_DATA && !plan->dg_fwd)) return CONV_ERR_UNSUPPORTED;
     const bool needs_bias = plan->epi == CONV_EPI_BIAS || plan->epi == CONV_EPI_BIAS_GELU;
     if (needs_bias && !bias) return CONV_ERR_INVALID_ARG;
     if (misaligned(x) || misaligned(w) || misaligned(y) || misaligned(scratch) || (needs_bias && misaligned(bias)))

@@ -146,15 +146,21 @@ cudaError_t launch_slab(const TcParams& p, const CUtensorMap* act_map, int grid,
 size_t slab_smem_bytes(int BN, int tf32, int sa, int sb, size_t a_stage, int btaps);
 
 // ---- SIMT FFMA implicit GEMM (fp32 I/O; also bf16 where channel counts rule out the tensor path) ----
+// Forward: GEMM rows are output pixels (N Do Ho Wo), columns the K output channels of a
+// group, the reduction index tap*C + c.  Backward data (dg = 1): rows are input pixels
+// (N D H W), columns the C input channels, the reduction index tap*K + k over dy, whose
+// source position per tap is (i + pad - tap*dil) / stride where that division is exact.
 struct SimtParams {
-    Geom g;
-    const void* x;          // T  N D H W G C
-    const void* wpack;      // T  [G][taps*C][Kpad]
+    Geom g;                 // the forward problem
+    const void* x;          // T  forward: x (N D H W G C); backward data: dy (N Do Ho Wo G K)
+    const void* wpack;      // T  [G][taps*rch][Kpad]
     const void* bias;       // T  G*K or null
-    void* y;                // T  N Do Ho Wo G K
-    float* ws;              // split-K partials [splits][M][G*K]
-    int Kg;                 // taps*C
-    int Kpad;               // K rounded up to the N tile
+    void* y;                // T  forward: y (N Do Ho Wo G K); backward data: dx (N D H W G C)
+    float* ws;              // split-K partials [splits][rows][G*cols]
+    int dg;                 // 1: backward data
+    int rows, cols, rch;    // GEMM rows, columns per group, reduction channels per tap
+    int Kg;                 // taps*rch
+    int Kpad;               // cols rounded up to the N tile
     int num_mt, num_nt;
     int nkt;                // K steps of 8 along Kg
     int splits, ktps;       // split-K factor, K steps per split
@@ -163,5 +169,21 @@ struct SimtParams {
 };
 
 cudaError_t launch_simt(const SimtParams& p, bool bf16, int BM, bool vec, cudaStream_t stream);
+
+// ---- backward weight ----
+// dw[g][k][tap][c] = sum over output pixels m of dy[m][g][k] * x[source of m at tap][g][c].
+// FFMA kernel: per CTA a 64 (k) x 64 (tap*C + c) tile of one group over a range of output
+// pixels; with splits > 1 each split writes fp32 partials [splits][G][K][taps*C].
+struct WgradParams {
+    Geom g;
+    const void* x;          // T  N D H W G C
+    const void* dy;         // T  N Do Ho Wo G K
+    void* dw;               // T  G K taps C (splits == 1)
+    float* ws;              // partials (splits > 1)
+    int num_kt, num_jt;     // tiles along K and along taps*C
+    int splits, mps;        // pixel splits, pixels per split
+    int pdl;
+};
+cudaError_t launch_wgrad_simt(const WgradParams& p, bool bf16, cudaStream_t stream);
 
 }  // namespace convfwd

@@ -56,6 +56,28 @@ struct PixelBase {
     int n, d0, h0, w0;   // n < 0 marks a row beyond M
 };
 
+// Backward data: the dy offset that tap `tap` draws on for an input pixel (pb holds its
+// coordinates plus the padding), or -1 where no output position maps onto it.
+__device__ __forceinline__ int src_pos(int num, int s, int O) {
+    if (num < 0) return -1;
+    const int o = num / s;
+    return (o * s == num && o < O) ? o : -1;
+}
+
+__device__ __forceinline__ long long dy_offset(const Geom& g, const PixelBase& pb, int tap, int k, int gi) {
+    if (pb.n < 0) return -1;
+    const int yx = g.Y * g.X;
+    const int z = tap / yx;
+    const int r = tap - z * yx;
+    const int y = r / g.X;
+    const int x = r - y * g.X;
+    const int od = src_pos(pb.d0 - z * g.dd, g.sd, g.Do);
+    const int oh = src_pos(pb.h0 - y * g.dh, g.sh, g.Ho);
+    const int ow = src_pos(pb.w0 - x * g.dw, g.sw, g.Wo);
+    if ((od | oh | ow) < 0) return -1;
+    return ((((long long)pb.n * g.Do + od) * g.Ho + oh) * g.Wo + ow) * (long long)(g.G * g.K) + (long long)gi * g.K + k;
+}
+
 __device__ __forceinline__ long long x_offset(const Geom& g, const PixelBase& pb, int tap, int c, int gi) {
     if (pb.n < 0) return -1;
     const int yx = g.Y * g.X;
@@ -68,7 +90,7 @@ __device__ __forceinline__ long long x_offset(const Geom& g, const PixelBase& pb
     return ((((long long)pb.n * g.D + id) * g.H + ih) * g.W + iw) * (long long)(g.G * g.C) + (long long)gi * g.C + c;
 }
 
-template <typename T, int BM, bool VEC>
+template <typename T, int BM, bool VEC, bool DG>
 __global__ void __launch_bounds__(THREADS) conv_fwd_simt_kernel(const __grid_constant__ SimtParams p) {
     if (p.pdl) {   // a programmatic dependent: let the next kernel start, wait for the previous one
         griddep_launch();
@@ -95,15 +117,25 @@ __global__ void __launch_bounds__(THREADS) conv_fwd_simt_kernel(const __grid_con
     PixelBase pb{-1, 0, 0, 0};
     if (a_loader) {
         const int m = mt * BM + a_row;
-        if (m < g.M) {
+        if (m < p.rows) {
             int t = m;
-            const int ow = t % g.Wo; t /= g.Wo;
-            const int oh = t % g.Ho; t /= g.Ho;
-            const int od = t % g.Do;
-            pb.n = t / g.Do;
-            pb.d0 = od * g.sd - g.pd;
-            pb.h0 = oh * g.sh - g.ph;
-            pb.w0 = ow * g.sw - g.pw;
+            if (DG) {   // an input pixel; its coordinates plus the padding
+                const int iw = t % g.W; t /= g.W;
+                const int ih = t % g.H; t /= g.H;
+                const int id = t % g.D;
+                pb.n = t / g.D;
+                pb.d0 = id + g.pd;
+                pb.h0 = ih + g.ph;
+                pb.w0 = iw + g.pw;
+            } else {
+                const int ow = t % g.Wo; t /= g.Wo;
+                const int oh = t % g.Ho; t /= g.Ho;
+                const int od = t % g.Do;
+                pb.n = t / g.Do;
+                pb.d0 = od * g.sd - g.pd;
+                pb.h0 = oh * g.sh - g.ph;
+                pb.w0 = ow * g.sw - g.pw;
+            }
         }
     }
     // this thread's B slot
@@ -119,8 +151,9 @@ __global__ void __launch_bounds__(THREADS) conv_fwd_simt_kernel(const __grid_con
             const int kk = kk0 + a_kq;
             if (VEC) {
                 if (kk < p.Kg) {
-                    const int tap = kk / g.C;
-                    const long long off = x_offset(g, pb, tap, kk - tap * g.C, gi);
+                    const int tap = kk / p.rch;
+                    const long long off = DG ? dy_offset(g, pb, tap, kk - tap * p.rch, gi)
+                                             : x_offset(g, pb, tap, kk - tap * p.rch, gi);
                     if (off >= 0) {
                         const float4 f = Io<T>::ld4(x + off);
                         v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
@@ -131,8 +164,9 @@ __global__ void __launch_bounds__(THREADS) conv_fwd_simt_kernel(const __grid_con
                 for (int e = 0; e < 4; ++e) {
                     const int k2 = kk + e;
                     if (k2 < p.Kg) {
-                        const int tap = k2 / g.C;
-                        const long long off = x_offset(g, pb, tap, k2 - tap * g.C, gi);
+                        const int tap = k2 / p.rch;
+                        const long long off = DG ? dy_offset(g, pb, tap, k2 - tap * p.rch, gi)
+                                                 : x_offset(g, pb, tap, k2 - tap * p.rch, gi);
                         if (off >= 0) v[e] = Io<T>::ld1(x + off);
                     }
                 }
@@ -191,37 +225,38 @@ __global__ void __launch_bounds__(THREADS) conv_fwd_simt_kernel(const __grid_con
     // epilogue
     T* y = reinterpret_cast<T*>(p.y);
     const T* bias = reinterpret_cast<const T*>(p.bias);
-    const int GK = g.G * g.K;
-    const bool add_bias = (p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU) && p.splits == 1;
-    const bool do_gelu = (p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU) && p.splits == 1;
+    const int NC = p.cols;
+    const int GK = g.G * NC;
+    const bool add_bias = !DG && (p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU) && p.splits == 1;
+    const bool do_gelu = !DG && (p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU) && p.splits == 1;
 #pragma unroll
     for (int i = 0; i < TM; ++i) {
         const int m = mt * BM + ty * TM + i;
-        if (m >= g.M) continue;
+        if (m >= p.rows) continue;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int n = nt * BN + h * 64 + tx * 4;
-            if (n >= g.K) continue;
+            if (n >= NC) continue;
             float v[4] = {acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]};
-            const size_t o = (size_t)m * GK + (size_t)gi * g.K + n;
+            const size_t o = (size_t)m * GK + (size_t)gi * NC + n;
             if (p.splits > 1) {
-                float* dst = p.ws + (size_t)split * g.M * GK + o;
+                float* dst = p.ws + (size_t)split * p.rows * GK + o;
                 if (VEC) {
                     *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
                 } else {
-                    for (int e = 0; e < 4 && n + e < g.K; ++e) dst[e] = v[e];
+                    for (int e = 0; e < 4 && n + e < NC; ++e) dst[e] = v[e];
                 }
                 continue;
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                if (add_bias && n + e < g.K) v[e] += Io<T>::ld1(bias + (size_t)gi * g.K + n + e);
+                if (add_bias && n + e < NC) v[e] += Io<T>::ld1(bias + (size_t)gi * NC + n + e);
                 if (do_gelu) v[e] = gelu(v[e]);
             }
             if (VEC) {
                 Io<T>::st4(y + o, v[0], v[1], v[2], v[3]);
             } else {
-                for (int e = 0; e < 4 && n + e < g.K; ++e) Io<T>::st1(y + o + e, v[e]);
+                for (int e = 0; e < 4 && n + e < NC; ++e) Io<T>::st1(y + o + e, v[e]);
             }
         }
     }
@@ -230,7 +265,8 @@ __global__ void __launch_bounds__(THREADS) conv_fwd_simt_kernel(const __grid_con
 template <typename T, int BM, bool VEC>
 cudaError_t launch_t(const SimtParams& p, cudaStream_t stream) {
     dim3 grid(p.num_mt, p.num_nt, p.g.G * p.splits);
-    return launch_kernel(conv_fwd_simt_kernel<T, BM, VEC>, grid, dim3(THREADS), 0, stream, p.pdl != 0, 1, p);
+    if (p.dg) return launch_kernel(conv_fwd_simt_kernel<T, BM, VEC, true>, grid, dim3(THREADS), 0, stream, p.pdl != 0, 1, p);
+    return launch_kernel(conv_fwd_simt_kernel<T, BM, VEC, false>, grid, dim3(THREADS), 0, stream, p.pdl != 0, 1, p);
 }
 
 }  // namespace

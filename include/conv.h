@@ -174,6 +174,63 @@ double conv_plan_flops(conv_plan_t plan);
 conv_status conv_plan_set_overlap(conv_plan_t plan, int enable);
 
 /*
+ * Backward passes (the "bwd_data" and "bwd_weight" variants that page "Learnings --
+ * Grouped-Conv Heuristic (Forward, 2D + 3D)", section 6, names for the same NHWGC x
+ * GKYXC -> NHWGK layouts).  Both take the FORWARD problem's description, exactly as
+ * conv_plan_create does (ndim, N, G, C, K, input extents, filter, stride, pad, dilation,
+ * dtype), and return CONV_ERR_INVALID_ARG / CONV_ERR_UNSUPPORTED on the same inputs.
+ * dy is the gradient of a loss with respect to the forward output y (N Do Ho Wo G K,
+ * the dtype of the plan); they differentiate the convolution's linear part only (bias
+ * and GELU are elementwise and outside it):
+ *
+ *   dx[n,i,g,c] = sum over k and taps t of dy[n,o,g,k] * w[g,k,t,c], over the o with
+ *                 o*stride - pad + t*dil = i in every spatial dimension
+ *   dw[g,k,t,c] = sum over n and output positions o of dy[n,o,g,k] * x[n, o*stride - pad + t*dil, g, c]
+ *
+ * accumulated in fp32 and rounded once to the plan's dtype.  conv_plan_output_shape
+ * returns the forward output extents (dy's), conv_plan_flops the forward problem's
+ * useful FLOPs (each backward pass performs as many), conv_plan_describe the variant.
+ * Workspaces (conv_workspace_bytes / conv_plan_set_workspace), conv_plan_check,
+ * conv_plan_set_overlap and conv_plan_destroy work as for forward plans; conv_fwd and
+ * conv_fwd_static_scratch refuse backward plans with CONV_ERR_INVALID_ARG.
+ */
+
+/*
+ * Backward-data plan.  Its packed weight comes from conv_prepack_weights(plan, w, ...)
+ * with w in the forward layout G K Z Y X C (conv_prepacked_weight_bytes gives the size).
+ * At unit stride (and pad <= dil*(F-1) per dimension) dx is the forward convolution of
+ * dy with every tap axis flipped, C and K swapped and padding dil*(F-1) - pad, and the
+ * plan runs the forward kernels on that problem; otherwise an FFMA kernel gathers, for
+ * each input pixel, the dy positions that map onto it.
+ */
+conv_status conv_bwd_data_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, int64_t C, int64_t K,
+                                      const int64_t* spatial, const int64_t* filter, const int64_t* stride,
+                                      const int64_t* pad, const int64_t* dilation, conv_dtype dtype);
+
+/*
+ * dx (N D H W G C, device) from dy (N Do Ho Wo G K, device) and the packed weight.  All
+ * three 16-byte aligned.  Asynchronous on `stream`; errors as conv_fwd
+ * (CONV_ERR_INVALID_ARG for NULL pointers or a plan of another direction).
+ */
+conv_status conv_bwd_data(conv_plan_t plan, const void* dy, const void* w_packed, void* dx, void* stream);
+
+/*
+ * Backward-weight plan.  No packed weight (conv_prepack_weights returns
+ * CONV_ERR_INVALID_ARG); the output pixels are split across CTAs, whose fp32 partial
+ * sums need a workspace of conv_workspace_bytes(plan) when that is non-zero.
+ */
+conv_status conv_bwd_weight_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, int64_t C, int64_t K,
+                                        const int64_t* spatial, const int64_t* filter, const int64_t* stride,
+                                        const int64_t* pad, const int64_t* dilation, conv_dtype dtype);
+
+/*
+ * dw (G K Z Y X C, device) from x (N D H W G C) and dy (N Do Ho Wo G K), all device and
+ * 16-byte aligned; dw is overwritten (not accumulated into).  Asynchronous on `stream`;
+ * errors as conv_fwd.
+ */
+conv_status conv_bwd_weight(conv_plan_t plan, const void* x, const void* dy, void* dw, void* stream);
+
+/*
  * Measured kernel selection.  conv_plan_create picks a variant and tiling by fixed rules
  * from the problem's geometry.  The selector instead times the candidate plans of one
  * problem on this device and keeps the fastest, in a process-wide table that later

@@ -193,7 +193,7 @@ def _table_key(layer, code):
     pad3 = lambda v, fill: [fill] * (3 - ndim) + [int(a) for a in v]
     j = lambda v, fill: "x".join(str(a) for a in pad3(v, fill))
     return (f"nd={ndim} N={N} G={G} C={C} K={K} in={j(sp, 1)} f={j(fl, 1)} s={j(st, 1)} p={j(pa, 0)} "
-            f"d={j(di, 1)} dtype={dtype} epi={epi} sm={_sm_count()}")
+            f"d={j(di, 1)} dtype={dtype} epi={epi} dir=0 sm={_sm_count()}")
 
 
 def test_selector_table_load_save_and_precedence(lib, tmp_path):
@@ -253,3 +253,81 @@ def test_selector_scratch_covers_every_candidate(lib):
             B.conv_plan_destroy(h)
     assert lib.conv_tune_scratch_bytes(None) == 0
     assert lib.conv_plan_tune(None, None, None, None, None, None, 0, 1, None) == B.CONV_ERR_INVALID_ARG
+
+
+def _bwd_plan(kind, ndim=2, N=1, G=2, C=16, K=24, spatial=(9, 11), filt=(3, 3), stride=(1, 1), pad=(1, 1),
+              dil=(1, 1), dtype=B.CONV_BF16):
+    create = B.conv_bwd_data_plan_create if kind == "data" else B.conv_bwd_weight_plan_create
+    return create(ndim, N, G, C, K, spatial, filt, stride, pad, dil, dtype)
+
+
+def test_backward_plans_describe_shape_flops_and_variant(lib):
+    fwd = plan(ndim=2, G=2, C=16, K=24, spatial=(9, 11), filt=(3, 3), stride=(1, 1), pad=(1, 1), dil=(1, 1))
+    try:
+        fshape = B.conv_plan_output_shape(fwd, 2)
+        fflops = B.conv_plan_flops(fwd)
+    finally:
+        B.conv_plan_destroy(fwd)
+    for kind in ("data", "weight"):
+        h = _bwd_plan(kind)
+        try:
+            assert B.conv_plan_output_shape(h, 2) == fshape          # dy's extents
+            assert B.conv_plan_flops(h) == fflops
+            d = B.conv_plan_describe(h)
+            if kind == "data":
+                # unit stride: the forward kernels on the transposed problem (C and K swapped)
+                assert "direction=bwd_data(transposed forward)" in d and d.startswith("variant=tc_bf16"), d
+                assert B.conv_prepacked_weight_bytes(h) > 0
+            else:
+                assert "direction=bwd_weight" in d, d
+                assert B.conv_prepacked_weight_bytes(h) == 0
+                with pytest.raises(B.ConvError) as e:
+                    B.conv_prepack_weights(h, 4096, 4096, 0)
+                assert e.value.status == B.CONV_ERR_INVALID_ARG
+        finally:
+            B.conv_plan_destroy(h)
+    # stride 2, and padding beyond the filter's reach: the gather kernel
+    for kw in (dict(stride=(2, 2)), dict(pad=(3, 1))):
+        h = _bwd_plan("data", **kw)
+        try:
+            assert "direction=bwd_data(gather)" in B.conv_plan_describe(h)
+        finally:
+            B.conv_plan_destroy(h)
+
+
+def test_backward_entry_points_check_direction_and_arguments(lib):
+    fwd = plan()
+    dg = _bwd_plan("data")
+    wg = _bwd_plan("weight")
+    try:
+        for h in (dg, wg):       # a backward plan is refused by the forward entry points
+            assert lib.conv_fwd(h, 4096, 4096, 4096, 4096, None) == B.CONV_ERR_INVALID_ARG
+            assert lib.conv_fwd_static_scratch(h, 4096, 4096, 4096, 4096, None) == B.CONV_ERR_INVALID_ARG
+        assert lib.conv_bwd_data(fwd, 4096, 4096, 4096, None) == B.CONV_ERR_INVALID_ARG
+        assert lib.conv_bwd_data(wg, 4096, 4096, 4096, None) == B.CONV_ERR_INVALID_ARG
+        assert lib.conv_bwd_weight(dg, 4096, 4096, 4096, None) == B.CONV_ERR_INVALID_ARG
+        assert lib.conv_bwd_data(dg, None, 4096, 4096, None) == B.CONV_ERR_INVALID_ARG
+        assert lib.conv_bwd_weight(wg, 4096, None, 4096, None) == B.CONV_ERR_INVALID_ARG
+        assert lib.conv_bwd_data(dg, 4100, 4096, 4096, None) == B.CONV_ERR_ALIGNMENT
+        assert lib.conv_bwd_weight(wg, 4096, 4096, 4104, None) == B.CONV_ERR_ALIGNMENT
+        assert lib.conv_tune_scratch_bytes(wg) == 0
+        for kw in (dict(ndim=0), dict(N=0), dict(stride=(0, 1)), dict(spatial=(1, 1), pad=(0, 0))):
+            for kind in ("data", "weight"):
+                with pytest.raises(B.ConvError) as e:
+                    _bwd_plan(kind, **kw)
+                assert e.value.status == B.CONV_ERR_INVALID_ARG
+    finally:
+        for h in (fwd, dg, wg):
+            B.conv_plan_destroy(h)
+
+
+def test_backward_weight_splits_pixels_and_needs_a_workspace(lib):
+    """A large reduction over output pixels is split across CTAs; the partials need a workspace."""
+    layer = WORKLOADS["grouped2d_g8_c64_d1"].layers[0]
+    h = B.conv_bwd_weight_plan_create(*layer.plan_args(B.CONV_BF16)[:11])
+    try:
+        d = dict(kv.split("=", 1) for kv in B.conv_plan_describe(h).split())
+        assert int(d["splits"]) > 1 and B.conv_workspace_bytes(h) > 0
+        assert lib.conv_bwd_weight(h, 4096, 4096, 4096, None) == B.CONV_ERR_WORKSPACE
+    finally:
+        B.conv_plan_destroy(h)

@@ -1,0 +1,163 @@
+"""GPU parity of the backward passes (backward data, backward weight) through the C-ABI
+against the CPU oracle, element by element, on seeded inputs; integer inputs bit-exact."""
+import dataclasses
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+from convolution_forward_implicit_gb300 import synthetic as syn
+from convolution_forward_implicit_gb300.binding import CONV_BF16, CONV_EPI_NONE, CONV_F32, ConvPlan
+from convolution_forward_implicit_gb300.workloads import WORKLOADS
+from tests.helpers import SENTINEL, assert_within, from_device, geom_of, sample_indices, to_device
+from tests.test_parity_gpu import L
+
+pytestmark = pytest.mark.gpu
+
+
+def make_bwd_inputs(layer, dtype, seed, kind="normal"):
+    g = geom_of(layer)
+    if kind == "int":
+        x = syn.gen_int(seed, layer.x_shape(), -3, 3, dtype)
+        w = syn.gen_int(seed + 1, layer.w_shape(), -3, 3, dtype)
+        dy = syn.gen_int(seed + 2, g.y_shape(), -3, 3, dtype)
+    else:
+        x = syn.gen_normal(seed, layer.x_shape(), dtype)
+        w = syn.gen_uniform_pm(seed + 1, layer.w_shape(), layer.w_bound, dtype)
+        dy = syn.gen_normal(seed + 2, g.y_shape(), dtype)
+    return x, w, dy
+
+
+def _guarded(n, tdt, guard=64):
+    import torch
+    buf = torch.full((n + 2 * guard,), SENTINEL, dtype=tdt, device="cuda")
+    return buf, buf[guard:guard + n]
+
+
+def _check_guard(buf, n, guard=64):
+    import torch
+    sent = torch.cat([buf[:guard], buf[guard + n:]]).float()
+    assert bool((sent == SENTINEL).all()), "kernel wrote outside its output"
+
+
+def run_bwd_data(layer, dtype, dy, w, env=None):
+    import torch
+    code = CONV_BF16 if dtype == "bf16" else CONV_F32
+    plan = ConvPlan(*layer.plan_args(code), direction="bwd_data")
+    plan.allocate()
+    plan.prepack(to_device(w, dtype))
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    n = int(np.prod(layer.x_shape()))
+    buf, dx = _guarded(n, tdt)
+    plan.backward_data(to_device(dy, dtype), dx)
+    plan.check()
+    torch.cuda.synchronize()
+    _check_guard(buf, n)
+    desc = plan.describe()
+    plan.close()
+    return from_device(dx, dtype), desc
+
+
+def run_bwd_weight(layer, dtype, x, dy):
+    import torch
+    code = CONV_BF16 if dtype == "bf16" else CONV_F32
+    plan = ConvPlan(*layer.plan_args(code), direction="bwd_weight")
+    plan.allocate()
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    n = int(np.prod(layer.w_shape()))
+    buf, dw = _guarded(n, tdt)
+    plan.backward_weight(to_device(x, dtype), to_device(dy, dtype), dw)
+    plan.check()
+    torch.cuda.synchronize()
+    _check_guard(buf, n)
+    desc = plan.describe()
+    plan.close()
+    return from_device(dw, dtype), desc
+
+
+def B_(ndim, N, G, C, K, spatial, filt, stride, pad, dil):
+    return L(ndim, N, G, C, K, spatial, filt, stride, pad, dil, CONV_EPI_NONE)
+
+
+CASES = [
+    # unit stride: backward data runs the forward kernels on the transposed problem
+    ("1d_s1", "bf16", B_(1, 2, 1, 64, 72, (301,), (3,), (1,), (1,), (1,))),
+    ("1d_s1_whisper_l1_shape", "bf16", B_(1, 1, 1, 80, 384, (517,), (3,), (1,), (1,), (1,))),
+    ("2d_s1_groups", "bf16", B_(2, 2, 4, 32, 40, (19, 23), (3, 3), (1, 1), (1, 1), (1, 1))),
+    ("2d_s1_dil2_g8", "bf16", B_(2, 1, 8, 64, 64, (20, 18), (3, 3), (1, 1), (2, 2), (2, 2))),
+    ("3d_s1_g4", "bf16", B_(3, 1, 4, 64, 64, (5, 9, 10), (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1))),
+    ("2d_s1_g32_c8", "bf16", B_(2, 2, 32, 8, 8, (17, 15), (3, 3), (1, 1), (1, 1), (1, 1))),
+    ("2d_s1_no_pad", "bf16", B_(2, 1, 1, 16, 24, (9, 12), (3, 2), (1, 1), (0, 0), (1, 1))),
+    ("1d_s1_f32", "f32", B_(1, 1, 1, 80, 96, (300,), (3,), (1,), (1,), (1,))),
+    ("2d_s1_f32_groups", "f32", B_(2, 2, 3, 40, 24, (11, 13), (3, 3), (1, 1), (1, 1), (1, 1))),
+    ("3d_s1_f32_odd", "f32", B_(3, 1, 2, 5, 7, (4, 6, 5), (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1))),
+    # stride > 1 or padding beyond the filter's reach: the gather kernel
+    ("1d_s2", "bf16", B_(1, 1, 1, 64, 96, (301,), (3,), (2,), (1,), (1,))),
+    ("1d_s2_whisper_l2_shape", "f32", B_(1, 1, 1, 96, 64, (400,), (3,), (2,), (1,), (1,))),
+    ("2d_s2_dil", "bf16", B_(2, 2, 2, 24, 16, (17, 15), (5, 3), (2, 3), (3, 2), (1, 2))),
+    ("3d_s2", "f32", B_(3, 1, 2, 8, 12, (7, 9, 8), (3, 3, 3), (2, 1, 2), (1, 1, 1), (1, 1, 1))),
+    ("2d_big_pad", "bf16", B_(2, 1, 1, 16, 16, (6, 6), (3, 3), (1, 1), (3, 3), (1, 1))),
+    ("1d_1x1_s2", "f32", B_(1, 2, 2, 12, 20, (33,), (1,), (2,), (0,), (1,))),
+]
+
+
+@pytest.mark.parametrize("name,dtype,layer", CASES, ids=[c[0] for c in CASES])
+def test_backward_data_matches_oracle(name, dtype, layer):
+    x, w, dy = make_bwd_inputs(layer, dtype, 7000 + zlib.crc32(name.encode()) % 1000)
+    got, desc = run_bwd_data(layer, dtype, dy, w)
+    ref, S = oracle.conv_bwd_data(geom_of(layer), syn.as_f32(dy, dtype), syn.as_f32(w, dtype))
+    assert_within(dtype, CONV_EPI_NONE, got, ref.reshape(-1), S.reshape(-1), f"{name} [{desc}]")
+
+
+@pytest.mark.parametrize("name,dtype,layer", CASES, ids=[c[0] for c in CASES])
+def test_backward_weight_matches_oracle(name, dtype, layer):
+    x, w, dy = make_bwd_inputs(layer, dtype, 8000 + zlib.crc32(name.encode()) % 1000)
+    got, desc = run_bwd_weight(layer, dtype, x, dy)
+    ref, S = oracle.conv_bwd_weight(geom_of(layer), syn.as_f32(x, dtype), syn.as_f32(dy, dtype))
+    assert_within(dtype, CONV_EPI_NONE, got, ref.reshape(-1), S.reshape(-1), f"{name} [{desc}]")
+
+
+@pytest.mark.parametrize("name", ["2d_s1_groups", "2d_s2_dil", "3d_s1_g4", "1d_s1_f32", "3d_s2"])
+def test_backward_integer_inputs_bit_exact(name):
+    """Small integers: every product and partial sum is exact in fp32, so fp32 results equal
+    the oracle exactly and bf16 results equal its round-to-nearest-even."""
+    dtype, layer = {c[0]: (c[1], c[2]) for c in CASES}[name]
+    x, w, dy = make_bwd_inputs(layer, dtype, 9000, kind="int")
+    g = geom_of(layer)
+    for kind in ("data", "weight"):
+        if kind == "data":
+            got, desc = run_bwd_data(layer, dtype, dy, w)
+            ref, _ = oracle.conv_bwd_data(g, syn.as_f32(dy, dtype), syn.as_f32(w, dtype))
+        else:
+            got, desc = run_bwd_weight(layer, dtype, x, dy)
+            ref, _ = oracle.conv_bwd_weight(g, syn.as_f32(x, dtype), syn.as_f32(dy, dtype))
+        if dtype == "f32":
+            assert np.array_equal(got.reshape(-1).astype(np.float64), ref.reshape(-1)), f"{name} {kind} [{desc}]"
+        else:
+            want = syn.f32_to_bf16_bits(ref.reshape(-1).astype(np.float32))
+            assert np.array_equal(got.reshape(-1), want), f"{name} {kind} [{desc}]"
+
+
+FULL = ["grouped2d_g8_c64_d1", "grouped2d_g32_c8_d2", "grouped3d_g4_c64_d2", "whisper_frontend_bf16",
+        "whisper_frontend_f32"]
+
+
+@pytest.mark.parametrize("wl_name", FULL)
+def test_backward_full_size_sampled(wl_name):
+    """The workloads at full size: sampled elements of dx and dw against the oracle."""
+    wl = WORKLOADS[wl_name]
+    for li, layer in enumerate(wl.layers):
+        layer = dataclasses.replace(layer, epilogue=CONV_EPI_NONE, bias_bound=None)
+        x, w, dy = make_bwd_inputs(layer, wl.dtype, 9500 + 10 * wl.index + li)
+        g = geom_of(layer)
+        dx, ddesc = run_bwd_data(layer, wl.dtype, dy, w)
+        idx = sample_indices(dx.size, 3000, 11 + li)
+        coords = np.array(np.unravel_index(idx, g.x_shape())).T
+        ref, S = oracle.conv_bwd_points(g, syn.as_f32(dy, wl.dtype), syn.as_f32(w, wl.dtype), False, coords)
+        assert_within(wl.dtype, CONV_EPI_NONE, dx.reshape(-1)[idx], ref, S, f"{wl_name} L{li + 1} dx [{ddesc}]")
+        dw, wdesc = run_bwd_weight(layer, wl.dtype, x, dy)
+        idx = sample_indices(dw.size, 600, 13 + li)
+        coords = np.array(np.unravel_index(idx, g.w_shape())).T
+        ref, S = oracle.conv_bwd_points(g, syn.as_f32(x, wl.dtype), syn.as_f32(dy, wl.dtype), True, coords)
+        assert_within(wl.dtype, CONV_EPI_NONE, dw.reshape(-1)[idx], ref, S, f"{wl_name} L{li + 1} dw [{wdesc}]")
