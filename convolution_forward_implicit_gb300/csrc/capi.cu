@@ -236,7 +236,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, l
 }  // namespace
 
 // ----------------------------------------------------------------------------- plan
-enum Variant { VAR_TC = 0, VAR_SIMT = 1, VAR_DG_SIMT = 2, VAR_WG_SIMT = 3 };
+enum Variant { VAR_TC = 0, VAR_SIMT = 1, VAR_DG_SIMT = 2, VAR_WG_SIMT = 3, VAR_WG_TC = 4 };
 enum Direction { DIR_FWD = 0, DIR_BWD_DATA = 1, DIR_BWD_WEIGHT = 2 };
 
 // Plan choices that can be fixed instead of decided by rule: by the measured selector
@@ -292,6 +292,7 @@ struct conv_plan {
     int dg_fwd;             // backward data run as the forward conv of dy with flipped, transposed weights
     size_t dg_src_off;      // where in w_packed the prepack stages those weights
     int wg_kt, wg_jt, wg_mps;   // backward weight (FFMA): tiles along K and taps*C, pixels per split
+    int wg_rt, wg_nt, wg_q, wg_qps, wg_nwb, wg_cbh;   // backward weight (tensor cores), see WgradTcParams
     char desc[320];
 };
 
@@ -878,6 +879,83 @@ static void plan_dg_simt(conv_plan* p) {
              p->dtype == CONV_BF16 ? "bf16" : "f32", p->BM, p->splits, p->num_mt, p->num_nt, f.G * p->splits, p->vec);
 }
 
+// The two tensor maps of the tensor-core backward weight: x as {G*C, W, H, D, N} with boxes of
+// 64 channels x 64 pixels at the conv stride along W, dy as {G*K, Wo, Ho, Do, N} with boxes of
+// 64 channels x 64 output pixels; bf16, 128-byte swizzle, out-of-range elements read as zero.
+static bool encode_wg_maps(const conv_plan* p, const void* x, const void* dy, CUtensorMap* xm, CUtensorMap* dym) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const Geom& g = p->fg;
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5], es[5];
+    dims[0] = (cuuint64_t)g.G * g.C; dims[1] = g.W; dims[2] = g.H; dims[3] = g.D; dims[4] = g.N;
+    strides[0] = dims[0] * 2; strides[1] = strides[0] * g.W; strides[2] = strides[1] * g.H; strides[3] = strides[2] * g.D;
+    box[0] = 64; box[1] = (cuuint32_t)(64 * g.sw); box[2] = box[3] = box[4] = 1;
+    es[0] = 1; es[1] = (cuuint32_t)g.sw; es[2] = es[3] = es[4] = 1;
+    if (fn(xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(x), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    dims[0] = (cuuint64_t)g.G * g.K; dims[1] = g.Wo; dims[2] = g.Ho; dims[3] = g.Do; dims[4] = g.N;
+    strides[0] = dims[0] * 2; strides[1] = strides[0] * g.Wo; strides[2] = strides[1] * g.Ho;
+    strides[3] = strides[2] * g.Do;
+    box[1] = 64;
+    es[1] = 1;
+    return fn(dym, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(dy), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Backward weight on the tensor cores (bf16, C and K multiples of 8 so that every box starts on a
+// 16-byte boundary, stride along W at most 4 so a box spans <= 256 elements): 128-row tiles of (tap, 64-channel
+// block) pairs x BN output channels; 64-pixel chunks along output rows split across CTAs until
+// the grid fills the SMs once.  Returns false where the problem does not fit.
+static bool plan_wg_tc(conv_plan* p) {
+    const Geom& f = p->fg;
+    if (p->dtype != CONV_BF16 || p->ch.simt) return false;
+    // every box starts at channel g*C + 64*b (x) or g*K + 64*j (dy): a multiple of 8 elements,
+    // the 16-byte alignment a tiled TMA copy needs of its innermost coordinate
+    if (f.C % 8 != 0 || f.K % 8 != 0 || f.sw > 4) return false;
+    p->wg_cbh = (int)cdiv(f.C, 64);
+    const int halves = f.taps * p->wg_cbh;
+    p->wg_rt = (int)cdiv(halves, 2);
+    int bn = 256;
+    for (int c : {256, 128, 64})   // the fewest padded columns, the wider tile on a tie
+        if (cdiv(f.K, c) * c < cdiv(f.K, bn) * bn) bn = c;
+    if (p->ch.bn == 64 || p->ch.bn == 128 || p->ch.bn == 256) bn = p->ch.bn;
+    p->BN = bn;
+    p->wg_nt = (int)cdiv(f.K, bn);
+    p->wg_nwb = (int)cdiv(f.Wo, 64);
+    const int64_t Q = (int64_t)f.N * f.Do * f.Ho * p->wg_nwb;
+    if (Q >= ((int64_t)1 << 31)) return false;
+    p->wg_q = (int)Q;
+    const int64_t base = (int64_t)f.G * p->wg_rt * p->wg_nt;
+    if (base >= ((int64_t)1 << 31)) return false;
+    int splits = (int)std::max<int64_t>(1, std::min<int64_t>(p->sm_count / base, Q / 2));
+    if (p->ch.splits >= 1) splits = (int)std::min<int64_t>(p->ch.splits, Q);
+    p->wg_qps = (int)cdiv(Q, splits);
+    p->splits = (int)cdiv(Q, p->wg_qps);
+    p->total_units = (int)(base * p->splits);
+    if ((int64_t)base * p->splits >= ((int64_t)1 << 31)) return false;
+    int dev = 0;   // a trial encode checks the boxes against the driver's limits
+    if (encode_fn() && cudaGetDevice(&dev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess) {
+        CUtensorMap a, b;
+        const void* fake = reinterpret_cast<const void*>((uintptr_t)4096);
+        const bool ok = encode_wg_maps(p, fake, fake, &a, &b);
+        cudaGetLastError();
+        if (!ok) return false;
+    }
+    cudaGetLastError();
+    p->variant = VAR_WG_TC;
+    p->prepack_bytes = p->packed_bytes = 0;
+    p->workspace_bytes = p->splits > 1 ? (size_t)p->splits * f.G * f.K * f.taps * f.C * sizeof(float) : 0;
+    snprintf(p->desc, sizeof(p->desc),
+             "variant=tc_bf16 direction=bwd_weight operands=mn-major tile=128x%d row_tiles=%d chunk=64px splits=%d "
+             "chunks_per_split=%d units=%d",
+             bn, p->wg_rt, p->splits, p->wg_qps, p->total_units);
+    return true;
+}
+
 // Backward weight on the FFMA pipe: 64 x 64 tiles of [K] x [taps*C] per group, the output
 // pixels split across CTAs until the grid covers the SMs twice (at least 64 pixels each).
 static void plan_wg_simt(conv_plan* p) {
@@ -970,7 +1048,10 @@ conv_status conv_bwd_weight_plan_create(conv_plan_t* out, int ndim, int64_t N, i
         delete p;
         return CONV_ERR_UNSUPPORTED;
     }
-    plan_wg_simt(p);
+    PlanChoice c;
+    choice_from_env(c);
+    p->ch = c;
+    if (!plan_wg_tc(p)) plan_wg_simt(p);
     *out = p;
     return CONV_OK;
 }
@@ -1202,6 +1283,24 @@ conv_status conv_bwd_weight(conv_plan_t plan, const void* x, const void* dy, voi
     if (st != CONV_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Geom& f = plan->fg;
+    if (plan->variant == VAR_WG_TC) {
+        unsigned* err = error_word_ptr();
+        if (!err) return CONV_ERR_CUDA;
+        CUtensorMap xm, dym;
+        if (!encode_wg_maps(plan, x, dy, &xm, &dym)) return CONV_ERR_CUDA;
+        WgradTcParams tp;
+        tp.g = f;
+        tp.dw = dw; tp.ws = ws; tp.err = err;
+        tp.BN = plan->BN; tp.RT = plan->wg_rt; tp.NT = plan->wg_nt;
+        tp.splits = plan->splits; tp.Q = plan->wg_q; tp.qps = plan->wg_qps; tp.nwb = plan->wg_nwb;
+        tp.cbh = plan->wg_cbh; tp.halves = f.taps * plan->wg_cbh; tp.total_units = plan->total_units;
+        tp.pdl = plan->overlap;
+        if (launch_wgrad_tc(tp, &xm, &dym, s) != cudaSuccess) return CONV_ERR_CUDA;
+        if (plan->splits > 1)
+            return launch_reduce_n(plan, ws, nullptr, dw, (long long)f.G * f.K * f.taps * f.C, f.taps * f.C, EPI_NONE,
+                                   s);
+        return CONV_OK;
+    }
     WgradParams wp;
     wp.g = f;
     wp.x = x; wp.dy = dy; wp.dw = dw; wp.ws = ws;

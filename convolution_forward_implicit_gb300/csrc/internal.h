@@ -186,4 +186,23 @@ struct WgradParams {
 };
 cudaError_t launch_wgrad_simt(const WgradParams& p, bool bf16, cudaStream_t stream);
 
+// Tensor-core backward weight (bf16): per group, D[(tap, c)][k] accumulates x * dy over output
+// pixels, both operands read by TMA in their own channels-last layouts and fed to tcgen05.mma
+// as MN-major tiles.  Rows: pairs of 64-channel "halves" h = tap * cbh + cb (2 per 128-row
+// tile); columns: BN output channels; reduction: chunks of 64 pixels along one output row.
+struct WgradTcParams {
+    Geom g;
+    void* dw;               // bf16 G K taps C (splits == 1)
+    float* ws;              // fp32 partials [splits][G][K][taps*C] (splits > 1)
+    unsigned* err;
+    int BN, RT, NT;         // N tile, row tiles, column tiles
+    int splits, Q, qps;     // pixel splits, 64-pixel chunks in all, chunks per split
+    int nwb;                // 64-pixel blocks per output row
+    int cbh, halves;        // 64-channel blocks per tap, taps * cbh
+    int total_units;
+    int pdl;
+};
+cudaError_t launch_wgrad_tc(const WgradTcParams& p, const CUtensorMap* xmap, const CUtensorMap* dymap,
+                            cudaStream_t stream);
+
 }  // namespace convfwd

@@ -1,0 +1,268 @@
+// Backward weight of the grouped convolution on the tensor cores (bf16 in, fp32 accumulate):
+// the "bwd_weight" variant that page "composable_kernel dispatcher/heuristics/
+// LEARNINGS_GROUPED_CONV.md", section 6, names for the NHWGC / GKYXC / NHWGK layouts.
+//
+//   dw[g][k][tap][c] = sum over output pixels m of x[source(m, tap)][g][c] * dy[m][g][k]
+//
+// Per group this is a GEMM whose reduction runs over output pixels.  Both operands are read
+// in the layouts they already have: a TMA box of 64 channels x 64 pixels (128-byte rows, one
+// pixel per row, 128-byte swizzle) is, for the MMA, an MN-major tile whose MN index is the
+// channel and whose K index is the pixel, so no transpose is ever materialised:
+//   A (rows of D): x at the pixels one tap reads, two 64-channel halves (tap, channel block)
+//                  per 128-row tile, 8 KB apart (the descriptor's MN-block stride);
+//   B (columns):   dy at the output pixels, BN/64 blocks of 64 output channels, 8 KB apart.
+// 8-pixel groups are 1 KB apart (the descriptor's K-group stride); each MMA consumes 16
+// pixels (2 KB of each tile).  Padding, the stride and the ragged end of a row come from the
+// TMA box: out-of-range pixels read as zero, and the conv stride is the box's element stride
+// along W.  Channels beyond C or K only feed accumulator rows / columns that are never stored.
+//
+// Roles (192 threads): warp 0 lane 0 issues the TMA loads into a ring of stages (each stage
+// holds CH chunks of 64 pixels); warp 1 issues the MMAs (elect.sync) and commits once per
+// stage; warps 2-5 (one per TMEM lane quarter) read the accumulator and store dw, or fp32
+// partial sums when the pixels are split across CTAs.  Every wait is bounded: on timeout the
+// kernel raises the error word and returns after releasing its tensor memory.
+#include <cuda.h>
+
+#include "tc_common.cuh"
+
+namespace convfwd {
+namespace {
+
+constexpr int WG_THREADS = 192;
+constexpr uint32_t HALF_BYTES = 64 * 128;   // one box: 64 pixels x 64 channels of bf16
+
+template <int BN, int CH>
+struct WgCfg {
+    static constexpr uint32_t A_CHUNK = 2 * HALF_BYTES;             // two channel halves
+    static constexpr uint32_t B_CHUNK = (BN / 64) * HALF_BYTES;     // BN/64 channel blocks of dy
+    static constexpr uint32_t CHUNK = A_CHUNK + B_CHUNK;
+    static constexpr uint32_t STAGE = CH * CHUNK;
+    static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+};
+
+// Shared-memory matrix descriptor of an MN-major operand, 128-byte swizzle: 64-element MN
+// blocks mn_stride bytes apart (leading byte offset), 8-row K groups 1 KB apart (stride byte
+// offset).
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t mn_stride) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+struct ChunkPos {
+    int n, od, oh, ow0;
+};
+
+__device__ __forceinline__ ChunkPos chunk_pos(const WgradTcParams& p, int q) {
+    const Geom& g = p.g;
+    ChunkPos c;
+    const int wb = q % p.nwb;
+    int r = q / p.nwb;
+    c.oh = r % g.Ho;
+    r /= g.Ho;
+    c.od = r % g.Do;
+    c.n = r / g.Do;
+    c.ow0 = wb * 64;
+    return c;
+}
+
+template <int BN, int CH, int STAGES>
+__global__ void __launch_bounds__(WG_THREADS, 1)
+    conv_wgrad_tc_kernel(const __grid_constant__ WgradTcParams p, const __grid_constant__ CUtensorMap xmap,
+                         const __grid_constant__ CUtensorMap dymap) {
+    using W = WgCfg<BN, CH>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (sbase - raw);
+    const uint32_t bar0 = sbase + STAGES * W::STAGE;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t done_bar = bar0 + 8u * (2 * STAGES);
+    uint8_t* misc = smem + (bar0 + 8u * (2 * STAGES + 1) - sbase);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const Geom& g = p.g;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), W::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (p.pdl) {   // the next kernel may start its set-up; x and dy may come from the previous one
+        griddep_launch();
+        griddep_wait();
+    }
+
+    // this CTA's unit: row tile fastest, so neighbouring CTAs share their dy chunks in L2
+    const int u = blockIdx.x;
+    const int rt = u % p.RT;
+    int r = u / p.RT;
+    const int split = r % p.splits;
+    r /= p.splits;
+    const int nt = r % p.NT;
+    const int gi = r / p.NT;
+    const int q0 = split * p.qps;
+    const int q1 = min(q0 + p.qps, p.Q);
+    const int nchunks = q1 - q0;
+    const int nstages = (nchunks + CH - 1) / CH;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // the two channel halves of this row tile: tap and channel block, tap offsets
+            int cin[2], dz[2], dyo[2], dxo[2];
+            bool hv[2];
+            for (int hh = 0; hh < 2; ++hh) {
+                const int h = 2 * rt + hh;
+                hv[hh] = h < p.halves;
+                const int tap = hv[hh] ? h / p.cbh : 0;
+                cin[hh] = gi * g.C + (hv[hh] ? (h - tap * p.cbh) * 64 : 0);
+                const int z = tap / (g.Y * g.X), rem = tap - z * g.Y * g.X;
+                const int y = rem / g.X, x = rem - y * g.X;
+                dz[hh] = z * g.dd - g.pd;
+                dyo[hh] = y * g.dh - g.ph;
+                dxo[hh] = x * g.dw - g.pw;
+            }
+            const uint32_t bytes_chunk = (hv[1] ? 2 : 1) * HALF_BYTES + W::B_CHUNK;
+            int issued = 0;
+            for (int st = 0; st < nstages; ++st) {
+                const int s = st % STAGES;
+                if (st >= STAGES && !wait_bar(empty_bar(s), ((st / STAGES) - 1) & 1, abort_flag, p.err)) break;
+                issued = st + 1;
+                const int nc = min(CH, nchunks - st * CH);
+                mbar_arrive_expect_tx(full_bar(s), nc * bytes_chunk);
+                for (int c = 0; c < nc; ++c) {
+                    const ChunkPos cp = chunk_pos(p, q0 + st * CH + c);
+                    const uint32_t dst = sbase + s * W::STAGE + c * W::CHUNK;
+                    for (int hh = 0; hh < 2; ++hh)
+                        if (hv[hh])
+                            tma_load_5d(dst + hh * HALF_BYTES, &xmap, cin[hh], cp.ow0 * g.sw + dxo[hh],
+                                        cp.oh * g.sh + dyo[hh], cp.od * g.sd + dz[hh], cp.n, full_bar(s));
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_5d(dst + W::A_CHUNK + j * HALF_BYTES, &dymap, gi * g.K + nt * BN + j * 64, cp.ow0,
+                                    cp.oh, cp.od, cp.n, full_bar(s));
+                }
+            }
+            // before the CTA can exit, the copies of the last stages issued must have landed
+            // (they have unless the MMA role gave up); a bounded wait, whatever the abort flag
+            const unsigned long long t0 = globaltimer();
+            for (int st = issued > STAGES ? issued - STAGES : 0; st < issued; ++st)
+                while (!mbar_try_wait(full_bar(st % STAGES), (st / STAGES) & 1) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+                }
+        }
+    } else if (warp == 1) {
+        constexpr uint32_t IDESC = idesc_f32acc(128, BN, 1u) | (1u << 15) | (1u << 16);   // A, B MN-major
+        bool ok = true;
+        for (int st = 0; st < nstages && ok; ++st) {
+            const int s = st % STAGES;
+            ok = wait_bar_warp(full_bar(s), (st / STAGES) & 1, abort_flag, p.err);
+            if (!ok) break;
+            tc_fence_after();
+            const int nc = min(CH, nchunks - st * CH);
+            for (int c = 0; c < nc; ++c) {
+                const uint32_t a = sbase + s * W::STAGE + c * W::CHUNK;
+                const uint32_t b = a + W::A_CHUNK;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16_warp(tmem, sw128_mn_desc(a + k * 2048, HALF_BYTES), sw128_mn_desc(b + k * 2048, HALF_BYTES),
+                                  IDESC, (st > 0 || c > 0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit_warp(empty_bar(s));
+        }
+        if (ok) mma_commit_warp(done_bar);
+    } else {
+        // epilogue: TMEM lane quarter (warp % 4); row -> (half, channel) -> (tap, c)
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const int h = 2 * rt + (row >> 6);
+        const int tap = h / p.cbh;
+        const int c = (h - tap * p.cbh) * 64 + (row & 63);
+        const bool row_ok = h < p.halves && c < g.C;
+        const bool ok = wait_bar_warp(done_bar, 0, abort_flag, p.err, true);
+        if (ok) {
+            tc_fence_after();
+            const int NJ = g.taps * g.C;
+            const long long col0 = (long long)tap * g.C + c;
+            const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16);
+            for (int cb = 0; cb < BN; cb += 16) {
+                if (nt * BN + cb >= g.K) break;   // warp-uniform
+                uint32_t v[16];
+                __syncwarp();
+                tmem_ld16(taddr + (uint32_t)cb, v);
+                tmem_ld_wait();
+                if (!row_ok) continue;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int k = nt * BN + cb + e;
+                    if (k >= g.K) break;
+                    const long long o = ((long long)gi * g.K + k) * NJ + col0;
+                    const float f = __uint_as_float(v[e]);
+                    if (p.splits > 1)
+                        p.ws[(long long)split * g.G * g.K * NJ + o] = f;
+                    else
+                        reinterpret_cast<__nv_bfloat16*>(p.dw)[o] = __float2bfloat16_rn(f);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, W::TMEM_COLS);
+    }
+}
+
+template <int BN, int CH, int STAGES>
+constexpr size_t wg_smem_bytes() {
+    return 1024 + (size_t)STAGES * WgCfg<BN, CH>::STAGE + 8 * (2 * STAGES + 1) + 16;
+}
+
+template <int BN, int CH, int STAGES>
+cudaError_t launch_wg(const WgradTcParams& p, const CUtensorMap& xmap, const CUtensorMap& dymap, cudaStream_t stream) {
+    auto kern = conv_wgrad_tc_kernel<BN, CH, STAGES>;
+    constexpr size_t smem = wg_smem_bytes<BN, CH, STAGES>();
+    static_assert(smem <= 232448, "shared memory budget");
+    static bool attr_set[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    return launch_kernel(kern, dim3(p.total_units), dim3(WG_THREADS), smem, stream, p.pdl != 0, 1, p, xmap, dymap);
+}
+
+}  // namespace
+
+cudaError_t launch_wgrad_tc(const WgradTcParams& p, const CUtensorMap* xmap, const CUtensorMap* dymap,
+                            cudaStream_t stream) {
+    switch (p.BN) {
+        case 64: return launch_wg<64, 2, 4>(p, *xmap, *dymap, stream);
+        case 128: return launch_wg<128, 2, 3>(p, *xmap, *dymap, stream);
+        case 256: return launch_wg<256, 1, 4>(p, *xmap, *dymap, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace convfwd

@@ -1,6 +1,7 @@
 """GPU parity of the backward passes (backward data, backward weight) through the C-ABI
 against the CPU oracle, element by element, on seeded inputs; integer inputs bit-exact."""
 import dataclasses
+import os
 import zlib
 
 import numpy as np
@@ -44,7 +45,7 @@ def _check_guard(buf, n, guard=64):
 def run_bwd_data(layer, dtype, dy, w, env=None):
     import torch
     code = CONV_BF16 if dtype == "bf16" else CONV_F32
-    plan = ConvPlan(*layer.plan_args(code), direction="bwd_data")
+    plan = _plan_with_env(layer, code, "bwd_data", env)
     plan.allocate()
     plan.prepack(to_device(w, dtype))
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
@@ -59,10 +60,25 @@ def run_bwd_data(layer, dtype, dy, w, env=None):
     return from_device(dx, dtype), desc
 
 
-def run_bwd_weight(layer, dtype, x, dy):
+def _plan_with_env(layer, code, direction, env):
+    old = {}
+    for k, v in (env or {}).items():
+        old[k] = os.environ.get(k)
+        os.environ[k] = str(v)
+    try:
+        return ConvPlan(*layer.plan_args(code), direction=direction)
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+def run_bwd_weight(layer, dtype, x, dy, env=None):
     import torch
     code = CONV_BF16 if dtype == "bf16" else CONV_F32
-    plan = ConvPlan(*layer.plan_args(code), direction="bwd_weight")
+    plan = _plan_with_env(layer, code, "bwd_weight", env)
     plan.allocate()
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     n = int(np.prod(layer.w_shape()))
@@ -161,3 +177,24 @@ def test_backward_full_size_sampled(wl_name):
         coords = np.array(np.unravel_index(idx, g.w_shape())).T
         ref, S = oracle.conv_bwd_points(g, syn.as_f32(x, wl.dtype), syn.as_f32(dy, wl.dtype), True, coords)
         assert_within(wl.dtype, CONV_EPI_NONE, dw.reshape(-1)[idx], ref, S, f"{wl_name} L{li + 1} dw [{wdesc}]")
+
+
+VARIANT_LAYERS = ["2d_s1_groups", "1d_s2", "2d_s1_g32_c8", "3d_s1_g4", "2d_s2_dil"]
+
+
+@pytest.mark.parametrize("env", [{"CONV_FORCE_SIMT": 1}, {"CONV_FORCE_BN": 64, "CONV_FORCE_SPLITK": 3},
+                                 {"CONV_FORCE_BN": 128, "CONV_FORCE_SPLITK": 1},
+                                 {"CONV_FORCE_BN": 256, "CONV_FORCE_SPLITK": 7}],
+                         ids=["ffma", "tc_bn64_split3", "tc_bn128_whole", "tc_bn256_split7"])
+@pytest.mark.parametrize("name", VARIANT_LAYERS)
+def test_backward_weight_variants(name, env):
+    """Both backward-weight kernels, every tensor-core N tile, whole and split reductions."""
+    dtype, layer = {c[0]: (c[1], c[2]) for c in CASES}[name]
+    x, w, dy = make_bwd_inputs(layer, dtype, 8500 + len(name))
+    got, desc = run_bwd_weight(layer, dtype, x, dy, env=env)
+    if "CONV_FORCE_SIMT" in env:
+        assert desc.startswith("variant=simt"), desc
+    else:
+        assert "operands=mn-major" in desc and f"tile=128x{env['CONV_FORCE_BN']}" in desc, desc
+    ref, S = oracle.conv_bwd_weight(geom_of(layer), syn.as_f32(x, dtype), syn.as_f32(dy, dtype))
+    assert_within(dtype, CONV_EPI_NONE, got, ref.reshape(-1), S.reshape(-1), f"{name} [{desc}]")
