@@ -222,6 +222,62 @@ class LayerRun:
         return esz * (n_out + n_x + n_w + n_b)
 
 
+class BwdRun:
+    """Backward data or backward weight of one layer: its plan, per-rotation-set buffers
+    (dy, x or the packed weight, and the output dx or dw) and CUDA graphs."""
+
+    def __init__(self, wl, li, layer, R, kind, x_sets, dy_sets, w):
+        import torch
+        from convolution_forward_implicit_gb300.binding import ConvPlan
+        self.wl, self.li, self.layer, self.kind = wl, li, layer, kind
+        self.plan = ConvPlan(*layer.plan_args(wl.dtype_code), direction=kind)
+        self.plan.allocate()
+        tdt = self.plan.torch_dtype()
+        self.x_sets, self.dy_sets = x_sets, dy_sets
+        self.wp_sets, self.y_sets = [], []
+        for r in range(R):
+            if kind == "bwd_data":
+                wp = torch.empty_like(self.plan.w_packed)
+                self.plan.prepack(w)
+                wp.copy_(self.plan.w_packed)
+                self.wp_sets.append(wp)
+                self.y_sets.append(torch.empty(self.plan.x_shape(), dtype=tdt, device="cuda"))
+            else:
+                self.y_sets.append(torch.empty(self.plan.w_shape(), dtype=tdt, device="cuda"))
+        self.graphs = []
+        fields = dict(kv.split("=", 1) for kv in self.plan.describe().split())
+        self.kernels_per_call = 1 + (1 if int(fields.get("splits", "1")) > 1 and
+                                     fields.get("reduce", "kernel") != "cluster" else 0)
+
+    def call(self, r):
+        from convolution_forward_implicit_gb300.binding import conv_bwd_data, conv_bwd_weight
+        import torch
+        s = torch.cuda.current_stream().cuda_stream
+        if self.kind == "bwd_data":
+            conv_bwd_data(self.plan.handle, self.dy_sets[r].data_ptr(), self.wp_sets[r].data_ptr(),
+                          self.y_sets[r].data_ptr(), s)
+        else:
+            conv_bwd_weight(self.plan.handle, self.x_sets[r].data_ptr(), self.dy_sets[r].data_ptr(),
+                            self.y_sets[r].data_ptr(), s)
+
+    capture = LayerRun.capture
+
+    @property
+    def flops(self):
+        return self.plan.flops
+
+    def name(self):
+        return f"{self.wl.dtype}_L{self.li + 1}_{'dx' if self.kind == 'bwd_data' else 'dw'}"
+
+    def bytes_alg(self):
+        L = self.layer
+        esz = 2 if self.wl.dtype == "bf16" else 4
+        n_x = int(np.prod(L.x_shape()))
+        n_w = int(np.prod(L.w_shape()))
+        n_dy = int(np.prod(self.plan.y_shape()))
+        return esz * (n_dy + n_w + n_x)   # dx: dy and w in, dx out; dw: x and dy in, dw out
+
+
 def to_device(a, dtype):
     import torch
     if dtype == "bf16":
@@ -247,16 +303,47 @@ def setup_layers(wls, R, tune_iters=0):
     return runs, inputs
 
 
-def rotation_sets(wls):
+def setup_bwd_layers(wls, R):
+    """Backward data and backward weight of every layer of every workload, on seeded x, w and
+    dy (the gradient of the layer's output); returns (runs, host inputs, output sets)."""
+    from convolution_forward_implicit_gb300 import synthetic as syn
+    from convolution_forward_implicit_gb300.workloads import gen_inputs
+    runs, host_in, outs = [], [], []
+    for wl in wls:
+        x0, params = gen_inputs(wl)
+        for li, layer in enumerate(wl.layers):
+            w, _ = params[li]
+            x = x0 if li == 0 else syn.gen_normal(7 + li, layer.x_shape(), wl.dtype)
+            y_shape = tuple(int(v) for v in np_y_shape(layer))
+            dy = syn.gen_normal(20261202 + 1000 * wl.index + 10 * li + 3, y_shape, wl.dtype)
+            xd, dyd, wd = to_device(x, wl.dtype), to_device(dy, wl.dtype), to_device(w, wl.dtype)
+            x_sets = [xd.clone() for _ in range(R)]
+            dy_sets = [dyd.clone() for _ in range(R)]
+            host_in += [(x, wl.dtype, x_sets), (dy, wl.dtype, dy_sets)]
+            for kind in ("bwd_data", "bwd_weight"):
+                br = BwdRun(wl, li, layer, R, kind, x_sets, dy_sets, wd)
+                runs.append(br)
+                outs.append(br.y_sets)
+    return runs, host_in, outs
+
+
+def np_y_shape(layer):
+    import oracle
+    g = oracle.Geom(layer.N, layer.G, layer.C, layer.K, layer.spatial, layer.filter, layer.stride, layer.pad,
+                    layer.dilation)
+    return (layer.N, *g.out_spatial[3 - layer.ndim:], layer.G, layer.K)
+
+
+def rotation_sets(wls, factor=1.0):
     """Copies needed so that one rotation of activations, packed weights and outputs
-    exceeds twice the L2 cache."""
+    exceeds twice the L2 cache (factor scales the bytes of one set)."""
     per_set = 0
     for wl in wls:
         for layer in wl.layers:
             esz = 2 if wl.dtype == "bf16" else 4
             per_set += esz * (int(np.prod(layer.x_shape())) + int(np.prod(layer.w_shape())))
     # outputs are roughly the inputs of the next layer plus the last output
-    per_set = int(per_set * 1.6) + 1
+    per_set = int(per_set * 1.6 * factor) + 1
     return max(4, int(np.ceil(2.2 * L2_BYTES / per_set))), per_set
 
 
@@ -302,8 +389,17 @@ def run_ours(args, ws, rank, local):
     import __graft_entry__
     __graft_entry__.build()
     wls = frontend_workloads(args.workload)
-    R, per_set = rotation_sets(wls)
-    runs, inputs = setup_layers(wls, R, args.tune)
+    bwd = args.pass_ == "bwd"
+    R, per_set = rotation_sets(wls, 2.0 if bwd else 1.0)
+    if bwd:
+        runs, host_in, out_sets = setup_bwd_layers(wls, R)
+    else:
+        runs, inputs = setup_layers(wls, R, args.tune)
+        host_in = [(x, wl.dtype, x_sets) for (wl, x, x_sets) in inputs]
+        last = {}
+        for lr in runs:
+            last[lr.wl.name] = lr
+        out_sets = [lr.y_sets for lr in last.values()]
     stream = torch.cuda.current_stream()
     if args.overlap:
         for lr in runs:
@@ -387,7 +483,7 @@ def run_ours(args, ws, rank, local):
     value = ws * step_flops / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end: pinned host inputs in, final outputs back to pinned host memory
-    e2e = run_e2e(args, runs, inputs, R, stream, ws, local, step)
+    e2e = run_e2e(args, runs, host_in, out_sets, R, stream, ws, local, step)
 
     # ---- roofline of the dominant kernel
     dom = int(np.argmax(per_layer_ms))
@@ -405,7 +501,9 @@ def run_ours(args, ws, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "+".join(sorted({wl.dtype for wl in wls}, key=lambda d: d != "f32")),
         "data": "synthetic (seeded N(0,1) inputs, U(+-1/sqrt(C_in*taps)) weights, U(+-0.05) bias)",
-        "config": {"workload": workload_description(args.workload),
+        "config": {"workload": workload_description(args.workload) + (
+                       "; backward: dx and dw of every layer per step (seeded N(0,1) dy)" if bwd else ""),
+                   "pass": "backward (data + weight)" if bwd else "forward",
                    "l2": f"inputs larger than L2: {R} rotating sets of activations, packed weights and outputs "
                          f"(~{R * per_set / 1e6:.0f} MB per rotation, L2 129 MB)",
                    "graphs": graph_mode,
@@ -420,34 +518,32 @@ def run_ours(args, ws, rank, local):
         "clocks": clk,
     }
     if rank == 0:
-        line["cpu_baseline"] = cpu_baseline(wls)
+        line["cpu_baseline"] = cpu_baseline_bwd(wls) if bwd else cpu_baseline(wls)
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, runs, inputs, R, stream, ws, local, step):
+def run_e2e(args, runs, in_specs, out_sets, R, stream, ws, local, step):
     """The same step through the public API with host buffers: each step copies its inputs
-    from pinned host memory, runs every layer, and copies the final outputs back."""
+    (in_specs: storage array, dtype, device copies) from pinned host memory, runs every layer,
+    and copies the results (out_sets: device copies) back to pinned host memory."""
     import torch
     host_in, host_out = [], []
-    for (wl, x, x_sets) in inputs:
-        h = to_device(x, wl.dtype).cpu().pin_memory()
-        host_in.append((h, x_sets))
-    last = {}
-    for lr in runs:
-        last[lr.wl.name] = lr
-    for lr in last.values():
-        host_out.append((torch.empty(lr.y_sets[0].shape, dtype=lr.y_sets[0].dtype).pin_memory(), lr))
+    for (a, dtype, sets) in in_specs:
+        h = to_device(a, dtype).cpu().pin_memory()
+        host_in.append((h, sets))
+    for sets in out_sets:
+        host_out.append((torch.empty(sets[0].shape, dtype=sets[0].dtype).pin_memory(), sets))
     bi = sum(h.numel() * h.element_size() for h, _ in host_in)
     bo = sum(h.numel() * h.element_size() for h, _ in host_out)
     K = args.steps
 
     def e2e_step(i):
         r = i % R
-        for h, x_sets in host_in:
-            x_sets[r].copy_(h, non_blocking=True)
+        for h, sets in host_in:
+            sets[r].copy_(h, non_blocking=True)
         step(i)
-        for h, lr in host_out:
-            h.copy_(lr.y_sets[r], non_blocking=True)
+        for h, sets in host_out:
+            h.copy_(sets[r], non_blocking=True)
 
     for i in range(args.warmup):
         e2e_step(i)
@@ -601,6 +697,44 @@ def cpu_baseline(wls):
             "sample": f"one full step (every layer, whole output), {flops / 1e9:.2f} GFLOP in {secs:.2f} s"}
 
 
+def cpu_baseline_bwd(wls, budget_flops=4e9):
+    """The backward oracle on the host cores: a random sample of dx and dw elements of every
+    layer (about budget_flops of useful work in all), split over threads."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    from convolution_forward_implicit_gb300 import synthetic as syn
+    from convolution_forward_implicit_gb300.workloads import gen_inputs
+    nthreads = os.cpu_count() or 1
+    total_flops = sum(2.0 * int(np.prod(np_y_shape(l))) * l.C * l.taps for wl in wls for l in wl.layers) * 2
+    frac = min(1.0, budget_flops / total_flops)
+    secs, flops = 0.0, 0.0
+    for wl in wls:
+        x0, params = gen_inputs(wl)
+        for li, layer in enumerate(wl.layers):
+            g = oracle.Geom(layer.N, layer.G, layer.C, layer.K, layer.spatial, layer.filter, layer.stride,
+                            layer.pad, layer.dilation)
+            w, _ = params[li]
+            x = syn.as_f32(x0 if li == 0 else syn.gen_normal(7 + li, layer.x_shape(), wl.dtype), wl.dtype)
+            dy = syn.as_f32(syn.gen_normal(3 + li, g.y_shape(), wl.dtype), wl.dtype)
+            wf = syn.as_f32(w, wl.dtype)
+            layer_flops = 2.0 * int(np.prod(g.y_shape())) * layer.C * layer.taps
+            for weight, shape, a, b in ((False, g.x_shape(), dy, wf), (True, g.w_shape(), x, dy)):
+                total = int(np.prod(shape))
+                n = max(nthreads, int(total * frac))
+                n = min(n, total)
+                idx = np.random.default_rng(li).choice(total, size=n, replace=False)
+                coords = np.array(np.unravel_index(idx, shape)).T.astype(np.int64)
+                chunks = np.array_split(coords, nthreads)
+                t = time.perf_counter()
+                with ThreadPoolExecutor(nthreads) as ex:
+                    list(ex.map(lambda c: oracle.conv_bwd_points(g, a, b, weight, c), chunks))
+                secs += time.perf_counter() - t
+                flops += layer_flops * n / total
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"random dx and dw elements of every layer ({frac:.2%} of each), {flops / 1e9:.2f} "
+                      f"GFLOP-equivalent in {secs:.2f} s"}
+
+
 def run_reference(args, ws, rank, local):
     """The oracle as the reference arm: each step evaluates a fixed random sample of each
     layer's outputs (1/32 of them) on all host cores; throughput counts the sampled FLOPs."""
@@ -661,6 +795,8 @@ def main():
     ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash and exit")
     ap.add_argument("--no-overlap", dest="overlap", action="store_false",
                     help="launch each layer only after the previous one completes (no programmatic dependents)")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="fwd: the forward pass of every layer; bwd: backward data and backward weight of every layer")
     ap.add_argument("--tune", type=int, default=0, metavar="ITERS",
                     help="before timing, let the measured selector time every candidate plan of each layer "
                          "(ITERS calls each) and keep the fastest; 0 = the planner's rules")

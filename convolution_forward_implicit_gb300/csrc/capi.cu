@@ -156,17 +156,28 @@ __global__ void prepack_simt_kernel(const T* __restrict__ w, T* __restrict__ out
 // Backward data at unit stride: the forward weight of the transposed problem,
 // w'[g][c][tap'][k] = w[g][k][taps-1-tap'][c] (every tap axis flipped, C and K swapped),
 // element type E (2 or 4 bytes), staged for the forward prepack.
+// For a stride phase the staged taps are a subset: staged tap t' = (z', y', x') of a Zs x Ys x Xs
+// filter is forward tap (t0 - t'*dt) per axis of the Zo x Yo x Xo one.
+struct TapMap {
+    int Zo, Yo, Xo, Zs, Ys, Xs;
+    int t0[3], dt[3];
+};
+
 template <typename E>
-__global__ void flip_transpose_kernel(const E* __restrict__ w, E* __restrict__ out, int K, int C, int taps,
+__global__ void flip_transpose_kernel(const E* __restrict__ w, E* __restrict__ out, int K, int C, TapMap tm,
                                       long long total) {
+    const int taps_s = tm.Zs * tm.Ys * tm.Xs, taps_o = tm.Zo * tm.Yo * tm.Xo;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
         const int k = (int)(idx % K);
         long long r = idx / K;
-        const int t = (int)(r % taps); r /= taps;
+        const int t = (int)(r % taps_s); r /= taps_s;
         const int c = (int)(r % C);
         const long long g = r / C;
-        out[idx] = w[((g * K + k) * taps + (taps - 1 - t)) * C + c];
+        const int xs = t % tm.Xs, ys = (t / tm.Xs) % tm.Ys, zs = t / (tm.Xs * tm.Ys);
+        const int tap = ((tm.t0[0] - zs * tm.dt[0]) * tm.Yo + (tm.t0[1] - ys * tm.dt[1])) * tm.Xo +
+                        (tm.t0[2] - xs * tm.dt[2]);
+        out[idx] = w[((g * K + k) * taps_o + tap) * C + c];
     }
 }
 
@@ -194,9 +205,21 @@ __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float
 __device__ __forceinline__ void from_f(float& d, float v) { d = v; }
 __device__ __forceinline__ void from_f(__nv_bfloat16& d, float v) { d = __float2bfloat16_rn(v); }
 
+// Row m of the partials (pixels in N Do Ho Wo order) -> its place in y.
+__device__ __forceinline__ long long reduce_row(const Lattice& L, long long m, int Do, int Ho, int Wo) {
+    if (!L.on) return m;
+    const int ow = (int)(m % Wo);
+    long long q = m / Wo;
+    const int oh = (int)(q % Ho);
+    q /= Ho;
+    const int od = (int)(q % Do);
+    return lattice_pixel(L, (int)(q / Do), od, oh, ow);
+}
+
 template <typename T>
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, long long MGK, int GK,
-                                     const T* __restrict__ bias, T* __restrict__ y, int epi, int pdl) {
+                                     const T* __restrict__ bias, T* __restrict__ y, int epi, int pdl, Lattice lat,
+                                     int Do, int Ho, int Wo) {
     if (pdl) {   // the partial sums come from the conv kernel just before this one
         griddep_launch();
         griddep_wait();
@@ -214,11 +237,12 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, l
             }
             float v[4] = {a.x, a.y, a.z, a.w};
             const int col = (int)((i * 4) % GK);
+            const long long o = reduce_row(lat, (i * 4) / GK, Do, Ho, Wo) * GK + col;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 if (add_bias) v[e] += to_f(bias[col + e]);
                 if (do_gelu) v[e] = gelu(v[e]);
-                from_f(y[i * 4 + e], v[e]);
+                from_f(y[o + e], v[e]);
             }
         }
     } else {
@@ -228,7 +252,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, l
             for (int s = 1; s < splits; ++s) a += ws[(long long)s * MGK + i];
             if (add_bias) a += to_f(bias[i % GK]);
             if (do_gelu) a = gelu(a);
-            from_f(y[i], a);
+            from_f(y[reduce_row(lat, i / GK, Do, Ho, Wo) * GK + i % GK], a);
         }
     }
 }
@@ -236,7 +260,8 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, l
 }  // namespace
 
 // ----------------------------------------------------------------------------- plan
-enum Variant { VAR_TC = 0, VAR_SIMT = 1, VAR_DG_SIMT = 2, VAR_WG_SIMT = 3, VAR_WG_TC = 4 };
+enum Variant { VAR_TC = 0, VAR_SIMT = 1, VAR_DG_SIMT = 2, VAR_WG_SIMT = 3, VAR_WG_TC = 4, VAR_DG_PHASED = 5 };
+constexpr int MAX_PHASES = 16;
 enum Direction { DIR_FWD = 0, DIR_BWD_DATA = 1, DIR_BWD_WEIGHT = 2 };
 
 // Plan choices that can be fixed instead of decided by rule: by the measured selector
@@ -291,6 +316,12 @@ struct conv_plan {
     Geom fg;                // the forward problem (g is the problem the kernels run)
     int dg_fwd;             // backward data run as the forward conv of dy with flipped, transposed weights
     size_t dg_src_off;      // where in w_packed the prepack stages those weights
+    int dg_t0[3], dg_dt[3]; // staged tap t' (per axis) is forward tap t0 - t'*dt
+    Lattice lat;            // output placement (stride phases of a backward data)
+    conv_plan* ph[MAX_PHASES];   // stride phases: forward plans whose outputs interleave in dx
+    size_t ph_off[MAX_PHASES];   // each phase's packed weight within w_packed
+    int nph;
+    int ph_zero;            // some input pixels receive no tap at all: dx is cleared first
     int wg_kt, wg_jt, wg_mps;   // backward weight (FFMA): tiles along K and taps*C, pixels per split
     int wg_rt, wg_nt, wg_q, wg_qps, wg_nwb, wg_cbh;   // backward weight (tensor cores), see WgradTcParams
     char desc[320];
@@ -511,7 +542,7 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     // Slab mode for stride-1 problems with several taps per plane (one box serves them all);
     // its shared-memory fit is checked once the N tile is known.
     p->slab = 0;
-    const bool want_slab = allow_slab && tma && g.sw == 1 && g.sh == 1 && g.sd == 1 && g.Y * g.X >= 3 &&
+    const bool want_slab = allow_slab && !p->lat.on && tma && g.sw == 1 && g.sh == 1 && g.sd == 1 && g.Y * g.X >= 3 &&
                            p->ch.gather != 2;
     if (tma) {
         p->map_kind = map_kind;
@@ -725,7 +756,7 @@ static void choose_variant(conv_plan* p) {
         p->dg_src_off = align256(p->prepack_bytes);
         p->prepack_bytes = p->dg_src_off + (size_t)G * C * K * p->g.taps * (p->dtype == CONV_BF16 ? 2 : 4);
         const size_t n = strlen(p->desc);
-        snprintf(p->desc + n, sizeof(p->desc) - n, " direction=bwd_data(transposed forward)");
+        snprintf(p->desc + n, sizeof(p->desc) - n, " direction=bwd_data(transposed_forward)");
     }
 }
 
@@ -846,6 +877,108 @@ static conv_status init_plan(conv_plan** pp, conv_plan_t* out, int ndim, int64_t
     p->Go = g.G; p->Co = g.C; p->Ko = g.K;
     *pp = p;
     return CONV_OK;
+}
+
+static int gcd_int(int a, int b) { return b ? gcd_int(b, a % b) : a; }
+
+// Backward data at stride > 1 as stride phases.  The input pixels i = r + s*j of one residue r
+// (per axis) receive exactly the taps t with (r + pad - t*dil) divisible by s, from output
+// position j + q_t, q_t = (r + pad - t*dil)/s.  Those taps are every (s / gcd(s, dil))-th one,
+// so a phase is a unit-stride forward convolution of dy with the subset of taps reversed,
+// dilation dil / gcd(s, dil) and padding -q of the last tap, C and K swapped, whose outputs land
+// on the lattice r + s*j of dx.  Each phase runs the tensor-core forward kernels; a residue that
+// no tap reaches leaves zeros (dx is cleared first).  Returns false where a phase does not fit
+// the tensor-core path (the gather kernel is used instead).
+static bool plan_dg_phased(conv_plan* p) {
+    const Geom& f = p->fg;
+    const int S[3] = {f.sd, f.sh, f.sw}, P[3] = {f.pd, f.ph, f.pw}, DL[3] = {f.dd, f.dh, f.dw};
+    const int F[3] = {f.Z, f.Y, f.X}, I[3] = {f.D, f.H, f.W}, O[3] = {f.Do, f.Ho, f.Wo};
+    if ((int64_t)S[0] * S[1] * S[2] > MAX_PHASES) return false;
+    if (p->dtype == CONV_BF16 ? (f.C % 8 || f.K % 8) : (f.C % 4 || f.K % 4)) return false;
+    // per axis and residue: taps, first (largest) tap, tap step, padding, dilation, lattice size
+    struct Axis { int nt, t0, dt, pad, dil, J; };
+    Axis ax[3][8];
+    for (int a = 0; a < 3; ++a) {
+        if (S[a] > 8) return false;
+        const int gg = gcd_int(S[a], DL[a]);
+        for (int r = 0; r < S[a]; ++r) {
+            Axis& A = ax[a][r];
+            A.J = r < I[a] ? (I[a] - r + S[a] - 1) / S[a] : 0;
+            A.nt = 0; A.t0 = -1;
+            for (int t = F[a] - 1; t >= 0; --t) {
+                const int num = r + P[a] - t * DL[a];
+                if (((num % S[a]) + S[a]) % S[a] == 0) {
+                    if (A.t0 < 0) A.t0 = t;
+                    ++A.nt;
+                }
+            }
+            A.dt = S[a] / gg;
+            A.dil = DL[a] / gg;
+            A.pad = A.t0 >= 0 ? -((r + P[a] - A.t0 * DL[a]) / S[a]) : 0;
+        }
+    }
+    p->nph = 0;
+    p->ph_zero = 0;
+    size_t off = 0, ws = 0;
+    bool ok = true;
+    for (int rd = 0; rd < S[0] && ok; ++rd)
+        for (int rh = 0; rh < S[1] && ok; ++rh)
+            for (int rw = 0; rw < S[2] && ok; ++rw) {
+                const Axis* A[3] = {&ax[0][rd], &ax[1][rh], &ax[2][rw]};
+                if (!A[0]->J || !A[1]->J || !A[2]->J) continue;             // no pixels in this residue
+                if (!A[0]->nt || !A[1]->nt || !A[2]->nt) { p->ph_zero = 1; continue; }
+                conv_plan* q = new (std::nothrow) conv_plan(*p);
+                if (!q) { ok = false; break; }
+                q->nph = 0;
+                Geom& g = q->g;
+                g.C = f.K; g.K = f.C;
+                g.D = f.Do; g.H = f.Ho; g.W = f.Wo;
+                g.Z = A[0]->nt; g.Y = A[1]->nt; g.X = A[2]->nt;
+                g.sd = g.sh = g.sw = 1;
+                g.pd = A[0]->pad; g.ph = A[1]->pad; g.pw = A[2]->pad;
+                g.dd = A[0]->dil; g.dh = A[1]->dil; g.dw = A[2]->dil;
+                g.Do = A[0]->J; g.Ho = A[1]->J; g.Wo = A[2]->J;
+                g.M = f.N * g.Do * g.Ho * g.Wo;
+                g.taps = g.Z * g.Y * g.X;
+                q->Go = g.G; q->Co = g.C; q->Ko = g.K;
+                q->dg_fwd = 1;
+                for (int a = 0; a < 3; ++a) { q->dg_t0[a] = A[a]->t0; q->dg_dt[a] = A[a]->dt; }
+                q->lat.on = 1;
+                q->lat.D = f.D; q->lat.H = f.H; q->lat.W = f.W;
+                q->lat.sd = S[0]; q->lat.sh = S[1]; q->lat.sw = S[2];
+                q->lat.rd = rd; q->lat.rh = rh; q->lat.rw = rw;
+                q->workspace = nullptr; q->workspace_size = 0;
+                choose_variant(q);
+                p->ph[p->nph++] = q;
+                if (q->variant != VAR_TC) { ok = false; break; }
+                p->ph_off[p->nph - 1] = off;
+                off += align256(q->prepack_bytes);
+                ws = std::max(ws, q->workspace_bytes);
+            }
+    if (!ok || p->nph == 0) {
+        for (int i = 0; i < p->nph; ++i) delete p->ph[i];
+        p->nph = 0;
+        return false;
+    }
+    p->variant = VAR_DG_PHASED;
+    p->prepack_bytes = p->packed_bytes = off;
+    p->workspace_bytes = ws;
+    const conv_plan* big = p->ph[0];
+    for (int i = 1; i < p->nph; ++i)
+        if (p->ph[i]->flops > big->flops) big = p->ph[i];
+    // "variant=<the largest phase's> direction=bwd_data(phases) phases=P zero_fill=Z largest=<its other
+    // fields, ':' for '=' and ',' for ' '>" (one key=value token each)
+    const char* sp = strchr(big->desc, ' ');
+    const int vlen = sp ? (int)(sp - big->desc) : (int)strlen(big->desc);
+    int n = snprintf(p->desc, sizeof(p->desc), "%.*s direction=bwd_data(phases) phases=%d zero_fill=%d largest=", vlen,
+                     big->desc, p->nph, p->ph_zero);
+    for (const char* c = sp ? sp + 1 : ""; *c && n + 1 < (int)sizeof(p->desc); ++c) {
+        if (strncmp(c, "direction=", 10) == 0) break;
+        p->desc[n++] = *c == ' ' ? ',' : *c == '=' ? ':' : *c;
+    }
+    while (n > 0 && p->desc[n - 1] == ',') --n;
+    p->desc[n] = 0;
+    return true;
 }
 
 // Backward data on the FFMA pipe: rows are the N*D*H*W input pixels, columns the C input
@@ -1016,6 +1149,7 @@ conv_status conv_bwd_data_plan_create(conv_plan_t* out, int ndim, int64_t N, int
     // kernel serves it.  Otherwise each input pixel gathers the dy positions that map onto it.
     const bool transposed = f.sd == 1 && f.sh == 1 && f.sw == 1 && f.dd * (f.Z - 1) >= f.pd &&
                             f.dh * (f.Y - 1) >= f.ph && f.dw * (f.X - 1) >= f.pw;
+    choice_from_env(p->ch);   // the test hooks reach every phase's plan too
     if (transposed) {
         Geom& g = p->g;
         g.C = f.K; g.K = f.C;
@@ -1025,11 +1159,13 @@ conv_status conv_bwd_data_plan_create(conv_plan_t* out, int ndim, int64_t N, int
         g.M = f.N * f.D * f.H * f.W;
         p->Go = g.G; p->Co = g.C; p->Ko = g.K;
         p->dg_fwd = 1;
+        p->dg_t0[0] = f.Z - 1; p->dg_t0[1] = f.Y - 1; p->dg_t0[2] = f.X - 1;
+        p->dg_dt[0] = p->dg_dt[1] = p->dg_dt[2] = 1;
         PlanChoice c;
         if (!choice_from_env(c)) tune_table_lookup(p, c);
         p->ch = c;
         choose_variant(p);
-    } else {
+    } else if (!plan_dg_phased(p)) {
         plan_dg_simt(p);
     }
     *out = p;
@@ -1098,18 +1234,28 @@ conv_status conv_prepack_weights(conv_plan_t plan, const void* w, void* w_packed
                                                                      plan->Kg, plan->Kpad, total);
         return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
     }
+    if (plan->variant == VAR_DG_PHASED) {
+        for (int i = 0; i < plan->nph; ++i) {
+            const conv_status st = conv_prepack_weights(plan->ph[i], w, static_cast<uint8_t*>(w_packed) + plan->ph_off[i],
+                                                        stream);
+            if (st != CONV_OK) return st;
+        }
+        return CONV_OK;
+    }
     if (plan->dg_fwd) {   // stage the flipped, transposed weight, then prepack it as a forward weight
         const Geom& f = plan->fg;
         void* stage = static_cast<uint8_t*>(w_packed) + plan->dg_src_off;
-        const long long total = (long long)f.G * f.K * f.taps * f.C;
+        TapMap tm;
+        tm.Zo = f.Z; tm.Yo = f.Y; tm.Xo = f.X; tm.Zs = g.Z; tm.Ys = g.Y; tm.Xs = g.X;
+        for (int i = 0; i < 3; ++i) { tm.t0[i] = plan->dg_t0[i]; tm.dt[i] = plan->dg_dt[i]; }
+        const long long total = (long long)f.G * f.K * g.taps * f.C;
         const int blocks = (int)std::min<long long>(cdiv(total, threads), 65535);
         if (plan->dtype == CONV_BF16)
             flip_transpose_kernel<uint16_t><<<blocks, threads, 0, s>>>(static_cast<const uint16_t*>(w),
-                                                                      static_cast<uint16_t*>(stage), f.K, f.C, f.taps,
-                                                                      total);
+                                                                      static_cast<uint16_t*>(stage), f.K, f.C, tm, total);
         else
             flip_transpose_kernel<float><<<blocks, threads, 0, s>>>(static_cast<const float*>(w),
-                                                                   static_cast<float*>(stage), f.K, f.C, f.taps, total);
+                                                                   static_cast<float*>(stage), f.K, f.C, tm, total);
         w = stage;
     }
     if (plan->variant == VAR_TC && plan->tf32) {
@@ -1142,7 +1288,8 @@ conv_status conv_prepack_weights(conv_plan_t plan, const void* w, void* w_packed
 
 // The split-K reduction: partial sums in split order, then the epilogue.
 static conv_status launch_reduce_n(conv_plan_t plan, const float* ws, const void* bias, void* y, long long MGK,
-                                   int GK, int epi, cudaStream_t s) {
+                                   int GK, int epi, cudaStream_t s, const Lattice& lat = Lattice{}) {
+    const Geom& g = plan->g;
     const int threads = 256;
     const long long work = GK % 4 == 0 ? MGK / 4 : MGK;
     const int blocks = (int)std::min<long long>(cdiv(work, threads), (long long)plan->sm_count * 8);
@@ -1151,16 +1298,17 @@ static conv_status launch_reduce_n(conv_plan_t plan, const float* ws, const void
     if (plan->dtype == CONV_BF16)
         e = launch_kernel(splitk_reduce_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, s, pdl, 1, ws,
                           plan->splits, MGK, GK, static_cast<const __nv_bfloat16*>(bias),
-                          static_cast<__nv_bfloat16*>(y), epi, (int)pdl);
+                          static_cast<__nv_bfloat16*>(y), epi, (int)pdl, lat, g.Do, g.Ho, g.Wo);
     else
         e = launch_kernel(splitk_reduce_kernel<float>, dim3(blocks), dim3(threads), 0, s, pdl, 1, ws, plan->splits, MGK,
-                          GK, static_cast<const float*>(bias), static_cast<float*>(y), epi, (int)pdl);
+                          GK, static_cast<const float*>(bias), static_cast<float*>(y), epi, (int)pdl, lat, g.Do, g.Ho,
+                          g.Wo);
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
 static conv_status launch_reduce(conv_plan_t plan, const float* ws, const void* bias, void* y, cudaStream_t s) {
     const Geom& g = plan->g;
-    return launch_reduce_n(plan, ws, bias, y, (long long)g.M * g.G * g.K, g.G * g.K, (int)plan->epi, s);
+    return launch_reduce_n(plan, ws, bias, y, (long long)g.M * g.G * g.K, g.G * g.K, (int)plan->epi, s, plan->lat);
 }
 
 // Argument checks shared by both forward entry points.
@@ -1202,6 +1350,7 @@ static conv_status run_forward(conv_plan_t plan, const void* x, const void* w_pa
         tp.pdl = plan->overlap;
         tp.epi_warps = plan->epi_warps ? plan->epi_warps : 8;
         tp.cluster_red = plan->cluster_red;
+        tp.lat = plan->lat;
         tp.f_splits = make_fastdiv(plan->splits); tp.f_num_nt = make_fastdiv(plan->num_nt);
         tp.f_G = make_fastdiv(plan->g.G); tp.f_tiles_w = make_fastdiv(plan->tiles_w);
         tp.f_tiles_h = make_fastdiv(plan->tiles_h); tp.f_Do = make_fastdiv(plan->g.Do);
@@ -1261,6 +1410,22 @@ conv_status conv_bwd_data(conv_plan_t plan, const void* dy, const void* w_packed
     if (st != CONV_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (plan->dg_fwd) return run_forward(plan, dy, w_packed, nullptr, dx, ws, s);
+    if (plan->variant == VAR_DG_PHASED) {
+        const Geom& f = plan->fg;
+        if (plan->ph_zero &&
+            cudaMemsetAsync(dx, 0, (size_t)f.N * f.D * f.H * f.W * f.G * f.C * (plan->dtype == CONV_BF16 ? 2 : 4), s) !=
+                cudaSuccess)
+            return CONV_ERR_CUDA;
+        for (int i = 0; i < plan->nph; ++i) {
+            conv_plan* q = plan->ph[i];
+            // phases write disjoint pixels of dx: each may overlap the one before it
+            q->overlap = (i > 0 || (plan->overlap && !plan->ph_zero)) ? 1 : 0;
+            const conv_status st = run_forward(q, dy, static_cast<const uint8_t*>(w_packed) + plan->ph_off[i], nullptr,
+                                               dx, ws, s);
+            if (st != CONV_OK) return st;
+        }
+        return CONV_OK;
+    }
     const Geom& f = plan->fg;
     SimtParams sp;
     sp.g = f;
@@ -1328,6 +1493,8 @@ conv_status conv_plan_check(conv_plan_t plan, void* stream) {
 }
 
 conv_status conv_plan_destroy(conv_plan_t plan) {
+    if (plan)
+        for (int i = 0; i < plan->nph; ++i) delete plan->ph[i];
     delete plan;
     return CONV_OK;
 }

@@ -88,6 +88,22 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
 // Device error word codes (bit flags).
 enum : unsigned { ERR_WAIT_TIMEOUT = 1u };
 
+// Output placement.  Normally output pixel (n, od, oh, ow) is row ((n*Do + od)*Ho + oh)*Wo + ow
+// of y.  With on = 1 the outputs are a lattice of a larger tensor of D x H x W pixels: pixel
+// (n, od, oh, ow) goes to (n, r_d + s_d*od, r_h + s_h*oh, r_w + s_w*ow) there (one stride phase
+// of a backward-data pass).
+struct Lattice {
+    int on;
+    int D, H, W;
+    int sd, sh, sw;
+    int rd, rh, rw;
+};
+
+__host__ __device__ __forceinline__ long long lattice_pixel(const Lattice& L, int n, int od, int oh, int ow) {
+    return (((long long)n * L.D + L.rd + (long long)L.sd * od) * L.H + L.rh + (long long)L.sh * oh) * L.W + L.rw +
+           (long long)L.sw * ow;
+}
+
 // ---- tensor-core (tcgen05) bf16 implicit GEMM ----
 struct TcParams {
     Geom g;
@@ -132,6 +148,7 @@ struct TcParams {
     int epi_warps;          // per-tap kernel: 8 or 16 epilogue warps
     int cluster_red;        // 1: the splits of a tile run as one cluster and sum their partial
                             // accumulators through distributed shared memory (no workspace)
+    Lattice lat;            // where the output pixels land in y (one phase of a strided backward data)
     // divisors of the per-tile index arithmetic
     FastDiv f_splits, f_num_nt, f_G, f_tiles_w, f_tiles_h, f_Do, f_Ho, f_Wo, f_cbt, f_cpt, f_X, f_YX, f_BW, f_bws;
 };

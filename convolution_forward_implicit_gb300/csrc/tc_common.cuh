@@ -244,6 +244,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Place in y of GEMM row m (pixels in N Do Ho Wo order) of a lattice-output problem.
+__device__ __forceinline__ long long out_pixel_linear(const TcParams& p, int m) {
+    const int q1 = fdiv(m, p.f_Wo);
+    const int ow = m - q1 * p.g.Wo;
+    const int q2 = fdiv(q1, p.f_Ho);
+    const int oh = q1 - q2 * p.g.Ho;
+    const int n = fdiv(q2, p.f_Do);
+    const int od = q2 - n * p.g.Do;
+    return lattice_pixel(p.lat, n, od, oh, ow);
+}
+
 __device__ __forceinline__ void decode_unit(const TcParams& p, int u, int& mt, int& g, int& nt, int& split) {
     const int r = fdiv(u, p.f_splits);
     split = u - r * p.splits;

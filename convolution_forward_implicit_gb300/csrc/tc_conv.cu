@@ -380,17 +380,18 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
             TileOrigin to{0, 0, 0, 0};
             if (T::TMA) to = tile_origin(p, mt);
             // element offset of accumulator row rr's pixel, or -1 if the row is outside the output
+            // (partial sums are indexed by the GEMM row; final outputs by their place in y)
             auto row_offset = [&](int rr) -> long long {
-                int m;
                 if (T::TMA) {
                     const int rh = fdiv(rr, p.f_BW);
                     const int oh = to.oh0 + rh, ow = to.ow0 + (rr - rh * p.BW);
                     if (rr >= p.BW * p.BH || oh >= g.Ho || ow >= g.Wo) return -1;
-                    m = ((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow;
-                } else {
-                    m = mt * BM + rr;
-                    if (m >= g.M) return -1;
+                    if (p.lat.on && !partial) return lattice_pixel(p.lat, to.n, to.od, oh, ow) * GK;
+                    return (long long)(((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow) * GK;
                 }
+                const int m = mt * BM + rr;
+                if (m >= g.M) return -1;
+                if (p.lat.on && !partial) return out_pixel_linear(p, m) * GK;
                 return (long long)m * GK;
             };
             if (p.cluster_red) {
@@ -458,15 +459,17 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                 const int col = (i - (i / per_row) * per_row) * 4;
                 const int n = nt * BN + col;
                 if (n >= g.K) continue;
-                int m;
+                long long m;
                 if (T::TMA) {
                     const int rh = fdiv(rr, p.f_BW);
                     const int oh = to.oh0 + rh, ow = to.ow0 + (rr - rh * p.BW);
                     if (rr >= p.BW * p.BH || oh >= g.Ho || ow >= g.Wo) continue;
-                    m = ((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow;
+                    m = p.lat.on ? lattice_pixel(p.lat, to.n, to.od, oh, ow)
+                                 : (long long)(((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow);
                 } else {
-                    m = mt * BM + rr;
-                    if (m >= g.M) continue;
+                    const int ml = mt * BM + rr;
+                    if (ml >= g.M) continue;
+                    m = p.lat.on ? out_pixel_linear(p, ml) : ml;
                 }
                 const uint32_t off = (uint32_t)(rr * RED_PITCH + col) * 4u;
                 float4 a = ld_cluster_f4(cluster_map(red0 + off, 0));

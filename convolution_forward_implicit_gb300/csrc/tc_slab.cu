@@ -442,7 +442,7 @@ size_t slab_smem_bytes(int BN, int tf32, int sa, int sb, size_t a_stage, int bta
 }
 
 cudaError_t launch_slab(const TcParams& p, const CUtensorMap* act_map, int grid, size_t smem, cudaStream_t stream) {
-    if (!act_map || p.slab_sa < 2 || p.slab_sa > SLAB_MAX_SA ||
+    if (!act_map || p.lat.on || p.slab_sa < 2 || p.slab_sa > SLAB_MAX_SA ||   // no lattice outputs here
         (!p.slab_resident && (p.slab_sb < 2 || p.slab_sb > SLAB_MAX_SB)) || smem > SLAB_SMEM_MAX)
         return cudaErrorInvalidValue;
 // (3xTF32 keeps the generic loop: unrolled, its 12 MMAs per tap measured slower; tile pairs

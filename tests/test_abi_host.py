@@ -276,7 +276,7 @@ def test_backward_plans_describe_shape_flops_and_variant(lib):
             d = B.conv_plan_describe(h)
             if kind == "data":
                 # unit stride: the forward kernels on the transposed problem (C and K swapped)
-                assert "direction=bwd_data(transposed forward)" in d and d.startswith("variant=tc_bf16"), d
+                assert "direction=bwd_data(transposed_forward)" in d and d.startswith("variant=tc_bf16"), d
                 assert B.conv_prepacked_weight_bytes(h) > 0
             else:
                 assert "direction=bwd_weight" in d, d
@@ -286,13 +286,24 @@ def test_backward_plans_describe_shape_flops_and_variant(lib):
                 assert e.value.status == B.CONV_ERR_INVALID_ARG
         finally:
             B.conv_plan_destroy(h)
-    # stride 2, and padding beyond the filter's reach: the gather kernel
-    for kw in (dict(stride=(2, 2)), dict(pad=(3, 1))):
+    # stride 2 (4 phases), and padding beyond the filter's reach (1 phase, negative padding):
+    # stride phases on the forward kernels
+    for kw, nph in ((dict(stride=(2, 2)), 4), (dict(pad=(3, 1)), 1), (dict(stride=(2, 3), filt=(1, 1), pad=(0, 0)), 1)):
         h = _bwd_plan("data", **kw)
         try:
-            assert "direction=bwd_data(gather)" in B.conv_plan_describe(h)
+            d = dict(kv.split("=", 1) for kv in B.conv_plan_describe(h).split())
+            assert d["direction"] == "bwd_data(phases)" and d["phases"] == str(nph), d
+            assert d["variant"] == "tc_bf16"
+            # a 1x1 filter at stride 2 x 3 reaches one input pixel in 6: the rest are cleared
+            assert d["zero_fill"] == ("1" if kw.get("filt") == (1, 1) else "0"), d
         finally:
             B.conv_plan_destroy(h)
+    # channel counts the tensor-core path cannot take: the gather kernel
+    h = _bwd_plan("data", C=6, K=10, stride=(2, 2), dtype=B.CONV_F32)
+    try:
+        assert "direction=bwd_data(gather)" in B.conv_plan_describe(h)
+    finally:
+        B.conv_plan_destroy(h)
 
 
 def test_backward_entry_points_check_direction_and_arguments(lib):
@@ -331,3 +342,18 @@ def test_backward_weight_splits_pixels_and_needs_a_workspace(lib):
         assert lib.conv_bwd_weight(h, 4096, 4096, 4096, None) == B.CONV_ERR_WORKSPACE
     finally:
         B.conv_plan_destroy(h)
+
+
+def test_every_plan_description_is_key_value_pairs(lib):
+    """The benchmark and the tests read plan descriptions as space-separated key=value pairs."""
+    for wl in WORKLOADS.values():
+        for layer in wl.layers:
+            args = layer.plan_args(wl.dtype_code)
+            for create in (lambda: B.conv_plan_create(*args), lambda: B.conv_bwd_data_plan_create(*args[:11]),
+                           lambda: B.conv_bwd_weight_plan_create(*args[:11])):
+                h = create()
+                try:
+                    d = B.conv_plan_describe(h)
+                finally:
+                    B.conv_plan_destroy(h)
+                assert all(len(kv.split("=", 1)) == 2 for kv in d.split()), d

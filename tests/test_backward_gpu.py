@@ -115,6 +115,15 @@ CASES = [
     ("3d_s2", "f32", B_(3, 1, 2, 8, 12, (7, 9, 8), (3, 3, 3), (2, 1, 2), (1, 1, 1), (1, 1, 1))),
     ("2d_big_pad", "bf16", B_(2, 1, 1, 16, 16, (6, 6), (3, 3), (1, 1), (3, 3), (1, 1))),
     ("1d_1x1_s2", "f32", B_(1, 2, 2, 12, 20, (33,), (1,), (2,), (0,), (1,))),
+    # stride phases on the tensor cores: outputs on a lattice of dx
+    ("1d_s2_c128", "bf16", B_(1, 2, 1, 128, 128, (1001,), (3,), (2,), (1,), (1,))),
+    ("2d_s2_3x3_c64", "bf16", B_(2, 2, 1, 64, 64, (29, 31), (3, 3), (2, 2), (1, 1), (1, 1))),
+    ("2d_1x1_s2_zero_fill", "bf16", B_(2, 1, 2, 64, 64, (15, 14), (1, 1), (2, 2), (0, 0), (1, 1))),
+    ("3d_s2_c64", "bf16", B_(3, 1, 1, 64, 64, (7, 9, 10), (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1))),
+    ("1d_s2_tf32", "f32", B_(1, 1, 1, 64, 96, (777,), (3,), (2,), (1,), (1,))),
+    ("2d_s2_dil2_pad3", "bf16", B_(2, 1, 2, 32, 48, (21, 19), (3, 3), (2, 2), (3, 3), (2, 2))),
+    ("1d_s3_k5", "bf16", B_(1, 1, 1, 64, 64, (500,), (5,), (3,), (2,), (1,))),
+    ("2d_s2_groups_c8", "bf16", B_(2, 1, 16, 8, 8, (20, 22), (3, 3), (2, 2), (1, 1), (1, 1))),
 ]
 
 
@@ -197,4 +206,17 @@ def test_backward_weight_variants(name, env):
     else:
         assert "operands=mn-major" in desc and f"tile=128x{env['CONV_FORCE_BN']}" in desc, desc
     ref, S = oracle.conv_bwd_weight(geom_of(layer), syn.as_f32(x, dtype), syn.as_f32(dy, dtype))
+    assert_within(dtype, CONV_EPI_NONE, got, ref.reshape(-1), S.reshape(-1), f"{name} [{desc}]")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3])
+@pytest.mark.parametrize("name", ["1d_s2_c128", "2d_s2_3x3_c64", "1d_s2_tf32"])
+def test_backward_data_phases_with_split_reductions(name, splits):
+    """Stride phases with whole reductions, cluster-summed splits (2) and the reduction kernel (3),
+    whose outputs land on the lattice too."""
+    dtype, layer = {c[0]: (c[1], c[2]) for c in CASES}[name]
+    x, w, dy = make_bwd_inputs(layer, dtype, 7700 + splits)
+    got, desc = run_bwd_data(layer, dtype, dy, w, env={"CONV_FORCE_SPLITK": splits})
+    assert "bwd_data(phases)" in desc, desc
+    ref, S = oracle.conv_bwd_data(geom_of(layer), syn.as_f32(dy, dtype), syn.as_f32(w, dtype))
     assert_within(dtype, CONV_EPI_NONE, got, ref.reshape(-1), S.reshape(-1), f"{name} [{desc}]")
