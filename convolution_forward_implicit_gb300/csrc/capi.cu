@@ -323,7 +323,7 @@ struct conv_plan {
     int nph;
     int ph_zero;            // some input pixels receive no tap at all: dx is cleared first
     int wg_kt, wg_jt, wg_mps;   // backward weight (FFMA): tiles along K and taps*C, pixels per split
-    int wg_rt, wg_nt, wg_q, wg_qps, wg_nwb, wg_cbh;   // backward weight (tensor cores), see WgradTcParams
+    int wg_rt, wg_nt, wg_q, wg_qps, wg_nwb, wg_cbh, wg_pack;   // backward weight (tensor cores), see WgradTcParams
     char desc[320];
 };
 
@@ -1049,20 +1049,25 @@ static bool plan_wg_tc(conv_plan* p) {
     // every box starts at channel g*C + 64*b (x) or g*K + 64*j (dy): a multiple of 8 elements,
     // the 16-byte alignment a tiled TMA copy needs of its innermost coordinate
     if (f.C % 8 != 0 || f.K % 8 != 0 || f.sw > 4) return false;
-    p->wg_cbh = (int)cdiv(f.C, 64);
+    // groups narrower than half a box: `pack` groups share each box (block-diagonal products)
+    p->wg_pack = 1;
+    if (f.G > 1 && f.C <= 32 && 64 % f.C == 0 && f.K <= 64 && 64 % f.K == 0 && p->ch.no_pack == 0)
+        p->wg_pack = std::min(64 / f.C, 64 / f.K);
+    p->wg_cbh = p->wg_pack > 1 ? 1 : (int)cdiv(f.C, 64);
     const int halves = f.taps * p->wg_cbh;
     p->wg_rt = (int)cdiv(halves, 2);
     int bn = 256;
     for (int c : {256, 128, 64})   // the fewest padded columns, the wider tile on a tie
         if (cdiv(f.K, c) * c < cdiv(f.K, bn) * bn) bn = c;
-    if (p->ch.bn == 64 || p->ch.bn == 128 || p->ch.bn == 256) bn = p->ch.bn;
+    if (p->wg_pack > 1) bn = 64;
+    else if (p->ch.bn == 64 || p->ch.bn == 128 || p->ch.bn == 256) bn = p->ch.bn;
     p->BN = bn;
-    p->wg_nt = (int)cdiv(f.K, bn);
+    p->wg_nt = p->wg_pack > 1 ? 1 : (int)cdiv(f.K, bn);
     p->wg_nwb = (int)cdiv(f.Wo, 64);
     const int64_t Q = (int64_t)f.N * f.Do * f.Ho * p->wg_nwb;
     if (Q >= ((int64_t)1 << 31)) return false;
     p->wg_q = (int)Q;
-    const int64_t base = (int64_t)f.G * p->wg_rt * p->wg_nt;
+    const int64_t base = cdiv(f.G, p->wg_pack) * p->wg_rt * p->wg_nt;
     if (base >= ((int64_t)1 << 31)) return false;
     int splits = (int)std::max<int64_t>(1, std::min<int64_t>(p->sm_count / base, Q / 2));
     if (p->ch.splits >= 1) splits = (int)std::min<int64_t>(p->ch.splits, Q);
@@ -1084,8 +1089,8 @@ static bool plan_wg_tc(conv_plan* p) {
     p->workspace_bytes = p->splits > 1 ? (size_t)p->splits * f.G * f.K * f.taps * f.C * sizeof(float) : 0;
     snprintf(p->desc, sizeof(p->desc),
              "variant=tc_bf16 direction=bwd_weight operands=mn-major tile=128x%d row_tiles=%d chunk=64px splits=%d "
-             "chunks_per_split=%d units=%d",
-             bn, p->wg_rt, p->splits, p->wg_qps, p->total_units);
+             "chunks_per_split=%d units=%d pack=%d",
+             bn, p->wg_rt, p->splits, p->wg_qps, p->total_units, p->wg_pack);
     return true;
 }
 
@@ -1459,6 +1464,7 @@ conv_status conv_bwd_weight(conv_plan_t plan, const void* x, const void* dy, voi
         tp.BN = plan->BN; tp.RT = plan->wg_rt; tp.NT = plan->wg_nt;
         tp.splits = plan->splits; tp.Q = plan->wg_q; tp.qps = plan->wg_qps; tp.nwb = plan->wg_nwb;
         tp.cbh = plan->wg_cbh; tp.halves = f.taps * plan->wg_cbh; tp.total_units = plan->total_units;
+        tp.pack = plan->wg_pack;
         tp.pdl = plan->overlap;
         if (launch_wgrad_tc(tp, &xm, &dym, s) != cudaSuccess) return CONV_ERR_CUDA;
         if (plan->splits > 1)

@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     const int split = r % p.splits;
     r /= p.splits;
     const int nt = r % p.NT;
-    const int gi = r / p.NT;
+    const int gi = r / p.NT;        // group (pack > 1: group pack)
+    const int cbase = gi * p.pack * g.C, kbase = gi * p.pack * g.K;
     const int q0 = split * p.qps;
     const int q1 = min(q0 + p.qps, p.Q);
     const int nchunks = q1 - q0;
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
                 const int h = 2 * rt + hh;
                 hv[hh] = h < p.halves;
                 const int tap = hv[hh] ? h / p.cbh : 0;
-                cin[hh] = gi * g.C + (hv[hh] ? (h - tap * p.cbh) * 64 : 0);
+                cin[hh] = cbase + (hv[hh] ? (h - tap * p.cbh) * 64 : 0);
                 const int z = tap / (g.Y * g.X), rem = tap - z * g.Y * g.X;
                 const int y = rem / g.X, x = rem - y * g.X;
                 dz[hh] = z * g.dd - g.pd;
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
                             tma_load_5d(dst + hh * HALF_BYTES, &xmap, cin[hh], cp.ow0 * g.sw + dxo[hh],
                                         cp.oh * g.sh + dyo[hh], cp.od * g.sd + dz[hh], cp.n, full_bar(s));
                     for (int j = 0; j < BN / 64; ++j)
-                        tma_load_5d(dst + W::A_CHUNK + j * HALF_BYTES, &dymap, gi * g.K + nt * BN + j * 64, cp.ow0,
+                        tma_load_5d(dst + W::A_CHUNK + j * HALF_BYTES, &dymap, kbase + nt * BN + j * 64, cp.ow0,
                                     cp.oh, cp.od, cp.n, full_bar(s));
                 }
             }
@@ -194,8 +195,12 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         const int row = wq * 32 + lane;
         const int h = 2 * rt + (row >> 6);
         const int tap = h / p.cbh;
-        const int c = (h - tap * p.cbh) * 64 + (row & 63);
-        const bool row_ok = h < p.halves && c < g.C;
+        // packed groups: row (row & 63) is channel c of group a of the pack, and only the
+        // columns of the same group (a*K .. a*K + K-1) belong to it
+        const int a = p.pack > 1 ? (row & 63) / g.C : 0;
+        const int c = p.pack > 1 ? (row & 63) - a * g.C : (h - tap * p.cbh) * 64 + (row & 63);
+        const int grp = gi * p.pack + a;
+        const bool row_ok = h < p.halves && c < g.C && a < p.pack && grp < g.G;
         const bool ok = wait_bar_warp(done_bar, 0, abort_flag, p.err, true);
         if (ok) {
             tc_fence_after();
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
             const long long col0 = (long long)tap * g.C + c;
             const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16);
             for (int cb = 0; cb < BN; cb += 16) {
-                if (nt * BN + cb >= g.K) break;   // warp-uniform
+                if (nt * BN + cb >= p.pack * g.K) break;   // warp-uniform
                 uint32_t v[16];
                 __syncwarp();
                 tmem_ld16(taddr + (uint32_t)cb, v);
@@ -211,9 +216,15 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
                 if (!row_ok) continue;
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const int k = nt * BN + cb + e;
-                    if (k >= g.K) break;
-                    const long long o = ((long long)gi * g.K + k) * NJ + col0;
+                    int k = nt * BN + cb + e;
+                    if (p.pack > 1) {   // column -> (group of the pack, channel); keep the diagonal block
+                        const int b = k / g.K;
+                        if (b != a) continue;
+                        k -= b * g.K;
+                    } else if (k >= g.K) {
+                        break;
+                    }
+                    const long long o = ((long long)grp * g.K + k) * NJ + col0;
                     const float f = __uint_as_float(v[e]);
                     if (p.splits > 1)
                         p.ws[(long long)split * g.G * g.K * NJ + o] = f;

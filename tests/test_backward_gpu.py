@@ -204,7 +204,8 @@ def test_backward_weight_variants(name, env):
     if "CONV_FORCE_SIMT" in env:
         assert desc.startswith("variant=simt"), desc
     else:
-        assert "operands=mn-major" in desc and f"tile=128x{env['CONV_FORCE_BN']}" in desc, desc
+        packed = "pack=1" not in desc          # packed small groups always use 64-wide tiles
+        assert "operands=mn-major" in desc and f"tile=128x{64 if packed else env['CONV_FORCE_BN']}" in desc, desc
     ref, S = oracle.conv_bwd_weight(geom_of(layer), syn.as_f32(x, dtype), syn.as_f32(dy, dtype))
     assert_within(dtype, CONV_EPI_NONE, got, ref.reshape(-1), S.reshape(-1), f"{name} [{desc}]")
 
@@ -220,3 +221,24 @@ def test_backward_data_phases_with_split_reductions(name, splits):
     assert "bwd_data(phases)" in desc, desc
     ref, S = oracle.conv_bwd_data(geom_of(layer), syn.as_f32(dy, dtype), syn.as_f32(w, dtype))
     assert_within(dtype, CONV_EPI_NONE, got, ref.reshape(-1), S.reshape(-1), f"{name} [{desc}]")
+
+
+PACKED = [
+    ("g32_c8_k8", B_(2, 2, 32, 8, 8, (17, 15), (3, 3), (1, 1), (1, 1), (1, 1))),
+    ("g16_c8_k16", B_(2, 1, 16, 8, 16, (13, 20), (3, 3), (1, 1), (1, 1), (1, 1))),
+    ("g8_c16_k8_s2", B_(2, 1, 8, 16, 8, (19, 23), (3, 3), (2, 2), (1, 1), (1, 1))),
+    ("g6_c16_k16_ragged_pack", B_(1, 2, 6, 16, 16, (200,), (3,), (1,), (1,), (1,))),
+    ("g12_c32_k32_3d", B_(3, 1, 12, 32, 32, (4, 7, 9), (3, 3, 3), (1, 1, 1), (1, 1, 1), (2, 1, 1))),
+]
+
+
+@pytest.mark.parametrize("no_pack", [0, 1])
+@pytest.mark.parametrize("name,layer", PACKED, ids=[c[0] for c in PACKED])
+def test_backward_weight_packed_small_groups(name, layer, no_pack):
+    """Groups narrower than half a 64-channel box share one tile (only the diagonal blocks are
+    stored), including a last pack with fewer groups; CONV_NO_PACK=1 runs them one per tile."""
+    x, w, dy = make_bwd_inputs(layer, "bf16", 8800 + len(name))
+    got, desc = run_bwd_weight(layer, "bf16", x, dy, env={"CONV_NO_PACK": no_pack} if no_pack else None)
+    assert ("pack=1" in desc) == bool(no_pack), desc
+    ref, S = oracle.conv_bwd_weight(geom_of(layer), syn.as_f32(x, "bf16"), syn.as_f32(dy, "bf16"))
+    assert_within("bf16", CONV_EPI_NONE, got, ref.reshape(-1), S.reshape(-1), f"{name} [{desc}]")
