@@ -472,11 +472,15 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                     m = p.lat.on ? out_pixel_linear(p, ml) : ml;
                 }
                 const uint32_t off = (uint32_t)(rr * RED_PITCH + col) * 4u;
-                float4 a = ld_cluster_f4(cluster_map(red0 + off, 0));
-                for (int j = 1; j < S; ++j) {
-                    const float4 b = ld_cluster_f4(cluster_map(red0 + off, (uint32_t)j));
-                    a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-                }
+                // all S partials requested before the first add, so their latencies overlap
+                float4 pv[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < S) pv[j] = ld_cluster_f4(cluster_map(red0 + off, (uint32_t)j));
+                float4 a = pv[0];
+#pragma unroll
+                for (int j = 1; j < 8; ++j)
+                    if (j < S) { a.x += pv[j].x; a.y += pv[j].y; a.z += pv[j].z; a.w += pv[j].w; }
                 float v[4] = {a.x, a.y, a.z, a.w};
                 const size_t o = (size_t)m * GK + (size_t)gi * g.K + n;
 #pragma unroll
