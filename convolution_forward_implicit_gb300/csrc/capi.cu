@@ -322,7 +322,7 @@ struct conv_plan {
     size_t ph_off[MAX_PHASES];   // each phase's packed weight within w_packed
     int nph;
     int ph_zero;            // some input pixels receive no tap at all: dx is cleared first
-    int wg_kt, wg_jt, wg_mps;   // backward weight (FFMA): tiles along K and taps*C, pixels per split
+    int wg_kt, wg_jt, wg_mps, wg_tile;   // backward weight (FFMA): tiles along K and taps*C, pixels per split, tile
     int wg_rt, wg_nt, wg_q, wg_qps, wg_nwb, wg_cbh, wg_pack;   // backward weight (tensor cores), see WgradTcParams
     char desc[320];
 };
@@ -1094,24 +1094,28 @@ static bool plan_wg_tc(conv_plan* p) {
     return true;
 }
 
-// Backward weight on the FFMA pipe: 64 x 64 tiles of [K] x [taps*C] per group, the output
-// pixels split across CTAs until the grid covers the SMs twice (at least 64 pixels each).
+// Backward weight on the FFMA pipe: 64 x 64 or 128 x 128 tiles of [K] x [taps*C] per group, the output
+// pixels split across CTAs until the grid covers the SMs twice (at least one tile width of pixels each).
 static void plan_wg_simt(conv_plan* p) {
     const Geom& f = p->fg;
     p->variant = VAR_WG_SIMT;
-    p->wg_kt = (int)cdiv(f.K, 64);
-    p->wg_jt = (int)cdiv((int64_t)f.taps * f.C, 64);
+    // 128 x 128 tiles (8 x 8 per thread) where both extents fill them, else 64 x 64
+    p->wg_tile = (f.K >= 96 && (int64_t)f.taps * f.C >= 96) ? 128 : 64;
+    p->wg_kt = (int)cdiv(f.K, p->wg_tile);
+    p->wg_jt = (int)cdiv((int64_t)f.taps * f.C, p->wg_tile);
     const int64_t tiles = (int64_t)p->wg_kt * p->wg_jt * f.G;
+    // at least `tile` pixels per split: shorter splits cost more in partial sums than they gain
     int splits = (int)std::max<int64_t>(1, std::min<int64_t>(2 * p->sm_count / std::max<int64_t>(tiles, 1),
-                                                             cdiv(f.M, 64)));
+                                                             cdiv(f.M, p->wg_tile)));
     splits = std::min(splits, 64);
     p->wg_mps = (int)(cdiv(cdiv(f.M, splits), 8) * 8);
     p->splits = (int)cdiv(f.M, p->wg_mps);
     p->prepack_bytes = p->packed_bytes = 0;
     p->workspace_bytes = p->splits > 1 ? (size_t)p->splits * f.G * f.K * f.taps * f.C * sizeof(float) : 0;
     snprintf(p->desc, sizeof(p->desc),
-             "variant=simt_%s direction=bwd_weight tile=64x64 pixel_step=8 splits=%d pixels_per_split=%d grid=%dx%dx%d",
-             p->dtype == CONV_BF16 ? "bf16" : "f32", p->splits, p->wg_mps, p->wg_kt, p->wg_jt, f.G * p->splits);
+             "variant=simt_%s direction=bwd_weight tile=%dx%d pixel_step=8 splits=%d pixels_per_split=%d grid=%dx%dx%d",
+             p->dtype == CONV_BF16 ? "bf16" : "f32", p->wg_tile, p->wg_tile, p->splits, p->wg_mps, p->wg_kt, p->wg_jt,
+             f.G * p->splits);
 }
 
 extern "C" {
@@ -1475,6 +1479,7 @@ conv_status conv_bwd_weight(conv_plan_t plan, const void* x, const void* dy, voi
     WgradParams wp;
     wp.g = f;
     wp.x = x; wp.dy = dy; wp.dw = dw; wp.ws = ws;
+    wp.tile = plan->wg_tile;
     wp.num_kt = plan->wg_kt; wp.num_jt = plan->wg_jt; wp.splits = plan->splits; wp.mps = plan->wg_mps;
     wp.pdl = plan->overlap;
     if (launch_wgrad_simt(wp, plan->dtype == CONV_BF16, s) != cudaSuccess) return CONV_ERR_CUDA;

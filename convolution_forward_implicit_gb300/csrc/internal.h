@@ -197,6 +197,7 @@ struct WgradParams {
     const void* dy;         // T  N Do Ho Wo G K
     void* dw;               // T  G K taps C (splits == 1)
     float* ws;              // partials (splits > 1)
+    int tile;               // 64 (64 x 64 tiles) or 128 (128 x 128)
     int num_kt, num_jt;     // tiles along K and along taps*C
     int splits, mps;        // pixel splits, pixels per split
     int pdl;
