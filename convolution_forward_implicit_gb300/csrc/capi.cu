@@ -1359,7 +1359,10 @@ static conv_status run_forward(conv_plan_t plan, const void* x, const void* w_pa
         tp.pdl = plan->overlap;
         tp.epi_warps = plan->epi_warps ? plan->epi_warps : 8;
         tp.cluster_red = plan->cluster_red;
-        tp.lat = plan->lat;
+        // outputs land on the plan's lattice only where the kernel writes final values; partial
+        // sums (split-K through the reduction kernel) are indexed by GEMM row
+        const bool partial = plan->splits > 1 && !plan->cluster_red;
+        tp.lat = (plan->lat.on && !partial) ? plan->lat : identity_lattice(plan->g.Do, plan->g.Ho, plan->g.Wo);
         tp.f_splits = make_fastdiv(plan->splits); tp.f_num_nt = make_fastdiv(plan->num_nt);
         tp.f_G = make_fastdiv(plan->g.G); tp.f_tiles_w = make_fastdiv(plan->tiles_w);
         tp.f_tiles_h = make_fastdiv(plan->tiles_h); tp.f_Do = make_fastdiv(plan->g.Do);

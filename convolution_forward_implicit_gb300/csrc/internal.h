@@ -99,9 +99,20 @@ struct Lattice {
     int rd, rh, rw;
 };
 
-__host__ __device__ __forceinline__ long long lattice_pixel(const Lattice& L, int n, int od, int oh, int ow) {
-    return (((long long)n * L.D + L.rd + (long long)L.sd * od) * L.H + L.rh + (long long)L.sh * oh) * L.W + L.rw +
-           (long long)L.sw * ow;
+// The identity placement of a problem whose output extents are Do x Ho x Wo (on = 0: the
+// kernels may still evaluate lattice_pixel with it, which gives the plain NDHW row).
+inline Lattice identity_lattice(int Do, int Ho, int Wo) {
+    Lattice L;
+    L.on = 0;
+    L.D = Do; L.H = Ho; L.W = Wo;
+    L.sd = L.sh = L.sw = 1;
+    L.rd = L.rh = L.rw = 0;
+    return L;
+}
+
+// (pixel indices of every tensor the plans accept stay below 2^31, so 32-bit arithmetic)
+__host__ __device__ __forceinline__ int lattice_pixel(const Lattice& L, int n, int od, int oh, int ow) {
+    return ((n * L.D + L.rd + L.sd * od) * L.H + L.rh + L.sh * oh) * L.W + L.rw + L.sw * ow;
 }
 
 // ---- tensor-core (tcgen05) bf16 implicit GEMM ----

@@ -245,7 +245,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 }
 
 // Place in y of GEMM row m (pixels in N Do Ho Wo order) of a lattice-output problem.
-__device__ __forceinline__ long long out_pixel_linear(const TcParams& p, int m) {
+__device__ __forceinline__ int out_pixel_linear(const TcParams& p, int m) {
     const int q1 = fdiv(m, p.f_Wo);
     const int ow = m - q1 * p.g.Wo;
     const int q2 = fdiv(q1, p.f_Ho);

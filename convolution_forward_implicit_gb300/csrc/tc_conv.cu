@@ -380,19 +380,18 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
             TileOrigin to{0, 0, 0, 0};
             if (T::TMA) to = tile_origin(p, mt);
             // element offset of accumulator row rr's pixel, or -1 if the row is outside the output
-            // (partial sums are indexed by the GEMM row; final outputs by their place in y)
+            // (p.lat is the identity placement unless final outputs land on a lattice of y; the
+            // host passes the identity to kernels that write partial sums)
             auto row_offset = [&](int rr) -> long long {
                 if (T::TMA) {
                     const int rh = fdiv(rr, p.f_BW);
                     const int oh = to.oh0 + rh, ow = to.ow0 + (rr - rh * p.BW);
                     if (rr >= p.BW * p.BH || oh >= g.Ho || ow >= g.Wo) return -1;
-                    if (p.lat.on && !partial) return lattice_pixel(p.lat, to.n, to.od, oh, ow) * GK;
-                    return (long long)(((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow) * GK;
+                    return (long long)lattice_pixel(p.lat, to.n, to.od, oh, ow) * GK;
                 }
                 const int m = mt * BM + rr;
                 if (m >= g.M) return -1;
-                if (p.lat.on && !partial) return out_pixel_linear(p, m) * GK;
-                return (long long)m * GK;
+                return (p.lat.on ? out_pixel_linear(p, m) : (long long)m) * GK;
             };
             if (p.cluster_red) {
                 // one unit per CTA: its partial accumulator goes to this CTA's shared memory
@@ -464,8 +463,7 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                     const int rh = fdiv(rr, p.f_BW);
                     const int oh = to.oh0 + rh, ow = to.ow0 + (rr - rh * p.BW);
                     if (rr >= p.BW * p.BH || oh >= g.Ho || ow >= g.Wo) continue;
-                    m = p.lat.on ? lattice_pixel(p.lat, to.n, to.od, oh, ow)
-                                 : (long long)(((to.n * g.Do + to.od) * g.Ho + oh) * g.Wo + ow);
+                    m = lattice_pixel(p.lat, to.n, to.od, oh, ow);
                 } else {
                     const int ml = mt * BM + rr;
                     if (ml >= g.M) continue;
