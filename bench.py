@@ -511,6 +511,7 @@ def run_ours(args, ws, rank, local):
                    "selector": (f"measured (conv_plan_tune, {args.tune} timed calls per candidate)" if args.tune
                                 else "rules"),
                    "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "kernel_sources": kernel_source_hash(),
                    "plans": {lr.name(): lr.plan.describe() for lr in runs}},
         "roofline": roof,
         "e2e": e2e,
