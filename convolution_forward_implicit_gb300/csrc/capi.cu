@@ -322,6 +322,8 @@ struct conv_plan {
     size_t ph_off[MAX_PHASES];   // each phase's packed weight within w_packed
     int nph;
     int ph_zero;            // some input pixels receive no tap at all: dx is cleared first
+    int test_stall;         // CONV_TEST_STALL: the tensor-core kernel's MMA role waits until its bounded
+                            // wait expires (exercises the timeout path; tests only)
     int wg_kt, wg_jt, wg_mps, wg_tile;   // backward weight (FFMA): tiles along K and taps*C, pixels per split, tile
     int wg_rt, wg_nt, wg_q, wg_qps, wg_nwb, wg_cbh, wg_pack;   // backward weight (tensor cores), see WgradTcParams
     char desc[320];
@@ -1130,6 +1132,7 @@ conv_status conv_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, i
     if (st != CONV_OK) return st;
     p->epi = epilogue;
     p->dir = DIR_FWD;
+    p->test_stall = env_int("CONV_TEST_STALL", 0) ? 1 : 0;
     // choices: the test hooks if set, else the measured selector's entry for this problem on
     // this device, else the rules
     PlanChoice c;
@@ -1363,6 +1366,7 @@ static conv_status run_forward(conv_plan_t plan, const void* x, const void* w_pa
         // sums (split-K through the reduction kernel) are indexed by GEMM row
         const bool partial = plan->splits > 1 && !plan->cluster_red;
         tp.lat = (plan->lat.on && !partial) ? plan->lat : identity_lattice(plan->g.Do, plan->g.Ho, plan->g.Wo);
+        tp.test_stall = plan->test_stall;
         tp.f_splits = make_fastdiv(plan->splits); tp.f_num_nt = make_fastdiv(plan->num_nt);
         tp.f_G = make_fastdiv(plan->g.G); tp.f_tiles_w = make_fastdiv(plan->tiles_w);
         tp.f_tiles_h = make_fastdiv(plan->tiles_h); tp.f_Do = make_fastdiv(plan->g.Do);

@@ -160,6 +160,7 @@ struct TcParams {
     int cluster_red;        // 1: the splits of a tile run as one cluster and sum their partial
                             // accumulators through distributed shared memory (no workspace)
     Lattice lat;            // where the output pixels land in y (one phase of a strided backward data)
+    int test_stall;         // test hook: the MMA role waits on a barrier nothing completes
     // divisors of the per-tile index arithmetic
     FastDiv f_splits, f_num_nt, f_G, f_tiles_w, f_tiles_h, f_Do, f_Ho, f_Wo, f_cbt, f_cpt, f_X, f_YX, f_BW, f_bws;
 };

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
             if (lane < 2) {
                 const uint32_t a_tx = (uint32_t)(p.BW * p.BH) * 128u;
                 const int cblk = T::TF32 ? 32 : 64;     // channels in one 128-byte row
-                uint32_t it = 0;
+                uint32_t it = 0, issued = 0;   // issued: 1 + the last iteration this warp loaded
                 bool aborted = false;
                 bool x_ready = !p.pdl;      // x may come from the previous kernel on the stream
                 for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                         ok = __shfl_sync(0x3u, ok, 0);
                         if (!ok) { aborted = true; break; }
                         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), a_tx + C::B_STAGE);
+                        issued = it + 1;
                         __syncwarp(0x3u);
                         if (lane == 0) {
                             if (!x_ready) {
@@ -183,6 +184,16 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                             bulk_g2s(sB + s * C::B_STAGE, wp + off, C::B_STAGE, full_bar(s));
                         }
                     }
+                }
+                if (aborted && lane == 0) {
+                    // before the CTA exits, the copies this warp issued into stages the MMA role never
+                    // consumed must have landed: a bounded wait on each of its last ring pass's stages
+                    const unsigned long long t0 = globaltimer();
+                    for (uint32_t k = issued > (uint32_t)STAGES ? issued - STAGES : 0u; k < issued; ++k)
+                        if ((int)((k % STAGES) % T::PROD_WARPS) == pw)
+                            while (!mbar_try_wait(full_bar(k % STAGES), (k / STAGES) & 1u) &&
+                                   globaltimer() - t0 < WAIT_LIMIT_NS) {
+                            }
                 }
             }
             __syncwarp();
@@ -271,6 +282,9 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
             constexpr uint32_t IDESC = idesc_f32acc(BM, BN, T::TF32 ? 2u : 1u);
             uint32_t it = 0, tile_i = 0;
             bool aborted = false;
+            // test hook: wait on a barrier nothing completes, so the bounded wait runs out and
+            // the abort path (error word, drained copies, freed tensor memory) is exercised
+            if (p.test_stall && !wait_bar(drain_bar, 0u, abort_flag, p.err, false)) aborted = true;
             for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x, ++tile_i) {
                 int mt, gi, nt, split;
                 decode_unit(p, u, mt, gi, nt, split);
