@@ -482,6 +482,32 @@ def run_ours(args, ws, rank, local):
     ms_per_step = total_ms / K
     value = ws * step_flops / (ms_per_step * 1e-3) / 1e12
 
+    # ---- hot L2 (the same rotation set every step) and the latency of one isolated step
+    for i in range(args.warmup):
+        step_graphs[0].replay()
+    torch.cuda.synchronize()
+    eh0, eh1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    eh0.record(stream)
+    for i in range(K):
+        step_graphs[0].replay()
+    eh1.record(stream)
+    torch.cuda.synchronize()
+    hot_ms = eh0.elapsed_time(eh1) / K
+    singles = []
+    for i in range(20):
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        step(i)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        singles.append(a0.elapsed_time(a1) * 1e3)
+    hot = {"ms_per_step": round(hot_ms, 6), "value": round(ws * step_flops / (hot_ms * 1e-3) / 1e12, 4),
+           "unit": "TFLOP/s", "note": "one rotation set replayed every step: inputs that fit stay in L2"}
+    single = {"median_us": round(float(np.median(singles)), 3), "p10_us": round(float(np.percentile(singles, 10)), 3),
+              "p90_us": round(float(np.percentile(singles, 90)), 3), "samples": len(singles),
+              "note": "one step between a device synchronize and events: launch latency included"}
+
     # ---- end to end: pinned host inputs in, final outputs back to pinned host memory
     e2e = run_e2e(args, runs, host_in, out_sets, R, stream, ws, local, step)
 
@@ -514,6 +540,8 @@ def run_ours(args, ws, rank, local):
                    "kernel_sources": kernel_source_hash(),
                    "plans": {lr.name(): lr.plan.describe() for lr in runs}},
         "roofline": roof,
+        "hot_l2": hot,
+        "single_step": single,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk,
