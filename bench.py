@@ -18,10 +18,13 @@ rotate over enough copies of every input, packed weight and output that one rota
 exceeds twice the L2 cache, so no step finds its data in L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
-                  [--no-overlap] [--tune ITERS] [--source-hash]
+                  [--no-overlap] [--serial] [--pass fwd|bwd] [--tune ITERS] [--source-hash]
 
 --tune ITERS lets the measured selector (conv_plan_tune) time every candidate plan of each
-layer before the run and keep the fastest; by default the planner's rules choose.
+layer before the run and keep the fastest; by default the planner's rules choose.  The step's
+independent chains (e.g. the fp32 and the bf16 frontend) run one after the other in the
+forward pass and as parallel branches of the step graph, each on its own stream, in the
+backward pass (--serial / --parallel override).
 
 Under torchrun each rank runs an independent replica on its own GPU (the forward pass
 has no exchange step); rank 0 prints the JSON line with the max time over ranks.
@@ -347,11 +350,13 @@ def rotation_sets(wls, factor=1.0):
     return max(4, int(np.ceil(2.2 * L2_BYTES / per_set))), per_set
 
 
-def capture_steps(runs, R, with_events):
+def capture_steps(runs, R, with_events, parallel=False):
     """One CUDA graph per rotation set holding every layer of the step.  With with_events,
     timing events are recorded between the layers inside the graph (they give each layer's
     device time, and they also keep consecutive layers from overlapping); returns (graphs,
-    events), or None when this PyTorch cannot record events inside a graph."""
+    events), or None when this PyTorch cannot record events inside a graph.  With parallel,
+    the step's independent chains (the layers of each workload) are captured as parallel
+    branches on their own streams, joined at the end of the step."""
     import torch
     events = None
     if with_events:
@@ -368,17 +373,34 @@ def capture_steps(runs, R, with_events):
                 lr.call(r)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
+    # the independent chains of the step (one per workload) as parallel branches of the graph
+    chains = {}
+    for lr in runs:
+        chains.setdefault(lr.wl.name, []).append(lr)
+    chains = list(chains.values())
+    branch = parallel and not events and len(chains) > 1
+    side = [torch.cuda.Stream() for _ in range(len(chains) - 1)] if branch else []
     graphs = []
     for r in range(R):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             cs = torch.cuda.current_stream()
-            if events:
-                events[r][0].record(cs)
-            for j, lr in enumerate(runs):
-                lr.call(r)
+            if branch:
+                for ss in side:
+                    ss.wait_stream(cs)
+                for ci, chain in enumerate(chains):
+                    with torch.cuda.stream(cs if ci == 0 else side[ci - 1]):
+                        for lr in chain:
+                            lr.call(r)
+                for ss in side:
+                    cs.wait_stream(ss)
+            else:
                 if events:
-                    events[r][j + 1].record(cs)
+                    events[r][0].record(cs)
+                for j, lr in enumerate(runs):
+                    lr.call(r)
+                    if events:
+                        events[r][j + 1].record(cs)
         graphs.append(g)
     return graphs, events
 
@@ -405,12 +427,13 @@ def run_ours(args, ws, rank, local):
         for lr in runs:
             lr.plan.set_overlap(True)
     # timed steps: one graph per step with no events inside, so consecutive kernels may overlap
-    step_graphs, _ = capture_steps(runs, R, with_events=False)
+    step_graphs, _ = capture_steps(runs, R, with_events=False, parallel=args.parallel)
     # per-layer device times: the same steps with events between the layers
     cap = capture_steps(runs, R, with_events=True)
     if cap is not None:
         layer_graphs, gev = cap
         graph_mode = ("one graph per step (all layers" + (", chained as programmatic dependents" if args.overlap else "")
+                      + ("; independent workloads as parallel branches" if args.parallel and len(wls) > 1 else "")
                       + "); per-layer times from a second run of graphs with events between the layers")
     else:
         for lr in runs:
@@ -834,6 +857,10 @@ def main():
     ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash and exit")
     ap.add_argument("--no-overlap", dest="overlap", action="store_false",
                     help="launch each layer only after the previous one completes (no programmatic dependents)")
+    ap.add_argument("--serial", dest="parallel", action="store_const", const=False, default=None,
+                    help="run the step's independent chains one after the other (the forward default)")
+    ap.add_argument("--parallel", dest="parallel", action="store_const", const=True,
+                    help="capture the step's independent chains as parallel graph branches (the backward default)")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="fwd: the forward pass of every layer; bwd: backward data and backward weight of every layer")
     ap.add_argument("--tune", type=int, default=0, metavar="ITERS",
@@ -845,6 +872,11 @@ def main():
         return
     if args.warmup < 3:
         args.warmup = 3
+    if args.parallel is None:
+        # measured: forward layers each fill every SM, so concurrent chains only contend (the
+        # Whisper step 51.3 -> 54.6 us); the backward step's long FFMA kernels overlap well
+        # (207 -> 189 us)
+        args.parallel = args.pass_ == "bwd"
     ws, rank, local = dist_setup()
     if ws > 1:
         import torch
