@@ -674,7 +674,12 @@ def roofline_for(lr, ms):
     byts = lr.bytes_alg()
     desc = lr.plan.describe()
     hbm = peaks["hbm_gbs"] * 1e9
-    if "variant=tc_bf16" in desc:
+    if "variant=tc_bf16x3" in desc:
+        # fp32 split into three bf16 planes: six bf16 products per useful product
+        pipe = peaks["bf16_tflops"] / 6.0 * 1e12
+        bound_c, unit_peak = "tensor", peaks["bf16_tflops"] / 6.0
+        note = f"bf16 dense tensor peak ({src}) / 6 plane products per useful product"
+    elif "variant=tc_bf16" in desc:
         pipe = peaks["bf16_tflops"] * 1e12
         bound_c, unit_peak = "tensor", peaks["bf16_tflops"]
         note = f"bf16 dense tensor peak, burst, {src}"

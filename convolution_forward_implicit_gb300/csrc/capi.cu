@@ -197,6 +197,22 @@ __global__ void prepack_dg_simt_kernel(const T* __restrict__ w, T* __restrict__ 
     }
 }
 
+// fp32 -> three bf16 planes: hi = bf16(v), mid = bf16(v - hi), lo = bf16(v - hi - mid).  Both
+// differences are exact in fp32 (each has at most 16 significant bits), so hi + mid + lo equals
+// v to within 2^-24 of it.  Plane p of element i at out[p * n + i].
+__global__ void split_planes_kernel(const float* __restrict__ in, __nv_bfloat16* __restrict__ out, long long n) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const float v = __ldg(in + i);
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        const float r1 = v - __bfloat162float(h);
+        const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(m);
+        out[i] = h;
+        out[n + i] = m;
+        out[2 * n + i] = __float2bfloat16_rn(r2);
+    }
+}
+
 // ----------------------------------------------------------------------------- split-K reduction
 // y = epilogue(sum over splits, in split order, of the fp32 partials): a fixed order,
 // so results do not change from run to run.
@@ -326,6 +342,8 @@ struct conv_plan {
                             // wait expires (exercises the timeout path; tests only)
     int wg_kt, wg_jt, wg_mps, wg_tile;   // backward weight (FFMA): tiles along K and taps*C, pixels per split, tile
     int wg_rt, wg_nt, wg_q, wg_qps, wg_nwb, wg_cbh, wg_pack;   // backward weight (tensor cores), see WgradTcParams
+    int wg_planes;                      // 1 (bf16) or 3 (fp32 split into bf16 planes)
+    size_t wg_xpl_off, wg_dypl_off;     // fp32: the x and dy planes within the workspace
     char desc[320];
 };
 
@@ -1023,7 +1041,8 @@ static bool encode_wg_maps(const conv_plan* p, const void* x, const void* dy, CU
     const Geom& g = p->fg;
     cuuint64_t dims[5], strides[4];
     cuuint32_t box[5], es[5];
-    dims[0] = (cuuint64_t)g.G * g.C; dims[1] = g.W; dims[2] = g.H; dims[3] = g.D; dims[4] = g.N;
+    const cuuint64_t images = (cuuint64_t)g.N * (p->wg_planes > 1 ? p->wg_planes : 1);   // plane pl, image n: pl*N + n
+    dims[0] = (cuuint64_t)g.G * g.C; dims[1] = g.W; dims[2] = g.H; dims[3] = g.D; dims[4] = images;
     strides[0] = dims[0] * 2; strides[1] = strides[0] * g.W; strides[2] = strides[1] * g.H; strides[3] = strides[2] * g.D;
     box[0] = 64; box[1] = (cuuint32_t)(64 * g.sw); box[2] = box[3] = box[4] = 1;
     es[0] = 1; es[1] = (cuuint32_t)g.sw; es[2] = es[3] = es[4] = 1;
@@ -1031,7 +1050,7 @@ static bool encode_wg_maps(const conv_plan* p, const void* x, const void* dy, CU
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
-    dims[0] = (cuuint64_t)g.G * g.K; dims[1] = g.Wo; dims[2] = g.Ho; dims[3] = g.Do; dims[4] = g.N;
+    dims[0] = (cuuint64_t)g.G * g.K; dims[1] = g.Wo; dims[2] = g.Ho; dims[3] = g.Do; dims[4] = images;
     strides[0] = dims[0] * 2; strides[1] = strides[0] * g.Wo; strides[2] = strides[1] * g.Ho;
     strides[3] = strides[2] * g.Do;
     box[1] = 64;
@@ -1047,7 +1066,9 @@ static bool encode_wg_maps(const conv_plan* p, const void* x, const void* dy, CU
 // the grid fills the SMs once.  Returns false where the problem does not fit.
 static bool plan_wg_tc(conv_plan* p) {
     const Geom& f = p->fg;
-    if (p->dtype != CONV_BF16 || p->ch.simt) return false;
+    if (p->ch.simt) return false;
+    // fp32: x and dy split into three bf16 planes each (six plane products per tile)
+    p->wg_planes = p->dtype == CONV_F32 ? 3 : 1;
     // every box starts at channel g*C + 64*b (x) or g*K + 64*j (dy): a multiple of 8 elements,
     // the 16-byte alignment a tiled TMA copy needs of its innermost coordinate
     if (f.C % 8 != 0 || f.K % 8 != 0 || f.sw > 4) return false;
@@ -1058,11 +1079,12 @@ static bool plan_wg_tc(conv_plan* p) {
     p->wg_cbh = p->wg_pack > 1 ? 1 : (int)cdiv(f.C, 64);
     const int halves = f.taps * p->wg_cbh;
     p->wg_rt = (int)cdiv(halves, 2);
-    int bn = 256;
+    const int bn_max = p->wg_planes > 1 ? 128 : 256;   // three planes of 256 columns do not fit a stage
+    int bn = bn_max;
     for (int c : {256, 128, 64})   // the fewest padded columns, the wider tile on a tie
-        if (cdiv(f.K, c) * c < cdiv(f.K, bn) * bn) bn = c;
+        if (c <= bn_max && cdiv(f.K, c) * c < cdiv(f.K, bn) * bn) bn = c;
     if (p->wg_pack > 1) bn = 64;
-    else if (p->ch.bn == 64 || p->ch.bn == 128 || p->ch.bn == 256) bn = p->ch.bn;
+    else if ((p->ch.bn == 64 || p->ch.bn == 128 || p->ch.bn == 256) && p->ch.bn <= bn_max) bn = p->ch.bn;
     p->BN = bn;
     p->wg_nt = p->wg_pack > 1 ? 1 : (int)cdiv(f.K, bn);
     p->wg_nwb = (int)cdiv(f.Wo, 64);
@@ -1089,10 +1111,16 @@ static bool plan_wg_tc(conv_plan* p) {
     p->variant = VAR_WG_TC;
     p->prepack_bytes = p->packed_bytes = 0;
     p->workspace_bytes = p->splits > 1 ? (size_t)p->splits * f.G * f.K * f.taps * f.C * sizeof(float) : 0;
+    if (p->wg_planes > 1) {   // the workspace also holds the bf16 planes of x and dy
+        const size_t nx = (size_t)f.N * f.D * f.H * f.W * f.G * f.C, ndy = (size_t)f.M * f.G * f.K;
+        p->wg_xpl_off = align256(p->workspace_bytes);
+        p->wg_dypl_off = align256(p->wg_xpl_off + 3 * nx * 2);
+        p->workspace_bytes = p->wg_dypl_off + 3 * ndy * 2;
+    }
     snprintf(p->desc, sizeof(p->desc),
-             "variant=tc_bf16 direction=bwd_weight operands=mn-major tile=128x%d row_tiles=%d chunk=64px splits=%d "
+             "variant=%s direction=bwd_weight operands=mn-major tile=128x%d row_tiles=%d chunk=64px splits=%d "
              "chunks_per_split=%d units=%d pack=%d",
-             bn, p->wg_rt, p->splits, p->wg_qps, p->total_units, p->wg_pack);
+             p->wg_planes > 1 ? "tc_bf16x3" : "tc_bf16", bn, p->wg_rt, p->splits, p->wg_qps, p->total_units, p->wg_pack);
     return true;
 }
 
@@ -1467,8 +1495,24 @@ conv_status conv_bwd_weight(conv_plan_t plan, const void* x, const void* dy, voi
     if (plan->variant == VAR_WG_TC) {
         unsigned* err = error_word_ptr();
         if (!err) return CONV_ERR_CUDA;
+        const void* xs = x;
+        const void* dys = dy;
+        if (plan->wg_planes > 1) {   // fp32: split x and dy into their bf16 planes first
+            uint8_t* wsb = reinterpret_cast<uint8_t*>(plan->workspace);
+            const long long nx = (long long)f.N * f.D * f.H * f.W * f.G * f.C, ndy = (long long)f.M * f.G * f.K;
+            __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(wsb + plan->wg_xpl_off);
+            __nv_bfloat16* dyp = reinterpret_cast<__nv_bfloat16*>(wsb + plan->wg_dypl_off);
+            const int threads = 256;
+            split_planes_kernel<<<(int)std::min<long long>(cdiv(nx, threads), (long long)plan->sm_count * 8), threads, 0, s>>>(
+                static_cast<const float*>(x), xp, nx);
+            split_planes_kernel<<<(int)std::min<long long>(cdiv(ndy, threads), (long long)plan->sm_count * 8), threads, 0,
+                                  s>>>(static_cast<const float*>(dy), dyp, ndy);
+            if (cudaGetLastError() != cudaSuccess) return CONV_ERR_CUDA;
+            xs = xp;
+            dys = dyp;
+        }
         CUtensorMap xm, dym;
-        if (!encode_wg_maps(plan, x, dy, &xm, &dym)) return CONV_ERR_CUDA;
+        if (!encode_wg_maps(plan, xs, dys, &xm, &dym)) return CONV_ERR_CUDA;
         WgradTcParams tp;
         tp.g = f;
         tp.dw = dw; tp.ws = ws; tp.err = err;
@@ -1476,6 +1520,7 @@ conv_status conv_bwd_weight(conv_plan_t plan, const void* x, const void* dy, voi
         tp.splits = plan->splits; tp.Q = plan->wg_q; tp.qps = plan->wg_qps; tp.nwb = plan->wg_nwb;
         tp.cbh = plan->wg_cbh; tp.halves = f.taps * plan->wg_cbh; tp.total_units = plan->total_units;
         tp.pack = plan->wg_pack;
+        tp.planes = plan->wg_planes;
         tp.pdl = plan->overlap;
         if (launch_wgrad_tc(tp, &xm, &dym, s) != cudaSuccess) return CONV_ERR_CUDA;
         if (plan->splits > 1)

@@ -229,6 +229,8 @@ struct WgradTcParams {
     int splits, Q, qps;     // pixel splits, 64-pixel chunks in all, chunks per split
     int nwb;                // 64-pixel blocks per output row
     int cbh, halves;        // 64-channel blocks per tap, taps * cbh
+    int planes;             // 1: bf16 x and dy; 3: fp32 split into hi, mid, lo bf16 planes (images
+                            // pl*N + n of the plane tensors), dw in fp32
     int pack;               // groups per tile (C, K dividing 64): x rows and dy columns of `pack`
                             // consecutive groups share one box; only the diagonal blocks are kept
     int total_units;

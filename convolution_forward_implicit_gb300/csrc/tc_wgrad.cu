@@ -31,10 +31,17 @@ namespace {
 constexpr int WG_THREADS = 192;
 constexpr uint32_t HALF_BYTES = 64 * 128;   // one box: 64 pixels x 64 channels of bf16
 
-template <int BN, int CH>
+// PL: bf16 planes per operand.  1 for bf16 I/O; 3 for fp32 I/O, whose x and dy arrive split
+// into hi + mid + lo bf16 planes (each the bf16 rounding of what the planes before it leave, so
+// the three sum to the fp32 value within 2^-24 of it); the tile then accumulates the six
+// products hi*hi, hi*mid, mid*hi, hi*lo, lo*hi, mid*mid (the dropped ones are below 2^-22 of
+// |x dy|), in fp32, and dw is stored in fp32.
+template <int BN, int CH, int PL>
 struct WgCfg {
-    static constexpr uint32_t A_CHUNK = 2 * HALF_BYTES;             // two channel halves
-    static constexpr uint32_t B_CHUNK = (BN / 64) * HALF_BYTES;     // BN/64 channel blocks of dy
+    static constexpr uint32_t A_PLANE = 2 * HALF_BYTES;             // two channel halves
+    static constexpr uint32_t B_PLANE = (BN / 64) * HALF_BYTES;     // BN/64 channel blocks of dy
+    static constexpr uint32_t A_CHUNK = PL * A_PLANE;
+    static constexpr uint32_t B_CHUNK = PL * B_PLANE;
     static constexpr uint32_t CHUNK = A_CHUNK + B_CHUNK;
     static constexpr uint32_t STAGE = CH * CHUNK;
     static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
@@ -69,11 +76,11 @@ __device__ __forceinline__ ChunkPos chunk_pos(const WgradTcParams& p, int q) {
     return c;
 }
 
-template <int BN, int CH, int STAGES>
+template <int BN, int CH, int STAGES, int PL>
 __global__ void __launch_bounds__(WG_THREADS, 1)
     conv_wgrad_tc_kernel(const __grid_constant__ WgradTcParams p, const __grid_constant__ CUtensorMap xmap,
                          const __grid_constant__ CUtensorMap dymap) {
-    using W = WgCfg<BN, CH>;
+    using W = WgCfg<BN, CH, PL>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -142,7 +149,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
                 dyo[hh] = y * g.dh - g.ph;
                 dxo[hh] = x * g.dw - g.pw;
             }
-            const uint32_t bytes_chunk = (hv[1] ? 2 : 1) * HALF_BYTES + W::B_CHUNK;
+            const uint32_t bytes_chunk = PL * ((hv[1] ? 2 : 1) * HALF_BYTES + W::B_PLANE);
             int issued = 0;
             for (int st = 0; st < nstages; ++st) {
                 const int s = st % STAGES;
@@ -153,13 +160,18 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
                 for (int c = 0; c < nc; ++c) {
                     const ChunkPos cp = chunk_pos(p, q0 + st * CH + c);
                     const uint32_t dst = sbase + s * W::STAGE + c * W::CHUNK;
-                    for (int hh = 0; hh < 2; ++hh)
-                        if (hv[hh])
-                            tma_load_5d(dst + hh * HALF_BYTES, &xmap, cin[hh], cp.ow0 * g.sw + dxo[hh],
-                                        cp.oh * g.sh + dyo[hh], cp.od * g.sd + dz[hh], cp.n, full_bar(s));
-                    for (int j = 0; j < BN / 64; ++j)
-                        tma_load_5d(dst + W::A_CHUNK + j * HALF_BYTES, &dymap, kbase + nt * BN + j * 64, cp.ow0,
-                                    cp.oh, cp.od, cp.n, full_bar(s));
+                    // plane pl of image n is image pl*N + n of the plane tensors
+                    for (int pl = 0; pl < PL; ++pl) {
+                        const int ni = pl * g.N + cp.n;
+                        for (int hh = 0; hh < 2; ++hh)
+                            if (hv[hh])
+                                tma_load_5d(dst + pl * W::A_PLANE + hh * HALF_BYTES, &xmap, cin[hh],
+                                            cp.ow0 * g.sw + dxo[hh], cp.oh * g.sh + dyo[hh], cp.od * g.sd + dz[hh], ni,
+                                            full_bar(s));
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_5d(dst + W::A_CHUNK + pl * W::B_PLANE + j * HALF_BYTES, &dymap,
+                                        kbase + nt * BN + j * 64, cp.ow0, cp.oh, cp.od, ni, full_bar(s));
+                    }
                 }
             }
             // before the CTA can exit, the copies of the last stages issued must have landed
@@ -181,10 +193,16 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
             for (int c = 0; c < nc; ++c) {
                 const uint32_t a = sbase + s * W::STAGE + c * W::CHUNK;
                 const uint32_t b = a + W::A_CHUNK;
+                // plane pairs (A, B): hi*hi only, or the six that carry fp32 accuracy
+                constexpr int NP = PL == 1 ? 1 : 6;
+                constexpr int PA[6] = {0, 0, 1, 0, 2, 1}, PB[6] = {0, 1, 0, 2, 0, 1};
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_bf16_warp(tmem, sw128_mn_desc(a + k * 2048, HALF_BYTES), sw128_mn_desc(b + k * 2048, HALF_BYTES),
-                                  IDESC, (st > 0 || c > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int q = 0; q < NP; ++q)
+                        mma_bf16_warp(tmem, sw128_mn_desc(a + PA[q] * W::A_PLANE + k * 2048, HALF_BYTES),
+                                      sw128_mn_desc(b + PB[q] * W::B_PLANE + k * 2048, HALF_BYTES), IDESC,
+                                      (st > 0 || c > 0 || k > 0 || q > 0) ? 1u : 0u);
             }
             mma_commit_warp(empty_bar(s));
         }
@@ -228,6 +246,8 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
                     const float f = __uint_as_float(v[e]);
                     if (p.splits > 1)
                         p.ws[(long long)split * g.G * g.K * NJ + o] = f;
+                    else if (PL == 3)
+                        reinterpret_cast<float*>(p.dw)[o] = f;
                     else
                         reinterpret_cast<__nv_bfloat16*>(p.dw)[o] = __float2bfloat16_rn(f);
                 }
@@ -242,15 +262,15 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     }
 }
 
-template <int BN, int CH, int STAGES>
+template <int BN, int CH, int STAGES, int PL>
 constexpr size_t wg_smem_bytes() {
-    return 1024 + (size_t)STAGES * WgCfg<BN, CH>::STAGE + 8 * (2 * STAGES + 1) + 16;
+    return 1024 + (size_t)STAGES * WgCfg<BN, CH, PL>::STAGE + 8 * (2 * STAGES + 1) + 16;
 }
 
-template <int BN, int CH, int STAGES>
+template <int BN, int CH, int STAGES, int PL>
 cudaError_t launch_wg(const WgradTcParams& p, const CUtensorMap& xmap, const CUtensorMap& dymap, cudaStream_t stream) {
-    auto kern = conv_wgrad_tc_kernel<BN, CH, STAGES>;
-    constexpr size_t smem = wg_smem_bytes<BN, CH, STAGES>();
+    auto kern = conv_wgrad_tc_kernel<BN, CH, STAGES, PL>;
+    constexpr size_t smem = wg_smem_bytes<BN, CH, STAGES, PL>();
     static_assert(smem <= 232448, "shared memory budget");
     static bool attr_set[64];
     int dev = 0;
@@ -268,10 +288,17 @@ cudaError_t launch_wg(const WgradTcParams& p, const CUtensorMap& xmap, const CUt
 
 cudaError_t launch_wgrad_tc(const WgradTcParams& p, const CUtensorMap* xmap, const CUtensorMap* dymap,
                             cudaStream_t stream) {
+    if (p.planes == 3) {
+        switch (p.BN) {
+            case 64: return launch_wg<64, 1, 3, 3>(p, *xmap, *dymap, stream);
+            case 128: return launch_wg<128, 1, 2, 3>(p, *xmap, *dymap, stream);
+        }
+        return cudaErrorInvalidValue;
+    }
     switch (p.BN) {
-        case 64: return launch_wg<64, 2, 4>(p, *xmap, *dymap, stream);
-        case 128: return launch_wg<128, 2, 3>(p, *xmap, *dymap, stream);
-        case 256: return launch_wg<256, 1, 4>(p, *xmap, *dymap, stream);
+        case 64: return launch_wg<64, 2, 4, 1>(p, *xmap, *dymap, stream);
+        case 128: return launch_wg<128, 2, 3, 1>(p, *xmap, *dymap, stream);
+        case 256: return launch_wg<256, 1, 4, 1>(p, *xmap, *dymap, stream);
     }
     return cudaErrorInvalidValue;
 }

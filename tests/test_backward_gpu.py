@@ -242,3 +242,16 @@ def test_backward_weight_packed_small_groups(name, layer, no_pack):
     assert ("pack=1" in desc) == bool(no_pack), desc
     ref, S = oracle.conv_bwd_weight(geom_of(layer), syn.as_f32(x, "bf16"), syn.as_f32(dy, "bf16"))
     assert_within("bf16", CONV_EPI_NONE, got, ref.reshape(-1), S.reshape(-1), f"{name} [{desc}]")
+
+
+@pytest.mark.parametrize("name", ["1d_s1_f32", "2d_s1_f32_groups", "1d_s2_whisper_l2_shape", "1d_s2_tf32"])
+def test_fp32_backward_weight_on_tensor_cores_meets_the_fp32_bound(name):
+    """fp32 x and dy split into three bf16 planes, six plane products per tile: the fp32 bound
+    (1e-5 of the sum of |x dy|) holds, and the plan is the tensor-core one."""
+    dtype, layer = {c[0]: (c[1], c[2]) for c in CASES}[name]
+    x, w, dy = make_bwd_inputs(layer, dtype, 8900 + len(name))
+    got, desc = run_bwd_weight(layer, dtype, x, dy)
+    assert desc.startswith("variant=tc_bf16x3"), desc
+    ref, S = oracle.conv_bwd_weight(geom_of(layer), syn.as_f32(x, dtype), syn.as_f32(dy, dtype))
+    ratio, _ = assert_within(dtype, CONV_EPI_NONE, got, ref.reshape(-1), S.reshape(-1), f"{name} [{desc}]")
+    assert ratio < 0.1, ratio      # two orders of magnitude inside the bound
