@@ -343,6 +343,7 @@ struct conv_plan {
     int wg_kt, wg_jt, wg_mps, wg_tile;   // backward weight (FFMA): tiles along K and taps*C, pixels per split, tile
     int wg_rt, wg_nt, wg_q, wg_qps, wg_nwb, wg_cbh, wg_pack;   // backward weight (tensor cores), see WgradTcParams
     int wg_planes;                      // 1 (bf16) or 3 (fp32 split into bf16 planes)
+    int wg_slab, wg_na, wg_hpp, wg_nbox, wg_box_rows, wg_box_bytes, wg_stage_bytes, wg_stages, wg_tmem;   // slab mode
     size_t wg_xpl_off, wg_dypl_off;     // fp32: the x and dy planes within the workspace
     char desc[320];
 };
@@ -1044,8 +1045,8 @@ static bool encode_wg_maps(const conv_plan* p, const void* x, const void* dy, CU
     const cuuint64_t images = (cuuint64_t)g.N * (p->wg_planes > 1 ? p->wg_planes : 1);   // plane pl, image n: pl*N + n
     dims[0] = (cuuint64_t)g.G * g.C; dims[1] = g.W; dims[2] = g.H; dims[3] = g.D; dims[4] = images;
     strides[0] = dims[0] * 2; strides[1] = strides[0] * g.W; strides[2] = strides[1] * g.H; strides[3] = strides[2] * g.D;
-    box[0] = 64; box[1] = (cuuint32_t)(64 * g.sw); box[2] = box[3] = box[4] = 1;
-    es[0] = 1; es[1] = (cuuint32_t)g.sw; es[2] = es[3] = es[4] = 1;
+    box[0] = 64; box[1] = (cuuint32_t)(p->wg_slab ? p->wg_box_rows : 64 * g.sw); box[2] = box[3] = box[4] = 1;
+    es[0] = 1; es[1] = (cuuint32_t)(p->wg_slab ? 1 : g.sw); es[2] = es[3] = es[4] = 1;
     if (fn(xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(x), dims, strides, box, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -1091,7 +1092,30 @@ static bool plan_wg_tc(conv_plan* p) {
     const int64_t Q = (int64_t)f.N * f.Do * f.Ho * p->wg_nwb;
     if (Q >= ((int64_t)1 << 31)) return false;
     p->wg_q = (int)Q;
-    const int64_t base = cdiv(f.G, p->wg_pack) * p->wg_rt * p->wg_nt;
+    // slab mode (unit stride along W): a unit holds every half of one filter plane in its
+    // accumulators and reads one x box per (filter row, channel block) per chunk
+    p->wg_slab = 0;
+    {
+        const int reach = f.dw * (f.X - 1);
+        const int hpp = f.Y * f.X * p->wg_cbh;
+        const int na = (int)cdiv(hpp, 2);
+        if (p->wg_planes == 1 && f.sw == 1 && p->ch.gather != 2 && na <= 8 && na * bn <= 512 && 64 + reach <= 256) {
+            const int box_rows = 64 + reach;
+            const int box_bytes = (int)cdiv((int64_t)box_rows * 128, 1024) * 1024;
+            const int nbox = f.Y * p->wg_cbh;
+            const int stage_bytes = nbox * box_bytes + (bn / 64) * 8192;
+            const int stages = std::min(8, (int)((232448 - 1024 - 256) / stage_bytes));
+            if (stages >= 2) {
+                p->wg_slab = 1;
+                p->wg_na = na; p->wg_hpp = hpp; p->wg_nbox = nbox; p->wg_box_rows = box_rows;
+                p->wg_box_bytes = box_bytes; p->wg_stage_bytes = stage_bytes; p->wg_stages = stages;
+                int cols = 32;
+                while (cols < na * bn) cols *= 2;
+                p->wg_tmem = cols;
+            }
+        }
+    }
+    const int64_t base = cdiv(f.G, p->wg_pack) * (p->wg_slab ? f.Z : p->wg_rt) * p->wg_nt;
     if (base >= ((int64_t)1 << 31)) return false;
     int splits = (int)std::max<int64_t>(1, std::min<int64_t>(p->sm_count / base, Q / 2));
     if (p->ch.splits >= 1) splits = (int)std::min<int64_t>(p->ch.splits, Q);
@@ -1118,9 +1142,14 @@ static bool plan_wg_tc(conv_plan* p) {
         p->workspace_bytes = p->wg_dypl_off + 3 * ndy * 2;
     }
     snprintf(p->desc, sizeof(p->desc),
-             "variant=%s direction=bwd_weight operands=mn-major tile=128x%d row_tiles=%d chunk=64px splits=%d "
+             "variant=%s direction=bwd_weight operands=%s tile=128x%d row_tiles=%d chunk=64px splits=%d "
              "chunks_per_split=%d units=%d pack=%d",
-             p->wg_planes > 1 ? "tc_bf16x3" : "tc_bf16", bn, p->wg_rt, p->splits, p->wg_qps, p->total_units, p->wg_pack);
+             p->wg_planes > 1 ? "tc_bf16x3" : "tc_bf16", p->wg_slab ? "mn-major-slab" : "mn-major", bn,
+             p->wg_slab ? p->wg_na : p->wg_rt, p->splits, p->wg_qps, p->total_units, p->wg_pack);
+    if (p->wg_slab) {
+        const size_t n = strlen(p->desc);
+        snprintf(p->desc + n, sizeof(p->desc) - n, " boxes=%dx%d stages=%d", p->wg_nbox, p->wg_box_rows, p->wg_stages);
+    }
     return true;
 }
 
@@ -1521,6 +1550,9 @@ conv_status conv_bwd_weight(conv_plan_t plan, const void* x, const void* dy, voi
         tp.cbh = plan->wg_cbh; tp.halves = f.taps * plan->wg_cbh; tp.total_units = plan->total_units;
         tp.pack = plan->wg_pack;
         tp.planes = plan->wg_planes;
+        tp.slab = plan->wg_slab; tp.na = plan->wg_na; tp.hpp = plan->wg_hpp; tp.nbox = plan->wg_nbox;
+        tp.box_rows = plan->wg_box_rows; tp.box_bytes = plan->wg_box_bytes; tp.stage_bytes = plan->wg_stage_bytes;
+        tp.stages = plan->wg_stages; tp.tmem_cols = plan->wg_tmem;
         tp.pdl = plan->overlap;
         if (launch_wgrad_tc(tp, &xm, &dym, s) != cudaSuccess) return CONV_ERR_CUDA;
         if (plan->splits > 1)

@@ -229,6 +229,13 @@ struct WgradTcParams {
     int splits, Q, qps;     // pixel splits, 64-pixel chunks in all, chunks per split
     int nwb;                // 64-pixel blocks per output row
     int cbh, halves;        // 64-channel blocks per tap, taps * cbh
+    // slab mode (unit stride along W): a unit covers every half of one filter plane z
+    int slab;               // 1: slab mode
+    int na;                 // accumulators per unit (halves of a plane / 2, rounded up)
+    int hpp;                // halves per filter plane: Y * X * cbh
+    int nbox;               // x boxes per chunk: Y * cbh, each box_rows pixels of 64 channels
+    int box_rows, box_bytes, stage_bytes, stages;
+    int tmem_cols;
     int planes;             // 1: bf16 x and dy; 3: fp32 split into hi, mid, lo bf16 planes (images
                             // pl*N + n of the plane tensors), dw in fp32
     int pack;               // groups per tile (C, K dividing 64): x rows and dy columns of `pack`

@@ -262,6 +262,200 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     }
 }
 
+// ---- slab mode (bf16, unit stride along W) ----
+// A unit is (group or group pack, N tile, pixel split, filter plane z); its p.na accumulators
+// hold every half of plane z: accumulator a the halves 2a and 2a + 1, half h = (y*X + x)*cbh + cb.
+// Per chunk of 64 output pixels a stage holds one x box per (filter row y, channel block cb),
+// 64 + (X-1)*dw pixels from column ow0 - pw, so tap (y, x) is the window x*dw pixel rows into
+// box (y, cb) (MN-major windows start at any 128-byte row: the MMA applies the swizzle by
+// absolute address, as the TMA did), plus the dy boxes, shared by every accumulator.  The two
+// halves of an accumulator are two MN blocks one descriptor stride apart, whatever boxes and
+// offsets they come from.
+constexpr int WG_SLAB_MAX_STAGES = 8;
+constexpr int WG_SLAB_MAX_NA = 8;
+
+__global__ void __launch_bounds__(WG_THREADS, 1)
+    conv_wgrad_slab_kernel(const __grid_constant__ WgradTcParams p, const __grid_constant__ CUtensorMap xmap,
+                           const __grid_constant__ CUtensorMap dymap) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (sbase - raw);
+    const int S = p.stages;
+    const uint32_t stage_bytes = (uint32_t)p.stage_bytes;
+    const uint32_t bar0 = sbase + (uint32_t)S * stage_bytes;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (WG_SLAB_MAX_STAGES + s); };
+    const uint32_t done_bar = bar0 + 8u * (2 * WG_SLAB_MAX_STAGES);
+    uint8_t* misc = smem + (done_bar + 8u - sbase);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const Geom& g = p.g;
+    const int BN = p.BN;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (p.pdl) {
+        griddep_launch();
+        griddep_wait();
+    }
+
+    // unit: filter plane fastest (the planes of one pixel range share their dy chunks in L2)
+    const int u = blockIdx.x;
+    const int z = u % g.Z;
+    int r = u / g.Z;
+    const int split = r % p.splits;
+    r /= p.splits;
+    const int nt = r % p.NT;
+    const int gi = r / p.NT;
+    const int cbase = gi * p.pack * g.C, kbase = gi * p.pack * g.K;
+    const int q0 = split * p.qps;
+    const int q1 = min(q0 + p.qps, p.Q);
+    const int nchunks = q1 - q0;
+    const uint32_t dy_off = (uint32_t)(p.nbox * p.box_bytes);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint32_t tx = (uint32_t)p.nbox * (uint32_t)p.box_rows * 128u + (uint32_t)(BN / 64) * HALF_BYTES;
+            int issued = 0;
+            bool aborted = false;
+            for (int st = 0; st < nchunks; ++st) {
+                const int s = st % S;
+                if (st >= S && !wait_bar(empty_bar(s), ((st / S) - 1) & 1, abort_flag, p.err)) {
+                    aborted = true;
+                    break;
+                }
+                issued = st + 1;
+                mbar_arrive_expect_tx(full_bar(s), tx);
+                const ChunkPos cp = chunk_pos(p, q0 + st);
+                const uint32_t dst = sbase + (uint32_t)s * stage_bytes;
+                const int dd = cp.od * g.sd - g.pd + z * g.dd;
+                for (int b = 0; b < p.nbox; ++b) {
+                    const int y = b / p.cbh, cb = b - y * p.cbh;
+                    tma_load_5d(dst + (uint32_t)(b * p.box_bytes), &xmap, cbase + cb * 64, cp.ow0 - g.pw,
+                                cp.oh * g.sh - g.ph + y * g.dh, dd, cp.n, full_bar(s));
+                }
+                for (int j = 0; j < BN / 64; ++j)
+                    tma_load_5d(dst + dy_off + (uint32_t)j * HALF_BYTES, &dymap, kbase + nt * BN + j * 64, cp.ow0, cp.oh,
+                                cp.od, cp.n, full_bar(s));
+            }
+            (void)aborted;
+            // the copies of the last stages issued must have landed before the CTA exits
+            const unsigned long long t0 = globaltimer();
+            for (int st = issued > S ? issued - S : 0; st < issued; ++st)
+                while (!mbar_try_wait(full_bar(st % S), (st / S) & 1) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+                }
+        }
+    } else if (warp == 1) {
+        const uint32_t IDESC = idesc_f32acc(128, BN, 1u) | (1u << 15) | (1u << 16);   // A, B MN-major
+        // per accumulator: its first half's window (bytes into a stage) and the distance to the second
+        uint32_t aoff[WG_SLAB_MAX_NA], albo[WG_SLAB_MAX_NA];
+#pragma unroll
+        for (int a = 0; a < WG_SLAB_MAX_NA; ++a) {
+            aoff[a] = albo[a] = 0;
+            if (a < p.na) {
+                uint32_t o[2];
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int h = min(2 * a + hh, p.hpp - 1);   // a missing second half repeats the first
+                    const int t = h / p.cbh, cb = h - t * p.cbh;
+                    const int y = t / g.X, x = t - y * g.X;
+                    o[hh] = (uint32_t)((y * p.cbh + cb) * p.box_bytes + x * g.dw * 128);
+                }
+                aoff[a] = o[0];
+                albo[a] = o[1] - o[0];
+            }
+        }
+        bool ok = true;
+        for (int st = 0; st < nchunks && ok; ++st) {
+            const int s = st % S;
+            ok = wait_bar_warp(full_bar(s), (st / S) & 1, abort_flag, p.err);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t base = sbase + (uint32_t)s * stage_bytes;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint64_t bd = sw128_mn_desc(base + dy_off + k * 2048, HALF_BYTES);
+#pragma unroll
+                for (int a = 0; a < WG_SLAB_MAX_NA; ++a)
+                    if (a < p.na)
+                        mma_bf16_warp(tmem + (uint32_t)(a * BN), sw128_mn_desc(base + aoff[a] + k * 2048, albo[a]), bd,
+                                      IDESC, (st > 0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit_warp(empty_bar(s));
+        }
+        if (ok) mma_commit_warp(done_bar);
+    } else {
+        // epilogue: TMEM lane quarter (warp % 4); per accumulator a, row -> half -> (tap, c)
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const bool ok = wait_bar_warp(done_bar, 0, abort_flag, p.err, true);
+        if (ok) {
+            tc_fence_after();
+            const int NJ = g.taps * g.C;
+            const int pa = p.pack > 1 ? (row & 63) / g.C : 0;
+            const int grp = gi * p.pack + pa;
+            for (int a = 0; a < p.na; ++a) {
+                const int h = 2 * a + (row >> 6);
+                const int t = h / p.cbh;
+                const int c = p.pack > 1 ? (row & 63) - pa * g.C : (h - t * p.cbh) * 64 + (row & 63);
+                const int tap = z * g.Y * g.X + t;
+                const bool row_ok = h < p.hpp && c < g.C && pa < p.pack && grp < g.G;
+                const long long col0 = (long long)tap * g.C + c;
+                const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(a * BN);
+                for (int cb = 0; cb < BN; cb += 16) {
+                    if (nt * BN + cb >= p.pack * g.K) break;   // warp-uniform
+                    uint32_t v[16];
+                    __syncwarp();
+                    tmem_ld16(taddr + (uint32_t)cb, v);
+                    tmem_ld_wait();
+                    if (!row_ok) continue;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        int k = nt * BN + cb + e;
+                        if (p.pack > 1) {
+                            const int b = k / g.K;
+                            if (b != pa) continue;
+                            k -= b * g.K;
+                        } else if (k >= g.K) {
+                            break;
+                        }
+                        const long long o = ((long long)grp * g.K + k) * NJ + col0;
+                        const float f = __uint_as_float(v[e]);
+                        if (p.splits > 1)
+                            p.ws[(long long)split * g.G * g.K * NJ + o] = f;
+                        else
+                            reinterpret_cast<__nv_bfloat16*>(p.dw)[o] = __float2bfloat16_rn(f);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
+    }
+}
+
 template <int BN, int CH, int STAGES, int PL>
 constexpr size_t wg_smem_bytes() {
     return 1024 + (size_t)STAGES * WgCfg<BN, CH, PL>::STAGE + 8 * (2 * STAGES + 1) + 16;
@@ -288,6 +482,23 @@ cudaError_t launch_wg(const WgradTcParams& p, const CUtensorMap& xmap, const CUt
 
 cudaError_t launch_wgrad_tc(const WgradTcParams& p, const CUtensorMap* xmap, const CUtensorMap* dymap,
                             cudaStream_t stream) {
+    if (p.slab) {
+        const size_t smem = 1024 + (size_t)p.stages * p.stage_bytes + 8 * (2 * WG_SLAB_MAX_STAGES + 1) + 16;
+        if (p.stages < 2 || p.stages > WG_SLAB_MAX_STAGES || p.na < 1 || p.na > WG_SLAB_MAX_NA || smem > 232448 ||
+            p.na * p.BN > p.tmem_cols || p.tmem_cols > 512 || p.planes != 1)
+            return cudaErrorInvalidValue;
+        static bool attr_set[64];
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+            e = cudaFuncSetAttribute(conv_wgrad_slab_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) attr_set[dev] = true;
+        }
+        return launch_kernel(conv_wgrad_slab_kernel, dim3(p.total_units), dim3(WG_THREADS), smem, stream, p.pdl != 0, 1,
+                             p, *xmap, *dymap);
+    }
     if (p.planes == 3) {
         switch (p.BN) {
             case 64: return launch_wg<64, 1, 3, 3>(p, *xmap, *dymap, stream);

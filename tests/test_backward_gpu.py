@@ -255,3 +255,25 @@ def test_fp32_backward_weight_on_tensor_cores_meets_the_fp32_bound(name):
     ref, S = oracle.conv_bwd_weight(geom_of(layer), syn.as_f32(x, dtype), syn.as_f32(dy, dtype))
     ratio, _ = assert_within(dtype, CONV_EPI_NONE, got, ref.reshape(-1), S.reshape(-1), f"{name} [{desc}]")
     assert ratio < 0.1, ratio      # two orders of magnitude inside the bound
+
+
+SLAB_W = [
+    ("2d_3x3_c64_g2_wide", B_(2, 2, 2, 64, 64, (20, 70), (3, 3), (1, 1), (1, 1), (1, 1))),
+    ("2d_3x3_c64_dil2", B_(2, 1, 1, 64, 64, (18, 33), (3, 3), (1, 1), (2, 2), (2, 2))),
+    ("3d_3x3x3_c64", B_(3, 1, 2, 64, 64, (5, 9, 70), (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1))),
+    ("1d_k5_c128", B_(1, 2, 1, 128, 64, (300,), (5,), (1,), (2,), (1,))),
+    ("2d_g16_c8_packed", B_(2, 1, 16, 8, 8, (20, 22), (3, 3), (1, 1), (1, 1), (1, 1))),
+    ("2d_s2_rows_only", B_(2, 1, 1, 64, 64, (21, 40), (3, 3), (2, 1), (1, 1), (1, 1))),
+]
+
+
+@pytest.mark.parametrize("per_tap", [0, 1])
+@pytest.mark.parametrize("name,layer", SLAB_W, ids=[c[0] for c in SLAB_W])
+def test_backward_weight_slab_windows(name, layer, per_tap):
+    """Unit stride along W: one x box per filter row serves every tap of that row as shifted
+    MN-major windows (slab mode); CONV_FORCE_GATHER=tma runs the per-tap boxes instead."""
+    x, w, dy = make_bwd_inputs(layer, "bf16", 9100 + len(name))
+    got, desc = run_bwd_weight(layer, "bf16", x, dy, env={"CONV_FORCE_GATHER": "tma"} if per_tap else None)
+    assert ("operands=mn-major-slab" in desc) == (not per_tap), desc
+    ref, S = oracle.conv_bwd_weight(geom_of(layer), syn.as_f32(x, "bf16"), syn.as_f32(dy, "bf16"))
+    assert_within("bf16", CONV_EPI_NONE, got, ref.reshape(-1), S.reshape(-1), f"{name} [{desc}]")
