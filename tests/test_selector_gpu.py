@@ -107,3 +107,35 @@ def test_every_selector_candidate_matches_oracle(dtype, bn, splits, gather):
     assert f"x{bn} " in desc, desc
     ref, S = oracle_full(layer, dtype, x, w, b)
     assert_within(dtype, layer.epilogue, got, ref, S, desc)
+
+
+def test_selector_tunes_a_unit_stride_backward_data_plan():
+    """Backward data at unit stride runs the forward kernels on the transposed problem, so the
+    selector can time its candidates too; the tuned plan still matches the oracle."""
+    import torch
+    import oracle
+    from convolution_forward_implicit_gb300 import synthetic as syn
+    from convolution_forward_implicit_gb300.binding import CONV_EPI_NONE
+    from tests.helpers import geom_of
+    layer = L(2, 1, 8, 64, 64, (20, 24), (3, 3), (1, 1), (1, 1), (1, 1), CONV_EPI_NONE)
+    g = geom_of(layer)
+    w = syn.gen_uniform_pm(4601, layer.w_shape(), layer.w_bound, "bf16")
+    dy = syn.gen_normal(4602, g.y_shape(), "bf16")
+    B.conv_tune_table_clear()
+    try:
+        plan = ConvPlan(*layer.plan_args(CONV_BF16), direction="bwd_data")
+        assert "transposed_forward" in plan.describe()
+        wd, dyd = to_device(w, "bf16"), to_device(dy, "bf16")
+        dx = torch.empty(layer.x_shape(), dtype=torch.bfloat16, device="cuda")
+        desc = plan.tune(dyd, wd, None, dx, iters=3)
+        assert "transposed_forward" in desc
+        dx.fill_(float("nan"))
+        plan.backward_data(dyd, dx)
+        plan.check()
+        torch.cuda.synchronize()
+        ref, S = oracle.conv_bwd_data(g, syn.as_f32(dy, "bf16"), syn.as_f32(w, "bf16"))
+        assert_within("bf16", CONV_EPI_NONE, from_device(dx, "bf16").reshape(-1), ref.reshape(-1), S.reshape(-1),
+                      desc)
+        plan.close()
+    finally:
+        B.conv_tune_table_clear()
