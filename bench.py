@@ -483,11 +483,14 @@ def run_ours(args, ws, rank, local):
     if ev is None:
         # the last replay of every rotation set's graph
         last = sorted({i % R: i for i in range(K)}.keys())
-        per_layer_ms = [sum(gev[r][j].elapsed_time(gev[r][j + 1]) for r in last) / len(last) for j in range(nL)]
-        layer_samples = len(last)
+        samples = [[gev[r][j].elapsed_time(gev[r][j + 1]) for r in last] for j in range(nL)]
     else:
-        per_layer_ms = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K for j in range(nL)]
-        layer_samples = K
+        samples = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)] for j in range(nL)]
+    per_layer_ms = [sum(v) / len(v) for v in samples]
+    layer_samples = len(samples[0]) if samples else 0
+    layer_spread = {lr.name(): {"median": round(float(np.median(v)) * 1e3, 3),
+                                "p10": round(float(np.percentile(v, 10)) * 1e3, 3),
+                                "p90": round(float(np.percentile(v, 90)) * 1e3, 3)} for lr, v in zip(runs, samples)}
     # keep sampling clocks over a sustained window of the same steps (at least ~1.5 s)
     t_end = time.time() + 1.5
     i = 0
@@ -546,6 +549,7 @@ def run_ours(args, ws, rank, local):
         "metric": METRIC, "value": round(value, 4), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "us_per_call": {lr.name(): round(t * 1e3, 3) for lr, t in zip(runs, per_layer_ms)},
+        "us_per_call_spread": layer_spread,
         "useful_gflop_per_step": round(step_flops / 1e9, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "+".join(sorted({wl.dtype for wl in wls}, key=lambda d: d != "f32")),
