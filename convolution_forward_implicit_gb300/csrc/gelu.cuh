@@ -4,8 +4,9 @@
 // Abramowitz & Stegun, Handbook of Mathematical Functions, eq. 7.1.28 (after Hastings):
 // erf(z) = 1 - (1 + a1 z + ... + a6 z^6)^-16 for z >= 0, |error| <= 3e-7.  Then
 // GELU(v) = v - h for v >= 0 and h for v < 0, with h = v (1 - erf(|v|/sqrt 2)) / 2, at one
-// reciprocal and no exponential per value.  The absolute GELU error, <= 1.5e-7 |v|, is far
-// below both output bounds (bf16 rounding; fp32: 1e-5 of the sum of |x w|).
+// reciprocal and no exponential per value.  Evaluated in fp32 over [-8, 8] the GELU error stays
+// below 8.3e-7 |v| (1.4e-7 |v| in exact arithmetic), far below both output bounds (bf16
+// rounding; fp32: 1e-5 of the sum of |x w|).
 #pragma once
 #include <stdint.h>
 
@@ -43,20 +44,24 @@ __device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
     return r;
 }
 
-// gelu on two values at once: the polynomial and the squarings as packed f32x2 operations,
-// so each value gets bit for bit the result of the scalar form.
+// gelu on two values at once, for bf16 outputs: the same A&S 7.1.28 form with the argument
+// scale 1/sqrt(2) and the factor 1/2 folded into the coefficients, y'(|v|) = 2^(1/16) *
+// (1 + a1 |v|/sqrt2 + ... + a6 (|v|/sqrt2)^6), so that y'^16 = 2 y^16 and h = v / y'^16 (two
+// multiplications fewer per value); the polynomial and the squarings run as packed f32x2
+// operations.  Evaluated in fp32 over [-8, 8] its error stays below 1.2e-6 |v|, far below the
+// bf16 rounding of the output (2^-9 relative).
 __device__ __forceinline__ void gelu2(float& a, float& b) {
-    const uint64_t z = f2pk(fabsf(a) * 0.70710678118654752f, fabsf(b) * 0.70710678118654752f);
-    uint64_t y = f2fma(z, f2pk(0.0000430638f, 0.0000430638f), f2pk(0.0002765672f, 0.0002765672f));
-    y = f2fma(z, y, f2pk(0.0001520143f, 0.0001520143f));
-    y = f2fma(z, y, f2pk(0.0092705272f, 0.0092705272f));
-    y = f2fma(z, y, f2pk(0.0422820123f, 0.0422820123f));
-    y = f2fma(z, y, f2pk(0.0705230784f, 0.0705230784f));
-    y = f2fma(z, y, f2pk(1.0f, 1.0f));
+    const uint64_t z = f2pk(fabsf(a), fabsf(b));
+    uint64_t y = f2fma(z, f2pk(5.6212996640e-06f, 5.6212996640e-06f), f2pk(5.1055209009e-05f, 5.1055209009e-05f));
+    y = f2fma(z, y, f2pk(3.9686137011e-05f, 3.9686137011e-05f));
+    y = f2fma(z, y, f2pk(3.4227392389e-03f, 3.4227392389e-03f));
+    y = f2fma(z, y, f2pk(2.2076998457e-02f, 2.2076998457e-02f));
+    y = f2fma(z, y, f2pk(5.2075163037e-02f, 5.2075163037e-02f));
+    y = f2fma(z, y, f2pk(1.0442737824e+00f, 1.0442737824e+00f));
     y = f2mul(y, y); y = f2mul(y, y); y = f2mul(y, y); y = f2mul(y, y);   // (.)^16
     float ya, yb;
     f2up(y, ya, yb);
-    const float ha = __fdividef(0.5f * a, ya), hb = __fdividef(0.5f * b, yb);
+    const float ha = __fdividef(a, ya), hb = __fdividef(b, yb);
     a = a >= 0.0f ? a - ha : ha;
     b = b >= 0.0f ? b - hb : hb;
 }

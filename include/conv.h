@@ -216,8 +216,10 @@ conv_status conv_bwd_data(conv_plan_t plan, const void* dy, const void* w_packed
 
 /*
  * Backward-weight plan.  No packed weight (conv_prepack_weights returns
- * CONV_ERR_INVALID_ARG); the output pixels are split across CTAs, whose fp32 partial
- * sums need a workspace of conv_workspace_bytes(plan) when that is non-zero.
+ * CONV_ERR_INVALID_ARG).  The output pixels are split across CTAs, whose fp32 partial sums
+ * live in the workspace; fp32 plans also stage x and dy there as three bf16 planes each (the
+ * tensor cores then accumulate six plane products per tile).  Attach a workspace of
+ * conv_workspace_bytes(plan) whenever that is non-zero.
  */
 conv_status conv_bwd_weight_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, int64_t C, int64_t K,
                                         const int64_t* spatial, const int64_t* filter, const int64_t* stride,
