@@ -581,7 +581,12 @@ def run_ours(args, ws, rank, local):
 def run_e2e(args, runs, in_specs, out_sets, R, stream, ws, local, step):
     """The same step through the public API with host buffers: each step copies its inputs
     (in_specs: storage array, dtype, device copies) from pinned host memory, runs every layer,
-    and copies the results (out_sets: device copies) back to pinned host memory."""
+    and copies the results (out_sets: device copies) back to pinned host memory.  The copies
+    run on their own streams, pipelined across steps: step i+1's inputs are copied in and
+    step i's results copied out while the next step computes, each rotating buffer guarded by
+    events (a set is refilled only after the step that last used it has finished and its
+    results were read back).  Every byte of every step stays inside the timed region.
+    With --e2e-serial the copies and the step run one after the other on one stream."""
     import torch
     host_in, host_out = [], []
     for (a, dtype, sets) in in_specs:
@@ -592,31 +597,68 @@ def run_e2e(args, runs, in_specs, out_sets, R, stream, ws, local, step):
     bi = sum(h.numel() * h.element_size() for h, _ in host_in)
     bo = sum(h.numel() * h.element_size() for h, _ in host_out)
     K = args.steps
+    copy_in, copy_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(R)]      # inputs of the set's current step are in
+    ev_done = [torch.cuda.Event() for _ in range(R)]    # the set's current step has computed
+    ev_out = [torch.cuda.Event() for _ in range(R)]     # the set's results have been read back
 
-    def e2e_step(i):
+    def h2d(i):
         r = i % R
-        for h, sets in host_in:
-            sets[r].copy_(h, non_blocking=True)
-        step(i)
-        for h, sets in host_out:
-            h.copy_(sets[r], non_blocking=True)
+        if i >= R:
+            copy_in.wait_event(ev_done[r])               # step i - R, the set's last user, is done
+        with torch.cuda.stream(copy_in):
+            for h, sets in host_in:
+                sets[r].copy_(h, non_blocking=True)
+        ev_in[r].record(copy_in)
 
-    for i in range(args.warmup):
-        e2e_step(i)
+    def e2e_step(i, last):
+        r = i % R
+        if args.e2e_serial:
+            for h, sets in host_in:
+                sets[r].copy_(h, non_blocking=True)
+            step(i)
+            for h, sets in host_out:
+                h.copy_(sets[r], non_blocking=True)
+            return
+        stream.wait_event(ev_in[r])
+        if i >= R:
+            stream.wait_event(ev_out[r])                 # step i - R's results were read back
+        step(i)
+        ev_done[r].record(stream)
+        copy_out.wait_event(ev_done[r])
+        with torch.cuda.stream(copy_out):
+            for h, sets in host_out:
+                h.copy_(sets[r], non_blocking=True)
+        ev_out[r].record(copy_out)
+        if i + 1 < last:
+            h2d(i + 1)
+
+    def run(first, count, start_event=None):
+        if not args.e2e_serial:
+            if start_event is not None:
+                copy_in.wait_event(start_event)
+            h2d(first)
+        for i in range(first, first + count):
+            e2e_step(i, first + count)
+        if not args.e2e_serial:
+            stream.wait_stream(copy_out)
+
+    run(0, args.warmup)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
     e0.record(stream)
-    for i in range(K):
-        e2e_step(i)
+    run(args.warmup, K, start_event=e0)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
     ms = max_over_ranks(e0.elapsed_time(e1), ws, torch.device("cuda", local))
     flops = sum(lr.flops for lr in runs)
     return {"value": round(ws * flops * K / (ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
-            "ms_per_step": round(ms / K, 6), "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
+            "ms_per_step": round(ms / K, 6), "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+            "copies": ("serial with the step on one stream" if args.e2e_serial else
+                       "pinned host buffers; H2D and D2H on their own streams, pipelined across steps")}
 
 
 def measured_peaks():
@@ -870,6 +912,8 @@ def main():
                     help="run the step's independent chains one after the other (the forward default)")
     ap.add_argument("--parallel", dest="parallel", action="store_const", const=True,
                     help="capture the step's independent chains as parallel graph branches (the backward default)")
+    ap.add_argument("--e2e-serial", action="store_true",
+                    help="end-to-end leg: copy in, step, copy out one after the other instead of pipelined")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="fwd: the forward pass of every layer; bwd: backward data and backward weight of every layer")
     ap.add_argument("--tune", type=int, default=0, metavar="ITERS",
