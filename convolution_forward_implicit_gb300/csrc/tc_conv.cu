@@ -334,8 +334,10 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
     } else if (T::TF32 && warp >= T::CVT_WARP0) {
         // ------------------------------------------------------------ hi/lo split (3xTF32)
         if (p.pdl) griddep_wait();
-        // Every fp32 activation x becomes hi = x with its low 13 mantissa bits cleared (exact
+        // Every fp32 activation x splits into hi = x with its low 13 mantissa bits cleared (exact
         // in TF32) and lo = x - hi (exact in fp32); the MMA then sums lo*w_hi + hi*w_lo + hi*w_hi.
+        // hi is the tile as the TMA wrote it: kind::tf32 reads an fp32 operand by ignoring those
+        // 13 bits (measured: every product equals the truncated operand's), so only lo is written.
         const int ct = threadIdx.x - T::CVT_WARP0 * 32;
         const int n16 = p.BW * p.BH * 8;   // 16-byte chunks the TMA box wrote
         uint32_t it = 0;
@@ -359,7 +361,6 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                     l.y = __float_as_uint(__uint_as_float(v.y) - __uint_as_float(h.y));
                     l.z = __float_as_uint(__uint_as_float(v.z) - __uint_as_float(h.z));
                     l.w = __float_as_uint(__uint_as_float(v.w) - __uint_as_float(h.w));
-                    hi[i] = h;
                     lo[i] = l;
                 }
                 fence_proxy_async();

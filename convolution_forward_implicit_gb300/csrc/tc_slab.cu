@@ -351,7 +351,6 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
                     l.y = __float_as_uint(__uint_as_float(v.y) - __uint_as_float(h.y));
                     l.z = __float_as_uint(__uint_as_float(v.z) - __uint_as_float(h.z));
                     l.w = __float_as_uint(__uint_as_float(v.w) - __uint_as_float(h.w));
-                    hi[i] = h;
                     lo[i] = l;
                 }
                 fence_proxy_async();
