@@ -43,7 +43,7 @@ def random_layer(rng):
     return L(ndim, N, G, C, K, spatial, filt, stride, pad, dil, epi)
 
 
-CASES = [(seed, "bf16" if seed % 2 else "f32") for seed in range(40)]
+CASES = [(seed, "bf16" if seed % 2 else "f32") for seed in range(120)]
 
 
 @pytest.mark.parametrize("seed,dtype", CASES, ids=[f"{s}_{d}" for s, d in CASES])
