@@ -396,8 +396,10 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
                                            2 * j;
                         const float4 a = __ldg(bp);
                         const float4 b = (nq + 8 * j + 4 < g.K) ? __ldg(bp + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        f[8 * j] += a.x; f[8 * j + 1] += a.y; f[8 * j + 2] += a.z; f[8 * j + 3] += a.w;
-                        f[8 * j + 4] += b.x; f[8 * j + 5] += b.y; f[8 * j + 6] += b.z; f[8 * j + 7] += b.w;
+                        add2(f[8 * j], f[8 * j + 1], a.x, a.y);
+                        add2(f[8 * j + 2], f[8 * j + 3], a.z, a.w);
+                        add2(f[8 * j + 4], f[8 * j + 5], b.x, b.y);
+                        add2(f[8 * j + 6], f[8 * j + 7], b.z, b.w);
                     } else {
                         const uint4 b4 = __ldg(reinterpret_cast<const uint4*>(
                                                    reinterpret_cast<const __nv_bfloat16*>(p.bias) + (size_t)gi * g.K +
@@ -405,10 +407,9 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
                                                j);
                         const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            f[8 * j + 2 * e] += __uint_as_float(bw[e] << 16);
-                            f[8 * j + 2 * e + 1] += __uint_as_float(bw[e] & 0xFFFF0000u);
-                        }
+                        for (int e = 0; e < 4; ++e)
+                            add2(f[8 * j + 2 * e], f[8 * j + 2 * e + 1], __uint_as_float(bw[e] << 16),
+                                 __uint_as_float(bw[e] & 0xFFFF0000u));
                     }
                 }
             }
