@@ -378,6 +378,17 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
 #pragma unroll
         for (int q = 0; q < CW / QW; ++q) {
             const int nq = n0 + QW * q;
+            // bf16 bias: its loads go out before the TMEM load, so that their latencies overlap
+            // (8-column groups past K read as zeros; those columns are never stored)
+            uint4 bq[ESZ == 2 ? QW / 8 : 1];
+            if (ESZ == 2 && add_bias) {
+#pragma unroll
+                for (int j = 0; j < QW / 8; ++j)
+                    bq[j] = nq + 8 * j < g.K ? __ldg(reinterpret_cast<const uint4*>(
+                                                         reinterpret_cast<const __nv_bfloat16*>(p.bias) +
+                                                         (size_t)gi * g.K + nq) + j)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+            }
             uint32_t v[QW];
             __syncwarp();                                   // tcgen05.ld is warp-aligned
             tmem_ld<QW>(taddr + (uint32_t)(cb + QW * q), v);
@@ -385,32 +396,30 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
             float f[QW];
 #pragma unroll
             for (int e = 0; e < QW; ++e) f[e] = __uint_as_float(v[e]);
-            if (add_bias) {
-                // only whole 8-column groups inside K are read; columns past K are never stored
+            if (ESZ == 2 && add_bias) {
+#pragma unroll
+                for (int j = 0; j < QW / 8; ++j) {
+                    const uint32_t bw[4] = {bq[j].x, bq[j].y, bq[j].z, bq[j].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        add2(f[8 * j + 2 * e], f[8 * j + 2 * e + 1], __uint_as_float(bw[e] << 16),
+                             __uint_as_float(bw[e] & 0xFFFF0000u));
+                }
+            } else if (add_bias) {
+                // fp32 bias: only whole 4-column groups inside K are read; columns past K are
+                // never stored
 #pragma unroll
                 for (int j = 0; j < QW / 8; ++j) {
                     if (nq + 8 * j >= g.K) break;
-                    if (ESZ == 4) {
-                        const float4* bp = reinterpret_cast<const float4*>(
-                                               reinterpret_cast<const float*>(p.bias) + (size_t)gi * g.K + nq) +
-                                           2 * j;
-                        const float4 a = __ldg(bp);
-                        const float4 b = (nq + 8 * j + 4 < g.K) ? __ldg(bp + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        add2(f[8 * j], f[8 * j + 1], a.x, a.y);
-                        add2(f[8 * j + 2], f[8 * j + 3], a.z, a.w);
-                        add2(f[8 * j + 4], f[8 * j + 5], b.x, b.y);
-                        add2(f[8 * j + 6], f[8 * j + 7], b.z, b.w);
-                    } else {
-                        const uint4 b4 = __ldg(reinterpret_cast<const uint4*>(
-                                                   reinterpret_cast<const __nv_bfloat16*>(p.bias) + (size_t)gi * g.K +
-                                                   nq) +
-                                               j);
-                        const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            add2(f[8 * j + 2 * e], f[8 * j + 2 * e + 1], __uint_as_float(bw[e] << 16),
-                                 __uint_as_float(bw[e] & 0xFFFF0000u));
-                    }
+                    const float4* bp =
+                        reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.bias) + (size_t)gi * g.K + nq) +
+                        2 * j;
+                    const float4 a = __ldg(bp);
+                    const float4 b = (nq + 8 * j + 4 < g.K) ? __ldg(bp + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    add2(f[8 * j], f[8 * j + 1], a.x, a.y);
+                    add2(f[8 * j + 2], f[8 * j + 3], a.z, a.w);
+                    add2(f[8 * j + 4], f[8 * j + 5], b.x, b.y);
+                    add2(f[8 * j + 6], f[8 * j + 7], b.z, b.w);
                 }
             }
             if (do_gelu) {

@@ -12,22 +12,24 @@
 // conv2d path already solves this", is never materialised: each A tile is gathered
 // straight from the channels-last input, zero-filled where a tap falls in the padding.
 //
-// One persistent CTA per SM (grid = min(units, SMs)), warp-specialised:
-//   warps 0-7   epilogue: two warps per TMEM lane quarter (warp w owns lanes 32(w%4)..+31
-//               and half of the columns); tcgen05.ld, bias, GELU, rounding, then stores
-//               through a per-warp staging buffer so each store instruction writes whole
-//               row segments (fp32 partial sums instead when the reduction is split).
-//   warps 8-11  producers, per K block (one tap x 64 bf16 or 32 fp32 channels):
-//               TMA gather: one 5-D tiled box of BH x BW output pixels (conv stride as the
-//               element stride, padding as out-of-bounds zero fill) plus one bulk copy of
-//               the prepacked weight tile, issued by the warp that owns the stage;
+// One persistent CTA per SM (grid = min(units, SMs)), warp-specialised (EW = 8 or 16
+// epilogue warps):
+//   warps 0..EW-1   epilogue: EW/4 warps per TMEM lane quarter (warp w owns lanes
+//               32(w%4)..+31 and a 1/(EW/4) share of the columns); tcgen05.ld, bias, GELU,
+//               rounding, then stores through a per-warp staging buffer so each store
+//               instruction writes whole row segments (fp32 partial sums instead when the
+//               reduction is split).
+//   next 4 warps (3 with EW = 16)   producers, per K block (one tap x 64 bf16 or 32 fp32
+//               channels): TMA gather: one 5-D tiled box of BH x BW output pixels (conv stride
+//               as the element stride, padding as out-of-bounds zero fill) plus one bulk copy
+//               of the prepacked weight tile, issued by the warp that owns the stage;
 //               cp.async gather: 16-byte zero-filling copies of 8-channel chunks packed
 //               densely across taps, for channel counts no box can serve.
-//   warp 12     MMA: one thread issues tcgen05.mma (M = 128, N = BN; 4 x K=16 bf16 or
+//   next warp   MMA: one thread issues tcgen05.mma (M = 128, N = BN; 4 x K=16 bf16 or
 //               12 x K=8 tf32 per K block) and tcgen05.commit frees the stage; the
 //               accumulator is double-buffered in TMEM so the epilogue of tile i overlaps
 //               the main loop of tile i+1.
-//   warps 13-16 (3xTF32 only) split each activation tile into hi and lo parts in place.
+//   last 4 warps (3xTF32 only) split each activation tile into hi and lo parts in place.
 // Every mbarrier wait is bounded: after ~1 s it raises the device error word, sets a
 // CTA-wide abort flag and the CTA winds down (drains copies, waits for issued MMAs,
 // frees TMEM).
@@ -46,12 +48,14 @@ enum Kind { KIND_BF16_CPASYNC = 0, KIND_BF16_TMA = 1, KIND_TF32X3 = 2 };
 // A thread has at most one TMA copy in flight (measured on this GPU: a second copy from the
 // same thread starts only when the first completes, ~700 cycles each), so the TMA producer
 // spreads its copies over 4 warps, pipeline stage s belonging to warp s % 4, where lane 0
-// copies the activation box and lane 1 the weight tile.
+// copies the activation box and lane 1 the weight tile.  With 16 epilogue warps there are 3
+// producer warps (those plans have 3 or 5 stages): 20 warps in all leave each SM sub-partition
+// 5 warps, so a thread may hold 96 registers (21 warps: 6 on one sub-partition, 80 registers).
 template <int KIND, int EW>
 struct Traits {
     static constexpr bool TMA = KIND != KIND_BF16_CPASYNC;
     static constexpr bool TF32 = KIND == KIND_TF32X3;
-    static constexpr int PROD_WARPS = 4;
+    static constexpr int PROD_WARPS = EW == 16 ? 3 : 4;
     static constexpr int CVT_WARPS = TF32 ? 4 : 0;
     static constexpr int MMA_WARP = EW + PROD_WARPS;
     static constexpr int CVT_WARP0 = MMA_WARP + 1;
