@@ -356,7 +356,8 @@ __device__ __forceinline__ void epilogue_rows(int lane, int wq, RowOffset row_of
 template <int BN, int COLS, int ESZ, bool QW32 = true>
 __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t taddr, int lane, int wq, int cb_begin,
                                                 int cb_end, int nt, int gi, int split, bool partial, bool add_bias,
-                                                bool do_gelu, uint8_t* stg, const long long (&roff)[EPI_MAX_LPR]) {
+                                                bool do_gelu, uint8_t* stg, const long long (&roff)[EPI_MAX_LPR],
+                                                const float* bsm = nullptr) {
     using S = EpiShape<COLS, ESZ>;
     constexpr int CW = S::CW;
     constexpr int RB = S::RB;
@@ -381,7 +382,7 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
             // bf16 bias: its loads go out before the TMEM load, so that their latencies overlap
             // (8-column groups past K read as zeros; those columns are never stored)
             uint4 bq[ESZ == 2 ? QW / 8 : 1];
-            if (ESZ == 2 && add_bias) {
+            if (ESZ == 2 && add_bias && !bsm) {
 #pragma unroll
                 for (int j = 0; j < QW / 8; ++j)
                     bq[j] = nq + 8 * j < g.K ? __ldg(reinterpret_cast<const uint4*>(
@@ -396,7 +397,17 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
             float f[QW];
 #pragma unroll
             for (int e = 0; e < QW; ++e) f[e] = __uint_as_float(v[e]);
-            if (ESZ == 2 && add_bias) {
+            if (ESZ == 2 && add_bias && bsm) {
+                // the warp's bias columns, already fp32 in shared memory (one broadcast read per
+                // 4 columns)
+                const float4* bp = reinterpret_cast<const float4*>(bsm + (cb - cb_begin) + QW * q);
+#pragma unroll
+                for (int j = 0; j < QW / 4; ++j) {
+                    const float4 b = bp[j];
+                    add2(f[4 * j], f[4 * j + 1], b.x, b.y);
+                    add2(f[4 * j + 2], f[4 * j + 3], b.z, b.w);
+                }
+            } else if (ESZ == 2 && add_bias) {
 #pragma unroll
                 for (int j = 0; j < QW / 8; ++j) {
                     const uint32_t bw[4] = {bq[j].x, bq[j].y, bq[j].z, bq[j].w};

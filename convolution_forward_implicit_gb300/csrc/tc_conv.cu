@@ -72,6 +72,23 @@ struct Cfg {
     static constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;    // power of two for BN in {16..256}
 };
 
+// Shared memory of one configuration: 1 KB alignment slack, the ring, the epilogue staging,
+// then (16 epilogue warps with bf16 outputs, where it fits) each epilogue warp's bias columns
+// in fp32, then the barriers.  With 16 warps every lane of a warp needs the same bias values,
+// so the warp converts its columns once per tile instead of each lane once per output.
+template <int BN, int STAGES, int KIND, int EW>
+struct Smem {
+    static constexpr size_t LIMIT = 232448;
+    static constexpr size_t RING = (size_t)STAGES * (Traits<KIND, EW>::A_STAGE + Cfg<BN, KIND>::B_STAGE);
+    static constexpr size_t STG = (size_t)EW * STG_WARP_BYTES;
+    static constexpr size_t BARS = 8 * (3 * STAGES + 5) + 16;
+    static constexpr size_t BIAS_NEED = (size_t)16 * BN;   // EW warps x BN/(EW/4) columns x 4 bytes
+    static constexpr bool BIAS_SMEM =
+        EW == 16 && KIND == KIND_BF16_TMA && 1024 + RING + STG + BIAS_NEED + BARS <= LIMIT;
+    static constexpr size_t BIAS_BYTES = BIAS_SMEM ? BIAS_NEED : 0;
+    static constexpr size_t TOTAL = 1024 + RING + STG + BIAS_BYTES + BARS;
+};
+
 template <int BN, int STAGES, int KIND, int EW>
 __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
     conv_fwd_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map) {
@@ -86,8 +103,10 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
     uint8_t* smem = smem_raw + (sbase - raw);
     const uint32_t sA = sbase;
     const uint32_t sB = sbase + STAGES * T::A_STAGE;
+    using SM = Smem<BN, STAGES, KIND, EW>;
     constexpr uint32_t STG_OFFSET = STAGES * (T::A_STAGE + C::B_STAGE);       // epilogue staging
-    const uint32_t bar0 = sbase + STG_OFFSET + EW * STG_WARP_BYTES;
+    constexpr uint32_t BIAS_OFFSET = STG_OFFSET + EW * STG_WARP_BYTES;        // fp32 bias columns
+    const uint32_t bar0 = sbase + BIAS_OFFSET + (uint32_t)SM::BIAS_BYTES;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto cvt_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
@@ -438,6 +457,23 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
             long long roff[EPI_MAX_LPR];
             if (wide) epilogue_rows<COLS, 4>(lane, wq, row_offset, roff);
             else epilogue_rows<COLS, 2>(lane, wq, row_offset, roff);
+            float* bsm = nullptr;
+            if (SM::BIAS_SMEM && add_bias) {
+                // this warp's bias columns of tile nt in fp32 (columns past K as zeros, never
+                // stored); the warp's previous tile has finished reading them
+                bsm = reinterpret_cast<float*>(smem + BIAS_OFFSET) + warp * COLS;
+                const __nv_bfloat16* bias = reinterpret_cast<const __nv_bfloat16*>(p.bias) + (size_t)gi * g.K;
+                for (int c = 2 * lane; c < cb_end - cb_begin; c += 64) {
+                    const int n = nt * BN + cb_begin + c;
+                    float2 bf = make_float2(0.f, 0.f);
+                    if (n < g.K) {
+                        const uint32_t w2 = __ldg(reinterpret_cast<const unsigned int*>(bias + n));
+                        bf = make_float2(__uint_as_float(w2 << 16), __uint_as_float(w2 & 0xFFFF0000u));
+                    }
+                    *reinterpret_cast<float2*>(bsm + c) = bf;
+                }
+                __syncwarp();
+            }
             if (!wait_bar_warp(tfull_bar(acc), aph, abort_flag, p.err, (p.sleep_mask & 2) != 0)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
@@ -446,7 +482,7 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                                        do_gelu, stg, roff);
             else
                 epilogue_chunks<BN, COLS, 2, EW == 8>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
-                                       do_gelu, stg, roff);
+                                       do_gelu, stg, roff, bsm);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -530,8 +566,7 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
 
 template <int BN, int STAGES, int KIND, int EW>
 constexpr size_t smem_bytes_for() {
-    return 1024 + (size_t)STAGES * (Traits<KIND, EW>::A_STAGE + Cfg<BN, KIND>::B_STAGE) + EW * STG_WARP_BYTES +
-           8 * (3 * STAGES + 5) + 16;
+    return Smem<BN, STAGES, KIND, EW>::TOTAL;
 }
 
 template <int BN, int STAGES, int KIND, int EW>
