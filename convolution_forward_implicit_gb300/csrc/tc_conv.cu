@@ -338,9 +338,7 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                             mma_tf32(d_tmem, ad + 2u * k, bd + 2u * k, IDESC, 1u);
                         }
                     } else {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)   // 4 x K=16 = 64 bf16 = one 128-byte row; +32 B each
-                            mma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                        mma_bf16_k4(d_tmem, ad, bd, IDESC, kb > kb0 ? 1u : 0u);   // 4 x K=16 = one 128-byte row
                     }
                     mma_commit(empty_bar(s));
                 }
