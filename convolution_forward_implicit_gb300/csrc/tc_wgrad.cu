@@ -196,12 +196,14 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
                 // plane pairs (A, B): hi*hi only, or the six that carry fp32 accuracy
                 constexpr int NP = PL == 1 ? 1 : 6;
                 constexpr int PA[6] = {0, 0, 1, 0, 2, 1}, PB[6] = {0, 1, 0, 2, 0, 1};
+                // plane and K-step offsets move only the descriptors' start-address field
+                const uint64_t da = sw128_mn_desc(a, HALF_BYTES), db = sw128_mn_desc(b, HALF_BYTES);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
 #pragma unroll
                     for (int q = 0; q < NP; ++q)
-                        mma_bf16_warp(tmem, sw128_mn_desc(a + PA[q] * W::A_PLANE + k * 2048, HALF_BYTES),
-                                      sw128_mn_desc(b + PB[q] * W::B_PLANE + k * 2048, HALF_BYTES), IDESC,
+                        mma_bf16_warp(tmem, da + (uint64_t)((PA[q] * W::A_PLANE + k * 2048) >> 4),
+                                      db + (uint64_t)((PB[q] * W::B_PLANE + k * 2048) >> 4), IDESC,
                                       (st > 0 || c > 0 || k > 0 || q > 0) ? 1u : 0u);
             }
             mma_commit_warp(empty_bar(s));
@@ -226,21 +228,39 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
             const long long col0 = (long long)tap * g.C + c;
             const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16);
             for (int cb = 0; cb < BN; cb += 16) {
-                if (nt * BN + cb >= p.pack * g.K) break;   // warp-uniform
+                const int k0 = nt * BN + cb;
+                if (k0 >= p.pack * g.K) break;   // warp-uniform
                 uint32_t v[16];
                 __syncwarp();
                 tmem_ld16(taddr + (uint32_t)cb, v);
                 tmem_ld_wait();
                 if (!row_ok) continue;
+                if (p.pack == 1) {
+                    // columns k0 .. k0+15 (those below K) of row (tap, c): element e at offset
+                    // e * NJ from the first; the warp's 32 rows are 32 consecutive c
+                    const int ne = g.K - k0 < 16 ? g.K - k0 : 16;
+                    const long long o0 = ((long long)grp * g.K + k0) * NJ + col0;
+                    if (p.splits > 1 || PL == 3) {
+                        float* w = (p.splits > 1 ? p.ws + (long long)split * g.G * g.K * NJ
+                                                 : reinterpret_cast<float*>(p.dw)) + o0;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (e < ne) w[e * NJ] = __uint_as_float(v[e]);
+                    } else {
+                        __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(p.dw) + o0;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (e < ne) w[e * NJ] = __float2bfloat16_rn(__uint_as_float(v[e]));
+                    }
+                    continue;
+                }
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    int k = nt * BN + cb + e;
-                    if (p.pack > 1) {   // column -> (group of the pack, channel); keep the diagonal block
+                    int k = k0 + e;
+                    {   // packed groups: column -> (group of the pack, channel); keep the diagonal block
                         const int b = k / g.K;
                         if (b != a) continue;
                         k -= b * g.K;
-                    } else if (k >= g.K) {
-                        break;
                     }
                     const long long o = ((long long)grp * g.K + k) * NJ + col0;
                     const float f = __uint_as_float(v[e]);
@@ -383,21 +403,29 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
                 albo[a] = o[1] - o[0];
             }
         }
+        // Descriptors of stage 0 built once; a stage, a K step (2048 bytes) and the stage
+        // offset move only the start-address field (address / 16, 14 bits: no carry within
+        // shared memory), so the issue loop adds to them instead of rebuilding them (measured:
+        // building every descriptor in the loop left the MMA thread at ~120 cycles per MMA).
+        uint64_t ad0[WG_SLAB_MAX_NA];
+#pragma unroll
+        for (int a = 0; a < WG_SLAB_MAX_NA; ++a) ad0[a] = sw128_mn_desc(sbase + aoff[a], albo[a]);
+        const uint64_t bd0 = sw128_mn_desc(sbase + dy_off, HALF_BYTES);
         bool ok = true;
         for (int st = 0; st < nchunks && ok; ++st) {
             const int s = st % S;
             ok = wait_bar_warp(full_bar(s), (st / S) & 1, abort_flag, p.err);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t base = sbase + (uint32_t)s * stage_bytes;
+            const uint64_t sd = (uint64_t)(((uint32_t)s * stage_bytes) >> 4);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const uint64_t bd = sw128_mn_desc(base + dy_off + k * 2048, HALF_BYTES);
+                const uint64_t kd = sd + (uint64_t)(k * (2048 >> 4));
+                const uint64_t bd = bd0 + kd;
 #pragma unroll
                 for (int a = 0; a < WG_SLAB_MAX_NA; ++a)
                     if (a < p.na)
-                        mma_bf16_warp(tmem + (uint32_t)(a * BN), sw128_mn_desc(base + aoff[a] + k * 2048, albo[a]), bd,
-                                      IDESC, (st > 0 || k > 0) ? 1u : 0u);
+                        mma_bf16_warp(tmem + (uint32_t)(a * BN), ad0[a] + kd, bd, IDESC, (st > 0 || k > 0) ? 1u : 0u);
             }
             mma_commit_warp(empty_bar(s));
         }
@@ -421,22 +449,37 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
                 const long long col0 = (long long)tap * g.C + c;
                 const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(a * BN);
                 for (int cb = 0; cb < BN; cb += 16) {
-                    if (nt * BN + cb >= p.pack * g.K) break;   // warp-uniform
+                    const int k0 = nt * BN + cb;
+                    if (k0 >= p.pack * g.K) break;   // warp-uniform
                     uint32_t v[16];
                     __syncwarp();
                     tmem_ld16(taddr + (uint32_t)cb, v);
                     tmem_ld_wait();
                     if (!row_ok) continue;
+                    if (p.pack == 1) {
+                        // columns k0 .. k0+15 (those below K) of row (tap, c): element e at
+                        // offset e * NJ from the first; the warp's 32 rows are 32 consecutive c
+                        const int ne = g.K - k0 < 16 ? g.K - k0 : 16;
+                        const long long o0 = ((long long)grp * g.K + k0) * NJ + col0;
+                        if (p.splits > 1) {
+                            float* w = p.ws + (long long)split * g.G * g.K * NJ + o0;
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                if (e < ne) w[e * NJ] = __uint_as_float(v[e]);
+                        } else {
+                            __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(p.dw) + o0;
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                if (e < ne) w[e * NJ] = __float2bfloat16_rn(__uint_as_float(v[e]));
+                        }
+                        continue;
+                    }
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        int k = nt * BN + cb + e;
-                        if (p.pack > 1) {
-                            const int b = k / g.K;
-                            if (b != pa) continue;
-                            k -= b * g.K;
-                        } else if (k >= g.K) {
-                            break;
-                        }
+                        int k = k0 + e;
+                        const int b = k / g.K;   // packed groups: keep the diagonal block
+                        if (b != pa) continue;
+                        k -= b * g.K;
                         const long long o = ((long long)grp * g.K + k) * NJ + col0;
                         const float f = __uint_as_float(v[e]);
                         if (p.splits > 1)
