@@ -357,3 +357,19 @@ def test_every_plan_description_is_key_value_pairs(lib):
                 finally:
                     B.conv_plan_destroy(h)
                 assert all(len(kv.split("=", 1)) == 2 for kv in d.split()), d
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the built library every entry point raises: there is no CPU or PyTorch fallback."""
+    import subprocess
+    import sys
+    code = ("from convolution_forward_implicit_gb300 import binding as B\n"
+            "try:\n"
+            "    B.conv_plan_create(1, 1, 1, 80, 384, [3000], [3], [1], [1], [1], B.CONV_BF16, B.CONV_EPI_BIAS)\n"
+            "except RuntimeError as e:\n"
+            "    print('raised:', 'not built' in str(e))\n")
+    env = dict(os.environ, CONVFWD_LIBRARY=str(tmp_path / "absent" / "libconvfwd.so"))
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                         timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "raised: True", out.stdout + out.stderr
