@@ -28,8 +28,10 @@
  * output, the oracle returns S = sum |x*w| over the receptive field, the
  * scale of the per-element error bound.
  *
- * Parallelism: independent output rows are split across pthreads; each output
- * is still one plain loop, so the arithmetic does not depend on the thread count.
+ * Parallelism: independent output pixels are split across pthreads (a conv1d has
+ * a single output row per sample, so rows alone would leave one thread); each
+ * output is still one plain loop, so the arithmetic does not depend on the thread
+ * count.
  */
 #include <math.h>
 #include <pthread.h>
@@ -108,23 +110,24 @@ typedef struct {
     const float *x, *w, *bias;
     int gelu;
     double *out, *absum;
-    int64_t row_begin, row_end;   /* rows = (n, od, oh) */
+    int64_t pix_begin, pix_end;   /* output pixels (n, od, oh, ow), flattened */
 } job;
 
-static void* run_rows(void* arg)
+static void* run_pixels(void* arg)
 {
     job* j = (job*)arg;
     const oracle_geom* g = j->g;
-    for (int64_t r = j->row_begin; r < j->row_end; ++r) {
-        int64_t oh = r % g->Ho, t = r / g->Ho;
+    for (int64_t q = j->pix_begin; q < j->pix_end; ++q) {
+        int64_t ow = q % g->Wo, t = q / g->Wo;
+        int64_t oh = t % g->Ho;
+        t /= g->Ho;
         int64_t od = t % g->Do, n = t / g->Do;
-        for (int64_t ow = 0; ow < g->Wo; ++ow)
-            for (int64_t gi = 0; gi < g->G; ++gi)
-                for (int64_t k = 0; k < g->K; ++k) {
-                    int64_t e = ((r * g->Wo + ow) * g->G + gi) * g->K + k;
-                    one_output(g, j->x, j->w, j->bias, j->gelu, n, od, oh, ow, gi, k,
-                               &j->out[e], j->absum ? &j->absum[e] : NULL);
-                }
+        for (int64_t gi = 0; gi < g->G; ++gi)
+            for (int64_t k = 0; k < g->K; ++k) {
+                int64_t e = (q * g->G + gi) * g->K + k;
+                one_output(g, j->x, j->w, j->bias, j->gelu, n, od, oh, ow, gi, k,
+                           &j->out[e], j->absum ? &j->absum[e] : NULL);
+            }
     }
     return NULL;
 }
@@ -141,18 +144,18 @@ int oracle_conv_fwd(const int64_t* params, const float* x, const float* w, const
     if (fill_geom(&g, params)) return -1;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
-    int64_t rows = g.N * g.Do * g.Ho;
-    if (nthreads > rows) nthreads = (int)rows;
+    int64_t pixels = g.N * g.Do * g.Ho * g.Wo;
+    if (nthreads > pixels) nthreads = (int)pixels;
     pthread_t th[256];
     job jobs[256];
     for (int i = 0; i < nthreads; ++i) {
         jobs[i].g = &g; jobs[i].x = x; jobs[i].w = w; jobs[i].bias = bias; jobs[i].gelu = gelu;
         jobs[i].out = out; jobs[i].absum = absum;
-        jobs[i].row_begin = rows * i / nthreads;
-        jobs[i].row_end = rows * (i + 1) / nthreads;
+        jobs[i].pix_begin = pixels * i / nthreads;
+        jobs[i].pix_end = pixels * (i + 1) / nthreads;
     }
-    for (int i = 1; i < nthreads; ++i) pthread_create(&th[i], NULL, run_rows, &jobs[i]);
-    run_rows(&jobs[0]);
+    for (int i = 1; i < nthreads; ++i) pthread_create(&th[i], NULL, run_pixels, &jobs[i]);
+    run_pixels(&jobs[0]);
     for (int i = 1; i < nthreads; ++i) pthread_join(th[i], NULL);
     return 0;
 }
@@ -265,22 +268,23 @@ typedef struct {
     const oracle_geom* g;
     const float *a, *b;     /* dx: dy, w;  dw: x, dy */
     double *out, *absum;
-    int64_t begin, end;     /* dx: rows (n, id, ih);  dw: (g, k) pairs */
+    int64_t begin, end;     /* dx: input pixels (n, id, ih, iw);  dw: (g, k) pairs */
 } bwd_job;
 
-static void* run_dx_rows(void* arg)
+static void* run_dx_pixels(void* arg)
 {
     bwd_job* j = (bwd_job*)arg;
     const oracle_geom* g = j->g;
-    for (int64_t r = j->begin; r < j->end; ++r) {
-        int64_t ih = r % g->H, t = r / g->H;
+    for (int64_t q = j->begin; q < j->end; ++q) {
+        int64_t iw = q % g->W, t = q / g->W;
+        int64_t ih = t % g->H;
+        t /= g->H;
         int64_t id = t % g->D, n = t / g->D;
-        for (int64_t iw = 0; iw < g->W; ++iw)
-            for (int64_t gi = 0; gi < g->G; ++gi)
-                for (int64_t c = 0; c < g->C; ++c) {
-                    int64_t e = ((r * g->W + iw) * g->G + gi) * g->C + c;
-                    one_dx(g, j->a, j->b, n, id, ih, iw, gi, c, &j->out[e], j->absum ? &j->absum[e] : NULL);
-                }
+        for (int64_t gi = 0; gi < g->G; ++gi)
+            for (int64_t c = 0; c < g->C; ++c) {
+                int64_t e = (q * g->G + gi) * g->C + c;
+                one_dx(g, j->a, j->b, n, id, ih, iw, gi, c, &j->out[e], j->absum ? &j->absum[e] : NULL);
+            }
     }
     return NULL;
 }
@@ -310,7 +314,7 @@ static int run_bwd(const int64_t* params, const float* a, const float* b, double
     if (fill_geom(&g, params)) return -1;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
-    int64_t rows = weight ? g.G * g.K : g.N * g.D * g.H;
+    int64_t rows = weight ? g.G * g.K : g.N * g.D * g.H * g.W;
     if (nthreads > rows) nthreads = (int)rows;
     pthread_t th[256];
     bwd_job jobs[256];
@@ -319,7 +323,7 @@ static int run_bwd(const int64_t* params, const float* a, const float* b, double
         jobs[i].begin = rows * i / nthreads;
         jobs[i].end = rows * (i + 1) / nthreads;
     }
-    void* (*fn)(void*) = weight ? run_dw_pairs : run_dx_rows;
+    void* (*fn)(void*) = weight ? run_dw_pairs : run_dx_pixels;
     for (int i = 1; i < nthreads; ++i) pthread_create(&th[i], NULL, fn, &jobs[i]);
     fn(&jobs[0]);
     for (int i = 1; i < nthreads; ++i) pthread_join(th[i], NULL);
