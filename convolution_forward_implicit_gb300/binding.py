@@ -22,7 +22,7 @@ __all__ = [
     "conv_plan_create", "conv_plan_output_shape", "conv_prepacked_weight_bytes", "conv_workspace_bytes",
     "conv_plan_set_workspace", "conv_prepack_weights", "conv_fwd", "conv_plan_check", "conv_plan_destroy",
     "conv_status_string", "conv_plan_describe", "conv_plan_flops", "ConvPlan", "EXPORTED",
-    "conv_fwd_static_scratch", "CONV_STATIC_SCRATCH_BYTES", "conv_plan_set_overlap",
+    "conv_fwd_static_scratch", "conv_static_scratch_bytes", "conv_plan_set_overlap",
 ]
 
 CONV_OK, CONV_ERR_INVALID_ARG, CONV_ERR_UNSUPPORTED, CONV_ERR_ALIGNMENT = 0, 1, 2, 3
@@ -52,6 +52,7 @@ _SIGS = {
     "conv_plan_describe": (ctypes.c_char_p, [_VP]),
     "conv_plan_flops": (ctypes.c_double, [_VP]),
     "conv_fwd_static_scratch": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP]),
+    "conv_static_scratch_bytes": (ctypes.c_size_t, []),
     "conv_plan_set_overlap": (ctypes.c_int, [_VP, ctypes.c_int]),
     "conv_bwd_data_plan_create": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                                  ctypes.c_int64, ctypes.c_int64, _I64P, _I64P, _I64P, _I64P, _I64P,
@@ -67,7 +68,6 @@ _SIGS = {
     "conv_tune_table_load": (ctypes.c_int, [ctypes.c_char_p]),
     "conv_tune_table_clear": (ctypes.c_int, []),
 }
-CONV_STATIC_SCRATCH_BYTES = 16 << 20
 EXPORTED = tuple(_SIGS)
 
 
@@ -176,9 +176,14 @@ def conv_fwd(plan: int, x_ptr: int, w_packed_ptr: int, bias_ptr: int, y_ptr: int
 
 def conv_fwd_static_scratch(plan: int, x_ptr: int, w_packed_ptr: int, bias_ptr: int, y_ptr: int, stream: int = 0):
     """conv_fwd for callers that cannot allocate: split-K scratch lives in the library's
-    own device array (CONV_STATIC_SCRATCH_BYTES); see include/conv.h."""
+    own device array (conv_static_scratch_bytes() of them); see include/conv.h."""
     _check(load_library().conv_fwd_static_scratch(plan, x_ptr, w_packed_ptr, bias_ptr or None, y_ptr,
                                                   stream or None), "conv_fwd_static_scratch")
+
+
+def conv_static_scratch_bytes() -> int:
+    """Size in bytes of the library's own device array that conv_fwd_static_scratch uses."""
+    return int(load_library().conv_static_scratch_bytes())
 
 
 def conv_plan_check(plan: int, stream: int = 0):

@@ -1650,6 +1650,8 @@ extern "C" conv_status conv_fwd_static_scratch(conv_plan_t plan, const void* x, 
 
 extern "C" {
 
+size_t conv_static_scratch_bytes(void) { return sizeof(g_static_scratch); }
+
 double conv_plan_flops(conv_plan_t plan) { return plan ? plan->flops : 0.0; }
 
 }  // extern "C"

@@ -21,9 +21,16 @@
  *   bias   G*K
  * Output size per spatial dimension: O = floor((I + 2*pad - dil*(F-1) - 1) / stride) + 1.
  *
- * Arithmetic: fp32 I/O is computed in fp32 (FFMA, no TF32); bf16 I/O multiplies bf16
- * on the tensor cores and accumulates in fp32; the epilogue (bias, GELU) runs in fp32
- * and the bf16 output is rounded once, to nearest even.
+ * Arithmetic: bf16 I/O multiplies bf16 on the tensor cores (tcgen05) and accumulates
+ * in fp32.  fp32 I/O runs by default on the tensor cores as 3xTF32: each operand splits
+ * into a TF32 high part and an fp32 remainder, and lo*hi + hi*lo + hi*hi are accumulated
+ * in fp32; what it drops (lo*lo, and the low bits of lo that TF32 does not carry) is
+ * below 2^-20 |x*w| per term (both splits truncate), so the result stays within 1e-5 of
+ * sum |x*w|, the bound an fp32 FFMA sum meets.  The FFMA kernel (plain fp32) takes the
+ * problems no tensor-core plan can express (channel counts that are not multiples of 8
+ * for bf16 or of 4 for fp32, fp32 inputs the TMA gather cannot address) and plans forced
+ * onto it.  The epilogue (bias, GELU) runs in fp32 and a bf16 output is rounded once, to
+ * nearest even.
  *
  * Conventions for every call:
  *  - Ownership: the caller allocates and frees every device buffer (x, w, w_packed,
@@ -83,8 +90,11 @@ typedef struct conv_plan* conv_plan_t;
  *   spatial   ndim input extents, outermost first (D, H, W)
  *   filter    ndim filter extents (Z, Y, X)
  *   stride, pad, dilation   ndim values each; stride >= 1, pad >= 0, dilation >= 1
- * bf16 problems with C and K multiples of 8 run on the tensor cores; other bf16
- * problems and all fp32 problems run on the FFMA kernel.
+ * bf16 problems with C and K multiples of 8 run on the tensor cores (kind::f16); fp32
+ * problems with C and K multiples of 4 whose input the TMA gather can address run on the
+ * tensor cores as 3xTF32 (kind::tf32, three products per useful product); everything
+ * else runs on the FFMA kernel.  conv_plan_describe names the choice ("variant=tc_bf16",
+ * "tc_tf32x3", "simt_bf16" or "simt_f32").
  * Returns CONV_ERR_INVALID_ARG for a bad argument or an empty output,
  * CONV_ERR_UNSUPPORTED when an index would overflow the kernels' 32-bit coordinates.  The plan queries the current
  * device's SM count; without a device it plans for 152 SMs.  *out is set only on CONV_OK.
@@ -94,13 +104,21 @@ conv_status conv_plan_create(conv_plan_t* out, int ndim, int64_t N, int64_t G, i
                              const int64_t* pad, const int64_t* dilation, conv_dtype dtype,
                              conv_epilogue epilogue);
 
-/* Output extents (ndim values, outermost first) into out_spatial. */
+/* Output extents (ndim values, outermost first) into out_spatial: per dimension
+ * O = floor((I + 2*pad - dil*(F-1) - 1) / stride) + 1, the size that gives the page's
+ * printed lengths 3000 (k3 s1 p1) and 1500 (k3 s2 p1) from L = 3000 (page "[ET-VK]
+ * conv1d ...", "Measurements").  out_spatial: caller-owned host array of ndim int64.
+ * CONV_ERR_INVALID_ARG on a NULL plan or array. */
 conv_status conv_plan_output_shape(conv_plan_t plan, int64_t* out_spatial);
 
 /* Bytes of the prepacked weight buffer that conv_prepack_weights writes (0 on a NULL plan). */
 size_t conv_prepacked_weight_bytes(conv_plan_t plan);
 
-/* Bytes of device workspace conv_fwd needs (0 unless the plan splits the reduction). */
+/* Bytes of device workspace conv_fwd needs: 0 unless the plan splits the reduction over
+ * K and sums the partial sums in a second kernel (splits x M x G*K fp32 values); split
+ * plans whose splits share a thread-block cluster need none.  Split-K is the small-
+ * problem variant of page "onnxruntime PR #33639", "Description" (it fills the GPU
+ * better than large tiles).  0 on a NULL plan. */
 size_t conv_workspace_bytes(conv_plan_t plan);
 
 /*
@@ -121,11 +139,18 @@ conv_status conv_plan_set_workspace(conv_plan_t plan, void* workspace, size_t by
 conv_status conv_prepack_weights(conv_plan_t plan, const void* w, void* w_packed, void* stream);
 
 /*
- * The forward pass (the hot path).  x, w_packed (from conv_prepack_weights with the
- * same plan), bias (G*K values of the plan's dtype; required when the epilogue adds a
- * bias, ignored otherwise) and y are device pointers; y must not overlap x.
- * Enqueues the kernel(s) on `stream` and returns; launch errors come back as
- * CONV_ERR_CUDA.  Plans that split the reduction need a workspace set first.
+ * The forward pass (the hot path): the operation at the top of this file, computed as an
+ * implicit GEMM whose activation tiles are gathered from x with no im2col matrix in
+ * memory (page "[ET-VK] conv1d ...", "The conv2d path already solves this": conv as
+ * im2col + GEMM; page "composable_kernel ... LEARNINGS_GROUPED_CONV.md", introduction:
+ * NHWGC x GKYXC -> NHWGK).  x, w_packed (from conv_prepack_weights with the same plan),
+ * bias (G*K values of the plan's dtype; required when the epilogue adds a bias, ignored
+ * otherwise) and y are device pointers; y must not overlap x.  Enqueues the kernel(s)
+ * on `stream` and returns; launch errors come back as CONV_ERR_CUDA, a missing or small
+ * workspace as CONV_ERR_WORKSPACE, a NULL or backward plan or a missing bias as
+ * CONV_ERR_INVALID_ARG, a pointer off 16 bytes as CONV_ERR_ALIGNMENT; all of these are
+ * checked before anything is launched.  Plans that split the reduction need a workspace
+ * set first.  Each call encodes the activation tensor map for this x on the host.
  */
 conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, const void* bias, void* y,
                      void* stream);
@@ -133,7 +158,10 @@ conv_status conv_fwd(conv_plan_t plan, const void* x, const void* w_packed, cons
 /*
  * Synchronise `stream`, then read and clear the device error word.  Returns
  * CONV_ERR_TIMEOUT if a kernel abandoned a pipeline wait since the last check,
- * CONV_ERR_CUDA if the stream reports an error, CONV_OK otherwise.
+ * CONV_ERR_CUDA if the stream reports an error, CONV_OK otherwise.  (The pages have no
+ * counterpart: their dispatches report nothing; this is how the library's bounded waits
+ * surface instead of hanging a stream.)  The error word is one per device and shared by
+ * every plan, so a check after several plans' calls reports a timeout in any of them.
  */
 conv_status conv_plan_check(conv_plan_t plan, void* stream);
 
@@ -327,6 +355,10 @@ conv_status conv_tune_table_clear(void);
 #define CONV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 conv_status conv_fwd_static_scratch(conv_plan_t plan, const void* x, const void* w_packed, const void* bias,
                                     void* y, void* stream);
+
+/* The size of that array in the library as built (CONV_STATIC_SCRATCH_BYTES when the
+ * library and this header agree), so that a binding need not restate the constant. */
+size_t conv_static_scratch_bytes(void);
 
 #ifdef __cplusplus
 }

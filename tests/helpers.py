@@ -2,13 +2,14 @@
 same inputs, and compare under the per-element bound.
 
 Tolerance (the bound the conv path must meet, per output element):
-    |gpu - oracle| <= L * rel * S + 2 * u_out * |oracle| + g * B
+    |gpu - oracle| <= L * rel * S + u_out * |oracle| + g * B
   rel   = 1e-5 for fp32 I/O, 8e-3 for bf16 I/O (fp32 accumulation);
   S     = sum |x*w| over the receptive field (fp64, from the oracle);
   L     = 1.13 when a GELU follows (a bound on the slope of x*Phi(x)), else 1;
-  u_out = unit roundoff of the output type (2^-24 fp32, 2^-8 bf16): the single rounding
-          of the stored result, and the fp32 bias add / GELU evaluation, which S does not
-          scale because the bias is outside the sum;
+  u_out = unit roundoff of the output type (2^-24 fp32, 2^-8 bf16): the one round-to-
+          nearest-even of the stored result, which S does not scale (the bias is outside
+          the sum); the fp32 bias add itself costs 2^-24 relative, inside rel * S for
+          bf16 and inside the same term for fp32;
   g * B = with a GELU only: the erf-GELU's own evaluation error in fp32 (below 9.5e-7 |v|,
           g = 1e-6) on the bias part of the pre-activation v (B = 0.05, the bound of the test
           biases), which S does not scale either: it is all that is left where every tap of
@@ -42,7 +43,7 @@ BIAS_BOUND = 0.05         # |bias| of the test inputs
 def tolerance(dtype, epilogue, ref, S):
     gelu = epilogue in (CONV_EPI_BIAS_GELU, CONV_EPI_GELU)
     L = GELU_LIPSCHITZ if gelu else 1.0
-    return (L * rel_for(dtype) * S + 2.0 * uout_for(dtype) * np.abs(ref) +
+    return (L * rel_for(dtype) * S + uout_for(dtype) * np.abs(ref) +
             (GELU_EVAL * BIAS_BOUND if gelu else 0.0) + 1e-30)
 
 
@@ -123,18 +124,11 @@ def oracle_full(layer, dtype, x, w, b):
     return ref.reshape(-1), S.reshape(-1)
 
 
-def oracle_points(layer, dtype, x, w, b, flat_idx, y_shape):
-    g = geom_of(layer)
-    gelu = layer.epilogue in (CONV_EPI_BIAS_GELU, CONV_EPI_GELU)
-    bb = syn.as_f32(b, dtype) if (b is not None and has_bias(layer.epilogue)) else None
-    # y_shape is the caller's ndim form; the oracle indexes n, od, oh, ow, g, k
-    full_shape = g.y_shape()
-    coords = np.array(np.unravel_index(flat_idx, full_shape)).T
-    ref, S = oracle.conv_fwd_points(g, syn.as_f32(x, dtype), syn.as_f32(w, dtype), bb, gelu, coords)
-    return ref, S
-
-
-def assert_within(dtype, epilogue, got_storage, ref, S, what=""):
+def assert_within(dtype, epilogue, got_storage, ref, S, what="", stats=None):
+    """Checks every element against the bound above; returns (max err / bound, cosine).  With
+    a dict as stats it also records there the largest ratio against the bare rel * S term
+    alone (the stated bound before the output rounding and GELU terms) over the elements with
+    S > 0, and how many elements were compared."""
     got = syn.as_f32(got_storage, dtype).astype(np.float64).reshape(-1)
     tol = tolerance(dtype, epilogue, ref, S)
     err = np.abs(got - ref)
@@ -145,12 +139,8 @@ def assert_within(dtype, epilogue, got_storage, ref, S, what=""):
                              f"oracle={ref[i]!r} S={S[i]!r} tol={tol[i]!r}")
     ratio = float(np.max(err / tol)) if len(err) else 0.0
     cos = float(np.dot(got, ref) / (np.linalg.norm(got) * np.linalg.norm(ref) + 1e-300))
+    if stats is not None:
+        pos = S > 0
+        stats["bare_ratio"] = float(np.max(err[pos] / (rel_for(dtype) * S[pos]))) if pos.any() else 0.0
+        stats["elements"] = int(len(ref))
     return ratio, cos
-
-
-def sample_indices(total: int, n: int, seed: int) -> np.ndarray:
-    """n distinct pseudo-random flat indices plus the first and last elements."""
-    rng = np.random.default_rng(seed)
-    n = min(n, total)
-    idx = rng.choice(total, size=n, replace=False) if total > n else np.arange(total)
-    return np.unique(np.concatenate([idx, [0, total - 1]])).astype(np.int64)

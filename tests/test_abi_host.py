@@ -373,3 +373,29 @@ def test_missing_library_fails_loudly(tmp_path):
                          timeout=120)
     assert out.returncode == 0, out.stderr
     assert out.stdout.strip() == "raised: True", out.stdout + out.stderr
+
+
+def test_static_scratch_size_agrees_with_the_header(lib):
+    """The allocation-free entry point's array: the library reports the size the header states."""
+    src = open(os.path.join(ROOT, "include", "conv.h")).read()
+    m = re.search(r"#define\s+CONV_STATIC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", src)
+    assert m, "CONV_STATIC_SCRATCH_BYTES not found in include/conv.h"
+    assert B.conv_static_scratch_bytes() == int(m.group(1)) << int(m.group(2))
+
+
+@pytest.mark.parametrize("name,li,variant", [
+    ("whisper_frontend_f32", 0, "tc_tf32x3"), ("whisper_frontend_f32", 1, "tc_tf32x3"),
+    ("conv1d_f32_80to384_L3000", 0, "tc_tf32x3"), ("whisper_mlp_f32", 0, "tc_tf32x3"),
+    ("whisper_frontend_bf16", 0, "tc_bf16"), ("sweep_bf16_n32", 1, "tc_bf16"), ("grouped2d_g32_c8_d1", 0, "tc_bf16"),
+])
+def test_default_arithmetic_is_the_one_the_header_documents(lib, name, li, variant):
+    """include/conv.h: fp32 I/O runs as 3xTF32 on the tensor cores by default, bf16 I/O as
+    bf16 tensor-core products; the FFMA kernel takes only what the tensor-core plans cannot."""
+    layer = WORKLOADS[name].layers[li]
+    h = B.conv_plan_create(*layer.plan_args(WORKLOADS[name].dtype_code))
+    assert f"variant={variant} " in B.conv_plan_describe(h) + " "
+    B.conv_plan_destroy(h)
+    # channel counts the tensor-core plans cannot take fall back to the FFMA kernel
+    h = B.conv_plan_create(1, 1, 1, 3, 5, (40,), (3,), (1,), (1,), (1,), B.CONV_F32, B.CONV_EPI_BIAS)
+    assert "variant=simt_f32" in B.conv_plan_describe(h)
+    B.conv_plan_destroy(h)
