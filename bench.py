@@ -1,10 +1,13 @@
 """Benchmark: useful TFLOP/s, % of roofline and us per call of the convolution forward pass.
 
-Default workload: the Whisper-tiny conv frontend at batch 1 (page "[ET-VK] conv1d runs at
-~3% of the GPU's matmul throughput ...", sections "Measurements" and "The conv2d path
-already solves this"): conv1d 80 -> 384 k3 s1 p1 on L=3000 + GELU, then conv1d 384 -> 384
-k3 s2 p1 + GELU, in fp32 and in bf16.  One step runs all four layers through the C-ABI.
-Useful FLOPs = 2 x MACs, padded taps counted (the page's convention).
+Default workload: the conv1d bf16 frontend sweep at batch 32, the largest configuration
+that the metric is quoted on: conv1d 128 -> 1280 k3 s1 p1 on L=3000 + GELU, then conv1d
+1280 -> 1280 k3 s2 p1 (L 3000 -> 1500) + GELU, 566 GFLOP per step.  One step runs both
+layers through the C-ABI.  Useful FLOPs = 2 x MACs, padded taps counted (the convention of
+page "[ET-VK] conv1d runs at ~3% of the GPU's matmul throughput ...", "Measurements").
+The same run also measures every other configuration (the 80 -> 384 fp32 conv1d, the
+Whisper-tiny frontend in fp32 and bf16, the sweep at batch 1 and 8, the grouped 2D and 3D
+layers) and reports each one's us per call and roofline fraction under `per_config`.
 
 Timing: W warm-up steps, then exactly K steps between CUDA events on the launching stream,
 bracketed by a barrier and a device synchronise.  A step is one CUDA graph holding every
@@ -15,10 +18,13 @@ this off).  Each layer's device time comes from a second run of the same steps w
 events recorded inside the graph between the layers (where PyTorch cannot record events
 inside a graph, each layer is its own graph and the events sit between them).  Steps
 rotate over enough copies of every input, packed weight and output that one rotation
-exceeds twice the L2 cache, so no step finds its data in L2.
+exceeds twice the L2 cache, so no step finds its data in L2.  `eager` times the same
+layers called from the host one by one (no graph): each call validates its arguments and
+encodes the activation tensor map before it launches.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
-                  [--no-overlap] [--serial] [--pass fwd|bwd] [--tune ITERS] [--source-hash]
+                  [--configs all|none|NAME,...] [--no-overlap] [--serial] [--pass fwd|bwd]
+                  [--tune ITERS] [--source-hash]
 
 --tune ITERS lets the measured selector (conv_plan_tune) time every candidate plan of each
 layer before the run and keep the fastest; by default the planner's rules choose.  The step's
@@ -28,7 +34,8 @@ backward pass (--serial / --parallel override).
 
 Under torchrun each rank runs an independent replica on its own GPU (the forward pass
 has no exchange step); rank 0 prints the JSON line with the max time over ranks.
---impl reference times the CPU oracle (fp64 direct loops) on the host cores instead.
+--impl reference times the CPU oracle (fp64 direct loops) on the host cores instead, with
+the same sampling method as the `cpu_baseline` field of our own line.
 """
 from __future__ import annotations
 
@@ -72,7 +79,26 @@ def workload_description(name):
     if name == "whisper_mlp":
         return ("whisper_tiny_encoder_mlp as 1x1 convs: 384->1536 +bias +GELU, 1536->384 +bias over 1500 "
                 "positions, batch 1, fp32 and bf16 I/O")
+    if name.startswith("sweep_bf16_n"):
+        n = name[len("sweep_bf16_n"):]
+        return (f"conv1d_bf16_frontend_sweep batch {n}: conv1d 128->1280 k3 s1 p1 L=3000 +GELU, conv1d "
+                f"1280->1280 k3 s2 p1 (L 3000->1500) +GELU, bf16 I/O")
+    from convolution_forward_implicit_gb300.workloads import WORKLOADS
+    wl = WORKLOADS.get(name)
+    if wl is not None:
+        L = wl.layers[0]
+        sp = "x".join(str(v) for v in L.spatial)
+        fl = "x".join(str(v) for v in L.filter)
+        dl = "x".join(str(v) for v in L.dilation)
+        return wl.note or (f"{name}: {L.ndim}D grouped conv N={L.N} {sp} G={L.G} C=K={L.C} filter {fl} "
+                           f"dilation {dl} {wl.dtype}")
     return name
+
+
+# every configuration the metric is quoted on (the per_config table of the JSON line)
+BASELINE_CONFIGS = ["conv1d_f32_80to384_L3000", "whisper_frontend_f32", "whisper_frontend_bf16", "sweep_bf16_n1",
+                    "sweep_bf16_n8", "sweep_bf16_n32", "grouped2d_g8_c64_d1", "grouped2d_g8_c64_d2",
+                    "grouped2d_g32_c8_d1", "grouped2d_g32_c8_d2", "grouped3d_g4_c64_d1", "grouped3d_g4_c64_d2"]
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -331,10 +357,15 @@ def setup_bwd_layers(wls, R):
 
 
 def np_y_shape(layer):
-    import oracle
-    g = oracle.Geom(layer.N, layer.G, layer.C, layer.K, layer.spatial, layer.filter, layer.stride, layer.pad,
-                    layer.dilation)
-    return (layer.N, *g.out_spatial[3 - layer.ndim:], layer.G, layer.K)
+    """The layer's output shape (N, spatial..., G, K), from the library's own size formula."""
+    from convolution_forward_implicit_gb300.binding import (conv_plan_create, conv_plan_destroy,
+                                                            conv_plan_output_shape)
+    h = conv_plan_create(*layer.plan_args(0))
+    try:
+        out = conv_plan_output_shape(h, layer.ndim)
+    finally:
+        conv_plan_destroy(h)
+    return (layer.N, *out, layer.G, layer.K)
 
 
 def rotation_sets(wls, factor=1.0):
@@ -405,13 +436,11 @@ def capture_steps(runs, R, with_events, parallel=False):
     return graphs, events
 
 
-def run_ours(args, ws, rank, local):
+def prepare(args, wls, bwd=False):
+    """Plans, rotating buffers and step graphs of the workloads.  Returns a dict with the
+    runs, the host inputs and output sets (for the end-to-end leg), the step graphs and the
+    graphs (or per-layer graphs) that time each layer."""
     import torch
-    torch.cuda.set_device(local)
-    import __graft_entry__
-    __graft_entry__.build()
-    wls = frontend_workloads(args.workload)
-    bwd = args.pass_ == "bwd"
     R, per_set = rotation_sets(wls, 2.0 if bwd else 1.0)
     if bwd:
         runs, host_in, out_sets = setup_bwd_layers(wls, R)
@@ -422,7 +451,6 @@ def run_ours(args, ws, rank, local):
         for lr in runs:
             last[lr.wl.name] = lr
         out_sets = [lr.y_sets for lr in last.values()]
-    stream = torch.cuda.current_stream()
     if args.overlap:
         for lr in runs:
             lr.plan.set_overlap(True)
@@ -440,34 +468,44 @@ def run_ours(args, ws, rank, local):
             lr.capture(R)
         layer_graphs, gev = None, None
         graph_mode = "one graph per step; per-layer times from one graph per layer with events between graphs"
+    torch.cuda.synchronize()
+    return {"R": R, "per_set": per_set, "runs": runs, "host_in": host_in, "out_sets": out_sets,
+            "step_graphs": step_graphs, "layer_graphs": layer_graphs, "gev": gev, "graph_mode": graph_mode}
 
-    K = args.steps
+
+def time_steps(st, K, W, stream, ws=1, on_start=None):
+    """W warm-up steps, then K steps of the step graphs between CUDA events (barrier and
+    synchronise on both sides); returns the total ms (max over ranks by the caller)."""
+    import torch
+    R, graphs = st["R"], st["step_graphs"]
+    for i in range(W):
+        graphs[i % R].replay()
+    torch.cuda.synchronize()
+    for lr in st["runs"]:
+        lr.plan.check()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if on_start:
+        on_start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(K):
+        graphs[i % R].replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    return e0.elapsed_time(e1)
+
+
+def time_layers(st, K, W, stream):
+    """Per-layer device times (ms) over K steps after W warm-up steps: the mean, and the
+    samples behind it (one per step, or the last replay of each rotation set)."""
+    import torch
+    R, runs, layer_graphs, gev = st["R"], st["runs"], st["layer_graphs"], st["gev"]
     nL = len(runs)
     ev = None if layer_graphs is not None else [[torch.cuda.Event(enable_timing=True) for _ in range(nL + 1)]
                                                 for _ in range(K)]
-
-    def step(i):
-        step_graphs[i % R].replay()
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    for lr in runs:
-        lr.plan.check()
-
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local).start()
-    barrier(ws)
-    torch.cuda.synchronize()
-    e_start.record(stream)
-    for i in range(K):
-        step(i)
-    e_end.record(stream)
-    torch.cuda.synchronize()
-    barrier(ws)
-    total_ms = e_start.elapsed_time(e_end)
-    # per-layer device times over the same number of steps (warm-up first)
-    for i in range(args.warmup):
+    for i in range(W):
         if layer_graphs is not None:
             layer_graphs[i % R].replay()
     torch.cuda.synchronize()
@@ -481,12 +519,90 @@ def run_ours(args, ws, rank, local):
                 ev[i][j + 1].record(stream)
     torch.cuda.synchronize()
     if ev is None:
-        # the last replay of every rotation set's graph
         last = sorted({i % R: i for i in range(K)}.keys())
         samples = [[gev[r][j].elapsed_time(gev[r][j + 1]) for r in last] for j in range(nL)]
     else:
         samples = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)] for j in range(nL)]
-    per_layer_ms = [sum(v) / len(v) for v in samples]
+    return [sum(v) / len(v) for v in samples], samples
+
+
+def time_eager(st, K, W, stream):
+    """The layers called from the host, one conv_fwd per layer per step with no graph: the
+    device time per step (CUDA events) and the host time per call (Python wall clock around
+    the calls: ctypes marshalling, argument checks, the tensor-map encode and the launch)."""
+    import torch
+    R, runs = st["R"], st["runs"]
+    for i in range(W):
+        for lr in runs:
+            lr.call(i % R)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    t0 = time.perf_counter()
+    for i in range(K):
+        for lr in runs:
+            lr.call(i % R)
+    host_s = time.perf_counter() - t0
+    e1.record(stream)
+    torch.cuda.synchronize()
+    for lr in runs:
+        lr.plan.check()
+    ms = e0.elapsed_time(e1) / K
+    return ms, host_s * 1e6 / (K * len(runs))
+
+
+def release(st):
+    import torch
+    st.clear()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def per_config_table(args, names, stream, done=None):
+    """Every configuration in `names`, each measured the way the headline is (rotating
+    buffers larger than twice the L2, one graph per step, per-layer events): us per step and
+    per layer, useful TFLOP/s and each layer's roofline fraction."""
+    K, W = min(args.steps, 50), max(3, min(args.warmup, 5))
+    table = {}
+    for name in names:
+        if done is not None and name in done:
+            table[name] = done[name]
+            continue
+        st = prepare(args, frontend_workloads(name))
+        ms = time_steps(st, K, W, stream) / K
+        per_layer_ms, _ = time_layers(st, K, W, stream)
+        runs = st["runs"]
+        flops = sum(lr.flops for lr in runs)
+        table[name] = config_entry(runs, ms, per_layer_ms, K)
+        release(st)
+    return table
+
+
+def config_entry(runs, ms, per_layer_ms, K):
+    flops = sum(lr.flops for lr in runs)
+    layers = {}
+    for lr, t in zip(runs, per_layer_ms):
+        roof = roofline_for(lr, t)
+        layers[lr.name()] = {"us_per_call": round(t * 1e3, 3), "tflops": round(lr.flops / (t * 1e-3) / 1e12, 2),
+                             "roofline_frac": roof["frac"], "bound": roof["bound"], "plan": lr.plan.describe()}
+    return {"us_per_step": round(ms * 1e3, 3), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+            "gflop_per_step": round(flops / 1e9, 3), "steps": K, "layers": layers}
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    wls = frontend_workloads(args.workload)
+    bwd = args.pass_ == "bwd"
+    stream = torch.cuda.current_stream()
+    st = prepare(args, wls, bwd)
+    runs, R, per_set = st["runs"], st["R"], st["per_set"]
+    K = args.steps
+    clocks = ClockSampler(local)
+    total_ms = time_steps(st, K, args.warmup, stream, ws, on_start=clocks.start)
+    per_layer_ms, samples = time_layers(st, K, args.warmup, stream)
     layer_samples = len(samples[0]) if samples else 0
     layer_spread = {lr.name(): {"median": round(float(np.median(v)) * 1e3, 3),
                                 "p10": round(float(np.percentile(v, 10)) * 1e3, 3),
@@ -495,8 +611,8 @@ def run_ours(args, ws, rank, local):
     t_end = time.time() + 1.5
     i = 0
     while time.time() < t_end:
-        for _ in range(200):
-            step(i)
+        for _ in range(50):
+            st["step_graphs"][i % R].replay()
             i += 1
         torch.cuda.synchronize()
     clk = clocks.stop()
@@ -509,13 +625,14 @@ def run_ours(args, ws, rank, local):
     value = ws * step_flops / (ms_per_step * 1e-3) / 1e12
 
     # ---- hot L2 (the same rotation set every step) and the latency of one isolated step
+    g0 = st["step_graphs"][0]
     for i in range(args.warmup):
-        step_graphs[0].replay()
+        g0.replay()
     torch.cuda.synchronize()
     eh0, eh1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     eh0.record(stream)
     for i in range(K):
-        step_graphs[0].replay()
+        g0.replay()
     eh1.record(stream)
     torch.cuda.synchronize()
     hot_ms = eh0.elapsed_time(eh1) / K
@@ -524,7 +641,7 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        step(i)
+        st["step_graphs"][i % R].replay()
         a1.record(stream)
         torch.cuda.synchronize()
         singles.append(a0.elapsed_time(a1) * 1e3)
@@ -534,8 +651,19 @@ def run_ours(args, ws, rank, local):
               "p90_us": round(float(np.percentile(singles, 90)), 3), "samples": len(singles),
               "note": "one step between a device synchronize and events: launch latency included"}
 
+    # ---- the same layers called from the host, no graph
+    eager = None
+    if not bwd:
+        e_ms, host_us = time_eager(st, min(K, 50), args.warmup, stream)
+        eager = {"us_per_step": round(e_ms * 1e3, 3), "value": round(ws * step_flops / (e_ms * 1e-3) / 1e12, 4),
+                 "unit": "TFLOP/s", "host_us_per_call": round(host_us, 3), "steps": min(K, 50),
+                 "note": "conv_fwd called from Python per layer per step, no graph: argument checks, the "
+                         "activation tensor-map encode and the launch on the host every call"}
+
     # ---- end to end: pinned host inputs in, final outputs back to pinned host memory
-    e2e = run_e2e(args, runs, host_in, out_sets, R, stream, ws, local, step)
+    def step(i):
+        st["step_graphs"][i % R].replay()
+    e2e = run_e2e(args, runs, st["host_in"], st["out_sets"], R, stream, ws, local, step)
 
     # ---- roofline of the dominant kernel
     dom = int(np.argmax(per_layer_ms))
@@ -559,7 +687,7 @@ def run_ours(args, ws, rank, local):
                    "pass": "backward (data + weight)" if bwd else "forward",
                    "l2": f"inputs larger than L2: {R} rotating sets of activations, packed weights and outputs "
                          f"(~{R * per_set / 1e6:.0f} MB per rotation, L2 129 MB)",
-                   "graphs": graph_mode,
+                   "graphs": st["graph_mode"],
                    "overlap": bool(args.overlap),
                    "selector": (f"measured (conv_plan_tune, {args.tune} timed calls per candidate)" if args.tune
                                 else "rules"),
@@ -573,6 +701,17 @@ def run_ours(args, ws, rank, local):
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if eager is not None:
+        line["eager"] = eager
+    headline = config_entry(runs, ms_per_step, per_layer_ms, K) if not bwd else None
+    release(st)
+    names = [] if bwd or args.configs == "none" else (
+        BASELINE_CONFIGS if args.configs == "all" else [n for n in args.configs.split(",") if n])
+    if names:
+        clocks_cfg = ClockSampler(local).start()
+        done = {args.workload: headline} if args.workload in names else None
+        line["per_config"] = per_config_table(args, names, stream, done)
+        line["per_config_clocks"] = clocks_cfg.stop()
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline_bwd(wls) if bwd else cpu_baseline(wls)
         print(json.dumps(line), flush=True)
@@ -712,6 +851,10 @@ def measured_traffic(desc):
     return None
 
 
+TRAFFIC_NOTE = ("DRAM bytes read + written while the kernel runs (ncu dram__bytes_read.sum + dram__bytes_write.sum, "
+                "one launch); outputs still in L2 when it ends are written back later and are not in this count")
+
+
 def roofline_for(lr, ms):
     """Roofline of one layer's kernel: the slower of its compute pipe and HBM bytes."""
     peaks, src = measured_peaks()
@@ -743,18 +886,20 @@ def roofline_for(lr, ms):
     if flops / pipe >= byts / hbm:
         ach = flops / t_s / 1e12
         return {"bound": bound_c, "achieved": round(ach, 4), "peak": round(unit_peak, 2), "unit": "TFLOP/s",
-                "frac": round(ach / unit_peak, 4), "traffic": measured_traffic(desc), "kernel": lr.name(),
-                "plan": desc, "peak_source": note, "algorithmic_flops": flops, "algorithmic_bytes": byts}
+                "frac": round(ach / unit_peak, 4), "traffic": measured_traffic(desc), "traffic_note": TRAFFIC_NOTE,
+                "kernel": lr.name(), "plan": desc, "peak_source": note, "algorithmic_flops": flops,
+                "algorithmic_bytes": byts}
     ach = byts / t_s / 1e9
     return {"bound": "hbm", "achieved": round(ach, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": measured_traffic(desc), "kernel": lr.name(), "plan": desc,
+            "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": measured_traffic(desc), "traffic_note": TRAFFIC_NOTE,
+            "kernel": lr.name(), "plan": desc,
             "peak_source": f"HBM copy bandwidth, {src}", "algorithmic_flops": flops, "algorithmic_bytes": byts}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def _oracle_layer_time(wl, li, layer, x, w, b, nthreads, sample_frac=1.0, seed=0):
-    """Time the oracle on one layer (whole output, or a sample of outputs split over threads).
-    Returns (seconds, useful flops computed)."""
+def _oracle_layer_sample(wl, layer, x, w, b, nthreads, frac, seed):
+    """Time the oracle on a random sample (a fraction frac, at least one per thread) of one
+    layer's outputs, split over nthreads host threads.  Returns (seconds, useful flops)."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
     from convolution_forward_implicit_gb300 import synthetic as syn
@@ -765,49 +910,66 @@ def _oracle_layer_time(wl, li, layer, x, w, b, nthreads, sample_frac=1.0, seed=0
     xf, wf = syn.as_f32(x, wl.dtype), syn.as_f32(w, wl.dtype)
     bf = syn.as_f32(b, wl.dtype) if (b is not None and layer.epilogue in (CONV_EPI_BIAS, CONV_EPI_BIAS_GELU)) else None
     total = int(np.prod(g.y_shape()))
-    per_out = 2.0 * layer.C * layer.taps
-    if sample_frac >= 1.0:
-        t = time.perf_counter()
-        out, _ = oracle.conv_fwd(g, xf, wf, bf, gelu=gelu, nthreads=nthreads)
-        return time.perf_counter() - t, per_out * total, out
-    n = max(1, int(total * sample_frac))
+    n = min(total, max(nthreads, int(total * frac)))
     idx = np.random.default_rng(seed).choice(total, size=n, replace=False)
     coords = np.array(np.unravel_index(idx, g.y_shape())).T.astype(np.int64)
     chunks = np.array_split(coords, nthreads)
     t = time.perf_counter()
     with ThreadPoolExecutor(nthreads) as ex:
         list(ex.map(lambda c: oracle.conv_fwd_points(g, xf, wf, bf, gelu, c), chunks))
-    return time.perf_counter() - t, per_out * n, None
+    return time.perf_counter() - t, 2.0 * layer.C * layer.taps * n
 
 
-def cpu_baseline(wls, budget_flops=30e9):
-    """The oracle as it stands on the host cores: one whole step of the workload (every
-    layer, each reading the oracle's own previous output, rounded to the I/O type) when the
-    step is at most budget_flops of useful work (about 10 s on 16 cores); otherwise the same
-    fraction of every layer's outputs, sampled at random (later layers then read a fresh
-    N(0,1) draw: the oracle's speed does not depend on the values)."""
+def oracle_inputs(wls):
+    """(workload, layer, x, w, bias) of every layer; layers after the first read a fresh
+    N(0,1) draw (the oracle's speed does not depend on the values)."""
     from convolution_forward_implicit_gb300 import synthetic as syn
     from convolution_forward_implicit_gb300.workloads import gen_inputs
-    nthreads = os.cpu_count() or 1
-    total = sum(2.0 * int(np.prod(np_y_shape(l))) * l.C * l.taps for wl in wls for l in wl.layers)
-    frac = min(1.0, budget_flops / total)
-    secs, flops = 0.0, 0.0
+    data = []
     for wl in wls:
         x, params = gen_inputs(wl)
-        cur = x
         for li, layer in enumerate(wl.layers):
-            w, b = params[li]
-            if frac < 1.0 and li > 0:
-                cur = syn.gen_normal(7 + li, layer.x_shape(), wl.dtype)
-            dt, fl, out = _oracle_layer_time(wl, li, layer, cur, w, b, nthreads, sample_frac=frac, seed=li)
-            secs += dt
-            flops += fl
-            if out is not None:
-                cur = syn.to_storage(out.reshape(-1), wl.dtype)
-    what = ("one full step (every layer, whole output)" if frac >= 1.0 else
-            f"a random {frac:.2%} of every layer's outputs")
+            xin = x if li == 0 else syn.gen_normal(7 + li, layer.x_shape(), wl.dtype)
+            data.append((wl, layer, xin, params[li][0], params[li][1]))
+    return data
+
+
+def oracle_step_flops(data):
+    import oracle
+    total = 0.0
+    for (wl, layer, _, _, _) in data:
+        g = oracle.Geom(layer.N, layer.G, layer.C, layer.K, layer.spatial, layer.filter, layer.stride, layer.pad,
+                        layer.dilation)
+        total += 2.0 * g.macs()
+    return total
+
+
+def oracle_sample(data, frac, seed, nthreads):
+    """The one CPU-baseline method, used by the cpu_baseline field and by --impl reference:
+    the oracle as it stands on a random fraction frac of every layer's outputs, each layer's
+    sample split evenly over nthreads threads.  Returns (seconds, useful flops)."""
+    secs, flops = 0.0, 0.0
+    for li, (wl, layer, x, w, b) in enumerate(data):
+        dt, fl = _oracle_layer_sample(wl, layer, x, w, b, nthreads, frac, seed * 100 + li)
+        secs += dt
+        flops += fl
+    return secs, flops
+
+
+CPU_BASELINE_FLOPS = 150e9      # the cpu_baseline sample: ~5-15 s on 16 cores
+REFERENCE_STEP_FLOPS = 3e9      # one --impl reference step
+
+
+def cpu_baseline(wls):
+    """The oracle timed on the host cores, on a bounded random sample of the workload's
+    outputs (the method of --impl reference, with a larger sample)."""
+    data = oracle_inputs(wls)
+    nthreads = os.cpu_count() or 1
+    frac = min(1.0, CPU_BASELINE_FLOPS / oracle_step_flops(data))
+    secs, flops = oracle_sample(data, frac, 0, nthreads)
     return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-            "sample": f"{what}, {flops / 1e9:.2f} GFLOP in {secs:.2f} s"}
+            "sample": f"a random {frac:.2%} of every layer's outputs, split over {nthreads} threads (fp64 direct "
+                      f"loops; the method of --impl reference): {flops / 1e9:.2f} GFLOP in {secs:.2f} s"}
 
 
 def cpu_baseline_bwd(wls, budget_flops=4e9):
@@ -849,40 +1011,23 @@ def cpu_baseline_bwd(wls, budget_flops=4e9):
 
 
 def run_reference(args, ws, rank, local):
-    """The oracle as the reference arm: each step evaluates a fixed random sample of each
-    layer's outputs (1/32 of them) on all host cores; throughput counts the sampled FLOPs."""
+    """The oracle as the reference arm: each step evaluates a fresh random sample of each
+    layer's outputs (about REFERENCE_STEP_FLOPS of useful work per step) on all host cores,
+    by the same method as the cpu_baseline field; throughput counts the sampled FLOPs."""
     if rank != 0:
         return
-    from convolution_forward_implicit_gb300 import synthetic as syn
-    from convolution_forward_implicit_gb300.workloads import gen_inputs
     import oracle
     oracle.build()
     wls = frontend_workloads(args.workload)
     nthreads = os.cpu_count() or 1
-    data = []
-    for wl in wls:
-        x, params = gen_inputs(wl)
-        for li, layer in enumerate(wl.layers):
-            # the oracle's speed does not depend on the values: later layers read a fresh N(0,1) draw
-            xin = x if li == 0 else syn.gen_normal(7 + li, layer.x_shape(), wl.dtype)
-            data.append((wl, li, layer, xin, params[li][0], params[li][1]))
-    frac = 1.0 / 32
-
-    def ref_step(seed):
-        secs, flops = 0.0, 0.0
-        for (wl, li, layer, xin, w, b) in data:
-            dt, fl, _ = _oracle_layer_time(wl, li, layer, xin, w, b, nthreads, sample_frac=frac, seed=seed)
-            secs += dt
-            flops += fl
-        return secs, flops
-
+    data = oracle_inputs(wls)
+    frac = min(1.0, REFERENCE_STEP_FLOPS / oracle_step_flops(data))
     for i in range(args.warmup):
-        ref_step(i)
-    tot_s, tot_f = 0.0, 0.0
+        oracle_sample(data, frac, 1 + i, nthreads)
+    tot_f = 0.0
     t0 = time.perf_counter()
     for i in range(args.steps):
-        s, f = ref_step(1000 + i)
-        tot_s += s
+        _, f = oracle_sample(data, frac, 1000 + i, nthreads)
         tot_f += f
     wall = time.perf_counter() - t0
     value = tot_f / wall / 1e12
@@ -893,7 +1038,8 @@ def run_reference(args, ws, rank, local):
             "data": "synthetic", "config": {"workload": workload_description(args.workload),
                                             "parallelism": "host threads"},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-                             "sample": f"each step: a fixed random 1/32 of every layer's outputs, fp64 direct loops"},
+                             "sample": f"each step: a fresh random {frac:.3%} of every layer's outputs split over "
+                                       f"{nthreads} threads, fp64 direct loops (the cpu_baseline method)"},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -904,7 +1050,10 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="whisper_frontend")
+    ap.add_argument("--workload", default="sweep_bf16_n32")
+    ap.add_argument("--configs", default="all",
+                    help="per_config table: 'all' (every configuration the metric is quoted on), 'none', or a "
+                         "comma-separated list of workload names")
     ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash and exit")
     ap.add_argument("--no-overlap", dest="overlap", action="store_false",
                     help="launch each layer only after the previous one completes (no programmatic dependents)")
