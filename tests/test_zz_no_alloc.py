@@ -28,16 +28,17 @@ def _plan(layer, dtype_code, env=None):
                 os.environ[k] = v
 
 
-SPLIT3 = Layer(1, 1, 1, 128, 128, (700,), (3,), (2,), (1,), (1,), B.CONV_EPI_BIAS_GELU, 0.05)
+SPLIT = Layer(1, 1, 1, 128, 128, (700,), (3,), (2,), (1,), (1,), B.CONV_EPI_BIAS_GELU, 0.05)
 # (name, dtype, layer, plan overrides, whether the plan must use the array)
 CASES = [
     ("whisper_l2_bf16", "bf16", WORKLOADS["whisper_frontend_bf16"].layers[1], None, False),
-    ("whisper_l2_f32", "f32", WORKLOADS["whisper_frontend_f32"].layers[1], None, False),
-    ("split3_bf16", "bf16", SPLIT3, {"CONV_FORCE_SPLITK": 3}, False),
+    ("whisper_l2_f32_cluster", "f32", WORKLOADS["whisper_frontend_f32"].layers[1], None, False),
+    ("split2_bf16_cluster", "bf16", SPLIT, {"CONV_FORCE_SPLITK": 2}, False),
     ("unsplit_2d_bf16", "bf16", Layer(2, 1, 2, 32, 40, (19, 23), (3, 3), (1, 1), (1, 1), (1, 1), B.CONV_EPI_BIAS,
                                       0.05), {"CONV_FORCE_SPLITK": 1}, False),
     # split-K partial sums through the reduction kernel: these write and read the array
-    ("split3_bf16_reduce_kernel", "bf16", SPLIT3, {"CONV_FORCE_SPLITK": 3, "CONV_FORCE_CLUSTER_RED": 0}, True),
+    ("split3_bf16", "bf16", SPLIT, {"CONV_FORCE_SPLITK": 3}, True),   # 3 splits cannot share out 128 rows
+    ("split2_bf16_reduce_kernel", "bf16", SPLIT, {"CONV_FORCE_SPLITK": 2, "CONV_FORCE_CLUSTER_RED": 0}, True),
     ("whisper_l2_f32_reduce_kernel", "f32", WORKLOADS["whisper_frontend_f32"].layers[1],
      {"CONV_FORCE_CLUSTER_RED": 0}, True),
     ("simt_split4_f32", "f32", Layer(2, 1, 3, 12, 20, (11, 14), (3, 3), (1, 1), (1, 1), (1, 1), B.CONV_EPI_BIAS_GELU,
