@@ -294,10 +294,11 @@ struct PlanChoice {
     int slab_pair = -1;    // 0 / 1: slab tile pairs off / on
     int epi_warps = 0;     // 8 or 16 epilogue warps in the per-tap kernel
     int cluster_red = -1;  // 0: split-K partials through the reduction kernel, not a cluster
+    int mc = -1;           // 0 / 1: CTA pairs sharing weight tiles by multicast off / on
     bool operator==(const PlanChoice& o) const {
         return simt == o.simt && no_pack == o.no_pack && bn == o.bn && bm == o.bm && splits == o.splits &&
                gather == o.gather && slab_stream == o.slab_stream && slab_pair == o.slab_pair &&
-               epi_warps == o.epi_warps && cluster_red == o.cluster_red;
+               epi_warps == o.epi_warps && cluster_red == o.cluster_red && mc == o.mc;
     }
 };
 
@@ -319,6 +320,7 @@ struct conv_plan {
     int overlap;            // launch as programmatic dependents (conv_plan_set_overlap)
     int epi_warps;          // per-tap kernel epilogue warps (8 or 16)
     int cluster_red;        // split-K partials summed inside a cluster (no workspace, no reduce kernel)
+    int mc;                 // CTA pairs share each weight tile by multicast (units are pairs of M tiles)
     size_t slab_smem;
     // SIMT plan
     int BM, Kg, Kpad, nkt, ktps, vec;
@@ -373,6 +375,7 @@ static bool choice_from_env(PlanChoice& c) {
     take("CONV_FORCE_SLAB_PAIR", c.slab_pair);
     take("CONV_FORCE_EPI_WARPS", c.epi_warps);
     take("CONV_FORCE_CLUSTER_RED", c.cluster_red);
+    take("CONV_FORCE_MC", c.mc);
     if (const char* v = getenv("CONV_FORCE_GATHER")) {
         if (strcmp(v, "cpasync") == 0) { c.gather = 1; any = true; }
         else if (strcmp(v, "tma") == 0) { c.gather = 2; any = true; }
@@ -684,6 +687,27 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
         g.K % 4 == 0 && p->ch.cluster_red != 0)
         p->cluster_red = 1;
     p->workspace_bytes = (p->splits > 1 && !p->cluster_red) ? (size_t)p->splits * g.M * g.G * g.K * sizeof(float) : 0;
+    // Weight multicast (bf16 per-tap TMA plans, N tiles of 128 or 256, no split): CTA pairs
+    // compute M tiles 2j and 2j+1 of the same (group, N tile) together and read each weight
+    // tile from L2 once per pair.  Only on request (the measured selector or CONV_FORCE_MC):
+    // measured on the 128 -> 1280 -> 1280 conv1d layers at batch 32 the pairs' lockstep costs
+    // more than the halved weight reads save (L1 105 -> 114 us, L2 309 -> 320 us).
+    p->mc = 0;
+    if (!tf32 && p->tma && !p->slab && p->splits == 1 && !p->cluster_red && bn >= 128 && p->num_mt >= 2 &&
+        p->ch.mc == 1) {
+        int clusters = p->sm_count / 2;
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) {
+            const int n = tc_mc_max_clusters(bn, p->epi_warps);
+            if (n > 0) clusters = std::min(clusters, n);
+        }
+        cudaGetLastError();
+        if (clusters >= 1) {
+            p->mc = 1;
+            p->total_units = (int)(cdiv(p->num_mt, 2) * g.G * p->num_nt);
+            p->grid = 2 * std::min(p->total_units, clusters);
+        }
+    }
     if (p->slab)
         snprintf(p->desc, sizeof(p->desc),
                  "variant=%s gather=tma-slab tile=%dx%d pixels=%dx%d slab=%dx%d k_block=%d stages=%d+%d%s splits=1 "
@@ -694,10 +718,10 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     else if (p->tma)
         snprintf(p->desc, sizeof(p->desc),
                  "variant=%s gather=tma tile=128x%d pixels=%dx%d k_block=%d stages=%d splits=%d units=%d "
-                 "grid=%d k_blocks=%d map=%d epi_warps=%d reduce=%s",
+                 "grid=%d k_blocks=%d map=%d epi_warps=%d reduce=%s%s",
                  tf32 ? "tc_tf32x3" : "tc_bf16", bn, p->BH, p->BW, cblk, p->stages, p->splits, p->total_units,
                  p->grid, p->nkb, p->map_kind, p->epi_warps,
-                 p->splits == 1 ? "none" : p->cluster_red ? "cluster" : "kernel");
+                 p->splits == 1 ? "none" : p->cluster_red ? "cluster" : "kernel", p->mc ? " weights=multicast2" : "");
     else
         snprintf(p->desc, sizeof(p->desc),
                  "variant=tc_bf16 gather=cp.async tile=128x%d k_block=64 stages=%d splits=%d units=%d grid=%d "
@@ -743,7 +767,7 @@ static void choose_variant(conv_plan* p) {
     Geom& g = p->g;
     const int64_t G = p->Go, C = p->Co, K = p->Ko;
     g.G = (int)G; g.C = (int)C; g.K = (int)K;
-    p->pack = 1; p->slab = 0; p->tma = 0; p->cluster_red = 0; p->epi_warps = 8; p->splits = 1;
+    p->pack = 1; p->slab = 0; p->tma = 0; p->cluster_red = 0; p->mc = 0; p->epi_warps = 8; p->splits = 1;
     // bf16 with C, K multiples of 8: tcgen05 kind::f16.  fp32 with C, K multiples of 4 that the
     // TMA gather can express: tcgen05 3xTF32.  Everything else: the FFMA kernel.
     const bool no_tc = p->ch.simt != 0;
@@ -823,6 +847,12 @@ static std::vector<conv_plan> tune_candidates(const conv_plan* p) {
                 c.bn = bn; c.splits = sp; c.gather = ga;
                 cs.push_back(c);
             }
+    for (int bn : {128, 256})      // wide unsplit tiles with and without weight multicast
+        for (int mc : {0, 1}) {
+            PlanChoice c;
+            c.bn = bn; c.splits = 1; c.mc = mc;
+            cs.push_back(c);
+        }
     PlanChoice f;
     f.simt = 1;
     cs.push_back(f);
@@ -1419,6 +1449,7 @@ static conv_status run_forward(conv_plan_t plan, const void* x, const void* w_pa
         tp.pdl = plan->overlap;
         tp.epi_warps = plan->epi_warps ? plan->epi_warps : 8;
         tp.cluster_red = plan->cluster_red;
+        tp.mc = plan->tma && !plan->slab ? plan->mc : 0;
         // outputs land on the plan's lattice only where the kernel writes final values; partial
         // sums (split-K through the reduction kernel) are indexed by GEMM row
         const bool partial = plan->splits > 1 && !plan->cluster_red;
@@ -1747,9 +1778,9 @@ conv_status conv_tune_table_save(const char* path) {
     for (const auto& kv : g_tune_table) {
         const PlanChoice& c = kv.second.c;
         fprintf(f, "%s | simt=%d no_pack=%d bn=%d bm=%d splits=%d gather=%d slab_stream=%d slab_pair=%d epi_warps=%d "
-                   "cluster_red=%d",
+                   "cluster_red=%d mc=%d",
                 kv.first.c_str(), c.simt, c.no_pack, c.bn, c.bm, c.splits, c.gather, c.slab_stream, c.slab_pair,
-                c.epi_warps, c.cluster_red);
+                c.epi_warps, c.cluster_red, c.mc);
         if (kv.second.us >= 0.0) fprintf(f, " | us=%.3f", kv.second.us);
         fputc('\n', f);
         // the measurements behind the choice, as comment lines (ignored by the loader)
@@ -1771,11 +1802,14 @@ conv_status conv_tune_table_load(const char* path) {
         char* bar = strstr(line, " | ");
         TuneEntry te;
         PlanChoice& c = te.c;
-        if (!bar || sscanf(bar + 3,
-                           "simt=%d no_pack=%d bn=%d bm=%d splits=%d gather=%d slab_stream=%d slab_pair=%d "
-                           "epi_warps=%d cluster_red=%d",
-                           &c.simt, &c.no_pack, &c.bn, &c.bm, &c.splits, &c.gather, &c.slab_stream, &c.slab_pair,
-                           &c.epi_warps, &c.cluster_red) != 10) {
+        // (rows written before the mc field existed carry ten fields: mc stays with the rules)
+        int nf = bar ? sscanf(bar + 3,
+                              "simt=%d no_pack=%d bn=%d bm=%d splits=%d gather=%d slab_stream=%d slab_pair=%d "
+                              "epi_warps=%d cluster_red=%d mc=%d",
+                              &c.simt, &c.no_pack, &c.bn, &c.bm, &c.splits, &c.gather, &c.slab_stream, &c.slab_pair,
+                              &c.epi_warps, &c.cluster_red, &c.mc)
+                     : 0;
+        if (nf != 10 && nf != 11) {
             st = CONV_ERR_INVALID_ARG;
             break;
         }

@@ -159,6 +159,8 @@ struct TcParams {
     int epi_warps;          // per-tap kernel: 8 or 16 epilogue warps
     int cluster_red;        // 1: the splits of a tile run as one cluster and sum their partial
                             // accumulators through distributed shared memory (no workspace)
+    int mc;                 // 1 (per-tap bf16 TMA kernel, no split): CTA pairs share each weight tile
+                            // by multicast; units are pairs of M tiles (see conv_fwd_tc_kernel)
     Lattice lat;            // where the output pixels land in y (one phase of a strided backward data)
     int test_stall;         // test hook: the MMA role waits on a barrier nothing completes
     // divisors of the per-tile index arithmetic
@@ -170,6 +172,9 @@ constexpr size_t SLAB_SMEM_MAX = 232448;   // dynamic shared memory a block may 
 // Launch the tensor-core kernel for the (BN, stages) pair the plan picked (see tc_stages_for).
 cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, int stages, int grid, cudaStream_t stream);
 int tc_stages_for(int BN, int tf32, int epi_warps);
+// Clusters of two CTAs of the weight-multicast kernel for (BN, epi_warps) that can be resident at
+// once on the current device (0 if it cannot be queried).
+int tc_mc_max_clusters(int BN, int epi_warps);
 // Slab-mode kernel; smem from slab_smem_bytes.
 cudaError_t launch_slab(const TcParams& p, const CUtensorMap* act_map, int grid, size_t smem, cudaStream_t stream);
 size_t slab_smem_bytes(int BN, int tf32, int sa, int sb, size_t a_stage, int btaps);

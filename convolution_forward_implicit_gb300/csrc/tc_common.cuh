@@ -119,6 +119,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
+// The same copy written to every CTA of the cluster in `mask`, at the same shared-memory offset
+// in each, completing `bytes` of transaction count on the mbarrier at offset `bar` in each.
+__device__ __forceinline__ void bulk_g2s_multicast(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                                   uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "h"(mask)
+        : "memory");
+}
 
 // ---- tcgen05 ----
 __device__ __forceinline__ void tc_fence_before() {
@@ -159,6 +169,14 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint6
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+// Arrive once on the mbarrier at offset `bar` in every CTA of the cluster in `mask` when the
+// MMAs issued so far have completed.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
 }
 // Whole-warp forms: every lane runs the MMA role's loop with the same (warp-uniform)
 // descriptors and elect.sync picks the one lane that issues.  In a converged warp it is the

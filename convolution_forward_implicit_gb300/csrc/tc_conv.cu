@@ -89,11 +89,17 @@ struct Smem {
     static constexpr size_t TOTAL = 1024 + RING + STG + BIAS_BYTES + BARS;
 };
 
-template <int BN, int STAGES, int KIND, int EW>
+// MC: the CTAs run as clusters of two that compute the tiles 2j and 2j+1 along M of the same
+// (group, N tile) in lockstep; each loads one half of every weight tile and multicasts it to
+// both, so the pair reads each weight tile from L2 once instead of twice.  A stage is then
+// refilled only after the MMAs of both CTAs have released it (each CTA's commits arrive on
+// the empty barriers of both).
+template <int BN, int STAGES, int KIND, int EW, bool MC>
 __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
     conv_fwd_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map) {
     using C = Cfg<BN, KIND>;
     using T = Traits<KIND, EW>;
+    static_assert(!MC || KIND == KIND_BF16_TMA, "weight multicast is built for the bf16 TMA kernel");
     constexpr int RED_PITCH = BN + 4;   // floats per row of the cluster-reduction buffer
     static_assert((size_t)BM * RED_PITCH * 4 <= (size_t)STAGES * (T::A_STAGE + C::B_STAGE),
                   "the cluster-reduction buffer reuses the stage area");
@@ -123,7 +129,7 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), T::FULL_COUNT);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), MC ? 2 : 1);
             mbar_init(cvt_bar(s), T::CVT_WARPS > 0 ? T::CVT_WARPS : 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -145,12 +151,23 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the peer CTA's copies and commits reach this CTA's barriers only after both are set up
+    if (MC) cluster_sync_all();
     // set up: the next kernel on the stream may start (its own set-up and weight loads)
     if (p.pdl) griddep_launch();
 
     const Geom& g = p.g;
     const int GC = g.G * g.C;
     const int GK = g.G * g.K;
+    // units of this CTA: u0, u0 + ustep, ...; with MC a unit is a pair of M tiles (the CTA of
+    // cluster rank r takes tile 2 mt + r of it)
+    const uint32_t crank = MC ? cluster_ctarank() : 0u;
+    const int u0 = MC ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int ustep = MC ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    auto unit_tile = [&](int u, int& mt, int& gi, int& nt, int& split) {
+        decode_unit(p, u, mt, gi, nt, split);
+        if (MC) mt = 2 * mt + (int)crank;
+    };
 
     if (warp >= EW && warp < T::MMA_WARP) {
         const uint8_t* wp = reinterpret_cast<const uint8_t*>(p.wpack);
@@ -163,9 +180,11 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                 uint32_t it = 0, issued = 0;   // issued: 1 + the last iteration this warp loaded
                 bool aborted = false;
                 bool x_ready = !p.pdl;      // x may come from the previous kernel on the stream
-                for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x) {
+                for (int u = u0; u < p.total_units && !aborted; u += ustep) {
                     int mt, gi, nt, split;
-                    decode_unit(p, u, mt, gi, nt, split);
+                    unit_tile(u, mt, gi, nt, split);
+                    // (with MC the second tile of the last pair may lie past the output: its boxes
+                    // are then out of range and read zeros, and the epilogue stores nothing)
                     const TileOrigin to = tile_origin(p, mt);
                     const int kb0 = split * p.kbps;
                     const int kb1 = min(kb0 + p.kbps, p.nkb);
@@ -204,9 +223,25 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                                 tma_load_5d(sA + s * T::A_STAGE, &act_map, c0, gi, wi, hi, to.n, full_bar(s));
                         } else {
                             const size_t off = ((size_t)(gi * p.num_nt + nt) * p.nkb + kb) * C::B_STAGE;
-                            bulk_g2s(sB + s * C::B_STAGE, wp + off, C::B_STAGE, full_bar(s));
+                            if (MC) {
+                                // this CTA's half of the weight tile (BN/2 rows), to both CTAs
+                                constexpr uint32_t HALF = C::B_STAGE / 2;
+                                bulk_g2s_multicast(sB + s * C::B_STAGE + crank * HALF, wp + off + crank * HALF, HALF,
+                                                   full_bar(s), (uint16_t)0x3);
+                            } else {
+                                bulk_g2s(sB + s * C::B_STAGE, wp + off, C::B_STAGE, full_bar(s));
+                            }
                         }
                     }
+                }
+                if (MC && lane == 0) {
+                    // before the CTA may exit, every commit the peer's MMA role sends to this CTA's
+                    // empty barriers must have arrived: wait (bounded) for the phases that would
+                    // precede this warp's next STAGES refills
+                    for (uint32_t k = it; k < it + (uint32_t)STAGES; ++k)
+                        if ((int)((k % STAGES) % T::PROD_WARPS) == pw &&
+                            !wait_bar(empty_bar(k % STAGES), ((k / STAGES) & 1u) ^ 1u, abort_flag, p.err, false))
+                            break;
                 }
                 if (aborted && lane == 0) {
                     // before the CTA exits, the copies this warp issued into stages the MMA role never
@@ -308,9 +343,9 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
             // test hook: wait on a barrier nothing completes, so the bounded wait runs out and
             // the abort path (error word, drained copies, freed tensor memory) is exercised
             if (p.test_stall && !wait_bar(drain_bar, 0u, abort_flag, p.err, false)) aborted = true;
-            for (int u = blockIdx.x; u < p.total_units && !aborted; u += gridDim.x, ++tile_i) {
+            for (int u = u0; u < p.total_units && !aborted; u += ustep, ++tile_i) {
                 int mt, gi, nt, split;
-                decode_unit(p, u, mt, gi, nt, split);
+                unit_tile(u, mt, gi, nt, split);
                 const int kb0 = split * p.kbps;
                 const int kb1 = min(kb0 + p.kbps, p.nkb);
                 const int acc = tile_i & 1;
@@ -340,7 +375,8 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                     } else {
                         mma_bf16_k4(d_tmem, ad, bd, IDESC, kb > kb0 ? 1u : 0u);   // 4 x K=16 = one 128-byte row
                     }
-                    mma_commit(empty_bar(s));
+                    if (MC) mma_commit_multicast(empty_bar(s), (uint16_t)0x3);   // both CTAs' copy of the stage
+                    else mma_commit(empty_bar(s));
                 }
                 if (!aborted) mma_commit(tfull_bar(acc));
             }
@@ -408,9 +444,9 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
         uint8_t* stg = smem + STG_OFFSET + warp * STG_WARP_BYTES;
         if (p.pdl) griddep_wait();   // y, the workspace and bias may belong to the previous kernel
         uint32_t tile_i = 0;
-        for (int u = blockIdx.x; u < p.total_units; u += gridDim.x, ++tile_i) {
+        for (int u = u0; u < p.total_units; u += ustep, ++tile_i) {
             int mt, gi, nt, split;
-            decode_unit(p, u, mt, gi, nt, split);
+            unit_tile(u, mt, gi, nt, split);
             const int acc = tile_i & 1;
             const uint32_t aph = (tile_i >> 1) & 1u;
             TileOrigin to{0, 0, 0, 0};
@@ -422,7 +458,7 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                 if (T::TMA) {
                     const int rh = fdiv(rr, p.f_BW);
                     const int oh = to.oh0 + rh, ow = to.ow0 + (rr - rh * p.BW);
-                    if (rr >= p.BW * p.BH || oh >= g.Ho || ow >= g.Wo) return -1;
+                    if (rr >= p.BW * p.BH || oh >= g.Ho || ow >= g.Wo || (MC && to.n >= g.N)) return -1;
                     return (long long)lattice_pixel(p.lat, to.n, to.od, oh, ow) * GK;
                 }
                 const int m = mt * BM + rr;
@@ -556,6 +592,8 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    // no CTA of a pair leaves while the other may still copy into or arrive on its shared memory
+    if (MC) cluster_sync_all();
     if (warp == T::MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -567,9 +605,9 @@ constexpr size_t smem_bytes_for() {
     return Smem<BN, STAGES, KIND, EW>::TOTAL;
 }
 
-template <int BN, int STAGES, int KIND, int EW>
+template <int BN, int STAGES, int KIND, int EW, bool MC = false>
 cudaError_t launch_one(const TcParams& p, const CUtensorMap& map, int grid, cudaStream_t stream) {
-    auto kern = conv_fwd_tc_kernel<BN, STAGES, KIND, EW>;
+    auto kern = conv_fwd_tc_kernel<BN, STAGES, KIND, EW, MC>;
     constexpr size_t smem = smem_bytes_for<BN, STAGES, KIND, EW>();
     static_assert(smem <= 232448, "shared memory budget");
     // opt in to the large dynamic shared memory once per device (not inside graph capture)
@@ -584,7 +622,8 @@ cudaError_t launch_one(const TcParams& p, const CUtensorMap& map, int grid, cuda
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    return launch_kernel(kern, dim3(grid), dim3(Traits<KIND, EW>::THREADS), smem, stream, p.pdl != 0, p.cluster_red ? p.splits : 1, p, map);
+    return launch_kernel(kern, dim3(grid), dim3(Traits<KIND, EW>::THREADS), smem, stream, p.pdl != 0,
+                         MC ? 2 : p.cluster_red ? p.splits : 1, p, map);
 }
 
 }  // namespace
@@ -593,12 +632,48 @@ cudaError_t launch_one(const TcParams& p, const CUtensorMap& map, int grid, cuda
 #define TC_BF16_CONFIGS(X) X(256, 4) X(128, 6) X(64, 8) X(32, 8) X(16, 8)
 #define TC_BF16_EPI16_CONFIGS(X) X(256, 3) X(128, 5)
 #define TC_TF32_CONFIGS(X) X(256, 2) X(128, 3) X(64, 4) X(32, 4) X(16, 5)
+// weight multicast (bf16, 8 or 16 epilogue warps at the stage counts above)
+#define TC_BF16_MC_CONFIGS(X) X(256, 4, 8) X(128, 6, 8) X(256, 3, 16) X(128, 5, 16)
 
 int tc_stages_for(int BN, int tf32, int epi_warps) {
 #define X(bn, st) if (BN == bn) return st;
     if (tf32) { TC_TF32_CONFIGS(X) }
     else if (epi_warps == 16) { TC_BF16_EPI16_CONFIGS(X) }
     else { TC_BF16_CONFIGS(X) }
+#undef X
+    return 0;
+}
+
+int tc_mc_max_clusters(int BN, int epi_warps) {
+    const int st = tc_stages_for(BN, 0, epi_warps);
+    auto query = [&](auto kern, size_t smem, int threads) -> int {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        return n;
+    };
+#define X(bn, stg, ew)                                                                                  \
+    if (BN == bn && st == stg && epi_warps == ew)                                                       \
+        return query(conv_fwd_tc_kernel<bn, stg, KIND_BF16_TMA, ew, true>, smem_bytes_for<bn, stg, KIND_BF16_TMA, ew>(), \
+                     Traits<KIND_BF16_TMA, ew>::THREADS);
+    TC_BF16_MC_CONFIGS(X)
 #undef X
     return 0;
 }
@@ -612,6 +687,16 @@ cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, int stages,
 #define X(bn, st) \
     if (p.BN == bn && stages == st) return launch_one<bn, st, KIND_TF32X3, 8>(p, map, grid, stream);
         TC_TF32_CONFIGS(X)
+#undef X
+        return cudaErrorInvalidValue;
+    }
+    if (p.mc) {
+        // pairs of CTAs: an even grid, one tile pair per unit, no split of the reduction
+        if (!p.tma || p.splits != 1 || p.cluster_red || (grid & 1)) return cudaErrorInvalidValue;
+#define X(bn, st, ew)                                                 \
+    if (p.BN == bn && stages == st && p.epi_warps == ew)              \
+        return launch_one<bn, st, KIND_BF16_TMA, ew, true>(p, map, grid, stream);
+        TC_BF16_MC_CONFIGS(X)
 #undef X
         return cudaErrorInvalidValue;
     }

@@ -221,7 +221,10 @@ def test_selector_table_load_save_and_precedence(lib, tmp_path):
         assert desc_of(other) == rules_other                   # other problems keep the rules
         out = tmp_path / "saved.txt"
         B.conv_tune_table_save(str(out))
-        assert out.read_text().splitlines() == [f"{_table_key(layer, B.CONV_BF16)} | {choice}"]
+        # (a row without the mc field, as older tables wrote it, loads with mc left to the rules)
+        assert out.read_text().splitlines() == [f"{_table_key(layer, B.CONV_BF16)} | {choice} mc=-1"]
+        B.conv_tune_table_load(str(out))
+        assert desc_of(layer).startswith("variant=simt_bf16")
         bad = tmp_path / "bad.txt"
         bad.write_text(f"{_table_key(other, B.CONV_BF16)} | {choice}\nnot a table line\n")
         with pytest.raises(B.ConvError) as e:
@@ -239,6 +242,44 @@ def test_selector_table_load_save_and_precedence(lib, tmp_path):
     finally:
         B.conv_tune_table_clear()
     assert desc_of(layer) == rules
+
+
+def test_weight_multicast_plans(lib):
+    """CTA pairs that share each weight tile run only on request (CONV_FORCE_MC or the
+    selector): wide unsplit bf16 per-tap plans then take them, with units covering the M tiles
+    two at a time and an even grid; the rules never pick them, and plans that cannot (slab,
+    3xTF32, narrow or split) ignore the request."""
+    for name, li, want in [("sweep_bf16_n32", 0, True), ("sweep_bf16_n32", 1, True), ("sweep_bf16_n8", 1, True),
+                           ("grouped3d_g4_c64_d1", 0, False), ("whisper_frontend_f32", 1, False)]:
+        wl = WORKLOADS[name]
+        h = B.conv_plan_create(*wl.layers[li].plan_args(wl.dtype_code))
+        assert "weights=" not in B.conv_plan_describe(h)
+        B.conv_plan_destroy(h)
+        os.environ["CONV_FORCE_MC"] = "1"
+        try:
+            h = B.conv_plan_create(*wl.layers[li].plan_args(wl.dtype_code))
+        finally:
+            os.environ.pop("CONV_FORCE_MC")
+        d = dict(kv.split("=", 1) for kv in B.conv_plan_describe(h).split())
+        B.conv_plan_destroy(h)
+        assert (d.get("weights") == "multicast2") == want, (name, li, d)
+        if want:
+            assert int(d["grid"]) % 2 == 0 and d["splits"] == "1"
+            BW = int(d["pixels"].split("x")[1])
+            L = wl.layers[li]
+            Wo = oracle.out_len(L.spatial[0], L.filter[0], L.stride[0], L.pad[0], L.dilation[0])
+            num_mt = L.N * -(-Wo // BW)
+            num_nt = -(-L.K // int(d["tile"].split("x")[1]))
+            assert int(d["units"]) == -(-num_mt // 2) * num_nt
+    os.environ.update({"CONV_FORCE_MC": "1", "CONV_FORCE_BN": "128"})
+    try:
+        h = B.conv_plan_create(1, 1, 1, 64, 128, (700,), (3,), (2,), (1,), (1,), B.CONV_BF16, B.CONV_EPI_BIAS)
+        d = B.conv_plan_describe(h)
+        B.conv_plan_destroy(h)
+        assert "weights=multicast2" in d and "tile=128x128" in d and "units=2 " in d, d   # 3 M tiles -> 2 pairs
+    finally:
+        os.environ.pop("CONV_FORCE_MC")
+        os.environ.pop("CONV_FORCE_BN")
 
 
 def test_selector_scratch_covers_every_candidate(lib):

@@ -483,3 +483,31 @@ def test_cluster_split_k_reduction_equals_the_reduction_kernel(splits, dtype):
     assert np.array_equal(a, c), "cluster and kernel reductions differ"
     ref, S = oracle_full(layer, dtype, x, w, b)
     assert_within(dtype, layer.epilogue, a, ref, S, da)
+
+
+MC_CASES = [
+    # odd number of M tiles (the last pair's second tile lies past the output), 256-wide N tiles
+    ("1d_s2_odd_mt_bn256", L(1, 3, 1, 128, 256, (701,), (3,), (2,), (1,), (1,)),
+     {"CONV_FORCE_BN": 256, "CONV_FORCE_SPLITK": 1}),
+    # even number of M tiles, 128-wide N tiles, per-tap boxes at unit stride
+    ("1d_s1_bn128", L(1, 2, 1, 64, 128, (500,), (3,), (1,), (1,), (1,), CONV_EPI_BIAS),
+     {"CONV_FORCE_BN": 128, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_GATHER": "tma"}),
+    # 2D tiles of several output rows, groups, a ragged N tile, 8 epilogue warps
+    ("2d_s2_groups_bn128_ew8", L(2, 2, 2, 64, 200, (27, 33), (3, 3), (2, 2), (1, 1), (1, 1), CONV_EPI_GELU),
+     {"CONV_FORCE_BN": 128, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_EPI_WARPS": 8}),
+    # a long reduction (60 K blocks) as in the wide conv1d layer, batch 1
+    ("1d_s2_c1280", L(1, 1, 1, 1280, 1280, (3000,), (3,), (2,), (1,), (1,)), {"CONV_FORCE_SPLITK": 1}),
+]
+
+
+@pytest.mark.parametrize("name,layer,env", MC_CASES, ids=[c[0] for c in MC_CASES])
+def test_weight_multicast_pairs_are_bit_identical(name, layer, env):
+    """CTA pairs that share each weight tile by multicast issue the same MMAs on the same data
+    as single CTAs: the outputs are bit-identical, and within the bound of the oracle."""
+    x, w, b = make_inputs(layer, "bf16", 900 + len(name))
+    on, don = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_MC": 1}, guard=64)
+    off, doff = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_MC": 0})
+    assert "weights=multicast2" in don and "weights=" not in doff, (don, doff)
+    assert np.array_equal(on, off), f"{name}: multicast result differs [{don}]"
+    ref, S = oracle_full(layer, "bf16", x, w, b)
+    assert_within("bf16", layer.epilogue, on, ref, S, don)
