@@ -18,7 +18,8 @@
 //
 // Roles (warps): 0-7 epilogue (as in the per-tap kernel), 8 slab copies, 9-11 weight copies
 // (X taps' weight tiles in one bulk copy; ring stage s owned by warp 9 + s % 3), 12 MMA
-// issue, 13-16 (3xTF32 only) the hi/lo split of each slab.
+// issue (with tile pairs, 12 and 13: one issuer per accumulator), then (3xTF32 only) 4 warps
+// for the hi/lo split of each slab.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -31,13 +32,18 @@ namespace {
 constexpr int SLAB_MAX_SA = 4;
 constexpr int SLAB_MAX_SB = 8;
 
-template <bool TF32>
+// NMMA MMA-issuing warps.  An N = 64 MMA (128x64x16) runs in ~48 cycles, while one thread
+// issues one only every ~75 cycles (its descriptors, the elect and the issue itself; measured:
+// MMAs of half the width, same count, took within 8% of the time): the kernel was bound by
+// issue.  With tile pairs, each accumulator gets its own issuer; the stages both read and the
+// accumulator-full barrier then take one commit from each.
+template <bool TF32, int NMMA>
 struct SlabRoles {
     static constexpr int A_WARP = EPI_WARPS;
     static constexpr int B_WARP0 = EPI_WARPS + 1;
     static constexpr int B_WARPS = 3;
     static constexpr int MMA_WARP = EPI_WARPS + 4;
-    static constexpr int CVT_WARP0 = MMA_WARP + 1;
+    static constexpr int CVT_WARP0 = MMA_WARP + NMMA;
     static constexpr int CVT_WARPS = TF32 ? 4 : 0;
     static constexpr int THREADS = (CVT_WARP0 + CVT_WARPS) * 32;
 };
@@ -52,9 +58,10 @@ struct SlabRoles {
 // its MMAs into both accumulators from windows slab_pair_rows apart, against the same weight
 // tile.  The per-unit waits, commits and copies then serve twice the MMAs.
 template <int BN, bool TF32, int BY, int BT, int NACC>
-__global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
+__global__ void __launch_bounds__(SlabRoles<TF32, (TF32 ? 1 : NACC)>::THREADS, 1)
     conv_fwd_slab_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map) {
-    using R = SlabRoles<TF32>;
+    constexpr int NMMA = TF32 ? 1 : NACC;          // MMA-issuing warps (one per accumulator of a unit)
+    using R = SlabRoles<TF32, NMMA>;
     constexpr uint32_t B_TILE = BN * 128;
     constexpr uint32_t TMEM_COLS = (2 * NACC * BN < 32) ? 32 : 2 * NACC * BN;   // 2 buffers of NACC accumulators
     const int SA = p.slab_sa, SB = p.slab_sb;
@@ -79,8 +86,8 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
     const uint32_t bar_t = bar0 + 8u * (3 * SLAB_MAX_SA + 2 * SLAB_MAX_SB);
     auto tfull_bar = [&](int a) { return bar_t + 8u * a; };
     auto tempty_bar = [&](int a) { return bar_t + 8u * (2 + a); };
-    const uint32_t drain_bar = bar_t + 8u * 4;
-    uint8_t* misc = smem + (drain_bar + 8u - sbase);
+    auto drain_bar = [&](int mw) { return bar_t + 8u * (4 + mw); };   // one per MMA warp
+    uint8_t* misc = smem + (bar_t + 8u * 6 - sbase);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
 
@@ -90,23 +97,23 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < SA; ++s) {
             mbar_init(full_a(s), 1);
-            mbar_init(empty_a(s), 1);
+            mbar_init(empty_a(s), NMMA);
             mbar_init(cvt_a(s), R::CVT_WARPS > 0 ? R::CVT_WARPS : 1);
         }
         if (p.slab_resident) {
             mbar_init(full_b(0), R::B_WARPS);
-            mbar_init(empty_b(0), 1);
+            mbar_init(empty_b(0), NMMA);
         } else {
             for (int s = 0; s < SB; ++s) {
                 mbar_init(full_b(s), 1);
-                mbar_init(empty_b(s), 1);
+                mbar_init(empty_b(s), NMMA);
             }
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(tfull_bar(a), 1);
+            mbar_init(tfull_bar(a), NMMA);
             mbar_init(tempty_bar(a), EPI_WARPS);
         }
-        mbar_init(drain_bar, 1);
+        for (int mw = 0; mw < NMMA; ++mw) mbar_init(drain_bar(mw), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
@@ -219,8 +226,11 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == R::MMA_WARP) {
+    } else if (warp >= R::MMA_WARP && warp < R::MMA_WARP + NMMA) {
         // ------------------------------------------------------------ MMA issue (whole warp)
+        // issuer mw takes accumulator mw of each unit (with NMMA = 1, all of them); every issuer
+        // waits for the same stages and commits each release once
+        const int mw = warp - R::MMA_WARP;
         // bounded waits start once the previous kernel on the stream has completed
         if (p.pdl) griddep_wait();
         constexpr uint32_t IDESC = idesc_f32acc(BM, BN, TF32 ? 2u : 1u);
@@ -288,6 +298,7 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
                         const uint64_t bd = sw128_desc(b0 + t * b_tap);
 #pragma unroll
                         for (int j = 0; j < NACC; ++j) {
+                            if (NMMA > 1 && j != mw) continue;
                             const uint32_t a_addr = a0 + (row + (uint32_t)(j * p.slab_pair_rows)) * 128u;
                             const uint64_t ad = sw128_desc(a_addr);
                             const uint32_t dj = d_tmem + (uint32_t)(j * BN);
@@ -320,10 +331,10 @@ __global__ void __launch_bounds__(SlabRoles<TF32>::THREADS, 1)
         }
         if (aborted) {
             // wait (bounded) until every MMA issued so far has completed
-            mma_commit_warp(drain_bar);
+            mma_commit_warp(drain_bar(mw));
             if (lane == 0) {
                 const unsigned long long t0 = globaltimer();
-                while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
+                while (!mbar_try_wait(drain_bar(mw), 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {}
             }
         }
         __syncwarp();
@@ -429,7 +440,8 @@ cudaError_t launch_slab_one(const TcParams& p, const CUtensorMap& map, int grid,
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    return launch_kernel(kern, dim3(grid), dim3(SlabRoles<TF32>::THREADS), smem, stream, p.pdl != 0, 1, p, map);
+    return launch_kernel(kern, dim3(grid), dim3(SlabRoles<TF32, (TF32 ? 1 : NACC)>::THREADS), smem, stream,
+                         p.pdl != 0, 1, p, map);
 }
 
 }  // namespace
@@ -437,7 +449,7 @@ cudaError_t launch_slab_one(const TcParams& p, const CUtensorMap& map, int grid,
 size_t slab_smem_bytes(int BN, int tf32, int sa, int sb, size_t a_stage, int btaps) {
     const size_t b_stage = (size_t)btaps * BN * 128 * (tf32 ? 2 : 1);
     return 1024 + (size_t)sa * a_stage + (size_t)sb * b_stage + (size_t)EPI_WARPS * STG_WARP_BYTES +
-           8 * (3 * SLAB_MAX_SA + 2 * SLAB_MAX_SB + 5) + 16;
+           8 * (3 * SLAB_MAX_SA + 2 * SLAB_MAX_SB + 6) + 16;
 }
 
 cudaError_t launch_slab(const TcParams& p, const CUtensorMap* act_map, int grid, size_t smem, cudaStream_t stream) {
