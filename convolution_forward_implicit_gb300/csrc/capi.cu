@@ -295,10 +295,11 @@ struct PlanChoice {
     int epi_warps = 0;     // 8 or 16 epilogue warps in the per-tap kernel
     int cluster_red = -1;  // 0: split-K partials through the reduction kernel, not a cluster
     int mc = -1;           // 0 / 1: CTA pairs sharing weight tiles by multicast off / on
+    int pair = -1;         // 0 / 1: M = 256 tiles over CTA pairs (.cta_group::2 MMAs) off / on
     bool operator==(const PlanChoice& o) const {
         return simt == o.simt && no_pack == o.no_pack && bn == o.bn && bm == o.bm && splits == o.splits &&
                gather == o.gather && slab_stream == o.slab_stream && slab_pair == o.slab_pair &&
-               epi_warps == o.epi_warps && cluster_red == o.cluster_red && mc == o.mc;
+               epi_warps == o.epi_warps && cluster_red == o.cluster_red && mc == o.mc && pair == o.pair;
     }
 };
 
@@ -321,6 +322,7 @@ struct conv_plan {
     int epi_warps;          // per-tap kernel epilogue warps (8 or 16)
     int cluster_red;        // split-K partials summed inside a cluster (no workspace, no reduce kernel)
     int mc;                 // CTA pairs share each weight tile by multicast (units are pairs of M tiles)
+    int pair;               // M = 256 tiles over CTA pairs with .cta_group::2 MMAs (units are pairs of M tiles)
     size_t slab_smem;
     // SIMT plan
     int BM, Kg, Kpad, nkt, ktps, vec;
@@ -376,6 +378,7 @@ static bool choice_from_env(PlanChoice& c) {
     take("CONV_FORCE_EPI_WARPS", c.epi_warps);
     take("CONV_FORCE_CLUSTER_RED", c.cluster_red);
     take("CONV_FORCE_MC", c.mc);
+    take("CONV_FORCE_PAIR", c.pair);
     if (const char* v = getenv("CONV_FORCE_GATHER")) {
         if (strcmp(v, "cpasync") == 0) { c.gather = 1; any = true; }
         else if (strcmp(v, "tma") == 0) { c.gather = 2; any = true; }
@@ -460,6 +463,22 @@ static bool encode_act_map(const conv_plan* p, const void* x, CUtensorMap* map) 
                           const_cast<void*>(x), dims, strides, box, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// The packed weights of a CTA-pair plan as a 2-D tensor of 128-byte rows (64 bf16), read in
+// boxes of BN/2 rows: each CTA of a pair loads its half of a weight tile.  The rows are copied
+// verbatim (they are already 128-byte swizzled by the prepack).
+static bool encode_w_map(const conv_plan* p, const void* w_packed, CUtensorMap* map) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {64, (cuuint64_t)p->g.G * p->num_nt * p->nkb * p->BN};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {64, (cuuint32_t)(p->BN / 2)};
+    cuuint32_t es[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w_packed), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -692,9 +711,34 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     // tile from L2 once per pair.  Only on request (the measured selector or CONV_FORCE_MC):
     // measured on the 128 -> 1280 -> 1280 conv1d layers at batch 32 the pairs' lockstep costs
     // more than the halved weight reads save (L1 105 -> 114 us, L2 309 -> 320 us).
+    // CTA pairs with M = 256 MMAs (tc_pair.cu): bf16 per-tap TMA plans with N tiles of 128 or
+    // 256, no split and long reductions (8 epilogue warps), when the pairs' units fill every
+    // pair of SMs at least once.  Each SM then stores and reads half of every weight tile
+    // (~64 KB instead of ~96 KB of shared-memory traffic per K block of 128x256 outputs).
+    // Measured on the 128 -> 1280 -> 1280 conv1d at batch 32: the 60-block layer 309 -> 287 us;
+    // the 6-block layer with 16 epilogue warps (4 ring stages as pairs) 105 -> 129 us, so plans
+    // with the wide epilogue keep single CTAs unless forced.
+    p->pair = 0;
+    if (!tf32 && p->tma && !p->slab && p->splits == 1 && !p->cluster_red && (bn == 128 || bn == 256) &&
+        p->num_mt >= 2 && p->ch.mc != 1) {
+        const int64_t pair_units = cdiv(p->num_mt, 2) * g.G * p->num_nt;
+        int clusters = p->sm_count / 2;
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) {
+            const int n = tc_pair_max_clusters(bn, p->epi_warps);
+            if (n > 0) clusters = std::min(clusters, n);
+        }
+        cudaGetLastError();
+        if (clusters >= 1 && (p->ch.pair >= 0 ? p->ch.pair == 1 : (p->epi_warps == 8 && pair_units >= clusters))) {
+            p->pair = 1;
+            p->stages = tc_pair_stages_for(bn, p->epi_warps);
+            p->total_units = (int)pair_units;
+            p->grid = 2 * (int)std::min<int64_t>(pair_units, clusters);
+        }
+    }
     p->mc = 0;
     if (!tf32 && p->tma && !p->slab && p->splits == 1 && !p->cluster_red && bn >= 128 && p->num_mt >= 2 &&
-        p->ch.mc == 1) {
+        !p->pair && p->ch.mc == 1) {
         int clusters = p->sm_count / 2;
         int dev = 0;
         if (cudaGetDevice(&dev) == cudaSuccess) {
@@ -721,7 +765,8 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
                  "grid=%d k_blocks=%d map=%d epi_warps=%d reduce=%s%s",
                  tf32 ? "tc_tf32x3" : "tc_bf16", bn, p->BH, p->BW, cblk, p->stages, p->splits, p->total_units,
                  p->grid, p->nkb, p->map_kind, p->epi_warps,
-                 p->splits == 1 ? "none" : p->cluster_red ? "cluster" : "kernel", p->mc ? " weights=multicast2" : "");
+                 p->splits == 1 ? "none" : p->cluster_red ? "cluster" : "kernel",
+                 p->pair ? " cta_pair=m256" : p->mc ? " weights=multicast2" : "");
     else
         snprintf(p->desc, sizeof(p->desc),
                  "variant=tc_bf16 gather=cp.async tile=128x%d k_block=64 stages=%d splits=%d units=%d grid=%d "
@@ -767,7 +812,7 @@ static void choose_variant(conv_plan* p) {
     Geom& g = p->g;
     const int64_t G = p->Go, C = p->Co, K = p->Ko;
     g.G = (int)G; g.C = (int)C; g.K = (int)K;
-    p->pack = 1; p->slab = 0; p->tma = 0; p->cluster_red = 0; p->mc = 0; p->epi_warps = 8; p->splits = 1;
+    p->pack = 1; p->slab = 0; p->tma = 0; p->cluster_red = 0; p->mc = 0; p->pair = 0; p->epi_warps = 8; p->splits = 1;
     // bf16 with C, K multiples of 8: tcgen05 kind::f16.  fp32 with C, K multiples of 4 that the
     // TMA gather can express: tcgen05 3xTF32.  Everything else: the FFMA kernel.
     const bool no_tc = p->ch.simt != 0;
@@ -847,12 +892,13 @@ static std::vector<conv_plan> tune_candidates(const conv_plan* p) {
                 c.bn = bn; c.splits = sp; c.gather = ga;
                 cs.push_back(c);
             }
-    for (int bn : {128, 256})      // wide unsplit tiles with and without weight multicast
-        for (int mc : {0, 1}) {
-            PlanChoice c;
-            c.bn = bn; c.splits = 1; c.mc = mc;
-            cs.push_back(c);
-        }
+    for (int bn : {128, 256}) {    // wide unsplit tiles: one CTA, CTA pairs, or weight multicast
+        PlanChoice c;
+        c.bn = bn; c.splits = 1;
+        c.pair = 0; cs.push_back(c);
+        c.pair = 1; cs.push_back(c);
+        c.pair = 0; c.mc = 1; cs.push_back(c);
+    }
     PlanChoice f;
     f.simt = 1;
     cs.push_back(f);
@@ -1464,8 +1510,14 @@ static conv_status run_forward(conv_plan_t plan, const void* x, const void* w_pa
         tp.f_bws = make_fastdiv(plan->slab_bws);
         CUtensorMap map;
         if (plan->tma && !encode_act_map(plan, x, &map)) return CONV_ERR_CUDA;
-        e = plan->slab ? launch_slab(tp, &map, plan->grid, plan->slab_smem, s)
-                       : launch_tc(tp, plan->tma ? &map : nullptr, plan->stages, plan->grid, s);
+        if (plan->pair) {
+            CUtensorMap wmap;
+            if (!encode_w_map(plan, w_packed, &wmap)) return CONV_ERR_CUDA;
+            e = launch_pair(tp, &map, &wmap, plan->stages, plan->grid, s);
+        } else {
+            e = plan->slab ? launch_slab(tp, &map, plan->grid, plan->slab_smem, s)
+                           : launch_tc(tp, plan->tma ? &map : nullptr, plan->stages, plan->grid, s);
+        }
     } else {
         SimtParams sp;
         sp.g = plan->g;
@@ -1778,9 +1830,9 @@ conv_status conv_tune_table_save(const char* path) {
     for (const auto& kv : g_tune_table) {
         const PlanChoice& c = kv.second.c;
         fprintf(f, "%s | simt=%d no_pack=%d bn=%d bm=%d splits=%d gather=%d slab_stream=%d slab_pair=%d epi_warps=%d "
-                   "cluster_red=%d mc=%d",
+                   "cluster_red=%d mc=%d pair=%d",
                 kv.first.c_str(), c.simt, c.no_pack, c.bn, c.bm, c.splits, c.gather, c.slab_stream, c.slab_pair,
-                c.epi_warps, c.cluster_red, c.mc);
+                c.epi_warps, c.cluster_red, c.mc, c.pair);
         if (kv.second.us >= 0.0) fprintf(f, " | us=%.3f", kv.second.us);
         fputc('\n', f);
         // the measurements behind the choice, as comment lines (ignored by the loader)
@@ -1802,14 +1854,15 @@ conv_status conv_tune_table_load(const char* path) {
         char* bar = strstr(line, " | ");
         TuneEntry te;
         PlanChoice& c = te.c;
-        // (rows written before the mc field existed carry ten fields: mc stays with the rules)
+        // (rows written before the mc and pair fields existed carry ten or eleven fields: the
+        // missing ones stay with the rules)
         int nf = bar ? sscanf(bar + 3,
                               "simt=%d no_pack=%d bn=%d bm=%d splits=%d gather=%d slab_stream=%d slab_pair=%d "
-                              "epi_warps=%d cluster_red=%d mc=%d",
+                              "epi_warps=%d cluster_red=%d mc=%d pair=%d",
                               &c.simt, &c.no_pack, &c.bn, &c.bm, &c.splits, &c.gather, &c.slab_stream, &c.slab_pair,
-                              &c.epi_warps, &c.cluster_red, &c.mc)
+                              &c.epi_warps, &c.cluster_red, &c.mc, &c.pair)
                      : 0;
-        if (nf != 10 && nf != 11) {
+        if (nf < 10 || nf > 12) {
             st = CONV_ERR_INVALID_ARG;
             break;
         }

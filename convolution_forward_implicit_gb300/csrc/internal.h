@@ -175,6 +175,12 @@ int tc_stages_for(int BN, int tf32, int epi_warps);
 // Clusters of two CTAs of the weight-multicast kernel for (BN, epi_warps) that can be resident at
 // once on the current device (0 if it cannot be queried).
 int tc_mc_max_clusters(int BN, int epi_warps);
+// CTA-pair kernel (tc_pair.cu): M = 256 tiles over two CTAs with .cta_group::2 MMAs; bf16 per-tap
+// TMA plans without a split.  w_map: the packed weights as 2-D rows of 128 bytes, boxes of BN/2 rows.
+cudaError_t launch_pair(const TcParams& p, const CUtensorMap* act_map, const CUtensorMap* w_map, int stages, int grid,
+                        cudaStream_t stream);
+int tc_pair_stages_for(int BN, int epi_warps);
+int tc_pair_max_clusters(int BN, int epi_warps);
 // Slab-mode kernel; smem from slab_smem_bytes.
 cudaError_t launch_slab(const TcParams& p, const CUtensorMap* act_map, int grid, size_t smem, cudaStream_t stream);
 size_t slab_smem_bytes(int BN, int tf32, int sa, int sb, size_t a_stage, int btaps);

@@ -222,7 +222,7 @@ def test_selector_table_load_save_and_precedence(lib, tmp_path):
         out = tmp_path / "saved.txt"
         B.conv_tune_table_save(str(out))
         # (a row without the mc field, as older tables wrote it, loads with mc left to the rules)
-        assert out.read_text().splitlines() == [f"{_table_key(layer, B.CONV_BF16)} | {choice} mc=-1"]
+        assert out.read_text().splitlines() == [f"{_table_key(layer, B.CONV_BF16)} | {choice} mc=-1 pair=-1"]
         B.conv_tune_table_load(str(out))
         assert desc_of(layer).startswith("variant=simt_bf16")
         bad = tmp_path / "bad.txt"
@@ -280,6 +280,39 @@ def test_weight_multicast_plans(lib):
     finally:
         os.environ.pop("CONV_FORCE_MC")
         os.environ.pop("CONV_FORCE_BN")
+
+
+def test_cta_pair_plans(lib):
+    """bf16 per-tap plans with 128- or 256-wide N tiles, no split and long reductions (8
+    epilogue warps) run on CTA pairs (M = 256 tiles) when the pairs' units fill every pair of
+    SMs: the 1280 -> 1280 sweep layer at batch 8 and 32; not the 128 -> 1280 layer (16 epilogue
+    warps), the batch-1 or Whisper layers, the slab, 3xTF32 or split plans.  Units cover the M
+    tiles two at a time and the grid is even."""
+    for name, li, want in [("sweep_bf16_n32", 0, False), ("sweep_bf16_n32", 1, True), ("sweep_bf16_n8", 0, False),
+                           ("sweep_bf16_n8", 1, True), ("sweep_bf16_n1", 1, False), ("whisper_frontend_bf16", 1, False),
+                           ("grouped3d_g4_c64_d1", 0, False), ("whisper_frontend_f32", 1, False)]:
+        wl = WORKLOADS[name]
+        L = wl.layers[li]
+        h = B.conv_plan_create(*L.plan_args(wl.dtype_code))
+        d = dict(kv.split("=", 1) for kv in B.conv_plan_describe(h).split())
+        B.conv_plan_destroy(h)
+        assert (d.get("cta_pair") == "m256") == want, (name, li, d)
+        if want:
+            assert int(d["grid"]) % 2 == 0 and d["splits"] == "1"
+            BW = int(d["pixels"].split("x")[1])
+            Wo = oracle.out_len(L.spatial[0], L.filter[0], L.stride[0], L.pad[0], L.dilation[0])
+            num_mt = L.N * -(-Wo // BW)
+            num_nt = -(-L.K // int(d["tile"].split("x")[1]))
+            assert int(d["units"]) == -(-num_mt // 2) * num_nt
+    os.environ.update({"CONV_FORCE_PAIR": "1", "CONV_FORCE_BN": "128", "CONV_FORCE_SPLITK": "1"})
+    try:
+        h = B.conv_plan_create(1, 1, 1, 64, 128, (700,), (3,), (2,), (1,), (1,), B.CONV_BF16, B.CONV_EPI_BIAS)
+        d = B.conv_plan_describe(h)
+        B.conv_plan_destroy(h)
+        assert "cta_pair=m256" in d and "units=2 " in d and "grid=4 " in d, d   # 3 M tiles -> 2 pairs
+    finally:
+        for k in ("CONV_FORCE_PAIR", "CONV_FORCE_BN", "CONV_FORCE_SPLITK"):
+            os.environ.pop(k)
 
 
 def test_selector_scratch_covers_every_candidate(lib):

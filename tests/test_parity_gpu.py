@@ -506,8 +506,22 @@ def test_weight_multicast_pairs_are_bit_identical(name, layer, env):
     as single CTAs: the outputs are bit-identical, and within the bound of the oracle."""
     x, w, b = make_inputs(layer, "bf16", 900 + len(name))
     on, don = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_MC": 1}, guard=64)
-    off, doff = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_MC": 0})
+    off, doff = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_MC": 0, "CONV_FORCE_PAIR": 0})
     assert "weights=multicast2" in don and "weights=" not in doff, (don, doff)
     assert np.array_equal(on, off), f"{name}: multicast result differs [{don}]"
+    ref, S = oracle_full(layer, "bf16", x, w, b)
+    assert_within("bf16", layer.epilogue, on, ref, S, don)
+
+
+@pytest.mark.parametrize("name,layer,env", MC_CASES, ids=[c[0] for c in MC_CASES])
+def test_cta_pair_tiles_are_bit_identical(name, layer, env):
+    """M = 256 tiles over a CTA pair (.cta_group::2 MMAs: each CTA holds its 128 rows of the
+    activations and half of every weight tile) give the same bits as 128-row tiles on single
+    CTAs, and meet the bound against the oracle."""
+    x, w, b = make_inputs(layer, "bf16", 950 + len(name))
+    on, don = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_PAIR": 1}, guard=64)
+    off, doff = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_PAIR": 0})
+    assert "cta_pair=m256" in don and "cta_pair" not in doff, (don, doff)
+    assert np.array_equal(on, off), f"{name}: CTA-pair result differs [{don}]"
     ref, S = oracle_full(layer, "bf16", x, w, b)
     assert_within("bf16", layer.epilogue, on, ref, S, don)
