@@ -161,6 +161,8 @@ struct TcParams {
                             // accumulators through distributed shared memory (no workspace)
     int mc;                 // 1 (per-tap bf16 TMA kernel, no split): CTA pairs share each weight tile
                             // by multicast; units are pairs of M tiles (see conv_fwd_tc_kernel)
+    int ystore;             // 1: the epilogue stores y through a tensor map (TMA), one 64-channel x
+                            // 32-pixel box per warp and chunk (tiles of one output row, BW % 32 == 0)
     Lattice lat;            // where the output pixels land in y (one phase of a strided backward data)
     int test_stall;         // test hook: the MMA role waits on a barrier nothing completes
     // divisors of the per-tile index arithmetic
@@ -170,15 +172,16 @@ struct TcParams {
 constexpr size_t SLAB_SMEM_MAX = 232448;   // dynamic shared memory a block may opt in to
 
 // Launch the tensor-core kernel for the (BN, stages) pair the plan picked (see tc_stages_for).
-cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, int stages, int grid, cudaStream_t stream);
+cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, const CUtensorMap* y_map, int stages, int grid,
+                      cudaStream_t stream);
 int tc_stages_for(int BN, int tf32, int epi_warps);
 // Clusters of two CTAs of the weight-multicast kernel for (BN, epi_warps) that can be resident at
 // once on the current device (0 if it cannot be queried).
 int tc_mc_max_clusters(int BN, int epi_warps);
 // CTA-pair kernel (tc_pair.cu): M = 256 tiles over two CTAs with .cta_group::2 MMAs; bf16 per-tap
 // TMA plans without a split.  w_map: the packed weights as 2-D rows of 128 bytes, boxes of BN/2 rows.
-cudaError_t launch_pair(const TcParams& p, const CUtensorMap* act_map, const CUtensorMap* w_map, int stages, int grid,
-                        cudaStream_t stream);
+cudaError_t launch_pair(const TcParams& p, const CUtensorMap* act_map, const CUtensorMap* w_map,
+                        const CUtensorMap* y_map, int stages, int grid, cudaStream_t stream);
 int tc_pair_stages_for(int BN, int epi_warps);
 int tc_pair_max_clusters(int BN, int epi_warps);
 // Slab-mode kernel; smem from slab_smem_bytes.

@@ -130,6 +130,21 @@ __device__ __forceinline__ void bulk_g2s_multicast(uint32_t dst, const void* src
         : "memory");
 }
 
+// Tiled TMA store of a 5-D box from shared memory (elements outside the tensor are not
+// written), tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4, uint32_t src) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(src)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of this thread's bulk stores have been read (they may be rewritten)
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// this thread's bulk stores have completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---- tcgen05 ----
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -387,14 +402,23 @@ __device__ __forceinline__ void epilogue_rows(int lane, int wq, RowOffset row_of
     }
 }
 
+// Where a warp's 32 rows go when the epilogue stores through a tensor map of y: rows are the
+// 32 consecutive output pixels starting at (n, od, oh, ow) along W.
+struct YBox {
+    int ow, oh, od, n;
+};
+
 // One warp's share of a tile's epilogue: its 32 accumulator rows (TMEM lane quarter wq) and
 // the columns [cb_begin, cb_end) of the BN-wide tile, COLS of them at most.  QW32: read TMEM
-// 32 columns at a time where the chunk allows (fewer round trips, more registers).
+// 32 columns at a time where the chunk allows (fewer round trips, more registers).  With ymap
+// (bf16 outputs in 64-column chunks), each chunk leaves the staging buffer as one TMA store of
+// a 64-channel x 32-pixel box at ybox instead of per-lane stores.
 template <int BN, int COLS, int ESZ, bool QW32 = true>
 __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t taddr, int lane, int wq, int cb_begin,
                                                 int cb_end, int nt, int gi, int split, bool partial, bool add_bias,
                                                 bool do_gelu, uint8_t* stg, const long long (&roff)[EPI_MAX_LPR],
-                                                const float* bsm = nullptr) {
+                                                const float* bsm = nullptr, const CUtensorMap* ymap = nullptr,
+                                                YBox ybox = YBox{0, 0, 0, 0}) {
     using S = EpiShape<COLS, ESZ>;
     constexpr int CW = S::CW;
     constexpr int RB = S::RB;
@@ -409,6 +433,11 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
     for (int cb = cb_begin; cb < cb_end; cb += CW) {
         const int n0 = nt * BN + cb;
         if (n0 >= g.K) break;                               // warp-uniform
+        if (ESZ == 2 && CW == 64 && ymap) {
+            // the staging buffer is rewritten only after the previous chunk's store has read it
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+        }
         // QW columns per TMEM load (32 where the chunk allows): TMEM -> fp32 -> bias, GELU ->
         // this lane's row slots in staging
         // (fp32 outputs keep 16: the 3xTF32 kernels run 544 threads and have fewer registers)
@@ -497,6 +526,16 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
             }
         }
         __syncwarp();
+        if (ESZ == 2 && CW == 64 && ymap) {
+            // 32 rows x 128 bytes in the 128-byte swizzle the tensor map expects: one box store
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_5d(ymap, gi * g.K + n0, ybox.ow, ybox.oh, ybox.od, ybox.n, smem_u32(stg));
+                bulk_commit_group();
+            }
+            continue;
+        }
         // row-wise store: lanes slot..slot+LPR-1 of a row write its whole segment
         const int col = n0 + slot * EPS;
         uint8_t* base = partial ? reinterpret_cast<uint8_t*>(p.ws) + ((size_t)split * g.M * GK) * 4

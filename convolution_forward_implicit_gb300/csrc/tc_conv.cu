@@ -96,7 +96,8 @@ struct Smem {
 // the empty barriers of both).
 template <int BN, int STAGES, int KIND, int EW, bool MC>
 __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
-    conv_fwd_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map) {
+    conv_fwd_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map,
+                       const __grid_constant__ CUtensorMap y_map) {
     using C = Cfg<BN, KIND>;
     using T = Traits<KIND, EW>;
     static_assert(!MC || KIND == KIND_BF16_TMA, "weight multicast is built for the bf16 TMA kernel");
@@ -516,11 +517,15 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                                        do_gelu, stg, roff);
             else
                 epilogue_chunks<BN, COLS, 2, EW == 8>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
-                                       do_gelu, stg, roff, bsm);
+                                       do_gelu, stg, roff, bsm, (T::TMA && p.ystore) ? &y_map : nullptr,
+                                       YBox{to.ow0 + wq * 32, to.oh0, to.od, to.n});
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
+        // the tensor-map stores have completed before this CTA may leave
+        if (p.ystore && lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     if (p.cluster_red) {
@@ -606,7 +611,8 @@ constexpr size_t smem_bytes_for() {
 }
 
 template <int BN, int STAGES, int KIND, int EW, bool MC = false>
-cudaError_t launch_one(const TcParams& p, const CUtensorMap& map, int grid, cudaStream_t stream) {
+cudaError_t launch_one(const TcParams& p, const CUtensorMap& map, const CUtensorMap& ymap, int grid,
+                       cudaStream_t stream) {
     auto kern = conv_fwd_tc_kernel<BN, STAGES, KIND, EW, MC>;
     constexpr size_t smem = smem_bytes_for<BN, STAGES, KIND, EW>();
     static_assert(smem <= 232448, "shared memory budget");
@@ -623,7 +629,7 @@ cudaError_t launch_one(const TcParams& p, const CUtensorMap& map, int grid, cuda
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     return launch_kernel(kern, dim3(grid), dim3(Traits<KIND, EW>::THREADS), smem, stream, p.pdl != 0,
-                         MC ? 2 : p.cluster_red ? p.splits : 1, p, map);
+                         MC ? 2 : p.cluster_red ? p.splits : 1, p, map, ymap);
 }
 
 }  // namespace
@@ -678,14 +684,18 @@ int tc_mc_max_clusters(int BN, int epi_warps) {
     return 0;
 }
 
-cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, int stages, int grid, cudaStream_t stream) {
+cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, const CUtensorMap* y_map, int stages, int grid,
+                      cudaStream_t stream) {
     static const CUtensorMap unused{};
     const CUtensorMap& map = act_map ? *act_map : unused;
+    const CUtensorMap& ymap = y_map ? *y_map : unused;
     if (p.tma && !act_map) return cudaErrorInvalidValue;
+    if (p.ystore && (!y_map || !p.tma || p.tf32 || p.splits != 1 || p.lat.on || p.BH != 1 || p.BW % 32 != 0))
+        return cudaErrorInvalidValue;
     if (p.tf32) {
         if (!p.tma || p.epi_warps != 8) return cudaErrorInvalidValue;
 #define X(bn, st) \
-    if (p.BN == bn && stages == st) return launch_one<bn, st, KIND_TF32X3, 8>(p, map, grid, stream);
+    if (p.BN == bn && stages == st) return launch_one<bn, st, KIND_TF32X3, 8>(p, map, ymap, grid, stream);
         TC_TF32_CONFIGS(X)
 #undef X
         return cudaErrorInvalidValue;
@@ -695,7 +705,7 @@ cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, int stages,
         if (!p.tma || p.splits != 1 || p.cluster_red || (grid & 1)) return cudaErrorInvalidValue;
 #define X(bn, st, ew)                                                 \
     if (p.BN == bn && stages == st && p.epi_warps == ew)              \
-        return launch_one<bn, st, KIND_BF16_TMA, ew, true>(p, map, grid, stream);
+        return launch_one<bn, st, KIND_BF16_TMA, ew, true>(p, map, ymap, grid, stream);
         TC_BF16_MC_CONFIGS(X)
 #undef X
         return cudaErrorInvalidValue;
@@ -703,7 +713,7 @@ cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, int stages,
     if (p.epi_warps == 16) {
         if (!p.tma) return cudaErrorInvalidValue;
 #define X(bn, st) \
-    if (p.BN == bn && stages == st) return launch_one<bn, st, KIND_BF16_TMA, 16>(p, map, grid, stream);
+    if (p.BN == bn && stages == st) return launch_one<bn, st, KIND_BF16_TMA, 16>(p, map, ymap, grid, stream);
         TC_BF16_EPI16_CONFIGS(X)
 #undef X
         return cudaErrorInvalidValue;
@@ -711,8 +721,8 @@ cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, int stages,
     if (p.epi_warps != 8) return cudaErrorInvalidValue;
 #define X(bn, st)                                                                              \
     if (p.BN == bn && stages == st)                                                            \
-        return p.tma ? launch_one<bn, st, KIND_BF16_TMA, 8>(p, map, grid, stream)              \
-                     : launch_one<bn, st, KIND_BF16_CPASYNC, 8>(p, map, grid, stream);
+        return p.tma ? launch_one<bn, st, KIND_BF16_TMA, 8>(p, map, ymap, grid, stream)              \
+                     : launch_one<bn, st, KIND_BF16_CPASYNC, 8>(p, map, ymap, grid, stream);
     TC_BF16_CONFIGS(X)
 #undef X
     return cudaErrorInvalidValue;

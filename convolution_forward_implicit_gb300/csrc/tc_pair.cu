@@ -112,7 +112,7 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
 template <int BN, int STAGES, int EW>
 __global__ void __launch_bounds__(PairTraits<EW>::THREADS, 1)
     conv_fwd_pair_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map,
-                         const __grid_constant__ CUtensorMap w_map) {
+                         const __grid_constant__ CUtensorMap w_map, const __grid_constant__ CUtensorMap y_map) {
     using T = PairTraits<EW>;
     using SM = PairSmem<BN, STAGES, EW>;
     constexpr uint32_t TMEM_COLS = 2 * BN;                   // two accumulators of BN columns
@@ -310,7 +310,8 @@ __global__ void __launch_bounds__(PairTraits<EW>::THREADS, 1)
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
             epilogue_chunks<BN, COLS, 2, EW == 8>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, 0, false, add_bias,
-                                                  do_gelu, stg, roff);
+                                                  do_gelu, stg, roff, nullptr, p.ystore ? &y_map : nullptr,
+                                                  YBox{to.ow0 + wq * 32, to.oh0, to.od, to.n});
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -318,6 +319,9 @@ __global__ void __launch_bounds__(PairTraits<EW>::THREADS, 1)
                 else mbar_arrive_cluster(tempty_leader0 + 8u * (uint32_t)acc);
             }
         }
+        // the tensor-map stores have completed before this CTA may leave
+        if (p.ystore && lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -331,8 +335,8 @@ __global__ void __launch_bounds__(PairTraits<EW>::THREADS, 1)
 }
 
 template <int BN, int STAGES, int EW>
-cudaError_t launch_pair_one(const TcParams& p, const CUtensorMap& amap, const CUtensorMap& wmap, int grid,
-                            cudaStream_t stream) {
+cudaError_t launch_pair_one(const TcParams& p, const CUtensorMap& amap, const CUtensorMap& wmap,
+                            const CUtensorMap& ymap, int grid, cudaStream_t stream) {
     auto kern = conv_fwd_pair_kernel<BN, STAGES, EW>;
     constexpr size_t smem = PairSmem<BN, STAGES, EW>::TOTAL;
     static_assert(smem <= 232448, "shared memory budget");
@@ -347,7 +351,8 @@ cudaError_t launch_pair_one(const TcParams& p, const CUtensorMap& amap, const CU
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    return launch_kernel(kern, dim3(grid), dim3(PairTraits<EW>::THREADS), smem, stream, p.pdl != 0, 2, p, amap, wmap);
+    return launch_kernel(kern, dim3(grid), dim3(PairTraits<EW>::THREADS), smem, stream, p.pdl != 0, 2, p, amap, wmap,
+                         ymap);
 }
 
 }  // namespace
@@ -395,13 +400,15 @@ int tc_pair_max_clusters(int BN, int epi_warps) {
     return 0;
 }
 
-cudaError_t launch_pair(const TcParams& p, const CUtensorMap* act_map, const CUtensorMap* w_map, int stages, int grid,
-                        cudaStream_t stream) {
+cudaError_t launch_pair(const TcParams& p, const CUtensorMap* act_map, const CUtensorMap* w_map,
+                        const CUtensorMap* y_map, int stages, int grid, cudaStream_t stream) {
+    static const CUtensorMap unused{};
     if (!act_map || !w_map || !p.tma || p.tf32 || p.splits != 1 || p.cluster_red || (grid & 1))
         return cudaErrorInvalidValue;
+    if (p.ystore && (!y_map || p.lat.on || p.BH != 1 || p.BW % 32 != 0)) return cudaErrorInvalidValue;
 #define X(bn, st, ew)                                                                \
     if (p.BN == bn && stages == st && p.epi_warps == ew)                             \
-        return launch_pair_one<bn, st, ew>(p, *act_map, *w_map, grid, stream);
+        return launch_pair_one<bn, st, ew>(p, *act_map, *w_map, y_map ? *y_map : unused, grid, stream);
     TC_PAIR_CONFIGS(X)
 #undef X
     return cudaErrorInvalidValue;

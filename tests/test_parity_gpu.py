@@ -525,3 +525,35 @@ def test_cta_pair_tiles_are_bit_identical(name, layer, env):
     assert np.array_equal(on, off), f"{name}: CTA-pair result differs [{don}]"
     ref, S = oracle_full(layer, "bf16", x, w, b)
     assert_within("bf16", layer.epilogue, on, ref, S, don)
+
+
+YSTORE_CASES = [
+    # ragged last tile (Wo = 351: the last box is clipped at the end of the row), 16 epilogue warps
+    ("1d_s2_ragged_bn256", L(1, 3, 1, 128, 256, (701,), (3,), (2,), (1,), (1,)),
+     {"CONV_FORCE_BN": 256, "CONV_FORCE_SPLITK": 1}),
+    # groups with K % 64 == 0, 8 epilogue warps (two 64-column chunks per warp)
+    ("1d_groups_k128_ew8", L(1, 2, 2, 64, 128, (517,), (3,), (1,), (1,), (1,), CONV_EPI_BIAS),
+     {"CONV_FORCE_BN": 128, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_GATHER": "tma", "CONV_FORCE_EPI_WARPS": 8}),
+    # CTA pairs and weight multicast with tensor-map stores
+    ("1d_pair_bn256", L(1, 3, 1, 128, 256, (701,), (3,), (2,), (1,), (1,), CONV_EPI_NONE),
+     {"CONV_FORCE_BN": 256, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_EPI_WARPS": 8, "CONV_FORCE_PAIR": 1}),
+    ("1d_mc_bn256", L(1, 3, 1, 128, 256, (701,), (3,), (2,), (1,), (1,)),
+     {"CONV_FORCE_BN": 256, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_MC": 1}),
+    # 2D problem with one-row tiles (Wo >= 128)
+    ("2d_one_row_tiles", L(2, 1, 1, 64, 256, (3, 512), (3, 3), (1, 2), (1, 1), (1, 1)),
+     {"CONV_FORCE_BN": 256, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_GATHER": "tma"}),
+]
+
+
+@pytest.mark.parametrize("name,layer,env", YSTORE_CASES, ids=[c[0] for c in YSTORE_CASES])
+def test_tensor_map_stores_are_bit_identical(name, layer, env):
+    """Epilogues that store y through a tensor map (one TMA box of 64 channels x 32 pixels per
+    warp and chunk) write the same bits as per-lane stores, nothing outside y, and meet the
+    bound against the oracle."""
+    x, w, b = make_inputs(layer, "bf16", 970 + len(name))
+    on, don = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_YSTORE": 1}, guard=4096)
+    off, doff = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_YSTORE": 0})
+    assert "store=tma" in don and "store=tma" not in doff, (don, doff)
+    assert np.array_equal(on, off), f"{name}: tensor-map stores differ [{don}]"
+    ref, S = oracle_full(layer, "bf16", x, w, b)
+    assert_within("bf16", layer.epilogue, on, ref, S, don)
