@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libconvfwd.so")
-SOURCES = ["capi.cu", "tc_conv.cu", "tc_pair.cu", "tc_slab.cu", "simt.cu", "wgrad.cu", "tc_wgrad.cu"]
+SOURCES = ["capi.cu", "tc_conv.cu", "tc_pair.cu", "tc_slab.cu", "tc_slab_pair.cu", "simt.cu", "wgrad.cu",
+           "tc_wgrad.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

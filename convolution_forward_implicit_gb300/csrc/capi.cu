@@ -743,6 +743,54 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     // the 6-block layer with 16 epilogue warps (4 ring stages as pairs) 105 -> 129 us, so plans
     // with the wide epilogue keep single CTAs unless forced.
     p->pair = 0;
+    // Slab plans with tile pairs on CTA pairs (tc_slab_pair.cu): each CTA keeps its own slab and
+    // half of every weight tile, and each M = 256 MMA reads a weight half per SM.  The rings are
+    // refitted for half-size weight stages (resident weight sets where they fit, with a third
+    // slab stage where possible).
+    if (p->slab && !tf32 && p->slab_nacc == 2 && (bn == 32 || bn == 64) && p->splits == 1 && p->num_mt >= 2 &&
+        !p->lat.on && p->ch.pair != 0) {
+        const int64_t pair_units = cdiv(p->num_mt, 2) * g.G * p->num_nt;
+        const int nchunk = p->slab_nkg * p->slab_nbg;
+        // three slab stages first (resident weights, else a weight ring), then two
+        int sa = 0, sb = 0, resident = 0;
+        for (int a = 3; a >= 2 && !sa; --a) {
+            if (p->ch.slab_stream == 0 &&
+                slab_pair_smem_bytes(bn, a, nchunk, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
+                sa = a; sb = nchunk; resident = 1;
+            }
+            for (int b = 8; b >= 2 && !sa; --b)
+                if (slab_pair_smem_bytes(bn, a, b, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
+                    sa = a; sb = b;
+                }
+        }
+        // By rule pairs need three slab stages and a ring of at least four weight stages: a stage
+        // is refilled only after both CTAs' copies of it were read, which shorter rings do not
+        // cover, and with resident weights the units' epilogues (both CTAs') set the pace.
+        // Measured (us per call, single CTA -> pair): 3D d1, 3 + 5 stages: 190.9 -> 137.4; 3D d2,
+        // 3 + 2: 168.8 -> 336.8; 2D d2, 3 + 2: 39.3 -> 75.7; 2D d1, resident weights: 38.8 -> 47.0.
+        if ((sa >= 3 && !resident && sb >= 4) || (sa && p->ch.pair == 1)) {
+            const size_t smem = slab_pair_smem_bytes(bn, sa, sb, (size_t)p->slab_a_stage, p->slab_btaps);
+            int clusters = p->sm_count / 2;
+            int dev = 0;
+            if (cudaGetDevice(&dev) == cudaSuccess) {
+                const int n = slab_pair_max_clusters(smem);
+                if (n > 0) clusters = std::min(clusters, n);
+            }
+            cudaGetLastError();
+            // resident weights stay loaded only if a cluster keeps its (group, N tile): pair
+            // units advance by the cluster count, so make it a multiple of the number of sets
+            const int KT = g.G * p->num_nt;
+            if (resident && KT <= clusters) clusters -= clusters % KT;
+            if (clusters >= 1 && (p->ch.pair == 1 || pair_units >= clusters)) {
+                p->pair = 1;
+                p->slab_sa = sa; p->slab_sb = sb; p->slab_resident = resident;
+                p->slab_smem = smem;
+                p->total_units = (int)pair_units;
+                p->grid = 2 * (int)std::min<int64_t>(pair_units, clusters);
+                p->prepack_bytes = (size_t)g.G * p->num_nt * p->nkb * bn * 128;
+            }
+        }
+    }
     if (!tf32 && p->tma && !p->slab && p->splits == 1 && !p->cluster_red && (bn == 128 || bn == 256) &&
         p->num_mt >= 2 && p->ch.mc != 1) {
         const int64_t pair_units = cdiv(p->num_mt, 2) * g.G * p->num_nt;
@@ -807,6 +855,10 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
                  "variant=tc_bf16 gather=cp.async tile=128x%d k_block=64 stages=%d splits=%d units=%d grid=%d "
                  "k_blocks=%d",
                  bn, p->stages, p->splits, p->total_units, p->grid, p->nkb);
+    if (p->slab && p->pair) {
+        const size_t n = strlen(p->desc);
+        snprintf(p->desc + n, sizeof(p->desc) - n, " cta_pair=m256");
+    }
     if (p->ystore) {
         const size_t n = strlen(p->desc);
         snprintf(p->desc + n, sizeof(p->desc) - n, " store=tma");
@@ -1555,7 +1607,8 @@ static conv_status run_forward(conv_plan_t plan, const void* x, const void* w_pa
         if (plan->pair) {
             CUtensorMap wmap;
             if (!encode_w_map(plan, w_packed, &wmap)) return CONV_ERR_CUDA;
-            e = launch_pair(tp, &map, &wmap, tp.ystore ? &ymap : nullptr, plan->stages, plan->grid, s);
+            e = plan->slab ? launch_slab_pair(tp, &map, &wmap, plan->grid, plan->slab_smem, s)
+                           : launch_pair(tp, &map, &wmap, tp.ystore ? &ymap : nullptr, plan->stages, plan->grid, s);
         } else {
             e = plan->slab ? launch_slab(tp, &map, plan->grid, plan->slab_smem, s)
                            : launch_tc(tp, plan->tma ? &map : nullptr, tp.ystore ? &ymap : nullptr, plan->stages,

@@ -184,6 +184,12 @@ cudaError_t launch_pair(const TcParams& p, const CUtensorMap* act_map, const CUt
                         const CUtensorMap* y_map, int stages, int grid, cudaStream_t stream);
 int tc_pair_stages_for(int BN, int epi_warps);
 int tc_pair_max_clusters(int BN, int epi_warps);
+// Slab kernel on CTA pairs (tc_slab_pair.cu): bf16 tile-pair slab plans (two accumulators per
+// unit), N tiles of 32 or 64; each CTA holds half of every weight tile (w_map as for launch_pair).
+cudaError_t launch_slab_pair(const TcParams& p, const CUtensorMap* act_map, const CUtensorMap* w_map, int grid,
+                             size_t smem, cudaStream_t stream);
+size_t slab_pair_smem_bytes(int BN, int sa, int sb, size_t a_stage, int btaps);
+int slab_pair_max_clusters(size_t smem);
 // Slab-mode kernel; smem from slab_smem_bytes.
 cudaError_t launch_slab(const TcParams& p, const CUtensorMap* act_map, int grid, size_t smem, cudaStream_t stream);
 size_t slab_smem_bytes(int BN, int tf32, int sa, int sb, size_t a_stage, int btaps);

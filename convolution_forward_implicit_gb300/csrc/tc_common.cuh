@@ -387,6 +387,17 @@ struct EpiShape {
     static constexpr int RPI = 32 / LPR;                            // rows per store instruction
 };
 constexpr int EPI_MAX_LPR = 8;
+// Staging bytes one warp's epilogue uses: 32 rows of one chunk's row segments.
+template <int COLS, int ESZ>
+__host__ __device__ constexpr uint32_t stg_warp_bytes() {
+    return 32u * (uint32_t)EpiShape<COLS, ESZ>::RB;
+}
+// The same on the host side for the slab kernels (BN/2 columns a warp, at least 16).
+inline size_t slab_stg_warp_bytes(int BN, int esz) {
+    const int cols = BN / 2 < 16 ? 16 : BN / 2;
+    const int cw = cols < 128 / esz ? cols : 128 / esz;
+    return (size_t)32 * cw * esz;
+}
 
 // The output offsets of the rows this lane stores (the same for every chunk of a tile), or -1
 // for rows outside the output.  Callers compute them before they wait for the accumulator:

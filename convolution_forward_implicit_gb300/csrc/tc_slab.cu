@@ -77,7 +77,9 @@ __global__ void __launch_bounds__(SlabRoles<TF32, (TF32 ? 1 : NACC)>::THREADS, 1
     const uint32_t sA = sbase;
     const uint32_t sB = sA + SA * a_stage;
     const uint32_t stg_off = SA * a_stage + SB * b_stage;
-    const uint32_t bar0 = sbase + stg_off + EPI_WARPS * STG_WARP_BYTES;
+    // each epilogue warp stages one chunk of its BN/2 columns: 32 rows x (BN/2 x element size)
+    constexpr uint32_t STG_W = stg_warp_bytes<(BN / 2 < 16 ? 16 : BN / 2), (TF32 ? 4 : 2)>();
+    const uint32_t bar0 = sbase + stg_off + EPI_WARPS * STG_W;
     auto full_a = [&](int s) { return bar0 + 8u * s; };
     auto empty_a = [&](int s) { return bar0 + 8u * (SLAB_MAX_SA + s); };
     auto cvt_a = [&](int s) { return bar0 + 8u * (2 * SLAB_MAX_SA + s); };
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(SlabRoles<TF32, (TF32 ? 1 : NACC)>::THREADS, 1
         const int cb_end = cb_begin + SCOLS < BN ? cb_begin + SCOLS : BN;
         const bool add_bias = p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU;
         const bool do_gelu = p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU;
-        uint8_t* stg = smem + stg_off + warp * STG_WARP_BYTES;
+        uint8_t* stg = smem + stg_off + warp * STG_W;
         if (p.pdl) griddep_wait();   // y and bias may belong to the previous kernel
         uint32_t tile_i = 0;
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x, ++tile_i) {
@@ -448,7 +450,7 @@ cudaError_t launch_slab_one(const TcParams& p, const CUtensorMap& map, int grid,
 
 size_t slab_smem_bytes(int BN, int tf32, int sa, int sb, size_t a_stage, int btaps) {
     const size_t b_stage = (size_t)btaps * BN * 128 * (tf32 ? 2 : 1);
-    return 1024 + (size_t)sa * a_stage + (size_t)sb * b_stage + (size_t)EPI_WARPS * STG_WARP_BYTES +
+    return 1024 + (size_t)sa * a_stage + (size_t)sb * b_stage + (size_t)EPI_WARPS * slab_stg_warp_bytes(BN, tf32 ? 4 : 2) +
            8 * (3 * SLAB_MAX_SA + 2 * SLAB_MAX_SB + 6) + 16;
 }
 

@@ -290,7 +290,7 @@ def test_cta_pair_plans(lib):
     tiles two at a time and the grid is even."""
     for name, li, want in [("sweep_bf16_n32", 0, False), ("sweep_bf16_n32", 1, True), ("sweep_bf16_n8", 0, False),
                            ("sweep_bf16_n8", 1, True), ("sweep_bf16_n1", 1, False), ("whisper_frontend_bf16", 1, False),
-                           ("grouped3d_g4_c64_d1", 0, False), ("whisper_frontend_f32", 1, False)]:
+                           ("whisper_frontend_f32", 1, False)]:
         wl = WORKLOADS[name]
         L = wl.layers[li]
         h = B.conv_plan_create(*L.plan_args(wl.dtype_code))
@@ -313,6 +313,35 @@ def test_cta_pair_plans(lib):
     finally:
         for k in ("CONV_FORCE_PAIR", "CONV_FORCE_BN", "CONV_FORCE_SPLITK"):
             os.environ.pop(k)
+
+
+def test_slab_cta_pair_plans(lib):
+    """Slab plans with tile pairs (two accumulators per unit) and N tiles of 32 or 64 run on
+    CTA pairs by rule when three slab stages and a ring of at least four weight stages fit
+    (each CTA holds half of every weight tile): the 3D dilation-1 configuration.  Shorter
+    rings and resident weights stay on single CTAs (measured slower as pairs), as do the
+    Whisper layers (one accumulator); CONV_FORCE_PAIR=1 still pairs them."""
+    for name, want, stages in [("grouped3d_g4_c64_d1", True, "3+5"), ("grouped3d_g4_c64_d2", False, None),
+                               ("grouped2d_g8_c64_d1", False, None), ("grouped2d_g32_c8_d1", False, None),
+                               ("whisper_frontend_bf16", False, None)]:
+        L = WORKLOADS[name].layers[0]
+        h = B.conv_plan_create(*L.plan_args(B.CONV_BF16))
+        d = dict(kv.split("=", 1) for kv in B.conv_plan_describe(h).split())
+        B.conv_plan_destroy(h)
+        assert (d.get("cta_pair") == "m256") == want, (name, d)
+        if want:
+            assert d["gather"] == "tma-slab" and d["acc"] == "2" and int(d["grid"]) % 2 == 0
+            if stages:
+                assert d["stages"] == stages, d
+    os.environ["CONV_FORCE_PAIR"] = "1"
+    try:
+        h = B.conv_plan_create(*WORKLOADS["grouped2d_g8_c64_d1"].layers[0].plan_args(B.CONV_BF16))
+        d = dict(kv.split("=", 1) for kv in B.conv_plan_describe(h).split())
+        B.conv_plan_destroy(h)
+        # resident weights: the pairs' grid is a multiple of the 8 weight sets, so each keeps its set
+        assert d["cta_pair"] == "m256" and d["stages"] == "3+1w" and (int(d["grid"]) // 2) % 8 == 0, d
+    finally:
+        os.environ.pop("CONV_FORCE_PAIR")
 
 
 def test_selector_scratch_covers_every_candidate(lib):

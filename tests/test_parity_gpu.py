@@ -557,3 +557,34 @@ def test_tensor_map_stores_are_bit_identical(name, layer, env):
     assert np.array_equal(on, off), f"{name}: tensor-map stores differ [{don}]"
     ref, S = oracle_full(layer, "bf16", x, w, b)
     assert_within("bf16", layer.epilogue, on, ref, S, don)
+
+
+SLAB_PAIR_CASES = [
+    # resident weights, groups, bias + GELU
+    ("2d_g2_c64_resident", L(2, 2, 2, 64, 64, (13, 21), (3, 3), (1, 1), (1, 1), (1, 1)), {}),
+    # packed small groups (8 groups of 8 channels per 64-channel tile), dilation 2
+    ("2d_g8_c8_packed_dil2", L(2, 2, 8, 8, 8, (15, 17), (3, 3), (1, 1), (2, 2), (2, 2), CONV_EPI_NONE), {}),
+    # streamed weights over three input planes (3D)
+    ("3d_streamed", L(3, 1, 2, 64, 64, (4, 20, 10), (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), CONV_EPI_BIAS),
+     {"CONV_FORCE_SLAB_STREAM": 1}),
+    # an odd number of slab units (the last pair's second unit lies past the output), 32-wide N tiles
+    ("2d_k32_odd_units", L(2, 1, 1, 64, 32, (15, 40), (3, 3), (1, 1), (1, 1), (1, 1), CONV_EPI_GELU), {}),
+]
+
+
+@pytest.mark.parametrize("name,layer,env", SLAB_PAIR_CASES, ids=[c[0] for c in SLAB_PAIR_CASES])
+def test_slab_cta_pairs_are_bit_identical(name, layer, env):
+    """Slab units on CTA pairs (each CTA its own slab and half of every weight tile, M = 256
+    MMAs) give the same bits as the single-CTA slab kernel and meet the bound against the
+    oracle."""
+    env = {"CONV_FORCE_SLAB_PAIR": 1, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_BN": 64 if layer.K * (64 // max(layer.C, 1)
+                                                                                           if layer.C < 64 else 1) >= 64
+                                                                              else 32, **env}
+    x, w, b = make_inputs(layer, "bf16", 990 + len(name))
+    on, don = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_PAIR": 1}, guard=64)
+    off, doff = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_PAIR": 0})
+    assert "cta_pair=m256" in don and "gather=tma-slab" in don and "acc=2" in don, don
+    assert "cta_pair" not in doff and "gather=tma-slab" in doff, doff
+    assert np.array_equal(on, off), f"{name}: slab CTA-pair result differs [{don}]"
+    ref, S = oracle_full(layer, "bf16", x, w, b)
+    assert_within("bf16", layer.epilogue, on, ref, S, don)
