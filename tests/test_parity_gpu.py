@@ -569,6 +569,9 @@ SLAB_PAIR_CASES = [
      {"CONV_FORCE_SLAB_STREAM": 1}),
     # an odd number of slab units (the last pair's second unit lies past the output), 32-wide N tiles
     ("2d_k32_odd_units", L(2, 1, 1, 64, 32, (15, 40), (3, 3), (1, 1), (1, 1), (1, 1), CONV_EPI_GELU), {}),
+    # dilation 2 in 3D with a short weight ring
+    ("3d_dil2_streamed", L(3, 1, 2, 64, 64, (6, 24, 56), (3, 3, 3), (1, 1, 1), (2, 2, 2), (2, 2, 2),
+                           CONV_EPI_BIAS), {"CONV_FORCE_SLAB_STREAM": 1}),
 ]
 
 
