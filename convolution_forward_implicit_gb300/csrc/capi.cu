@@ -470,19 +470,37 @@ static bool encode_act_map(const conv_plan* p, const void* x, CUtensorMap* map) 
     return r == CUDA_SUCCESS;
 }
 
-// The packed weights of a CTA-pair plan as a 2-D tensor of 128-byte rows (64 bf16), read in
-// boxes of BN/2 rows: each CTA of a pair loads its half of a weight tile.  The rows are copied
-// verbatim (they are already 128-byte swizzled by the prepack).
+// The packed weights of a CTA-pair plan as a tensor of 128-byte rows (64 bf16) from which each
+// CTA of a pair loads its half (BN/2 rows) of every weight tile: per-tap plans one tile per
+// copy, slab plans all the tap tiles of a weight stage in one copy (a second copy from the same
+// thread waits for the first, so one copy per tap made the first stages arrive microseconds
+// late).  The rows are copied verbatim (they are already 128-byte swizzled by the prepack).
 static bool encode_w_map(const conv_plan* p, const void* w_packed, CUtensorMap* map) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {64, (cuuint64_t)p->g.G * p->num_nt * p->nkb * p->BN};
-    cuuint64_t strides[1] = {128};
-    cuuint32_t box[2] = {64, (cuuint32_t)(p->BN / 2)};
-    cuuint32_t es[2] = {1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w_packed), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const cuuint64_t tiles = (cuuint64_t)p->g.G * p->num_nt * p->nkb;
+    const cuuint32_t half = (cuuint32_t)(p->BN / 2);
+    CUresult r;
+    if (p->slab) {
+        // {64 channels, BN/2 rows, 2 halves, tap tiles}: a box of one half of `slab_btaps`
+        // consecutive tap tiles is one slab weight stage of one CTA
+        cuuint64_t dims[4] = {64, half, 2, tiles};
+        cuuint64_t strides[3] = {128, (cuuint64_t)half * 128, (cuuint64_t)p->BN * 128};
+        cuuint32_t box[4] = {64, half, 1, (cuuint32_t)p->slab_btaps};
+        cuuint32_t es[4] = {1, 1, 1, 1};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(w_packed), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        // {64 channels, rows}: a box of BN/2 rows is one CTA's half of a tap tile
+        cuuint64_t dims[2] = {64, tiles * p->BN};
+        cuuint64_t strides[1] = {128};
+        cuuint32_t box[2] = {64, half};
+        cuuint32_t es[2] = {1, 1};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w_packed), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS;
 }
 

@@ -105,8 +105,13 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
         : "memory");
 }
+// Remote arrival of the odd CTA's epilogue on the leader's accumulator-empty barrier.  Relaxed:
+// it only says that this warp's tensor-memory loads have completed (tcgen05.wait::ld), which the
+// tcgen05 fence before it orders; a release at cluster scope would also hold the arrival until
+// the warp's global stores of y were acknowledged, which delayed every other unit of the 2D
+// grouped layers by 1-2 us (clock stamps).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 template <int BN, int STAGES, int EW>

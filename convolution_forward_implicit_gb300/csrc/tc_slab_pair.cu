@@ -78,15 +78,21 @@ __device__ __forceinline__ void sp_tma_5d(uint32_t dst, const CUtensorMap* map, 
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar_cluster)
         : "memory");
 }
-__device__ __forceinline__ void sp_tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar_cluster) {
+// one weight stage of this CTA: its half (BN/2 rows) of each of the stage's consecutive tap tiles
+__device__ __forceinline__ void sp_tma_w(uint32_t dst, const CUtensorMap* map, int half, int tap, uint32_t bar_cluster) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
-        "%3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+        "%3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(half), "r"(tap), "r"(bar_cluster)
         : "memory");
 }
+// Remote arrival of the odd CTA's epilogue on the leader's accumulator-empty barrier.  Relaxed:
+// it only says that this warp's tensor-memory loads have completed (tcgen05.wait::ld), which the
+// tcgen05 fence before it orders; a release at cluster scope would also hold the arrival until
+// the warp's global stores of y were acknowledged, which delayed every other unit of the 2D
+// grouped layers by 1-2 us (clock stamps).
 __device__ __forceinline__ void sp_arrive_cluster(uint32_t bar_cluster) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 // BY, BT: filter rows and columns fixed at compile time (3x3 filters), 0: from the parameters.
@@ -216,7 +222,6 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         if (lane == 0) {
             const int bw = warp - SP_B_WARP0;
             const int nchunk = p.slab_nkg * nbg;     // chunks of btaps taps, in slab order
-            const int rhalf = (int)crank * (BN / 2);
             bool aborted = false;
             if (p.slab_resident) {
                 // the weight set of the current (group, N tile), this CTA's half of every tap
@@ -236,10 +241,8 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
                     }
                     const int mine = nchunk > bw ? (nchunk - bw + SP_B_WARPS - 1) / SP_B_WARPS : 0;
                     if (leader) mbar_arrive_expect_tx(full_b(0), 2u * (uint32_t)mine * b_stage);
-                    const int row0 = key * p.nkb * BN + rhalf;
                     for (int c = bw; c < nchunk; c += SP_B_WARPS)
-                        for (int t = 0; t < btaps; ++t)
-                            sp_tma_2d(sB + c * b_stage + t * B_HALF, &w_map, 0, row0 + (c * btaps + t) * BN, fb);
+                        sp_tma_w(sB + c * b_stage, &w_map, (int)crank, key * p.nkb + c * btaps, fb);
                     ++j;
                 }
                 // the leader's release of the last weight set has arrived before exit
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
                 for (int u = u0; u < p.total_units && !aborted; u += ustep) {
                     int mt, gi, nt;
                     unit_tile(u, mt, gi, nt);
-                    const int row0 = (gi * p.num_nt + nt) * p.nkb * BN + rhalf;
+                    const int tap0 = (gi * p.num_nt + nt) * p.nkb;
                     for (int c = 0; c < nchunk; ++c, ++ib, rb.next()) {
                         const int s = rb.s;
                         if (s % SP_B_WARPS != bw) continue;
@@ -265,9 +268,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
                             break;
                         }
                         if (leader) mbar_arrive_expect_tx(full_b(s), 2u * b_stage);
-                        for (int t = 0; t < btaps; ++t)
-                            sp_tma_2d(sB + s * b_stage + t * B_HALF, &w_map, 0, row0 + (c * btaps + t) * BN,
-                                      fb0 + 8u * (uint32_t)s);
+                        sp_tma_w(sB + s * b_stage, &w_map, (int)crank, tap0 + c * btaps, fb0 + 8u * (uint32_t)s);
                     }
                 }
                 // every release of this warp's stages has arrived before exit
