@@ -10,11 +10,14 @@ Whisper-tiny frontend in fp32 and bf16, the sweep at batch 1 and 8, the grouped 
 layers) and reports each one's us per call and roofline fraction under `per_config`.
 
 Timing: W warm-up steps, then exactly K steps between CUDA events on the launching stream,
-bracketed by a barrier and a device synchronise.  A step is one CUDA graph holding every
-layer (each conv_fwd call: the conv kernel, plus the reduction for split plans); by
-default the plans chain their kernels as programmatic dependents (conv_plan_set_overlap),
-so each kernel's set-up and weight loads overlap the previous one (--no-overlap turns
-this off).  Each layer's device time comes from a second run of the same steps with timing
+bracketed by a barrier and a device synchronise.  A step runs every layer (each conv_fwd
+call: the conv kernel, plus the reduction for split plans); the steps are captured in CUDA
+graphs, one graph holding R consecutive steps (one per rotation set) that is replayed
+K // R times, then one single-step graph for each of the remaining K % R steps.  By default
+the plans chain their kernels as programmatic dependents (conv_plan_set_overlap), so each
+kernel's set-up and weight loads overlap the previous one, across steps too inside a graph
+(--no-overlap turns this off); a graph boundary after every step costs 4-7 us of launch
+latency, which a layer inside a larger graph does not pay.  Each layer's device time comes from a second run of the same steps with timing
 events recorded inside the graph between the layers (where PyTorch cannot record events
 inside a graph, each layer is its own graph and the events sit between them).  Steps
 rotate over enough copies of every input, packed weight and output that one rotation
@@ -381,13 +384,17 @@ def rotation_sets(wls, factor=1.0):
     return max(4, int(np.ceil(2.2 * L2_BYTES / per_set))), per_set
 
 
-def capture_steps(runs, R, with_events, parallel=False):
+def capture_steps(runs, R, with_events, parallel=False, chain=None):
     """One CUDA graph per rotation set holding every layer of the step.  With with_events,
     timing events are recorded between the layers inside the graph (they give each layer's
     device time, and they also keep consecutive layers from overlapping); returns (graphs,
     events), or None when this PyTorch cannot record events inside a graph.  With parallel,
     the step's independent chains (the layers of each workload) are captured as parallel
-    branches on their own streams, joined at the end of the step."""
+    branches on their own streams, joined at the end of the step.  With chain (a list of
+    rotation sets), one graph holds one step per listed set, one after the other, so that a
+    step's first kernel is launched as a programmatic dependent of the previous step's last
+    one, as it would be inside a larger graph, instead of after a graph boundary; returns
+    ([graph], None)."""
     import torch
     events = None
     if with_events:
@@ -411,27 +418,37 @@ def capture_steps(runs, R, with_events, parallel=False):
     chains = list(chains.values())
     branch = parallel and not events and len(chains) > 1
     side = [torch.cuda.Stream() for _ in range(len(chains) - 1)] if branch else []
+
+    def emit_step(r, cs):
+        if branch:
+            for ss in side:
+                ss.wait_stream(cs)
+            for ci, chain_ in enumerate(chains):
+                with torch.cuda.stream(cs if ci == 0 else side[ci - 1]):
+                    for lr in chain_:
+                        lr.call(r)
+            for ss in side:
+                cs.wait_stream(ss)
+        else:
+            if events:
+                events[r][0].record(cs)
+            for j, lr in enumerate(runs):
+                lr.call(r)
+                if events:
+                    events[r][j + 1].record(cs)
+
+    if chain is not None:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream()
+            for r in chain:
+                emit_step(r, cs)
+        return [g], None
     graphs = []
     for r in range(R):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            cs = torch.cuda.current_stream()
-            if branch:
-                for ss in side:
-                    ss.wait_stream(cs)
-                for ci, chain in enumerate(chains):
-                    with torch.cuda.stream(cs if ci == 0 else side[ci - 1]):
-                        for lr in chain:
-                            lr.call(r)
-                for ss in side:
-                    cs.wait_stream(ss)
-            else:
-                if events:
-                    events[r][0].record(cs)
-                for j, lr in enumerate(runs):
-                    lr.call(r)
-                    if events:
-                        events[r][j + 1].record(cs)
+            emit_step(r, torch.cuda.current_stream())
         graphs.append(g)
     return graphs, events
 
@@ -454,32 +471,40 @@ def prepare(args, wls, bwd=False):
     if args.overlap:
         for lr in runs:
             lr.plan.set_overlap(True)
-    # timed steps: one graph per step with no events inside, so consecutive kernels may overlap
+    # timed steps: graphs with no events inside, so consecutive kernels may overlap; one graph
+    # per step, and one holding all R steps in rotation order
     step_graphs, _ = capture_steps(runs, R, with_events=False, parallel=args.parallel)
+    chain_graph = capture_steps(runs, R, with_events=False, parallel=args.parallel, chain=list(range(R)))[0][0]
     # per-layer device times: the same steps with events between the layers
     cap = capture_steps(runs, R, with_events=True)
     if cap is not None:
         layer_graphs, gev = cap
-        graph_mode = ("one graph per step (all layers" + (", chained as programmatic dependents" if args.overlap else "")
+        graph_mode = (f"steps timed through one graph of {R} consecutive steps (one per rotation set; all layers"
+                      + (", chained as programmatic dependents" if args.overlap else "")
                       + ("; independent workloads as parallel branches" if args.parallel and len(wls) > 1 else "")
-                      + "); per-layer times from a second run of graphs with events between the layers")
+                      + "), replayed K // R times, then one graph per step for the remaining K % R; per-layer "
+                      "times from a second run of one graph per step with events between the layers")
     else:
         for lr in runs:
             lr.capture(R)
         layer_graphs, gev = None, None
-        graph_mode = "one graph per step; per-layer times from one graph per layer with events between graphs"
+        graph_mode = (f"steps timed through one graph of {R} consecutive steps, replayed K // R times, then one graph "
+                      "per step for the remaining K % R; per-layer times from one graph per layer with events between "
+                      "graphs")
     torch.cuda.synchronize()
     return {"R": R, "per_set": per_set, "runs": runs, "host_in": host_in, "out_sets": out_sets,
-            "step_graphs": step_graphs, "layer_graphs": layer_graphs, "gev": gev, "graph_mode": graph_mode}
+            "step_graphs": step_graphs, "chain_graph": chain_graph, "layer_graphs": layer_graphs, "gev": gev,
+            "graph_mode": graph_mode}
 
 
 def time_steps(st, K, W, stream, ws=1, on_start=None):
     """W warm-up steps, then K steps of the step graphs between CUDA events (barrier and
     synchronise on both sides); returns the total ms (max over ranks by the caller)."""
     import torch
-    R, graphs = st["R"], st["step_graphs"]
+    R, graphs, chain = st["R"], st["step_graphs"], st["chain_graph"]
     for i in range(W):
         graphs[i % R].replay()
+    chain.replay()
     torch.cuda.synchronize()
     for lr in st["runs"]:
         lr.plan.check()
@@ -488,9 +513,12 @@ def time_steps(st, K, W, stream, ws=1, on_start=None):
         on_start()
     barrier(ws)
     torch.cuda.synchronize()
+    # exactly K steps: K // R replays of the R-step graph, then single steps (rotation sets 0..)
     e0.record(stream)
-    for i in range(K):
-        graphs[i % R].replay()
+    for i in range(K // R):
+        chain.replay()
+    for i in range(K % R):
+        graphs[i].replay()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
@@ -560,15 +588,18 @@ def release(st):
 
 def per_config_table(args, names, stream, done=None):
     """Every configuration in `names`, each measured the way the headline is (rotating
-    buffers larger than twice the L2, one graph per step, per-layer events): us per step and
-    per layer, useful TFLOP/s and each layer's roofline fraction."""
-    K, W = min(args.steps, 50), max(3, min(args.warmup, 5))
+    buffers larger than twice the L2, graphs of R consecutive steps, per-layer events): us per
+    step and per layer, useful TFLOP/s and each layer's roofline fraction."""
+    W = max(3, min(args.warmup, 5))
     table = {}
     for name in names:
         if done is not None and name in done:
             table[name] = done[name]
             continue
         st = prepare(args, frontend_workloads(name))
+        # about 50 steps (at most --steps), a whole number of R-step graphs
+        R = st["R"]
+        K = R * max(1, round(min(args.steps, 50) / R))
         ms = time_steps(st, K, W, stream) / K
         per_layer_ms, _ = time_layers(st, K, W, stream)
         runs = st["runs"]
@@ -585,6 +616,11 @@ def config_entry(runs, ms, per_layer_ms, K):
         roof = roofline_for(lr, t)
         layers[lr.name()] = {"us_per_call": round(t * 1e3, 3), "tflops": round(lr.flops / (t * 1e-3) / 1e12, 2),
                              "roofline_frac": roof["frac"], "bound": roof["bound"], "plan": lr.plan.describe()}
+    if len(runs) == 1:
+        # one layer per step: the step time is the call's time inside a graph of consecutive
+        # calls (no event around it, launched as a programmatic dependent of the previous call)
+        roof = roofline_for(runs[0], ms)
+        layers[runs[0].name()].update({"us_per_call_chained": round(ms * 1e3, 3), "roofline_frac_chained": roof["frac"]})
     return {"us_per_step": round(ms * 1e3, 3), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
             "gflop_per_step": round(flops / 1e9, 3), "steps": K, "layers": layers}
 
@@ -624,14 +660,19 @@ def run_ours(args, ws, rank, local):
     ms_per_step = total_ms / K
     value = ws * step_flops / (ms_per_step * 1e-3) / 1e12
 
-    # ---- hot L2 (the same rotation set every step) and the latency of one isolated step
+    # ---- hot L2 (the same rotation set every step, R steps per graph as in the timed run) and
+    # the latency of one isolated step
     g0 = st["step_graphs"][0]
+    hot_graph = capture_steps(runs, R, with_events=False, parallel=args.parallel, chain=[0] * R)[0][0]
     for i in range(args.warmup):
         g0.replay()
+    hot_graph.replay()
     torch.cuda.synchronize()
     eh0, eh1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     eh0.record(stream)
-    for i in range(K):
+    for i in range(K // R):
+        hot_graph.replay()
+    for i in range(K % R):
         g0.replay()
     eh1.record(stream)
     torch.cuda.synchronize()
