@@ -758,8 +758,8 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     // pair of SMs at least once.  Each SM then stores and reads half of every weight tile
     // (~64 KB instead of ~96 KB of shared-memory traffic per K block of 128x256 outputs).
     // Measured on the 128 -> 1280 -> 1280 conv1d at batch 32: the 60-block layer 309 -> 287 us;
-    // the 6-block layer with 16 epilogue warps (4 ring stages as pairs) 105 -> 129 us, so plans
-    // with the wide epilogue keep single CTAs unless forced.
+    // the 6-block layer with 16 epilogue warps 102 -> 107 us, so plans with the wide epilogue
+    // keep single CTAs unless forced.
     p->pair = 0;
     // Slab plans with tile pairs on CTA pairs (tc_slab_pair.cu): each CTA keeps its own slab and
     // half of every weight tile, and each M = 256 MMA reads a weight half per SM.  The rings are
@@ -788,7 +788,8 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
         // is refilled only after both CTAs' copies of it were read, which shorter rings do not
         // cover, and with resident weights the units' epilogues (both CTAs') set the pace.
         // Measured (us per call, single CTA -> pair): 3D d1, 3 + 5 stages: 190.9 -> 137.4; 3D d2,
-        // 3 + 2: 168.8 -> 336.8; 2D d2, 3 + 2: 39.3 -> 75.7; 2D d1, resident weights: 38.8 -> 47.0.
+        // 3 + 2: 168.3 -> 331.7; 2D d2, 3 + 2: 39.9 -> 72.6; 2D d1, resident weights: 39.3 -> 39.8,
+        // streamed (3 + 5): 39.3 -> 41.9.
         if ((sa >= 3 && !resident && sb >= 4) || (sa && p->ch.pair == 1)) {
             const size_t smem = slab_pair_smem_bytes(bn, sa, sb, (size_t)p->slab_a_stage, p->slab_btaps);
             int clusters = p->sm_count / 2;
