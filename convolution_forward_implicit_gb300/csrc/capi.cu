@@ -761,13 +761,11 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
     // the 6-block layer with 16 epilogue warps 102 -> 107 us, so plans with the wide epilogue
     // keep single CTAs unless forced.
     p->pair = 0;
-    // Slab plans with tile pairs on CTA pairs (tc_slab_pair.cu): each CTA keeps its own slab and
-    // half of every weight tile, and each M = 256 MMA reads a weight half per SM.  The rings are
-    // refitted for half-size weight stages (resident weight sets where they fit, with a third
-    // slab stage where possible).
-    if (p->slab && !tf32 && p->slab_nacc == 2 && (bn == 32 || bn == 64) && p->splits == 1 && p->num_mt >= 2 &&
-        !p->lat.on && p->ch.pair != 0) {
-        const int64_t pair_units = cdiv(p->num_mt, 2) * g.G * p->num_nt;
+    // Slab plans on CTA pairs (tc_slab_pair.cu): each CTA keeps its own slab and half of every
+    // weight tile, and each M = 256 MMA reads a weight half per SM.  The rings are refitted for
+    // half-size weight stages (resident weight sets where they fit, with a third slab stage
+    // where possible).
+    if (p->slab && !tf32 && (bn == 32 || bn == 64) && p->splits == 1 && !p->lat.on && p->ch.pair != 0) {
         const int nchunk = p->slab_nkg * p->slab_nbg;
         // three slab stages first (resident weights, else a ring of weight stages of one filter
         // row each), then two.  (Stages of one tap each, which would let more of them fit, were
@@ -790,7 +788,14 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
         // Measured (us per call, single CTA -> pair): 3D d1, 3 + 5 stages: 190.9 -> 137.4; 3D d2,
         // 3 + 2: 168.3 -> 331.7; 2D d2, 3 + 2: 39.9 -> 72.6; 2D d1, resident weights: 39.3 -> 39.8,
         // streamed (3 + 5): 39.3 -> 41.9.
-        if ((sa >= 3 && !resident && sb >= 4) || (sa && p->ch.pair == 1)) {
+        // Slab units of one accumulator per CTA run as pairs only on request (CONV_FORCE_PAIR=1
+        // with a one-accumulator plan): each slab then serves half the MMAs, and on the 3D layers
+        // they measured slower than single CTAs with tile pairs (d2, 3 + 5 stages: 164.2 ->
+        // 182.4 us; d1: 137 -> 226 us against tile pairs).
+        const bool ok = p->num_mt >= 2 && ((sa >= 3 && !resident && sb >= 4 && p->slab_nacc == 2) ||
+                                           (sa && p->ch.pair == 1));
+        if (ok) {
+            const int64_t pair_units = cdiv(p->num_mt, 2) * g.G * p->num_nt;
             const size_t smem = slab_pair_smem_bytes(bn, sa, sb, (size_t)p->slab_a_stage, p->slab_btaps);
             int clusters = p->sm_count / 2;
             int dev = 0;
@@ -995,7 +1000,9 @@ static void tune_table_lookup(const conv_plan* p, PlanChoice& c) {
 }
 
 // The candidates the selector times: the rules' own plan, each N tile x split factor x
-// gather mode, and the FFMA kernel; candidates that land on the same plan are timed once.
+// gather mode, CTA pairs and weight multicast for wide tiles, slab units of one or two
+// accumulators on one CTA or a pair for narrow ones, and the FFMA kernel; candidates that land
+// on the same plan are timed once.
 static std::vector<conv_plan> tune_candidates(const conv_plan* p) {
     std::vector<PlanChoice> cs;
     cs.push_back(PlanChoice{});
@@ -1013,6 +1020,13 @@ static std::vector<conv_plan> tune_candidates(const conv_plan* p) {
         c.pair = 1; cs.push_back(c);
         c.pair = 0; c.mc = 1; cs.push_back(c);
     }
+    for (int bn : {32, 64})        // slab units of one or two accumulators, on one CTA or a pair
+        for (int tp : {0, 1})
+            for (int pr : {0, 1}) {
+                PlanChoice c;
+                c.bn = bn; c.splits = 1; c.slab_pair = tp; c.pair = pr;
+                cs.push_back(c);
+            }
     PlanChoice f;
     f.simt = 1;
     cs.push_back(f);

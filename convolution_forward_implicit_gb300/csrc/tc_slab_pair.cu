@@ -96,13 +96,14 @@ __device__ __forceinline__ void sp_arrive_cluster(uint32_t bar_cluster) {
 }
 
 // BY, BT: filter rows and columns fixed at compile time (3x3 filters), 0: from the parameters.
-// Units are pairs of slab units (each a tile pair of two 128-row accumulators stacked along H);
-// the CTA of cluster rank r takes slab unit 2 mt + r.
-template <int BN, int BY, int BT>
+// NACC: 128-row accumulators per CTA and unit, stacked along H (2: a tile pair sharing one slab;
+// 1: one accumulator per slab, for slabs too tall to leave room for a weight ring), each issued
+// by its own MMA warp.  Units are pairs of slab units; the CTA of cluster rank r takes slab unit
+// 2 mt + r.
+template <int BN, int BY, int BT, int NACC>
 __global__ void __launch_bounds__(SP_THREADS, 1)
     conv_fwd_slab_pair_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map,
                               const __grid_constant__ CUtensorMap w_map) {
-    constexpr int NACC = 2;
     constexpr uint32_t B_HALF = (BN / 2) * 128;                 // one tap's half weight tile
     constexpr uint32_t TMEM_COLS = (2 * NACC * BN < 32) ? 32 : 2 * NACC * BN;
     const int SA = p.slab_sa, SB = p.slab_sb;
@@ -141,22 +142,22 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < SA; ++s) {
             mbar_init(full_a(s), 1);          // the leader's slab warp (both CTAs' bytes)
-            mbar_init(empty_a(s), 2);         // the leader's two MMA warps, multicast to both
+            mbar_init(empty_a(s), NACC);      // the leader's MMA warps, multicast to both
         }
         if (p.slab_resident) {
             mbar_init(full_b(0), SP_B_WARPS);
-            mbar_init(empty_b(0), 2);
+            mbar_init(empty_b(0), NACC);
         } else {
             for (int s = 0; s < SB; ++s) {
                 mbar_init(full_b(s), 1);
-                mbar_init(empty_b(s), 2);
+                mbar_init(empty_b(s), NACC);
             }
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(tfull_bar(a), 2);
+            mbar_init(tfull_bar(a), NACC);
             mbar_init(tempty_bar(a), 2 * EPI_WARPS);   // both CTAs' epilogue warps (used in the leader)
         }
-        for (int mw = 0; mw < 2; ++mw) mbar_init(drain_bar(mw), 1);
+        for (int mw = 0; mw < NACC; ++mw) mbar_init(drain_bar(mw), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp >= SP_MMA_WARP && warp < SP_MMA_WARP + 2) {
+    } else if (warp >= SP_MMA_WARP && warp < SP_MMA_WARP + NACC) {
         // ------------------------------------------------------------ MMA issue (leader only)
         // warp mw issues accumulator mw of every unit; both wait for the same stages
         const int mw = warp - SP_MMA_WARP;
@@ -427,10 +428,10 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     }
 }
 
-template <int BN, int BY, int BT>
+template <int BN, int BY, int BT, int NACC>
 cudaError_t launch_slab_pair_one(const TcParams& p, const CUtensorMap& amap, const CUtensorMap& wmap, int grid,
                                  size_t smem, cudaStream_t stream) {
-    auto kern = conv_fwd_slab_pair_kernel<BN, BY, BT>;
+    auto kern = conv_fwd_slab_pair_kernel<BN, BY, BT, NACC>;
     static bool attr_set[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -465,7 +466,7 @@ int slab_pair_max_clusters(size_t smem) {
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    auto kern = conv_fwd_slab_pair_kernel<64, 3, 3>;
+    auto kern = conv_fwd_slab_pair_kernel<64, 3, 3, 2>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SLAB_SMEM_MAX) != cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -480,17 +481,17 @@ int slab_pair_max_clusters(size_t smem) {
 
 cudaError_t launch_slab_pair(const TcParams& p, const CUtensorMap* act_map, const CUtensorMap* w_map, int grid,
                              size_t smem, cudaStream_t stream) {
-    if (!act_map || !w_map || p.tf32 || p.lat.on || p.slab_nacc != 2 || (grid & 1) || p.slab_sa < 2 ||
+    if (!act_map || !w_map || p.tf32 || p.lat.on || p.slab_nacc < 1 || p.slab_nacc > 2 || (grid & 1) || p.slab_sa < 2 ||
         p.slab_sa > SP_MAX_SA || (!p.slab_resident && (p.slab_sb < 2 || p.slab_sb > SP_MAX_SB)) ||
         smem > SLAB_SMEM_MAX)
         return cudaErrorInvalidValue;
-#define X(bn)                                                                                           \
-    if (p.BN == bn) {                                                                                   \
+#define X(bn, nacc)                                                                                     \
+    if (p.BN == bn && p.slab_nacc == nacc) {                                                            \
         if (p.slab_btaps == 3 && p.slab_nbg == 3)                                                       \
-            return launch_slab_pair_one<bn, 3, 3>(p, *act_map, *w_map, grid, smem, stream);             \
-        return launch_slab_pair_one<bn, 0, 0>(p, *act_map, *w_map, grid, smem, stream);                 \
+            return launch_slab_pair_one<bn, 3, 3, nacc>(p, *act_map, *w_map, grid, smem, stream);       \
+        return launch_slab_pair_one<bn, 0, 0, nacc>(p, *act_map, *w_map, grid, smem, stream);           \
     }
-    X(32) X(64)
+    X(32, 2) X(64, 2) X(32, 1) X(64, 1)
 #undef X
     return cudaErrorInvalidValue;
 }

@@ -591,3 +591,32 @@ def test_slab_cta_pairs_are_bit_identical(name, layer, env):
     assert np.array_equal(on, off), f"{name}: slab CTA-pair result differs [{don}]"
     ref, S = oracle_full(layer, "bf16", x, w, b)
     assert_within("bf16", layer.epilogue, on, ref, S, don)
+
+
+ONE_ACC_PAIR_CASES = [
+    # 3D dilation 2 (the rules' plan for the 3D G=4 C=K=64 d2 shape, at a smaller size)
+    ("3d_dil2", L(3, 1, 2, 64, 64, (6, 20, 56), (3, 3, 3), (1, 1, 1), (1, 1, 1), (2, 2, 2), CONV_EPI_BIAS), {}),
+    # 2D, an odd number of slab units (the last pair's second unit lies past the output), GELU,
+    # streamed weights
+    ("2d_odd_units_gelu", L(2, 1, 1, 64, 64, (13, 40), (3, 3), (1, 1), (1, 1), (1, 1), CONV_EPI_GELU),
+     {"CONV_FORCE_SLAB_STREAM": 1}),
+    # 32-wide N tiles, two groups, resident weights
+    ("2d_g2_k32", L(2, 2, 2, 64, 32, (20, 30), (3, 3), (1, 1), (1, 1), (1, 1), CONV_EPI_BIAS), {}),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,layer,env", ONE_ACC_PAIR_CASES, ids=[c[0] for c in ONE_ACC_PAIR_CASES])
+def test_slab_cta_pairs_with_one_accumulator_are_bit_identical(name, layer, env):
+    """Slab units of one accumulator per CTA on CTA pairs (M = 256 MMAs, one issuing warp) give
+    the same bits as the single-CTA slab kernel with one accumulator, and meet the bound
+    against the oracle."""
+    env = {"CONV_FORCE_SLAB_PAIR": 0, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_BN": 64 if layer.K >= 64 else 32, **env}
+    x, w, b = make_inputs(layer, "bf16", 1990 + len(name))
+    on, don = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_PAIR": 1}, guard=64)
+    off, doff = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_PAIR": 0})
+    assert "cta_pair=m256" in don and "gather=tma-slab" in don and "acc=1" in don, don
+    assert "cta_pair" not in doff and "gather=tma-slab" in doff and "acc=1" in doff, doff
+    assert np.array_equal(on, off), f"{name}: one-accumulator CTA-pair result differs [{don}]"
+    ref, S = oracle_full(layer, "bf16", x, w, b)
+    assert_within("bf16", layer.epilogue, on, ref, S, don)
