@@ -297,11 +297,12 @@ struct PlanChoice {
     int mc = -1;           // 0 / 1: CTA pairs sharing weight tiles by multicast off / on
     int pair = -1;         // 0 / 1: M = 256 tiles over CTA pairs (.cta_group::2 MMAs) off / on
     int ystore = -1;       // 0: per-lane stores of y even where a tensor-map (TMA) store could serve
+    int slab_bw = 0;       // > 0: slab tiles this many output columns wide
     bool operator==(const PlanChoice& o) const {
         return simt == o.simt && no_pack == o.no_pack && bn == o.bn && bm == o.bm && splits == o.splits &&
                gather == o.gather && slab_stream == o.slab_stream && slab_pair == o.slab_pair &&
                epi_warps == o.epi_warps && cluster_red == o.cluster_red && mc == o.mc && pair == o.pair &&
-               ystore == o.ystore;
+               ystore == o.ystore && slab_bw == o.slab_bw;
     }
 };
 
@@ -383,6 +384,7 @@ static bool choice_from_env(PlanChoice& c) {
     take("CONV_FORCE_MC", c.mc);
     take("CONV_FORCE_PAIR", c.pair);
     take("CONV_FORCE_YSTORE", c.ystore);
+    take("CONV_FORCE_SLAB_BW", c.slab_bw);
     if (const char* v = getenv("CONV_FORCE_GATHER")) {
         if (strcmp(v, "cpasync") == 0) { c.gather = 1; any = true; }
         else if (strcmp(v, "tma") == 0) { c.gather = 2; any = true; }
@@ -548,11 +550,21 @@ static void choose_tile_shape(conv_plan* p) {
 // Slab geometry for a stride-1 problem (see tc_slab.cu): output tiles of BH rows x BW columns
 // whose slab (BH + dh(Y-1)) x (BW + dw(X-1)) input pixels fit a 128-row accumulator.  Returns
 // false when the problem has no such tile.
+static bool set_slab_width(conv_plan* p, int bw);
 static bool choose_slab_shape(conv_plan* p) {
     const Geom& g = p->g;
-    const int reach_w = g.dw * (g.X - 1), reach_h = g.dh * (g.Y - 1);
-    const int bw = std::min(g.Wo, 128 - reach_w);
+    const int reach_w = g.dw * (g.X - 1);
+    int bw = std::min(g.Wo, 128 - reach_w);
+    if (p->ch.slab_bw > 0) bw = std::min(bw, p->ch.slab_bw);
     if (bw < 8) return false;
+    return set_slab_width(p, bw);
+}
+
+// Slab geometry for tiles bw output columns wide: as many output rows as fit a 128-row
+// accumulator at the slab's row pitch bw + dw(X-1).
+static bool set_slab_width(conv_plan* p, int bw) {
+    const Geom& g = p->g;
+    const int reach_w = g.dw * (g.X - 1), reach_h = g.dh * (g.Y - 1);
     const int bws = bw + reach_w;
     const int bh = std::max(1, std::min(g.Ho, 128 / bws));
     const int hr = bh + reach_h;
@@ -772,16 +784,20 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
         // measured 2.35x slower on the 3D d1 layer: four MMAs a stage cannot cover the pair's
         // hand-off of a stage.)
         int sa = 0, sb = 0, resident = 0;
-        for (int a = 3; a >= 2 && !sa; --a) {
-            if (p->ch.slab_stream == 0 &&
-                slab_pair_smem_bytes(bn, a, nchunk, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
-                sa = a; sb = nchunk; resident = 1;
-            }
-            for (int b = 8; b >= 2 && !sa; --b)
-                if (slab_pair_smem_bytes(bn, a, b, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
-                    sa = a; sb = b;
+        auto fit_pair_rings = [&]() {
+            sa = sb = resident = 0;
+            for (int a = 3; a >= 2 && !sa; --a) {
+                if (p->ch.slab_stream == 0 &&
+                    slab_pair_smem_bytes(bn, a, nchunk, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
+                    sa = a; sb = nchunk; resident = 1;
                 }
-        }
+                for (int b = 8; b >= 2 && !sa; --b)
+                    if (slab_pair_smem_bytes(bn, a, b, (size_t)p->slab_a_stage, p->slab_btaps) <= SLAB_SMEM_MAX) {
+                        sa = a; sb = b;
+                    }
+            }
+        };
+        fit_pair_rings();
         // By rule pairs need three slab stages and a ring of at least four weight stages: a stage
         // is refilled only after both CTAs' copies of it were read, which shorter rings do not
         // cover, and with resident weights the units' epilogues (both CTAs') set the pace.
@@ -792,8 +808,23 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
         // with a one-accumulator plan): each slab then serves half the MMAs, and on the 3D layers
         // they measured slower than single CTAs with tile pairs (d2, 3 + 5 stages: 164.2 ->
         // 182.4 us; d1: 137 -> 226 us against tile pairs).
-        const bool ok = p->num_mt >= 2 && ((sa >= 3 && !resident && sb >= 4 && p->slab_nacc == 2) ||
-                                           (sa && p->ch.pair == 1));
+        auto by_rule = [&]() { return p->num_mt >= 2 && sa >= 3 && !resident && sb >= 4 && p->slab_nacc == 2; };
+        bool ok = by_rule() || (p->num_mt >= 2 && sa && p->ch.pair == 1);
+        // A tile-pair slab too tall for that ring (dilation 2 in 3D: 8 input rows of 58 pixels
+        // leave room for two weight stages) is made narrower instead: tiles of half the output
+        // width hold twice the output rows, so the pair's slab has 12 rows of 31 pixels (47 KB
+        // against 59 KB) and the ring of the dilation-1 layer fits.
+        const int reach_w = g.dw * (g.X - 1);
+        if (!ok && !resident && p->slab_nacc == 2 && p->ch.pair != 1 && p->ch.slab_bw <= 0) {
+            const conv_plan saved = *p;
+            for (int k = 2; k <= 4 && !ok; ++k) {
+                const int bw = (int)cdiv(g.Wo, k);
+                if (bw < 8 || bw + reach_w > 128 || !set_slab_width(p, bw) || !set_slab_pair(p, true)) break;
+                fit_pair_rings();
+                ok = by_rule();
+            }
+            if (!ok) *p = saved;
+        }
         if (ok) {
             const int64_t pair_units = cdiv(p->num_mt, 2) * g.G * p->num_nt;
             const size_t smem = slab_pair_smem_bytes(bn, sa, sb, (size_t)p->slab_a_stage, p->slab_btaps);

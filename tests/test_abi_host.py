@@ -318,11 +318,12 @@ def test_cta_pair_plans(lib):
 def test_slab_cta_pair_plans(lib):
     """Slab plans with tile pairs and N tiles of 32 or 64 run on CTA pairs by rule when three
     slab stages and a ring of at least four weight stages fit (each CTA holds half of every
-    weight tile): the 3D dilation-1 configuration.  Shorter rings (3D dilation 2: its 8-row
-    slab leaves room for two weight stages) and resident weights stay on single CTAs (measured
-    slower or no faster as pairs), as do the Whisper layers (too few units);
-    CONV_FORCE_PAIR=1 still pairs them."""
-    for name, want, stages, acc in [("grouped3d_g4_c64_d1", True, "3+5", "2"), ("grouped3d_g4_c64_d2", False, None, "2"),
+    weight tile): the 3D dilation-1 configuration, and the 3D dilation-2 one with tiles of half
+    the output width (its full-width tile-pair slab of 8 rows leaves room for two weight stages;
+    the narrow one has 12 rows of 31 pixels).  Resident weights stay on single CTAs (measured
+    no faster as pairs), as do the Whisper layers (too few units); CONV_FORCE_PAIR=1 still
+    pairs them."""
+    for name, want, stages, acc in [("grouped3d_g4_c64_d1", True, "3+5", "2"), ("grouped3d_g4_c64_d2", True, "3+5", "2"),
                                     ("grouped2d_g8_c64_d1", False, None, "2"), ("grouped2d_g8_c64_d2", False, None, "2"),
                                     ("grouped2d_g32_c8_d1", False, None, "2"), ("whisper_frontend_bf16", False, None, None)]:
         L = WORKLOADS[name].layers[0]
@@ -336,6 +337,8 @@ def test_slab_cta_pair_plans(lib):
             assert d["gather"] == "tma-slab" and int(d["grid"]) % 2 == 0
             if stages:
                 assert d["stages"] == stages, d
+        if name == "grouped3d_g4_c64_d2":
+            assert d["pixels"] == "8x27" and d["slab"] == "12x31", d
     os.environ["CONV_FORCE_PAIR"] = "1"
     try:
         h = B.conv_plan_create(*WORKLOADS["grouped2d_g8_c64_d1"].layers[0].plan_args(B.CONV_BF16))

@@ -572,6 +572,10 @@ SLAB_PAIR_CASES = [
     # dilation 2 in 3D with a short weight ring
     ("3d_dil2_streamed", L(3, 1, 2, 64, 64, (6, 24, 56), (3, 3, 3), (1, 1, 1), (2, 2, 2), (2, 2, 2),
                            CONV_EPI_BIAS), {"CONV_FORCE_SLAB_STREAM": 1}),
+    # dilation 2 in 3D on tiles of half the output width (27 of 54 columns, slab rows of 31
+    # pixels), the plan the rules choose for the full-size 3D d2 layer
+    ("3d_dil2_narrow", L(3, 1, 2, 64, 64, (6, 24, 56), (3, 3, 3), (1, 1, 1), (1, 1, 1), (2, 2, 2),
+                         CONV_EPI_BIAS), {"CONV_FORCE_SLAB_BW": 27}),
 ]
 
 
