@@ -506,8 +506,8 @@ static bool encode_w_map(const conv_plan* p, const void* w_packed, CUtensorMap* 
     return r == CUDA_SUCCESS;
 }
 
-// y as a 5-D tensor {G*K, Wo, Ho, Do, N} for TMA stores of 64 channels x 32 pixels along Wo
-// (bf16, 128-byte swizzle: the epilogue's staging layout).
+// y as a 5-D tensor {G*K, Wo, Ho, Do, N} for TMA stores of one warp's chunk, 64 or 32 channels
+// x 32 pixels along Wo (bf16, 128- or 64-byte swizzle: the epilogue's staging layout).
 static bool encode_y_map(const conv_plan* p, const void* y, CUtensorMap* map) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
@@ -518,11 +518,12 @@ static bool encode_y_map(const conv_plan* p, const void* y, CUtensorMap* map) {
     strides[1] = strides[0] * dims[1];
     strides[2] = strides[1] * dims[2];
     strides[3] = strides[2] * dims[3];
-    cuuint32_t box[5] = {64, 32, 1, 1, 1};
+    const int cw = tc_store_cols(p->BN, p->epi_warps, p->pair != 0);
+    cuuint32_t box[5] = {(cuuint32_t)cw, 32, 1, 1, 1};
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(y), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, cw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -883,14 +884,14 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
         }
     }
     // Epilogue stores through a tensor map of y (bf16 per-tap plans, no split, tiles of one output
-    // row whose width is a multiple of 32, 64-column chunks per warp, and columns that never
-    // run into the next group): each warp's staged 32 x 64 block leaves as one TMA store.  By
+    // row whose width is a multiple of 32, chunks of 64 or 32 columns per warp, and columns that
+    // never run into the next group): each warp's staged 32-row block leaves as one TMA store.  By
     // rule where CTAs run several tiles (measured on the conv1d sweep: 128 -> 1280 at batch 32
     // 107.0 -> 102.2 us; at batch 1, one tile per CTA, the final wait for the stores made it
     // 0.6 us slower).
     p->ystore = 0;
     if (!tf32 && p->tma && !p->slab && p->splits == 1 && !p->cluster_red && !p->lat.on && p->BH == 1 &&
-        p->BW % 32 == 0 && (g.G == 1 || g.K % 64 == 0) && bn / (p->epi_warps / 4) >= 64 &&
+        p->BW % 32 == 0 && (g.G == 1 || g.K % 64 == 0) && tc_store_cols(bn, p->epi_warps, p->pair != 0) >= 32 &&
         (p->ch.ystore >= 0 ? p->ch.ystore == 1 : p->total_units > p->sm_count))
         p->ystore = 1;
     if (p->slab)

@@ -171,6 +171,15 @@ struct TcParams {
 
 constexpr size_t SLAB_SMEM_MAX = 232448;   // dynamic shared memory a block may opt in to
 
+// Output columns one epilogue warp of the per-tap kernels (one CTA or a pair) stages and stores
+// at a time for bf16 outputs: its columns, up to 64 (a 128-byte row segment).  (Chunks of 32
+// for 256-wide tiles with 16 epilogue warps would halve their staging and make room for a
+// fourth ring stage: measured no faster, since the three producer warps keep three stages in
+// flight either way.)
+__host__ __device__ constexpr int tc_store_cols(int bn, int ew, bool pair) {
+    return (void)pair, (bn / (ew / 4) < 64 ? bn / (ew / 4) : 64);
+}
+
 // Launch the tensor-core kernel for the (BN, stages) pair the plan picked (see tc_stages_for).
 cudaError_t launch_tc(const TcParams& p, const CUtensorMap* act_map, const CUtensorMap* y_map, int stages, int grid,
                       cudaStream_t stream);

@@ -420,10 +420,10 @@ struct YBox {
 };
 
 // One warp's share of a tile's epilogue: its 32 accumulator rows (TMEM lane quarter wq) and
-// the columns [cb_begin, cb_end) of the BN-wide tile, COLS of them at most.  QW32: read TMEM
-// 32 columns at a time where the chunk allows (fewer round trips, more registers).  With ymap
-// (bf16 outputs in 64-column chunks), each chunk leaves the staging buffer as one TMA store of
-// a 64-channel x 32-pixel box at ybox instead of per-lane stores.
+// the columns [cb_begin, cb_end) of the BN-wide tile, in chunks of up to COLS columns.  QW32:
+// read TMEM 32 columns at a time where the chunk allows (fewer round trips, more registers).
+// With ymap (bf16 outputs in 64- or 32-column chunks), each chunk leaves the staging buffer as
+// one TMA store of a 64- or 32-channel x 32-pixel box at ybox instead of per-lane stores.
 template <int BN, int COLS, int ESZ, bool QW32 = true>
 __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t taddr, int lane, int wq, int cb_begin,
                                                 int cb_end, int nt, int gi, int split, bool partial, bool add_bias,
@@ -444,7 +444,7 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
     for (int cb = cb_begin; cb < cb_end; cb += CW) {
         const int n0 = nt * BN + cb;
         if (n0 >= g.K) break;                               // warp-uniform
-        if (ESZ == 2 && CW == 64 && ymap) {
+        if (ESZ == 2 && (CW == 64 || CW == 32) && ymap) {
             // the staging buffer is rewritten only after the previous chunk's store has read it
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
@@ -537,8 +537,9 @@ __device__ __forceinline__ void epilogue_chunks(const TcParams& p, uint32_t tadd
             }
         }
         __syncwarp();
-        if (ESZ == 2 && CW == 64 && ymap) {
-            // 32 rows x 128 bytes in the 128-byte swizzle the tensor map expects: one box store
+        if (ESZ == 2 && (CW == 64 || CW == 32) && ymap) {
+            // 32 rows x 128 (64) bytes in the 128-byte (64-byte) swizzle the tensor map expects:
+            // one box store
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) {

@@ -80,7 +80,8 @@ template <int BN, int STAGES, int KIND, int EW>
 struct Smem {
     static constexpr size_t LIMIT = 232448;
     static constexpr size_t RING = (size_t)STAGES * (Traits<KIND, EW>::A_STAGE + Cfg<BN, KIND>::B_STAGE);
-    static constexpr size_t STG = (size_t)EW * STG_WARP_BYTES;
+    static constexpr size_t STG_W = STG_WARP_BYTES;   // staging per epilogue warp
+    static constexpr size_t STG = (size_t)EW * STG_W;
     static constexpr size_t BARS = 8 * (3 * STAGES + 5) + 16;
     static constexpr size_t BIAS_NEED = (size_t)16 * BN;   // EW warps x BN/(EW/4) columns x 4 bytes
     static constexpr bool BIAS_SMEM =
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
     const uint32_t sB = sbase + STAGES * T::A_STAGE;
     using SM = Smem<BN, STAGES, KIND, EW>;
     constexpr uint32_t STG_OFFSET = STAGES * (T::A_STAGE + C::B_STAGE);       // epilogue staging
-    constexpr uint32_t BIAS_OFFSET = STG_OFFSET + EW * STG_WARP_BYTES;        // fp32 bias columns
+    constexpr uint32_t BIAS_OFFSET = STG_OFFSET + (uint32_t)SM::STG;          // fp32 bias columns
     const uint32_t bar0 = sbase + BIAS_OFFSET + (uint32_t)SM::BIAS_BYTES;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -437,12 +438,13 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
         // pieces.  Split plans store fp32 partial sums to the workspace the same way.
         const int wq = warp & 3;
         constexpr int COLS = BN / (EW / 4) < 16 ? 16 : BN / (EW / 4);   // EW/4 warps share a lane quarter
+        constexpr int CC2 = COLS, CC4 = COLS;   // columns per staged chunk: bf16, fp32 outputs
         const int cb_begin = (warp >> 2) * COLS;
         const int cb_end = cb_begin + COLS < BN ? cb_begin + COLS : BN;
         const bool partial = p.splits > 1;
         const bool add_bias = (p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU) && !partial;
         const bool do_gelu = (p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU) && !partial;
-        uint8_t* stg = smem + STG_OFFSET + warp * STG_WARP_BYTES;
+        uint8_t* stg = smem + STG_OFFSET + warp * (uint32_t)SM::STG_W;
         if (p.pdl) griddep_wait();   // y, the workspace and bias may belong to the previous kernel
         uint32_t tile_i = 0;
         for (int u = u0; u < p.total_units; u += ustep, ++tile_i) {
@@ -490,8 +492,8 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
             }
             const bool wide = partial || T::TF32;     // fp32 stores
             long long roff[EPI_MAX_LPR];
-            if (wide) epilogue_rows<COLS, 4>(lane, wq, row_offset, roff);
-            else epilogue_rows<COLS, 2>(lane, wq, row_offset, roff);
+            if (wide) epilogue_rows<CC4, 4>(lane, wq, row_offset, roff);
+            else epilogue_rows<CC2, 2>(lane, wq, row_offset, roff);
             float* bsm = nullptr;
             if (SM::BIAS_SMEM && add_bias) {
                 // this warp's bias columns of tile nt in fp32 (columns past K as zeros, never
@@ -513,10 +515,10 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
             if (wide)
-                epilogue_chunks<BN, COLS, 4, EW == 8>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
+                epilogue_chunks<BN, CC4, 4, EW == 8>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
                                        do_gelu, stg, roff);
             else
-                epilogue_chunks<BN, COLS, 2, EW == 8>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
+                epilogue_chunks<BN, CC2, 2, EW == 8>(p, taddr, lane, wq, cb_begin, cb_end, nt, gi, split, partial, add_bias,
                                        do_gelu, stg, roff, bsm, (T::TMA && p.ystore) ? &y_map : nullptr,
                                        YBox{to.ow0 + wq * 32, to.oh0, to.od, to.n});
             tc_fence_before();

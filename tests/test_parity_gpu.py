@@ -542,13 +542,21 @@ YSTORE_CASES = [
     # 2D problem with one-row tiles (Wo >= 128)
     ("2d_one_row_tiles", L(2, 1, 1, 64, 256, (3, 512), (3, 3), (1, 2), (1, 1), (1, 1)),
      {"CONV_FORCE_BN": 256, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_GATHER": "tma"}),
+    # 32-column chunks (64-byte swizzle): 128-wide tiles with 16 epilogue warps, 64-wide tiles
+    # with 8, and 128-wide CTA pairs with 16; K not a multiple of the tile width
+    ("1d_bn128_ew16", L(1, 2, 1, 128, 320, (650,), (3,), (1,), (1,), (1,)),
+     {"CONV_FORCE_BN": 128, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_GATHER": "tma", "CONV_FORCE_EPI_WARPS": 16}),
+    ("1d_bn64_ew8", L(1, 2, 1, 128, 192, (650,), (3,), (1,), (1,), (1,), CONV_EPI_BIAS),
+     {"CONV_FORCE_BN": 64, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_GATHER": "tma", "CONV_FORCE_EPI_WARPS": 8}),
+    ("1d_pair_bn128_ew16", L(1, 3, 1, 128, 256, (701,), (3,), (2,), (1,), (1,)),
+     {"CONV_FORCE_BN": 128, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_EPI_WARPS": 16, "CONV_FORCE_PAIR": 1}),
 ]
 
 
 @pytest.mark.parametrize("name,layer,env", YSTORE_CASES, ids=[c[0] for c in YSTORE_CASES])
 def test_tensor_map_stores_are_bit_identical(name, layer, env):
-    """Epilogues that store y through a tensor map (one TMA box of 64 channels x 32 pixels per
-    warp and chunk) write the same bits as per-lane stores, nothing outside y, and meet the
+    """Epilogues that store y through a tensor map (one TMA box of 64 or 32 channels x 32 pixels
+    per warp and chunk) write the same bits as per-lane stores, nothing outside y, and meet the
     bound against the oracle."""
     x, w, b = make_inputs(layer, "bf16", 970 + len(name))
     on, don = run_gpu(layer, "bf16", x, w, b, env={**env, "CONV_FORCE_YSTORE": 1}, guard=4096)
