@@ -11,7 +11,7 @@
 //
 // Pair protocol (the per-tap pair kernel's, tc_pair.cu): both CTAs' slab and weight copies
 // (.cta_group::2 TMA) complete on the leader's barriers, whose copy warps alone post the byte
-// counts of both CTAs; the leader's two MMA warps (one per accumulator of the tile pair) commit
+// counts of both CTAs; the leader's MMA warps (one per accumulator of a unit) commit
 // every release to both CTAs' barriers; both epilogues arrive on the leader's accumulator-empty
 // barrier; tensor memory is allocated and freed by both CTAs together.  Every wait is bounded;
 // each CTA drains the arrivals the other may still send it before the cluster barrier at exit.
@@ -29,7 +29,8 @@ constexpr int SP_MAX_SB = 8;
 constexpr int SP_A_WARP = EPI_WARPS;          // slab copies
 constexpr int SP_B_WARP0 = EPI_WARPS + 1;     // weight copies (3 warps)
 constexpr int SP_B_WARPS = 3;
-constexpr int SP_MMA_WARP = EPI_WARPS + 4;    // two MMA warps (leader only issues)
+constexpr int SP_MMA_WARP = EPI_WARPS + 4;    // one MMA warp per accumulator (leader only issues; the
+                                              // second idles in one-accumulator units)
 constexpr int SP_THREADS = (SP_MMA_WARP + 2) * 32;
 
 __device__ __forceinline__ void sp_tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
