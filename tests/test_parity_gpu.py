@@ -584,6 +584,10 @@ SLAB_PAIR_CASES = [
     # pixels), the plan the rules choose for the full-size 3D d2 layer
     ("3d_dil2_narrow", L(3, 1, 2, 64, 64, (6, 24, 56), (3, 3, 3), (1, 1, 1), (1, 1, 1), (2, 2, 2),
                          CONV_EPI_BIAS), {"CONV_FORCE_SLAB_BW": 27}),
+    # 2D dilation 2, narrow tiles that do not divide the output width (20 + 20 + 10 of 50
+    # columns), GELU, streamed weights
+    ("2d_dil2_narrow_ragged", L(2, 2, 1, 64, 64, (33, 54), (3, 3), (1, 1), (1, 1), (2, 2), CONV_EPI_BIAS_GELU),
+     {"CONV_FORCE_SLAB_BW": 20, "CONV_FORCE_SLAB_STREAM": 1}),
 ]
 
 
