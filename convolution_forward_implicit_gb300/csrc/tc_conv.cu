@@ -182,6 +182,29 @@ __global__ void __launch_bounds__(Traits<KIND, EW>::THREADS, 1)
                 uint32_t it = 0, issued = 0;   // issued: 1 + the last iteration this warp loaded
                 bool aborted = false;
                 bool x_ready = !p.pdl;      // x may come from the previous kernel on the stream
+                if (!x_ready && lane == 0 && u0 < p.total_units) {
+                    // this warp's activation boxes of the first unit's first stages go into L2
+                    // while the previous kernel finishes
+                    int mt, gi, nt, split;
+                    unit_tile(u0, mt, gi, nt, split);
+                    if (mt < p.num_mt) {
+                        const TileOrigin to = tile_origin(p, mt);
+                        const int kb0 = split * p.kbps, kb1 = min(kb0 + p.kbps, p.nkb);
+                        for (int kb = kb0 + pw; kb < kb1 && kb < kb0 + STAGES; kb += T::PROD_WARPS) {
+                            const int tap = fdiv(kb, p.f_cbt);
+                            const int c0 = (kb - tap * p.cbt) * cblk;
+                            const int zz = fdiv(tap, p.f_YX);
+                            const int rem = tap - zz * g.Y * g.X;
+                            const int yy = fdiv(rem, p.f_X);
+                            const int xx = rem - yy * g.X;
+                            const int wi = to.ow0 * g.sw - g.pw + xx * g.dw, hi = to.oh0 * g.sh - g.ph + yy * g.dh;
+                            if (p.map_kind == 0)
+                                tma_prefetch_5d(&act_map, gi * g.C + c0, wi, hi, to.od * g.sd - g.pd + zz * g.dd, to.n);
+                            else
+                                tma_prefetch_5d(&act_map, c0, gi, wi, hi, to.n);
+                        }
+                    }
+                }
                 for (int u = u0; u < p.total_units && !aborted; u += ustep) {
                     int mt, gi, nt, split;
                     unit_tile(u, mt, gi, nt, split);

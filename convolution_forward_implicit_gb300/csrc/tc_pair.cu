@@ -190,6 +190,28 @@ __global__ void __launch_bounds__(PairTraits<EW>::THREADS, 1)
             uint32_t it = 0;
             bool aborted = false;
             bool x_ready = !p.pdl;
+            if (!x_ready && lane == 0 && u0 < p.total_units) {
+                // this warp's activation boxes of the first unit's first stages go into L2 while
+                // the previous kernel finishes
+                int mt, gi, nt, split;
+                unit_tile(u0, mt, gi, nt, split);
+                if (mt < p.num_mt) {
+                    const TileOrigin to = tile_origin(p, mt);
+                    for (int kb = pw; kb < p.nkb && kb < STAGES; kb += T::PROD_WARPS) {
+                        const int tap = fdiv(kb, p.f_cbt);
+                        const int c0 = (kb - tap * p.cbt) * 64;
+                        const int zz = fdiv(tap, p.f_YX);
+                        const int rem = tap - zz * g.Y * g.X;
+                        const int yy = fdiv(rem, p.f_X);
+                        const int xx = rem - yy * g.X;
+                        const int wi = to.ow0 * g.sw - g.pw + xx * g.dw, hi = to.oh0 * g.sh - g.ph + yy * g.dh;
+                        if (p.map_kind == 0)
+                            tma_prefetch_5d(&act_map, gi * g.C + c0, wi, hi, to.od * g.sd - g.pd + zz * g.dd, to.n);
+                        else
+                            tma_prefetch_5d(&act_map, c0, gi, wi, hi, to.n);
+                    }
+                }
+            }
             for (int u = u0; u < p.total_units && !aborted; u += ustep) {
                 int mt, gi, nt, split;
                 unit_tile(u, mt, gi, nt, split);

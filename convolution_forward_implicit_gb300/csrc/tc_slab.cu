@@ -141,6 +141,20 @@ __global__ void __launch_bounds__(SlabRoles<TF32, (TF32 ? 1 : NACC)>::THREADS, 1
     if (warp == R::A_WARP) {
         // ------------------------------------------------------------ slab copies
         if (lane == 0) {
+            if (p.pdl && (int)blockIdx.x < p.total_units) {
+                // the first unit's first slabs go into L2 while the previous kernel finishes
+                int mt, gi, nt, split;
+                decode_unit(p, blockIdx.x, mt, gi, nt, split);
+                const TileOrigin to = tile_origin(p, mt);
+                for (int kg = 0; kg < p.slab_nkg && kg < SA; ++kg) {
+                    const int zz = fdiv(kg, p.f_cbt), cb = kg - zz * p.cbt;
+                    if (p.map_kind == 0)
+                        tma_prefetch_5d(&act_map, gi * g.C + cb * cblk, to.ow0 - g.pw, to.oh0 - g.ph,
+                                        to.od - g.pd + zz * g.dd, to.n);
+                    else
+                        tma_prefetch_5d(&act_map, cb * cblk, gi, to.ow0 - g.pw, to.oh0 - g.ph, to.n);
+                }
+            }
             if (p.pdl) griddep_wait();   // x may come from the previous kernel on the stream
             const uint32_t a_tx = (uint32_t)(p.slab_hr * p.slab_bws) * 128u;
             Ring ra(SA);
