@@ -57,7 +57,10 @@ struct SlabRoles {
 // H that share one slab (their halo rows once) and one pass over the weights: every tap issues
 // its MMAs into both accumulators from windows slab_pair_rows apart, against the same weight
 // tile.  The per-unit waits, commits and copies then serve twice the MMAs.
-template <int BN, bool TF32, int BY, int BT, int NACC>
+//
+// PLAIN: compiled for layers with no bias and no activation (the bias and GELU code left out:
+// 2D grouped layers 1.6% faster).
+template <int BN, bool TF32, int BY, int BT, int NACC, bool PLAIN = false>
 __global__ void __launch_bounds__(SlabRoles<TF32, (TF32 ? 1 : NACC)>::THREADS, 1)
     conv_fwd_slab_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap act_map) {
     constexpr int NMMA = TF32 ? 1 : NACC;          // MMA-issuing warps (one per accumulator of a unit)
@@ -391,8 +394,8 @@ __global__ void __launch_bounds__(SlabRoles<TF32, (TF32 ? 1 : NACC)>::THREADS, 1
         constexpr int SCOLS = BN / 2 < 16 ? 16 : BN / 2;   // two warps per TMEM lane quarter
         const int cb_begin = (warp >> 2) * SCOLS;
         const int cb_end = cb_begin + SCOLS < BN ? cb_begin + SCOLS : BN;
-        const bool add_bias = p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU;
-        const bool do_gelu = p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU;
+        const bool add_bias = !PLAIN && (p.epi == EPI_BIAS || p.epi == EPI_BIAS_GELU);
+        const bool do_gelu = !PLAIN && (p.epi == EPI_BIAS_GELU || p.epi == EPI_GELU);
         uint8_t* stg = smem + stg_off + warp * STG_W;
         if (p.pdl) griddep_wait();   // y and bias may belong to the previous kernel
         uint32_t tile_i = 0;
@@ -442,9 +445,9 @@ __global__ void __launch_bounds__(SlabRoles<TF32, (TF32 ? 1 : NACC)>::THREADS, 1
     }
 }
 
-template <int BN, bool TF32, int BY, int BT, int NACC = 1>
+template <int BN, bool TF32, int BY, int BT, int NACC = 1, bool PLAIN = false>
 cudaError_t launch_slab_one(const TcParams& p, const CUtensorMap& map, int grid, size_t smem, cudaStream_t stream) {
-    auto kern = conv_fwd_slab_kernel<BN, TF32, BY, BT, NACC>;
+    auto kern = conv_fwd_slab_kernel<BN, TF32, BY, BT, NACC, PLAIN>;
     static bool attr_set[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -482,7 +485,9 @@ cudaError_t launch_slab(const TcParams& p, const CUtensorMap* act_map, int grid,
         if (p.slab_nacc == 2) {                                                                              \
             if (bn > 64) return cudaErrorInvalidValue;                                                       \
             if (p.slab_btaps == 3 && p.slab_nbg == 3)                                                        \
-                return launch_slab_one<bn, false, 3, 3, (bn > 64 ? 1 : 2)>(p, *act_map, grid, smem, stream); \
+                return p.epi == EPI_NONE                                                                     \
+                           ? launch_slab_one<bn, false, 3, 3, (bn > 64 ? 1 : 2), true>(p, *act_map, grid, smem, stream) \
+                           : launch_slab_one<bn, false, 3, 3, (bn > 64 ? 1 : 2)>(p, *act_map, grid, smem, stream); \
             return launch_slab_one<bn, false, 0, 0, (bn > 64 ? 1 : 2)>(p, *act_map, grid, smem, stream);    \
         }                                                                                                    \
         if (p.slab_nacc != 1) return cudaErrorInvalidValue;                                                  \
