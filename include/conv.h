@@ -94,7 +94,11 @@ typedef struct conv_plan* conv_plan_t;
  * problems with C and K multiples of 4 whose input the TMA gather can address run on the
  * tensor cores as 3xTF32 (kind::tf32, three products per useful product); everything
  * else runs on the FFMA kernel.  conv_plan_describe names the choice ("variant=tc_bf16",
- * "tc_tf32x3", "simt_bf16" or "simt_f32").
+ * "tc_tf32x3", "simt_bf16" or "simt_f32") and, for tensor-core plans, the gather (per-tap
+ * boxes or slabs), the tile, the ring stages and whether tiles of 256 rows run on a pair of
+ * SMs ("cta_pair=m256": the two CTAs of a cluster issue .cta_group::2 MMAs, each holding half
+ * of every weight tile) or y leaves through a TMA tensor store ("store=tma").  Results are the
+ * same bits either way: every output is one sum in a fixed order.
  * Returns CONV_ERR_INVALID_ARG for a bad argument or an empty output,
  * CONV_ERR_UNSUPPORTED when an index would overflow the kernels' 32-bit coordinates.  The plan queries the current
  * device's SM count; without a device it plans for 152 SMs.  *out is set only on CONV_OK.
@@ -173,7 +177,7 @@ const char* conv_status_string(conv_status status);
 
 /*
  * Static-per-plan description of the choice made: variant, tile, stages, splits,
- * grid and gather mode.  Valid until the plan is destroyed.
+ * grid, gather mode, CTA pairs and tensor-map stores.  Valid until the plan is destroyed.
  */
 const char* conv_plan_describe(conv_plan_t plan);
 
