@@ -816,15 +816,16 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
         // width hold twice the output rows, so the pair's slab has 12 rows of 31 pixels (47 KB
         // against 59 KB) and the ring of the dilation-1 layer fits.
         const int reach_w = g.dw * (g.X - 1);
+        const conv_plan saved = *p;    // the single-CTA plan, restored if the pairs are not taken
+        bool narrowed = false;
         if (!ok && !resident && p->slab_nacc == 2 && p->ch.pair != 1 && p->ch.slab_bw <= 0) {
-            const conv_plan saved = *p;
             for (int k = 2; k <= 4 && !ok; ++k) {
                 const int bw = (int)cdiv(g.Wo, k);
                 if (bw < 8 || bw + reach_w > 128 || !set_slab_width(p, bw) || !set_slab_pair(p, true)) break;
+                narrowed = true;
                 fit_pair_rings();
                 ok = by_rule();
             }
-            if (!ok) *p = saved;
         }
         if (ok) {
             const int64_t pair_units = cdiv(p->num_mt, 2) * g.G * p->num_nt;
@@ -849,6 +850,7 @@ static bool plan_tc(conv_plan* p, bool tf32, bool allow_slab) {
                 p->prepack_bytes = (size_t)g.G * p->num_nt * p->nkb * bn * 128;
             }
         }
+        if (narrowed && !p->pair) *p = saved;   // the narrow tiles were only for the pairs
     }
     if (!tf32 && p->tma && !p->slab && p->splits == 1 && !p->cluster_red && (bn == 128 || bn == 256) &&
         p->num_mt >= 2 && p->ch.mc != 1) {

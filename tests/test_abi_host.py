@@ -508,3 +508,58 @@ def test_default_arithmetic_is_the_one_the_header_documents(lib, name, li, varia
     h = B.conv_plan_create(1, 1, 1, 3, 5, (40,), (3,), (1,), (1,), (1,), B.CONV_F32, B.CONV_EPI_BIAS)
     assert "variant=simt_f32" in B.conv_plan_describe(h)
     B.conv_plan_destroy(h)
+
+
+def _slab_units_expected(layer, d):
+    """Units a slab plan's description implies: output tiles of BH x BW pixels per image and
+    output plane, times groups and N tiles (packed groups count as one), halved (rounded up
+    along M) on CTA pairs."""
+    import math
+    nd = len(layer.spatial)
+    sp = (1,) * (3 - nd) + tuple(layer.spatial)
+    f = (1,) * (3 - nd) + tuple(layer.filter)
+    st = (1,) * (3 - nd) + tuple(layer.stride)
+    pa = (0,) * (3 - nd) + tuple(layer.pad)
+    di = (1,) * (3 - nd) + tuple(layer.dilation)
+    out = [(sp[i] + 2 * pa[i] - di[i] * (f[i] - 1) - 1) // st[i] + 1 for i in range(3)]
+    bh, bw = (int(v) for v in d["pixels"].split("x"))
+    pack = int(d.get("pack", "1"))
+    bn = int(d["tile"].split("x")[1])
+    num_mt = layer.N * out[0] * math.ceil(out[1] / bh) * math.ceil(out[2] / bw)
+    if d.get("cta_pair") == "m256":
+        num_mt = math.ceil(num_mt / 2)
+    return num_mt * (layer.G // pack) * math.ceil(pack * layer.K / bn)
+
+
+@pytest.mark.parametrize("env", [{}, {"CONV_FORCE_SLAB_PAIR": "1"}, {"CONV_FORCE_SLAB_PAIR": "0"},
+                                 {"CONV_FORCE_SLAB_BW": "20"}, {"CONV_FORCE_PAIR": "1"},
+                                 {"CONV_FORCE_SLAB_PAIR": "1", "CONV_FORCE_SLAB_STREAM": "1"}])
+def test_slab_plan_units_match_their_tiles(lib, env):
+    """Every slab plan's unit count is the one its tile shape implies, whatever the rules
+    tried on the way (narrower tiles for CTA pairs are dropped with the pairs when the pairs
+    are not taken): the grouped workloads and small 2D/3D problems of every dilation."""
+    from tests.test_parity_gpu import L
+    layers = [WORKLOADS[n].layers[0] for n in ("grouped2d_g8_c64_d1", "grouped2d_g8_c64_d2", "grouped2d_g32_c8_d1",
+                                                "grouped3d_g4_c64_d1", "grouped3d_g4_c64_d2")]
+    layers += [L(3, 1, 2, 64, 64, (6, 24, 56), (3, 3, 3), (1, 1, 1), (1, 1, 1), (2, 2, 2)),
+               L(2, 2, 1, 64, 32, (33, 54), (3, 3), (1, 1), (1, 1), (2, 2)),
+               L(3, 2, 4, 64, 64, (7, 28, 40), (3, 3, 3), (1, 1, 1), (2, 2, 2), (2, 2, 2))]
+    old = {k: os.environ.get(k) for k in env}
+    os.environ.update(env)
+    try:
+        seen = 0
+        for layer in layers:
+            h = B.conv_plan_create(*layer.plan_args(B.CONV_BF16))
+            d = dict(kv.split("=", 1) for kv in B.conv_plan_describe(h).split())
+            B.conv_plan_destroy(h)
+            if d["gather"] != "tma-slab":
+                continue
+            seen += 1
+            assert int(d["units"]) == _slab_units_expected(layer, d), (layer, env, d)
+        assert seen
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
