@@ -95,3 +95,76 @@ def test_random_plans_are_consistent(lib, kind):
         finally:
             B.conv_plan_destroy(h)
     assert accepted > 1000
+
+
+FORCINGS = [
+    {}, {"CONV_FORCE_PAIR": "1"}, {"CONV_FORCE_PAIR": "0"}, {"CONV_FORCE_GATHER": "tma"},
+    {"CONV_FORCE_GATHER": "cp.async"}, {"CONV_FORCE_SLAB_PAIR": "1"}, {"CONV_FORCE_SLAB_STREAM": "1"},
+    {"CONV_FORCE_MC": "1"}, {"CONV_FORCE_BN": "64"}, {"CONV_FORCE_BN": "256"}, {"CONV_FORCE_SPLITK": "3"},
+    {"CONV_FORCE_EPI_WARPS": "16"}, {"CONV_NO_PACK": "1"}, {"CONV_FORCE_SLAB_BW": "20"},
+    {"CONV_FORCE_PAIR": "1", "CONV_FORCE_BN": "128", "CONV_FORCE_GATHER": "tma"},
+    {"CONV_FORCE_SLAB_PAIR": "1", "CONV_FORCE_PAIR": "1"},
+]
+
+
+def _expected_units(g, kv):
+    """Work units a tensor-core forward plan implies: output tiles (BH x BW pixels of one output
+    plane per unit where the plan names its pixels, else 128 GEMM rows), times the groups (packed
+    groups counting once) and N tiles, halved along M (rounded up) on CTA pairs or weight-sharing
+    clusters, times the K splits."""
+    pack = int(kv.get("pack", "1"))
+    bn = int(kv["tile"].split("x")[1])
+    N = g.N
+    do, ho, wo = (1,) * (3 - len(g.out_spatial)) + tuple(g.out_spatial)
+    if "pixels" in kv:
+        bh, bw = (int(v) for v in kv["pixels"].split("x"))
+        num_mt = N * do * -(-ho // bh) * -(-wo // bw)
+    else:
+        num_mt = -(-(N * do * ho * wo) // 128)
+    if kv.get("cta_pair") == "m256" or kv.get("weights") == "multicast2":
+        num_mt = -(-num_mt // 2)
+    return num_mt * (g.G // pack) * -(-(pack * g.K) // bn) * int(kv["splits"])
+
+
+def test_tensor_core_plan_units_match_their_tiles(lib, monkeypatch):
+    """Every tensor-core forward plan, under each of the planner's forcing variables, holds the
+    unit count its tile shape implies and a grid that fits it: at most one CTA per SM and per
+    unit, in whole clusters of two on CTA pairs.  (A plan whose rules tried a shape on the way
+    and kept a stale count would give kernels units past the output, or leave some out.)"""
+    rng = np.random.default_rng(14)
+    sm_count = _sm_count()
+    checked = 0
+    for i in range(1200):
+        nd, N, G, C, K, sp, f, s, p, d, dt = _geometry(rng)
+        if nd > 1 and rng.random() < 0.5:
+            # grouped layers of the slab and CTA-pair sizes: unit stride, 3-tap filters, C = K = 64
+            sp = [int(rng.integers(4, 12))] + [int(rng.integers(14, 60)) for _ in range(nd - 1)]
+            f, s, C, K, G = [3] * nd, [1] * nd, 64, int(rng.choice([32, 64])), int(rng.choice([1, 2, 4, 8]))
+            dt = B.CONV_BF16
+        g = oracle.Geom(N, G, C, K, sp, f, s, p, d)
+        if min(g.out_spatial) <= 0:
+            continue
+        env = FORCINGS[i % len(FORCINGS)]
+        with monkeypatch.context() as m:
+            for k, v in env.items():
+                m.setenv(k, v)
+            try:
+                h = CREATE["fwd"](nd, N, G, C, K, sp, f, s, p, d, dt)
+            except B.ConvError:
+                continue        # a forced choice the problem cannot take
+        try:
+            kv = dict(tok.split("=", 1) for tok in B.conv_plan_describe(h).split())
+        finally:
+            B.conv_plan_destroy(h)
+        if not kv["variant"].startswith("tc"):
+            continue
+        where = f"nd={nd} N={N} G={G} C={C} K={K} in={sp} f={f} s={s} p={p} d={d} dtype={dt} env={env} {kv}"
+        units, grid = int(kv["units"]), int(kv["grid"])
+        assert units == _expected_units(g, kv), where
+        assert 1 <= grid <= sm_count, where
+        if kv.get("cta_pair") == "m256" or kv.get("weights") == "multicast2":
+            assert grid % 2 == 0 and grid // 2 <= units, where
+        else:
+            assert grid <= units, where
+        checked += 1
+    assert checked > 600
