@@ -497,6 +497,18 @@ MC_CASES = [
      {"CONV_FORCE_BN": 128, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_EPI_WARPS": 8}),
     # a long reduction (60 K blocks) as in the wide conv1d layer, batch 1
     ("1d_s2_c1280", L(1, 1, 1, 1280, 1280, (3000,), (3,), (2,), (1,), (1,)), {"CONV_FORCE_SPLITK": 1}),
+    # no padding, two images, a ragged last tile per image, 8 epilogue warps
+    ("1d_s2_pad0_n2", L(1, 2, 1, 384, 256, (1000,), (3,), (2,), (0,), (1,), CONV_EPI_BIAS),
+     {"CONV_FORCE_BN": 256, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_EPI_WARPS": 8}),
+    # two groups, GELU
+    ("1d_s2_groups", L(1, 1, 2, 256, 256, (1200,), (3,), (2,), (1,), (1,), CONV_EPI_GELU),
+     {"CONV_FORCE_BN": 256, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_EPI_WARPS": 8}),
+    # padding 2, three channel blocks, an odd number of M tiles
+    ("1d_s2_pad2_odd_mt", L(1, 1, 1, 192, 256, (640,), (3,), (2,), (2,), (1,), CONV_EPI_NONE),
+     {"CONV_FORCE_BN": 256, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_EPI_WARPS": 8}),
+    # 2D with a 1x3 filter at stride (1, 2): tiles of one output row on three rows
+    ("2d_1x3_s12", L(2, 1, 1, 128, 256, (3, 512), (1, 3), (1, 2), (0, 1), (1, 1), CONV_EPI_BIAS_GELU),
+     {"CONV_FORCE_BN": 256, "CONV_FORCE_SPLITK": 1, "CONV_FORCE_EPI_WARPS": 8}),
 ]
 
 
